@@ -1,0 +1,95 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each mutant is a copy of ``oracle/oracle.c`` with one plausible mistake
+(a dropped term, a wrong sign or index, a swapped operand), compiled into a
+temporary directory.  The real oracle is never modified.  A mutant that
+passes every pin would mean the pins leave that part of the oracle unchecked.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+import oracle_pins
+from oracle import build as obuild
+
+# (name, original snippet, mutated snippet, replace every occurrence?)
+MUTANTS = [
+    ("sink_dropped_from_denominator",
+     "if (j->sinks) denom += exp(sink - m);", ";", False),
+    ("sink_scaled_like_a_score",
+     "sink = (double)j->sinks[h];", "sink = (double)j->scale * j->sinks[h];", False),
+    ("rope_first_row_sign",
+     "y[i] = x0 * c - x1 * s;", "y[i] = x0 * c + x1 * s;", False),
+    ("rope_second_row_sign",
+     "y[i + half] = x1 * c + x0 * s;", "y[i + half] = x1 * c - x0 * s;", False),
+    ("rope_adjacent_pairs",
+     "uint32_t half = hd / 2;", "uint32_t half = 1;", False),
+    ("rope_angle_in_f64",
+     "float angle_f32 = (float)pos * inv_freq[i];",
+     "double angle_f32 = (double)pos * (double)inv_freq[i];", False),
+    ("range_excludes_pos",
+     "t <= p;", "t < p;", True),
+    ("values_read_from_k",
+     "const float* v_row = j->V + row0", "const float* v_row = j->K + row0", False),
+    ("gqa_interleaved_heads",
+     "const uint32_t g = h / group;", "const uint32_t g = h % j->n_kv_head;", False),
+    ("score_unscaled",
+     "score[t] = (double)j->scale * dot;", "score[t] = dot;", False),
+    ("norm_weight_plus_one",
+     "y[i] = (double)x[i] * inv_rms * (double)w[i];",
+     "y[i] = (double)x[i] * inv_rms * (1.0 + (double)w[i]);", False),
+    ("eps_outside_sqrt",
+     "1.0 / sqrt(sum_sq / (double)n + eps);", "1.0 / (sqrt(sum_sq / (double)n) + eps);",
+     False),
+    ("norm_over_sum_not_mean",
+     "sqrt(sum_sq / (double)n + eps)", "sqrt(sum_sq + eps)", False),
+    ("cached_k_not_rotated",
+     "oracle_norm_rope_head(k_in, j->k_norm_w, hd, j->eps, p, j->inv_freq, kv);",
+     "oracle_norm_rope_head(k_in, j->k_norm_w, hd, j->eps, 0, j->inv_freq, kv);", False),
+    ("query_not_rotated",
+     "oracle_norm_rope_head(q_in, j->q_norm_w, hd, j->eps, p, j->inv_freq, qv);",
+     "oracle_norm_rope_head(q_in, j->q_norm_w, hd, j->eps, 0, j->inv_freq, qv);", False),
+    ("query_uses_k_norm_weight",
+     "oracle_norm_rope_head(q_in, j->q_norm_w,", "oracle_norm_rope_head(q_in, j->k_norm_w,",
+     False),
+    ("cached_v_not_raw",
+     "j->V[at_p + (uint64_t)g * hd + i] = v_in[i];",
+     "j->V[at_p + (uint64_t)g * hd + i] = (float)kv[i];", False),
+    ("offset_missing_slot_ctx",
+     "return ((uint64_t)slot * slot_ctx + pos)", "return ((uint64_t)slot + pos)", False),
+    ("row_base_ignores_slot",
+     "const uint64_t row0 = (uint64_t)slot * j->slot_ctx * kv_dim;",
+     "const uint64_t row0 = 0;", False),
+    ("exp_without_max_subtraction",
+     "score[t] = exp(score[t] - m);", "score[t] = exp(score[t]);", False),
+    ("max_taken_over_first_key_only",
+     "if (score[t] > m) m = score[t];", "if (t == 0) m = score[t];", False),
+]
+
+
+def _mutant_lib(tmp_path, name, old, new, every):
+    src = open(obuild.SRC).read()
+    n = src.count(old)
+    assert n >= 1, f"mutant {name}: snippet not found in oracle.c"
+    if not every:
+        assert n == 1, f"mutant {name}: snippet is not unique in oracle.c"
+    mutated = src.replace(old, new) if every else src.replace(old, new, 1)
+    d = tmp_path / name
+    d.mkdir()
+    shutil.copy(os.path.join(obuild.HERE, "oracle.h"), d / "oracle.h")
+    (d / "oracle.c").write_text(mutated)
+    return obuild.build_oracle(str(d / "oracle.c"), str(d / "liboracle.so"), str(d))
+
+
+@pytest.mark.parametrize("name,old,new,every", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, every):
+    lib = oracle.Oracle(_mutant_lib(tmp_path, name, old, new, every))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except Exception:  # noqa: BLE001 -- any failure counts as caught
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
