@@ -1,0 +1,397 @@
+"""Benchmark: batched slot-KV decode attention on GB300.
+
+A step is one decode_batch_attn call over the workload's B rows (for the
+multi-step workload, its 64 consecutive calls).  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mid]
+                    [--impl gpu|reference]
+
+value      rows/s with every input resident in HBM, CUDA events on the
+           launching stream around exactly K steps (max over ranks);
+e2e        the same metric through decode_batch_attn_host: per step the
+           inputs are copied from pinned host memory and the output back;
+roofline   the decode kernel's algorithmic HBM bytes per launch over its
+           average launch time, against the measured copy bandwidth;
+cpu_baseline  the CPU oracle on the host's cores over a bounded sample.
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(rows are independent; no collective on the data path): weak scaling.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+HBM_FALLBACK_GBS = 6800.0
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        used = inside if inside else sorted(rows, key=lambda r: abs(r[0] - self.t0))[:2]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in used:
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                pass
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(used),
+                "samples_in_region": len(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, device=None):
+    """The largest value of ``x`` over all ranks (identity when not
+    distributed).  Timing only; rows never cross ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rows_per_s(rows_per_rank_step, steps, world, max_seconds):
+    """Weak scaling: every rank runs its own copy of the workload."""
+    return world * rows_per_rank_step * steps / max_seconds
+
+
+def oracle_sample(w, rows, n_threads):
+    """Compact host slot buffers for the oracle over ``rows`` (untimed set-up)."""
+    slots = w.slots()
+    p = w.positions(0)
+    ctx = int(max(p[r] for r in rows)) + w.steps
+    K = np.empty((len(rows), ctx, w.n_kv_head, w.head_dim), dtype=np.float32)
+    V = np.empty_like(K)
+    for i, r in enumerate(rows):
+        K[i] = w.hist_rows("k", slots[r], 0, ctx)
+        V[i] = w.hist_rows("v", slots[r], 0, ctx)
+    return K, V
+
+
+class OracleSample:
+    """The CPU oracle, as it stands, over a fixed sample of the workload's
+    rows (min(B, cores) rows of its first step, at evenly spaced quantiles of
+    position).  The sample's slot
+    history is regenerated on the host once, outside any timing; the oracle
+    rewrites the same K/V rows on every call, so calls repeat exactly."""
+
+    def __init__(self, w, n_threads):
+        import oracle
+        self.o = oracle.default()
+        self.w = w
+        self.n_threads = n_threads
+        # rows at evenly spaced quantiles of position, so the sample has the
+        # workload's mix of history lengths
+        k = min(w.B, n_threads)
+        order = np.argsort(w.positions(0), kind="stable")
+        self.rows = sorted(int(order[int(i)]) for i in
+                           np.linspace(0, w.B - 1, k).round().astype(int))
+        r = self.rows
+        self.K, self.V = oracle_sample(w, r, n_threads)
+        self.args = (w.q(0)[r], w.k_new(0)[r], w.v_new(0)[r], w.positions(0)[r],
+                     np.arange(len(r), dtype=np.uint32), w.q_norm_w(), w.k_norm_w(),
+                     w.inv_freq(), w.sink_logits(), w.eps, w.scale)
+
+    def step(self):
+        t0 = time.perf_counter()
+        self.o.decode_batch(self.K, self.V, *self.args, n_threads=self.n_threads)
+        return time.perf_counter() - t0
+
+    def describe(self, steps, seconds):
+        pos = self.w.positions(0)[self.rows]
+        return (f"{len(self.rows)} rows (positions {pos.min()}..{pos.max()}, mean "
+                f"{pos.mean():.0f}) of the {self.w.name} workload's "
+                f"first step per oracle call, {steps} calls, {seconds:.1f} s, rows split "
+                f"over {self.n_threads} threads")
+
+
+def time_oracle(w, budget_s, n_threads):
+    """rows/s of the oracle over calls on its sample until ``budget_s``."""
+    smp = OracleSample(w, n_threads)
+    smp.step()                                       # warm caches and pages
+    calls, spent = 0, 0.0
+    while spent < budget_s:
+        spent += smp.step()
+        calls += 1
+    return len(smp.rows) * calls / spent, smp.describe(calls, spent)
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    smp = OracleSample(w, cores)
+    for _ in range(args.warmup):
+        smp.step()
+    spent = sum(smp.step() for _ in range(args.steps))
+    value = len(smp.rows) * args.steps / spent
+    line = {
+        "impl": "reference", "metric": "slot-attn decode rows/s", "value": value,
+        "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": smp.describe(args.steps, spent)},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "n_slots": w.n_slots, "slot_ctx": w.slot_ctx,
+            "n_head": w.n_head, "n_kv_head": w.n_kv_head, "head_dim": w.head_dim,
+            "steps_per_call_sequence": w.steps, "sinks": w.sinks,
+            "l2": "inputs larger than L2 (history K/V read per step >> 129 MB)"}
+
+
+def run_gpu(args, w):
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import sequence_slot_kv_gb300 as skv
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    with torch.cuda.stream(stream):
+        K = torch.empty(shape, dtype=torch.float32, device=dev)
+        V = torch.empty(shape, dtype=torch.float32, device=dev)
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), sp)
+    kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head,
+                    k_buf=K, v_buf=V)
+    if args.split:
+        kv.set_split(*args.split)
+
+    def dev_t(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.to(dtype) if dtype is not None else t).to(dev)
+
+    qw, kw, inv = dev_t(w.q_norm_w()), dev_t(w.k_norm_w()), dev_t(w.inv_freq())
+    sinks = None if not w.sinks else dev_t(w.sink_logits())
+    slots_np = w.slots().astype(np.int32)
+    slots = dev_t(slots_np)
+    nsub = w.steps
+    q = [dev_t(w.q(t)) for t in range(nsub)]
+    kn = [dev_t(w.k_new(t)) for t in range(nsub)]
+    vn = [dev_t(w.v_new(t)) for t in range(nsub)]
+    pos = [dev_t(w.positions(t).astype(np.int32)) for t in range(nsub)]
+    out = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32, device=dev)
+    bytes_per_launch = [w.alg_bytes(w.positions(t)) for t in range(nsub)]
+    torch.cuda.synchronize(dev)
+
+    def one_step():
+        for t in range(nsub):
+            kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
+                                 w.eps, w.scale, stream=sp)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+    assert kv.get_status(sp) == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * nsub)]
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.mark("begin")
+    begin.record(stream)
+    i = 0
+    for _ in range(args.steps):
+        for t in range(nsub):
+            ev[i][0].record(stream)
+            kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
+                                 w.eps, w.scale, stream=sp)
+            ev[i][1].record(stream)
+            i += 1
+    end.record(stream)
+    barrier()
+    clocks.mark("end")
+    clk = clocks.stop()
+    total_ms = begin.elapsed_time(end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    assert kv.get_status(sp) == 0
+    total_ms = max_over_ranks(total_ms, dev)
+    rows_per_step = w.B * nsub
+    value = whole_job_rows_per_s(rows_per_step, args.steps, world, total_ms / 1e3)
+
+    # e2e: host inputs -> device -> host output through decode_batch_attn_host
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    hq = [pin(w.q(t)) for t in range(nsub)]
+    hk = [pin(w.k_new(t)) for t in range(nsub)]
+    hv = [pin(w.v_new(t)) for t in range(nsub)]
+    hp = [pin(w.positions(t).astype(np.int32)) for t in range(nsub)]
+    hs = pin(slots_np)
+    hout = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for t in range(nsub):
+            kv.decode_batch_attn_host(hq[t], hk[t], hv[t], hp[t], hs, qw, kw, inv, sinks, hout,
+                                      w.eps, w.scale, stream=sp)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, dev)
+    e2e_value = whole_job_rows_per_s(rows_per_step, args.steps, world, e2e_s)
+    h2d = nsub * (hq[0].numel() + hk[0].numel() + hv[0].numel() + hp[0].numel()
+                  + hs.numel()) * 4
+    d2h = nsub * hout.numel() * 4
+
+    peak, peak_kind = peak_hbm()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    alg_bytes = statistics.mean(bytes_per_launch)
+    achieved = alg_bytes / avg_launch_s / 1e9
+    line = {
+        "metric": "slot-attn decode rows/s", "value": value, "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": args.traffic,
+                     "alg_bytes_per_launch": alg_bytes,
+                     "avg_launch_us": avg_launch_s * 1e6,
+                     "kernel": "slotkv_decode_attn_kernel"},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * nsub,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        v, desc = time_oracle(w, args.cpu_budget, cores)
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    kv.free()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mid", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--split", type=int, nargs=2, default=None,
+                    metavar=("MIN_CHUNK_KEYS", "MAX_SPLITS"))
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the decode kernel, if measured")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

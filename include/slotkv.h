@@ -1,0 +1,210 @@
+/*
+ * slotkv.h -- C ABI of libslotkv: batched multi-sequence decode attention over
+ * slot-based KV caches, for NVIDIA GB300 (sm_103a).
+ *
+ * Source of the semantics: the zinc engine's API pages,
+ *   "Forward Cuda Gemma" -- allocSlotKv, slotKvOffsetBytes, slotKvSmoke and
+ *     decodeBatch (per-row Q/K norm, RoPE, KV write, causal softmax over the
+ *     row's own slot history, and the fused batched-seq attention kernel
+ *     named there as the next step);
+ *   "Forward Cuda" -- slot state allocation, the slot KV byte offset, the
+ *     upload of inv_freq and attention sinks at init, and the note that
+ *     attention slot KV needs no reset between occupants.
+ *
+ * Conventions for every call:
+ *   - All tensors are f32, row-major and contiguous.  positions and slots are
+ *     u32.  Notation: hd = head_dim, kv_dim = n_kv_head * hd,
+ *     G = n_head / n_kv_head (query heads per kv head).
+ *   - "device" pointers must be CUDA device memory on the handle's device;
+ *     "host" pointers are ordinary (preferably pinned) host memory.
+ *   - The caller owns every buffer it passes.  The library owns only what
+ *     slot_kv_alloc allocates (the KV buffers when none were adopted, the
+ *     split-K workspace and small staging buffers).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns without synchronising, unless stated otherwise.
+ *   - Calls that use one handle must be ordered on the GPU (same stream, or
+ *     synchronised): they share the handle's workspace.
+ *   - Every call returns SLOTKV_OK (0) or an SLOTKV_ERR_* code and never
+ *     aborts the process; slot_kv_last_error() gives a message for the
+ *     calling thread's last failure.
+ */
+#ifndef SLOTKV_H
+#define SLOTKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct slotkv_s* slotkv_t;
+typedef void* slotkv_stream_t; /* a cudaStream_t */
+
+enum slotkv_status {
+    SLOTKV_OK = 0,
+    SLOTKV_ERR_ARG = 1,         /* bad pointer, size or geometry */
+    SLOTKV_ERR_CUDA = 2,        /* a CUDA runtime or driver call failed */
+    SLOTKV_ERR_UNSUPPORTED = 3, /* geometry outside the compiled kernels */
+    SLOTKV_ERR_STATE = 4        /* handle not allocated / already freed */
+};
+
+/* Sticky device-side flags, read and cleared by slot_kv_get_status. */
+enum slotkv_device_flags {
+    SLOTKV_DEV_RANGE = 1u,  /* some row had slots[b] >= n_slots or
+                               positions[b] >= slot_ctx: that row was skipped,
+                               its out rows and the KV were left untouched */
+    SLOTKV_DEV_TIMEOUT = 2u /* a pipeline wait ran out its limit; that call's
+                               results are not valid */
+};
+
+/*
+ * slot_kv_alloc -- allocate (or adopt) one attention layer's slot KV and the
+ * decode workspace.  "Forward Cuda Gemma", allocSlotKv; "Forward Cuda", slot
+ * state allocation.
+ *
+ *   *handle    in/out.  Must be NULL or a live handle on entry; a live handle
+ *              is freed first, so re-calling is allowed (the pages' allocSlotKv
+ *              frees any prior slot KV first).  Receives the new handle.
+ *   n_slots    number of concurrent sequences (slots), >= 1.
+ *   slot_ctx   positions per slot, >= 1; n_slots * slot_ctx < 2^31 - 256.
+ *   n_kv_head  kv heads per position, >= 1.
+ *   head_dim   64, 128 or 256.
+ *   k_buf, v_buf
+ *              NULL, NULL: the library allocates both buffers (zero-filled)
+ *              and frees them in slot_kv_free.  Otherwise both must be device
+ *              buffers of n_slots*slot_ctx*kv_dim f32, 16-byte aligned; they are
+ *              adopted (used in place, never freed by the library).
+ *              Layout of each: [n_slots][slot_ctx][n_kv_head][head_dim].
+ *   max_rows   the largest B a decode call will pass, >= 1.
+ *   max_n_head the largest n_head a decode call will pass; G = n_head /
+ *              n_kv_head must be 1..8.
+ *
+ * Errors: SLOTKV_ERR_ARG for a bad size or a half-given buffer pair,
+ * SLOTKV_ERR_CUDA if an allocation or the TMA descriptor set-up fails (nothing
+ * is leaked and *handle is set to NULL).
+ */
+int slot_kv_alloc(slotkv_t* handle, uint32_t n_slots, uint32_t slot_ctx,
+                  uint32_t n_kv_head, uint32_t head_dim, float* k_buf, float* v_buf,
+                  uint32_t max_rows, uint32_t max_n_head);
+
+/* slot_kv_free -- release what slot_kv_alloc allocated (not adopted
+ * buffers).  NULL is a no-op.  Synchronises the device. */
+int slot_kv_free(slotkv_t handle);
+
+/*
+ * slot_kv_offset_bytes -- byte offset of (slot, pos) in the K (and V) buffer:
+ * (slot * slot_ctx + pos) * kv_dim * sizeof(float).  "Forward Cuda Gemma",
+ * slotKvOffsetBytes; "Forward Cuda", slot KV offset.  The kernels index the
+ * buffers exactly this way.  Returns SIZE_MAX for a NULL handle,
+ * slot >= n_slots or pos >= slot_ctx.  Host only; no device work.
+ */
+size_t slot_kv_offset_bytes(slotkv_t handle, uint32_t slot, uint32_t pos);
+
+/*
+ * slot_kv_reset -- zero every position of one slot's K and V (asynchronous,
+ * on `stream`).  The pages note that attention slot KV needs no reset when a
+ * slot is reused ("Forward Cuda", slot state reset on admit): a step reads
+ * only positions 0..pos of its own slot, which the sequence wrote itself.
+ * This call exists for hygiene and tests; no result depends on it.
+ * SLOTKV_ERR_ARG if slot >= n_slots.
+ */
+int slot_kv_reset(slotkv_t handle, uint32_t slot, slotkv_stream_t stream);
+
+/* slot_kv_k_ptr / slot_kv_v_ptr -- device address of the K / V buffer. */
+int slot_kv_k_ptr(slotkv_t handle, float** k);
+int slot_kv_v_ptr(slotkv_t handle, float** v);
+
+/* slot_kv_geometry -- the handle's sizes (any output pointer may be NULL). */
+int slot_kv_geometry(slotkv_t handle, uint32_t* n_slots, uint32_t* slot_ctx,
+                     uint32_t* n_kv_head, uint32_t* head_dim, uint32_t* max_rows,
+                     uint32_t* max_n_head);
+
+/*
+ * decode_batch_attn -- one batched decode attention step for B independent
+ * rows.  "Forward Cuda Gemma", decodeBatch (the attention inner part, fused
+ * across rows as the batched-seq attention kernel).  For each row b, with
+ * p = positions[b], s = slots[b], and each kv head g:
+ *   1. q' = RoPE_p(RMSnorm(q[b][h]) * q_norm_w) for the query heads h of g,
+ *      k' = RoPE_p(RMSnorm(k_new[b][g]) * k_norm_w); RMSnorm(x) =
+ *      x / sqrt(mean(x^2) + eps); RoPE_p rotates the pairs (i, i + hd/2) by
+ *      the f32 angle fl32((float)p * inv_freq[i]).
+ *   2. K[s][p][g] = k', V[s][p][g] = v_new[b][g] (raw), at the byte offset
+ *      slot_kv_offset_bytes(s, p).
+ *   3. out[b][h] = sum_{t=0..p} w_t V[s][t][g] with w = softmax over
+ *      scale * <q', K[s][t][g]> for t = 0..p, where a non-NULL sinks[h] adds
+ *      one logit to the normaliser (it joins the max and the denominator,
+ *      is not scaled, and carries no value).  Query head h uses kv head
+ *      h / G.  Positions after p in the slot are never read.
+ *
+ *   handle      from slot_kv_alloc.
+ *   B           rows, 0 <= B <= max_rows (B = 0 does nothing).
+ *   n_head      query heads, a multiple of n_kv_head, <= max_n_head.
+ *   q           device, [B][n_head][hd].
+ *   k_new       device, [B][n_kv_head][hd].
+ *   v_new       device, [B][n_kv_head][hd].
+ *   positions   device, u32[B]; the slot must already hold 0..p-1.
+ *   slots       device, u32[B]; pairwise distinct within one call
+ *               (duplicates give an undefined result, never a fault).
+ *   q_norm_w    device, [hd].        k_norm_w  device, [hd].
+ *   inv_freq    device, [hd/2].      sinks     device [n_head], or NULL.
+ *   out         device, [B][n_head][hd]; written for every in-range row.
+ *   eps         RMS-norm epsilon.    scale     softmax scale (e.g. 1/sqrt(hd)).
+ *
+ * Out-of-range rows (slots[b] >= n_slots or positions[b] >= slot_ctx, the
+ * decodeBatch precondition) are skipped on the device and raise
+ * SLOTKV_DEV_RANGE.  Host-side errors: SLOTKV_ERR_ARG (NULL pointer, B or
+ * n_head too large, n_head not a multiple of n_kv_head),
+ * SLOTKV_ERR_UNSUPPORTED (G outside 1..8), SLOTKV_ERR_CUDA (launch failure).
+ */
+int decode_batch_attn(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
+                      const float* k_new, const float* v_new, const uint32_t* positions,
+                      const uint32_t* slots, const float* q_norm_w,
+                      const float* k_norm_w, const float* inv_freq, const float* sinks,
+                      float* out, float eps, float scale, slotkv_stream_t stream);
+
+/*
+ * decode_batch_attn_host -- decode_batch_attn for callers whose per-step
+ * inputs and output live in host memory.  q, k_new, v_new, positions, slots
+ * and out are HOST pointers with the layouts above (pinned memory gives
+ * asynchronous copies); q_norm_w, k_norm_w, inv_freq and sinks stay device
+ * pointers (resident parameters).  The call copies the inputs into
+ * handle-owned device staging buffers on `stream`, runs the step, copies out
+ * back and synchronises `stream` before returning, so out is ready on return.
+ * Errors as decode_batch_attn, plus SLOTKV_ERR_CUDA for a failed copy.
+ */
+int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
+                           const float* k_new, const float* v_new,
+                           const uint32_t* positions, const uint32_t* slots,
+                           const float* q_norm_w, const float* k_norm_w,
+                           const float* inv_freq, const float* sinks, float* out,
+                           float eps, float scale, slotkv_stream_t stream);
+
+/*
+ * slot_kv_get_status -- synchronise `stream`, return the sticky device flags
+ * (SLOTKV_DEV_*) raised since the last call in *flags, and clear them.  After
+ * SLOTKV_DEV_TIMEOUT the workspace is also cleared so later calls are valid.
+ */
+int slot_kv_get_status(slotkv_t handle, slotkv_stream_t stream, uint32_t* flags);
+
+/*
+ * slot_kv_set_split -- split-K policy.  A row with n = p + 1 keys is cut into
+ * nsplit = ceil(n / C) chunks of C = max(min_chunk_keys, ceil(n / max_splits)
+ * rounded up to the tile) keys; chunks run on separate CTAs and are merged by
+ * the last one to finish.  C depends only on n and the geometry, never on B or
+ * on the other rows, so a row's result is the same in any batch.
+ * min_chunk_keys must be a positive multiple of the tile (4096 / head_dim
+ * keys); max_splits 1..256.  Reallocates the workspace (synchronises).
+ * The defaults are min_chunk_keys = 256 KiB of K+V per kv head and
+ * max_splits = 64.
+ */
+int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_splits);
+
+/* slot_kv_last_error -- message for the calling thread's last failed call
+ * ("" if none).  The pointer stays valid until that thread's next call. */
+const char* slot_kv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SLOTKV_H */

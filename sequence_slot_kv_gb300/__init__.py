@@ -1,0 +1,252 @@
+"""Python binding of libslotkv: batched decode attention over slot KV on GB300.
+
+Argument marshalling only.  Every step of the decode attention runs in the
+library's CUDA kernels; PyTorch supplies device memory and streams.  There is
+no CPU fallback: importing this package raises if ``libslotkv.so`` has not
+been built (``__graft_entry__.build()`` or ``python -m
+sequence_slot_kv_gb300.build``).
+
+The functions mirror the C ABI in ``include/slotkv.h`` name for name:
+``slot_kv_alloc``, ``slot_kv_free``, ``slot_kv_offset_bytes``,
+``slot_kv_reset``, ``decode_batch_attn``, ``decode_batch_attn_host``,
+``slot_kv_get_status``, ``slot_kv_set_split``; ``SlotKV`` wraps a handle.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
+    "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "slot_kv_get_status",
+    "slot_kv_set_split", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libslotkv.so")
+DEV_RANGE = 1
+DEV_TIMEOUT = 2
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+_u32, _f32, _vp, _int = ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+_DECODE_ARGS = [_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                _f32, _f32, _vp]
+EXPORTS = {
+    "slot_kv_alloc": ([ctypes.POINTER(_vp), _u32, _u32, _u32, _u32, _vp, _vp, _u32, _u32],
+                      _int),
+    "slot_kv_free": ([_vp], _int),
+    "slot_kv_offset_bytes": ([_vp, _u32, _u32], ctypes.c_size_t),
+    "slot_kv_reset": ([_vp, _u32, _vp], _int),
+    "slot_kv_k_ptr": ([_vp, ctypes.POINTER(_vp)], _int),
+    "slot_kv_v_ptr": ([_vp, ctypes.POINTER(_vp)], _int),
+    "slot_kv_geometry": ([_vp] + [ctypes.POINTER(_u32)] * 6, _int),
+    "decode_batch_attn": (_DECODE_ARGS, _int),
+    "decode_batch_attn_host": (_DECODE_ARGS, _int),
+    "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
+    "slot_kv_set_split": ([_vp, _u32, _u32], _int),
+    "slot_kv_last_error": ([], ctypes.c_char_p),
+}
+
+
+class SlotKVError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what} failed with status {code}: {last_error()}")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run __graft_entry__.build() (no CPU fallback exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in EXPORTS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def last_error():
+    msg = _lib.slot_kv_last_error()
+    return msg.decode() if msg else ""
+
+
+def _check(code, what):
+    if code != 0:
+        raise SlotKVError(code, what)
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    """Device (or host) address of a contiguous tensor; None stays NULL."""
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class SlotKV:
+    """One attention layer's slot KV: ``[n_slots][slot_ctx][n_kv_head][head_dim]``
+    f32 K and V, plus the split-K workspace for up to ``max_rows`` rows and
+    ``max_n_head`` query heads.  ``k_buf``/``v_buf`` (torch CUDA tensors) are
+    adopted in place when given; otherwise the library allocates them."""
+
+    def __init__(self, n_slots, slot_ctx, n_kv_head, head_dim, max_rows, max_n_head,
+                 k_buf=None, v_buf=None):
+        import torch
+        self._h = _vp()
+        self.n_slots, self.slot_ctx = int(n_slots), int(slot_ctx)
+        self.n_kv_head, self.head_dim = int(n_kv_head), int(head_dim)
+        self.kv_dim = self.n_kv_head * self.head_dim
+        self.max_rows, self.max_n_head = int(max_rows), int(max_n_head)
+        self._keep = (k_buf, v_buf)
+        kp = _ptr(k_buf, torch.float32, "k_buf")
+        vp = _ptr(v_buf, torch.float32, "v_buf")
+        _check(_lib.slot_kv_alloc(ctypes.byref(self._h), n_slots, slot_ctx, n_kv_head,
+                                  head_dim, kp, vp, max_rows, max_n_head), "slot_kv_alloc")
+
+    @property
+    def handle(self):
+        return self._h.value
+
+    def free(self):
+        if self._h.value:
+            _check(_lib.slot_kv_free(self._h), "slot_kv_free")
+            self._h = _vp()
+        self._keep = (None, None)
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
+
+    def offset_bytes(self, slot, pos):
+        v = _lib.slot_kv_offset_bytes(self._h, slot, pos)
+        return None if v == SIZE_MAX else int(v)
+
+    def reset(self, slot, stream=None):
+        _check(_lib.slot_kv_reset(self._h, slot, _stream_ptr(stream)), "slot_kv_reset")
+
+    def k_ptr(self):
+        p = _vp()
+        _check(_lib.slot_kv_k_ptr(self._h, ctypes.byref(p)), "slot_kv_k_ptr")
+        return p.value
+
+    def v_ptr(self):
+        p = _vp()
+        _check(_lib.slot_kv_v_ptr(self._h, ctypes.byref(p)), "slot_kv_v_ptr")
+        return p.value
+
+    def kv_tensors(self):
+        """(K, V) as torch views of the slot buffers (adopted or owned)."""
+        if self._keep[0] is not None:
+            return self._keep
+        # owned buffers: wrap the device addresses without copying
+        n = self.n_slots * self.slot_ctx * self.kv_dim
+        shape = (self.n_slots, self.slot_ctx, self.n_kv_head, self.head_dim)
+        return tuple(_wrap_device(ptr, n).view(shape) for ptr in (self.k_ptr(), self.v_ptr()))
+
+    def decode_batch_attn(self, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                          inv_freq, sinks, out, eps, scale, stream=None):
+        import torch
+        B, n_head = int(q.shape[0]), int(q.shape[1])
+        f, u = torch.float32, torch.int32
+        _check(_lib.decode_batch_attn(
+            self._h, B, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
+            _ptr(v_new, f, "v_new"), _ptr(positions, u, "positions"), _ptr(slots, u, "slots"),
+            _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"), _ptr(out, f, "out"),
+            eps, scale, _stream_ptr(stream)), "decode_batch_attn")
+        return out
+
+    def decode_batch_attn_host(self, q, k_new, v_new, positions, slots, q_norm_w,
+                               k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
+        """As decode_batch_attn, with q/k_new/v_new/positions/slots/out in host
+        memory (CPU tensors, ideally pinned); synchronous."""
+        import torch
+        B, n_head = int(q.shape[0]), int(q.shape[1])
+        f, u = torch.float32, torch.int32
+        _check(_lib.decode_batch_attn_host(
+            self._h, B, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
+            _ptr(v_new, f, "v_new"), _ptr(positions, u, "positions"), _ptr(slots, u, "slots"),
+            _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"), _ptr(out, f, "out"),
+            eps, scale, _stream_ptr(stream)), "decode_batch_attn_host")
+        return out
+
+    def get_status(self, stream=None):
+        v = _u32()
+        _check(_lib.slot_kv_get_status(self._h, _stream_ptr(stream), ctypes.byref(v)),
+               "slot_kv_get_status")
+        return int(v.value)
+
+    def set_split(self, min_chunk_keys, max_splits):
+        _check(_lib.slot_kv_set_split(self._h, min_chunk_keys, max_splits), "slot_kv_set_split")
+
+
+def _wrap_device(ptr, numel):
+    """A float32 CUDA tensor aliasing ``numel`` floats at device address ``ptr``."""
+    import torch
+
+    class _Holder:
+        pass
+
+    h = _Holder()
+    h.__cuda_array_interface__ = {
+        "shape": (numel,), "typestr": "<f4", "data": (ptr, False), "version": 3,
+        "strides": None,
+    }
+    return torch.as_tensor(h, device="cuda")
+
+
+# ---- C-ABI names ---------------------------------------------------------
+def slot_kv_alloc(n_slots, slot_ctx, n_kv_head, head_dim, max_rows, max_n_head,
+                  k_buf=None, v_buf=None):
+    return SlotKV(n_slots, slot_ctx, n_kv_head, head_dim, max_rows, max_n_head, k_buf, v_buf)
+
+
+def slot_kv_free(h):
+    h.free()
+
+
+def slot_kv_offset_bytes(h, slot, pos):
+    return h.offset_bytes(slot, pos)
+
+
+def slot_kv_reset(h, slot, stream=None):
+    h.reset(slot, stream)
+
+
+def decode_batch_attn(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
+                      sinks, out, eps, scale, stream=None):
+    return h.decode_batch_attn(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                               inv_freq, sinks, out, eps, scale, stream)
+
+
+def decode_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                           inv_freq, sinks, out, eps, scale, stream=None):
+    return h.decode_batch_attn_host(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                                    inv_freq, sinks, out, eps, scale, stream)
+
+
+def slot_kv_get_status(h, stream=None):
+    return h.get_status(stream)
+
+
+def slot_kv_set_split(h, min_chunk_keys, max_splits):
+    h.set_split(min_chunk_keys, max_splits)

@@ -1,0 +1,13 @@
+// decode_attn_hd256.cu -- instantiations of the fused decode attention kernel
+// for head_dim 256 (G = 1..8 query heads per kv head).  One translation unit
+// per head dim so the builds run in parallel.
+#include "decode_attn.cuh"
+
+namespace slotkv {
+
+int launch_decode_hd256(int G, const DecodeParams& p, const CUtensorMap& tmK,
+                       const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
+    return launch_hd<256>(G, p, tmK, tmV, grid, stream);
+}
+
+}  // namespace slotkv

@@ -1,0 +1,436 @@
+// slotkv.cu -- host side of the libslotkv C ABI (declared in include/slotkv.h):
+// handle life cycle, slot offsets, argument checks, the split-K workspace,
+// TMA descriptors for the slot buffers, and kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/slotkv.h"
+#include "params.h"
+
+using slotkv::DecodeParams;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(SLOTKV_ERR_CUDA, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+}
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                    CUtensorMapFloatOOBfill);
+
+encode_tiled_fn get_encoder() {
+    static encode_tiled_fn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<encode_tiled_fn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+struct slotkv_s {
+    int device = 0;
+    uint32_t n_slots = 0, slot_ctx = 0, n_kv_head = 0, head_dim = 0, kv_dim = 0;
+    float* K = nullptr;
+    float* V = nullptr;
+    bool owns_kv = false;
+    uint32_t max_rows = 0, max_n_head = 0;
+    uint32_t chunk_min = 0, max_splits = 0;
+    float* ws_ml = nullptr;
+    float* ws_acc = nullptr;
+    uint32_t* counters = nullptr;
+    uint32_t* status = nullptr;
+    // device staging for decode_batch_attn_host
+    float* st_q = nullptr;
+    float* st_k = nullptr;
+    float* st_v = nullptr;
+    float* st_out = nullptr;
+    uint32_t* st_pos = nullptr;
+    uint32_t* st_slots = nullptr;
+    CUtensorMap tmK, tmV;
+};
+
+namespace {
+
+void free_workspace(slotkv_s* h) {
+    cudaFree(h->ws_ml);
+    cudaFree(h->ws_acc);
+    cudaFree(h->counters);
+    h->ws_ml = h->ws_acc = nullptr;
+    h->counters = nullptr;
+}
+
+void release(slotkv_s* h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_workspace(h);
+    cudaFree(h->status);
+    cudaFree(h->st_q);
+    cudaFree(h->st_k);
+    cudaFree(h->st_v);
+    cudaFree(h->st_out);
+    cudaFree(h->st_pos);
+    cudaFree(h->st_slots);
+    if (h->owns_kv) {
+        cudaFree(h->K);
+        cudaFree(h->V);
+    }
+    delete h;
+}
+
+// Split-K workspace: partial (m, l) and acc per (row, query head, split),
+// plus one finished-split counter per (row, kv head), zeroed.
+int alloc_workspace(slotkv_s* h) {
+    free_workspace(h);
+    const size_t units = (size_t)h->max_rows * h->max_n_head * h->max_splits;
+    cudaError_t e;
+    if ((e = cudaMalloc(&h->ws_ml, units * 2 * sizeof(float))) != cudaSuccess)
+        return cuda_fail(e, "workspace (m, l)");
+    if ((e = cudaMalloc(&h->ws_acc, units * h->head_dim * sizeof(float))) != cudaSuccess)
+        return cuda_fail(e, "workspace (acc)");
+    const size_t nc = (size_t)h->max_rows * h->n_kv_head;
+    if ((e = cudaMalloc(&h->counters, nc * sizeof(uint32_t))) != cudaSuccess)
+        return cuda_fail(e, "workspace (counters)");
+    if ((e = cudaMemset(h->counters, 0, nc * sizeof(uint32_t))) != cudaSuccess)
+        return cuda_fail(e, "workspace clear");
+    return SLOTKV_OK;
+}
+
+int encode_maps(slotkv_s* h) {
+    encode_tiled_fn enc = get_encoder();
+    if (!enc) return fail(SLOTKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {h->kv_dim, (cuuint64_t)h->n_slots * h->slot_ctx};
+    const cuuint64_t strides[1] = {(cuuint64_t)h->kv_dim * sizeof(float)};
+    const cuuint32_t box[2] = {h->head_dim, (cuuint32_t)slotkv::tile_keys((int)h->head_dim)};
+    const cuuint32_t estr[2] = {1, 1};
+    float* bufs[2] = {h->K, h->V};
+    CUtensorMap* maps[2] = {&h->tmK, &h->tmV};
+    for (int i = 0; i < 2; ++i) {
+        CUresult r = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, bufs[i], dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(SLOTKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+    return SLOTKV_OK;
+}
+
+bool valid_handle(slotkv_t h) { return h && h->K && h->V && h->status; }
+
+// The most splits any row of this slot_ctx can need: nsplit(n) <= ceil(n /
+// chunk_min) because chunks are >= chunk_min keys, and <= max_splits.
+uint32_t grid_splits(const slotkv_s* h) {
+    const uint64_t bound = ((uint64_t)h->slot_ctx + h->chunk_min - 1) / h->chunk_min;
+    return (uint32_t)(bound < h->max_splits ? bound : h->max_splits);
+}
+
+int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float* k_new,
+           const float* v_new, const uint32_t* positions, const uint32_t* slots,
+           const float* q_norm_w, const float* k_norm_w, const float* inv_freq,
+           const float* sinks, float* out, float eps, float scale, cudaStream_t stream) {
+    DecodeParams P;
+    P.q = q;
+    P.k_new = k_new;
+    P.v_new = v_new;
+    P.positions = positions;
+    P.slots = slots;
+    P.q_norm_w = q_norm_w;
+    P.k_norm_w = k_norm_w;
+    P.inv_freq = inv_freq;
+    P.sinks = sinks;
+    P.out = out;
+    P.K = h->K;
+    P.V = h->V;
+    P.ws_ml = h->ws_ml;
+    P.ws_acc = h->ws_acc;
+    P.counters = h->counters;
+    P.status = h->status;
+    P.n_slots = h->n_slots;
+    P.slot_ctx = h->slot_ctx;
+    P.n_head = n_head;
+    P.n_kv_head = h->n_kv_head;
+    P.B = B;
+    P.chunk_min = h->chunk_min;
+    P.max_splits = h->max_splits;
+    P.eps = eps;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    const int G = (int)(n_head / h->n_kv_head);
+    dim3 grid(grid_splits(h), h->n_kv_head, B);
+    int rc;
+    switch (h->head_dim) {
+        case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, grid, stream); break;
+        case 128: rc = slotkv::launch_decode_hd128(G, P, h->tmK, h->tmV, grid, stream); break;
+        case 256: rc = slotkv::launch_decode_hd256(G, P, h->tmK, h->tmV, grid, stream); break;
+        default: return fail(SLOTKV_ERR_UNSUPPORTED, "head_dim %u", h->head_dim);
+    }
+    if (rc != 0) return cuda_fail((cudaError_t)rc, "decode kernel launch");
+    return SLOTKV_OK;
+}
+
+int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
+                      const void* k_new, const void* v_new, const void* positions,
+                      const void* slots, const void* q_norm_w, const void* k_norm_w,
+                      const void* inv_freq, const void* out) {
+    if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (B > h->max_rows) return fail(SLOTKV_ERR_ARG, "B=%u exceeds max_rows=%u", B, h->max_rows);
+    if (n_head == 0 || n_head % h->n_kv_head != 0)
+        return fail(SLOTKV_ERR_ARG, "n_head=%u is not a multiple of n_kv_head=%u", n_head,
+                    h->n_kv_head);
+    if (n_head > h->max_n_head)
+        return fail(SLOTKV_ERR_ARG, "n_head=%u exceeds max_n_head=%u", n_head, h->max_n_head);
+    const uint32_t G = n_head / h->n_kv_head;
+    if (G < 1 || G > 8) return fail(SLOTKV_ERR_UNSUPPORTED, "G=%u outside 1..8", G);
+    if (B == 0) return SLOTKV_OK;
+    if (!q || !k_new || !v_new || !positions || !slots || !q_norm_w || !k_norm_w || !inv_freq ||
+        !out)
+        return fail(SLOTKV_ERR_ARG, "null tensor pointer");
+    return SLOTKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* slot_kv_last_error(void) { return g_err; }
+
+int slot_kv_alloc(slotkv_t* handle, uint32_t n_slots, uint32_t slot_ctx, uint32_t n_kv_head,
+                  uint32_t head_dim, float* k_buf, float* v_buf, uint32_t max_rows,
+                  uint32_t max_n_head) {
+    g_err[0] = 0;
+    if (!handle) return fail(SLOTKV_ERR_ARG, "handle pointer is null");
+    if (*handle) {
+        release(*handle);
+        *handle = nullptr;
+    }
+    if (n_slots == 0 || slot_ctx == 0 || n_kv_head == 0)
+        return fail(SLOTKV_ERR_ARG, "n_slots, slot_ctx and n_kv_head must be >= 1");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(SLOTKV_ERR_UNSUPPORTED, "head_dim=%u (64, 128 or 256)", head_dim);
+    // TMA row coordinates are int32: keep every tile start (row + tile) below 2^31
+    if ((uint64_t)n_slots * slot_ctx + 256 >= (1ull << 31))
+        return fail(SLOTKV_ERR_ARG, "n_slots*slot_ctx must be < 2^31 - 256");
+    if ((uint64_t)n_kv_head * head_dim > 65536)
+        return fail(SLOTKV_ERR_ARG, "kv_dim too large");
+    if ((k_buf == nullptr) != (v_buf == nullptr))
+        return fail(SLOTKV_ERR_ARG, "give both k_buf and v_buf, or neither");
+    if ((k_buf && ((uintptr_t)k_buf & 15)) || (v_buf && ((uintptr_t)v_buf & 15)))
+        return fail(SLOTKV_ERR_ARG, "k_buf and v_buf must be 16-byte aligned");
+    if (max_rows == 0 || max_rows > 65535)
+        return fail(SLOTKV_ERR_ARG, "max_rows must be 1..65535");
+    if (max_n_head < n_kv_head || max_n_head > 8 * n_kv_head)
+        return fail(SLOTKV_ERR_ARG, "max_n_head must be n_kv_head..8*n_kv_head");
+
+    slotkv_s* h = new (std::nothrow) slotkv_s();
+    if (!h) return fail(SLOTKV_ERR_ARG, "out of host memory");
+    cudaGetDevice(&h->device);
+    h->n_slots = n_slots;
+    h->slot_ctx = slot_ctx;
+    h->n_kv_head = n_kv_head;
+    h->head_dim = head_dim;
+    h->kv_dim = n_kv_head * head_dim;
+    h->max_rows = max_rows;
+    h->max_n_head = max_n_head;
+    // default split policy: chunks of >= 256 KiB of K+V per kv head, <= 64 splits
+    h->chunk_min = (256u * 1024u) / (8u * head_dim);
+    h->max_splits = 64;
+
+    const size_t elems = (size_t)n_slots * slot_ctx * h->kv_dim;
+    cudaError_t e;
+    int rc = SLOTKV_OK;
+    if (k_buf) {
+        h->K = k_buf;
+        h->V = v_buf;
+        h->owns_kv = false;
+    } else {
+        h->owns_kv = true;
+        if ((e = cudaMalloc(&h->K, elems * sizeof(float))) != cudaSuccess ||
+            (e = cudaMalloc(&h->V, elems * sizeof(float))) != cudaSuccess) {
+            rc = cuda_fail(e, "slot KV allocation");
+        } else if ((e = cudaMemset(h->K, 0, elems * sizeof(float))) != cudaSuccess ||
+                   (e = cudaMemset(h->V, 0, elems * sizeof(float))) != cudaSuccess) {
+            rc = cuda_fail(e, "slot KV clear");
+        }
+    }
+    if (rc == SLOTKV_OK) {
+        if ((e = cudaMalloc(&h->status, sizeof(uint32_t))) != cudaSuccess ||
+            (e = cudaMemset(h->status, 0, sizeof(uint32_t))) != cudaSuccess)
+            rc = cuda_fail(e, "status word");
+    }
+    if (rc == SLOTKV_OK) {
+        const size_t nq = (size_t)max_rows * max_n_head * head_dim;
+        const size_t nk = (size_t)max_rows * h->kv_dim;
+        if ((e = cudaMalloc(&h->st_q, nq * 4)) != cudaSuccess ||
+            (e = cudaMalloc(&h->st_out, nq * 4)) != cudaSuccess ||
+            (e = cudaMalloc(&h->st_k, nk * 4)) != cudaSuccess ||
+            (e = cudaMalloc(&h->st_v, nk * 4)) != cudaSuccess ||
+            (e = cudaMalloc(&h->st_pos, (size_t)max_rows * 4)) != cudaSuccess ||
+            (e = cudaMalloc(&h->st_slots, (size_t)max_rows * 4)) != cudaSuccess)
+            rc = cuda_fail(e, "host-call staging");
+    }
+    if (rc == SLOTKV_OK) rc = alloc_workspace(h);
+    if (rc == SLOTKV_OK) rc = encode_maps(h);
+    if (rc != SLOTKV_OK) {
+        char keep[sizeof(g_err)];
+        memcpy(keep, g_err, sizeof(keep));
+        release(h);
+        memcpy(g_err, keep, sizeof(keep));
+        return rc;
+    }
+    *handle = h;
+    return SLOTKV_OK;
+}
+
+int slot_kv_free(slotkv_t handle) {
+    g_err[0] = 0;
+    release(handle);
+    return SLOTKV_OK;
+}
+
+size_t slot_kv_offset_bytes(slotkv_t h, uint32_t slot, uint32_t pos) {
+    if (!h || slot >= h->n_slots || pos >= h->slot_ctx) return SIZE_MAX;
+    return ((size_t)slot * h->slot_ctx + pos) * h->kv_dim * sizeof(float);
+}
+
+int slot_kv_reset(slotkv_t h, uint32_t slot, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (slot >= h->n_slots) return fail(SLOTKV_ERR_ARG, "slot=%u >= n_slots=%u", slot, h->n_slots);
+    const size_t off = slot_kv_offset_bytes(h, slot, 0);
+    const size_t bytes = (size_t)h->slot_ctx * h->kv_dim * sizeof(float);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync((char*)h->K + off, 0, bytes, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync((char*)h->V + off, 0, bytes, s)) != cudaSuccess)
+        return cuda_fail(e, "slot reset");
+    return SLOTKV_OK;
+}
+
+int slot_kv_k_ptr(slotkv_t h, float** k) {
+    if (!valid_handle(h) || !k) return fail(SLOTKV_ERR_ARG, "bad handle or output pointer");
+    *k = h->K;
+    return SLOTKV_OK;
+}
+
+int slot_kv_v_ptr(slotkv_t h, float** v) {
+    if (!valid_handle(h) || !v) return fail(SLOTKV_ERR_ARG, "bad handle or output pointer");
+    *v = h->V;
+    return SLOTKV_OK;
+}
+
+int slot_kv_geometry(slotkv_t h, uint32_t* n_slots, uint32_t* slot_ctx, uint32_t* n_kv_head,
+                     uint32_t* head_dim, uint32_t* max_rows, uint32_t* max_n_head) {
+    if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (n_slots) *n_slots = h->n_slots;
+    if (slot_ctx) *slot_ctx = h->slot_ctx;
+    if (n_kv_head) *n_kv_head = h->n_kv_head;
+    if (head_dim) *head_dim = h->head_dim;
+    if (max_rows) *max_rows = h->max_rows;
+    if (max_n_head) *max_n_head = h->max_n_head;
+    return SLOTKV_OK;
+}
+
+int decode_batch_attn(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
+                      const float* k_new, const float* v_new, const uint32_t* positions,
+                      const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
+                      const float* inv_freq, const float* sinks, float* out, float eps,
+                      float scale, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, slots, q_norm_w,
+                               k_norm_w, inv_freq, out);
+    if (rc != SLOTKV_OK || B == 0) return rc;
+    return launch(h, B, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
+                  sinks, out, eps, scale, (cudaStream_t)stream);
+}
+
+int decode_batch_attn_host(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
+                           const float* k_new, const float* v_new, const uint32_t* positions,
+                           const uint32_t* slots, const float* q_norm_w,
+                           const float* k_norm_w, const float* inv_freq, const float* sinks,
+                           float* out, float eps, float scale, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, slots, q_norm_w,
+                               k_norm_w, inv_freq, out);
+    if (rc != SLOTKV_OK || B == 0) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
+    const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
+    const size_t ni = (size_t)B * sizeof(uint32_t);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(h->st_q, q, nq, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_k, k_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_v, v_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_pos, positions, ni, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_slots, slots, ni, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "host-to-device input copy");
+    rc = launch(h, B, n_head, h->st_q, h->st_k, h->st_v, h->st_pos, h->st_slots, q_norm_w,
+                k_norm_w, inv_freq, sinks, h->st_out, eps, scale, s);
+    if (rc != SLOTKV_OK) return rc;
+    if ((e = cudaMemcpyAsync(out, h->st_out, nq, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "device-to-host output copy");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+    return SLOTKV_OK;
+}
+
+int slot_kv_get_status(slotkv_t h, slotkv_stream_t stream, uint32_t* flags) {
+    g_err[0] = 0;
+    if (!valid_handle(h) || !flags) return fail(SLOTKV_ERR_ARG, "bad handle or flags pointer");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t v = 0;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return cuda_fail(e, "status read");
+    if (v) {
+        if ((e = cudaMemsetAsync(h->status, 0, sizeof(uint32_t), s)) != cudaSuccess)
+            return cuda_fail(e, "status clear");
+        if (v & SLOTKV_DEV_TIMEOUT) {
+            const size_t nc = (size_t)h->max_rows * h->n_kv_head * sizeof(uint32_t);
+            if ((e = cudaMemsetAsync(h->counters, 0, nc, s)) != cudaSuccess)
+                return cuda_fail(e, "workspace clear");
+        }
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+    }
+    *flags = v;
+    return SLOTKV_OK;
+}
+
+int slot_kv_set_split(slotkv_t h, uint32_t min_chunk_keys, uint32_t max_splits) {
+    g_err[0] = 0;
+    if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    const uint32_t T = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+    if (min_chunk_keys == 0 || min_chunk_keys % T != 0)
+        return fail(SLOTKV_ERR_ARG, "min_chunk_keys must be a positive multiple of %u", T);
+    if (max_splits == 0 || max_splits > 256) return fail(SLOTKV_ERR_ARG, "max_splits 1..256");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "synchronize");
+    h->chunk_min = min_chunk_keys;
+    h->max_splits = max_splits;
+    return alloc_workspace(h);
+}
+
+}  // extern "C"

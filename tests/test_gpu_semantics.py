@@ -1,0 +1,243 @@
+"""Properties of the CUDA path that hold at any size: slot addressing and
+non-overlap, batch and permutation invariance, stale history, precondition
+violations, the host-pointer entry, reset, repeatability."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_slot_kv_gb300 as skv
+import synth
+from gpu_harness import DeviceRun, assert_close, oracle_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _wl(B=8, slot_ctx=700, hd=128, G=4, sinks=True, idx=300):
+    rng = np.random.default_rng(idx)
+    pos = tuple(int(x) for x in rng.integers(0, slot_ctx, size=B))
+    return synth.Workload(f"sem{idx}", idx, B=B, n_slots=B + 4, slot_ctx=slot_ctx,
+                          n_head=2 * G, n_kv_head=2, head_dim=hd, theta=10000.0,
+                          sinks=sinks, pos_rule="fixed", fixed_positions=pos,
+                          slot_rule="perm")
+
+
+def test_slot_kv_smoke_offsets_and_no_overlap():
+    """The pages' slotKvSmoke: a sentinel at (slot 0, pos 0) and a pattern at
+    the last (slot, pos) of K, read back; neither clobbers the other.  The
+    offsets agree with the oracle's everywhere we look."""
+    n_slots, ctx, nkv, hd = 5, 37, 3, 64
+    kv = skv.SlotKV(n_slots, ctx, nkv, hd, max_rows=4, max_n_head=nkv)
+    try:
+        K, V = kv.kv_tensors()
+        assert torch.count_nonzero(K) == 0 and torch.count_nonzero(V) == 0
+        o = oracle.default()
+        for s, p in ((0, 0), (1, 3), (4, 36), (2, 17)):
+            assert kv.offset_bytes(s, p) == o.offset_bytes(s, p, ctx, nkv * hd)
+        assert kv.offset_bytes(n_slots, 0) is None and kv.offset_bytes(0, ctx) is None
+        row = nkv * hd
+        flatK = K.view(-1)
+        first = kv.offset_bytes(0, 0) // 4
+        last = kv.offset_bytes(n_slots - 1, ctx - 1) // 4
+        flatK[first: first + row] = 1234.5
+        flatK[last: last + row] = torch.arange(row, dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        assert torch.all(flatK[first: first + row] == 1234.5)
+        assert torch.equal(flatK[last: last + row], torch.arange(row, dtype=torch.float32,
+                                                                  device="cuda"))
+        assert last + row == flatK.numel()
+        assert torch.count_nonzero(flatK[first + row: last]) == 0
+    finally:
+        kv.free()
+
+
+@pytest.mark.parametrize("split", [None, (32, 8)])
+def test_rows_are_independent_bit_exact(split):
+    """One B-row call equals B one-row calls bit for bit (the split depends
+    on the row's own position only), and permuting rows permutes outputs."""
+    w = _wl()
+    run = DeviceRun(w, split=split)
+    try:
+        q, kn, vn, pos = run.inputs(0)
+        K0, V0 = run.K.clone(), run.V.clone()
+        full = run.step(0).cpu()
+        Kfull, Vfull = run.K.clone(), run.V.clone()
+        run.K.copy_(K0)
+        run.V.copy_(V0)
+        for b in range(w.B):
+            out1 = torch.full((1, w.n_head, w.head_dim), float("nan"), device="cuda")
+            run.kv.decode_batch_attn(to_dev(q[b:b + 1]), to_dev(kn[b:b + 1]),
+                                     to_dev(vn[b:b + 1]), to_dev(pos[b:b + 1].astype(np.int32)),
+                                     run.slots[b:b + 1].contiguous(), run.qw, run.kw, run.inv,
+                                     run.sinks, out1, w.eps, w.scale)
+            assert torch.equal(out1.cpu()[0], full[b]), f"row {b} differs alone"
+        assert torch.equal(run.K, Kfull) and torch.equal(run.V, Vfull)
+        perm = np.array([3, 0, 7, 1, 6, 2, 5, 4])
+        run.K.copy_(K0)
+        run.V.copy_(V0)
+        outp = torch.full_like(full.cuda(), float("nan"))
+        run.kv.decode_batch_attn(to_dev(q[perm]), to_dev(kn[perm]), to_dev(vn[perm]),
+                                 to_dev(pos[perm].astype(np.int32)),
+                                 to_dev(run.slots_np[perm].astype(np.int32)), run.qw, run.kw,
+                                 run.inv, run.sinks, outp, w.eps, w.scale)
+        assert torch.equal(outp.cpu(), full[perm])
+        assert run.status() == 0
+    finally:
+        run.close()
+
+
+def test_stale_history_is_never_read():
+    """NaN in every position after pos of each row's slot changes nothing."""
+    w = _wl(sinks=False, idx=301)
+    run = DeviceRun(w)
+    try:
+        K0, V0 = run.K.clone(), run.V.clone()
+        a = run.step(0).cpu()
+        run.K.copy_(K0)
+        run.V.copy_(V0)
+        pos = w.positions0()
+        for b in range(w.B):
+            s = int(run.slots_np[b])
+            run.K[s, pos[b] + 1:] = float("nan")
+            run.V[s, pos[b] + 1:] = float("nan")
+        b_ = run.step(0).cpu()
+        assert torch.equal(a, b_)
+    finally:
+        run.close()
+
+
+def test_out_of_range_rows_are_skipped_and_flagged():
+    w = _wl(B=4, idx=302)
+    run = DeviceRun(w)
+    try:
+        q, kn, vn, pos = run.inputs(0)
+        pos = pos.copy()
+        slots = run.slots_np.copy()
+        pos[1] = w.slot_ctx                 # position out of range
+        slots[2] = w.n_slots + 7            # slot out of range
+        K0, V0 = run.K.clone(), run.V.clone()
+        out = torch.full((w.B, w.n_head, w.head_dim), 7.0, device="cuda")
+        run.kv.decode_batch_attn(to_dev(q), to_dev(kn), to_dev(vn), to_dev(pos.astype(np.int32)),
+                                 to_dev(slots.astype(np.int32)), run.qw, run.kw, run.inv,
+                                 run.sinks, out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert run.status() & skv.DEV_RANGE
+        assert run.status() == 0            # read-and-clear
+        got = out.cpu().numpy()
+        assert np.all(got[1] == 7.0) and np.all(got[2] == 7.0)
+        ref, _, _ = oracle_rows(w, [0, 3])
+        assert_close(got[[0, 3]], ref[0], "in-range rows")
+        # only rows 0 and 3 wrote
+        changed = torch.nonzero((run.K != K0).any(-1).any(-1)).cpu().numpy().tolist()
+        want = sorted([[int(slots[b]), int(pos[b])] for b in (0, 3)])
+        assert sorted(changed) == want
+    finally:
+        run.close()
+
+
+def test_zero_rows_is_a_no_op():
+    w = _wl(B=2, idx=303)
+    run = DeviceRun(w)
+    try:
+        e = torch.empty(0, device="cuda")
+        rc = skv._lib.decode_batch_attn(run.kv._h, 0, w.n_head, e.data_ptr(), e.data_ptr(),
+                                        e.data_ptr(), e.data_ptr(), e.data_ptr(),
+                                        run.qw.data_ptr(), run.kw.data_ptr(), run.inv.data_ptr(),
+                                        None, e.data_ptr(), w.eps, w.scale, None)
+        assert rc == 0
+    finally:
+        run.close()
+
+
+def test_host_entry_equals_device_entry():
+    w = _wl(idx=304)
+    run = DeviceRun(w)
+    try:
+        K0, V0 = run.K.clone(), run.V.clone()
+        dev = run.step(0).cpu()
+        Kd = run.K.clone()
+        run.K.copy_(K0)
+        run.V.copy_(V0)
+        q, kn, vn, pos = run.inputs(0)
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        out_h = torch.full((w.B, w.n_head, w.head_dim), float("nan")).pin_memory()
+        run.kv.decode_batch_attn_host(pin(q), pin(kn), pin(vn), pin(pos.astype(np.int32)),
+                                      pin(run.slots_np.astype(np.int32)), run.qw, run.kw,
+                                      run.inv, run.sinks, out_h, w.eps, w.scale)
+        assert torch.equal(out_h, dev)
+        assert torch.equal(run.K, Kd)
+    finally:
+        run.close()
+
+
+def test_reset_zeroes_exactly_one_slot():
+    w = _wl(B=2, idx=305)
+    run = DeviceRun(w)
+    try:
+        K0 = run.K.clone()
+        run.kv.reset(3)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(run.K[3]) == 0 and torch.count_nonzero(run.V[3]) == 0
+        keep = [s for s in range(w.n_slots) if s != 3]
+        assert torch.equal(run.K[keep], K0[keep])
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("split", [None, (32, 16)])
+def test_repeated_calls_are_identical(split):
+    """Re-running a step at the same positions rewrites the same bytes and
+    gives the same output (the merge counters reset themselves)."""
+    w = _wl(idx=306, slot_ctx=3000)
+    run = DeviceRun(w, split=split)
+    try:
+        outs = [run.step(0).cpu() for _ in range(4)]
+        for o in outs[1:]:
+            assert torch.equal(o, outs[0])
+        assert run.status() == 0
+    finally:
+        run.close()
+
+
+def test_argument_errors():
+    w = _wl(B=2, idx=307)
+    run = DeviceRun(w)
+    try:
+        q, kn, vn, pos = run.inputs(0)
+        out = torch.empty((w.B, w.n_head, w.head_dim), device="cuda")
+        with pytest.raises(skv.SlotKVError) as ei:      # B > max_rows
+            big = np.concatenate([q] * 3)
+            run.kv.decode_batch_attn(to_dev(big), to_dev(kn), to_dev(vn),
+                                     to_dev(pos.astype(np.int32)), run.slots, run.qw, run.kw,
+                                     run.inv, None, out, w.eps, w.scale)
+        assert ei.value.code == 1
+        with pytest.raises(skv.SlotKVError):            # null output
+            rc = skv._lib.decode_batch_attn(run.kv._h, w.B, w.n_head, 1, 1, 1, 1, 1, 1, 1, 1,
+                                            None, None, w.eps, w.scale, None)
+            skv._check(rc, "decode_batch_attn")
+        with pytest.raises(skv.SlotKVError):
+            run.kv.set_split(5, 8)                       # not a multiple of the tile
+        h = ctypes.c_void_p()
+        rc = skv._lib.slot_kv_alloc(ctypes.byref(h), 4, 16, 2, 96, None, None, 2, 2)
+        assert rc == 3 and not h.value                   # head_dim 96 unsupported
+    finally:
+        run.close()
+
+
+def test_realloc_frees_first():
+    """slot_kv_alloc on a live handle frees it and allocates anew (the pages'
+    allocSlotKv is re-callable)."""
+    h = ctypes.c_void_p()
+    assert skv._lib.slot_kv_alloc(ctypes.byref(h), 4, 64, 2, 64, None, None, 4, 8) == 0
+    first = h.value
+    assert skv._lib.slot_kv_alloc(ctypes.byref(h), 8, 32, 2, 128, None, None, 4, 8) == 0
+    assert h.value
+    ctx = ctypes.c_uint32()
+    hd = ctypes.c_uint32()
+    assert skv._lib.slot_kv_geometry(h, None, ctypes.byref(ctx), None, ctypes.byref(hd),
+                                     None, None) == 0
+    assert (ctx.value, hd.value) == (32, 128)
+    assert skv._lib.slot_kv_free(h) == 0
+    del first
