@@ -181,6 +181,60 @@ int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const f
                            float eps, float scale, slotkv_stream_t stream);
 
 /*
+ * decode_batch_attn_noalloc -- the same decode step as decode_batch_attn for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * to this entry point.
+ *
+ * Who needs it: code that runs under a host framework which owns every byte
+ * of device memory (its own pool or a fixed budget), and code paths that
+ * cannot afford the device-wide synchronisation cudaMalloc and cudaFree may
+ * cause.  decode_batch_attn needs a handle, and slot_kv_alloc allocates.
+ * This call needs no handle and allocates nothing, directly or through any
+ * library.
+ *
+ * Scratch: the split-K partials, the merge counters and a status word live in
+ * one fixed device array of SLOTKV_NOALLOC_SCRATCH_BYTES inside the library.
+ * Every GPU that loads the library holds it until the process exits.  A batch
+ * needs 256 + align256(4*B*n_kv_head) + align256(8*B*n_head*16) +
+ * 4*B*n_head*16*head_dim bytes of it (up to 16 splits per row).  A batch that
+ * needs more is rejected with SLOTKV_ERR_ARG and a message naming both sizes;
+ * use decode_batch_attn with a handle then.
+ * All calls in the process share the array, which keeps the last call's
+ * contents.  Each call clears the status word and the counters first, on
+ * `stream`.  Calls that overlap on the GPU (different streams, or different
+ * host threads without ordering) race on it: order them.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * with that device current and caches it.  Make that first call before any
+ * stream capture begins.
+ *
+ *   K, V        device slot buffers, [n_slots][slot_ctx][n_kv_head][head_dim]
+ *               f32, 16-byte aligned (the caller owns them).
+ *   n_slots, slot_ctx, n_kv_head, head_dim
+ *               their geometry (head_dim 64, 128 or 256; n_slots*slot_ctx
+ *               < 2^31 - 256).
+ *   B, n_head, q ... out, eps, scale, stream
+ *               as decode_batch_attn (B <= 65535; G = n_head/n_kv_head 1..8).
+ *   dev_flags   device u32 that receives the SLOTKV_DEV_* flags raised by
+ *               this call (OR-ed in; the caller clears it), or NULL to
+ *               discard them.
+ *
+ * Returns SLOTKV_OK, SLOTKV_ERR_ARG, SLOTKV_ERR_UNSUPPORTED or
+ * SLOTKV_ERR_CUDA; slot_kv_last_error() says why.  Results match
+ * decode_batch_attn's within f32 rounding: rows with more than 16 chunks of
+ * the default size are split into 16 larger chunks instead.
+ */
+#define SLOTKV_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int decode_batch_attn_noalloc(float* K, float* V, uint32_t n_slots, uint32_t slot_ctx,
+                              uint32_t n_kv_head, uint32_t head_dim, uint32_t B,
+                              uint32_t n_head, const float* q, const float* k_new,
+                              const float* v_new, const uint32_t* positions,
+                              const uint32_t* slots, const float* q_norm_w,
+                              const float* k_norm_w, const float* inv_freq,
+                              const float* sinks, float* out, uint32_t* dev_flags,
+                              float eps, float scale, slotkv_stream_t stream);
+
+/*
  * slot_kv_get_status -- synchronise `stream`, return the sticky device flags
  * (SLOTKV_DEV_*) raised since the last call in *flags, and clear them.  After
  * SLOTKV_DEV_TIMEOUT the workspace is also cleared so later calls are valid.

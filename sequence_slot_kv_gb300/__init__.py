@@ -17,7 +17,7 @@ import os
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "slot_kv_get_status",
-    "slot_kv_set_split", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
+    "slot_kv_set_split", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libslotkv.so")
@@ -41,6 +41,9 @@ EXPORTS = {
     "decode_batch_attn_host": (_DECODE_ARGS, _int),
     "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
     "slot_kv_set_split": ([_vp, _u32, _u32], _int),
+    "decode_batch_attn_noalloc": ([_vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp],
+                                  _int),
     "slot_kv_last_error": ([], ctypes.c_char_p),
 }
 
@@ -250,3 +253,26 @@ def slot_kv_get_status(h, stream=None):
 
 def slot_kv_set_split(h, min_chunk_keys, max_splits):
     h.set_split(min_chunk_keys, max_splits)
+
+
+def decode_batch_attn_noalloc(K, V, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                              inv_freq, sinks, out, eps, scale, dev_flags=None, stream=None):
+    """The decode step for callers that cannot allocate device memory: no
+    handle; the slot buffers K, V ([n_slots][slot_ctx][n_kv_head][head_dim]
+    torch CUDA tensors) and every input and output come from the caller, and
+    the library's split-K scratch is a fixed array inside it.  ``dev_flags``
+    is an optional int32 CUDA tensor of one element that receives the device
+    flags.  The first call on a device should come before any stream capture;
+    calls that overlap on the GPU race on the shared scratch."""
+    import torch
+    n_slots, slot_ctx, n_kv_head, head_dim = (int(x) for x in K.shape)
+    B, n_head = int(q.shape[0]), int(q.shape[1])
+    f, u = torch.float32, torch.int32
+    _check(_lib.decode_batch_attn_noalloc(
+        _ptr(K, f, "K"), _ptr(V, f, "V"), n_slots, slot_ctx, n_kv_head, head_dim, B, n_head,
+        _ptr(q, f, "q"), _ptr(k_new, f, "k_new"), _ptr(v_new, f, "v_new"),
+        _ptr(positions, u, "positions"), _ptr(slots, u, "slots"), _ptr(q_norm_w, f, "q_norm_w"),
+        _ptr(k_norm_w, f, "k_norm_w"), _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"),
+        _ptr(out, f, "out"), _ptr(dev_flags, u, "dev_flags"), eps, scale, _stream_ptr(stream)),
+        "decode_batch_attn_noalloc")
+    return out

@@ -1,0 +1,187 @@
+// noalloc.cu -- decode_batch_attn_noalloc: the batched decode attention step
+// for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: a host framework may own every byte of
+// device memory through its own pool or budget, or the calling code path may
+// not tolerate the device synchronisation that cudaMalloc/cudaFree can imply.
+// The regular entry point needs a handle from slot_kv_alloc, which allocates
+// the split-K workspace.  This entry point takes the slot K/V buffers and
+// every input and output from the caller and allocates nothing: the split-K
+// partials, the merge counters and a status word live in one file-scope
+// device array of fixed size (kNoAllocScratchBytes), which every GPU that
+// loads the library holds until the process exits.
+//
+// It launches the same fused kernel as decode_batch_attn.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/slotkv.h"
+#include "params.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = SLOTKV_NOALLOC_SCRATCH_BYTES;
+// split policy of this entry point: at most 16 splits per row keeps the
+// partials of typical batches inside the fixed scratch
+constexpr uint32_t kNoAllocMaxSplits = 16;
+constexpr int kMaxDevices = 64;
+
+// The scratch.  In host code this name is only a stand-in for the symbol; the
+// device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Failures are reported like every other call: a status code, and a message
+// for slot_kv_last_error().
+int noalloc_fail(int code, const char* fmt, ...) {
+    char msg[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(msg, sizeof(msg), fmt, ap);
+    va_end(ap);
+    slotkv::set_last_error(msg);
+    return code;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                    CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+extern "C" int decode_batch_attn_noalloc(
+    float* K, float* V, uint32_t n_slots, uint32_t slot_ctx, uint32_t n_kv_head,
+    uint32_t head_dim, uint32_t B, uint32_t n_head, const float* q, const float* k_new,
+    const float* v_new, const uint32_t* positions, const uint32_t* slots,
+    const float* q_norm_w, const float* k_norm_w, const float* inv_freq, const float* sinks,
+    float* out, uint32_t* dev_flags, float eps, float scale, slotkv_stream_t stream) {
+    slotkv::set_last_error("");
+    if (B == 0) return SLOTKV_OK;
+    if (!K || !V || !q || !k_new || !v_new || !positions || !slots || !q_norm_w || !k_norm_w ||
+        !inv_freq || !out)
+        return noalloc_fail(SLOTKV_ERR_ARG, "null tensor pointer");
+    if (((uintptr_t)K & 15) || ((uintptr_t)V & 15))
+        return noalloc_fail(SLOTKV_ERR_ARG, "K and V must be 16-byte aligned");
+    if (n_slots == 0 || slot_ctx == 0 || n_kv_head == 0)
+        return noalloc_fail(SLOTKV_ERR_ARG, "n_slots, slot_ctx and n_kv_head must be >= 1");
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return noalloc_fail(SLOTKV_ERR_UNSUPPORTED, "head_dim=%u (64, 128 or 256)", head_dim);
+    if ((uint64_t)n_slots * slot_ctx + 256 >= (1ull << 31))
+        return noalloc_fail(SLOTKV_ERR_ARG, "n_slots*slot_ctx must be < 2^31 - 256");
+    if (n_head == 0 || n_head % n_kv_head != 0 || n_head / n_kv_head > 8)
+        return noalloc_fail(SLOTKV_ERR_UNSUPPORTED, "n_head/n_kv_head must be 1..8");
+    if (B > 65535) return noalloc_fail(SLOTKV_ERR_ARG, "B must be <= 65535");
+
+    // scratch layout: status word | counters [B][n_kv_head] | (m, l) | acc
+    const uint32_t chunk_min = (256u * 1024u) / (8u * head_dim);
+    const size_t units = (size_t)B * n_head * kNoAllocMaxSplits;
+    const size_t off_cnt = 256;
+    const size_t off_ml = off_cnt + align256((size_t)B * n_kv_head * sizeof(uint32_t));
+    const size_t off_acc = off_ml + align256(units * 2 * sizeof(float));
+    const size_t need = off_acc + units * head_dim * sizeof(float);
+    if (need > kNoAllocScratchBytes)
+        return noalloc_fail(SLOTKV_ERR_ARG,
+                            "batch needs %zu bytes of scratch; decode_batch_attn_noalloc holds "
+                            "%zu (use decode_batch_attn with a handle for larger batches)",
+                            need, kNoAllocScratchBytes);
+
+    // once per device, with that device current: the scratch's device address
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return noalloc_fail(SLOTKV_ERR_CUDA, "cudaGetDevice failed");
+    unsigned char* scratch;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        if (!g_scratch_addr[dev]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr)
+                return noalloc_fail(SLOTKV_ERR_CUDA, "cudaGetSymbolAddress: %s",
+                                    cudaGetErrorString(e));
+            g_scratch_addr[dev] = ptr;
+        }
+        scratch = static_cast<unsigned char*>(g_scratch_addr[dev]);
+    }
+
+    // the status word and the merge counters must start at zero
+    cudaStream_t s = (cudaStream_t)stream;
+    e = cudaMemsetAsync(scratch, 0, off_ml, s);
+    if (e != cudaSuccess)
+        return noalloc_fail(SLOTKV_ERR_CUDA, "scratch clear: %s", cudaGetErrorString(e));
+
+    // TMA descriptors for the caller's K and V (host-side encoding only)
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &qres) != cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess || !fn)
+        return noalloc_fail(SLOTKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    encode_tiled_fn enc = reinterpret_cast<encode_tiled_fn>(fn);
+    const uint32_t kv_dim = n_kv_head * head_dim;
+    const cuuint64_t dims[2] = {kv_dim, (cuuint64_t)n_slots * slot_ctx};
+    const cuuint64_t strides[1] = {(cuuint64_t)kv_dim * sizeof(float)};
+    const cuuint32_t box[2] = {head_dim, (cuuint32_t)slotkv::tile_keys((int)head_dim)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap tmK, tmV;
+    if (enc(&tmK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, K, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, V, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return noalloc_fail(SLOTKV_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+
+    slotkv::DecodeParams P;
+    P.q = q;
+    P.k_new = k_new;
+    P.v_new = v_new;
+    P.positions = positions;
+    P.slots = slots;
+    P.q_norm_w = q_norm_w;
+    P.k_norm_w = k_norm_w;
+    P.inv_freq = inv_freq;
+    P.sinks = sinks;
+    P.out = out;
+    P.K = K;
+    P.V = V;
+    P.status = dev_flags ? dev_flags : reinterpret_cast<uint32_t*>(scratch);
+    P.counters = reinterpret_cast<uint32_t*>(scratch + off_cnt);
+    P.ws_ml = reinterpret_cast<float*>(scratch + off_ml);
+    P.ws_acc = reinterpret_cast<float*>(scratch + off_acc);
+    P.n_slots = n_slots;
+    P.slot_ctx = slot_ctx;
+    P.n_head = n_head;
+    P.n_kv_head = n_kv_head;
+    P.B = B;
+    P.chunk_min = chunk_min;
+    P.max_splits = kNoAllocMaxSplits;
+    P.eps = eps;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    const uint64_t bound = ((uint64_t)slot_ctx + chunk_min - 1) / chunk_min;
+    const uint32_t splits = (uint32_t)(bound < kNoAllocMaxSplits ? bound : kNoAllocMaxSplits);
+    const dim3 grid(splits, n_kv_head, B);
+    const int G = (int)(n_head / n_kv_head);
+    int rc;
+    switch (head_dim) {
+        case 64: rc = slotkv::launch_decode_hd64(G, P, tmK, tmV, grid, s); break;
+        case 128: rc = slotkv::launch_decode_hd128(G, P, tmK, tmV, grid, s); break;
+        default: rc = slotkv::launch_decode_hd256(G, P, tmK, tmV, grid, s); break;
+    }
+    if (rc != 0)
+        return noalloc_fail(SLOTKV_ERR_CUDA, "decode kernel launch: %s",
+                            cudaGetErrorString((cudaError_t)rc));
+    return SLOTKV_OK;
+}

@@ -43,6 +43,9 @@ __host__ __device__ inline uint32_t split_chunk(uint32_t n_keys, uint32_t chunk_
 // Tile height (keys per pipeline stage) for a head dim: 16 KiB of K + 16 KiB of V.
 __host__ __device__ constexpr int tile_keys(int hd) { return 4096 / hd; }
 
+// Sets the calling thread's slot_kv_last_error() message.
+void set_last_error(const char* msg);
+
 // Launchers, one translation unit per head dim.  Return a cudaError_t value.
 int launch_decode_hd64(int G, const DecodeParams& p, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);

@@ -213,6 +213,10 @@ int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
 
 }  // namespace
 
+namespace slotkv {
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+}  // namespace slotkv
+
 extern "C" {
 
 const char* slot_kv_last_error(void) { return g_err; }
