@@ -195,10 +195,11 @@ int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const f
  * Scratch: the split-K partials, the merge counters and a status word live in
  * one fixed device array of SLOTKV_NOALLOC_SCRATCH_BYTES inside the library.
  * Every GPU that loads the library holds it until the process exits.  A batch
- * needs 256 + align256(4*B*n_kv_head) + align256(8*B*n_head*16) +
- * 4*B*n_head*16*head_dim bytes of it (up to 16 splits per row).  A batch that
- * needs more is rejected with SLOTKV_ERR_ARG and a message naming both sizes;
- * use decode_batch_attn with a handle then.
+ * needs 256 + align256(4*B*n_kv_head) + align256(256*B*n_kv_head) +
+ * align256(128*B*n_head) + 64*B*n_head*head_dim bytes of it (work list and
+ * partials for up to 16 splits per row).  A batch that needs more is rejected
+ * with SLOTKV_ERR_ARG and a message naming both sizes; use decode_batch_attn
+ * with a handle then.
  * All calls in the process share the array, which keeps the last call's
  * contents.  Each call clears the status word and the counters first, on
  * `stream`.  Calls that overlap on the GPU (different streams, or different
@@ -249,7 +250,7 @@ int slot_kv_get_status(slotkv_t handle, slotkv_stream_t stream, uint32_t* flags)
  * on the other rows, so a row's result is the same in any batch.
  * min_chunk_keys must be a positive multiple of the tile (4096 / head_dim
  * keys); max_splits 1..256.  Reallocates the workspace (synchronises).
- * The defaults are min_chunk_keys = 256 KiB of K+V per kv head and
+ * The defaults are min_chunk_keys = 512 KiB of K+V per kv head and
  * max_splits = 64.
  */
 int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_splits);

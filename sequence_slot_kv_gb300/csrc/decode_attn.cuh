@@ -1,26 +1,35 @@
-// decode_attn.cuh -- the fused batched decode attention kernel over slot KV.
+// decode_attn.cuh -- the fused batched decode attention over slot KV.
 //
-// One CTA handles one work item (row b, kv head g, split s): the keys
-// [s*C, min((s+1)*C, p+1)) of slot slots[b] for the G query heads that share
-// kv head g (GQA), so every history K/V byte is read from HBM exactly once.
+// Work item = (row b, kv head g, split s): the keys [s*C, min((s+1)*C, p+1))
+// of slot slots[b] for the G query heads that share kv head g (GQA), so every
+// history K/V byte is read from HBM exactly once.  C depends only on the
+// row's own p (see split_chunk), never on the batch.
 //
-// Per CTA (the steps of "Forward Cuda Gemma", decodeBatch, fused):
-//   * warp 4 (producer): streams the history K and V tiles of the chunk into
-//     a 3-stage shared-memory ring with 2-D TMA copies (cp.async.bulk.tensor,
-//     one [T keys x hd] box per tensor per stage) signalled on mbarriers;
-//   * warps 0-3 (consumers): meanwhile per-head RMS-norm + RoPE of the G query
-//     vectors (pre-multiplied by scale*log2 e) and, in the split holding key p,
-//     of k_new; then for each tile, groups of L lanes each own one key: every
-//     lane holds E = hd/L elements of the G queries and of G output
-//     accumulators in registers, forms partial dots, reduces them with
-//     xor-shuffles, and runs a base-2 online softmax that rescales only when
-//     its running max grows;
-//   * the split holding key p adds that key from shared memory (its K is the
-//     freshly normed+rotated k', its V the raw v_new) and writes both rows to
-//     the slot buffers at (slot*slot_ctx + p)*kv_dim;
-//   * the groups' (m, l, acc) are merged in shared memory; a single-split row
-//     writes out directly, otherwise the partial goes to the workspace and the
-//     last CTA of the (row, kv head) to finish merges the splits in split order.
+// Two kernels per call, on one stream:
+//   * slotkv_plan_kernel (one CTA): checks every row's slot and position,
+//     lists the valid work items and resets the hand-out counter;
+//   * slotkv_decode_attn_kernel (persistent, 2 CTAs per SM, launched as a
+//     programmatic dependent of the plan): each CTA runs until the list is
+//     exhausted.  The steps of "Forward Cuda Gemma", decodeBatch, fused:
+//       - warp 4 (producer) takes items from the list and streams their
+//         history K and V tiles into a 3-stage shared-memory ring with 2-D
+//         TMA copies (cp.async.bulk.tensor, one [T keys x hd] box per tensor
+//         per stage) on mbarriers.  It runs ahead across item boundaries, so
+//         the stream does not stop while the consumers start or finish an item;
+//       - warps 0-3 (consumers), per item: per-head RMS norm + RoPE of the G
+//         query vectors (pre-scaled by scale*log2 e) and, in the split that
+//         holds key p, of k_new; then for each tile, groups of L lanes each
+//         take one key: every lane keeps E = hd/L elements of the G queries
+//         and of G output accumulators in registers, forms partial dots,
+//         reduces them with xor shuffles and runs a base-2 online softmax that
+//         rescales only when its running max grows;
+//       - the split holding key p adds that key from shared memory (its K is
+//         the freshly normed+rotated k', its V the raw v_new) and writes both
+//         rows into the slot buffers at (slot*slot_ctx + p)*kv_dim;
+//       - the groups' (m, l, acc) merge by shuffles within each warp, then
+//         across the four warps in shared memory; a one-split row writes out,
+//         otherwise the partial goes to the workspace and the last CTA of the
+//         (row, kv head) to finish merges the splits in split order.
 //
 // Every wait on an mbarrier is bounded; on expiry the CTA raises
 // SLOTKV_DEV_TIMEOUT, drains its own copies in flight (bounded) and returns.
@@ -37,6 +46,7 @@ namespace slotkv {
 
 constexpr uint32_t kDevRange = 1u;
 constexpr uint32_t kDevTimeout = 2u;
+constexpr int kPlanThreads = 1024;
 
 __host__ __device__ constexpr int pow2_floor(int x) {
     int r = 1;
@@ -48,9 +58,16 @@ __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 template <int HD, int G>
 struct KCfg {
-    static constexpr int W = 4;                   // consumer warps
+    static constexpr int W = 4;                   // consumer warps (warpgroup 0)
     static constexpr int CONS = W * 32;           // consumer threads
-    static constexpr int THREADS = CONS + 32;     // + one producer warp
+    // + warpgroup 1: warp 4 streams (TMA), warp 5 prepares the next item's
+    // vectors, warp 6 merges splits, warp 7 only hands its registers over
+    static constexpr int THREADS = CONS + 128;
+    static constexpr int WARP_TMA = 4, WARP_PREP = 5, WARP_MERGE = 6;
+    // registers per thread: launched at 128 (two CTAs per SM), then moved from
+    // warpgroup 1 to warpgroup 0: 128 * REG_CONS + 128 * REG_HELP = 256 * 128
+    static constexpr int REG_CONS = 184;
+    static constexpr int REG_HELP = 72;
     static constexpr int S = 3;                   // pipeline stages
     static constexpr int T = tile_keys(HD);       // keys per tile
     // elements per lane: keep G*E <= 64 (queries + accumulators in registers)
@@ -62,25 +79,47 @@ struct KCfg {
     static constexpr int RC = pow2_floor(cmax(1, cmin(R, 16 / G)));
     static constexpr int TILE_BYTES = T * HD * 4;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int OFF_QS = S * STAGE_BYTES;
-    static constexpr int OFF_KS = OFF_QS + G * HD * 4;
-    static constexpr int OFF_VS = OFF_KS + HD * 4;
-    static constexpr int OFF_CS = OFF_VS + HD * 4;
-    static constexpr int OFF_SN = OFF_CS + HD * 2;
-    static constexpr int OFF_BAR = OFF_SN + HD * 2;
-    static constexpr int OFF_MISC = OFF_BAR + 2 * S * 8;
+    static constexpr int NMS = 4;                 // split-merge hand-off slots
+    // shared memory: ring | chain scratch acc [G][HD], m, l [G] | per-item
+    // slots [2] of (q [G][HD], k [HD], v [HD]) | norm weights, inv_freq |
+    // item descriptors [2] | hand-offs [NMS] | mbarriers | flags
+    static constexpr int OFF_CHAIN = S * STAGE_BYTES;
+    static constexpr int CHAIN_FLOATS = (G * HD + 2 * G + 3) / 4 * 4;
+    static constexpr int OFF_QBUF = OFF_CHAIN + CHAIN_FLOATS * 4;
+    static constexpr int OFF_KBUF = OFF_QBUF + 2 * G * HD * 4;
+    static constexpr int OFF_VBUF = OFF_KBUF + 2 * HD * 4;
+    static constexpr int OFF_QW = OFF_VBUF + 2 * HD * 4;
+    static constexpr int OFF_KW = OFF_QW + HD * 4;
+    static constexpr int OFF_IF = OFF_KW + HD * 4;
+    static constexpr int OFF_DESC = OFF_IF + HD * 2;
+    static constexpr int OFF_HAND = OFF_DESC + 2 * 64;
+    static constexpr int OFF_BAR = OFF_HAND + NMS * 16;
+    // mbarriers: full[S], empty[S], staged[2], prepared[2], slot_free[2],
+    // handed[NMS], hand_free[NMS]
+    static constexpr int NBAR = 2 * S + 6 + 2 * NMS;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16;
     static_assert(L >= 1 && L <= 32 && (32 % L) == 0, "lane group must divide a warp");
     static_assert(E % 4 == 0 && E * L == HD, "lane slice must be whole float4s");
     static_assert(R >= 1 && R * NG == T, "tile must split evenly over the groups");
     static_assert(R % RC == 0, "row chunks must divide the rows per tile");
     static_assert(G * E <= 64, "register budget");
-    // merge scratch (reuses the stage ring): acc [NG][G][HD], m, l [NG][G],
-    // merged max/sum [G], weights [NG][G] or [G][max_splits]
-    static_assert(NG * G * HD * 4 + 4 * NG * G * 4 + 2 * G * 4 + G * 256 * 4 <=
-                      S * STAGE_BYTES,
-                  "merge scratch must fit in the stage ring");
     static_assert(HD == 64 || HD == 128 || HD == 256, "head dim");
+    static_assert(OFF_CHAIN % 16 == 0 && OFF_QBUF % 16 == 0 && OFF_KBUF % 16 == 0 &&
+                      OFF_VBUF % 16 == 0 && OFF_BAR % 8 == 0,
+                  "alignment");
+    static_assert(CONS * REG_CONS + 128 * REG_HELP == THREADS * 128,
+                  "register hand-over must add up to the launch's registers");
+};
+
+// What the producer tells the other warps about an item.
+struct ItemDesc {
+    uint32_t b, kvh, split, nsplit, p, slot, k0, hist_end, ntiles, is_last, end, pad;
+};
+
+// A finished multi-split partial handed to the merge warp.
+struct HandOff {
+    uint32_t b, kvh, nsplit, end;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -113,6 +152,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test: has the phase of `bar` with parity `parity` completed?
+// (try_wait may suspend the thread for a while; this never does.)
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Bounded by
 // both an iteration count and about 2^31 SM clocks (~1 s); false on expiry.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
@@ -135,9 +188,49 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Contiguous global -> shared copy on the async proxy, completing on `bar`.
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// atomicAdd with acquire-release semantics at GPU scope.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Warpgroup register re-allocation (all four warps of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int N>
 __device__ __forceinline__ void named_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Programmatic dependent launch: let the dependent grid start launching.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Attend NR keys held in shared memory rows (row[r] of the K tile Kt and V
@@ -223,348 +316,726 @@ __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
     }
 }
 
+// exp2(m - M) as the weight of a partial whose running max is m, with an
+// empty partial (m = -inf) weighing 0 even when M is -inf too.
+__device__ __forceinline__ float partial_weight(float m, float M) {
+    return m == -CUDART_INF_F ? 0.f : exp2f(m - M);
+}
+
+// ------------------------------------------------------------------ plan
+// One CTA.  Lists every valid (row, split, kv head) in row order as a
+// 16-byte record (packed item, position, slot), raises
+// SLOTKV_DEV_RANGE for rows whose slot or position is out of range (they get
+// no items), and resets the hand-out counter.
+template <int T>
+__global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const DecodeParams P) {
+    __shared__ uint32_t warp_tot[kPlanThreads / 32];
+    __shared__ uint32_t row_first[kPlanThreads];
+    __shared__ uint32_t row_n[kPlanThreads];
+    __shared__ uint32_t row_p[kPlanThreads];
+    __shared__ uint32_t row_slot[kPlanThreads];
+    __shared__ uint32_t base;
+    grid_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) base = 0;
+    __syncthreads();
+    for (uint32_t c0 = 0; c0 < P.B; c0 += kPlanThreads) {
+        const uint32_t b = c0 + tid;
+        uint32_t ns = 0, p = 0, slot = 0;
+        if (b < P.B) {
+            p = P.positions[b];
+            slot = P.slots[b];
+            if (slot >= P.n_slots || p >= P.slot_ctx) {
+                atomicOr(P.status, kDevRange);
+            } else {
+                const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
+                ns = (p + 1 + chunk - 1) / chunk;
+            }
+        }
+        // block-wide exclusive scan of the split counts
+        uint32_t incl = ns;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t t = warp_tot[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, t, off);
+                if (lane >= off) t += y;
+            }
+            warp_tot[lane] = t;  // inclusive over warps
+        }
+        __syncthreads();
+        const uint32_t before = base + (warp ? warp_tot[warp - 1] : 0) + incl - ns;
+        row_first[tid] = before;
+        row_n[tid] = ns;
+        row_p[tid] = p;
+        row_slot[tid] = slot;
+        __syncthreads();
+        // one warp per row writes that row's items, lanes in parallel
+        const uint32_t rows = P.B - c0 < (uint32_t)kPlanThreads ? P.B - c0 : kPlanThreads;
+        for (uint32_t r = warp; r < rows; r += kPlanThreads / 32) {
+            const uint32_t n = row_n[r] * P.n_kv_head;
+            uint4* dst = reinterpret_cast<uint4*>(P.items) + (size_t)row_first[r] * P.n_kv_head;
+            for (uint32_t i = lane; i < n; i += 32)
+                dst[i] = make_uint4(pack_item(c0 + r, i / P.n_kv_head, i % P.n_kv_head), row_p[r],
+                                    row_slot[r], 0u);
+        }
+        __syncthreads();
+        if (tid == 0) base += warp_tot[kPlanThreads / 32 - 1];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        P.plan[0] = base * P.n_kv_head;
+        P.plan[1] = 0;
+    }
+}
+
+// ------------------------------------------------------------------ decode
 template <int HD, int G>
 __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
     slotkv_decode_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                               const __grid_constant__ CUtensorMap tmV,
                               const DecodeParams P) {
     using C = KCfg<HD, G>;
-    constexpr int E = C::E, L = C::L, NG = C::NG, R = C::R, T = C::T, S = C::S;
+    constexpr int E = C::E, L = C::L, NG = C::NG, R = C::R, T = C::T, S = C::S, W = C::W;
+    constexpr int NMS = C::NMS;
+    constexpr float kLog2e = 1.4426950408889634f;
     extern __shared__ __align__(1024) uint8_t smem[];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const uint32_t split = blockIdx.x;
-    const uint32_t kvh = blockIdx.y;
-    const uint32_t b = blockIdx.z;
 
-    const uint32_t p = P.positions[b];
-    const uint32_t slot = P.slots[b];
-    if (slot >= P.n_slots || p >= P.slot_ctx) {
-        if (split == 0 && kvh == 0 && tid == 0) atomicOr(P.status, kDevRange);
-        return;
-    }
-    const uint32_t n_keys = p + 1;
-    const uint32_t chunk = split_chunk(n_keys, P.chunk_min, P.max_splits, T);
-    const uint32_t nsplit = (n_keys + chunk - 1) / chunk;
-    if (split >= nsplit) return;
-    const uint32_t k0 = split * chunk;
-    const bool is_last = split == nsplit - 1;
-    // keys read from the slot buffers: [k0, hist_end); key p comes from k_new
-    const uint32_t hist_end = is_last ? p : k0 + chunk;
-    const uint32_t n_hist = hist_end > k0 ? hist_end - k0 : 0;
-    const uint32_t ntiles = (n_hist + T - 1) / T;
-    const int row_k0 = static_cast<int>(slot * P.slot_ctx + k0);
-
-    float* qs = reinterpret_cast<float*>(smem + C::OFF_QS);
-    float* ks = reinterpret_cast<float*>(smem + C::OFF_KS);
-    float* vs = reinterpret_cast<float*>(smem + C::OFF_VS);
-    float* cs = reinterpret_cast<float*>(smem + C::OFF_CS);
-    float* sn = reinterpret_cast<float*>(smem + C::OFF_SN);
-    const uint32_t full0 = smem_addr(smem + C::OFF_BAR);
-    const uint32_t empty0 = full0 + 8 * S;
+    float* chain = reinterpret_cast<float*>(smem + C::OFF_CHAIN);  // acc [G][HD], m [G], l [G]
+    float* chain_m = chain + G * HD;
+    float* chain_l = chain_m + G;
+    float* qbuf = reinterpret_cast<float*>(smem + C::OFF_QBUF);  // [2][G][HD]
+    float* kbuf = reinterpret_cast<float*>(smem + C::OFF_KBUF);  // [2][HD]
+    float* vbuf = reinterpret_cast<float*>(smem + C::OFF_VBUF);  // [2][HD]
+    float* qw_s = reinterpret_cast<float*>(smem + C::OFF_QW);
+    float* kw_s = reinterpret_cast<float*>(smem + C::OFF_KW);
+    float* if_s = reinterpret_cast<float*>(smem + C::OFF_IF);
+    volatile ItemDesc* desc = reinterpret_cast<volatile ItemDesc*>(smem + C::OFF_DESC);
+    volatile HandOff* hand = reinterpret_cast<volatile HandOff*>(smem + C::OFF_HAND);
+    const uint32_t full0 = smem_addr(smem + C::OFF_BAR);  // tile landed
+    const uint32_t empty0 = full0 + 8 * S;                 // tile consumed
+    const uint32_t staged0 = empty0 + 8 * S;               // item vectors landed
+    const uint32_t prepared0 = staged0 + 16;               // item vectors normed+rotated
+    const uint32_t free0 = prepared0 + 16;                 // item slot released
+    const uint32_t handed0 = free0 + 16;                   // partial handed to the merge warp
+    const uint32_t hfree0 = handed0 + 8 * NMS;             // hand-off slot released
     volatile int* misc = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
-    // misc[0]: abort, misc[1]: this CTA merges the splits, misc[2]: tiles issued
+    // misc[0]: abort, misc[2]: tiles issued, misc[3]: items staged
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, C::W);
+            mbar_init(empty0 + 8 * i, W);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(staged0 + 8 * i, 1);
+            mbar_init(prepared0 + 8 * i, 1);
+            mbar_init(free0 + 8 * i, W);
+        }
+        for (int i = 0; i < NMS; ++i) {
+            mbar_init(handed0 + 8 * i, 1);
+            mbar_init(hfree0 + 8 * i, 1);
         }
         misc[0] = 0;
         misc[1] = 0;
         misc[2] = 0;
+        misc[3] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    for (int i = tid; i < HD; i += C::THREADS) {
+        qw_s[i] = P.q_norm_w[i];
+        kw_s[i] = P.k_norm_w[i];
+        if (i < HD / 2) if_s[i] = P.inv_freq[i];
+    }
     __syncthreads();
 
-    // ---------------------------------------------------------------- producer
-    if (warp == C::W) {
-        if (lane == 0) {
-            for (uint32_t t = 0; t < ntiles; ++t) {
-                const int st = t % S;
-                if (t >= static_cast<uint32_t>(S)) {
-                    if (!mbar_wait(empty0 + 8 * st, ((t / S) - 1) & 1)) {
+    if (warp >= W) {
+        regs_decrease<C::REG_HELP>();
+        // ------------------------------------------------------------ producer
+        // Items are staged one ahead: item k+1's descriptor and vectors go into
+        // its slot as soon as the consumers release that slot (they finish item
+        // k-1), while item k's tiles are still streaming, so the prep warp has
+        // item k+1 ready before the consumers reach it.
+        if (warp == C::WARP_TMA && lane == 0) {
+            grid_dependency_wait();  // the plan's list and counters
+            const uint32_t n_items = __ldcg(P.plan);
+            const uint4* recs = reinterpret_cast<const uint4*>(P.items);
+            // stage item k from record `rec` (or the end marker); returns the
+            // item's tile stream: kv head, first tensor row, tile count
+            auto stage = [&](uint32_t k, bool valid, uint4 rec, uint32_t& kvh_o, int& row_o,
+                             uint32_t& ntiles_o) {
+                const uint32_t is = k & 1;
+                volatile ItemDesc* d = desc + is;
+                const uint32_t staged = staged0 + 8 * is;
+                if (!valid) {
+                    d->end = 1;
+                    mbar_arrive(staged);
+                    return false;
+                }
+                const uint32_t b = rec.x >> 16, split = (rec.x >> 8) & 255u, kvh = rec.x & 255u;
+                const uint32_t p = rec.y, slot = rec.z;
+                const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
+                const uint32_t nsplit = (p + 1 + chunk - 1) / chunk;
+                const uint32_t k0 = split * chunk;
+                const bool is_last = split == nsplit - 1;
+                const uint32_t hist_end = is_last ? p : k0 + chunk;
+                const uint32_t n_hist = hist_end > k0 ? hist_end - k0 : 0;
+                const uint32_t ntiles = (n_hist + T - 1) / T;
+                d->b = b;
+                d->kvh = kvh;
+                d->split = split;
+                d->nsplit = nsplit;
+                d->p = p;
+                d->slot = slot;
+                d->k0 = k0;
+                d->hist_end = hist_end;
+                d->ntiles = ntiles;
+                d->is_last = is_last ? 1u : 0u;
+                d->end = 0;
+                mbar_expect_tx(staged, G * HD * 4 + (is_last ? 2 * HD * 4 : 0));
+                bulk_load(smem_addr(qbuf + is * G * HD),
+                          P.q + (static_cast<size_t>(b) * P.n_head + kvh * G) * HD, G * HD * 4,
+                          staged);
+                if (is_last) {
+                    const size_t kv_off = (static_cast<size_t>(b) * P.n_kv_head + kvh) * HD;
+                    bulk_load(smem_addr(kbuf + is * HD), P.k_new + kv_off, HD * 4, staged);
+                    bulk_load(smem_addr(vbuf + is * HD), P.v_new + kv_off, HD * 4, staged);
+                }
+                misc[3] = static_cast<int>(k + 1);
+                kvh_o = kvh;
+                row_o = static_cast<int>(slot * P.slot_ctx + k0);
+                ntiles_o = ntiles;
+                return true;
+            };
+            uint32_t it = atomicAdd(P.plan + 1, 1u);
+            uint4 rec = it < n_items ? __ldcg(recs + it) : make_uint4(0, 0, 0, 0);
+            uint32_t cur_kvh = 0, cur_nt = 0, nxt_kvh = 0, nxt_nt = 0;
+            int cur_row = 0, nxt_row = 0;
+            bool cur_ok = stage(0, it < n_items, rec, cur_kvh, cur_row, cur_nt);
+            // the record of the item after the staged one, claimed early
+            uint32_t it_n = cur_ok ? atomicAdd(P.plan + 1, 1u) : n_items;
+            uint4 rec_n = make_uint4(0, 0, 0, 0);
+            bool rec_n_loaded = false;
+            uint32_t tile_g = 0;
+            for (uint32_t k = 0; cur_ok; ++k) {
+                bool nxt_staged = false, nxt_ok = false;
+                // slot of item k+1 is free once the consumers release item k-1
+                const uint32_t nfree = free0 + 8 * ((k + 1) & 1);
+                const uint32_t nparity = k >= 1 ? (((k + 1) >> 1) - 1) & 1 : 0;
+                for (uint32_t t = 0; t < cur_nt; ++t, ++tile_g) {
+                    const int st = tile_g % S;
+                    if (tile_g >= static_cast<uint32_t>(S) &&
+                        !mbar_wait(empty0 + 8 * st, ((tile_g / S) - 1) & 1)) {
                         atomicOr(P.status, kDevTimeout);
                         misc[0] = 1;
                         break;
                     }
+                    if (misc[0]) break;
+                    const uint32_t full = full0 + 8 * st;
+                    const uint32_t dst = smem_addr(smem + st * C::STAGE_BYTES);
+                    mbar_expect_tx(full, C::STAGE_BYTES);
+                    tma_load_2d(dst, &tmK, static_cast<int>(cur_kvh * HD),
+                                cur_row + static_cast<int>(t * T), full);
+                    tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(cur_kvh * HD),
+                                cur_row + static_cast<int>(t * T), full);
+                    misc[2] = static_cast<int>(tile_g + 1);
+                    if (!rec_n_loaded) {
+                        if (it_n < n_items) rec_n = __ldcg(recs + it_n);
+                        rec_n_loaded = true;
+                    } else if (!nxt_staged && (k == 0 || mbar_test(nfree, nparity))) {
+                        nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt);
+                        nxt_staged = true;
+                    }
                 }
                 if (misc[0]) break;
-                const uint32_t full = full0 + 8 * st;
-                const uint32_t dst = smem_addr(smem + st * C::STAGE_BYTES);
-                mbar_expect_tx(full, C::STAGE_BYTES);
-                tma_load_2d(dst, &tmK, static_cast<int>(kvh * HD), row_k0 + static_cast<int>(t * T),
-                            full);
-                tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(kvh * HD),
-                            row_k0 + static_cast<int>(t * T), full);
-                misc[2] = static_cast<int>(t + 1);
+                if (!nxt_staged) {
+                    if (!rec_n_loaded && it_n < n_items) rec_n = __ldcg(recs + it_n);
+                    if (k >= 1 && !mbar_wait(nfree, nparity)) {
+                        atomicOr(P.status, kDevTimeout);
+                        misc[0] = 1;
+                        break;
+                    }
+                    nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt);
+                }
+                if (nxt_ok) it_n = atomicAdd(P.plan + 1, 1u);
+                rec_n_loaded = false;
+                cur_ok = nxt_ok;
+                cur_kvh = nxt_kvh;
+                cur_row = nxt_row;
+                cur_nt = nxt_nt;
+            }
+        }
+        // ------------------------------------------------------------ prep
+        // Per item: RoPE cos/sin at p (each lane for its own rotation pairs),
+        // then per-head RMS norm + RoPE in place on the staged G query vectors
+        // (pre-scaled by scale*log2 e) and, in the split owning key p, k_new.
+        if (warp == C::WARP_PREP) {
+            constexpr int PPL = HD / 64;  // rotation pairs per lane
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t is = k & 1;
+                if (!mbar_wait(staged0 + 8 * is, (k >> 1) & 1)) {
+                    if (lane == 0) atomicOr(P.status, kDevTimeout);
+                    misc[0] = 1;
+                    break;
+                }
+                if (misc[0]) break;
+                const bool end = desc[is].end != 0;
+                const uint32_t p = desc[is].p;
+                const bool is_last = desc[is].is_last != 0;
+                if (!end) {
+                    float cs[PPL], sn[PPL];
+                    const float fp = static_cast<float>(p);
+#pragma unroll
+                    for (int j = 0; j < PPL; ++j)
+                        sincosf(__fmul_rn(fp, if_s[lane + 32 * j]), &sn[j], &cs[j]);
+                    const int nvec = G + (is_last ? 1 : 0);
+                    for (int x = 0; x < nvec; ++x) {
+                        const bool isq = x < G;
+                        float* v = isq ? qbuf + (is * G + x) * HD : kbuf + is * HD;
+                        const float* w = isq ? qw_s : kw_s;
+                        float x0[PPL], x1[PPL];
+                        float ss = 0.f;
+#pragma unroll
+                        for (int j = 0; j < PPL; ++j) {
+                            x0[j] = v[lane + 32 * j];
+                            x1[j] = v[lane + 32 * j + HD / 2];
+                            ss = fmaf(x0[j], x0[j], ss);
+                            ss = fmaf(x1[j], x1[j], ss);
+                        }
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                        const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + P.eps);
+                        const float mul = isq ? P.scale_log2 : 1.0f;
+#pragma unroll
+                        for (int j = 0; j < PPL; ++j) {
+                            const int i = lane + 32 * j;
+                            const float y0 = x0[j] * inv * w[i];
+                            const float y1 = x1[j] * inv * w[i + HD / 2];
+                            v[i] = (y0 * cs[j] - y1 * sn[j]) * mul;
+                            v[i + HD / 2] = (y1 * cs[j] + y0 * sn[j]) * mul;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(prepared0 + 8 * is);
+                if (end) break;
+            }
+        }
+        // ------------------------------------------------------------ merge
+        // The last CTA of a (row, kv head) to finish merges its splits, in
+        // split order, so the result does not depend on timing.
+        if (warp == C::WARP_MERGE) {
+            const size_t MS = P.max_splits;
+            for (uint32_t j = 0;; ++j) {
+                const uint32_t hs = j % NMS;
+                if (!mbar_wait(handed0 + 8 * hs, (j / NMS) & 1)) {
+                    if (lane == 0) atomicOr(P.status, kDevTimeout);
+                    misc[0] = 1;
+                    break;
+                }
+                if (misc[0]) break;
+                const uint32_t b = hand[hs].b, kvh = hand[hs].kvh, nsplit = hand[hs].nsplit;
+                const bool end = hand[hs].end != 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hfree0 + 8 * hs);
+                if (end) break;
+                uint32_t* counter = P.counters + static_cast<size_t>(b) * P.n_kv_head + kvh;
+                uint32_t old = 0;
+                if (lane == 0) old = atomic_add_acq_rel(counter, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old != nsplit - 1) continue;
+                // Merge, up to 4 heads at a time so each lane keeps several loads
+                // in flight: per head h the max M_h and weighted sum L_h over the
+                // splits (sink included), then out = sum_s w_hs acc_hs / L_h with
+                // w_hs = exp2(m_hs - M_h), taking the splits 32 at a time.
+                constexpr int HG = G < 4 ? G : 4;
+                const uint32_t hq0 = kvh * G;
+                for (int h0 = 0; h0 < G; h0 += HG) {
+                    const int nh = G - h0 < HG ? G - h0 : HG;
+                    const size_t base0 = (static_cast<size_t>(b) * P.n_head + hq0 + h0) * MS;
+                    float Mh[HG], Lh[HG];
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) Mh[h] = -CUDART_INF_F;
+                    for (uint32_t s2 = lane; s2 < nsplit; s2 += 32) {
+#pragma unroll
+                        for (int h = 0; h < HG; ++h)
+                            if (h < nh)
+                                Mh[h] = fmaxf(Mh[h], __ldcg(P.ws_ml + (base0 + h * MS + s2) * 2));
+                    }
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            Mh[h] = fmaxf(Mh[h], __shfl_xor_sync(0xffffffffu, Mh[h], off));
+                        Lh[h] = 0.f;
+                    }
+                    for (uint32_t s2 = lane; s2 < nsplit; s2 += 32) {
+#pragma unroll
+                        for (int h = 0; h < HG; ++h) {
+                            if (h < nh) {
+                                const size_t at = (base0 + h * MS + s2) * 2;
+                                Lh[h] += __ldcg(P.ws_ml + at + 1) *
+                                         exp2f(__ldcg(P.ws_ml + at) - Mh[h]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            Lh[h] += __shfl_xor_sync(0xffffffffu, Lh[h], off);
+                        if (P.sinks && h < nh) {
+                            const float sk = P.sinks[hq0 + h0 + h] * kLog2e;
+                            const float M2 = fmaxf(Mh[h], sk);
+                            Lh[h] = Lh[h] * exp2f(Mh[h] - M2) + exp2f(sk - M2);
+                            Mh[h] = M2;
+                        }
+                    }
+                    // outputs: lanes over the hd/4 float4 columns (every lane
+                    // runs every iteration: the shuffles name the whole warp),
+                    // one head at a time, 8 splits' loads in flight per round
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+                        if (h >= nh) break;
+                        float* orow =
+                            P.out + (static_cast<size_t>(b) * P.n_head + hq0 + h0 + h) * HD;
+                        const float inv = 1.f / Lh[h];
+                        const float Mhh = Mh[h];
+                        const float* wsa = P.ws_acc + (base0 + h * MS) * HD;
+                        const float* wsm = P.ws_ml + (base0 + h * MS) * 2;
+                        for (int d0 = 0; d0 < HD / 4; d0 += 32) {
+                            const int d4 = d0 + lane;
+                            const bool act = d4 < HD / 4;
+                            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (uint32_t r0 = 0; r0 < nsplit; r0 += 32) {
+                                const uint32_t mine = r0 + lane;
+                                // this lane's split's weight; lanes past the end weigh 0
+                                const float wl = mine < nsplit ? exp2f(__ldcg(wsm + mine * 2) - Mhh) : 0.f;
+                                const uint32_t n = nsplit - r0 < 32u ? nsplit - r0 : 32u;
+                                for (uint32_t i0 = 0; i0 < n; i0 += 8) {
+                                    float4 v[8];
+#pragma unroll
+                                    for (int u = 0; u < 8; ++u) {
+                                        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                        if (act && i0 + u < n)
+                                            v[u] = __ldcg(reinterpret_cast<const float4*>(
+                                                              wsa + (r0 + i0 + u) * HD) + d4);
+                                    }
+#pragma unroll
+                                    for (int u = 0; u < 8; ++u) {
+                                        const float w = __shfl_sync(0xffffffffu, wl, (i0 + u) & 31);
+                                        a.x = fmaf(w, v[u].x, a.x);
+                                        a.y = fmaf(w, v[u].y, a.y);
+                                        a.z = fmaf(w, v[u].z, a.z);
+                                        a.w = fmaf(w, v[u].w, a.w);
+                                    }
+                                }
+                            }
+                            if (act)
+                                reinterpret_cast<float4*>(orow)[d4] =
+                                    make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) *counter = 0u;
             }
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    // cos/sin of the f32 RoPE angles fl32(p * inv_freq[i])
-    const float fp = static_cast<float>(p);
-    for (int i = tid; i < HD / 2; i += C::CONS) {
-        float s_, c_;
-        sincosf(__fmul_rn(fp, P.inv_freq[i]), &s_, &c_);
-        sn[i] = s_;
-        cs[i] = c_;
-    }
-    named_sync<C::CONS>();
-    {
-        // per-head RMS norm + RoPE: the G query heads of this kv head, and k_new
-        // in the split that owns key p.  One warp per head vector.
-        const int nvec = G + (is_last ? 1 : 0);
-        constexpr int PPL = HD / 64;  // rotation pairs per lane
-        for (int x = warp; x < nvec; x += C::W) {
-            const bool isq = x < G;
-            const float* src = isq ? P.q + (static_cast<size_t>(b) * P.n_head + kvh * G + x) * HD
-                                   : P.k_new + (static_cast<size_t>(b) * P.n_kv_head + kvh) * HD;
-            const float* w = isq ? P.q_norm_w : P.k_norm_w;
-            float x0[PPL], x1[PPL];
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < PPL; ++j) {
-                x0[j] = src[lane + 32 * j];
-                x1[j] = src[lane + 32 * j + HD / 2];
-                ss = fmaf(x0[j], x0[j], ss);
-                ss = fmaf(x1[j], x1[j], ss);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + P.eps);
-            const float mul = isq ? P.scale_log2 : 1.0f;
-            float* dst = isq ? qs + x * HD : ks;
-#pragma unroll
-            for (int j = 0; j < PPL; ++j) {
-                const int i = lane + 32 * j;
-                const float y0 = x0[j] * inv * w[i];
-                const float y1 = x1[j] * inv * w[i + HD / 2];
-                dst[i] = (y0 * cs[i] - y1 * sn[i]) * mul;
-                dst[i + HD / 2] = (y1 * cs[i] + y0 * sn[i]) * mul;
-            }
-        }
-        if (is_last) {
-            const float* vsrc = P.v_new + (static_cast<size_t>(b) * P.n_kv_head + kvh) * HD;
-            for (int d = tid; d < HD; d += C::CONS) vs[d] = vsrc[d];
-        }
-    }
-    named_sync<C::CONS>();
-
+    regs_increase<C::REG_CONS>();
     const int gid = warp * (32 / L) + lane / L;  // key group
     const int li = lane % L;                     // lane within the group
-    float q[G][E], m[G], l[G], acc[G][E];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int c = 0; c < E / 4; ++c) {
-            const float4 v = *reinterpret_cast<const float4*>(qs + h * HD + c * 4 * L + li * 4);
-            q[h][4 * c + 0] = v.x;
-            q[h][4 * c + 1] = v.y;
-            q[h][4 * c + 2] = v.z;
-            q[h][4 * c + 3] = v.w;
-        }
-        m[h] = -CUDART_INF_F;
-        l[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
-    }
-
-    for (uint32_t t = 0; t < ntiles; ++t) {
-        const int st = t % S;
-        if (misc[0] || !mbar_wait(full0 + 8 * st, (t / S) & 1)) {
+    uint32_t tile_g = 0, handed = 0;
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t is = k & 1;
+        if (!misc[0] && !mbar_wait(prepared0 + 8 * is, (k >> 1) & 1)) {
             atomicOr(P.status, kDevTimeout);
             misc[0] = 1;
+        }
+        named_sync<C::CONS>();  // every consumer warp takes the same branch
+        if (misc[0]) break;
+        const uint32_t end = desc[is].end;
+        if (end) {
+            // tell the merge warp there is nothing more
+            if (warp == W - 1 && lane == 0) {
+                const uint32_t hs = handed % NMS;
+                if (handed < NMS || mbar_wait(hfree0 + 8 * hs, ((handed / NMS) - 1) & 1)) {
+                    hand[hs].end = 1;
+                    mbar_arrive(handed0 + 8 * hs);
+                } else {
+                    atomicOr(P.status, kDevTimeout);
+                    misc[0] = 1;
+                }
+            }
             break;
         }
-        const float* Kt = reinterpret_cast<const float*>(smem + st * C::STAGE_BYTES);
-        const float* Vt = Kt + T * HD;
-        const uint32_t kbase = k0 + t * T;
+        const uint32_t b = desc[is].b, kvh = desc[is].kvh, split = desc[is].split;
+        const uint32_t nsplit = desc[is].nsplit, p = desc[is].p, slot = desc[is].slot;
+        const uint32_t k0 = desc[is].k0, hist_end = desc[is].hist_end;
+        const uint32_t ntiles = desc[is].ntiles;
+        const bool is_last = desc[is].is_last != 0;
+        const float* qs = qbuf + is * G * HD;
+        const float* ks = kbuf + is * HD;
+        const float* vs = vbuf + is * HD;
+
+        float q[G][E], m[G], l[G], acc[G][E];
 #pragma unroll
-        for (int r0 = 0; r0 < R; r0 += C::RC) {
-            int row[C::RC];
-            bool valid[C::RC];
+        for (int h = 0; h < G; ++h) {
 #pragma unroll
-            for (int r = 0; r < C::RC; ++r) {
-                row[r] = gid + NG * (r0 + r);
-                valid[r] = kbase + static_cast<uint32_t>(row[r]) < hist_end;
+            for (int c = 0; c < E / 4; ++c) {
+                const float4 v =
+                    *reinterpret_cast<const float4*>(qs + h * HD + c * 4 * L + li * 4);
+                q[h][4 * c + 0] = v.x;
+                q[h][4 * c + 1] = v.y;
+                q[h][4 * c + 2] = v.z;
+                q[h][4 * c + 3] = v.w;
             }
-            attend_rows<HD, G, E, L, C::RC>(Kt, Vt, row, valid, li, q, m, l, acc);
+            m[h] = -CUDART_INF_F;
+            l[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+        }
+
+        for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
+            const int st = tile_g % S;
+            if (misc[0] || !mbar_wait(full0 + 8 * st, (tile_g / S) & 1)) {
+                atomicOr(P.status, kDevTimeout);
+                misc[0] = 1;
+                break;
+            }
+            const float* Kt = reinterpret_cast<const float*>(smem + st * C::STAGE_BYTES);
+            const float* Vt = Kt + T * HD;
+            const uint32_t kbase = k0 + t * T;
+#pragma unroll
+            for (int r0 = 0; r0 < R; r0 += C::RC) {
+                int row[C::RC];
+                bool valid[C::RC];
+#pragma unroll
+                for (int r = 0; r < C::RC; ++r) {
+                    row[r] = gid + NG * (r0 + r);
+                    valid[r] = kbase + static_cast<uint32_t>(row[r]) < hist_end;
+                }
+                attend_rows<HD, G, E, L, C::RC>(Kt, Vt, row, valid, li, q, m, l, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        }
+        // an abort by any warp must send every consumer warp to the drain
+        named_sync<C::CONS>();
+        if (misc[0]) break;
+
+        if (is_last && warp == 0) {
+            const int row1[1] = {0};
+            const bool valid1[1] = {gid == 0};
+            attend_rows<HD, G, E, L, 1>(ks, vs, row1, valid1, li, q, m, l, acc);
+            // key p's K and V rows go into the slot at (slot*slot_ctx + p)
+            const size_t at = (static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh;
+            float4* kd = reinterpret_cast<float4*>(P.K + at * HD);
+            float4* vd = reinterpret_cast<float4*>(P.V + at * HD);
+            for (int i = lane; i < HD / 4; i += 32) {
+                kd[i] = reinterpret_cast<const float4*>(ks)[i];
+                vd[i] = reinterpret_cast<const float4*>(vs)[i];
+            }
+        }
+
+        // ------------------------------------ merge the groups of each warp
+#pragma unroll
+        for (int off = L; off < 32; off <<= 1) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+                const float M = fmaxf(m[h], mo);
+                const float c1 = partial_weight(m[h], M), c2 = partial_weight(mo, M);
+                l[h] = l[h] * c1 + lo * c2;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+                    acc[h][e] = acc[h][e] * c1 + ao * c2;
+                }
+                m[h] = M;
+            }
+        }
+        // ------------------------------------ chain the four warps: 0 -> 1 -> 2 -> 3
+        for (int w2 = 0; w2 < W; ++w2) {
+            if (warp == w2) {
+                if (w2 > 0) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float Mc = chain_m[h], Lc = chain_l[h];
+                        const float M = fmaxf(m[h], Mc);
+                        const float c1 = partial_weight(m[h], M), c2 = partial_weight(Mc, M);
+                        l[h] = l[h] * c1 + Lc * c2;
+#pragma unroll
+                        for (int c = 0; c < E / 4; ++c) {
+                            const float4 v = *reinterpret_cast<const float4*>(
+                                chain + h * HD + c * 4 * L + li * 4);
+                            acc[h][4 * c + 0] = acc[h][4 * c + 0] * c1 + v.x * c2;
+                            acc[h][4 * c + 1] = acc[h][4 * c + 1] * c1 + v.y * c2;
+                            acc[h][4 * c + 2] = acc[h][4 * c + 2] * c1 + v.z * c2;
+                            acc[h][4 * c + 3] = acc[h][4 * c + 3] * c1 + v.w * c2;
+                        }
+                        m[h] = M;
+                    }
+                    __syncwarp();
+                }
+                if (w2 < W - 1 && lane < L) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+#pragma unroll
+                        for (int c = 0; c < E / 4; ++c)
+                            *reinterpret_cast<float4*>(chain + h * HD + c * 4 * L + li * 4) =
+                                make_float4(acc[h][4 * c], acc[h][4 * c + 1], acc[h][4 * c + 2],
+                                            acc[h][4 * c + 3]);
+                        if (lane == 0) {
+                            chain_m[h] = m[h];
+                            chain_l[h] = l[h];
+                        }
+                    }
+                }
+            }
+            if (w2 < W - 1) named_sync<C::CONS>();
+        }
+
+        // ------------------------------------ warp 3 holds the item's result
+        if (warp == W - 1) {
+            const uint32_t hq0 = kvh * G;  // first query head of this kv head
+            if (nsplit == 1) {
+                if (lane < L) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float c = 1.f, Ls = l[h];
+                        if (P.sinks) {
+                            const float sk = P.sinks[hq0 + h] * kLog2e;
+                            const float M2 = fmaxf(m[h], sk);
+                            c = exp2f(m[h] - M2);
+                            Ls = Ls * c + exp2f(sk - M2);
+                        }
+                        float* o = P.out + (static_cast<size_t>(b) * P.n_head + hq0 + h) * HD;
+#pragma unroll
+                        for (int cc = 0; cc < E / 4; ++cc)
+                            *reinterpret_cast<float4*>(o + cc * 4 * L + li * 4) = make_float4(
+                                (acc[h][4 * cc] * c) / Ls, (acc[h][4 * cc + 1] * c) / Ls,
+                                (acc[h][4 * cc + 2] * c) / Ls, (acc[h][4 * cc + 3] * c) / Ls);
+                    }
+                }
+            } else {
+                const size_t MS = P.max_splits;
+                if (lane < L) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const size_t base =
+                            (static_cast<size_t>(b) * P.n_head + hq0 + h) * MS + split;
+                        float* a = P.ws_acc + base * HD;
+#pragma unroll
+                        for (int cc = 0; cc < E / 4; ++cc)
+                            *reinterpret_cast<float4*>(a + cc * 4 * L + li * 4) =
+                                make_float4(acc[h][4 * cc], acc[h][4 * cc + 1],
+                                            acc[h][4 * cc + 2], acc[h][4 * cc + 3]);
+                        if (lane == 0) {
+                            P.ws_ml[base * 2 + 0] = m[h];
+                            P.ws_ml[base * 2 + 1] = l[h];
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t hs = handed % NMS;
+                    if (handed < NMS || mbar_wait(hfree0 + 8 * hs, ((handed / NMS) - 1) & 1)) {
+                        hand[hs].b = b;
+                        hand[hs].kvh = kvh;
+                        hand[hs].nsplit = nsplit;
+                        hand[hs].end = 0;
+                        mbar_arrive(handed0 + 8 * hs);
+                    } else {
+                        atomicOr(P.status, kDevTimeout);
+                        misc[0] = 1;
+                    }
+                }
+                ++handed;
+            }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        if (lane == 0) mbar_arrive(free0 + 8 * is);  // this warp is done with the slot
     }
-    // every consumer warp is past the ring; an abort by any of them is visible
-    named_sync<C::CONS>();
+
     if (misc[0]) {
         // drain this CTA's own copies that may still be in flight: the newest
-        // issued tile of each stage (older phases have completed already)
+        // tile of each stage and the newest staged items
+        named_sync<C::CONS>();
         if (tid == 0) {
-            const uint32_t issued = static_cast<uint32_t>(misc[2]);
-            for (uint32_t u = issued > static_cast<uint32_t>(S) ? issued - S : 0; u < issued; ++u)
+            const uint32_t tiles = static_cast<uint32_t>(misc[2]);
+            for (uint32_t u = tiles > static_cast<uint32_t>(S) ? tiles - S : 0; u < tiles; ++u)
                 mbar_wait(full0 + 8 * (u % S), (u / S) & 1, 1ll << 28);
-        }
-        named_sync<C::CONS>();
-        return;
-    }
-    if (is_last && warp == 0) {
-        const int row1[1] = {0};
-        const bool valid1[1] = {gid == 0};
-        attend_rows<HD, G, E, L, 1>(ks, vs, row1, valid1, li, q, m, l, acc);
-    }
-
-    // ---------------------------------------------- merge the groups' partials
-    named_sync<C::CONS>();  // warp 0 is done with key p
-    float* red_acc = reinterpret_cast<float*>(smem);  // [NG][G][HD]
-    float* red_m = red_acc + NG * G * HD;             // [NG][G]
-    float* red_l = red_m + NG * G;                    // [NG][G]
-    float* wgt = red_l + NG * G;                      // [NG][G]
-    float* hM = wgt + NG * G;                         // [G]
-    float* hL = hM + G;                               // [G]
-    float* sw = hL + G;                               // [G][<=256]
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int c = 0; c < E / 4; ++c) {
-            *reinterpret_cast<float4*>(red_acc + (gid * G + h) * HD + c * 4 * L + li * 4) =
-                make_float4(acc[h][4 * c], acc[h][4 * c + 1], acc[h][4 * c + 2], acc[h][4 * c + 3]);
-        }
-        if (li == 0) {
-            red_m[gid * G + h] = m[h];
-            red_l[gid * G + h] = l[h];
-        }
-    }
-    named_sync<C::CONS>();
-    if (tid < G) {
-        float M = -CUDART_INF_F;
-        for (int g = 0; g < NG; ++g) M = fmaxf(M, red_m[g * G + tid]);
-        float Ls = 0.f;
-        for (int g = 0; g < NG; ++g) Ls += red_l[g * G + tid] * exp2f(red_m[g * G + tid] - M);
-        hM[tid] = M;
-        hL[tid] = Ls;
-    }
-    named_sync<C::CONS>();
-    for (int i = tid; i < NG * G; i += C::CONS) wgt[i] = exp2f(red_m[i] - hM[i % G]);
-    named_sync<C::CONS>();
-
-    const uint32_t hq0 = kvh * G;  // first query head of this kv head
-    constexpr float kLog2e = 1.4426950408889634f;
-    if (nsplit == 1) {
-        for (int o = tid; o < G * HD; o += C::CONS) {
-            const int h = o / HD, d = o % HD;
-            float A = 0.f;
-            for (int g = 0; g < NG; ++g) A = fmaf(red_acc[(g * G + h) * HD + d], wgt[g * G + h], A);
-            float M = hM[h], Ls = hL[h], c = 1.f;
-            if (P.sinks) {
-                const float sk = P.sinks[hq0 + h] * kLog2e;
-                const float M2 = fmaxf(M, sk);
-                c = exp2f(M - M2);
-                Ls = Ls * c + exp2f(sk - M2);
-            }
-            P.out[(static_cast<size_t>(b) * P.n_head + hq0 + h) * HD + d] = (A * c) / Ls;
-        }
-    } else {
-        const size_t MS = P.max_splits;
-        for (int o = tid; o < G * HD; o += C::CONS) {
-            const int h = o / HD, d = o % HD;
-            float A = 0.f;
-            for (int g = 0; g < NG; ++g) A = fmaf(red_acc[(g * G + h) * HD + d], wgt[g * G + h], A);
-            const size_t base = (static_cast<size_t>(b) * P.n_head + hq0 + h) * MS + split;
-            P.ws_acc[base * HD + d] = A;
-            if (d == 0) {
-                P.ws_ml[base * 2 + 0] = hM[h];
-                P.ws_ml[base * 2 + 1] = hL[h];
-            }
-        }
-        __threadfence();
-        named_sync<C::CONS>();
-        uint32_t* counter = P.counters + static_cast<size_t>(b) * P.n_kv_head + kvh;
-        if (tid == 0) misc[1] = atomicAdd(counter, 1u) == nsplit - 1 ? 1 : 0;
-        named_sync<C::CONS>();
-        if (misc[1]) {
-            // the last CTA of (row, kv head) to finish merges the splits, in
-            // split order, so the result does not depend on finishing order
-            __threadfence();
-            if (tid < G) {
-                const size_t base = (static_cast<size_t>(b) * P.n_head + hq0 + tid) * MS;
-                float M = -CUDART_INF_F;
-                for (uint32_t s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(P.ws_ml + (base + s2) * 2));
-                float Ls = 0.f;
-                for (uint32_t s2 = 0; s2 < nsplit; ++s2)
-                    Ls += __ldcg(P.ws_ml + (base + s2) * 2 + 1) *
-                          exp2f(__ldcg(P.ws_ml + (base + s2) * 2) - M);
-                if (P.sinks) {
-                    const float sk = P.sinks[hq0 + tid] * kLog2e;
-                    const float M2 = fmaxf(M, sk);
-                    Ls = Ls * exp2f(M - M2) + exp2f(sk - M2);
-                    M = M2;
-                }
-                hM[tid] = M;
-                hL[tid] = Ls;
-            }
-            named_sync<C::CONS>();
-            for (uint32_t i = tid; i < G * nsplit; i += C::CONS) {
-                const uint32_t h = i / nsplit, s2 = i % nsplit;
-                const size_t base = (static_cast<size_t>(b) * P.n_head + hq0 + h) * MS + s2;
-                sw[h * nsplit + s2] = exp2f(__ldcg(P.ws_ml + base * 2) - hM[h]);
-            }
-            named_sync<C::CONS>();
-            for (int o = tid; o < G * HD; o += C::CONS) {
-                const int h = o / HD, d = o % HD;
-                const size_t base = (static_cast<size_t>(b) * P.n_head + hq0 + h) * MS;
-                float A = 0.f;
-                for (uint32_t s2 = 0; s2 < nsplit; ++s2)
-                    A = fmaf(__ldcg(P.ws_acc + (base + s2) * HD + d), sw[h * nsplit + s2], A);
-                P.out[(static_cast<size_t>(b) * P.n_head + hq0 + h) * HD + d] = A / hL[h];
-            }
-            if (tid == 0) *counter = 0u;
-        }
-    }
-
-    // ------------------------------------------------ write key p into the slot
-    if (is_last) {
-        const size_t at = (static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh;
-        float4* kd = reinterpret_cast<float4*>(P.K + at * HD);
-        float4* vd = reinterpret_cast<float4*>(P.V + at * HD);
-        for (int i = tid; i < HD / 4; i += C::CONS) {
-            kd[i] = reinterpret_cast<const float4*>(ks)[i];
-            vd[i] = reinterpret_cast<const float4*>(vs)[i];
+            const uint32_t items = static_cast<uint32_t>(misc[3]);
+            for (uint32_t u = items > 2u ? items - 2 : 0; u < items; ++u)
+                mbar_wait(staged0 + 8 * (u & 1), (u >> 1) & 1, 1ll << 28);
         }
     }
 }
 
 template <int HD, int G>
 int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-               dim3 grid, cudaStream_t stream) {
+               unsigned ctas, cudaStream_t stream) {
     using C = KCfg<HD, G>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(slotkv_decode_attn_kernel<HD, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return static_cast<int>(e);
+        // the register hand-over assumes the launch gives every thread 128
+        // registers; with fewer, the consumers' request could never be met
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, slotkv_decode_attn_kernel<HD, G>);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        if (fa.numRegs != 128) return static_cast<int>(cudaErrorInvalidConfiguration);
         configured = true;
     }
-    slotkv_decode_attn_kernel<HD, G><<<grid, C::THREADS, C::SMEM, stream>>>(tmK, tmV, p);
-    return static_cast<int>(cudaGetLastError());
+    slotkv_plan_kernel<C::T><<<1, kPlanThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, slotkv_decode_attn_kernel<HD, G>, tmK, tmV, p);
+    return static_cast<int>(e);
 }
 
 template <int HD>
 int launch_hd(int G, const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-              dim3 grid, cudaStream_t stream) {
+              unsigned ctas, cudaStream_t stream) {
     switch (G) {
-        case 1: return launch_one<HD, 1>(p, tmK, tmV, grid, stream);
-        case 2: return launch_one<HD, 2>(p, tmK, tmV, grid, stream);
-        case 3: return launch_one<HD, 3>(p, tmK, tmV, grid, stream);
-        case 4: return launch_one<HD, 4>(p, tmK, tmV, grid, stream);
-        case 5: return launch_one<HD, 5>(p, tmK, tmV, grid, stream);
-        case 6: return launch_one<HD, 6>(p, tmK, tmV, grid, stream);
-        case 7: return launch_one<HD, 7>(p, tmK, tmV, grid, stream);
-        case 8: return launch_one<HD, 8>(p, tmK, tmV, grid, stream);
+        case 1: return launch_one<HD, 1>(p, tmK, tmV, ctas, stream);
+        case 2: return launch_one<HD, 2>(p, tmK, tmV, ctas, stream);
+        case 3: return launch_one<HD, 3>(p, tmK, tmV, ctas, stream);
+        case 4: return launch_one<HD, 4>(p, tmK, tmV, ctas, stream);
+        case 5: return launch_one<HD, 5>(p, tmK, tmV, ctas, stream);
+        case 6: return launch_one<HD, 6>(p, tmK, tmV, ctas, stream);
+        case 7: return launch_one<HD, 7>(p, tmK, tmV, ctas, stream);
+        case 8: return launch_one<HD, 8>(p, tmK, tmV, ctas, stream);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }

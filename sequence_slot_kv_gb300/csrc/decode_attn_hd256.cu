@@ -6,8 +6,8 @@
 namespace slotkv {
 
 int launch_decode_hd256(int G, const DecodeParams& p, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
-    return launch_hd<256>(G, p, tmK, tmV, grid, stream);
+                       const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream) {
+    return launch_hd<256>(G, p, tmK, tmV, ctas, stream);
 }
 
 }  // namespace slotkv

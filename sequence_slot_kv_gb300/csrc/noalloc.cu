@@ -80,15 +80,21 @@ extern "C" int decode_batch_attn_noalloc(
         return noalloc_fail(SLOTKV_ERR_UNSUPPORTED, "head_dim=%u (64, 128 or 256)", head_dim);
     if ((uint64_t)n_slots * slot_ctx + 256 >= (1ull << 31))
         return noalloc_fail(SLOTKV_ERR_ARG, "n_slots*slot_ctx must be < 2^31 - 256");
+    if (n_kv_head > 256) return noalloc_fail(SLOTKV_ERR_ARG, "n_kv_head must be <= 256");
     if (n_head == 0 || n_head % n_kv_head != 0 || n_head / n_kv_head > 8)
         return noalloc_fail(SLOTKV_ERR_UNSUPPORTED, "n_head/n_kv_head must be 1..8");
     if (B > 65535) return noalloc_fail(SLOTKV_ERR_ARG, "B must be <= 65535");
 
-    // scratch layout: status word | counters [B][n_kv_head] | (m, l) | acc
-    const uint32_t chunk_min = (256u * 1024u) / (8u * head_dim);
+    // scratch layout: status word | plan counters | merge counters [B][n_kv_head]
+    //                 | work list | (m, l) | acc
+    const uint32_t chunk_min = (512u * 1024u) / (8u * head_dim);
     const size_t units = (size_t)B * n_head * kNoAllocMaxSplits;
+    const size_t off_plan = 128;
     const size_t off_cnt = 256;
-    const size_t off_ml = off_cnt + align256((size_t)B * n_kv_head * sizeof(uint32_t));
+    const size_t off_items = off_cnt + align256((size_t)B * n_kv_head * sizeof(uint32_t));
+    const size_t off_ml =
+        off_items + align256(slotkv::plan_capacity(B, n_kv_head, kNoAllocMaxSplits) * 4 *
+                             slotkv::kItemWords);
     const size_t off_acc = off_ml + align256(units * 2 * sizeof(float));
     const size_t need = off_acc + units * head_dim * sizeof(float);
     if (need > kNoAllocScratchBytes)
@@ -118,7 +124,7 @@ extern "C" int decode_batch_attn_noalloc(
 
     // the status word and the merge counters must start at zero
     cudaStream_t s = (cudaStream_t)stream;
-    e = cudaMemsetAsync(scratch, 0, off_ml, s);
+    e = cudaMemsetAsync(scratch, 0, off_items, s);
     if (e != cudaSuccess)
         return noalloc_fail(SLOTKV_ERR_CUDA, "scratch clear: %s", cudaGetErrorString(e));
 
@@ -159,6 +165,8 @@ extern "C" int decode_batch_attn_noalloc(
     P.V = V;
     P.status = dev_flags ? dev_flags : reinterpret_cast<uint32_t*>(scratch);
     P.counters = reinterpret_cast<uint32_t*>(scratch + off_cnt);
+    P.items = reinterpret_cast<uint32_t*>(scratch + off_items);
+    P.plan = reinterpret_cast<uint32_t*>(scratch + off_plan);
     P.ws_ml = reinterpret_cast<float*>(scratch + off_ml);
     P.ws_acc = reinterpret_cast<float*>(scratch + off_acc);
     P.n_slots = n_slots;
@@ -171,14 +179,18 @@ extern "C" int decode_batch_attn_noalloc(
     P.eps = eps;
     P.scale_log2 = scale * 1.4426950408889634f;
     const uint64_t bound = ((uint64_t)slot_ctx + chunk_min - 1) / chunk_min;
-    const uint32_t splits = (uint32_t)(bound < kNoAllocMaxSplits ? bound : kNoAllocMaxSplits);
-    const dim3 grid(splits, n_kv_head, B);
+    const uint64_t splits = bound < kNoAllocMaxSplits ? bound : kNoAllocMaxSplits;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const uint64_t most = (uint64_t)B * n_kv_head * splits;
+    const uint64_t want = 2ull * (uint64_t)(sms > 0 ? sms : 1);
+    const unsigned ctas = (unsigned)(most < want ? most : want);
     const int G = (int)(n_head / n_kv_head);
     int rc;
     switch (head_dim) {
-        case 64: rc = slotkv::launch_decode_hd64(G, P, tmK, tmV, grid, s); break;
-        case 128: rc = slotkv::launch_decode_hd128(G, P, tmK, tmV, grid, s); break;
-        default: rc = slotkv::launch_decode_hd256(G, P, tmK, tmV, grid, s); break;
+        case 64: rc = slotkv::launch_decode_hd64(G, P, tmK, tmV, ctas, s); break;
+        case 128: rc = slotkv::launch_decode_hd128(G, P, tmK, tmV, ctas, s); break;
+        default: rc = slotkv::launch_decode_hd256(G, P, tmK, tmV, ctas, s); break;
     }
     if (rc != 0)
         return noalloc_fail(SLOTKV_ERR_CUDA, "decode kernel launch: %s",

@@ -23,6 +23,9 @@ struct DecodeParams {
     float* ws_ml;            // split partials (m, l): [rows][n_head][max_splits][2]
     float* ws_acc;           // split partials acc:    [rows][n_head][max_splits][hd]
     uint32_t* counters;      // finished-split counters: [rows][n_kv_head]
+    uint32_t* items;         // work list: [rows * n_kv_head * max_splits][4] records
+                             // (packed item, position, slot, 0)
+    uint32_t* plan;          // [0] items in the list, [1] next item to hand out
     uint32_t* status;        // sticky SLOTKV_DEV_* flags
     uint32_t n_slots, slot_ctx, n_head, n_kv_head, B;
     uint32_t chunk_min;      // split policy, see split_chunk()
@@ -43,15 +46,30 @@ __host__ __device__ inline uint32_t split_chunk(uint32_t n_keys, uint32_t chunk_
 // Tile height (keys per pipeline stage) for a head dim: 16 KiB of K + 16 KiB of V.
 __host__ __device__ constexpr int tile_keys(int hd) { return 4096 / hd; }
 
+// A work item is one (row, split, kv head), packed as row << 16 | split << 8 |
+// kv head; rows <= 65535, splits and kv heads <= 256.
+__host__ __device__ inline uint32_t pack_item(uint32_t b, uint32_t split, uint32_t kvh) {
+    return (b << 16) | (split << 8) | kvh;
+}
+
+// Work-list records the workspace must hold: one per (row, kv head, split);
+// each record is 4 u32 (16 bytes).
+inline size_t plan_capacity(uint32_t rows, uint32_t n_kv_head, uint32_t max_splits) {
+    return (size_t)rows * n_kv_head * max_splits;
+}
+constexpr int kItemWords = 4;
+
 // Sets the calling thread's slot_kv_last_error() message.
 void set_last_error(const char* msg);
 
-// Launchers, one translation unit per head dim.  Return a cudaError_t value.
+// Launchers, one translation unit per head dim.  Each enqueues the plan kernel
+// and then the persistent decode kernel on `stream` with `ctas` CTAs.  Return a
+// cudaError_t value.
 int launch_decode_hd64(int G, const DecodeParams& p, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+                       const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
 int launch_decode_hd128(int G, const DecodeParams& p, const CUtensorMap& tmK,
-                        const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+                        const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
 int launch_decode_hd256(int G, const DecodeParams& p, const CUtensorMap& tmK,
-                        const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+                        const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
 
 }  // namespace slotkv

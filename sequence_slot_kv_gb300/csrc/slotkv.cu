@@ -63,7 +63,10 @@ struct slotkv_s {
     float* ws_ml = nullptr;
     float* ws_acc = nullptr;
     uint32_t* counters = nullptr;
+    uint32_t* items = nullptr;  // work list built by the plan kernel
+    uint32_t* plan = nullptr;   // [0] list length, [1] hand-out counter
     uint32_t* status = nullptr;
+    int sm_count = 0;
     // device staging for decode_batch_attn_host
     float* st_q = nullptr;
     float* st_k = nullptr;
@@ -80,8 +83,10 @@ void free_workspace(slotkv_s* h) {
     cudaFree(h->ws_ml);
     cudaFree(h->ws_acc);
     cudaFree(h->counters);
+    cudaFree(h->items);
+    cudaFree(h->plan);
     h->ws_ml = h->ws_acc = nullptr;
-    h->counters = nullptr;
+    h->counters = h->items = h->plan = nullptr;
 }
 
 void release(slotkv_s* h) {
@@ -103,7 +108,8 @@ void release(slotkv_s* h) {
 }
 
 // Split-K workspace: partial (m, l) and acc per (row, query head, split),
-// plus one finished-split counter per (row, kv head), zeroed.
+// one finished-split counter per (row, kv head) (zeroed), and the work list
+// with its two counters (rebuilt by every call).
 int alloc_workspace(slotkv_s* h) {
     free_workspace(h);
     const size_t units = (size_t)h->max_rows * h->max_n_head * h->max_splits;
@@ -117,6 +123,11 @@ int alloc_workspace(slotkv_s* h) {
         return cuda_fail(e, "workspace (counters)");
     if ((e = cudaMemset(h->counters, 0, nc * sizeof(uint32_t))) != cudaSuccess)
         return cuda_fail(e, "workspace clear");
+    const size_t ni = slotkv::plan_capacity(h->max_rows, h->n_kv_head, h->max_splits);
+    if ((e = cudaMalloc(&h->items, ni * slotkv::kItemWords * sizeof(uint32_t))) != cudaSuccess)
+        return cuda_fail(e, "workspace (work list)");
+    if ((e = cudaMalloc(&h->plan, 2 * sizeof(uint32_t))) != cudaSuccess)
+        return cuda_fail(e, "workspace (plan counters)");
     return SLOTKV_OK;
 }
 
@@ -168,6 +179,8 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.ws_ml = h->ws_ml;
     P.ws_acc = h->ws_acc;
     P.counters = h->counters;
+    P.items = h->items;
+    P.plan = h->plan;
     P.status = h->status;
     P.n_slots = h->n_slots;
     P.slot_ctx = h->slot_ctx;
@@ -179,12 +192,15 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.eps = eps;
     P.scale_log2 = scale * 1.4426950408889634f;
     const int G = (int)(n_head / h->n_kv_head);
-    dim3 grid(grid_splits(h), h->n_kv_head, B);
+    // persistent CTAs: two per SM, never more than there can be work items
+    const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h);
+    const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
+    const unsigned ctas = (unsigned)(most < want ? most : want);
     int rc;
     switch (h->head_dim) {
-        case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, grid, stream); break;
-        case 128: rc = slotkv::launch_decode_hd128(G, P, h->tmK, h->tmV, grid, stream); break;
-        case 256: rc = slotkv::launch_decode_hd256(G, P, h->tmK, h->tmV, grid, stream); break;
+        case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, ctas, stream); break;
+        case 128: rc = slotkv::launch_decode_hd128(G, P, h->tmK, h->tmV, ctas, stream); break;
+        case 256: rc = slotkv::launch_decode_hd256(G, P, h->tmK, h->tmV, ctas, stream); break;
         default: return fail(SLOTKV_ERR_UNSUPPORTED, "head_dim %u", h->head_dim);
     }
     if (rc != 0) return cuda_fail((cudaError_t)rc, "decode kernel launch");
@@ -237,8 +253,7 @@ int slot_kv_alloc(slotkv_t* handle, uint32_t n_slots, uint32_t slot_ctx, uint32_
     // TMA row coordinates are int32: keep every tile start (row + tile) below 2^31
     if ((uint64_t)n_slots * slot_ctx + 256 >= (1ull << 31))
         return fail(SLOTKV_ERR_ARG, "n_slots*slot_ctx must be < 2^31 - 256");
-    if ((uint64_t)n_kv_head * head_dim > 65536)
-        return fail(SLOTKV_ERR_ARG, "kv_dim too large");
+    if (n_kv_head > 256) return fail(SLOTKV_ERR_ARG, "n_kv_head must be <= 256");
     if ((k_buf == nullptr) != (v_buf == nullptr))
         return fail(SLOTKV_ERR_ARG, "give both k_buf and v_buf, or neither");
     if ((k_buf && ((uintptr_t)k_buf & 15)) || (v_buf && ((uintptr_t)v_buf & 15)))
@@ -251,6 +266,7 @@ int slot_kv_alloc(slotkv_t* handle, uint32_t n_slots, uint32_t slot_ctx, uint32_
     slotkv_s* h = new (std::nothrow) slotkv_s();
     if (!h) return fail(SLOTKV_ERR_ARG, "out of host memory");
     cudaGetDevice(&h->device);
+    cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
     h->n_slots = n_slots;
     h->slot_ctx = slot_ctx;
     h->n_kv_head = n_kv_head;
@@ -258,8 +274,8 @@ int slot_kv_alloc(slotkv_t* handle, uint32_t n_slots, uint32_t slot_ctx, uint32_
     h->kv_dim = n_kv_head * head_dim;
     h->max_rows = max_rows;
     h->max_n_head = max_n_head;
-    // default split policy: chunks of >= 256 KiB of K+V per kv head, <= 64 splits
-    h->chunk_min = (256u * 1024u) / (8u * head_dim);
+    // default split policy: chunks of >= 512 KiB of K+V per kv head, <= 64 splits
+    h->chunk_min = (512u * 1024u) / (8u * head_dim);
     h->max_splits = 64;
 
     const size_t elems = (size_t)n_slots * slot_ctx * h->kv_dim;
