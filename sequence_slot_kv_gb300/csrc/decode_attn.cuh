@@ -53,6 +53,11 @@ __host__ __device__ constexpr int pow2_floor(int x) {
     while (r * 2 <= x) r *= 2;
     return r;
 }
+__host__ __device__ constexpr int pow2_ceil(int x) {
+    int r = 1;
+    while (r < x) r *= 2;
+    return r;
+}
 __host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -77,6 +82,12 @@ struct KCfg {
     static constexpr int R = T / NG;              // keys per group per tile
     // keys attended per softmax update: keeps the live scores (RC*G) <= 16
     static constexpr int RC = pow2_floor(cmax(1, cmin(R, 16 / G)));
+    // transposed reduction (see attend_rows_tr): G padded to a power of two,
+    // values per lane after the reduction; used when every lane keeps >= 1
+    static constexpr int GP = pow2_ceil(G);
+    static constexpr int NV = RC * GP;
+    static constexpr bool TR = NV >= L && NV >= 4;
+    static constexpr int CNT = TR ? NV / L : 1;
     static constexpr int TILE_BYTES = T * HD * 4;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int NMS = 4;                 // split-merge hand-off slots
@@ -91,7 +102,8 @@ struct KCfg {
     static constexpr int OFF_QW = OFF_VBUF + 2 * HD * 4;
     static constexpr int OFF_KW = OFF_QW + HD * 4;
     static constexpr int OFF_IF = OFF_KW + HD * 4;
-    static constexpr int OFF_DESC = OFF_IF + HD * 2;
+    static constexpr int OFF_PBUF = OFF_IF + HD * 2;   // [NG][NV] probabilities
+    static constexpr int OFF_DESC = OFF_PBUF + (TR ? NG * NV * 4 : 0);
     static constexpr int OFF_HAND = OFF_DESC + 2 * 64;
     static constexpr int OFF_BAR = OFF_HAND + NMS * 16;
     // mbarriers: full[S], empty[S], staged[2], prepared[2], slot_free[2],
@@ -313,6 +325,163 @@ __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
                 for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pr, vv[e], acc[h][e]);
             }
         }
+    }
+}
+
+// Attend NR keys like attend_rows, with a transposed reduction: the NV =
+// NR * GP partial dots of a lane (key r, head h at index r * GP + h; heads
+// past G are zero) are summed over the L lanes of the group by halving, so
+// after log2(L) levels lane li holds the complete scores of indices
+// li * CNT + j, j < CNT: one key, CNT consecutive heads.  Only those scores
+// get exponentials; the probabilities go to the group's NV-float buffer
+// `pg` and every lane reads all of them back for the value update.
+// State: the running max m_t[j] and sum l_t[j] of this lane's heads (equal
+// across the lanes holding the same heads for other keys), acc as usual.
+// The running max is lazy: it is raised (and acc, l rescaled) only when a
+// score exceeds it by more than 2^8, so every probability stays <= 2^8.
+template <int HD, int G, int E, int L, int NR, int GP, int CNT>
+__device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
+                                               const float* __restrict__ Vt,
+                                               const int (&row)[NR], const bool (&valid)[NR],
+                                               const int li, const int lane,
+                                               const float (&q)[G][E], float (&m_t)[CNT],
+                                               float (&l_t)[CNT], float (&acc)[G][E],
+                                               float* __restrict__ pg) {
+    constexpr int NV = NR * GP;
+    constexpr float kLazy = 8.0f;
+    float s[NV];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const float* kp = Kt + row[r] * HD + li * 4;
+        float kv[E];
+#pragma unroll
+        for (int c = 0; c < E / 4; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(kp + c * 4 * L);
+            kv[4 * c + 0] = v.x;
+            kv[4 * c + 1] = v.y;
+            kv[4 * c + 2] = v.z;
+            kv[4 * c + 3] = v.w;
+        }
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            float d = 0.f;
+            if (h < G) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) d = fmaf(q[h < G ? h : 0][e], kv[e], d);
+            }
+            s[r * GP + h] = d;
+        }
+    }
+    // halving reduction over the group's lanes
+#pragma unroll
+    for (int off = L / 2, cnt = NV; off >= 1; off >>= 1, cnt >>= 1) {
+        const bool upper = (li & off) != 0;
+#pragma unroll
+        for (int i = 0; i < cnt / 2; ++i) {
+            const float send = upper ? s[i] : s[i + cnt / 2];
+            const float keep = upper ? s[i + cnt / 2] : s[i];
+            s[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    // this lane's key and first head
+    const int v0 = li * CNT;
+    const int my_r = v0 / GP;
+    bool my_valid = valid[0];
+#pragma unroll
+    for (int r = 1; r < NR; ++r)
+        if (my_r == r) my_valid = valid[r];
+    float mx[CNT];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+        s[j] = my_valid ? s[j] : -CUDART_INF_F;
+        mx[j] = s[j];
+    }
+    // max over the keys, per head: lanes holding the same heads for other keys
+#pragma unroll
+    for (int off = GP / CNT; off < L && off < NR * GP / CNT; off <<= 1) {
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+    }
+    bool need = false;
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) need |= mx[j] > m_t[j] + kLazy;
+    if (__any_sync(0xffffffffu, need)) {
+        float corr[CNT];
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) {
+            const float mn = mx[j] > m_t[j] + kLazy ? mx[j] : m_t[j];
+            corr[j] = m_t[j] == -CUDART_INF_F ? 0.f : exp2f(m_t[j] - mn);
+            l_t[j] *= corr[j];
+            m_t[j] = mn;
+        }
+        // every lane rescales acc for every head: take head h's factor from
+        // the lane that holds it for key 0
+        const int gbase = lane - li;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float c = __shfl_sync(0xffffffffu, corr[h % CNT], gbase + h / CNT);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[h][e] *= c;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+        const float pj = s[j] == -CUDART_INF_F ? 0.f : exp2f(s[j] - m_t[j]);
+        l_t[j] += pj;
+        pg[v0 + j] = pj;
+    }
+    __syncwarp();
+    float pr[NV];
+#pragma unroll
+    for (int i = 0; i < NV / 4; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(pg + 4 * i);
+        pr[4 * i + 0] = v.x;
+        pr[4 * i + 1] = v.y;
+        pr[4 * i + 2] = v.z;
+        pr[4 * i + 3] = v.w;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        if (valid[r]) {
+            const float* vp = Vt + row[r] * HD + li * 4;
+            float vv[E];
+#pragma unroll
+            for (int c = 0; c < E / 4; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(vp + c * 4 * L);
+                vv[4 * c + 0] = v.x;
+                vv[4 * c + 1] = v.y;
+                vv[4 * c + 2] = v.z;
+                vv[4 * c + 3] = v.w;
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float p = pr[r * GP + h];
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[h][e] = fmaf(p, vv[e], acc[h][e]);
+            }
+        }
+    }
+}
+
+// The per-lane state of attend_rows_tr turned into the replicated form of
+// attend_rows (every lane holds m and l of every head): l summed over the
+// lanes holding the same heads for the other keys, then each head's m and l
+// taken from the lane that holds it.
+template <int G, int L, int NR, int GP, int CNT>
+__device__ __forceinline__ void tr_state_to_heads(const int li, const int lane, float (&m_t)[CNT],
+                                                  float (&l_t)[CNT], float (&m)[G],
+                                                  float (&l)[G]) {
+#pragma unroll
+    for (int off = GP / CNT; off < L && off < NR * GP / CNT; off <<= 1) {
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) l_t[j] += __shfl_xor_sync(0xffffffffu, l_t[j], off);
+    }
+    const int gbase = lane - li;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = __shfl_sync(0xffffffffu, m_t[h % CNT], gbase + h / CNT);
+        l[h] = __shfl_sync(0xffffffffu, l_t[h % CNT], gbase + h / CNT);
     }
 }
 
@@ -795,6 +964,12 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         const float* vs = vbuf + is * HD;
 
         float q[G][E], m[G], l[G], acc[G][E];
+        float m_t[C::CNT], l_t[C::CNT];
+#pragma unroll
+        for (int j = 0; j < C::CNT; ++j) {
+            m_t[j] = -CUDART_INF_F;
+            l_t[j] = 0.f;
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -831,7 +1006,12 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     row[r] = gid + NG * (r0 + r);
                     valid[r] = kbase + static_cast<uint32_t>(row[r]) < hist_end;
                 }
-                attend_rows<HD, G, E, L, C::RC>(Kt, Vt, row, valid, li, q, m, l, acc);
+                if constexpr (C::TR)
+                    attend_rows_tr<HD, G, E, L, C::RC, C::GP, C::CNT>(
+                        Kt, Vt, row, valid, li, lane, q, m_t, l_t, acc,
+                        reinterpret_cast<float*>(smem + C::OFF_PBUF) + gid * C::NV);
+                else
+                    attend_rows<HD, G, E, L, C::RC>(Kt, Vt, row, valid, li, q, m, l, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -839,6 +1019,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         // an abort by any warp must send every consumer warp to the drain
         named_sync<C::CONS>();
         if (misc[0]) break;
+        if constexpr (C::TR) tr_state_to_heads<G, L, C::RC, C::GP, C::CNT>(li, lane, m_t, l_t, m, l);
 
         if (is_last && warp == 0) {
             const int row1[1] = {0};
