@@ -34,6 +34,24 @@ import synth  # noqa: E402
 
 HBM_FALLBACK_GBS = 6800.0
 
+# DRAM bytes (read + write) per decode launch from one ncu capture, valid for
+# the kernel source it was taken on (sha256 prefix of decode_attn.cuh); see
+# profiles/decode_attn_<workload>.md.
+MEASURED_TRAFFIC = {
+    "181216b49294d3f6": {"mid": 555_490_816, "sinks": 2_358_888_960},
+}
+
+
+def kernel_source_hash():
+    import hashlib
+    path = os.path.join(ROOT, "sequence_slot_kv_gb300", "csrc", "decode_attn.cuh")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    return MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(workload)
+
 
 def peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -349,7 +367,8 @@ def run_gpu(args, w):
         "config": config_of(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": args.traffic,
+                     "traffic": args.traffic if args.traffic is not None
+                     else measured_traffic(w.name),
                      "alg_bytes_per_launch": alg_bytes,
                      "avg_launch_us": avg_launch_s * 1e6,
                      "kernel": "slotkv_decode_attn_kernel"},
