@@ -7,7 +7,8 @@
 //
 // Two kernels per call, on one stream:
 //   * slotkv_plan_kernel (one CTA): checks every row's slot and position,
-//     lists the valid work items and resets the hand-out counter;
+//     lists the valid work items, largest first, and resets the hand-out
+//     counter;
 //   * slotkv_decode_attn_kernel (persistent, 2 CTAs per SM, launched as a
 //     programmatic dependent of the plan): each CTA runs until the list is
 //     exhausted.  The steps of "Forward Cuda Gemma", decodeBatch, fused:
@@ -492,75 +493,86 @@ __device__ __forceinline__ float partial_weight(float m, float M) {
 }
 
 // ------------------------------------------------------------------ plan
-// One CTA.  Lists every valid (row, split, kv head) in row order as a
-// 16-byte record (packed item, position, slot), raises
-// SLOTKV_DEV_RANGE for rows whose slot or position is out of range (they get
-// no items), and resets the hand-out counter.
+// One CTA.  Lists every valid (row, split, kv head) as a 16-byte record
+// (packed item, position, slot), largest first: items are binned by their
+// tile count and the bins laid out in descending order, so the small ragged
+// last splits come last and fill the end of the kernel (the order of work
+// never changes a result; only the split sizes could, and they depend on
+// the row alone).  Raises SLOTKV_DEV_RANGE for rows whose slot or position
+// is out of range (they get no items) and resets the hand-out counter.
+constexpr int kPlanBins = 64;
+
 template <int T>
 __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const DecodeParams P) {
-    __shared__ uint32_t warp_tot[kPlanThreads / 32];
-    __shared__ uint32_t row_first[kPlanThreads];
-    __shared__ uint32_t row_n[kPlanThreads];
-    __shared__ uint32_t row_p[kPlanThreads];
-    __shared__ uint32_t row_slot[kPlanThreads];
-    __shared__ uint32_t base;
+    __shared__ uint32_t bin_count[kPlanBins];
+    __shared__ uint32_t bin_cursor[kPlanBins];
+    __shared__ uint32_t total;
     grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) base = 0;
+    const uint32_t nkv = P.n_kv_head;
+    for (int i = tid; i < kPlanBins; i += kPlanThreads) bin_count[i] = 0;
     __syncthreads();
-    for (uint32_t c0 = 0; c0 < P.B; c0 += kPlanThreads) {
-        const uint32_t b = c0 + tid;
-        uint32_t ns = 0, p = 0, slot = 0;
-        if (b < P.B) {
-            p = P.positions[b];
-            slot = P.slots[b];
-            if (slot >= P.n_slots || p >= P.slot_ctx) {
-                atomicOr(P.status, kDevRange);
-            } else {
-                const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
-                ns = (p + 1 + chunk - 1) / chunk;
-            }
+    // a row's split count and the tile counts of its full and last splits
+    auto row_shape = [&](uint32_t b, uint32_t& p, uint32_t& slot, uint32_t& nsplit,
+                         uint32_t& full_tiles, uint32_t& last_tiles) {
+        p = P.positions[b];
+        slot = P.slots[b];
+        if (slot >= P.n_slots || p >= P.slot_ctx) return false;
+        const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
+        nsplit = (p + 1 + chunk - 1) / chunk;
+        full_tiles = chunk / T;
+        last_tiles = (p - (nsplit - 1) * chunk + T - 1) / T;
+        return true;
+    };
+    auto bin_of = [](uint32_t tiles) { return tiles < kPlanBins ? tiles : kPlanBins - 1u; };
+    // pass 1: histogram of item sizes
+    for (uint32_t b = tid; b < P.B; b += kPlanThreads) {
+        uint32_t p, slot, nsplit, ft, lt;
+        if (!row_shape(b, p, slot, nsplit, ft, lt)) {
+            atomicOr(P.status, kDevRange);
+            continue;
         }
-        // block-wide exclusive scan of the split counts
-        uint32_t incl = ns;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            uint32_t t = warp_tot[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, t, off);
-                if (lane >= off) t += y;
-            }
-            warp_tot[lane] = t;  // inclusive over warps
-        }
-        __syncthreads();
-        const uint32_t before = base + (warp ? warp_tot[warp - 1] : 0) + incl - ns;
-        row_first[tid] = before;
-        row_n[tid] = ns;
-        row_p[tid] = p;
-        row_slot[tid] = slot;
-        __syncthreads();
-        // one warp per row writes that row's items, lanes in parallel
-        const uint32_t rows = P.B - c0 < (uint32_t)kPlanThreads ? P.B - c0 : kPlanThreads;
-        for (uint32_t r = warp; r < rows; r += kPlanThreads / 32) {
-            const uint32_t n = row_n[r] * P.n_kv_head;
-            uint4* dst = reinterpret_cast<uint4*>(P.items) + (size_t)row_first[r] * P.n_kv_head;
-            for (uint32_t i = lane; i < n; i += 32)
-                dst[i] = make_uint4(pack_item(c0 + r, i / P.n_kv_head, i % P.n_kv_head), row_p[r],
-                                    row_slot[r], 0u);
-        }
-        __syncthreads();
-        if (tid == 0) base += warp_tot[kPlanThreads / 32 - 1];
-        __syncthreads();
+        if (nsplit > 1) atomicAdd(&bin_count[bin_of(ft)], (nsplit - 1) * nkv);
+        atomicAdd(&bin_count[bin_of(lt)], nkv);
     }
+    __syncthreads();
     if (tid == 0) {
-        P.plan[0] = base * P.n_kv_head;
+        uint32_t run = 0;
+        for (int i = kPlanBins - 1; i >= 0; --i) {
+            bin_cursor[i] = run;
+            run += bin_count[i];
+        }
+        total = run;
+    }
+    __syncthreads();
+    // pass 2: one warp per row reserves the row's ranges and writes them
+    uint4* recs = reinterpret_cast<uint4*>(P.items);
+    for (uint32_t b = warp; b < P.B; b += kPlanThreads / 32) {
+        uint32_t p = 0, slot = 0, nsplit = 0, ft = 0, lt = 0, full_base = 0, last_base = 0;
+        bool ok = false;
+        if (lane == 0) {
+            ok = row_shape(b, p, slot, nsplit, ft, lt);
+            if (ok) {
+                if (nsplit > 1) full_base = atomicAdd(&bin_cursor[bin_of(ft)], (nsplit - 1) * nkv);
+                last_base = atomicAdd(&bin_cursor[bin_of(lt)], nkv);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) continue;
+        p = __shfl_sync(0xffffffffu, p, 0);
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+        nsplit = __shfl_sync(0xffffffffu, nsplit, 0);
+        full_base = __shfl_sync(0xffffffffu, full_base, 0);
+        last_base = __shfl_sync(0xffffffffu, last_base, 0);
+        const uint32_t nfull = (nsplit - 1) * nkv;
+        for (uint32_t i = lane; i < nfull; i += 32)
+            recs[full_base + i] = make_uint4(pack_item(b, i / nkv, i % nkv), p, slot, 0u);
+        for (uint32_t i = lane; i < nkv; i += 32)
+            recs[last_base + i] = make_uint4(pack_item(b, nsplit - 1, i), p, slot, 0u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        P.plan[0] = total;
         P.plan[1] = 0;
     }
 }
