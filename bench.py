@@ -299,17 +299,35 @@ def run_gpu(args, w):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
+    graph = None
+    if args.graph:
+        # one step (all its decode calls) captured once and replayed per step
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                one_step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps * nsub)]
+          for _ in range(args.steps * (1 if graph else nsub))]
     begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     clocks.mark("begin")
     begin.record(stream)
     i = 0
     for _ in range(args.steps):
+        if graph is not None:
+            ev[i][0].record(stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            ev[i][1].record(stream)
+            i += 1
+            continue
         for t in range(nsub):
             ev[i][0].record(stream)
             kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
@@ -356,7 +374,7 @@ def run_gpu(args, w):
     d2h = nsub * hout.numel() * 4
 
     peak, peak_kind = peak_hbm()
-    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    avg_launch_s = statistics.mean(launch_ms) / 1e3 / (nsub if graph is not None else 1)
     alg_bytes = statistics.mean(bytes_per_launch)
     achieved = alg_bytes / avg_launch_s / 1e9
     line = {
@@ -374,7 +392,9 @@ def run_gpu(args, w):
                      "kernel": "slotkv_decode_attn_kernel"},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * nsub,
+        # each decode call is two kernels: the work-list plan and the decode
+        "gpu_launches": args.steps * nsub * 2,
+        "graph": bool(args.graph),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -400,6 +420,8 @@ def main():
                     metavar=("MIN_CHUNK_KEYS", "MAX_SPLITS"))
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the decode kernel, if measured")
     args = ap.parse_args()

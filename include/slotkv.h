@@ -236,6 +236,19 @@ int decode_batch_attn_noalloc(float* K, float* V, uint32_t n_slots, uint32_t slo
                               float eps, float scale, slotkv_stream_t stream);
 
 /*
+ * slot_kv_advance_positions -- positions[b] += delta for b < B, on the device
+ * (asynchronous, on `stream`).  "Forward Cuda Gemma", decodeBatch: after a
+ * step the caller advances each sequence's position and feeds it back; doing
+ * it on the device keeps a multi-step decode free of host work, so a run of
+ * steps (decode_batch_attn, slot_kv_advance_positions, ...) can be captured
+ * into one CUDA graph and replayed.  Make one decode_batch_attn call on the
+ * handle before capturing (it sets kernel attributes on first use).
+ * positions: device u32[B].  SLOTKV_ERR_ARG for a NULL pointer.
+ */
+int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,
+                              slotkv_stream_t stream);
+
+/*
  * slot_kv_get_status -- synchronise `stream`, return the sticky device flags
  * (SLOTKV_DEV_*) raised since the last call in *flags, and clear them.  After
  * SLOTKV_DEV_TIMEOUT the workspace is also cleared so later calls are valid.
@@ -254,6 +267,21 @@ int slot_kv_get_status(slotkv_t handle, slotkv_stream_t stream, uint32_t* flags)
  * max_splits = 64.
  */
 int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_splits);
+
+/*
+ * slot_kv_set_options -- norm options of the per-head "V/Q/K norm" of the
+ * Gemma path ("Forward Cuda Gemma", decodeBatch), for later decode calls on
+ * this handle.  flags is a bitwise OR of:
+ *   SLOTKV_OPT_VNORM          normalise v_new with a weightless RMS norm
+ *                             (x / sqrt(mean(x^2) + eps)) before it is cached
+ *                             and attended;
+ *   SLOTKV_OPT_NORM_PLUS_ONE  apply the Q and K norm weights as (1 + w).
+ * 0 (the default) is the plain form of decode_batch_attn.  SLOTKV_ERR_ARG for
+ * unknown bits.  Host only; takes effect at the next call.
+ */
+#define SLOTKV_OPT_VNORM 1u
+#define SLOTKV_OPT_NORM_PLUS_ONE 2u
+int slot_kv_set_options(slotkv_t handle, uint32_t flags);
 
 /* slot_kv_last_error -- message for the calling thread's last failed call
  * ("" if none).  The pointer stays valid until that thread's next call. */

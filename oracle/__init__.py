@@ -16,6 +16,10 @@ import numpy as np
 from . import build as _build
 
 
+VNORM = 1
+NORM_PLUS_ONE = 2
+
+
 class Oracle:
     def __init__(self, lib_path=None):
         if lib_path is None:
@@ -31,6 +35,10 @@ class Oracle:
                                             vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             f32, f32, vp, vp, vp, vp, ctypes.c_int]
         lib.oracle_decode_batch.restype = ctypes.c_int
+        lib.oracle_decode_batch_opts.argtypes = [u32, u32, u32, u32, u32, u32,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 f32, f32, u32, vp, vp, vp, vp, ctypes.c_int]
+        lib.oracle_decode_batch_opts.restype = ctypes.c_int
         self.lib = lib
 
     def offset_bytes(self, slot, pos, slot_ctx, kv_dim):
@@ -47,7 +55,8 @@ class Oracle:
         return y
 
     def decode_batch(self, K, V, q, k_new, v_new, positions, slots, q_norm_w,
-                     k_norm_w, inv_freq, sinks, eps, scale, n_threads=1, want64=False):
+                     k_norm_w, inv_freq, sinks, eps, scale, n_threads=1, want64=False,
+                     flags=0):
         """One decode step.  K, V: f32[n_slots][slot_ctx][n_kv_head][hd] (updated
         in place).  Returns (out f32[B][n_head][hd], out64 or None, skipped)."""
         assert K.dtype == np.float32 and V.dtype == np.float32
@@ -68,11 +77,11 @@ class Oracle:
         sk = None if sinks is None else np.ascontiguousarray(sinks, dtype=np.float32)
         out = np.zeros((B, n_head, hd), dtype=np.float32)
         out64 = np.zeros((B, n_head, hd), dtype=np.float64) if want64 else None
-        rc = self.lib.oracle_decode_batch(
+        rc = self.lib.oracle_decode_batch_opts(
             n_slots, slot_ctx, n_head, n_kv_head, hd, B,
             q.ctypes.data, k_new.ctypes.data, v_new.ctypes.data,
             positions.ctypes.data, slots.ctypes.data, qw.ctypes.data, kw.ctypes.data,
-            fr.ctypes.data, None if sk is None else sk.ctypes.data, eps, scale,
+            fr.ctypes.data, None if sk is None else sk.ctypes.data, eps, scale, int(flags),
             K.ctypes.data, V.ctypes.data, out.ctypes.data,
             None if out64 is None else out64.ctypes.data, int(n_threads))
         if rc < 0:

@@ -25,6 +25,11 @@
  * denominator and carries no value; query head h reads kv head h / (n_head /
  * n_kv_head).
  *
+ * Options (oracle_decode_batch_opts), from the per-head "V/Q/K norm" of the
+ * Gemma path on the same page: ORACLE_VNORM caches and attends the
+ * weightless RMS norm of v_new instead of v_new; ORACLE_NORM_PLUS_ONE applies
+ * the Q and K norm weights as (1 + w).
+ *
  * Build with -ffp-contract=off: the one f32 product (the RoPE angle) must be
  * a single rounded multiply.
  */
@@ -46,6 +51,15 @@ static void rms_norm(const float* x, const float* w, uint32_t n, double eps, dou
     for (uint32_t i = 0; i < n; ++i) sum_sq += (double)x[i] * (double)x[i];
     double inv_rms = 1.0 / sqrt(sum_sq / (double)n + eps);
     for (uint32_t i = 0; i < n; ++i) y[i] = (double)x[i] * inv_rms * (double)w[i];
+}
+
+/* Gemma's forms: the weight applied as (1 + w), or no weight at all (w NULL) */
+static void rms_norm_gemma(const float* x, const float* w, uint32_t n, double eps, double* y) {
+    double sum_sq = 0.0;
+    for (uint32_t i = 0; i < n; ++i) sum_sq += (double)x[i] * (double)x[i];
+    double inv_rms = 1.0 / sqrt(sum_sq / (double)n + eps);
+    for (uint32_t i = 0; i < n; ++i)
+        y[i] = (double)x[i] * inv_rms * (w ? 1.0 + (double)w[i] : 1.0);
 }
 
 /* Rotate pairs (i, i + hd/2) by angle fl32(pos * inv_freq[i]). */
@@ -74,6 +88,7 @@ typedef struct {
     const uint32_t *positions, *slots;
     const float *q_norm_w, *k_norm_w, *inv_freq, *sinks;
     float eps, scale;
+    uint32_t flags;
     float *K, *V, *out;
     double* out64;
     uint32_t row_begin, row_end;
@@ -100,10 +115,19 @@ static void decode_row(batch_job* j, uint32_t b, double* qv, double* kv, double*
     for (uint32_t g = 0; g < j->n_kv_head; ++g) {
         const float* k_in = j->k_new + ((uint64_t)b * j->n_kv_head + g) * hd;
         const float* v_in = j->v_new + ((uint64_t)b * j->n_kv_head + g) * hd;
-        oracle_norm_rope_head(k_in, j->k_norm_w, hd, j->eps, p, j->inv_freq, kv);
-        for (uint32_t i = 0; i < hd; ++i) {
-            j->K[at_p + (uint64_t)g * hd + i] = (float)kv[i];
-            j->V[at_p + (uint64_t)g * hd + i] = v_in[i];
+        if (j->flags & ORACLE_NORM_PLUS_ONE) {
+            rms_norm_gemma(k_in, j->k_norm_w, hd, (double)j->eps, kv);
+            rope(kv, hd, p, j->inv_freq);
+        } else {
+            oracle_norm_rope_head(k_in, j->k_norm_w, hd, j->eps, p, j->inv_freq, kv);
+        }
+        for (uint32_t i = 0; i < hd; ++i) j->K[at_p + (uint64_t)g * hd + i] = (float)kv[i];
+        if (j->flags & ORACLE_VNORM) {
+            /* the cached V is the weightless RMS norm of v_new */
+            rms_norm_gemma(v_in, NULL, hd, (double)j->eps, kv);
+            for (uint32_t i = 0; i < hd; ++i) j->V[at_p + (uint64_t)g * hd + i] = (float)kv[i];
+        } else {
+            for (uint32_t i = 0; i < hd; ++i) j->V[at_p + (uint64_t)g * hd + i] = v_in[i];
         }
     }
 
@@ -111,7 +135,12 @@ static void decode_row(batch_job* j, uint32_t b, double* qv, double* kv, double*
     for (uint32_t h = 0; h < j->n_head; ++h) {
         const uint32_t g = h / group;
         const float* q_in = j->q + ((uint64_t)b * j->n_head + h) * hd;
-        oracle_norm_rope_head(q_in, j->q_norm_w, hd, j->eps, p, j->inv_freq, qv);
+        if (j->flags & ORACLE_NORM_PLUS_ONE) {
+            rms_norm_gemma(q_in, j->q_norm_w, hd, (double)j->eps, qv);
+            rope(qv, hd, p, j->inv_freq);
+        } else {
+            oracle_norm_rope_head(q_in, j->q_norm_w, hd, j->eps, p, j->inv_freq, qv);
+        }
 
         double m = -INFINITY;
         for (uint32_t t = 0; t <= p; ++t) {
@@ -175,6 +204,20 @@ int oracle_decode_batch(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
                         const float* inv_freq, const float* sinks, float eps,
                         float scale, float* K, float* V, float* out, double* out64,
                         int n_threads) {
+    return oracle_decode_batch_opts(n_slots, slot_ctx, n_head, n_kv_head, head_dim, B, q,
+                                    k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                                    inv_freq, sinks, eps, scale, 0u, K, V, out, out64,
+                                    n_threads);
+}
+
+int oracle_decode_batch_opts(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
+                             uint32_t n_kv_head, uint32_t head_dim, uint32_t B,
+                             const float* q, const float* k_new, const float* v_new,
+                             const uint32_t* positions, const uint32_t* slots,
+                             const float* q_norm_w, const float* k_norm_w,
+                             const float* inv_freq, const float* sinks, float eps,
+                             float scale, uint32_t flags, float* K, float* V, float* out,
+                             double* out64, int n_threads) {
     if (B == 0) return 0;
     if (!q || !k_new || !v_new || !positions || !slots || !q_norm_w || !k_norm_w ||
         !inv_freq || !K || !V || !out)
@@ -214,6 +257,7 @@ int oracle_decode_batch(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
         j->sinks = sinks;
         j->eps = eps;
         j->scale = scale;
+        j->flags = flags;
         j->K = K;
         j->V = V;
         j->out = out;

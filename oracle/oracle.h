@@ -44,6 +44,21 @@ int oracle_decode_batch(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
                         float scale, float* K, float* V, float* out, double* out64,
                         int n_threads);
 
+/* The same step with options (bit flags):
+ *   ORACLE_VNORM          the cached and attended V is the weightless RMS norm
+ *                         of v_new (rounded to f32);
+ *   ORACLE_NORM_PLUS_ONE  the Q and K norm weights apply as (1 + w). */
+#define ORACLE_VNORM 1u
+#define ORACLE_NORM_PLUS_ONE 2u
+int oracle_decode_batch_opts(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
+                             uint32_t n_kv_head, uint32_t head_dim, uint32_t B,
+                             const float* q, const float* k_new, const float* v_new,
+                             const uint32_t* positions, const uint32_t* slots,
+                             const float* q_norm_w, const float* k_norm_w,
+                             const float* inv_freq, const float* sinks, float eps,
+                             float scale, uint32_t flags, float* K, float* V, float* out,
+                             double* out64, int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

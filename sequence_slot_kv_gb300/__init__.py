@@ -17,12 +17,14 @@ import os
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "slot_kv_get_status",
-    "slot_kv_set_split", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
+    "slot_kv_set_split", "slot_kv_advance_positions", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libslotkv.so")
 DEV_RANGE = 1
 DEV_TIMEOUT = 2
+OPT_VNORM = 1
+OPT_NORM_PLUS_ONE = 2
 SIZE_MAX = ctypes.c_size_t(-1).value
 
 _u32, _f32, _vp, _int = ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
@@ -41,6 +43,8 @@ EXPORTS = {
     "decode_batch_attn_host": (_DECODE_ARGS, _int),
     "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
     "slot_kv_set_split": ([_vp, _u32, _u32], _int),
+    "slot_kv_advance_positions": ([_vp, _u32, _u32, _vp], _int),
+    "slot_kv_set_options": ([_vp, _u32], _int),
     "decode_batch_attn_noalloc": ([_vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp],
                                   _int),
@@ -198,6 +202,10 @@ class SlotKV:
                "slot_kv_get_status")
         return int(v.value)
 
+    def set_options(self, flags):
+        """OPT_VNORM and/or OPT_NORM_PLUS_ONE (see slot_kv_set_options)."""
+        _check(_lib.slot_kv_set_options(self._h, flags), "slot_kv_set_options")
+
     def set_split(self, min_chunk_keys, max_splits):
         _check(_lib.slot_kv_set_split(self._h, min_chunk_keys, max_splits), "slot_kv_set_split")
 
@@ -253,6 +261,14 @@ def slot_kv_get_status(h, stream=None):
 
 def slot_kv_set_split(h, min_chunk_keys, max_splits):
     h.set_split(min_chunk_keys, max_splits)
+
+
+def slot_kv_advance_positions(positions, delta=1, stream=None):
+    """positions += delta on the device (int32 CUDA tensor), on ``stream``."""
+    import torch
+    _check(_lib.slot_kv_advance_positions(_ptr(positions, torch.int32, "positions"),
+                                          int(positions.numel()), int(delta),
+                                          _stream_ptr(stream)), "slot_kv_advance_positions")
 
 
 def decode_batch_attn_noalloc(K, V, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,

@@ -47,6 +47,8 @@ namespace slotkv {
 
 constexpr uint32_t kDevRange = 1u;
 constexpr uint32_t kDevTimeout = 2u;
+constexpr uint32_t kOptVNorm = 1u;        // SLOTKV_OPT_VNORM
+constexpr uint32_t kOptNormPlusOne = 2u;  // SLOTKV_OPT_NORM_PLUS_ONE
 constexpr int kPlanThreads = 1024;
 
 __host__ __device__ constexpr int pow2_floor(int x) {
@@ -636,8 +638,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     for (int i = tid; i < HD; i += C::THREADS) {
-        qw_s[i] = P.q_norm_w[i];
-        kw_s[i] = P.k_norm_w[i];
+        // Gemma's form applies the norm weights as (1 + w)
+        const float w1 = (P.flags & kOptNormPlusOne) ? 1.0f : 0.0f;
+        qw_s[i] = w1 + P.q_norm_w[i];
+        kw_s[i] = w1 + P.k_norm_w[i];
         if (i < HD / 2) if_s[i] = P.inv_freq[i];
     }
     __syncthreads();
@@ -808,6 +812,23 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                             v[i] = (y0 * cs[j] - y1 * sn[j]) * mul;
                             v[i + HD / 2] = (y1 * cs[j] + y0 * sn[j]) * mul;
                         }
+                    }
+                    if (is_last && (P.flags & kOptVNorm)) {
+                        // weightless RMS norm of v_new, cached and attended
+                        float* v = vbuf + is * HD;
+                        float x[HD / 32];
+                        float ss = 0.f;
+#pragma unroll
+                        for (int j = 0; j < HD / 32; ++j) {
+                            x[j] = v[lane + 32 * j];
+                            ss = fmaf(x[j], x[j], ss);
+                        }
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                        const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + P.eps);
+#pragma unroll
+                        for (int j = 0; j < HD / 32; ++j) v[lane + 32 * j] = x[j] * inv;
                     }
                 }
                 __syncwarp();

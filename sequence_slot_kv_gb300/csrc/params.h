@@ -32,6 +32,7 @@ struct DecodeParams {
     uint32_t max_splits;
     float eps;
     float scale_log2;        // softmax scale * log2(e): scores live in base 2
+    uint32_t flags;          // SLOTKV_OPT_* norm options
 };
 
 // Keys per split chunk for a row with n_keys keys (p + 1).  Depends only on

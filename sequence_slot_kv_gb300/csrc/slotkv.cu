@@ -60,6 +60,7 @@ struct slotkv_s {
     bool owns_kv = false;
     uint32_t max_rows = 0, max_n_head = 0;
     uint32_t chunk_min = 0, max_splits = 0;
+    uint32_t options = 0;
     float* ws_ml = nullptr;
     float* ws_acc = nullptr;
     uint32_t* counters = nullptr;
@@ -191,6 +192,7 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.max_splits = h->max_splits;
     P.eps = eps;
     P.scale_log2 = scale * 1.4426950408889634f;
+    P.flags = h->options;
     const int G = (int)(n_head / h->n_kv_head);
     // persistent CTAs: two per SM, never more than there can be work items
     const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h);
@@ -231,6 +233,12 @@ int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
 
 namespace slotkv {
 void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
+__global__ void advance_positions_kernel(uint32_t* __restrict__ pos, uint32_t B,
+                                         uint32_t delta) {
+    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) pos[b] += delta;
+}
 }  // namespace slotkv
 
 extern "C" {
@@ -416,6 +424,18 @@ int decode_batch_attn_host(slotkv_t h, uint32_t B, uint32_t n_head, const float*
     return SLOTKV_OK;
 }
 
+int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,
+                              slotkv_stream_t stream) {
+    g_err[0] = 0;
+    if (B == 0) return SLOTKV_OK;
+    if (!positions) return fail(SLOTKV_ERR_ARG, "positions is null");
+    slotkv::advance_positions_kernel<<<(B + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
+        positions, B, delta);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "advance kernel launch");
+    return SLOTKV_OK;
+}
+
 int slot_kv_get_status(slotkv_t h, slotkv_stream_t stream, uint32_t* flags) {
     g_err[0] = 0;
     if (!valid_handle(h) || !flags) return fail(SLOTKV_ERR_ARG, "bad handle or flags pointer");
@@ -436,6 +456,15 @@ int slot_kv_get_status(slotkv_t h, slotkv_stream_t stream, uint32_t* flags) {
         if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
     }
     *flags = v;
+    return SLOTKV_OK;
+}
+
+int slot_kv_set_options(slotkv_t h, uint32_t flags) {
+    g_err[0] = 0;
+    if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (flags & ~(SLOTKV_OPT_VNORM | SLOTKV_OPT_NORM_PLUS_ONE))
+        return fail(SLOTKV_ERR_ARG, "unknown option bits 0x%x", flags);
+    h->options = flags;
     return SLOTKV_OK;
 }
 

@@ -82,7 +82,7 @@ class DeviceRun:
         self.kv.free()
 
 
-def oracle_rows(w, rows, steps=1, n_threads=None, first_step=0):
+def oracle_rows(w, rows, steps=1, n_threads=None, first_step=0, flags=0):
     """Run the oracle for rows ``rows`` over ``steps`` consecutive steps on
     compact host slot buffers regenerated from the history recipe.
     Returns (outs [steps][len(rows)][n_head][hd], K, V, ctx_end) where K/V are
@@ -104,7 +104,7 @@ def oracle_rows(w, rows, steps=1, n_threads=None, first_step=0):
         out, _, skipped = o.decode_batch(
             K, V, q[rows], kn[rows], vn[rows], pos[rows],
             np.arange(len(rows), dtype=np.uint32), w.q_norm_w(), w.k_norm_w(), w.inv_freq(),
-            w.sink_logits(), w.eps, w.scale, n_threads=nt)
+            w.sink_logits(), w.eps, w.scale, n_threads=nt, flags=flags)
         assert skipped == 0
         outs.append(out)
     return np.stack(outs), K, V

@@ -47,7 +47,7 @@ class Case:
         self.positions = np.zeros(B, dtype=np.uint32)
         self.slots = np.arange(B, dtype=np.uint32) % n_slots
 
-    def run(self, o, want64=True, **over):
+    def run(self, o, want64=True, flags=0, **over):
         K = over.pop("K", self.K)
         V = over.pop("V", self.V)
         args = dict(q=self.q, k_new=self.k_new, v_new=self.v_new,
@@ -55,7 +55,7 @@ class Case:
                     k_norm_w=self.k_norm_w, inv_freq=self.inv_freq, sinks=self.sinks,
                     eps=self.eps, scale=self.scale)
         args.update(over)
-        return o.decode_batch(K, V, want64=want64, **args)
+        return o.decode_batch(K, V, want64=want64, flags=flags, **args)
 
 
 def _close(a, b, tol, what):
@@ -450,6 +450,53 @@ def pin_one_dominant_key(o):
     out, out64, _ = c.run(o, K=K, V=c.V.copy())
     for h in range(2):
         _close(out64[0, h], c.V[0, 6, 0].astype(np.float64), 1e-300, "dominant key")
+
+
+def pin_option_norm_plus_one(o):
+    """Gemma's norm form: with NORM_PLUS_ONE the written K at pos 0 is torch's
+    RMS norm with weight (1 + w), and the whole step equals the plain step
+    run with weights fl32(1 + w) (up to that one rounding)."""
+    import oracle as oracle_pkg
+    c = Case(B=2, n_slots=2, slot_ctx=12, n_head=4, n_kv_head=2, hd=16)
+    c.positions = np.array([0, 9], dtype=np.uint32)
+    c.slots = np.array([1, 0], dtype=np.uint32)
+    c.q_norm_w = (0.1 * np.random.default_rng(21).standard_normal(16)).astype(np.float32)
+    c.k_norm_w = (0.1 * np.random.default_rng(22).standard_normal(16)).astype(np.float32)
+    K, V = c.K.copy(), c.V.copy()
+    _, a64, _ = c.run(o, K=K, V=V, flags=oracle_pkg.NORM_PLUS_ONE)
+    ref = torch.nn.functional.rms_norm(
+        torch.from_numpy(c.k_new[0].astype(np.float64)), (16,),
+        torch.from_numpy(1.0 + c.k_norm_w.astype(np.float64)),
+        eps=float(np.float32(c.eps))).numpy()
+    _close(K[1, 0], ref, 1e-6, "(1+w) written K")
+    c2 = Case(B=2, n_slots=2, slot_ctx=12, n_head=4, n_kv_head=2, hd=16)
+    c2.positions, c2.slots = c.positions, c.slots
+    c2.q_norm_w = (np.float32(1) + c.q_norm_w).astype(np.float32)
+    c2.k_norm_w = (np.float32(1) + c.k_norm_w).astype(np.float32)
+    _, b64, _ = c2.run(o, K=c.K.copy(), V=c.V.copy())
+    _close(a64, b64, 1e-6, "(1+w) vs shifted weights")
+
+
+def pin_option_vnorm(o):
+    """With VNORM the cached V row is the weightless RMS norm of v_new, and at
+    pos 0 (only that key) the output is that normed vector."""
+    import oracle as oracle_pkg
+    c = Case(B=2, n_slots=2, slot_ctx=10, n_head=4, n_kv_head=2, hd=16)
+    c.positions = np.array([0, 7], dtype=np.uint32)
+    c.slots = np.array([0, 1], dtype=np.uint32)
+    K, V = c.K.copy(), c.V.copy()
+    _, out64, _ = c.run(o, K=K, V=V, flags=oracle_pkg.VNORM)
+    for b in range(2):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(c.v_new[b].astype(np.float64)),
+                                           (16,), eps=float(np.float32(c.eps))).numpy()
+        _close(V[c.slots[b], c.positions[b]], ref, 1e-6, "normed V row")
+        if c.positions[b] == 0:
+            for h in range(4):
+                assert np.array_equal(out64[b, h], V[0, 0, h // 2].astype(np.float64))
+    # the history rows are used as stored
+    mask = np.ones(K.shape[:2], dtype=bool)
+    mask[0, 0] = mask[1, 7] = False
+    assert np.array_equal(V[mask], c.V[mask])
 
 
 def pin_brute_force_tiny(o):

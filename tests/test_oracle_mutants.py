@@ -42,9 +42,9 @@ MUTANTS = [
      "y[i] = (double)x[i] * inv_rms * (1.0 + (double)w[i]);", False),
     ("eps_outside_sqrt",
      "1.0 / sqrt(sum_sq / (double)n + eps);", "1.0 / (sqrt(sum_sq / (double)n) + eps);",
-     False),
+     True),
     ("norm_over_sum_not_mean",
-     "sqrt(sum_sq / (double)n + eps)", "sqrt(sum_sq + eps)", False),
+     "sqrt(sum_sq / (double)n + eps)", "sqrt(sum_sq + eps)", True),
     ("cached_k_not_rotated",
      "oracle_norm_rope_head(k_in, j->k_norm_w, hd, j->eps, p, j->inv_freq, kv);",
      "oracle_norm_rope_head(k_in, j->k_norm_w, hd, j->eps, 0, j->inv_freq, kv);", False),
@@ -62,6 +62,12 @@ MUTANTS = [
     ("row_base_ignores_slot",
      "const uint64_t row0 = (uint64_t)slot * j->slot_ctx * kv_dim;",
      "const uint64_t row0 = 0;", False),
+    ("vnorm_with_weight",
+     "rms_norm_gemma(v_in, NULL, hd,", "rms_norm_gemma(v_in, j->k_norm_w, hd,", False),
+    ("vnorm_ignored",
+     "if (j->flags & ORACLE_VNORM) {", "if (0) {", False),
+    ("plus_one_dropped",
+     "(w ? 1.0 + (double)w[i] : 1.0)", "(w ? (double)w[i] : 1.0)", False),
     ("exp_without_max_subtraction",
      "score[t] = exp(score[t] - m);", "score[t] = exp(score[t]);", False),
     ("max_taken_over_first_key_only",
