@@ -409,6 +409,67 @@ def run_gpu(args, w):
         torch.distributed.destroy_process_group()
 
 
+def run_prefill(args):
+    """Batched causal prefill at the mid geometry: 8 sequences, each adding a
+    512-token prompt chunk after 1536 positions of history.  A step is one
+    prefill_batch_attn call over all 4096 tokens."""
+    import torch
+    import sequence_slot_kv_gb300 as skv
+    n_seq, hist, chunk = 8, 1536, 512
+    base = synth.WORKLOADS["mid"]
+    n_tok = n_seq * chunk
+    w = base.replace(name="prefill", index=20, B=n_tok, n_slots=16, slot_ctx=hist + chunk,
+                     pos_rule="fixed", fixed_positions=tuple([0] * n_tok))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    K = torch.empty(shape, device=dev)
+    V = torch.empty(shape, device=dev)
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), sp)
+    kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, n_tok, w.n_head,
+                    k_buf=K, v_buf=V)
+    slots = np.repeat(np.arange(n_seq, dtype=np.int32) * 2, chunk)
+    pos = np.tile(np.arange(hist, hist + chunk, dtype=np.int32), n_seq)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    q, kn, vn = d(w.q()), d(w.k_new()), d(w.v_new())
+    ps, ss = d(pos), d(slots)
+    qw, kw, inv = d(w.q_norm_w()), d(w.k_norm_w()), d(w.inv_freq())
+    out = torch.empty((n_tok, w.n_head, w.head_dim), device=dev)
+
+    def step():
+        kv.prefill_batch_attn(q, kn, vn, ps, ss, qw, kw, inv, None, out, w.eps, w.scale,
+                              stream=sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert kv.get_status(sp) == 0
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = b.elapsed_time(e) / args.steps
+    # bytes as the path reads them: every token reads its own keys 0..pos
+    per_token_bytes = int((pos.astype(np.int64) + 1).sum()) * 2 * w.kv_dim * 4
+    io = n_tok * (2 * w.n_head * w.head_dim + 4 * w.kv_dim) * 4
+    line = {"metric": "slot-attn prefill tokens/s", "value": n_tok / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "prefill", "sequences": n_seq, "history": hist,
+                       "prompt_chunk": chunk, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
+                       "head_dim": w.head_dim},
+            "key_bytes_read_per_step": per_token_bytes, "io_bytes_per_step": io,
+            "effective_GBps": (per_token_bytes + io) / (ms / 1e3) / 1e9,
+            "gpu_launches": args.steps * 3}
+    print(json.dumps(line), flush=True)
+    kv.free()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,6 +481,8 @@ def main():
                     metavar=("MIN_CHUNK_KEYS", "MAX_SPLITS"))
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time batched causal prefill instead of the decode step")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--traffic", type=float, default=None,
@@ -427,6 +490,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.prefill:
+        run_prefill(args)
+        return
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -164,6 +164,28 @@ int decode_batch_attn(slotkv_t handle, uint32_t B, uint32_t n_head, const float*
                       float* out, float eps, float scale, slotkv_stream_t stream);
 
 /*
+ * prefill_batch_attn -- batched causal prefill into slots: n_tok new tokens,
+ * each with its own slot and position, written and attended in one call.
+ * "Forward Cuda Gemma", prefillBatched (batched causal attention and
+ * batched norm/RoPE/KV write, equal to running the tokens one decode step
+ * at a time) and "Forward Cuda", batched prefill into the given slot.
+ * Tokens may share a slot; within a slot their positions must be distinct,
+ * and the slot must already hold every position below its tokens' that is
+ * not itself a token of this call.  The result for every token equals
+ * decode_batch_attn run on the tokens one at a time in increasing position
+ * (up to f32 rounding): first every token's k' and v go into its slot row,
+ * then each token attends keys 0..pos of its slot, new rows included.
+ * Arguments as decode_batch_attn with B = n_tok (<= max_rows); q, k_new,
+ * v_new, positions, slots and out are indexed by token.  The options of
+ * slot_kv_set_options apply.  Errors as decode_batch_attn.
+ */
+int prefill_batch_attn(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const float* q,
+                       const float* k_new, const float* v_new, const uint32_t* positions,
+                       const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
+                       const float* inv_freq, const float* sinks, float* out, float eps,
+                       float scale, slotkv_stream_t stream);
+
+/*
  * decode_batch_attn_host -- decode_batch_attn for callers whose per-step
  * inputs and output live in host memory.  q, k_new, v_new, positions, slots
  * and out are HOST pointers with the layouts above (pinned memory gives

@@ -16,7 +16,7 @@ import os
 
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
-    "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "slot_kv_get_status",
+    "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn", "slot_kv_get_status",
     "slot_kv_set_split", "slot_kv_advance_positions", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
 ]
 
@@ -41,6 +41,7 @@ EXPORTS = {
     "slot_kv_geometry": ([_vp] + [ctypes.POINTER(_u32)] * 6, _int),
     "decode_batch_attn": (_DECODE_ARGS, _int),
     "decode_batch_attn_host": (_DECODE_ARGS, _int),
+    "prefill_batch_attn": (_DECODE_ARGS, _int),
     "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
     "slot_kv_set_split": ([_vp, _u32, _u32], _int),
     "slot_kv_advance_positions": ([_vp, _u32, _u32, _vp], _int),
@@ -181,6 +182,22 @@ class SlotKV:
             eps, scale, _stream_ptr(stream)), "decode_batch_attn")
         return out
 
+    def prefill_batch_attn(self, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                           inv_freq, sinks, out, eps, scale, stream=None):
+        """Batched causal prefill: tokens (rows of q, k_new, v_new, positions,
+        slots, out) are written into their slots and each attends keys
+        0..pos of its slot, the call's other new rows included."""
+        import torch
+        n, n_head = int(q.shape[0]), int(q.shape[1])
+        f, u = torch.float32, torch.int32
+        _check(_lib.prefill_batch_attn(
+            self._h, n, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
+            _ptr(v_new, f, "v_new"), _ptr(positions, u, "positions"), _ptr(slots, u, "slots"),
+            _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"), _ptr(out, f, "out"),
+            eps, scale, _stream_ptr(stream)), "prefill_batch_attn")
+        return out
+
     def decode_batch_attn_host(self, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
         """As decode_batch_attn, with q/k_new/v_new/positions/slots/out in host
@@ -247,6 +264,12 @@ def decode_batch_attn(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, 
                       sinks, out, eps, scale, stream=None):
     return h.decode_batch_attn(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                                inv_freq, sinks, out, eps, scale, stream)
+
+
+def prefill_batch_attn(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
+                       sinks, out, eps, scale, stream=None):
+    return h.prefill_batch_attn(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                                inv_freq, sinks, out, eps, scale, stream)
 
 
 def decode_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,

@@ -494,6 +494,69 @@ __device__ __forceinline__ float partial_weight(float m, float M) {
     return m == -CUDART_INF_F ? 0.f : exp2f(m - M);
 }
 
+// ------------------------------------------------ per-warp vector routines
+// Shared by the decode kernel's prep warp and the prefill KV-write kernel, so
+// both produce bit-identical vectors.  A lane owns the rotation pairs
+// (i, i + hd/2) for i = lane + 32 j, j < hd/64.
+
+// cos/sin of the f32 RoPE angles fl32((float)p * inv_freq[i]) of this lane's pairs.
+template <int HD>
+__device__ __forceinline__ void warp_rope_angles(uint32_t p, const float* inv_freq,
+                                                 float (&cs)[HD / 64], float (&sn)[HD / 64],
+                                                 int lane) {
+    const float fp = static_cast<float>(p);
+#pragma unroll
+    for (int j = 0; j < HD / 64; ++j) sincosf(__fmul_rn(fp, inv_freq[lane + 32 * j]), &sn[j], &cs[j]);
+}
+
+// dst = RoPE(src / sqrt(mean(src^2) + eps) * (w1 + w)) * mul, one head vector;
+// w1 is 0 (plain weights) or 1 (Gemma's (1 + w)).  src may equal dst.
+template <int HD>
+__device__ __forceinline__ void warp_norm_rope(const float* src, float* dst, const float* w,
+                                               float w1, float mul, float eps,
+                                               const float (&cs)[HD / 64],
+                                               const float (&sn)[HD / 64], int lane) {
+    constexpr int PPL = HD / 64;
+    float x0[PPL], x1[PPL];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < PPL; ++j) {
+        x0[j] = src[lane + 32 * j];
+        x1[j] = src[lane + 32 * j + HD / 2];
+        ss = fmaf(x0[j], x0[j], ss);
+        ss = fmaf(x1[j], x1[j], ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + eps);
+#pragma unroll
+    for (int j = 0; j < PPL; ++j) {
+        const int i = lane + 32 * j;
+        const float y0 = x0[j] * inv * (w1 + w[i]);
+        const float y1 = x1[j] * inv * (w1 + w[i + HD / 2]);
+        dst[i] = (y0 * cs[j] - y1 * sn[j]) * mul;
+        dst[i + HD / 2] = (y1 * cs[j] + y0 * sn[j]) * mul;
+    }
+}
+
+// dst = src / sqrt(mean(src^2) + eps), the weightless RMS norm.  src may equal dst.
+template <int HD>
+__device__ __forceinline__ void warp_rms_norm_plain(const float* src, float* dst, float eps,
+                                                    int lane) {
+    float x[HD / 32];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) {
+        x[j] = src[lane + 32 * j];
+        ss = fmaf(x[j], x[j], ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + eps);
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) dst[lane + 32 * j] = x[j] * inv;
+}
+
 // ------------------------------------------------------------------ plan
 // One CTA.  Lists every valid (row, split, kv head) as a 16-byte record
 // (packed item, position, slot), largest first: items are binned by their
@@ -523,7 +586,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
         nsplit = (p + 1 + chunk - 1) / chunk;
         full_tiles = chunk / T;
-        last_tiles = (p - (nsplit - 1) * chunk + T - 1) / T;
+        last_tiles = (p + (P.prefill ? 1u : 0u) - (nsplit - 1) * chunk + T - 1) / T;
         return true;
     };
     auto bin_of = [](uint32_t tiles) { return tiles < kPlanBins ? tiles : kPlanBins - 1u; };
@@ -638,10 +701,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     for (int i = tid; i < HD; i += C::THREADS) {
-        // Gemma's form applies the norm weights as (1 + w)
-        const float w1 = (P.flags & kOptNormPlusOne) ? 1.0f : 0.0f;
-        qw_s[i] = w1 + P.q_norm_w[i];
-        kw_s[i] = w1 + P.k_norm_w[i];
+        qw_s[i] = P.q_norm_w[i];
+        kw_s[i] = P.k_norm_w[i];
         if (i < HD / 2) if_s[i] = P.inv_freq[i];
     }
     __syncthreads();
@@ -674,8 +735,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
                 const uint32_t nsplit = (p + 1 + chunk - 1) / chunk;
                 const uint32_t k0 = split * chunk;
-                const bool is_last = split == nsplit - 1;
-                const uint32_t hist_end = is_last ? p : k0 + chunk;
+                // in prefill mode every key, p included, is read from the slot
+                // (the KV-write kernel has written the new rows already)
+                const bool is_last = !P.prefill && split == nsplit - 1;
+                const uint32_t hist_end = is_last ? p : (k0 + chunk < p + 1 ? k0 + chunk : p + 1);
                 const uint32_t n_hist = hist_end > k0 ? hist_end - k0 : 0;
                 const uint32_t ntiles = (n_hist + T - 1) / T;
                 d->b = b;
@@ -781,55 +844,17 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 const bool is_last = desc[is].is_last != 0;
                 if (!end) {
                     float cs[PPL], sn[PPL];
-                    const float fp = static_cast<float>(p);
-#pragma unroll
-                    for (int j = 0; j < PPL; ++j)
-                        sincosf(__fmul_rn(fp, if_s[lane + 32 * j]), &sn[j], &cs[j]);
+                    warp_rope_angles<HD>(p, if_s, cs, sn, lane);
+                    const float w1 = (P.flags & kOptNormPlusOne) ? 1.0f : 0.0f;
                     const int nvec = G + (is_last ? 1 : 0);
                     for (int x = 0; x < nvec; ++x) {
                         const bool isq = x < G;
                         float* v = isq ? qbuf + (is * G + x) * HD : kbuf + is * HD;
-                        const float* w = isq ? qw_s : kw_s;
-                        float x0[PPL], x1[PPL];
-                        float ss = 0.f;
-#pragma unroll
-                        for (int j = 0; j < PPL; ++j) {
-                            x0[j] = v[lane + 32 * j];
-                            x1[j] = v[lane + 32 * j + HD / 2];
-                            ss = fmaf(x0[j], x0[j], ss);
-                            ss = fmaf(x1[j], x1[j], ss);
-                        }
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                        const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + P.eps);
-                        const float mul = isq ? P.scale_log2 : 1.0f;
-#pragma unroll
-                        for (int j = 0; j < PPL; ++j) {
-                            const int i = lane + 32 * j;
-                            const float y0 = x0[j] * inv * w[i];
-                            const float y1 = x1[j] * inv * w[i + HD / 2];
-                            v[i] = (y0 * cs[j] - y1 * sn[j]) * mul;
-                            v[i + HD / 2] = (y1 * cs[j] + y0 * sn[j]) * mul;
-                        }
+                        warp_norm_rope<HD>(v, v, isq ? qw_s : kw_s, w1,
+                                           isq ? P.scale_log2 : 1.0f, P.eps, cs, sn, lane);
                     }
-                    if (is_last && (P.flags & kOptVNorm)) {
-                        // weightless RMS norm of v_new, cached and attended
-                        float* v = vbuf + is * HD;
-                        float x[HD / 32];
-                        float ss = 0.f;
-#pragma unroll
-                        for (int j = 0; j < HD / 32; ++j) {
-                            x[j] = v[lane + 32 * j];
-                            ss = fmaf(x[j], x[j], ss);
-                        }
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                        const float inv = 1.0f / sqrtf(ss * (1.0f / HD) + P.eps);
-#pragma unroll
-                        for (int j = 0; j < HD / 32; ++j) v[lane + 32 * j] = x[j] * inv;
-                    }
+                    if (is_last && (P.flags & kOptVNorm))
+                        warp_rms_norm_plain<HD>(vbuf + is * HD, vbuf + is * HD, P.eps, lane);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(prepared0 + 8 * is);
@@ -1204,6 +1229,32 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
     }
 }
 
+// ------------------------------------------------------------ prefill KV write
+// One warp per (token, kv head): k' = RoPE(RMSnorm(k_new)) and v (or its
+// weightless norm) into the slot row (slot*slot_ctx + pos).  Out-of-range
+// tokens are skipped (the plan kernel raises the flag).
+template <int HD>
+__global__ void __launch_bounds__(128) slotkv_write_kv_kernel(const DecodeParams P) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t wg = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const uint32_t tok = wg / P.n_kv_head, kvh = wg % P.n_kv_head;
+    if (tok >= P.B) return;
+    const uint32_t p = P.positions[tok], slot = P.slots[tok];
+    if (slot >= P.n_slots || p >= P.slot_ctx) return;
+    float cs[HD / 64], sn[HD / 64];
+    warp_rope_angles<HD>(p, P.inv_freq, cs, sn, lane);
+    const float w1 = (P.flags & kOptNormPlusOne) ? 1.0f : 0.0f;
+    const size_t src = (static_cast<size_t>(tok) * P.n_kv_head + kvh) * HD;
+    const size_t dst = ((static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh) * HD;
+    warp_norm_rope<HD>(P.k_new + src, P.K + dst, P.k_norm_w, w1, 1.0f, P.eps, cs, sn, lane);
+    if (P.flags & kOptVNorm) {
+        warp_rms_norm_plain<HD>(P.v_new + src, P.V + dst, P.eps, lane);
+    } else {
+#pragma unroll
+        for (int j = 0; j < HD / 32; ++j) P.V[dst + lane + 32 * j] = P.v_new[src + lane + 32 * j];
+    }
+}
+
 template <int HD, int G>
 int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                unsigned ctas, cudaStream_t stream) {
@@ -1220,6 +1271,10 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
         if (e != cudaSuccess) return static_cast<int>(e);
         if (fa.numRegs != 128) return static_cast<int>(cudaErrorInvalidConfiguration);
         configured = true;
+    }
+    if (p.prefill) {
+        const uint32_t warps = p.B * p.n_kv_head;
+        slotkv_write_kv_kernel<HD><<<(warps + 3) / 4, 128, 0, stream>>>(p);
     }
     slotkv_plan_kernel<C::T><<<1, kPlanThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();

@@ -179,6 +179,7 @@ extern "C" int decode_batch_attn_noalloc(
     P.eps = eps;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.flags = 0;
+    P.prefill = 0;
     const uint64_t bound = ((uint64_t)slot_ctx + chunk_min - 1) / chunk_min;
     const uint64_t splits = bound < kNoAllocMaxSplits ? bound : kNoAllocMaxSplits;
     int sms = 0;

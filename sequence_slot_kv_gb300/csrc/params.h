@@ -33,6 +33,7 @@ struct DecodeParams {
     float eps;
     float scale_log2;        // softmax scale * log2(e): scores live in base 2
     uint32_t flags;          // SLOTKV_OPT_* norm options
+    uint32_t prefill;        // 1: rows are prefill tokens (keys all read from the slot)
 };
 
 // Keys per split chunk for a row with n_keys keys (p + 1).  Depends only on

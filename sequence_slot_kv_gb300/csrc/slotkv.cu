@@ -163,8 +163,10 @@ uint32_t grid_splits(const slotkv_s* h) {
 int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float* k_new,
            const float* v_new, const uint32_t* positions, const uint32_t* slots,
            const float* q_norm_w, const float* k_norm_w, const float* inv_freq,
-           const float* sinks, float* out, float eps, float scale, cudaStream_t stream) {
+           const float* sinks, float* out, float eps, float scale, cudaStream_t stream,
+           bool prefill = false) {
     DecodeParams P;
+    P.prefill = prefill ? 1u : 0u;
     P.q = q;
     P.k_new = k_new;
     P.v_new = v_new;
@@ -392,6 +394,19 @@ int decode_batch_attn(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
     if (rc != SLOTKV_OK || B == 0) return rc;
     return launch(h, B, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
                   sinks, out, eps, scale, (cudaStream_t)stream);
+}
+
+int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
+                       const float* k_new, const float* v_new, const uint32_t* positions,
+                       const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
+                       const float* inv_freq, const float* sinks, float* out, float eps,
+                       float scale, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w,
+                               k_norm_w, inv_freq, out);
+    if (rc != SLOTKV_OK || n_tok == 0) return rc;
+    return launch(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                  inv_freq, sinks, out, eps, scale, (cudaStream_t)stream, true);
 }
 
 int decode_batch_attn_host(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
