@@ -30,6 +30,12 @@
  * weightless RMS norm of v_new instead of v_new; ORACLE_NORM_PLUS_ONE applies
  * the Q and K norm weights as (1 + w).
  *
+ * Paged mode (oracle_decode_batch_paged): the buffers are a pool of n_slots
+ * blocks of slot_ctx positions, and row b's key t lives in block
+ * block_tables[b][t / slot_ctx] at offset t % slot_ctx (the paged KV cache
+ * with per-sequence block tables of the Qwen3SsmLayer page,
+ * decode_multi_seq).
+ *
  * Build with -ffp-contract=off: the one f32 product (the RoPE angle) must be
  * a single rounded multiply.
  */
@@ -89,27 +95,48 @@ typedef struct {
     const float *q_norm_w, *k_norm_w, *inv_freq, *sinks;
     float eps, scale;
     uint32_t flags;
+    const uint32_t* block_tables; /* paged mode: [B][bt_stride] block ids, else NULL */
+    uint32_t bt_stride;
     float *K, *V, *out;
     double* out64;
     uint32_t row_begin, row_end;
     int skipped;
 } batch_job;
 
+/* Element offset of key (position) t of row b in the K/V buffers.  Slot
+ * mode: (slot * slot_ctx + t) * kv_dim.  Paged mode, where the buffers are
+ * n_slots blocks of slot_ctx positions: block block_tables[b][t / slot_ctx],
+ * offset t % slot_ctx within it. */
+static uint64_t key_offset(const batch_job* j, uint32_t b, uint32_t t) {
+    const uint64_t kv_dim = (uint64_t)j->n_kv_head * j->hd;
+    if (j->block_tables) {
+        const uint32_t blk = j->block_tables[(uint64_t)b * j->bt_stride + t / j->slot_ctx];
+        return ((uint64_t)blk * j->slot_ctx + t % j->slot_ctx) * kv_dim;
+    }
+    return ((uint64_t)j->slots[b] * j->slot_ctx + t) * kv_dim;
+}
+
+/* Does row b satisfy the precondition (its keys 0..p all addressable)? */
+static int row_in_range(const batch_job* j, uint32_t b) {
+    const uint32_t p = j->positions[b];
+    if (!j->block_tables) return j->slots[b] < j->n_slots && p < j->slot_ctx;
+    if ((uint64_t)p >= (uint64_t)j->bt_stride * j->slot_ctx) return 0;
+    for (uint32_t i = 0; i <= p / j->slot_ctx; ++i)
+        if (j->block_tables[(uint64_t)b * j->bt_stride + i] >= j->n_slots) return 0;
+    return 1;
+}
+
 /* One row of the step: write its new K/V, then attend for every query head. */
 static void decode_row(batch_job* j, uint32_t b, double* qv, double* kv, double* score,
                        double* acc) {
     const uint32_t hd = j->hd;
-    const uint32_t kv_dim = j->n_kv_head * hd;
     const uint32_t group = j->n_head / j->n_kv_head;
     const uint32_t p = j->positions[b];
-    const uint32_t slot = j->slots[b];
-    if (slot >= j->n_slots || p >= j->slot_ctx) {
+    if (!row_in_range(j, b)) {
         j->skipped += 1;
         return;
     }
-    /* element offset of (slot, pos) in the slot buffers */
-    const uint64_t row0 = (uint64_t)slot * j->slot_ctx * kv_dim;
-    const uint64_t at_p = row0 + (uint64_t)p * kv_dim;
+    const uint64_t at_p = key_offset(j, b, p);
 
     /* KV write: the cache holds the normed, rotated K (rounded to f32) and the raw V */
     for (uint32_t g = 0; g < j->n_kv_head; ++g) {
@@ -144,7 +171,7 @@ static void decode_row(batch_job* j, uint32_t b, double* qv, double* kv, double*
 
         double m = -INFINITY;
         for (uint32_t t = 0; t <= p; ++t) {
-            const float* k_row = j->K + row0 + (uint64_t)t * kv_dim + (uint64_t)g * hd;
+            const float* k_row = j->K + key_offset(j, b, t) + (uint64_t)g * hd;
             double dot = 0.0;
             for (uint32_t i = 0; i < hd; ++i) dot += qv[i] * (double)k_row[i];
             score[t] = (double)j->scale * dot;
@@ -165,7 +192,7 @@ static void decode_row(batch_job* j, uint32_t b, double* qv, double* kv, double*
 
         for (uint32_t i = 0; i < hd; ++i) acc[i] = 0.0;
         for (uint32_t t = 0; t <= p; ++t) {
-            const float* v_row = j->V + row0 + (uint64_t)t * kv_dim + (uint64_t)g * hd;
+            const float* v_row = j->V + key_offset(j, b, t) + (uint64_t)g * hd;
             for (uint32_t i = 0; i < hd; ++i) acc[i] += score[t] * (double)v_row[i];
         }
         for (uint32_t i = 0; i < hd; ++i) {
@@ -181,7 +208,11 @@ static void* batch_worker(void* arg) {
     batch_job* j = (batch_job*)arg;
     double* qv = (double*)malloc(sizeof(double) * j->hd);
     double* kv = (double*)malloc(sizeof(double) * j->hd);
-    double* score = (double*)malloc(sizeof(double) * j->slot_ctx);
+    /* a row attends over at most slot_ctx keys (slot mode) or the span of
+     * its block table (paged mode) */
+    const uint64_t max_keys =
+        j->block_tables ? (uint64_t)j->bt_stride * j->slot_ctx : (uint64_t)j->slot_ctx;
+    double* score = (double*)malloc(sizeof(double) * max_keys);
     double* acc = (double*)malloc(sizeof(double) * j->hd);
     if (!qv || !kv || !score || !acc) {
         j->skipped = -1;
@@ -210,6 +241,47 @@ int oracle_decode_batch(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
                                     n_threads);
 }
 
+static int run_batch(batch_job* proto, int n_threads);
+
+int oracle_decode_batch_paged(uint32_t n_blocks, uint32_t block_size, uint32_t n_head,
+                              uint32_t n_kv_head, uint32_t head_dim, uint32_t B,
+                              const float* q, const float* k_new, const float* v_new,
+                              const uint32_t* positions, const uint32_t* block_tables,
+                              uint32_t bt_stride, const float* q_norm_w,
+                              const float* k_norm_w, const float* inv_freq,
+                              const float* sinks, float eps, float scale, uint32_t flags,
+                              float* K, float* V, float* out, double* out64, int n_threads) {
+    if (B == 0) return 0;
+    if (!block_tables || bt_stride == 0 || block_size == 0) return -1;
+    batch_job proto;
+    memset(&proto, 0, sizeof(proto));
+    proto.n_slots = n_blocks;
+    proto.slot_ctx = block_size;
+    proto.n_head = n_head;
+    proto.n_kv_head = n_kv_head;
+    proto.hd = head_dim;
+    proto.B = B;
+    proto.q = q;
+    proto.k_new = k_new;
+    proto.v_new = v_new;
+    proto.positions = positions;
+    proto.slots = NULL;
+    proto.block_tables = block_tables;
+    proto.bt_stride = bt_stride;
+    proto.q_norm_w = q_norm_w;
+    proto.k_norm_w = k_norm_w;
+    proto.inv_freq = inv_freq;
+    proto.sinks = sinks;
+    proto.eps = eps;
+    proto.scale = scale;
+    proto.flags = flags;
+    proto.K = K;
+    proto.V = V;
+    proto.out = out;
+    proto.out64 = out64;
+    return run_batch(&proto, n_threads);
+}
+
 int oracle_decode_batch_opts(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_head,
                              uint32_t n_kv_head, uint32_t head_dim, uint32_t B,
                              const float* q, const float* k_new, const float* v_new,
@@ -219,10 +291,44 @@ int oracle_decode_batch_opts(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_hea
                              float scale, uint32_t flags, float* K, float* V, float* out,
                              double* out64, int n_threads) {
     if (B == 0) return 0;
-    if (!q || !k_new || !v_new || !positions || !slots || !q_norm_w || !k_norm_w ||
-        !inv_freq || !K || !V || !out)
+    if (!slots) return -1;
+    batch_job proto;
+    memset(&proto, 0, sizeof(proto));
+    proto.n_slots = n_slots;
+    proto.slot_ctx = slot_ctx;
+    proto.n_head = n_head;
+    proto.n_kv_head = n_kv_head;
+    proto.hd = head_dim;
+    proto.B = B;
+    proto.q = q;
+    proto.k_new = k_new;
+    proto.v_new = v_new;
+    proto.positions = positions;
+    proto.slots = slots;
+    proto.block_tables = NULL;
+    proto.q_norm_w = q_norm_w;
+    proto.k_norm_w = k_norm_w;
+    proto.inv_freq = inv_freq;
+    proto.sinks = sinks;
+    proto.eps = eps;
+    proto.scale = scale;
+    proto.flags = flags;
+    proto.K = K;
+    proto.V = V;
+    proto.out = out;
+    proto.out64 = out64;
+    return run_batch(&proto, n_threads);
+}
+
+/* Rows split over threads (rows touch disjoint slots or blocks). */
+static int run_batch(batch_job* proto, int n_threads) {
+    const uint32_t B = proto->B;
+    if (!proto->q || !proto->k_new || !proto->v_new || !proto->positions ||
+        !proto->q_norm_w || !proto->k_norm_w || !proto->inv_freq || !proto->K || !proto->V ||
+        !proto->out)
         return -1;
-    if (n_kv_head == 0 || n_head % n_kv_head != 0 || head_dim == 0 || head_dim % 2 != 0)
+    if (proto->n_kv_head == 0 || proto->n_head % proto->n_kv_head != 0 || proto->hd == 0 ||
+        proto->hd % 2 != 0)
         return -1;
     if (n_threads < 1) n_threads = 1;
     if ((uint32_t)n_threads > B) n_threads = (int)B;
@@ -239,31 +345,10 @@ int oracle_decode_batch_opts(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_hea
     }
     uint32_t per = (B + (uint32_t)n_threads - 1) / (uint32_t)n_threads;
     for (int t = 0; t < n_threads; ++t) {
-        batch_job* j = &jobs[t];
-        j->n_slots = n_slots;
-        j->slot_ctx = slot_ctx;
-        j->n_head = n_head;
-        j->n_kv_head = n_kv_head;
-        j->hd = head_dim;
-        j->B = B;
-        j->q = q;
-        j->k_new = k_new;
-        j->v_new = v_new;
-        j->positions = positions;
-        j->slots = slots;
-        j->q_norm_w = q_norm_w;
-        j->k_norm_w = k_norm_w;
-        j->inv_freq = inv_freq;
-        j->sinks = sinks;
-        j->eps = eps;
-        j->scale = scale;
-        j->flags = flags;
-        j->K = K;
-        j->V = V;
-        j->out = out;
-        j->out64 = out64;
-        j->row_begin = per * (uint32_t)t < B ? per * (uint32_t)t : B;
-        j->row_end = per * (uint32_t)(t + 1) < B ? per * (uint32_t)(t + 1) : B;
+        jobs[t] = *proto;
+        jobs[t].row_begin = per * (uint32_t)t < B ? per * (uint32_t)t : B;
+        jobs[t].row_end = per * (uint32_t)(t + 1) < B ? per * (uint32_t)(t + 1) : B;
+        jobs[t].skipped = 0;
     }
     for (int t = 1; t < n_threads; ++t)
         started[t] = pthread_create(&tids[t], NULL, batch_worker, &jobs[t]) == 0;

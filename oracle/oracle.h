@@ -59,6 +59,19 @@ int oracle_decode_batch_opts(uint32_t n_slots, uint32_t slot_ctx, uint32_t n_hea
                              float scale, uint32_t flags, float* K, float* V, float* out,
                              double* out64, int n_threads);
 
+/* The same step over a paged pool: K, V are f32[n_blocks][block_size][kv_dim];
+ * row b's key t is at block block_tables[b * bt_stride + t / block_size],
+ * offset t % block_size.  A row whose position is >= bt_stride * block_size
+ * or whose blocks 0..pos/block_size include an id >= n_blocks is skipped. */
+int oracle_decode_batch_paged(uint32_t n_blocks, uint32_t block_size, uint32_t n_head,
+                              uint32_t n_kv_head, uint32_t head_dim, uint32_t B,
+                              const float* q, const float* k_new, const float* v_new,
+                              const uint32_t* positions, const uint32_t* block_tables,
+                              uint32_t bt_stride, const float* q_norm_w,
+                              const float* k_norm_w, const float* inv_freq,
+                              const float* sinks, float eps, float scale, uint32_t flags,
+                              float* K, float* V, float* out, double* out64, int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

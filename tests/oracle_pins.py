@@ -543,4 +543,115 @@ def pin_brute_force_tiny(o):
             _close(out64[b, h], prob @ vals[:, h // g, :], 1e-12, f"brute b={b} h={h}")
 
 
+def _paged_from_slots(c, bs, rng, spare=3):
+    """Scatter the slot buffers of case ``c`` into a pool of blocks of ``bs``
+    positions under a random block permutation (plus ``spare`` unused blocks
+    filled with other data).  Returns (Kp, Vp, tables[n_slots][slot_ctx/bs])."""
+    per = c.slot_ctx // bs
+    n_blocks = c.n_slots * per + spare
+    perm = rng.permutation(n_blocks)[: c.n_slots * per]
+    tables = perm.reshape(c.n_slots, per).astype(np.uint32)
+    Kp = rng.standard_normal((n_blocks, bs, c.n_kv_head, c.hd)).astype(np.float32)
+    Vp = rng.standard_normal(Kp.shape).astype(np.float32)
+    for s in range(c.n_slots):
+        for i in range(per):
+            Kp[tables[s, i]] = c.K[s, i * bs:(i + 1) * bs]
+            Vp[tables[s, i]] = c.V[s, i * bs:(i + 1) * bs]
+    return Kp, Vp, tables
+
+
+def pin_paged_is_an_addressing_change(o):
+    """Paged KV (the Qwen3SsmLayer page, decode_multi_seq over per-sequence
+    block tables) changes where a key lives, not what is computed: scattering
+    each slot's rows into shuffled blocks and passing the matching tables gives
+    the slot step's output bit for bit, and the key/value write lands in block
+    table[pos // bs] at offset pos % bs."""
+    rng = np.random.default_rng(31)
+    bs = 4
+    c = Case(B=3, n_slots=3, slot_ctx=16, n_head=4, n_kv_head=2, hd=8)
+    c.positions = np.array([13, 2, 8], dtype=np.uint32)
+    c.slots = np.array([1, 2, 0], dtype=np.uint32)
+    Kp, Vp, tables = _paged_from_slots(c, bs, rng)
+    K, V = c.K.copy(), c.V.copy()
+    _, ref64, _ = c.run(o, K=K, V=V)
+    bt = tables[c.slots]
+    Kp0, Vp0 = Kp.copy(), Vp.copy()
+    _, got64, skipped = o.decode_batch_paged(
+        Kp, Vp, c.q, c.k_new, c.v_new, c.positions, bt, c.q_norm_w, c.k_norm_w,
+        c.inv_freq, None, c.eps, c.scale, want64=True)
+    assert skipped == 0
+    assert np.array_equal(got64, ref64)
+    written = np.zeros(Kp.shape[:2], dtype=bool)
+    for b in range(c.B):
+        p = int(c.positions[b])
+        blk, off = bt[b, p // bs], p % bs
+        written[blk, off] = True
+        assert np.array_equal(Kp[blk, off], K[c.slots[b], p])
+        assert np.array_equal(Vp[blk, off], c.v_new[b])
+    assert np.array_equal(Kp[~written], Kp0[~written])
+    assert np.array_equal(Vp[~written], Vp0[~written])
+
+
+def pin_paged_brute_force(o):
+    """Paged step on a tiny case against keys gathered one by one through the
+    table, softmax from scipy: every row reads only its own blocks."""
+    import scipy.special
+
+    rng = np.random.default_rng(32)
+    bs, nb, hd = 2, 9, 8
+    c = Case(B=2, n_slots=1, slot_ctx=2, n_head=2, n_kv_head=1, hd=hd)
+    Kp = rng.standard_normal((nb, bs, 1, hd)).astype(np.float32)
+    Vp = rng.standard_normal(Kp.shape).astype(np.float32)
+    bt = np.array([[7, 2, 5, 0], [3, 8, 1, 6]], dtype=np.uint32)
+    pos = np.array([6, 3], dtype=np.uint32)
+    K, V = Kp.copy(), Vp.copy()
+    _, out64, skipped = o.decode_batch_paged(
+        K, V, c.q, c.k_new, c.v_new, pos, bt, c.q_norm_w, c.k_norm_w, c.inv_freq, None,
+        c.eps, c.scale, want64=True)
+    assert skipped == 0
+    for b in range(2):
+        p = int(pos[b])
+        keys = np.stack([K[bt[b, t // bs], t % bs, 0] for t in range(p + 1)]).astype(np.float64)
+        vals = np.stack([V[bt[b, t // bs], t % bs, 0] for t in range(p + 1)]).astype(np.float64)
+        # the history rows come from the untouched pool, the last from the write
+        for t in range(p):
+            assert np.array_equal(keys[t], Kp[bt[b, t // bs], t % bs, 0])
+        assert np.array_equal(vals[p], c.v_new[b, 0])
+        for h in range(2):
+            qr = o.norm_rope_head(c.q[b, h], c.q_norm_w, c.eps, p, c.inv_freq)
+            prob = scipy.special.softmax(float(c.scale) * keys @ qr)
+            _close(out64[b, h], prob @ vals, 1e-12, f"paged brute b={b} h={h}")
+
+
+def pin_paged_out_of_range(o):
+    """A row is skipped (nothing written, output zero) when a block it uses
+    (blocks 0..pos // bs of its table) is not in the pool, or when pos is past
+    its table; ids in table entries beyond its last used block are never read."""
+    rng = np.random.default_rng(33)
+    bs, nb, hd = 4, 6, 8
+    c = Case(B=4, n_slots=1, slot_ctx=4, n_head=2, n_kv_head=1, hd=hd)
+    Kp = rng.standard_normal((nb, bs, 1, hd)).astype(np.float32)
+    Vp = rng.standard_normal(Kp.shape).astype(np.float32)
+    bad = np.uint32(nb)
+    bt = np.array([[0, 1, bad],       # pos 5 uses blocks 0, 1: fine, entry 2 unused
+                   [2, bad, 3],       # pos 6 uses block entry 1: skipped
+                   [4, 5, 3],         # pos 12 = 3 * bs, past the table: skipped
+                   [bad, 3, 3]],      # pos 0 uses entry 0: skipped
+                  dtype=np.uint32)
+    pos = np.array([5, 6, 12, 0], dtype=np.uint32)
+    c.q = rng.standard_normal((4, 2, hd)).astype(np.float32)
+    c.k_new = rng.standard_normal((4, 1, hd)).astype(np.float32)
+    c.v_new = rng.standard_normal((4, 1, hd)).astype(np.float32)
+    K, V = Kp.copy(), Vp.copy()
+    out, _, skipped = o.decode_batch_paged(
+        K, V, c.q, c.k_new, c.v_new, pos, bt, c.q_norm_w, c.k_norm_w, c.inv_freq, None,
+        c.eps, c.scale)
+    assert skipped == 3
+    assert np.any(out[0]) and not np.any(out[1:])
+    mask = np.ones(K.shape[:2], dtype=bool)
+    mask[1, 1] = False                # row 0's write: block 1, offset 1
+    assert np.array_equal(K[mask], Kp[mask]) and np.array_equal(V[mask], Vp[mask])
+    assert np.array_equal(V[1, 1], c.v_new[0])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

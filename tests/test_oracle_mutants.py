@@ -7,6 +7,8 @@ passes every pin would mean the pins leave that part of the oracle unchecked.
 """
 import os
 import shutil
+import subprocess
+import sys
 
 import pytest
 
@@ -32,7 +34,7 @@ MUTANTS = [
     ("range_excludes_pos",
      "t <= p;", "t < p;", True),
     ("values_read_from_k",
-     "const float* v_row = j->V + row0", "const float* v_row = j->K + row0", False),
+     "const float* v_row = j->V + key_offset", "const float* v_row = j->K + key_offset", False),
     ("gqa_interleaved_heads",
      "const uint32_t g = h / group;", "const uint32_t g = h % j->n_kv_head;", False),
     ("score_unscaled",
@@ -60,8 +62,22 @@ MUTANTS = [
     ("offset_missing_slot_ctx",
      "return ((uint64_t)slot * slot_ctx + pos)", "return ((uint64_t)slot + pos)", False),
     ("row_base_ignores_slot",
-     "const uint64_t row0 = (uint64_t)slot * j->slot_ctx * kv_dim;",
-     "const uint64_t row0 = 0;", False),
+     "return ((uint64_t)j->slots[b] * j->slot_ctx + t) * kv_dim;",
+     "return ((uint64_t)t) * kv_dim;", False),
+    ("paged_table_ignored",
+     "if (j->block_tables) {", "if (0) {", False),
+    ("paged_block_index_dropped",
+     "j->block_tables[(uint64_t)b * j->bt_stride + t / j->slot_ctx];",
+     "j->block_tables[(uint64_t)b * j->bt_stride];", False),
+    ("paged_block_and_offset_swapped",
+     "j->block_tables[(uint64_t)b * j->bt_stride + t / j->slot_ctx];",
+     "j->block_tables[(uint64_t)b * j->bt_stride + t % j->slot_ctx];", False),
+    ("paged_table_row_stride_dropped",
+     "j->block_tables[(uint64_t)b * j->bt_stride + t / j->slot_ctx];",
+     "j->block_tables[t / j->slot_ctx];", False),
+    ("paged_range_checks_first_block_only",
+     "for (uint32_t i = 0; i <= p / j->slot_ctx; ++i)",
+     "for (uint32_t i = 0; i < 1; ++i)", False),
     ("vnorm_with_weight",
      "rms_norm_gemma(v_in, NULL, hd,", "rms_norm_gemma(v_in, j->k_norm_w, hd,", False),
     ("vnorm_ignored",
@@ -73,6 +89,27 @@ MUTANTS = [
     ("max_taken_over_first_key_only",
      "if (score[t] > m) m = score[t];", "if (t == 0) m = score[t];", False),
 ]
+
+
+# Mutants of the paged addressing can index outside the pool (or, with the
+# table ignored, the absent slot array): their pins run in a child process, and
+# a crash there counts as caught.
+ISOLATED = {"paged_table_ignored", "paged_block_and_offset_swapped",
+            "paged_table_row_stride_dropped", "paged_range_checks_first_block_only",
+            "paged_block_index_dropped"}
+
+_CHILD = """
+import sys
+import oracle, oracle_pins
+lib = oracle.Oracle(sys.argv[1])
+caught = 0
+for pin in oracle_pins.ALL_PINS:
+    try:
+        pin(lib)
+    except Exception:
+        caught += 1
+sys.exit(3 if caught else 0)
+"""
 
 
 def _mutant_lib(tmp_path, name, old, new, every):
@@ -91,7 +128,17 @@ def _mutant_lib(tmp_path, name, old, new, every):
 
 @pytest.mark.parametrize("name,old,new,every", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, name, old, new, every):
-    lib = oracle.Oracle(_mutant_lib(tmp_path, name, old, new, every))
+    path = _mutant_lib(tmp_path, name, old, new, every)
+    if name in ISOLATED:
+        here = os.path.dirname(os.path.abspath(__file__))
+        env = dict(os.environ)
+        env["PYTHONPATH"] = os.pathsep.join([here, os.path.dirname(here),
+                                             env.get("PYTHONPATH", "")])
+        r = subprocess.run([sys.executable, "-c", _CHILD, path], cwd=here, env=env,
+                           capture_output=True, timeout=600)
+        assert r.returncode != 0, f"mutant {name} passed every pin"
+        return
+    lib = oracle.Oracle(path)
     caught = []
     for pin in oracle_pins.ALL_PINS:
         try:
