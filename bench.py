@@ -262,14 +262,34 @@ def run_gpu(args, w):
         K = torch.empty(shape, dtype=torch.float32, device=dev)
         V = torch.empty(shape, dtype=torch.float32, device=dev)
     w.dev_fill_history(K.data_ptr(), V.data_ptr(), sp)
-    kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head,
-                    k_buf=K, v_buf=V)
-    if args.split:
-        kv.set_split(*args.split)
 
     def dev_t(a, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(a))
         return (t.to(dtype) if dtype is not None else t).to(dev)
+
+    bs = args.paged
+    if bs:
+        # paged layout: the same history cut into blocks of bs positions,
+        # shuffled over a pool; each row reads its blocks through its table
+        pshape = (w.n_slots * (w.slot_ctx // bs), bs, w.n_kv_head, w.head_dim)
+        perm = dev_t(w.block_perm(bs).astype(np.int64))
+        torch.cuda.synchronize(dev)
+        pools = []
+        for src in (K, V):
+            dst = torch.empty(pshape, dtype=torch.float32, device=dev)
+            dst[perm] = src.view(pshape)
+            pools.append(dst)
+        torch.cuda.synchronize(dev)
+        del K, V
+        K, V = pools
+        tables_np = w.block_tables(bs).astype(np.int32)
+        tables = dev_t(tables_np)
+        kv = skv.SlotKV(pshape[0], bs, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
+    else:
+        kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head,
+                        k_buf=K, v_buf=V)
+    if args.split:
+        kv.set_split(*args.split)
 
     qw, kw, inv = dev_t(w.q_norm_w()), dev_t(w.k_norm_w()), dev_t(w.inv_freq())
     sinks = None if not w.sinks else dev_t(w.sink_logits())
@@ -281,13 +301,23 @@ def run_gpu(args, w):
     vn = [dev_t(w.v_new(t)) for t in range(nsub)]
     pos = [dev_t(w.positions(t).astype(np.int32)) for t in range(nsub)]
     out = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32, device=dev)
-    bytes_per_launch = [w.alg_bytes(w.positions(t)) for t in range(nsub)]
+    # paged mode also reads each used table entry once
+    bytes_per_launch = [w.alg_bytes(w.positions(t)) +
+                        (int((w.positions(t).astype(np.int64) // bs + 1).sum()) * 4 if bs else 0)
+                        for t in range(nsub)]
     torch.cuda.synchronize(dev)
+
+    def decode(t):
+        if bs:
+            kv.decode_batch_attn_paged(q[t], kn[t], vn[t], pos[t], tables, qw, kw, inv, sinks,
+                                       out, w.eps, w.scale, stream=sp)
+        else:
+            kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
+                                 w.eps, w.scale, stream=sp)
 
     def one_step():
         for t in range(nsub):
-            kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
-                                 w.eps, w.scale, stream=sp)
+            decode(t)
 
     for _ in range(args.warmup):
         one_step()
@@ -330,8 +360,7 @@ def run_gpu(args, w):
             continue
         for t in range(nsub):
             ev[i][0].record(stream)
-            kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
-                                 w.eps, w.scale, stream=sp)
+            decode(t)
             ev[i][1].record(stream)
             i += 1
     end.record(stream)
@@ -351,13 +380,26 @@ def run_gpu(args, w):
     hk = [pin(w.k_new(t)) for t in range(nsub)]
     hv = [pin(w.v_new(t)) for t in range(nsub)]
     hp = [pin(w.positions(t).astype(np.int32)) for t in range(nsub)]
-    hs = pin(slots_np)
+    hs = pin(tables_np if bs else slots_np)
     hout = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32).pin_memory()
+    if bs:
+        dq, dk, dv = torch.empty_like(q[0]), torch.empty_like(kn[0]), torch.empty_like(vn[0])
+        dp, dt = torch.empty_like(pos[0]), torch.empty_like(tables)
 
     def e2e_step():
         for t in range(nsub):
-            kv.decode_batch_attn_host(hq[t], hk[t], hv[t], hp[t], hs, qw, kw, inv, sinks, hout,
-                                      w.eps, w.scale, stream=sp)
+            if not bs:
+                kv.decode_batch_attn_host(hq[t], hk[t], hv[t], hp[t], hs, qw, kw, inv, sinks,
+                                          hout, w.eps, w.scale, stream=sp)
+                continue
+            # no host entry for the paged step: the same copies around the call
+            with torch.cuda.stream(stream):
+                for d_, h_ in ((dq, hq[t]), (dk, hk[t]), (dv, hv[t]), (dp, hp[t]), (dt, hs)):
+                    d_.copy_(h_, non_blocking=True)
+                kv.decode_batch_attn_paged(dq, dk, dv, dp, dt, qw, kw, inv, sinks, out, w.eps,
+                                           w.scale, stream=sp)
+                hout.copy_(out, non_blocking=True)
+            stream.synchronize()
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -382,11 +424,13 @@ def run_gpu(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(w),
+        "config": dict(config_of(w), **({"kv_layout": "paged", "block_size": bs,
+                                          "block_order": "seeded shuffle over the pool"}
+                                         if bs else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": args.traffic if args.traffic is not None
-                     else measured_traffic(w.name),
+                     else (None if bs else measured_traffic(w.name)),
                      "alg_bytes_per_launch": alg_bytes,
                      "avg_launch_us": avg_launch_s * 1e6,
                      "kernel": "slotkv_decode_attn_kernel"},
@@ -483,6 +527,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="time batched causal prefill instead of the decode step")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
+                    help="run the workload over a shuffled paged pool of this block size")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--traffic", type=float, default=None,

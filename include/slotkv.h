@@ -186,6 +186,44 @@ int prefill_batch_attn(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const f
                        float scale, slotkv_stream_t stream);
 
 /*
+ * decode_batch_attn_paged -- the decode step over a paged KV pool: instead of
+ * one contiguous slot per sequence, each row's keys live in fixed-size blocks
+ * named by its block table (the paged cache with per-sequence block tables of
+ * the Qwen3SsmLayer page, decode_multi_seq; the same step as "Forward Cuda
+ * Gemma", decodeBatch, with only the addressing changed).
+ *
+ * The handle's buffers are the pool: allocate it with n_slots = the number of
+ * blocks and slot_ctx = the block size, so K and V are
+ * f32[n_blocks][block_size][n_kv_head][head_dim].  The block size must be a
+ * multiple of 4096/head_dim (64 for head_dim 64, 32 for 128, 16 for 256), the
+ * keys of one pipeline tile, else SLOTKV_ERR_UNSUPPORTED.
+ *
+ *   block_tables  device u32[B][bt_stride]: row b's key t (0 <= t <= pos) is at
+ *                 block block_tables[b*bt_stride + t/block_size], offset
+ *                 t % block_size.  Entries past a row's last used block are
+ *                 never read.  Rows may share blocks they only read, but the
+ *                 block holding a row's key pos must belong to that row alone
+ *                 in this call, and appear once in its table.
+ *   bt_stride     entries per row of block_tables (>= 1): the longest context
+ *                 is bt_stride*block_size keys.
+ * The other arguments are those of decode_batch_attn (slots is replaced by
+ * the tables).  The step writes key pos's K' and V into its block, then
+ * attends keys 0..pos through the table.  Per row the result equals
+ * decode_batch_attn on a slot holding the same keys, bit for bit.  A row whose
+ * pos >= bt_stride*block_size, or whose used entries (blocks 0..pos/block_size)
+ * hold an id >= n_blocks, is skipped: nothing of it is written and
+ * SLOTKV_DEV_RANGE is raised.  The options of slot_kv_set_options apply.
+ * Errors as decode_batch_attn.
+ */
+int decode_batch_attn_paged(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
+                            const float* k_new, const float* v_new,
+                            const uint32_t* positions, const uint32_t* block_tables,
+                            uint32_t bt_stride, const float* q_norm_w,
+                            const float* k_norm_w, const float* inv_freq,
+                            const float* sinks, float* out, float eps, float scale,
+                            slotkv_stream_t stream);
+
+/*
  * decode_batch_attn_host -- decode_batch_attn for callers whose per-step
  * inputs and output live in host memory.  q, k_new, v_new, positions, slots
  * and out are HOST pointers with the layouts above (pinned memory gives

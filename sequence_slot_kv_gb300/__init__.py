@@ -17,7 +17,7 @@ import os
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn", "slot_kv_get_status",
-    "slot_kv_set_split", "slot_kv_advance_positions", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
+    "slot_kv_set_split", "slot_kv_advance_positions", "decode_batch_attn_paged", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libslotkv.so")
@@ -42,6 +42,8 @@ EXPORTS = {
     "decode_batch_attn": (_DECODE_ARGS, _int),
     "decode_batch_attn_host": (_DECODE_ARGS, _int),
     "prefill_batch_attn": (_DECODE_ARGS, _int),
+    "decode_batch_attn_paged": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp, _vp,
+                                 _vp, _vp, _f32, _f32, _vp], _int),
     "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
     "slot_kv_set_split": ([_vp, _u32, _u32], _int),
     "slot_kv_advance_positions": ([_vp, _u32, _u32, _vp], _int),
@@ -198,6 +200,25 @@ class SlotKV:
             eps, scale, _stream_ptr(stream)), "prefill_batch_attn")
         return out
 
+    def decode_batch_attn_paged(self, q, k_new, v_new, positions, block_tables, q_norm_w,
+                                k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
+        """Decode over a paged pool (this handle's buffers as blocks of
+        slot_ctx positions): block_tables is int32 [B][max_blocks], row b's
+        key t in block block_tables[b][t // slot_ctx]."""
+        import torch
+        B, n_head = int(q.shape[0]), int(q.shape[1])
+        f, u = torch.float32, torch.int32
+        if block_tables.dim() != 2 or int(block_tables.shape[0]) != B:
+            raise ValueError("block_tables must be [B][max_blocks]")
+        _check(_lib.decode_batch_attn_paged(
+            self._h, B, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
+            _ptr(v_new, f, "v_new"), _ptr(positions, u, "positions"),
+            _ptr(block_tables, u, "block_tables"), int(block_tables.shape[1]),
+            _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"), _ptr(out, f, "out"),
+            eps, scale, _stream_ptr(stream)), "decode_batch_attn_paged")
+        return out
+
     def decode_batch_attn_host(self, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
         """As decode_batch_attn, with q/k_new/v_new/positions/slots/out in host
@@ -270,6 +291,12 @@ def prefill_batch_attn(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                        sinks, out, eps, scale, stream=None):
     return h.prefill_batch_attn(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                                 inv_freq, sinks, out, eps, scale, stream)
+
+
+def decode_batch_attn_paged(h, q, k_new, v_new, positions, block_tables, q_norm_w, k_norm_w,
+                            inv_freq, sinks, out, eps, scale, stream=None):
+    return h.decode_batch_attn_paged(q, k_new, v_new, positions, block_tables, q_norm_w,
+                                     k_norm_w, inv_freq, sinks, out, eps, scale, stream)
 
 
 def decode_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,

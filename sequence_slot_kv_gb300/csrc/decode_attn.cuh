@@ -26,11 +26,18 @@
 //         rescales only when its running max grows;
 //       - the split holding key p adds that key from shared memory (its K is
 //         the freshly normed+rotated k', its V the raw v_new) and writes both
-//         rows into the slot buffers at (slot*slot_ctx + p)*kv_dim;
+//         rows into the slot buffers at (slot*slot_ctx + p)*kv_dim (in
+//         paged mode, into key p's block);
 //       - the groups' (m, l, acc) merge by shuffles within each warp, then
 //         across the four warps in shared memory; a one-split row writes out,
 //         otherwise the partial goes to the workspace and the last CTA of the
 //         (row, kv head) to finish merges the splits in split order.
+//
+// Paged mode (DecodeParams::block_tables set): the buffers are a pool of
+// blocks and row b's key t sits in block block_tables[b][t / block_size].
+// Block sizes are multiples of T and tile starts are multiples of T, so each
+// tile lies inside one block: the producer only swaps the tile's first row
+// (looked up one tile ahead), and the plan checks every used table entry.
 //
 // Every wait on an mbarrier is bounded; on expiry the CTA raises
 // SLOTKV_DEV_TIMEOUT, drains its own copies in flight (bounded) and returns.
@@ -128,8 +135,9 @@ struct KCfg {
 };
 
 // What the producer tells the other warps about an item.
+// prow: row of key p in the [rows][kv_dim] view of the K and V buffers.
 struct ItemDesc {
-    uint32_t b, kvh, split, nsplit, p, slot, k0, hist_end, ntiles, is_last, end, pad;
+    uint32_t b, kvh, split, nsplit, p, prow, k0, hist_end, ntiles, is_last, end, pad;
 };
 
 // A finished multi-split partial handed to the merge warp.
@@ -559,30 +567,65 @@ __device__ __forceinline__ void warp_rms_norm_plain(const float* src, float* dst
 
 // ------------------------------------------------------------------ plan
 // One CTA.  Lists every valid (row, split, kv head) as a 16-byte record
-// (packed item, position, slot), largest first: items are binned by their
-// tile count and the bins laid out in descending order, so the small ragged
-// last splits come last and fill the end of the kernel (the order of work
-// never changes a result; only the split sizes could, and they depend on
+// (packed item, position, row of key p), largest first: items are binned by
+// their tile count and the bins laid out in descending order, so the small
+// ragged last splits come last and fill the end of the kernel (the order of
+// work never changes a result; only the split sizes could, and they depend on
 // the row alone).  Raises SLOTKV_DEV_RANGE for rows whose slot or position
-// is out of range (they get no items) and resets the hand-out counter.
+// is out of range -- in paged mode, whose position is past its table or any
+// of whose blocks 0..p/block_size is not in the pool -- (they get no items)
+// and resets the hand-out counter.
 constexpr int kPlanBins = 64;
+constexpr int kPlanMaxRows = 65536;
 
 template <int T>
 __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const DecodeParams P) {
     __shared__ uint32_t bin_count[kPlanBins];
     __shared__ uint32_t bin_cursor[kPlanBins];
     __shared__ uint32_t total;
+    __shared__ uint32_t row_bad[kPlanMaxRows / 32];  // paged mode: rows failing the check
     grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t nkv = P.n_kv_head;
+    const bool paged = P.block_tables != nullptr;
     for (int i = tid; i < kPlanBins; i += kPlanThreads) bin_count[i] = 0;
+    if (paged) {
+        for (uint32_t i = tid; i < (P.B + 31) / 32; i += kPlanThreads) row_bad[i] = 0;
+        __syncthreads();
+        // pass 0 (paged): one warp per row checks the row's used table entries,
+        // four loads in flight per lane
+        for (uint32_t b = warp; b < P.B; b += kPlanThreads / 32) {
+            const uint32_t p = P.positions[b];
+            bool bad = static_cast<uint64_t>(p) >=
+                       static_cast<uint64_t>(P.bt_stride) * P.slot_ctx;
+            if (!bad) {
+                const uint32_t* tab = P.block_tables + static_cast<size_t>(b) * P.bt_stride;
+                const uint32_t used = p / P.slot_ctx + 1;
+                for (uint32_t i0 = 0; i0 < used; i0 += 128) {
+                    uint32_t id[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t i = i0 + u * 32 + lane;
+                        id[u] = i < used ? __ldg(tab + i) : 0u;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) bad |= id[u] >= P.n_slots;
+                }
+            }
+            bad = __any_sync(0xffffffffu, bad);
+            if (bad && lane == 0) atomicOr(&row_bad[b >> 5], 1u << (b & 31));
+        }
+    }
     __syncthreads();
     // a row's split count and the tile counts of its full and last splits
-    auto row_shape = [&](uint32_t b, uint32_t& p, uint32_t& slot, uint32_t& nsplit,
-                         uint32_t& full_tiles, uint32_t& last_tiles) {
+    auto row_shape = [&](uint32_t b, uint32_t& p, uint32_t& nsplit, uint32_t& full_tiles,
+                         uint32_t& last_tiles) {
         p = P.positions[b];
-        slot = P.slots[b];
-        if (slot >= P.n_slots || p >= P.slot_ctx) return false;
+        if (paged) {
+            if (row_bad[b >> 5] & (1u << (b & 31))) return false;
+        } else if (P.slots[b] >= P.n_slots || p >= P.slot_ctx) {
+            return false;
+        }
         const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
         nsplit = (p + 1 + chunk - 1) / chunk;
         full_tiles = chunk / T;
@@ -592,8 +635,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     auto bin_of = [](uint32_t tiles) { return tiles < kPlanBins ? tiles : kPlanBins - 1u; };
     // pass 1: histogram of item sizes
     for (uint32_t b = tid; b < P.B; b += kPlanThreads) {
-        uint32_t p, slot, nsplit, ft, lt;
-        if (!row_shape(b, p, slot, nsplit, ft, lt)) {
+        uint32_t p, nsplit, ft, lt;
+        if (!row_shape(b, p, nsplit, ft, lt)) {
             atomicOr(P.status, kDevRange);
             continue;
         }
@@ -613,11 +656,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     // pass 2: one warp per row reserves the row's ranges and writes them
     uint4* recs = reinterpret_cast<uint4*>(P.items);
     for (uint32_t b = warp; b < P.B; b += kPlanThreads / 32) {
-        uint32_t p = 0, slot = 0, nsplit = 0, ft = 0, lt = 0, full_base = 0, last_base = 0;
+        uint32_t p = 0, prow = 0, nsplit = 0, ft = 0, lt = 0, full_base = 0, last_base = 0;
         bool ok = false;
         if (lane == 0) {
-            ok = row_shape(b, p, slot, nsplit, ft, lt);
+            ok = row_shape(b, p, nsplit, ft, lt);
             if (ok) {
+                // the row of key p in the [rows][kv_dim] view of K and V
+                if (paged)
+                    prow = __ldg(P.block_tables + static_cast<size_t>(b) * P.bt_stride +
+                                 p / P.slot_ctx) * P.slot_ctx + p % P.slot_ctx;
+                else
+                    prow = P.slots[b] * P.slot_ctx + p;
                 if (nsplit > 1) full_base = atomicAdd(&bin_cursor[bin_of(ft)], (nsplit - 1) * nkv);
                 last_base = atomicAdd(&bin_cursor[bin_of(lt)], nkv);
             }
@@ -625,15 +674,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) continue;
         p = __shfl_sync(0xffffffffu, p, 0);
-        slot = __shfl_sync(0xffffffffu, slot, 0);
+        prow = __shfl_sync(0xffffffffu, prow, 0);
         nsplit = __shfl_sync(0xffffffffu, nsplit, 0);
         full_base = __shfl_sync(0xffffffffu, full_base, 0);
         last_base = __shfl_sync(0xffffffffu, last_base, 0);
         const uint32_t nfull = (nsplit - 1) * nkv;
         for (uint32_t i = lane; i < nfull; i += 32)
-            recs[full_base + i] = make_uint4(pack_item(b, i / nkv, i % nkv), p, slot, 0u);
+            recs[full_base + i] = make_uint4(pack_item(b, i / nkv, i % nkv), p, prow, 0u);
         for (uint32_t i = lane; i < nkv; i += 32)
-            recs[last_base + i] = make_uint4(pack_item(b, nsplit - 1, i), p, slot, 0u);
+            recs[last_base + i] = make_uint4(pack_item(b, nsplit - 1, i), p, prow, 0u);
     }
     __syncthreads();
     if (tid == 0) {
@@ -720,8 +769,11 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             const uint4* recs = reinterpret_cast<const uint4*>(P.items);
             // stage item k from record `rec` (or the end marker); returns the
             // item's tile stream: kv head, first tensor row, tile count
+            const bool paged = P.block_tables != nullptr;
+            // stage item k from record `rec` (or the end marker); in paged mode
+            // row_o is the item's first key and blk_o the block holding it
             auto stage = [&](uint32_t k, bool valid, uint4 rec, uint32_t& kvh_o, int& row_o,
-                             uint32_t& ntiles_o) {
+                             uint32_t& ntiles_o, const uint32_t*& tab_o, uint32_t& blk_o) {
                 const uint32_t is = k & 1;
                 volatile ItemDesc* d = desc + is;
                 const uint32_t staged = staged0 + 8 * is;
@@ -731,7 +783,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     return false;
                 }
                 const uint32_t b = rec.x >> 16, split = (rec.x >> 8) & 255u, kvh = rec.x & 255u;
-                const uint32_t p = rec.y, slot = rec.z;
+                const uint32_t p = rec.y, prow = rec.z;
                 const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
                 const uint32_t nsplit = (p + 1 + chunk - 1) / chunk;
                 const uint32_t k0 = split * chunk;
@@ -746,7 +798,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 d->split = split;
                 d->nsplit = nsplit;
                 d->p = p;
-                d->slot = slot;
+                d->prow = prow;
                 d->k0 = k0;
                 d->hist_end = hist_end;
                 d->ntiles = ntiles;
@@ -763,15 +815,26 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 }
                 misc[3] = static_cast<int>(k + 1);
                 kvh_o = kvh;
-                row_o = static_cast<int>(slot * P.slot_ctx + k0);
                 ntiles_o = ntiles;
+                if (paged) {
+                    // the first block id is used only when the item's tiles
+                    // start, so its load completes while earlier tiles stream
+                    tab_o = P.block_tables + static_cast<size_t>(b) * P.bt_stride;
+                    row_o = static_cast<int>(k0);
+                    if (ntiles) blk_o = __ldg(tab_o + k0 / P.slot_ctx);
+                } else {
+                    row_o = static_cast<int>(prow - p + k0);
+                }
                 return true;
             };
             uint32_t it = atomicAdd(P.plan + 1, 1u);
             uint4 rec = it < n_items ? __ldcg(recs + it) : make_uint4(0, 0, 0, 0);
             uint32_t cur_kvh = 0, cur_nt = 0, nxt_kvh = 0, nxt_nt = 0;
             int cur_row = 0, nxt_row = 0;
-            bool cur_ok = stage(0, it < n_items, rec, cur_kvh, cur_row, cur_nt);
+            const uint32_t* cur_tab = nullptr;
+            const uint32_t* nxt_tab = nullptr;
+            uint32_t cur_blk = 0, nxt_blk = 0;
+            bool cur_ok = stage(0, it < n_items, rec, cur_kvh, cur_row, cur_nt, cur_tab, cur_blk);
             // the record of the item after the staged one, claimed early
             uint32_t it_n = cur_ok ? atomicAdd(P.plan + 1, 1u) : n_items;
             uint4 rec_n = make_uint4(0, 0, 0, 0);
@@ -793,17 +856,24 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     if (misc[0]) break;
                     const uint32_t full = full0 + 8 * st;
                     const uint32_t dst = smem_addr(smem + st * C::STAGE_BYTES);
+                    // the tile's first row: contiguous in a slot; in paged mode
+                    // the tile lies inside one block (block size and tile starts
+                    // are multiples of T), whose id was loaded one tile ahead
+                    const uint32_t key = static_cast<uint32_t>(cur_row) + t * T;
+                    const int trow = paged ? static_cast<int>(cur_blk * P.slot_ctx + key % P.slot_ctx)
+                                           : cur_row + static_cast<int>(t * T);
+                    if (paged && t + 1 < cur_nt) cur_blk = __ldg(cur_tab + (key + T) / P.slot_ctx);
                     mbar_expect_tx(full, C::STAGE_BYTES);
-                    tma_load_2d(dst, &tmK, static_cast<int>(cur_kvh * HD),
-                                cur_row + static_cast<int>(t * T), full);
-                    tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(cur_kvh * HD),
-                                cur_row + static_cast<int>(t * T), full);
+                    tma_load_2d(dst, &tmK, static_cast<int>(cur_kvh * HD), trow, full);
+                    tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(cur_kvh * HD), trow,
+                                full);
                     misc[2] = static_cast<int>(tile_g + 1);
                     if (!rec_n_loaded) {
                         if (it_n < n_items) rec_n = __ldcg(recs + it_n);
                         rec_n_loaded = true;
                     } else if (!nxt_staged && (k == 0 || mbar_test(nfree, nparity))) {
-                        nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt);
+                        nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt,
+                                       nxt_tab, nxt_blk);
                         nxt_staged = true;
                     }
                 }
@@ -815,7 +885,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                         misc[0] = 1;
                         break;
                     }
-                    nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt);
+                    nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt,
+                                   nxt_tab, nxt_blk);
                 }
                 if (nxt_ok) it_n = atomicAdd(P.plan + 1, 1u);
                 rec_n_loaded = false;
@@ -823,6 +894,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 cur_kvh = nxt_kvh;
                 cur_row = nxt_row;
                 cur_nt = nxt_nt;
+                cur_tab = nxt_tab;
+                cur_blk = nxt_blk;
             }
         }
         // ------------------------------------------------------------ prep
@@ -1013,7 +1086,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             break;
         }
         const uint32_t b = desc[is].b, kvh = desc[is].kvh, split = desc[is].split;
-        const uint32_t nsplit = desc[is].nsplit, p = desc[is].p, slot = desc[is].slot;
+        const uint32_t nsplit = desc[is].nsplit, p = desc[is].p, prow = desc[is].prow;
         const uint32_t k0 = desc[is].k0, hist_end = desc[is].hist_end;
         const uint32_t ntiles = desc[is].ntiles;
         const bool is_last = desc[is].is_last != 0;
@@ -1083,8 +1156,9 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             const int row1[1] = {0};
             const bool valid1[1] = {gid == 0};
             attend_rows<HD, G, E, L, 1>(ks, vs, row1, valid1, li, q, m, l, acc);
-            // key p's K and V rows go into the slot at (slot*slot_ctx + p)
-            const size_t at = (static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh;
+            // key p's K and V rows go to row prow: (slot*slot_ctx + p) in a slot,
+            // (block*block_size + p % block_size) in paged mode
+            const size_t at = static_cast<size_t>(prow) * P.n_kv_head + kvh;
             float4* kd = reinterpret_cast<float4*>(P.K + at * HD);
             float4* vd = reinterpret_cast<float4*>(P.V + at * HD);
             for (int i = lane; i < HD / 4; i += 32) {

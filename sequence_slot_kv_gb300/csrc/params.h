@@ -24,7 +24,7 @@ struct DecodeParams {
     float* ws_acc;           // split partials acc:    [rows][n_head][max_splits][hd]
     uint32_t* counters;      // finished-split counters: [rows][n_kv_head]
     uint32_t* items;         // work list: [rows * n_kv_head * max_splits][4] records
-                             // (packed item, position, slot, 0)
+                             // (packed item, position, tensor row of key p, 0)
     uint32_t* plan;          // [0] items in the list, [1] next item to hand out
     uint32_t* status;        // sticky SLOTKV_DEV_* flags
     uint32_t n_slots, slot_ctx, n_head, n_kv_head, B;
@@ -34,6 +34,12 @@ struct DecodeParams {
     float scale_log2;        // softmax scale * log2(e): scores live in base 2
     uint32_t flags;          // SLOTKV_OPT_* norm options
     uint32_t prefill;        // 1: rows are prefill tokens (keys all read from the slot)
+    // Paged mode (block_tables non-null): K and V are a pool of n_slots blocks
+    // of slot_ctx positions and row b's key t lives in block
+    // block_tables[b * bt_stride + t / slot_ctx] at offset t % slot_ctx;
+    // slot_ctx is then a multiple of the tile height.  slots is unused.
+    const uint32_t* block_tables = nullptr;
+    uint32_t bt_stride = 0;
 };
 
 // Keys per split chunk for a row with n_keys keys (p + 1).  Depends only on

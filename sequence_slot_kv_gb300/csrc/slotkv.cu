@@ -155,8 +155,8 @@ bool valid_handle(slotkv_t h) { return h && h->K && h->V && h->status; }
 
 // The most splits any row of this slot_ctx can need: nsplit(n) <= ceil(n /
 // chunk_min) because chunks are >= chunk_min keys, and <= max_splits.
-uint32_t grid_splits(const slotkv_s* h) {
-    const uint64_t bound = ((uint64_t)h->slot_ctx + h->chunk_min - 1) / h->chunk_min;
+uint32_t grid_splits(const slotkv_s* h, uint64_t max_keys) {
+    const uint64_t bound = (max_keys + h->chunk_min - 1) / h->chunk_min;
     return (uint32_t)(bound < h->max_splits ? bound : h->max_splits);
 }
 
@@ -164,9 +164,12 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
            const float* v_new, const uint32_t* positions, const uint32_t* slots,
            const float* q_norm_w, const float* k_norm_w, const float* inv_freq,
            const float* sinks, float* out, float eps, float scale, cudaStream_t stream,
-           bool prefill = false) {
+           bool prefill = false, const uint32_t* block_tables = nullptr,
+           uint32_t bt_stride = 0) {
     DecodeParams P;
     P.prefill = prefill ? 1u : 0u;
+    P.block_tables = block_tables;
+    P.bt_stride = bt_stride;
     P.q = q;
     P.k_new = k_new;
     P.v_new = v_new;
@@ -197,7 +200,8 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.flags = h->options;
     const int G = (int)(n_head / h->n_kv_head);
     // persistent CTAs: two per SM, never more than there can be work items
-    const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h);
+    const uint64_t max_keys = block_tables ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
+    const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h, max_keys);
     const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
     const unsigned ctas = (unsigned)(most < want ? most : want);
     int rc;
@@ -407,6 +411,27 @@ int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float*
     if (rc != SLOTKV_OK || n_tok == 0) return rc;
     return launch(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                   inv_freq, sinks, out, eps, scale, (cudaStream_t)stream, true);
+}
+
+int decode_batch_attn_paged(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
+                            const float* k_new, const float* v_new, const uint32_t* positions,
+                            const uint32_t* block_tables, uint32_t bt_stride,
+                            const float* q_norm_w, const float* k_norm_w,
+                            const float* inv_freq, const float* sinks, float* out, float eps,
+                            float scale, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, block_tables,
+                               q_norm_w, k_norm_w, inv_freq, out);
+    if (rc != SLOTKV_OK) return rc;
+    const uint32_t T = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+    if (h->slot_ctx % T != 0)
+        return fail(SLOTKV_ERR_UNSUPPORTED, "block size %u is not a multiple of %u keys",
+                    h->slot_ctx, T);
+    if (bt_stride == 0) return fail(SLOTKV_ERR_ARG, "bt_stride must be >= 1");
+    if (B == 0) return SLOTKV_OK;
+    return launch(h, B, n_head, q, k_new, v_new, positions, nullptr, q_norm_w, k_norm_w,
+                  inv_freq, sinks, out, eps, scale, (cudaStream_t)stream, false, block_tables,
+                  bt_stride);
 }
 
 int decode_batch_attn_host(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,

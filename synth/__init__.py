@@ -20,6 +20,7 @@ from . import build as _build
 
 S_HIST_K, S_HIST_V, S_Q, S_KNEW, S_VNEW = 1, 2, 3, 4, 5
 S_QNORM_W, S_KNORM_W, S_SINKS, S_POS, S_SLOTS = 6, 7, 8, 9, 10
+S_BLOCKS = 11
 STEP_STRIDE = 16
 
 _host = None
@@ -220,6 +221,22 @@ class Workload:
                 n = min(chunk, total - off)
                 dev_fill_normal(ptr + 4 * off, n, self.seed, which, off, cuda_stream)
                 off += n
+
+    # --- paged layout ------------------------------------------------------
+    # The paged pool of a workload is its slot buffers cut into blocks of
+    # ``block_size`` positions and shuffled: slot s's i-th block goes to pool
+    # block perm[s * per + i] (per = slot_ctx / block_size), and a row's table
+    # lists the pool blocks of its slot in order.
+    def block_perm(self, block_size):
+        assert self.slot_ctx % block_size == 0
+        n_blocks = self.n_slots * (self.slot_ctx // block_size)
+        return subset(n_blocks, n_blocks, self.seed, S_BLOCKS)
+
+    def block_tables(self, block_size):
+        """u32[B][slot_ctx / block_size]: row b's pool blocks, in key order."""
+        per = self.slot_ctx // block_size
+        perm = self.block_perm(block_size).reshape(self.n_slots, per)
+        return perm[self.slots()].copy()
 
     def alg_bytes(self, positions):
         """Algorithmic HBM bytes of one decode step at ``positions``: history
