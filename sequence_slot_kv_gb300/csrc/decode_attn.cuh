@@ -39,6 +39,12 @@
 // tile lies inside one block: the producer only swaps the tile's first row
 // (looked up one tile ahead), and the plan checks every used table entry.
 //
+// Paged mode (DecodeParams::block_tables set): the buffers are a pool of
+// blocks and row b's key t sits in block block_tables[b][t / block_size].
+// Block sizes are multiples of T and tile starts are multiples of T, so each
+// tile lies inside one block: the producer only swaps the tile's first row
+// (looked up one tile ahead), and the plan checks every used table entry.
+//
 // Every wait on an mbarrier is bounded; on expiry the CTA raises
 // SLOTKV_DEV_TIMEOUT, drains its own copies in flight (bounded) and returns.
 #pragma once
@@ -260,6 +266,42 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // tile Vt, hd floats each).  Lane `li` of its L-lane group owns elements
 // c*4L + 4*li + {0..3}, c < E/4, of every vector.  All 32 lanes of the warp
 // must call this together (the reductions shuffle across the whole warp).
+// Packed f32x2 helpers (one instruction for two lanes of arithmetic, each
+// element rounded exactly as the scalar operation would be).
+//   dot_e: <q, k> over E elements as two interleaved partial sums (even and
+//          odd elements), added at the end;
+//   axpy_e: acc[e] += p * v[e] for every e;
+//   scale_e: acc[e] *= c for every e.
+template <int E>
+__device__ __forceinline__ float dot_e(const float (&q)[E], const float (&k)[E]) {
+    float2 d = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i)
+        d = __ffma2_rn(make_float2(q[2 * i], q[2 * i + 1]), make_float2(k[2 * i], k[2 * i + 1]), d);
+    return d.x + d.y;
+}
+template <int E>
+__device__ __forceinline__ void axpy_e(float p, const float (&v)[E], float (&acc)[E]) {
+    const float2 pp = make_float2(p, p);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+        const float2 a = __ffma2_rn(pp, make_float2(v[2 * i], v[2 * i + 1]),
+                                    make_float2(acc[2 * i], acc[2 * i + 1]));
+        acc[2 * i] = a.x;
+        acc[2 * i + 1] = a.y;
+    }
+}
+template <int E>
+__device__ __forceinline__ void scale_e(float c, float (&acc)[E]) {
+    const float2 cc = make_float2(c, c);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+        const float2 a = __fmul2_rn(cc, make_float2(acc[2 * i], acc[2 * i + 1]));
+        acc[2 * i] = a.x;
+        acc[2 * i + 1] = a.y;
+    }
+}
+
 template <int HD, int G, int E, int L, int NR>
 __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
                                             const float* __restrict__ Vt,
@@ -281,12 +323,7 @@ __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
             kv[4 * c + 3] = v.w;
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) d = fmaf(q[h][e], kv[e], d);
-            s[r][h] = d;
-        }
+        for (int h = 0; h < G; ++h) s[r][h] = dot_e<E>(q[h], kv);
     }
 #pragma unroll
     for (int off = 1; off < L; off <<= 1) {
@@ -310,8 +347,7 @@ __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
         if (mx > m[h]) {
             const float corr = exp2f(m[h] - mx);
             l[h] *= corr;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[h][e] *= corr;
+            scale_e<E>(corr, acc[h]);
             m[h] = mx;
         }
     }
@@ -332,8 +368,7 @@ __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
             for (int h = 0; h < G; ++h) {
                 const float pr = exp2f(s[r][h] - m[h]);
                 l[h] += pr;
-#pragma unroll
-                for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pr, vv[e], acc[h][e]);
+                axpy_e<E>(pr, vv, acc[h]);
             }
         }
     }
@@ -374,14 +409,7 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
             kv[4 * c + 3] = v.w;
         }
 #pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            float d = 0.f;
-            if (h < G) {
-#pragma unroll
-                for (int e = 0; e < E; ++e) d = fmaf(q[h < G ? h : 0][e], kv[e], d);
-            }
-            s[r * GP + h] = d;
-        }
+        for (int h = 0; h < GP; ++h) s[r * GP + h] = h < G ? dot_e<E>(q[h < G ? h : 0], kv) : 0.f;
     }
     // halving reduction over the group's lanes
 #pragma unroll
@@ -431,8 +459,7 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float c = __shfl_sync(0xffffffffu, corr[h % CNT], gbase + h / CNT);
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[h][e] *= c;
+            scale_e<E>(c, acc[h]);
         }
     }
 #pragma unroll
@@ -466,11 +493,7 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
                 vv[4 * c + 3] = v.w;
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float p = pr[r * GP + h];
-#pragma unroll
-                for (int e = 0; e < E; ++e) acc[h][e] = fmaf(p, vv[e], acc[h][e]);
-            }
+            for (int h = 0; h < G; ++h) axpy_e<E>(pr[r * GP + h], vv, acc[h]);
         }
     }
 }
