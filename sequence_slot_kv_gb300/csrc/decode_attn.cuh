@@ -640,9 +640,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         }
     }
     __syncthreads();
-    // a row's split count and the tile counts of its full and last splits
+    // a row's split count, the tile counts of its full and last splits, and
+    // how many of its listed items are full / last splits (split 0 of the
+    // first static_items (row, kv head) pairs belongs to the decode CTAs)
     auto row_shape = [&](uint32_t b, uint32_t& p, uint32_t& nsplit, uint32_t& full_tiles,
-                         uint32_t& last_tiles) {
+                         uint32_t& last_tiles, uint32_t& nfull, uint32_t& nlast,
+                         uint32_t& ns) {
         p = P.positions[b];
         if (paged) {
             if (row_bad[b >> 5] & (1u << (b & 31))) return false;
@@ -653,36 +656,50 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         nsplit = (p + 1 + chunk - 1) / chunk;
         full_tiles = chunk / T;
         last_tiles = (p + (P.prefill ? 1u : 0u) - (nsplit - 1) * chunk + T - 1) / T;
+        const uint32_t first = b * nkv;
+        ns = P.static_items > first ? (P.static_items - first < nkv ? P.static_items - first : nkv)
+                                    : 0u;
+        nfull = nsplit > 1 ? (nsplit - 1) * nkv - ns : 0u;
+        nlast = nsplit > 1 ? nkv : nkv - ns;
         return true;
     };
     auto bin_of = [](uint32_t tiles) { return tiles < kPlanBins ? tiles : kPlanBins - 1u; };
     // pass 1: histogram of item sizes
     for (uint32_t b = tid; b < P.B; b += kPlanThreads) {
-        uint32_t p, nsplit, ft, lt;
-        if (!row_shape(b, p, nsplit, ft, lt)) {
+        uint32_t p, nsplit, ft, lt, nfull, nlast, ns;
+        if (!row_shape(b, p, nsplit, ft, lt, nfull, nlast, ns)) {
             atomicOr(P.status, kDevRange);
             continue;
         }
-        if (nsplit > 1) atomicAdd(&bin_count[bin_of(ft)], (nsplit - 1) * nkv);
-        atomicAdd(&bin_count[bin_of(lt)], nkv);
+        if (nfull) atomicAdd(&bin_count[bin_of(ft)], nfull);
+        if (nlast) atomicAdd(&bin_count[bin_of(lt)], nlast);
     }
     __syncthreads();
-    if (tid == 0) {
-        uint32_t run = 0;
-        for (int i = kPlanBins - 1; i >= 0; --i) {
-            bin_cursor[i] = run;
-            run += bin_count[i];
+    // bins in descending order: lane l holds bins 63-2l and 62-2l; an
+    // exclusive scan over the lanes gives each bin's first record
+    static_assert(kPlanBins == 64, "the scan covers 64 bins with one warp");
+    if (warp == 0) {
+        const uint32_t hi = bin_count[63 - 2 * lane], lo = bin_count[62 - 2 * lane];
+        uint32_t incl = hi + lo;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
         }
-        total = run;
+        const uint32_t excl = incl - hi - lo;
+        bin_cursor[63 - 2 * lane] = excl;
+        bin_cursor[62 - 2 * lane] = excl + hi;
+        if (lane == 31) total = incl;
     }
     __syncthreads();
     // pass 2: one warp per row reserves the row's ranges and writes them
     uint4* recs = reinterpret_cast<uint4*>(P.items);
     for (uint32_t b = warp; b < P.B; b += kPlanThreads / 32) {
         uint32_t p = 0, prow = 0, nsplit = 0, ft = 0, lt = 0, full_base = 0, last_base = 0;
+        uint32_t nfull = 0, nlast = 0, ns = 0;
         bool ok = false;
         if (lane == 0) {
-            ok = row_shape(b, p, nsplit, ft, lt);
+            ok = row_shape(b, p, nsplit, ft, lt, nfull, nlast, ns);
             if (ok) {
                 // the row of key p in the [rows][kv_dim] view of K and V
                 if (paged)
@@ -690,8 +707,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
                                  p / P.slot_ctx) * P.slot_ctx + p % P.slot_ctx;
                 else
                     prow = P.slots[b] * P.slot_ctx + p;
-                if (nsplit > 1) full_base = atomicAdd(&bin_cursor[bin_of(ft)], (nsplit - 1) * nkv);
-                last_base = atomicAdd(&bin_cursor[bin_of(lt)], nkv);
+                if (nfull) full_base = atomicAdd(&bin_cursor[bin_of(ft)], nfull);
+                if (nlast) last_base = atomicAdd(&bin_cursor[bin_of(lt)], nlast);
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -701,11 +718,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         nsplit = __shfl_sync(0xffffffffu, nsplit, 0);
         full_base = __shfl_sync(0xffffffffu, full_base, 0);
         last_base = __shfl_sync(0xffffffffu, last_base, 0);
-        const uint32_t nfull = (nsplit - 1) * nkv;
+        nfull = __shfl_sync(0xffffffffu, nfull, 0);
+        nlast = __shfl_sync(0xffffffffu, nlast, 0);
+        ns = __shfl_sync(0xffffffffu, ns, 0);
+        // listed full splits: (split, kv head) = divmod(i + ns, nkv); listed
+        // last splits: kv heads nkv - nlast .. nkv - 1
         for (uint32_t i = lane; i < nfull; i += 32)
-            recs[full_base + i] = make_uint4(pack_item(b, i / nkv, i % nkv), p, prow, 0u);
-        for (uint32_t i = lane; i < nkv; i += 32)
-            recs[last_base + i] = make_uint4(pack_item(b, nsplit - 1, i), p, prow, 0u);
+            recs[full_base + i] = make_uint4(pack_item(b, (i + ns) / nkv, (i + ns) % nkv), p, prow, 0u);
+        for (uint32_t i = lane; i < nlast; i += 32)
+            recs[last_base + i] = make_uint4(pack_item(b, nsplit - 1, i + (nkv - nlast)), p, prow, 0u);
     }
     __syncthreads();
     if (tid == 0) {
@@ -787,12 +808,18 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         // k-1), while item k's tiles are still streaming, so the prep warp has
         // item k+1 ready before the consumers reach it.
         if (warp == C::WARP_TMA && lane == 0) {
-            grid_dependency_wait();  // the plan's list and counters
-            const uint32_t n_items = __ldcg(P.plan);
             const uint4* recs = reinterpret_cast<const uint4*>(P.items);
-            // stage item k from record `rec` (or the end marker); returns the
-            // item's tile stream: kv head, first tensor row, tile count
             const bool paged = P.block_tables != nullptr;
+            // The plan's list, its length and the hand-out counter may be read
+            // only once the plan kernel has finished.  A CTA with a static
+            // first item waits for that lazily, streaming the item meanwhile.
+            bool planned = false;
+            uint32_t n_items = 0;
+            auto await_plan = [&]() {
+                grid_dependency_wait();
+                n_items = __ldcg(P.plan);
+                planned = true;
+            };
             // stage item k from record `rec` (or the end marker); in paged mode
             // row_o is the item's first key and blk_o the block holding it
             auto stage = [&](uint32_t k, bool valid, uint4 rec, uint32_t& kvh_o, int& row_o,
@@ -850,16 +877,36 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 }
                 return true;
             };
-            uint32_t it = atomicAdd(P.plan + 1, 1u);
-            uint4 rec = it < n_items ? __ldcg(recs + it) : make_uint4(0, 0, 0, 0);
+            // first item: CTA c < static_items owns split 0 of (row, kv head)
+            // pair c.  Its inputs come from work that precedes the plan kernel
+            // on the stream, so they are complete; the plan checks the row the
+            // same way and leaves the item out of its list.
+            uint4 rec = make_uint4(0, 0, 0, 0);
+            bool first_ok = false;
+            if (blockIdx.x < P.static_items) {
+                const uint32_t b = blockIdx.x / P.n_kv_head, kvh = blockIdx.x % P.n_kv_head;
+                const uint32_t p = __ldg(P.positions + b), slot = __ldg(P.slots + b);
+                if (slot < P.n_slots && p < P.slot_ctx) {
+                    rec = make_uint4(pack_item(b, 0, kvh), p, slot * P.slot_ctx + p, 0u);
+                    first_ok = true;
+                }
+            }
+            if (!first_ok) {
+                await_plan();
+                const uint32_t it = atomicAdd(P.plan + 1, 1u);
+                first_ok = it < n_items;
+                if (first_ok) rec = __ldcg(recs + it);
+            }
             uint32_t cur_kvh = 0, cur_nt = 0, nxt_kvh = 0, nxt_nt = 0;
             int cur_row = 0, nxt_row = 0;
             const uint32_t* cur_tab = nullptr;
             const uint32_t* nxt_tab = nullptr;
             uint32_t cur_blk = 0, nxt_blk = 0;
-            bool cur_ok = stage(0, it < n_items, rec, cur_kvh, cur_row, cur_nt, cur_tab, cur_blk);
-            // the record of the item after the staged one, claimed early
-            uint32_t it_n = cur_ok ? atomicAdd(P.plan + 1, 1u) : n_items;
+            bool cur_ok = stage(0, first_ok, rec, cur_kvh, cur_row, cur_nt, cur_tab, cur_blk);
+            // the record of the item after the staged one, claimed early (a
+            // static first item claims it once its tiles fill the ring)
+            uint32_t it_n = 0;
+            if (planned) it_n = cur_ok ? atomicAdd(P.plan + 1, 1u) : n_items;
             uint4 rec_n = make_uint4(0, 0, 0, 0);
             bool rec_n_loaded = false;
             uint32_t tile_g = 0;
@@ -891,7 +938,12 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(cur_kvh * HD), trow,
                                 full);
                     misc[2] = static_cast<int>(tile_g + 1);
-                    if (!rec_n_loaded) {
+                    if (!planned) {
+                        if (t + 1 >= static_cast<uint32_t>(S) || t + 1 == cur_nt) {
+                            await_plan();
+                            it_n = atomicAdd(P.plan + 1, 1u);
+                        }
+                    } else if (!rec_n_loaded) {
                         if (it_n < n_items) rec_n = __ldcg(recs + it_n);
                         rec_n_loaded = true;
                     } else if (!nxt_staged && (k == 0 || mbar_test(nfree, nparity))) {
@@ -901,6 +953,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     }
                 }
                 if (misc[0]) break;
+                if (!planned) {  // a static first item without tiles
+                    await_plan();
+                    it_n = atomicAdd(P.plan + 1, 1u);
+                }
                 if (!nxt_staged) {
                     if (!rec_n_loaded && it_n < n_items) rec_n = __ldcg(recs + it_n);
                     if (k >= 1 && !mbar_wait(nfree, nparity)) {
