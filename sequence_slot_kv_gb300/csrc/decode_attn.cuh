@@ -607,6 +607,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     __shared__ uint32_t bin_cursor[kPlanBins];
     __shared__ uint32_t total;
     __shared__ uint32_t row_bad[kPlanMaxRows / 32];  // paged mode: rows failing the check
+    // one round of rows (one per thread) handed from reservation to writing
+    __shared__ uint32_t sh_p[kPlanThreads], sh_prow[kPlanThreads], sh_meta[kPlanThreads];
+    __shared__ uint32_t sh_fb[kPlanThreads], sh_lb[kPlanThreads];
+    __shared__ uint32_t sh_nf[kPlanThreads], sh_nl[kPlanThreads];
     grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t nkv = P.n_kv_head;
@@ -615,64 +619,92 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     if (paged) {
         for (uint32_t i = tid; i < (P.B + 31) / 32; i += kPlanThreads) row_bad[i] = 0;
         __syncthreads();
-        // pass 0 (paged): one warp per row checks the row's used table entries,
-        // four loads in flight per lane
-        for (uint32_t b = warp; b < P.B; b += kPlanThreads / 32) {
-            const uint32_t p = P.positions[b];
-            bool bad = static_cast<uint64_t>(p) >=
-                       static_cast<uint64_t>(P.bt_stride) * P.slot_ctx;
-            if (!bad) {
-                const uint32_t* tab = P.block_tables + static_cast<size_t>(b) * P.bt_stride;
-                const uint32_t used = p / P.slot_ctx + 1;
-                for (uint32_t i0 = 0; i0 < used; i0 += 128) {
-                    uint32_t id[4];
+        // pass 0 (paged): each warp checks the used table entries of four rows
+        // at a time, two loads per row and lane in flight
+        constexpr int RW = 4;
+        for (uint32_t b0 = warp * RW; b0 < P.B; b0 += (kPlanThreads / 32) * RW) {
+            uint32_t used[RW];
+            bool bad[RW];
+            const uint32_t* tab[RW];
+            uint32_t most = 0;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t i = i0 + u * 32 + lane;
-                        id[u] = i < used ? __ldg(tab + i) : 0u;
+            for (int u = 0; u < RW; ++u) {
+                const uint32_t b = b0 + u;
+                const uint32_t p = b < P.B ? P.positions[b] : 0u;
+                bad[u] = b < P.B && static_cast<uint64_t>(p) >=
+                                        static_cast<uint64_t>(P.bt_stride) * P.slot_ctx;
+                used[u] = (b < P.B && !bad[u]) ? p / P.slot_ctx + 1 : 0u;
+                tab[u] = P.block_tables + static_cast<size_t>(b < P.B ? b : 0) * P.bt_stride;
+                most = used[u] > most ? used[u] : most;
+            }
+            for (uint32_t i0 = 0; i0 < most; i0 += 64) {
+                uint32_t id[RW][2];
+#pragma unroll
+                for (int u = 0; u < RW; ++u)
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const uint32_t i = i0 + v * 32 + lane;
+                        id[u][v] = i < used[u] ? __ldg(tab[u] + i) : 0u;
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) bad |= id[u] >= P.n_slots;
-                }
+                for (int u = 0; u < RW; ++u) bad[u] |= id[u][0] >= P.n_slots || id[u][1] >= P.n_slots;
             }
-            bad = __any_sync(0xffffffffu, bad);
-            if (bad && lane == 0) atomicOr(&row_bad[b >> 5], 1u << (b & 31));
+#pragma unroll
+            for (int u = 0; u < RW; ++u) {
+                const bool any = __any_sync(0xffffffffu, bad[u]);
+                if (any && lane == 0) atomicOr(&row_bad[(b0 + u) >> 5], 1u << ((b0 + u) & 31));
+            }
         }
     }
     __syncthreads();
-    // a row's split count, the tile counts of its full and last splits, and
-    // how many of its listed items are full / last splits (split 0 of the
-    // first static_items (row, kv head) pairs belongs to the decode CTAs)
-    auto row_shape = [&](uint32_t b, uint32_t& p, uint32_t& nsplit, uint32_t& full_tiles,
-                         uint32_t& last_tiles, uint32_t& nfull, uint32_t& nlast,
-                         uint32_t& ns) {
-        p = P.positions[b];
+    // A row's shape: position, row of key p in the [rows][kv_dim] view of K
+    // and V, split count, the tile counts of its full and last splits, and how
+    // many of its listed items are full / last splits (split 0 of the first
+    // static_items (row, kv head) pairs belongs to the decode CTAs).
+    struct Shape {
+        uint32_t p, prow, nsplit, ft, lt, nfull, nlast, ns;
+    };
+    auto row_shape = [&](uint32_t b, Shape& r) {
+        r.p = P.positions[b];
         if (paged) {
             if (row_bad[b >> 5] & (1u << (b & 31))) return false;
-        } else if (P.slots[b] >= P.n_slots || p >= P.slot_ctx) {
-            return false;
+            r.prow = __ldg(P.block_tables + static_cast<size_t>(b) * P.bt_stride +
+                           r.p / P.slot_ctx) * P.slot_ctx + r.p % P.slot_ctx;
+        } else {
+            const uint32_t slot = P.slots[b];
+            if (slot >= P.n_slots || r.p >= P.slot_ctx) return false;
+            r.prow = slot * P.slot_ctx + r.p;
         }
-        const uint32_t chunk = split_chunk(p + 1, P.chunk_min, P.max_splits, T);
-        nsplit = (p + 1 + chunk - 1) / chunk;
-        full_tiles = chunk / T;
-        last_tiles = (p + (P.prefill ? 1u : 0u) - (nsplit - 1) * chunk + T - 1) / T;
+        const uint32_t chunk = split_chunk(r.p + 1, P.chunk_min, P.max_splits, T);
+        r.nsplit = (r.p + 1 + chunk - 1) / chunk;
+        r.ft = chunk / T;
+        r.lt = (r.p + (P.prefill ? 1u : 0u) - (r.nsplit - 1) * chunk + T - 1) / T;
         const uint32_t first = b * nkv;
-        ns = P.static_items > first ? (P.static_items - first < nkv ? P.static_items - first : nkv)
-                                    : 0u;
-        nfull = nsplit > 1 ? (nsplit - 1) * nkv - ns : 0u;
-        nlast = nsplit > 1 ? nkv : nkv - ns;
+        r.ns = P.static_items > first
+                   ? (P.static_items - first < nkv ? P.static_items - first : nkv)
+                   : 0u;
+        r.nfull = r.nsplit > 1 ? (r.nsplit - 1) * nkv - r.ns : 0u;
+        r.nlast = r.nsplit > 1 ? nkv : nkv - r.ns;
         return true;
     };
     auto bin_of = [](uint32_t tiles) { return tiles < kPlanBins ? tiles : kPlanBins - 1u; };
-    // pass 1: histogram of item sizes
+    // pass 1: one thread per row, histogram of item sizes.  A thread keeps its
+    // first row's shape for pass 2 (all of them when B <= kPlanThreads).
+    Shape mine{};
+    bool mine_ok = false;
     for (uint32_t b = tid; b < P.B; b += kPlanThreads) {
-        uint32_t p, nsplit, ft, lt, nfull, nlast, ns;
-        if (!row_shape(b, p, nsplit, ft, lt, nfull, nlast, ns)) {
+        Shape r{};
+        const bool ok = row_shape(b, r);
+        if (!ok) {
             atomicOr(P.status, kDevRange);
-            continue;
+        } else {
+            if (r.nfull) atomicAdd(&bin_count[bin_of(r.ft)], r.nfull);
+            if (r.nlast) atomicAdd(&bin_count[bin_of(r.lt)], r.nlast);
         }
-        if (nfull) atomicAdd(&bin_count[bin_of(ft)], nfull);
-        if (nlast) atomicAdd(&bin_count[bin_of(lt)], nlast);
+        if (b == static_cast<uint32_t>(tid)) {
+            mine = r;
+            mine_ok = ok;
+        }
     }
     __syncthreads();
     // bins in descending order: lane l holds bins 63-2l and 62-2l; an
@@ -692,43 +724,44 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         if (lane == 31) total = incl;
     }
     __syncthreads();
-    // pass 2: one warp per row reserves the row's ranges and writes them
+    // pass 2, by rounds of kPlanThreads rows: each thread reserves its row's
+    // ranges in the bins, then warps write the rows' records
     uint4* recs = reinterpret_cast<uint4*>(P.items);
-    for (uint32_t b = warp; b < P.B; b += kPlanThreads / 32) {
-        uint32_t p = 0, prow = 0, nsplit = 0, ft = 0, lt = 0, full_base = 0, last_base = 0;
-        uint32_t nfull = 0, nlast = 0, ns = 0;
-        bool ok = false;
-        if (lane == 0) {
-            ok = row_shape(b, p, nsplit, ft, lt, nfull, nlast, ns);
+    for (uint32_t r0 = 0; r0 < P.B; r0 += kPlanThreads) {
+        const uint32_t b = r0 + tid;
+        uint32_t meta = 0;  // nsplit | ns << 16 of a row with items, else 0
+        if (b < P.B) {
+            Shape r = mine;
+            const bool ok = r0 == 0 ? mine_ok : row_shape(b, r);
             if (ok) {
-                // the row of key p in the [rows][kv_dim] view of K and V
-                if (paged)
-                    prow = __ldg(P.block_tables + static_cast<size_t>(b) * P.bt_stride +
-                                 p / P.slot_ctx) * P.slot_ctx + p % P.slot_ctx;
-                else
-                    prow = P.slots[b] * P.slot_ctx + p;
-                if (nfull) full_base = atomicAdd(&bin_cursor[bin_of(ft)], nfull);
-                if (nlast) last_base = atomicAdd(&bin_cursor[bin_of(lt)], nlast);
+                sh_p[tid] = r.p;
+                sh_prow[tid] = r.prow;
+                sh_nf[tid] = r.nfull;
+                sh_nl[tid] = r.nlast;
+                sh_fb[tid] = r.nfull ? atomicAdd(&bin_cursor[bin_of(r.ft)], r.nfull) : 0u;
+                sh_lb[tid] = r.nlast ? atomicAdd(&bin_cursor[bin_of(r.lt)], r.nlast) : 0u;
+                meta = r.nsplit | (r.ns << 16);
             }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) continue;
-        p = __shfl_sync(0xffffffffu, p, 0);
-        prow = __shfl_sync(0xffffffffu, prow, 0);
-        nsplit = __shfl_sync(0xffffffffu, nsplit, 0);
-        full_base = __shfl_sync(0xffffffffu, full_base, 0);
-        last_base = __shfl_sync(0xffffffffu, last_base, 0);
-        nfull = __shfl_sync(0xffffffffu, nfull, 0);
-        nlast = __shfl_sync(0xffffffffu, nlast, 0);
-        ns = __shfl_sync(0xffffffffu, ns, 0);
-        // listed full splits: (split, kv head) = divmod(i + ns, nkv); listed
-        // last splits: kv heads nkv - nlast .. nkv - 1
-        for (uint32_t i = lane; i < nfull; i += 32)
-            recs[full_base + i] = make_uint4(pack_item(b, (i + ns) / nkv, (i + ns) % nkv), p, prow, 0u);
-        for (uint32_t i = lane; i < nlast; i += 32)
-            recs[last_base + i] = make_uint4(pack_item(b, nsplit - 1, i + (nkv - nlast)), p, prow, 0u);
+        sh_meta[tid] = meta;
+        __syncthreads();
+        const uint32_t nrows = P.B - r0 < static_cast<uint32_t>(kPlanThreads)
+                                   ? P.B - r0 : static_cast<uint32_t>(kPlanThreads);
+        for (uint32_t i = warp; i < nrows; i += kPlanThreads / 32) {
+            const uint32_t m = sh_meta[i];
+            if (!m) continue;
+            const uint32_t row = r0 + i, nsplit = m & 0xffffu, ns = m >> 16;
+            const uint32_t p = sh_p[i], prow = sh_prow[i];
+            const uint32_t nfull = sh_nf[i], nlast = sh_nl[i], fb = sh_fb[i], lb = sh_lb[i];
+            // listed full splits: (split, kv head) = divmod(j + ns, nkv); listed
+            // last splits: kv heads nkv - nlast .. nkv - 1
+            for (uint32_t j = lane; j < nfull; j += 32)
+                recs[fb + j] = make_uint4(pack_item(row, (j + ns) / nkv, (j + ns) % nkv), p, prow, 0u);
+            for (uint32_t j = lane; j < nlast; j += 32)
+                recs[lb + j] = make_uint4(pack_item(row, nsplit - 1, j + (nkv - nlast)), p, prow, 0u);
+        }
+        __syncthreads();
     }
-    __syncthreads();
     if (tid == 0) {
         P.plan[0] = total;
         P.plan[1] = 0;
