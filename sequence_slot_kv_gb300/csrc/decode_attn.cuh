@@ -126,7 +126,8 @@ struct KCfg {
     // handed[NMS], hand_free[NMS]
     static constexpr int NBAR = 2 * S + 6 + 2 * NMS;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 16;
+    static constexpr int OFF_PEND = OFF_MISC + 16;  // the consumers' unmerged partial
+    static constexpr int SMEM = OFF_PEND + 32;
     static_assert(L >= 1 && L <= 32 && (32 % L) == 0, "lane group must divide a warp");
     static_assert(E % 4 == 0 && E * L == HD, "lane slice must be whole float4s");
     static_assert(R >= 1 && R * NG == T, "tile must split evenly over the groups");
@@ -519,6 +520,61 @@ __device__ __forceinline__ void tr_state_to_heads(const int li, const int lane, 
     }
 }
 
+// Merge statistics of nsplit split partials for NH query heads (nh of them
+// used), by one warp: per head the max M over the splits' running maxima and
+// L = sum_s l_s * exp2(m_s - M), then the sink joins both.  Head h's pairs
+// (m_s, l_s) sit at ml0 + h * hstride + 2 s.  Lanes take splits lane, lane +
+// 32, ... and the sums meet in a fixed xor tree, so every caller gets the
+// same bits for the same partials.
+template <int NH>
+__device__ __forceinline__ void merge_stats(const float* ml0, size_t hstride, int nh,
+                                            uint32_t nsplit, const float* sinks, int lane,
+                                            float (&M)[NH], float (&L)[NH]) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    float2 c[NH];  // this lane's first split
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+        c[h] = make_float2(-CUDART_INF_F, 0.f);
+        if (h < nh && static_cast<uint32_t>(lane) < nsplit)
+            c[h] = __ldcg(reinterpret_cast<const float2*>(ml0 + h * hstride) + lane);
+        M[h] = c[h].x;
+    }
+    for (uint32_t s = lane + 32; s < nsplit; s += 32) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+            if (h < nh) M[h] = fmaxf(M[h], __ldcg(ml0 + h * hstride + 2 * s));
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+        L[h] = static_cast<uint32_t>(lane) < nsplit && h < nh
+                   ? __fmaf_rn(c[h].y, exp2f(c[h].x - M[h]), 0.f) : 0.f;
+    }
+    for (uint32_t s = lane + 32; s < nsplit; s += 32) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            if (h < nh) {
+                const float2 e = __ldcg(reinterpret_cast<const float2*>(ml0 + h * hstride) + s);
+                L[h] = __fmaf_rn(e.y, exp2f(e.x - M[h]), L[h]);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            L[h] = __fadd_rn(L[h], __shfl_xor_sync(0xffffffffu, L[h], off));
+        if (sinks && h < nh) {
+            const float sk = __fmul_rn(sinks[h], kLog2e);
+            const float M2 = fmaxf(M[h], sk);
+            L[h] = __fmaf_rn(L[h], exp2f(M[h] - M2), exp2f(sk - M2));
+            M[h] = M2;
+        }
+    }
+}
+
 // exp2(m - M) as the weight of a partial whose running max is m, with an
 // empty partial (m = -inf) weighing 0 even when M is -inf too.
 __device__ __forceinline__ float partial_weight(float m, float M) {
@@ -803,6 +859,9 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
     const uint32_t handed0 = free0 + 16;                   // partial handed to the merge warp
     const uint32_t hfree0 = handed0 + 8 * NMS;             // hand-off slot released
     volatile int* misc = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+    // pend[0..3]: the last item's partial awaits its merge (flag, row, kv
+    // head, splits); pend[4]: the consumers' tail-merge decision
+    volatile uint32_t* pend = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_PEND);
     // misc[0]: abort, misc[2]: tiles issued, misc[3]: items staged
 
     if (tid == 0) {
@@ -821,6 +880,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         }
         misc[0] = 0;
         misc[1] = 0;
+        pend[0] = 0;
         misc[2] = 0;
         misc[3] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1079,43 +1139,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     const int nh = G - h0 < HG ? G - h0 : HG;
                     const size_t base0 = (static_cast<size_t>(b) * P.n_head + hq0 + h0) * MS;
                     float Mh[HG], Lh[HG];
-#pragma unroll
-                    for (int h = 0; h < HG; ++h) Mh[h] = -CUDART_INF_F;
-                    for (uint32_t s2 = lane; s2 < nsplit; s2 += 32) {
-#pragma unroll
-                        for (int h = 0; h < HG; ++h)
-                            if (h < nh)
-                                Mh[h] = fmaxf(Mh[h], __ldcg(P.ws_ml + (base0 + h * MS + s2) * 2));
-                    }
-#pragma unroll
-                    for (int h = 0; h < HG; ++h) {
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            Mh[h] = fmaxf(Mh[h], __shfl_xor_sync(0xffffffffu, Mh[h], off));
-                        Lh[h] = 0.f;
-                    }
-                    for (uint32_t s2 = lane; s2 < nsplit; s2 += 32) {
-#pragma unroll
-                        for (int h = 0; h < HG; ++h) {
-                            if (h < nh) {
-                                const size_t at = (base0 + h * MS + s2) * 2;
-                                Lh[h] += __ldcg(P.ws_ml + at + 1) *
-                                         exp2f(__ldcg(P.ws_ml + at) - Mh[h]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int h = 0; h < HG; ++h) {
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            Lh[h] += __shfl_xor_sync(0xffffffffu, Lh[h], off);
-                        if (P.sinks && h < nh) {
-                            const float sk = P.sinks[hq0 + h0 + h] * kLog2e;
-                            const float M2 = fmaxf(Mh[h], sk);
-                            Lh[h] = Lh[h] * exp2f(Mh[h] - M2) + exp2f(sk - M2);
-                            Mh[h] = M2;
-                        }
-                    }
+                    merge_stats<HG>(P.ws_ml + base0 * 2, MS * 2, nh, nsplit,
+                                    P.sinks ? P.sinks + hq0 + h0 : nullptr, lane, Mh, Lh);
                     // outputs: lanes over the hd/4 float4 columns (every lane
                     // runs every iteration: the shuffles name the whole warp),
                     // one head at a time, 8 splits' loads in flight per round
@@ -1124,7 +1149,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                         if (h >= nh) break;
                         float* orow =
                             P.out + (static_cast<size_t>(b) * P.n_head + hq0 + h0 + h) * HD;
-                        const float inv = 1.f / Lh[h];
+                        const float inv = __frcp_rn(Lh[h]);
                         const float Mhh = Mh[h];
                         const float* wsa = P.ws_acc + (base0 + h * MS) * HD;
                         const float* wsm = P.ws_ml + (base0 + h * MS) * 2;
@@ -1149,16 +1174,17 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
 #pragma unroll
                                     for (int u = 0; u < 8; ++u) {
                                         const float w = __shfl_sync(0xffffffffu, wl, (i0 + u) & 31);
-                                        a.x = fmaf(w, v[u].x, a.x);
-                                        a.y = fmaf(w, v[u].y, a.y);
-                                        a.z = fmaf(w, v[u].z, a.z);
-                                        a.w = fmaf(w, v[u].w, a.w);
+                                        a.x = __fmaf_rn(w, v[u].x, a.x);
+                                        a.y = __fmaf_rn(w, v[u].y, a.y);
+                                        a.z = __fmaf_rn(w, v[u].z, a.z);
+                                        a.w = __fmaf_rn(w, v[u].w, a.w);
                                     }
                                 }
                             }
                             if (act)
                                 reinterpret_cast<float4*>(orow)[d4] =
-                                    make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+                                    make_float4(__fmul_rn(a.x, inv), __fmul_rn(a.y, inv),
+                                                __fmul_rn(a.z, inv), __fmul_rn(a.w, inv));
                         }
                     }
                 }
@@ -1183,6 +1209,87 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         named_sync<C::CONS>();  // every consumer warp takes the same branch
         if (misc[0]) break;
         const uint32_t end = desc[is].end;
+        // The previous item's partial, if it left one: handed to the merge
+        // warp, or, when no item follows in this CTA (the kernel's tail, where
+        // the consumers would idle), counted and merged here by all consumer
+        // threads with one round of loads.  Both paths compute the same bits.
+        if (pend[0]) {
+            const uint32_t pb = pend[1], pkvh = pend[2], pns = pend[3];
+            if (!end || pns > static_cast<uint32_t>(HD)) {
+                if (warp == W - 1) {
+                    if (lane == 0) {
+                        const uint32_t hs = handed % NMS;
+                        if (handed < NMS || mbar_wait(hfree0 + 8 * hs, ((handed / NMS) - 1) & 1)) {
+                            hand[hs].b = pb;
+                            hand[hs].kvh = pkvh;
+                            hand[hs].nsplit = pns;
+                            hand[hs].end = 0;
+                            mbar_arrive(handed0 + 8 * hs);
+                        } else {
+                            atomicOr(P.status, kDevTimeout);
+                            misc[0] = 1;
+                        }
+                    }
+                    ++handed;
+                }
+            } else {
+                uint32_t* counter = P.counters + static_cast<size_t>(pb) * P.n_kv_head + pkvh;
+                if (tid == 0) {
+                    const uint32_t old = atomic_add_acq_rel(counter, 1u);
+                    const uint32_t last = old == pns - 1 ? 1u : 0u;
+                    if (last) *counter = 0u;  // every split has arrived
+                    pend[4] = last;
+                }
+                named_sync<C::CONS>();
+                if (pend[4]) {
+                    const size_t MS = P.max_splits;
+                    const uint32_t hq0 = pkvh * G;
+                    float* wts = chain;             // split weights [G][pns]
+                    float* invl = chain + G * pns;  // 1 / L per head
+                    for (int h = warp; h < G; h += W) {
+                        const size_t hb = (static_cast<size_t>(pb) * P.n_head + hq0 + h) * MS;
+                        float M1[1], L1[1];
+                        merge_stats<1>(P.ws_ml + hb * 2, 0, 1, pns,
+                                       P.sinks ? P.sinks + hq0 + h : nullptr, lane, M1, L1);
+                        for (uint32_t s2 = lane; s2 < pns; s2 += 32)
+                            wts[h * pns + s2] = exp2f(__ldcg(P.ws_ml + (hb + s2) * 2) - M1[0]);
+                        if (lane == 0) invl[h] = __frcp_rn(L1[0]);
+                    }
+                    named_sync<C::CONS>();
+                    // out = sum over the splits, in split order, of w * acc, times 1 / L
+                    for (int c = tid; c < G * (HD / 4); c += C::CONS) {
+                        const int h = c / (HD / 4), d4 = c % (HD / 4);
+                        const size_t hb = (static_cast<size_t>(pb) * P.n_head + hq0 + h) * MS;
+                        const float* wsa = P.ws_acc + hb * HD;
+                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (uint32_t s0 = 0; s0 < pns; s0 += 8) {
+                            float4 v[8];
+                            float wv[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const bool in = s0 + u < pns;
+                                v[u] = in ? __ldcg(reinterpret_cast<const float4*>(wsa + (s0 + u) * HD) + d4)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                                wv[u] = in ? wts[h * pns + s0 + u] : 0.f;
+                            }
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                a.x = __fmaf_rn(wv[u], v[u].x, a.x);
+                                a.y = __fmaf_rn(wv[u], v[u].y, a.y);
+                                a.z = __fmaf_rn(wv[u], v[u].z, a.z);
+                                a.w = __fmaf_rn(wv[u], v[u].w, a.w);
+                            }
+                        }
+                        const float inv = invl[h];
+                        float* orow = P.out + (static_cast<size_t>(pb) * P.n_head + hq0 + h) * HD;
+                        reinterpret_cast<float4*>(orow)[d4] =
+                            make_float4(__fmul_rn(a.x, inv), __fmul_rn(a.y, inv),
+                                        __fmul_rn(a.z, inv), __fmul_rn(a.w, inv));
+                    }
+                }
+                named_sync<C::CONS>();  // the chain scratch is free again
+            }
+        }
         if (end) {
             // tell the merge warp there is nothing more
             if (warp == W - 1 && lane == 0) {
@@ -1380,20 +1487,13 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    const uint32_t hs = handed % NMS;
-                    if (handed < NMS || mbar_wait(hfree0 + 8 * hs, ((handed / NMS) - 1) & 1)) {
-                        hand[hs].b = b;
-                        hand[hs].kvh = kvh;
-                        hand[hs].nsplit = nsplit;
-                        hand[hs].end = 0;
-                        mbar_arrive(handed0 + 8 * hs);
-                    } else {
-                        atomicOr(P.status, kDevTimeout);
-                        misc[0] = 1;
-                    }
-                }
-                ++handed;
+            }
+            // the partial's merge is arranged at the next item's start
+            if (lane == 0) {
+                pend[1] = b;
+                pend[2] = kvh;
+                pend[3] = nsplit;
+                pend[0] = nsplit > 1 ? 1u : 0u;
             }
         }
         __syncwarp();
