@@ -1387,23 +1387,46 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         }
 
         // ------------------------------------ merge the groups of each warp
+        // Halving: at each level a lane keeps half of its elements (the upper
+        // half if its group bit is set) and takes its partner group's share of
+        // that half, so afterwards lane (li, group bits) holds, for every head,
+        // the warp's merged elements e0 .. e0 + EF - 1 of its slice in
+        // acc[h][0 .. EF), EF = hd / 32.  m and l are merged in one fixed
+        // order (lower group first) and stay equal on all lanes.
+        constexpr int EF = HD / 32;
+        int e0 = 0;
 #pragma unroll
-        for (int off = L; off < 32; off <<= 1) {
+        for (int off = L, cnt = E; off < 32; off <<= 1, cnt >>= 1) {
+            const bool upper = (lane & off) != 0;
+            float c_lo[G], c_hi[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
                 const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
-                const float M = fmaxf(m[h], mo);
-                const float c1 = partial_weight(m[h], M), c2 = partial_weight(mo, M);
-                l[h] = l[h] * c1 + lo * c2;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
-                    acc[h][e] = acc[h][e] * c1 + ao * c2;
-                }
+                const float m_lo = upper ? mo : m[h], m_hi = upper ? m[h] : mo;
+                const float l_lo = upper ? lo : l[h], l_hi = upper ? l[h] : lo;
+                const float M = fmaxf(m_lo, m_hi);
+                c_lo[h] = partial_weight(m_lo, M);
+                c_hi[h] = partial_weight(m_hi, M);
+                l[h] = __fmaf_rn(l_lo, c_lo[h], __fmul_rn(l_hi, c_hi[h]));
                 m[h] = M;
             }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+#pragma unroll
+                for (int i = 0; i < cnt / 2; ++i) {
+                    const float send = upper ? acc[h][i] : acc[h][i + cnt / 2];
+                    const float keep = upper ? acc[h][i + cnt / 2] : acc[h][i];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+                    const float v_lo = upper ? recv : keep, v_hi = upper ? keep : recv;
+                    acc[h][i] = __fmaf_rn(v_lo, c_lo[h], __fmul_rn(v_hi, c_hi[h]));
+                }
+            }
+            e0 += upper ? cnt / 2 : 0;
         }
+        // element t < EF of this lane's slice sits at dimension dim(t) of a head
+        // (pairs t, t + 1 are adjacent: EF and e0 are even)
+        auto dim = [&](int t) { return ((e0 + t) >> 2) * 4 * L + 4 * li + ((e0 + t) & 3); };
         // ------------------------------------ chain the four warps: 0 -> 1 -> 2 -> 3
         for (int w2 = 0; w2 < W; ++w2) {
             if (warp == w2) {
@@ -1413,28 +1436,24 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                         const float Mc = chain_m[h], Lc = chain_l[h];
                         const float M = fmaxf(m[h], Mc);
                         const float c1 = partial_weight(m[h], M), c2 = partial_weight(Mc, M);
-                        l[h] = l[h] * c1 + Lc * c2;
+                        l[h] = __fmaf_rn(l[h], c1, __fmul_rn(Lc, c2));
 #pragma unroll
-                        for (int c = 0; c < E / 4; ++c) {
-                            const float4 v = *reinterpret_cast<const float4*>(
-                                chain + h * HD + c * 4 * L + li * 4);
-                            acc[h][4 * c + 0] = acc[h][4 * c + 0] * c1 + v.x * c2;
-                            acc[h][4 * c + 1] = acc[h][4 * c + 1] * c1 + v.y * c2;
-                            acc[h][4 * c + 2] = acc[h][4 * c + 2] * c1 + v.z * c2;
-                            acc[h][4 * c + 3] = acc[h][4 * c + 3] * c1 + v.w * c2;
+                        for (int t = 0; t < EF; t += 2) {
+                            const float2 v = *reinterpret_cast<const float2*>(chain + h * HD + dim(t));
+                            acc[h][t] = __fmaf_rn(acc[h][t], c1, __fmul_rn(v.x, c2));
+                            acc[h][t + 1] = __fmaf_rn(acc[h][t + 1], c1, __fmul_rn(v.y, c2));
                         }
                         m[h] = M;
                     }
                     __syncwarp();
                 }
-                if (w2 < W - 1 && lane < L) {
+                if (w2 < W - 1) {
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
 #pragma unroll
-                        for (int c = 0; c < E / 4; ++c)
-                            *reinterpret_cast<float4*>(chain + h * HD + c * 4 * L + li * 4) =
-                                make_float4(acc[h][4 * c], acc[h][4 * c + 1], acc[h][4 * c + 2],
-                                            acc[h][4 * c + 3]);
+                        for (int t = 0; t < EF; t += 2)
+                            *reinterpret_cast<float2*>(chain + h * HD + dim(t)) =
+                                make_float2(acc[h][t], acc[h][t + 1]);
                         if (lane == 0) {
                             chain_m[h] = m[h];
                             chain_l[h] = l[h];
@@ -1449,41 +1468,34 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         if (warp == W - 1) {
             const uint32_t hq0 = kvh * G;  // first query head of this kv head
             if (nsplit == 1) {
-                if (lane < L) {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float c = 1.f, Ls = l[h];
-                        if (P.sinks) {
-                            const float sk = P.sinks[hq0 + h] * kLog2e;
-                            const float M2 = fmaxf(m[h], sk);
-                            c = exp2f(m[h] - M2);
-                            Ls = Ls * c + exp2f(sk - M2);
-                        }
-                        float* o = P.out + (static_cast<size_t>(b) * P.n_head + hq0 + h) * HD;
-#pragma unroll
-                        for (int cc = 0; cc < E / 4; ++cc)
-                            *reinterpret_cast<float4*>(o + cc * 4 * L + li * 4) = make_float4(
-                                (acc[h][4 * cc] * c) / Ls, (acc[h][4 * cc + 1] * c) / Ls,
-                                (acc[h][4 * cc + 2] * c) / Ls, (acc[h][4 * cc + 3] * c) / Ls);
+                for (int h = 0; h < G; ++h) {
+                    float c = 1.f, Ls = l[h];
+                    if (P.sinks) {
+                        const float sk = P.sinks[hq0 + h] * kLog2e;
+                        const float M2 = fmaxf(m[h], sk);
+                        c = exp2f(m[h] - M2);
+                        Ls = Ls * c + exp2f(sk - M2);
                     }
+                    float* o = P.out + (static_cast<size_t>(b) * P.n_head + hq0 + h) * HD;
+                    const float f = __fmul_rn(c, __frcp_rn(Ls));  // one reciprocal per head
+#pragma unroll
+                    for (int t = 0; t < EF; t += 2)
+                        *reinterpret_cast<float2*>(o + dim(t)) =
+                            make_float2(acc[h][t] * f, acc[h][t + 1] * f);
                 }
             } else {
                 const size_t MS = P.max_splits;
-                if (lane < L) {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const size_t base =
-                            (static_cast<size_t>(b) * P.n_head + hq0 + h) * MS + split;
-                        float* a = P.ws_acc + base * HD;
+                for (int h = 0; h < G; ++h) {
+                    const size_t base = (static_cast<size_t>(b) * P.n_head + hq0 + h) * MS + split;
+                    float* a = P.ws_acc + base * HD;
 #pragma unroll
-                        for (int cc = 0; cc < E / 4; ++cc)
-                            *reinterpret_cast<float4*>(a + cc * 4 * L + li * 4) =
-                                make_float4(acc[h][4 * cc], acc[h][4 * cc + 1],
-                                            acc[h][4 * cc + 2], acc[h][4 * cc + 3]);
-                        if (lane == 0) {
-                            P.ws_ml[base * 2 + 0] = m[h];
-                            P.ws_ml[base * 2 + 1] = l[h];
-                        }
+                    for (int t = 0; t < EF; t += 2)
+                        *reinterpret_cast<float2*>(a + dim(t)) = make_float2(acc[h][t], acc[h][t + 1]);
+                    if (lane == 0) {
+                        P.ws_ml[base * 2 + 0] = m[h];
+                        P.ws_ml[base * 2 + 1] = l[h];
                     }
                 }
                 __syncwarp();
