@@ -316,15 +316,20 @@ int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,
 int slot_kv_get_status(slotkv_t handle, slotkv_stream_t stream, uint32_t* flags);
 
 /*
- * slot_kv_set_split -- split-K policy.  A row with n = p + 1 keys is cut into
- * nsplit = ceil(n / C) chunks of C = max(min_chunk_keys, ceil(n / max_splits)
- * rounded up to the tile) keys; chunks run on separate CTAs and are merged by
- * the last one to finish.  C depends only on n and the geometry, never on B or
- * on the other rows, so a row's result is the same in any batch.
+ * slot_kv_set_split -- fix the split-K policy.  A row with n = p + 1 keys is
+ * cut into nsplit = ceil(n / C) chunks of C = max(min_chunk_keys, ceil(n /
+ * max_splits) rounded up to the tile) keys; chunks run on separate CTAs and
+ * are merged by the last one to finish.  After this call C depends only on n
+ * and the geometry, never on B or on the other rows, so a row's result is the
+ * same bits in any batch.
  * min_chunk_keys must be a positive multiple of the tile (4096 / head_dim
  * keys); max_splits 1..256.  Reallocates the workspace (synchronises).
- * The defaults are min_chunk_keys = 512 KiB of K+V per kv head and
- * max_splits = 64.
+ * Until it is called, a handle uses the default policy: max_splits = 64 and
+ * min_chunk_keys chosen per call from the batch's shape (B, n_kv_head, the
+ * context capacity, the SM count), between 512 KiB and 2 MiB of K+V per kv
+ * head, so that large batches run fewer, larger chunks.  Results are then
+ * deterministic for a given batch size but may differ in the last bits
+ * between batch sizes (within f32 rounding).
  */
 int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_splits);
 

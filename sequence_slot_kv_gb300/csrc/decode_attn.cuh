@@ -1562,6 +1562,19 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
         cudaError_t e = cudaFuncSetAttribute(slotkv_decode_attn_kernel<HD, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return static_cast<int>(e);
+        // one shared-memory carve-out for every kernel of a call, so the SMs
+        // need no reconfiguration between them
+        const int carve = cudaSharedmemCarveoutMaxShared;
+        if ((e = cudaFuncSetAttribute(slotkv_decode_attn_kernel<HD, G>,
+                                      cudaFuncAttributePreferredSharedMemoryCarveout, carve)) !=
+                cudaSuccess ||
+            (e = cudaFuncSetAttribute(slotkv_plan_kernel<C::T>,
+                                      cudaFuncAttributePreferredSharedMemoryCarveout, carve)) !=
+                cudaSuccess ||
+            (e = cudaFuncSetAttribute(slotkv_write_kv_kernel<HD>,
+                                      cudaFuncAttributePreferredSharedMemoryCarveout, carve)) !=
+                cudaSuccess)
+            return static_cast<int>(e);
         // the register hand-over assumes the launch gives every thread 128
         // registers; with fewer, the consumers' request could never be met
         cudaFuncAttributes fa;

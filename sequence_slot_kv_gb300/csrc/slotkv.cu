@@ -60,6 +60,7 @@ struct slotkv_s {
     bool owns_kv = false;
     uint32_t max_rows = 0, max_n_head = 0;
     uint32_t chunk_min = 0, max_splits = 0;
+    bool auto_split = true;  // chunk size from the batch's shape until slot_kv_set_split
     uint32_t options = 0;
     float* ws_ml = nullptr;
     float* ws_acc = nullptr;
@@ -155,9 +156,24 @@ bool valid_handle(slotkv_t h) { return h && h->K && h->V && h->status; }
 
 // The most splits any row of this slot_ctx can need: nsplit(n) <= ceil(n /
 // chunk_min) because chunks are >= chunk_min keys, and <= max_splits.
-uint32_t grid_splits(const slotkv_s* h, uint64_t max_keys) {
-    const uint64_t bound = (max_keys + h->chunk_min - 1) / h->chunk_min;
+uint32_t grid_splits(const slotkv_s* h, uint64_t max_keys, uint32_t chunk_min) {
+    const uint64_t bound = (max_keys + chunk_min - 1) / chunk_min;
     return (uint32_t)(bound < h->max_splits ? bound : h->max_splits);
+}
+
+// The default policy's chunk size, from the batch's shape alone (rows, kv
+// heads, the context capacity max_keys, the SM count): about three items per
+// persistent CTA if contexts were half full, between chunk_min (512 KiB of
+// K+V per kv head) and four times that.  Fewer, larger items mean fewer item
+// boundaries and split merges; a small batch still gets the splits it needs
+// to fill the GPU.
+uint32_t auto_chunk(const slotkv_s* h, uint32_t B, uint64_t max_keys) {
+    const uint32_t T = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+    const uint64_t lo = h->chunk_min, hi = 4ull * h->chunk_min;
+    const uint64_t ctas = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
+    uint64_t c = (uint64_t)B * h->n_kv_head * (max_keys / 2) / (3 * ctas);
+    c = c / T * T;
+    return (uint32_t)(c < lo ? lo : (c > hi ? hi : c));
 }
 
 int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float* k_new,
@@ -193,15 +209,16 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.n_head = n_head;
     P.n_kv_head = h->n_kv_head;
     P.B = B;
-    P.chunk_min = h->chunk_min;
+    const uint64_t max_keys = block_tables ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
+    const uint32_t chunk = h->auto_split ? auto_chunk(h, B, max_keys) : h->chunk_min;
+    P.chunk_min = chunk;
     P.max_splits = h->max_splits;
     P.eps = eps;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.flags = h->options;
     const int G = (int)(n_head / h->n_kv_head);
     // persistent CTAs: two per SM, never more than there can be work items
-    const uint64_t max_keys = block_tables ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
-    const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h, max_keys);
+    const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h, max_keys, chunk);
     const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
     const unsigned ctas = (unsigned)(most < want ? most : want);
     // slot mode: each CTA's first item is split 0 of one (row, kv head) pair
@@ -522,6 +539,7 @@ int slot_kv_set_split(slotkv_t h, uint32_t min_chunk_keys, uint32_t max_splits) 
     if (e != cudaSuccess) return cuda_fail(e, "synchronize");
     h->chunk_min = min_chunk_keys;
     h->max_splits = max_splits;
+    h->auto_split = false;
     return alloc_workspace(h);
 }
 

@@ -53,10 +53,11 @@ def test_slot_kv_smoke_offsets_and_no_overlap():
         kv.free()
 
 
-@pytest.mark.parametrize("split", [None, (32, 8)])
+@pytest.mark.parametrize("split", [(512, 64), (32, 8)])
 def test_rows_are_independent_bit_exact(split):
-    """One B-row call equals B one-row calls bit for bit (the split depends
-    on the row's own position only), and permuting rows permutes outputs."""
+    """Under a fixed split policy one B-row call equals B one-row calls bit
+    for bit (the split depends on the row's own position only), and
+    permuting rows permutes outputs."""
     w = _wl()
     run = DeviceRun(w, split=split)
     try:
@@ -80,6 +81,47 @@ def test_rows_are_independent_bit_exact(split):
         outp = torch.full_like(full.cuda(), float("nan"))
         run.kv.decode_batch_attn(to_dev(q[perm]), to_dev(kn[perm]), to_dev(vn[perm]),
                                  to_dev(pos[perm].astype(np.int32)),
+                                 to_dev(run.slots_np[perm].astype(np.int32)), run.qw, run.kw,
+                                 run.inv, run.sinks, outp, w.eps, w.scale)
+        assert torch.equal(outp.cpu(), full[perm])
+        assert run.status() == 0
+    finally:
+        run.close()
+
+
+def test_default_policy_batch_and_alone():
+    """The default policy sizes chunks from the batch's shape: a 64-row batch
+    (8 kv heads, 4096-key slots) runs larger chunks than one row alone.  Each
+    row alone then agrees with its row of the batch within tolerance, and a
+    permutation of the batch (same size, same chunks) permutes the outputs
+    bit for bit."""
+    B = 64
+    rng = np.random.default_rng(310)
+    pos = tuple(int(x) for x in rng.integers(0, 4096, size=B))
+    w = synth.Workload("sem_auto", 310, B=B, n_slots=B, slot_ctx=4096, n_head=32, n_kv_head=8,
+                       head_dim=128, theta=1e6, sinks=True, pos_rule="fixed",
+                       fixed_positions=pos, slot_rule="perm")
+    run = DeviceRun(w)
+    try:
+        q, kn, vn, p = run.inputs(0)
+        K0, V0 = run.K.clone(), run.V.clone()
+        full = run.step(0).cpu()
+        rows = [int(np.argmax(p)), int(np.argmin(p)), 5, 17, 40]
+        for b in rows:
+            run.K.copy_(K0)
+            run.V.copy_(V0)
+            out1 = torch.full((1, w.n_head, w.head_dim), float("nan"), device="cuda")
+            run.kv.decode_batch_attn(to_dev(q[b:b + 1]), to_dev(kn[b:b + 1]),
+                                     to_dev(vn[b:b + 1]), to_dev(p[b:b + 1].astype(np.int32)),
+                                     run.slots[b:b + 1].contiguous(), run.qw, run.kw, run.inv,
+                                     run.sinks, out1, w.eps, w.scale)
+            assert_close(out1.cpu().numpy()[0], full[b].numpy(), f"row {b} alone")
+        perm = rng.permutation(B)
+        run.K.copy_(K0)
+        run.V.copy_(V0)
+        outp = torch.full_like(full.cuda(), float("nan"))
+        run.kv.decode_batch_attn(to_dev(q[perm]), to_dev(kn[perm]), to_dev(vn[perm]),
+                                 to_dev(p[perm].astype(np.int32)),
                                  to_dev(run.slots_np[perm].astype(np.int32)), run.qw, run.kw,
                                  run.inv, run.sinks, outp, w.eps, w.scale)
         assert torch.equal(outp.cpu(), full[perm])
