@@ -864,6 +864,13 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
     volatile uint32_t* pend = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_PEND);
     // misc[0]: abort, misc[2]: tiles issued, misc[3]: items staged
 
+    // The producer's static first item needs its row's position and slot:
+    // issue those loads before anything else so they land during set-up.
+    uint32_t pre_p = 0, pre_slot = 0;
+    if (warp == C::WARP_TMA && blockIdx.x < P.static_items) {
+        pre_p = __ldg(P.positions + blockIdx.x / P.n_kv_head);
+        if (!P.block_tables) pre_slot = __ldg(P.slots + blockIdx.x / P.n_kv_head);
+    }
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(full0 + 8 * i, 1);
@@ -886,11 +893,6 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    for (int i = tid; i < HD; i += C::THREADS) {
-        qw_s[i] = P.q_norm_w[i];
-        kw_s[i] = P.k_norm_w[i];
-        if (i < HD / 2) if_s[i] = P.inv_freq[i];
-    }
     __syncthreads();
 
     if (warp >= W) {
@@ -900,6 +902,31 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         // its slot as soon as the consumers release that slot (they finish item
         // k-1), while item k's tiles are still streaming, so the prep warp has
         // item k+1 ready before the consumers reach it.
+        // Paged mode: the whole producer warp checks the static first item's
+        // row the way the plan does (p within the table, every used entry in
+        // the pool) and finds the row of key p.
+        uint32_t pg_ok = 0, pg_prow = 0;
+        if (warp == C::WARP_TMA && P.block_tables != nullptr && blockIdx.x < P.static_items) {
+            const uint32_t* tab =
+                P.block_tables + static_cast<size_t>(blockIdx.x / P.n_kv_head) * P.bt_stride;
+            bool bad = static_cast<uint64_t>(pre_p) >=
+                       static_cast<uint64_t>(P.bt_stride) * P.slot_ctx;
+            const uint32_t used = bad ? 0u : pre_p / P.slot_ctx + 1;
+            for (uint32_t i0 = 0; i0 < used; i0 += 128) {
+                uint32_t id[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t i = i0 + u * 32 + lane;
+                    id[u] = i < used ? __ldg(tab + i) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) bad |= id[u] >= P.n_slots;
+            }
+            if (!__any_sync(0xffffffffu, bad)) {
+                pg_ok = 1;
+                pg_prow = __ldg(tab + pre_p / P.slot_ctx) * P.slot_ctx + pre_p % P.slot_ctx;
+            }
+        }
         if (warp == C::WARP_TMA && lane == 0) {
             const uint4* recs = reinterpret_cast<const uint4*>(P.items);
             const bool paged = P.block_tables != nullptr;
@@ -973,13 +1000,19 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             // first item: CTA c < static_items owns split 0 of (row, kv head)
             // pair c.  Its inputs come from work that precedes the plan kernel
             // on the stream, so they are complete; the plan checks the row the
-            // same way and leaves the item out of its list.
+            // same way and leaves the item out of its list.  (The loads of p and
+            // the slot were issued at kernel entry.)
             uint4 rec = make_uint4(0, 0, 0, 0);
             bool first_ok = false;
             if (blockIdx.x < P.static_items) {
                 const uint32_t b = blockIdx.x / P.n_kv_head, kvh = blockIdx.x % P.n_kv_head;
-                const uint32_t p = __ldg(P.positions + b), slot = __ldg(P.slots + b);
-                if (slot < P.n_slots && p < P.slot_ctx) {
+                const uint32_t p = pre_p, slot = pre_slot;
+                if (paged) {
+                    if (pg_ok) {
+                        rec = make_uint4(pack_item(b, 0, kvh), p, pg_prow, 0u);
+                        first_ok = true;
+                    }
+                } else if (slot < P.n_slots && p < P.slot_ctx) {
                     rec = make_uint4(pack_item(b, 0, kvh), p, slot * P.slot_ctx + p, 0u);
                     first_ok = true;
                 }
@@ -1076,6 +1109,26 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         // (pre-scaled by scale*log2 e) and, in the split owning key p, k_new.
         if (warp == C::WARP_PREP) {
             constexpr int PPL = HD / 64;  // rotation pairs per lane
+            // the norm weights and inverse frequencies, used by this warp only:
+            // every load in flight at once, then the stores
+            {
+                float wq[HD / 32], wk[HD / 32], wf[HD / 64];
+#pragma unroll
+                for (int j = 0; j < HD / 32; ++j) {
+                    wq[j] = __ldg(P.q_norm_w + lane + 32 * j);
+                    wk[j] = __ldg(P.k_norm_w + lane + 32 * j);
+                }
+#pragma unroll
+                for (int j = 0; j < HD / 64; ++j) wf[j] = __ldg(P.inv_freq + lane + 32 * j);
+#pragma unroll
+                for (int j = 0; j < HD / 32; ++j) {
+                    qw_s[lane + 32 * j] = wq[j];
+                    kw_s[lane + 32 * j] = wk[j];
+                }
+#pragma unroll
+                for (int j = 0; j < HD / 64; ++j) if_s[lane + 32 * j] = wf[j];
+            }
+            __syncwarp();
             for (uint32_t k = 0;; ++k) {
                 const uint32_t is = k & 1;
                 if (!mbar_wait(staged0 + 8 * is, (k >> 1) & 1)) {

@@ -40,7 +40,7 @@ struct DecodeParams {
     // slot_ctx is then a multiple of the tile height.  slots is unused.
     const uint32_t* block_tables = nullptr;
     uint32_t bt_stride = 0;
-    // Static first items (slot mode): decode CTA c < static_items starts with
+    // Static first items: decode CTA c < static_items starts with
     // split 0 of (row c / n_kv_head, kv head c % n_kv_head) without waiting for
     // the plan, which leaves those items out of its list.  0: none.
     uint32_t static_items = 0;

@@ -221,9 +221,9 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h, max_keys, chunk);
     const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
     const unsigned ctas = (unsigned)(most < want ? most : want);
-    // slot mode: each CTA's first item is split 0 of one (row, kv head) pair
+    // each CTA's first item is split 0 of one (row, kv head) pair
     const uint64_t pairs = (uint64_t)B * h->n_kv_head;
-    P.static_items = block_tables ? 0u : (unsigned)(pairs < ctas ? pairs : ctas);
+    P.static_items = (unsigned)(pairs < ctas ? pairs : ctas);
     int rc;
     switch (h->head_dim) {
         case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, ctas, stream); break;
