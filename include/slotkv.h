@@ -340,12 +340,22 @@ int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_spl
  *   SLOTKV_OPT_VNORM          normalise v_new with a weightless RMS norm
  *                             (x / sqrt(mean(x^2) + eps)) before it is cached
  *                             and attended;
- *   SLOTKV_OPT_NORM_PLUS_ONE  apply the Q and K norm weights as (1 + w).
+ *   SLOTKV_OPT_NORM_PLUS_ONE  apply the Q and K norm weights as (1 + w);
+ *   SLOTKV_OPT_TEST_STALL     for testing the failure path only: the first
+ *                             work item of every CTA is never marked ready,
+ *                             so the consumers' bounded wait expires (after
+ *                             about a second), every CTA abandons its work
+ *                             and the call ends with SLOTKV_DEV_TIMEOUT set,
+ *                             having written nothing.  The context stays
+ *                             usable; clear the flags with
+ *                             slot_kv_get_status and the option with
+ *                             slot_kv_set_options(handle, 0).
  * 0 (the default) is the plain form of decode_batch_attn.  SLOTKV_ERR_ARG for
  * unknown bits.  Host only; takes effect at the next call.
  */
 #define SLOTKV_OPT_VNORM 1u
 #define SLOTKV_OPT_NORM_PLUS_ONE 2u
+#define SLOTKV_OPT_TEST_STALL 0x80000000u
 int slot_kv_set_options(slotkv_t handle, uint32_t flags);
 
 /* slot_kv_last_error -- message for the calling thread's last failed call

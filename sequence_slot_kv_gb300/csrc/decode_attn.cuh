@@ -62,6 +62,7 @@ constexpr uint32_t kDevRange = 1u;
 constexpr uint32_t kDevTimeout = 2u;
 constexpr uint32_t kOptVNorm = 1u;        // SLOTKV_OPT_VNORM
 constexpr uint32_t kOptNormPlusOne = 2u;  // SLOTKV_OPT_NORM_PLUS_ONE
+constexpr uint32_t kOptTestStall = 0x80000000u;  // SLOTKV_OPT_TEST_STALL
 constexpr int kPlanThreads = 1024;
 
 __host__ __device__ constexpr int pow2_floor(int x) {
@@ -936,8 +937,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             bool planned = false;
             uint32_t n_items = 0;
             auto await_plan = [&]() {
-                grid_dependency_wait();
-                n_items = __ldcg(P.plan);
+                if (!P.no_plan) {
+                    grid_dependency_wait();
+                    n_items = __ldcg(P.plan);
+                }
                 planned = true;
             };
             // stage item k from record `rec` (or the end marker); in paged mode
@@ -1016,6 +1019,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     rec = make_uint4(pack_item(b, 0, kvh), p, slot * P.slot_ctx + p, 0u);
                     first_ok = true;
                 }
+                // without a plan kernel, the range flag is raised here
+                if (!first_ok && P.no_plan) atomicOr(P.status, kDevRange);
             }
             if (!first_ok) {
                 await_plan();
@@ -1065,7 +1070,9 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                                 full);
                     misc[2] = static_cast<int>(tile_g + 1);
                     if (!planned) {
-                        if (t + 1 >= static_cast<uint32_t>(S) || t + 1 == cur_nt) {
+                        // the plan is needed only to stage the next item: wait
+                        // for it a few tiles in, by when it has long finished
+                        if (t + 1 >= 8u || t + 1 == cur_nt) {
                             await_plan();
                             it_n = atomicAdd(P.plan + 1, 1u);
                         }
@@ -1155,7 +1162,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                         warp_rms_norm_plain<HD>(vbuf + is * HD, vbuf + is * HD, P.eps, lane);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(prepared0 + 8 * is);
+                // (the failure-path test option withholds the first item, so
+                // the consumers' bounded wait runs out)
+                if (lane == 0 && !(k == 0 && (P.flags & kOptTestStall)))
+                    mbar_arrive(prepared0 + 8 * is);
                 if (end) break;
             }
         }
@@ -1640,9 +1650,12 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
         const uint32_t warps = p.B * p.n_kv_head;
         slotkv_write_kv_kernel<HD><<<(warps + 3) / 4, 128, 0, stream>>>(p);
     }
-    slotkv_plan_kernel<C::T><<<1, kPlanThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return static_cast<int>(e);
+    cudaError_t e;
+    if (!p.no_plan) {
+        slotkv_plan_kernel<C::T><<<1, kPlanThreads, 0, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return static_cast<int>(e);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(C::THREADS);
@@ -1652,7 +1665,7 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.no_plan ? 0 : 1;  // programmatic dependent of the plan kernel
     e = cudaLaunchKernelEx(&cfg, slotkv_decode_attn_kernel<HD, G>, tmK, tmV, p);
     return static_cast<int>(e);
 }

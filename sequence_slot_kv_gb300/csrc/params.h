@@ -44,6 +44,10 @@ struct DecodeParams {
     // split 0 of (row c / n_kv_head, kv head c % n_kv_head) without waiting for
     // the plan, which leaves those items out of its list.  0: none.
     uint32_t static_items = 0;
+    // 1: every item is a static first item (no more (row, kv head) pairs than
+    // CTAs, one split each): no plan kernel runs, its list is empty, and the
+    // decode kernel is launched in plain stream order.
+    uint32_t no_plan = 0;
 };
 
 // Keys per split chunk for a row with n_keys keys (p + 1).  Depends only on

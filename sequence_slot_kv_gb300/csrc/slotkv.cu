@@ -218,12 +218,15 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.flags = h->options;
     const int G = (int)(n_head / h->n_kv_head);
     // persistent CTAs: two per SM, never more than there can be work items
-    const uint64_t most = (uint64_t)B * h->n_kv_head * grid_splits(h, max_keys, chunk);
+    const uint32_t gsplits = grid_splits(h, max_keys, chunk);
+    const uint64_t most = (uint64_t)B * h->n_kv_head * gsplits;
     const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
     const unsigned ctas = (unsigned)(most < want ? most : want);
-    // each CTA's first item is split 0 of one (row, kv head) pair
+    // each CTA's first item is split 0 of one (row, kv head) pair; when that
+    // covers every item (one split per row, a CTA per pair) no plan is needed
     const uint64_t pairs = (uint64_t)B * h->n_kv_head;
     P.static_items = (unsigned)(pairs < ctas ? pairs : ctas);
+    P.no_plan = (gsplits == 1 && pairs <= ctas) ? 1u : 0u;
     int rc;
     switch (h->head_dim) {
         case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, ctas, stream); break;
@@ -522,7 +525,7 @@ int slot_kv_get_status(slotkv_t h, slotkv_stream_t stream, uint32_t* flags) {
 int slot_kv_set_options(slotkv_t h, uint32_t flags) {
     g_err[0] = 0;
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
-    if (flags & ~(SLOTKV_OPT_VNORM | SLOTKV_OPT_NORM_PLUS_ONE))
+    if (flags & ~(SLOTKV_OPT_VNORM | SLOTKV_OPT_NORM_PLUS_ONE | SLOTKV_OPT_TEST_STALL))
         return fail(SLOTKV_ERR_ARG, "unknown option bits 0x%x", flags);
     h->options = flags;
     return SLOTKV_OK;
