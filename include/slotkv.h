@@ -150,11 +150,14 @@ int slot_kv_geometry(slotkv_t handle, uint32_t* n_slots, uint32_t* slot_ctx,
  *   inv_freq    device, [hd/2].      sinks     device [n_head], or NULL.
  *   out         device, [B][n_head][hd]; written for every in-range row.
  *   eps         RMS-norm epsilon.    scale     softmax scale (e.g. 1/sqrt(hd)).
+ * q, k_new, v_new and out must be 16-byte aligned (the kernel stages them with
+ * bulk copies and writes out in 16-byte stores), the other arrays 4-byte
+ * aligned.
  *
  * Out-of-range rows (slots[b] >= n_slots or positions[b] >= slot_ctx, the
  * decodeBatch precondition) are skipped on the device and raise
- * SLOTKV_DEV_RANGE.  Host-side errors: SLOTKV_ERR_ARG (NULL pointer, B or
- * n_head too large, n_head not a multiple of n_kv_head),
+ * SLOTKV_DEV_RANGE.  Host-side errors: SLOTKV_ERR_ARG (NULL or misaligned
+ * pointer, B or n_head too large, n_head not a multiple of n_kv_head),
  * SLOTKV_ERR_UNSUPPORTED (G outside 1..8), SLOTKV_ERR_CUDA (launch failure).
  */
 int decode_batch_attn(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
@@ -226,11 +229,16 @@ int decode_batch_attn_paged(slotkv_t handle, uint32_t B, uint32_t n_head, const 
 /*
  * decode_batch_attn_host -- decode_batch_attn for callers whose per-step
  * inputs and output live in host memory.  q, k_new, v_new, positions, slots
- * and out are HOST pointers with the layouts above (pinned memory gives
- * asynchronous copies); q_norm_w, k_norm_w, inv_freq and sinks stay device
- * pointers (resident parameters).  The call copies the inputs into
- * handle-owned device staging buffers on `stream`, runs the step, copies out
- * back and synchronises `stream` before returning, so out is ready on return.
+ * and out are HOST pointers with the layouts above; q_norm_w, k_norm_w,
+ * inv_freq and sinks stay device pointers (resident parameters).  The call
+ * moves the inputs into handle-owned device staging buffers on `stream`,
+ * runs the step, moves out back and synchronises `stream` before returning,
+ * so out is ready on return.  When all six host buffers are page-locked
+ * (pinned, hence mapped into the device's address space) one copy kernel
+ * gathers the inputs over the host link and the step writes out straight into
+ * host memory (through a second copy kernel if out is not 16-byte aligned);
+ * otherwise each buffer is copied with cudaMemcpyAsync.  Host buffers need only 4-byte
+ * alignment.
  * Errors as decode_batch_attn, plus SLOTKV_ERR_CUDA for a failed copy.
  */
 int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,

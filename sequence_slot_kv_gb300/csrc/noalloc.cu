@@ -74,6 +74,11 @@ extern "C" int decode_batch_attn_noalloc(
         return noalloc_fail(SLOTKV_ERR_ARG, "null tensor pointer");
     if (((uintptr_t)K & 15) || ((uintptr_t)V & 15))
         return noalloc_fail(SLOTKV_ERR_ARG, "K and V must be 16-byte aligned");
+    if (((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)out) & 15)
+        return noalloc_fail(SLOTKV_ERR_ARG, "q, k_new, v_new and out must be 16-byte aligned");
+    if (((uintptr_t)positions | (uintptr_t)slots | (uintptr_t)q_norm_w | (uintptr_t)k_norm_w |
+         (uintptr_t)inv_freq | (uintptr_t)sinks) & 3)
+        return noalloc_fail(SLOTKV_ERR_ARG, "tensor pointers must be 4-byte aligned");
     if (n_slots == 0 || slot_ctx == 0 || n_kv_head == 0)
         return noalloc_fail(SLOTKV_ERR_ARG, "n_slots, slot_ctx and n_kv_head must be >= 1");
     if (head_dim != 64 && head_dim != 128 && head_dim != 256)

@@ -241,7 +241,7 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
 int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
                       const void* k_new, const void* v_new, const void* positions,
                       const void* slots, const void* q_norm_w, const void* k_norm_w,
-                      const void* inv_freq, const void* out) {
+                      const void* inv_freq, const void* out, bool device_ptrs = true) {
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
     if (B > h->max_rows) return fail(SLOTKV_ERR_ARG, "B=%u exceeds max_rows=%u", B, h->max_rows);
     if (n_head == 0 || n_head % h->n_kv_head != 0)
@@ -255,6 +255,14 @@ int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
     if (!q || !k_new || !v_new || !positions || !slots || !q_norm_w || !k_norm_w || !inv_freq ||
         !out)
         return fail(SLOTKV_ERR_ARG, "null tensor pointer");
+    if (((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)positions |
+         (uintptr_t)slots | (uintptr_t)q_norm_w | (uintptr_t)k_norm_w | (uintptr_t)inv_freq |
+         (uintptr_t)out) & 3)
+        return fail(SLOTKV_ERR_ARG, "tensor pointers must be 4-byte aligned");
+    // the kernel stages q, k_new and v_new with bulk copies and writes out in
+    // 16-byte stores
+    if (device_ptrs && (((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)out) & 15))
+        return fail(SLOTKV_ERR_ARG, "q, k_new, v_new and out must be 16-byte aligned");
     return SLOTKV_OK;
 }
 
@@ -262,6 +270,37 @@ int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
 
 namespace slotkv {
 void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
+// Copies up to kMaxSegs byte ranges (each a multiple of 4 bytes) with one
+// grid: the host entry's inputs from pinned host memory (mapped into the
+// device's address space) to device staging, or its output back.  16-byte
+// accesses where a segment allows them.
+constexpr int kMaxSegs = 6;
+struct CopySegs {
+    const uint8_t* src[kMaxSegs];
+    uint8_t* dst[kMaxSegs];
+    size_t bytes[kMaxSegs];
+    int n;
+};
+
+__global__ void copy_segments_kernel(const CopySegs c) {
+    const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t nth = (size_t)gridDim.x * blockDim.x;
+    for (int k = 0; k < c.n; ++k) {
+        const uint8_t* src = c.src[k];
+        uint8_t* dst = c.dst[k];
+        const size_t bytes = c.bytes[k];
+        if ((((uintptr_t)src | (uintptr_t)dst | bytes) & 15) == 0) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(src);
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            for (size_t i = tid; i < bytes / 16; i += nth) d4[i] = s4[i];
+        } else {
+            const uint32_t* s1 = reinterpret_cast<const uint32_t*>(src);
+            uint32_t* d1 = reinterpret_cast<uint32_t*>(dst);
+            for (size_t i = tid; i < bytes / 4; i += nth) d1[i] = s1[i];
+        }
+    }
+}
 
 __global__ void advance_positions_kernel(uint32_t* __restrict__ pos, uint32_t B,
                                          uint32_t delta) {
@@ -464,13 +503,60 @@ int decode_batch_attn_host(slotkv_t h, uint32_t B, uint32_t n_head, const float*
                            float* out, float eps, float scale, slotkv_stream_t stream) {
     g_err[0] = 0;
     int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, slots, q_norm_w,
-                               k_norm_w, inv_freq, out);
+                               k_norm_w, inv_freq, out, false);
     if (rc != SLOTKV_OK || B == 0) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
     const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
     const size_t ni = (size_t)B * sizeof(uint32_t);
     cudaError_t e;
+    // Pinned host buffers are mapped into the device's address space: one
+    // copy kernel gathers the inputs over the host link and one returns the
+    // output, instead of six small copy-engine transfers.
+    const void* hp[6] = {q, k_new, v_new, positions, slots, out};
+    void* dp[6];
+    bool mapped = true;
+    for (int i = 0; i < 6 && mapped; ++i) {
+        cudaPointerAttributes at;
+        mapped = cudaPointerGetAttributes(&at, hp[i]) == cudaSuccess &&
+                 at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
+        dp[i] = mapped ? at.devicePointer : nullptr;
+    }
+    cudaGetLastError();  // a failed attribute query leaves an error behind
+    if (mapped) {
+        const int threads = 256;
+        const unsigned grid = (unsigned)(h->sm_count > 0 ? h->sm_count : 1);
+        slotkv::CopySegs in{};
+        void* st[5] = {h->st_q, h->st_k, h->st_v, h->st_pos, h->st_slots};
+        const size_t nb[5] = {nq, nk, nk, ni, ni};
+        for (int i = 0; i < 5; ++i) {
+            in.src[i] = static_cast<const uint8_t*>(dp[i]);
+            in.dst[i] = static_cast<uint8_t*>(st[i]);
+            in.bytes[i] = nb[i];
+        }
+        in.n = 5;
+        slotkv::copy_segments_kernel<<<grid, threads, 0, s>>>(in);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "input gather launch");
+        // an aligned out is written by the decode kernel itself, over the link
+        const bool direct_out = ((uintptr_t)dp[5] & 15) == 0;
+        rc = launch(h, B, n_head, h->st_q, h->st_k, h->st_v, h->st_pos, h->st_slots, q_norm_w,
+                    k_norm_w, inv_freq, sinks, direct_out ? static_cast<float*>(dp[5]) : h->st_out,
+                    eps, scale, s);
+        if (rc != SLOTKV_OK) return rc;
+        if (direct_out) {
+            if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+            return SLOTKV_OK;
+        }
+        slotkv::CopySegs outc{};
+        outc.src[0] = reinterpret_cast<const uint8_t*>(h->st_out);
+        outc.dst[0] = static_cast<uint8_t*>(dp[5]);
+        outc.bytes[0] = nq;
+        outc.n = 1;
+        slotkv::copy_segments_kernel<<<grid, threads, 0, s>>>(outc);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "output scatter launch");
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+        return SLOTKV_OK;
+    }
     if ((e = cudaMemcpyAsync(h->st_q, q, nq, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (e = cudaMemcpyAsync(h->st_k, k_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (e = cudaMemcpyAsync(h->st_v, v_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||

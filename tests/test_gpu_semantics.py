@@ -193,23 +193,44 @@ def test_zero_rows_is_a_no_op():
         run.close()
 
 
-def test_host_entry_equals_device_entry():
+def _host_tensor(a, kind):
+    """A host copy of array a: pinned, pageable, or pinned but starting one
+    element into its allocation (4-byte aligned only)."""
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if kind == "pageable":
+        return t.clone()
+    if kind == "pinned":
+        return t.pin_memory()
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype).pin_memory()
+    view = buf[1:].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+@pytest.mark.parametrize("kind", ["pinned", "pageable", "pinned_offset"])
+def test_host_entry_equals_device_entry(kind):
+    """decode_batch_attn_host equals the device entry bit for bit, whether
+    its buffers are pinned (gathered and returned by copy kernels over the
+    host link), pageable (copy-engine transfers), or pinned at an address
+    that allows only 4-byte accesses."""
     w = _wl(idx=304)
     run = DeviceRun(w)
     try:
         K0, V0 = run.K.clone(), run.V.clone()
         dev = run.step(0).cpu()
-        Kd = run.K.clone()
-        run.K.copy_(K0)
-        run.V.copy_(V0)
-        q, kn, vn, pos = run.inputs(0)
-        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-        out_h = torch.full((w.B, w.n_head, w.head_dim), float("nan")).pin_memory()
-        run.kv.decode_batch_attn_host(pin(q), pin(kn), pin(vn), pin(pos.astype(np.int32)),
-                                      pin(run.slots_np.astype(np.int32)), run.qw, run.kw,
-                                      run.inv, run.sinks, out_h, w.eps, w.scale)
-        assert torch.equal(out_h, dev)
-        assert torch.equal(run.K, Kd)
+        Kd, Vd = run.K.clone(), run.V.clone()
+        for rep in range(2):
+            run.K.copy_(K0)
+            run.V.copy_(V0)
+            q, kn, vn, pos = run.inputs(0)
+            h = lambda a: _host_tensor(a, kind)  # noqa: E731
+            out_h = h(np.full((w.B, w.n_head, w.head_dim), np.nan, dtype=np.float32))
+            run.kv.decode_batch_attn_host(h(q), h(kn), h(vn), h(pos.astype(np.int32)),
+                                          h(run.slots_np.astype(np.int32)), run.qw, run.kw,
+                                          run.inv, run.sinks, out_h, w.eps, w.scale)
+            assert torch.equal(out_h, dev), f"{kind} call {rep}"
+            assert torch.equal(run.K, Kd) and torch.equal(run.V, Vd)
+        assert run.status() == 0
     finally:
         run.close()
 
@@ -259,6 +280,26 @@ def test_argument_errors():
             rc = skv._lib.decode_batch_attn(run.kv._h, w.B, w.n_head, 1, 1, 1, 1, 1, 1, 1, 1,
                                             None, None, w.eps, w.scale, None)
             skv._check(rc, "decode_batch_attn")
+        # a q, k_new, v_new or out that is not 16-byte aligned is refused on
+        # the host (the kernel's bulk copies and 16-byte stores need it)
+        def misaligned(a):
+            base = torch.empty(a.size + 4, dtype=torch.float32, device="cuda")
+            view = base[1:1 + a.size].view(a.shape)
+            view.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+            return view
+        args = [to_dev(q), to_dev(kn), to_dev(vn), to_dev(pos.astype(np.int32)), run.slots,
+                run.qw, run.kw, run.inv, None, out, w.eps, w.scale]
+        for i, a in ((0, q), (1, kn), (2, vn), (9, np.zeros(out.shape, np.float32))):
+            bad = list(args)
+            bad[i] = misaligned(a)
+            with pytest.raises(skv.SlotKVError) as ei:
+                run.kv.decode_batch_attn(*bad)
+            assert ei.value.code == 1 and "aligned" in str(ei.value)
+        with pytest.raises(skv.SlotKVError) as ei:
+            skv.decode_batch_attn_noalloc(run.K, run.V, misaligned(q), to_dev(kn), to_dev(vn),
+                                          to_dev(pos.astype(np.int32)), run.slots, run.qw,
+                                          run.kw, run.inv, None, out, w.eps, w.scale)
+        assert ei.value.code == 1 and "aligned" in str(ei.value)
         with pytest.raises(skv.SlotKVError):
             run.kv.set_split(5, 8)                       # not a multiple of the tile
         h = ctypes.c_void_p()
