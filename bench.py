@@ -38,7 +38,7 @@ HBM_FALLBACK_GBS = 6800.0
 # the kernel source it was taken on (sha256 prefix of decode_attn.cuh); see
 # profiles/decode_attn_<workload>.md.
 MEASURED_TRAFFIC = {
-    "b37deefa27a8f440": {"mid": 555_808_256, "sinks": 2_342_700_288},
+    "e6c1eed1e9aa80c9": {"mid": 555_917_056, "sinks": 2_342_451_456},
 }
 
 
