@@ -173,11 +173,13 @@ class OracleSample:
     history is regenerated on the host once, outside any timing; the oracle
     rewrites the same K/V rows on every call, so calls repeat exactly."""
 
-    def __init__(self, w, n_threads):
+    def __init__(self, w, n_threads, flags=0, paged_bs=0):
         import oracle
         self.o = oracle.default()
         self.w = w
         self.n_threads = n_threads
+        self.flags = flags
+        self.paged_bs = paged_bs
         # rows at evenly spaced quantiles of position, so the sample has the
         # workload's mix of history lengths
         k = min(w.B, n_threads)
@@ -185,27 +187,60 @@ class OracleSample:
         self.rows = sorted(int(order[int(i)]) for i in
                            np.linspace(0, w.B - 1, k).round().astype(int))
         r = self.rows
-        self.K, self.V = oracle_sample(w, r, n_threads)
+        if paged_bs:
+            # the sampled rows' blocks only, in a compact pool, with tables into it
+            self.K, self.V, addr = paged_oracle_sample(w, r, paged_bs)
+        else:
+            self.K, self.V = oracle_sample(w, r, n_threads)
+            addr = np.arange(len(r), dtype=np.uint32)
         self.args = (w.q(0)[r], w.k_new(0)[r], w.v_new(0)[r], w.positions(0)[r],
-                     np.arange(len(r), dtype=np.uint32), w.q_norm_w(), w.k_norm_w(),
+                     addr, w.q_norm_w(), w.k_norm_w(),
                      w.inv_freq(), w.sink_logits(), w.eps, w.scale)
 
     def step(self):
         t0 = time.perf_counter()
-        self.o.decode_batch(self.K, self.V, *self.args, n_threads=self.n_threads)
+        if self.paged_bs:
+            self.o.decode_batch_paged(self.K, self.V, *self.args, n_threads=self.n_threads,
+                                      flags=self.flags)
+        else:
+            self.o.decode_batch(self.K, self.V, *self.args, n_threads=self.n_threads,
+                                flags=self.flags)
         return time.perf_counter() - t0
 
     def describe(self, steps, seconds):
         pos = self.w.positions(0)[self.rows]
+        how = (f" over {self.paged_bs}-key blocks" if self.paged_bs else "") + \
+              (f", norm options {self.flags}" if self.flags else "")
         return (f"{len(self.rows)} rows (positions {pos.min()}..{pos.max()}, mean "
                 f"{pos.mean():.0f}) of the {self.w.name} workload's "
-                f"first step per oracle call, {steps} calls, {seconds:.1f} s, rows split "
+                f"first step per oracle call{how}, {steps} calls, {seconds:.1f} s, rows split "
                 f"over {self.n_threads} threads")
 
 
-def time_oracle(w, budget_s, n_threads):
+def paged_oracle_sample(w, rows, bs):
+    """Compact host block pool holding only the blocks of ``rows``, and their
+    tables into it (untimed set-up)."""
+    slots = w.slots()
+    p = w.positions(0)
+    used = [int(p[r]) // bs + 1 for r in rows]
+    K = np.empty((sum(used), bs, w.n_kv_head, w.head_dim), dtype=np.float32)
+    V = np.empty_like(K)
+    tab = np.zeros((len(rows), max(used)), dtype=np.uint32)
+    base = 0
+    for i, r in enumerate(rows):
+        n = used[i]
+        K[base:base + n] = w.hist_rows("k", slots[r], 0, n * bs).reshape(n, bs, w.n_kv_head,
+                                                                        w.head_dim)
+        V[base:base + n] = w.hist_rows("v", slots[r], 0, n * bs).reshape(n, bs, w.n_kv_head,
+                                                                        w.head_dim)
+        tab[i, :n] = np.arange(base, base + n, dtype=np.uint32)
+        base += n
+    return K, V, tab
+
+
+def time_oracle(w, budget_s, n_threads, flags=0, paged_bs=0):
     """rows/s of the oracle over calls on its sample until ``budget_s``."""
-    smp = OracleSample(w, n_threads)
+    smp = OracleSample(w, n_threads, flags, paged_bs)
     smp.step()                                       # warm caches and pages
     calls, spent = 0, 0.0
     while spent < budget_s:
@@ -236,6 +271,12 @@ def run_reference(args, w):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# the library's and the oracle's option bits agree: 1 weightless V norm,
+# 2 (1 + w) norm weights
+OPTION_NAMES = {1: "weightless V norm", 2: "(1 + w) Q/K norm weights",
+                3: "weightless V norm and (1 + w) Q/K norm weights"}
 
 
 def config_of(w):
@@ -290,6 +331,8 @@ def run_gpu(args, w):
                         k_buf=K, v_buf=V)
     if args.split:
         kv.set_split(*args.split)
+    if args.options:
+        kv.set_options(args.options)
 
     qw, kw, inv = dev_t(w.q_norm_w()), dev_t(w.k_norm_w()), dev_t(w.inv_freq())
     sinks = None if not w.sinks else dev_t(w.sink_logits())
@@ -426,11 +469,12 @@ def run_gpu(args, w):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(config_of(w), **({"kv_layout": "paged", "block_size": bs,
                                           "block_order": "seeded shuffle over the pool"}
-                                         if bs else {})),
+                                         if bs else {}),
+                       **({"norm_options": OPTION_NAMES[args.options]} if args.options else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": args.traffic if args.traffic is not None
-                     else (None if bs else measured_traffic(w.name)),
+                     else (None if bs or args.options else measured_traffic(w.name)),
                      "alg_bytes_per_launch": alg_bytes,
                      "avg_launch_us": avg_launch_s * 1e6,
                      "kernel": "slotkv_decode_attn_kernel"},
@@ -443,7 +487,7 @@ def run_gpu(args, w):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        v, desc = time_oracle(w, args.cpu_budget, cores)
+        v, desc = time_oracle(w, args.cpu_budget, cores, flags=args.options, paged_bs=bs)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
     if rank == 0:
@@ -500,6 +544,11 @@ def run_prefill(args):
     # bytes as the path reads them: every token reads its own keys 0..pos
     per_token_bytes = int((pos.astype(np.int64) + 1).sum()) * 2 * w.kv_dim * 4
     io = n_tok * (2 * w.n_head * w.head_dim + 4 * w.kv_dim) * 4
+    # The prefill is bound by f32 arithmetic: per token and query head, 2 hd
+    # flops per key for the score and 2 hd per key for the value sum.
+    flops = 4 * w.head_dim * w.n_head * int((pos.astype(np.int64) + 1).sum())
+    tflops = flops / (ms / 1e3) / 1e12
+    peak, peak_kind = alu_peak_f32(dev)
     line = {"metric": "slot-attn prefill tokens/s", "value": n_tok / (ms / 1e3),
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -507,11 +556,66 @@ def run_prefill(args):
             "config": {"workload": "prefill", "sequences": n_seq, "history": hist,
                        "prompt_chunk": chunk, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
                        "head_dim": w.head_dim},
+            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_kind": peak_kind, "traffic": None,
+                         "alg_flops_per_launch": flops, "avg_launch_us": ms * 1e3,
+                         "kernel": "slotkv_decode_attn_kernel (prefill mode)"},
             "key_bytes_read_per_step": per_token_bytes, "io_bytes_per_step": io,
             "effective_GBps": (per_token_bytes + io) / (ms / 1e3) / 1e9,
             "gpu_launches": args.steps * 3}
+    if not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        v, desc = time_oracle_prefill(w, slots, pos, n_seq, chunk, args.cpu_budget, cores)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     kv.free()
+
+
+def alu_peak_f32(dev):
+    """f32 FMA peak: SMs x 128 FP32 lanes x 2 flops x the maximum SM clock
+    (MEASURED_PEAKS.json's sm_max_mhz, else 2070 MHz), in TFLOP/s."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except (OSError, ValueError):
+        pass
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 FP32 lanes x 2 x {mhz:.0f} MHz"
+
+
+def time_oracle_prefill(w, slots, pos, n_seq, chunk, budget_s, n_threads):
+    """tokens/s of the oracle on the prefill workload: each call takes the next
+    token of every sequence (one decode step per token, in position order,
+    the sequences' tokens in parallel) on host copies of their slots, until
+    ``budget_s``."""
+    import oracle
+    o = oracle.default()
+    seq_slots = slots[::chunk].astype(np.int64)
+    first = pos[::chunk].astype(np.int64)
+    ctx = int(first.max()) + chunk
+    K = np.empty((n_seq, ctx, w.n_kv_head, w.head_dim), dtype=np.float32)
+    V = np.empty_like(K)
+    for i, s_ in enumerate(seq_slots):
+        K[i] = w.hist_rows("k", s_, 0, ctx)
+        V[i] = w.hist_rows("v", s_, 0, ctx)
+    q, kn, vn = w.q(), w.k_new(), w.v_new()
+    compact = np.arange(n_seq, dtype=np.uint32)
+    calls, spent = 0, 0.0
+    while spent < budget_s and calls < chunk:
+        rows = np.arange(n_seq) * chunk + calls
+        t0 = time.perf_counter()
+        o.decode_batch(K, V, q[rows], kn[rows], vn[rows], pos[rows].astype(np.uint32), compact,
+                       w.q_norm_w(), w.k_norm_w(), w.inv_freq(), w.sink_logits(), w.eps,
+                       w.scale, n_threads=min(n_threads, n_seq))
+        spent += time.perf_counter() - t0
+        calls += 1
+    desc = (f"the first {calls} prompt tokens of each of the {n_seq} sequences (one decode "
+            f"step per token, positions {int(first.min())}..{int(first.max()) + calls - 1}), "
+            f"{spent:.1f} s, the sequences split over {min(n_threads, n_seq)} threads")
+    return n_seq * calls / spent, desc
 
 
 def main():
@@ -527,6 +631,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="time batched causal prefill instead of the decode step")
+    ap.add_argument("--options", default="", choices=["", "vnorm", "plus_one", "both"],
+                    help="Gemma norm forms: weightless V norm, (1 + w) Q/K weights, or both")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
                     help="run the workload over a shuffled paged pool of this block size")
     ap.add_argument("--graph", action="store_true",
@@ -536,6 +642,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.options = {"": 0, "vnorm": 1, "plus_one": 2, "both": 3}[args.options]
     if args.prefill:
         run_prefill(args)
         return

@@ -2,48 +2,49 @@
 //
 // Work item = (row b, kv head g, split s): the keys [s*C, min((s+1)*C, p+1))
 // of slot slots[b] for the G query heads that share kv head g (GQA), so every
-// history K/V byte is read from HBM exactly once.  C depends only on the
-// row's own p (see split_chunk), never on the batch.
+// history K/V byte is read from HBM exactly once.  C comes from the split
+// policy (see split_chunk and the host's choice of chunk_min).
 //
-// Two kernels per call, on one stream:
+// Kernels per call, on one stream:
 //   * slotkv_plan_kernel (one CTA): checks every row's slot and position,
-//     lists the valid work items, largest first, and resets the hand-out
-//     counter;
+//     lists the valid work items, largest first (leaving out each CTA's
+//     static first item), and resets the hand-out counter.  Skipped when the
+//     static first items are all the work;
 //   * slotkv_decode_attn_kernel (persistent, 2 CTAs per SM, launched as a
-//     programmatic dependent of the plan): each CTA runs until the list is
-//     exhausted.  The steps of "Forward Cuda Gemma", decodeBatch, fused:
-//       - warp 4 (producer) takes items from the list and streams their
-//         history K and V tiles into a 3-stage shared-memory ring with 2-D
-//         TMA copies (cp.async.bulk.tensor, one [T keys x hd] box per tensor
-//         per stage) on mbarriers.  It runs ahead across item boundaries, so
-//         the stream does not stop while the consumers start or finish an item;
-//       - warps 0-3 (consumers), per item: per-head RMS norm + RoPE of the G
-//         query vectors (pre-scaled by scale*log2 e) and, in the split that
-//         holds key p, of k_new; then for each tile, groups of L lanes each
-//         take one key: every lane keeps E = hd/L elements of the G queries
-//         and of G output accumulators in registers, forms partial dots,
-//         reduces them with xor shuffles and runs a base-2 online softmax that
-//         rescales only when its running max grows;
+//     programmatic dependent of the plan): each CTA starts on its static
+//     first item -- split 0 of (row, kv head) pair blockIdx.x -- while the
+//     plan runs, then takes items from the list until it is exhausted.  The
+//     steps of "Forward Cuda Gemma", decodeBatch, fused:
+//       - warp 4 (producer) streams the items' history K and V tiles into a
+//         3-stage shared-memory ring with 2-D TMA copies (cp.async.bulk.tensor,
+//         one [T keys x hd] box per tensor per stage) on mbarriers, running
+//         ahead across item boundaries, and stages each item's q (and, in the
+//         split holding key p, k_new and v_new) one item ahead;
+//       - warp 5 (prep) applies per-head RMS norm + RoPE to the staged vectors
+//         (q pre-scaled by scale*log2 e);
+//       - warps 0-3 (consumers), per tile: groups of L lanes each take one
+//         key; every lane keeps E = hd/L elements of the G queries and of G
+//         output accumulators in registers, forms partial dots with packed
+//         f32x2 FMAs, reduces them over the group and runs a base-2 online
+//         softmax whose running max is raised lazily;
 //       - the split holding key p adds that key from shared memory (its K is
 //         the freshly normed+rotated k', its V the raw v_new) and writes both
-//         rows into the slot buffers at (slot*slot_ctx + p)*kv_dim (in
-//         paged mode, into key p's block);
-//       - the groups' (m, l, acc) merge by shuffles within each warp, then
+//         rows into the slot buffers at (slot*slot_ctx + p)*kv_dim (in paged
+//         mode, into key p's block);
+//       - the groups' (m, l, acc) merge by halving within each warp, then
 //         across the four warps in shared memory; a one-split row writes out,
-//         otherwise the partial goes to the workspace and the last CTA of the
-//         (row, kv head) to finish merges the splits in split order.
+//         otherwise the partial goes to the workspace and the last split of
+//         the (row, kv head) to finish is merged, in split order, by warp 6
+//         (merge) or, at the kernel's tail, by the consumers themselves.
+//   * slotkv_write_kv_kernel (prefill only, first): every token's K and V
+//     rows, before the attention reads them.
 //
 // Paged mode (DecodeParams::block_tables set): the buffers are a pool of
 // blocks and row b's key t sits in block block_tables[b][t / block_size].
 // Block sizes are multiples of T and tile starts are multiples of T, so each
 // tile lies inside one block: the producer only swaps the tile's first row
-// (looked up one tile ahead), and the plan checks every used table entry.
-//
-// Paged mode (DecodeParams::block_tables set): the buffers are a pool of
-// blocks and row b's key t sits in block block_tables[b][t / block_size].
-// Block sizes are multiples of T and tile starts are multiples of T, so each
-// tile lies inside one block: the producer only swaps the tile's first row
-// (looked up one tile ahead), and the plan checks every used table entry.
+// (looked up one tile ahead), and the plan (or, for a static first item, the
+// producer warp) checks every used table entry.
 //
 // Every wait on an mbarrier is bounded; on expiry the CTA raises
 // SLOTKV_DEV_TIMEOUT, drains its own copies in flight (bounded) and returns.
@@ -53,6 +54,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "params.h"
 
@@ -1620,8 +1623,13 @@ template <int HD, int G>
 int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                unsigned ctas, cudaStream_t stream) {
     using C = KCfg<HD, G>;
-    static bool configured = false;
-    if (!configured) {
+    // kernel attributes belong to each device's copy of the kernels: set them
+    // once per device (bit d of the mask; devices past 63 set them every time)
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!(configured.load(std::memory_order_acquire) & bit) || bit == 0) {
         cudaError_t e = cudaFuncSetAttribute(slotkv_decode_attn_kernel<HD, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return static_cast<int>(e);
@@ -1644,7 +1652,7 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
         e = cudaFuncGetAttributes(&fa, slotkv_decode_attn_kernel<HD, G>);
         if (e != cudaSuccess) return static_cast<int>(e);
         if (fa.numRegs != 128) return static_cast<int>(cudaErrorInvalidConfiguration);
-        configured = true;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     if (p.prefill) {
         const uint32_t warps = p.B * p.n_kv_head;
