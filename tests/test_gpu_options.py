@@ -48,6 +48,39 @@ def test_options_match_oracle(hd, name):
         run.close()
 
 
+@pytest.mark.parametrize("name", list(FLAGS))
+def test_options_paged(name):
+    """The options over the paged path (64-key blocks of a shuffled pool),
+    against the paged oracle with the same flags."""
+    from test_gpu_paged import PagedRun, host_pool, oracle_paged, written_mask
+    gflags, oflags = FLAGS[name]
+    hd, bs = 128, 64
+    T = 4096 // hd
+    pos = (0, 5, T + 1, bs, 3 * bs + 7, 6 * bs - 1)
+    w = synth.Workload(f"opt_paged_{name}", 620 + list(FLAGS).index(name), B=len(pos),
+                       n_slots=len(pos) + 2, slot_ctx=6 * bs, n_head=16, n_kv_head=4,
+                       head_dim=hd, theta=1e4, sinks=True, pos_rule="fixed",
+                       fixed_positions=pos, slot_rule="perm")
+    run = PagedRun(w, bs, split=(T, 8))
+    try:
+        run.kv.set_options(gflags)
+        out = run.step(0)
+        torch.cuda.synchronize()
+        assert run.kv.get_status() == 0
+        Kr, Vr = host_pool(w, bs)
+        ref, skipped = oracle_paged(w, bs, Kr, Vr, run.tables_np, flags=oflags)
+        assert skipped == 0
+        assert_close(out.cpu().numpy(), ref, f"paged out {name}")
+        written = written_mask(run, run.tables_np, w.positions(0))
+        Kg, Vg = run.K.cpu().numpy(), run.V.cpu().numpy()
+        assert_close(Kg[written], Kr[written], f"paged written K {name}")
+        assert_close(Vg[written], Vr[written], f"paged written V {name}")
+        assert np.array_equal(Kg[~written].view(np.uint32), Kr[~written].view(np.uint32))
+        assert np.array_equal(Vg[~written].view(np.uint32), Vr[~written].view(np.uint32))
+    finally:
+        run.close()
+
+
 def test_unknown_option_bits_rejected():
     w = _wl(128, 9)
     run = DeviceRun(w)

@@ -15,9 +15,9 @@ from sequence_slot_kv_gb300 import SlotKV
 pytestmark = pytest.mark.gpu
 
 
-def _setup(hd, G, idx, seqs):
-    """seqs: [(slot, history_len, prompt_len)].  Returns the geometry, token
-    arrays (interleaved) and the input draws."""
+def _setup(hd, G, idx, seqs, contiguous=False):
+    """seqs: [(slot, history_len, prompt_len)].  Returns the geometry and the
+    token arrays: interleaved round-robin, or one sequence after another."""
     n_kv = 2
     n_tok = sum(t for _, _, t in seqs)
     ctx = max(h + t for _, h, t in seqs) + 5
@@ -25,20 +25,24 @@ def _setup(hd, G, idx, seqs):
     w = synth.Workload(f"prefill_hd{hd}", 700 + idx, B=n_tok, n_slots=n_slots, slot_ctx=ctx,
                        n_head=G * n_kv, n_kv_head=n_kv, head_dim=hd, theta=1e4, sinks=True,
                        pos_rule="fixed", fixed_positions=tuple([0] * n_tok), slot_rule="perm")
-    # interleave the sequences' tokens round-robin
     order = []
-    cursor = [0] * len(seqs)
-    while len(order) < n_tok:
+    if contiguous:
         for i, (_, _, t) in enumerate(seqs):
-            if cursor[i] < t:
-                order.append((i, cursor[i]))
-                cursor[i] += 1
+            order.extend((i, j) for j in range(t))
+    else:
+        # interleave the sequences' tokens round-robin
+        cursor = [0] * len(seqs)
+        while len(order) < n_tok:
+            for i, (_, _, t) in enumerate(seqs):
+                if cursor[i] < t:
+                    order.append((i, cursor[i]))
+                    cursor[i] += 1
     slots = np.array([seqs[i][0] for i, _ in order], dtype=np.uint32)
     pos = np.array([seqs[i][1] + j for i, j in order], dtype=np.uint32)
     return w, slots, pos
 
 
-def _oracle(w, slots, pos):
+def _oracle(w, slots, pos, flags=0):
     """The tokens as single decode steps in position order, on host copies of
     the used slots."""
     o = oracle.default()
@@ -50,7 +54,7 @@ def _oracle(w, slots, pos):
     for i in np.lexsort((pos, slots)):
         r, _, _ = o.decode_batch(K, V, q[i:i + 1], kn[i:i + 1], vn[i:i + 1], pos[i:i + 1],
                                  slots[i:i + 1], w.q_norm_w(), w.k_norm_w(), w.inv_freq(),
-                                 w.sink_logits(), w.eps, w.scale)
+                                 w.sink_logits(), w.eps, w.scale, flags=flags)
         out[i] = r[0]
     return out, K, V
 
@@ -88,6 +92,82 @@ def test_prefill_equals_token_by_token_decode(hd, G):
         assert np.array_equal(Vg[mask].view(np.uint32), Vr[mask].view(np.uint32))
         assert np.array_equal(Kg[~mask].view(np.uint32), Kr[~mask].view(np.uint32))
         assert np.array_equal(Vg[~mask].view(np.uint32), Vr[~mask].view(np.uint32))
+    finally:
+        kv.free()
+
+
+GROUPED = [(128, 4), (128, 3), (64, 2), (64, 1), (256, 1)]
+
+
+@pytest.mark.parametrize("hd,G", GROUPED, ids=[f"hd{h}_g{g}" for h, g in GROUPED])
+def test_prefill_contiguous_sequences(hd, G):
+    """Sequences given one after another (the usual layout of a prompt
+    chunk), with a one-token sequence and a position gap: every token must
+    still equal one decode step at a time."""
+    T = 4096 // hd
+    seqs = [(1, 37, 7), (4, 5 * T + 3, 6), (0, 0, 2 * T + 1), (3, 200, 1), (5, 11, 9)]
+    idx = 40 + GROUPED.index((hd, G))
+    w, slots, pos = _setup(hd, G, idx, seqs, contiguous=True)
+    pos = pos.copy()
+    last = len(pos) - 1
+    pos[last] += 3          # a gap: the last sequence's final token sits 3 positions on
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    K = torch.empty(shape, device="cuda")
+    V = torch.empty(shape, device="cuda")
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    kv = SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
+    try:
+        out = torch.full((w.B, w.n_head, w.head_dim), float("nan"), device="cuda")
+        kv.prefill_batch_attn(to_dev(w.q()), to_dev(w.k_new()), to_dev(w.v_new()),
+                              to_dev(pos.astype(np.int32)), to_dev(slots.astype(np.int32)),
+                              to_dev(w.q_norm_w()), to_dev(w.k_norm_w()), to_dev(w.inv_freq()),
+                              to_dev(w.sink_logits()), out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert kv.get_status() == 0
+        ref, Kr, Vr = _oracle(w, slots, pos)
+        assert_close(out.cpu().numpy(), ref, f"contiguous prefill hd={hd} G={G}")
+        Kg, Vg = K.cpu().numpy(), V.cpu().numpy()
+        mask = np.zeros(shape[:2], dtype=bool)
+        mask[slots, pos] = True
+        assert_close(Kg[mask], Kr[mask], "prefill written K")
+        assert np.array_equal(Vg[mask].view(np.uint32), Vr[mask].view(np.uint32))
+        assert np.array_equal(Kg[~mask].view(np.uint32), Kr[~mask].view(np.uint32))
+    finally:
+        kv.free()
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3], ids=["vnorm", "plus_one", "both"])
+def test_prefill_with_norm_options(flags):
+    """Prefill with the Gemma norm forms: the KV-write kernel caches the
+    weightless-normed V and the (1 + w) norms apply to q and k, as in one
+    decode step at a time with the same options."""
+    import sequence_slot_kv_gb300 as skv
+    hd, G = 128, 4
+    T = 4096 // hd
+    w, slots, pos = _setup(hd, G, 60 + flags, [(2, 9, T + 3), (0, 40, 5)], contiguous=True)
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    K = torch.empty(shape, device="cuda")
+    V = torch.empty(shape, device="cuda")
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    kv = SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
+    try:
+        kv.set_options(flags)
+        assert skv.OPT_VNORM == 1 and skv.OPT_NORM_PLUS_ONE == 2
+        out = torch.full((w.B, w.n_head, w.head_dim), float("nan"), device="cuda")
+        kv.prefill_batch_attn(to_dev(w.q()), to_dev(w.k_new()), to_dev(w.v_new()),
+                              to_dev(pos.astype(np.int32)), to_dev(slots.astype(np.int32)),
+                              to_dev(w.q_norm_w()), to_dev(w.k_norm_w()), to_dev(w.inv_freq()),
+                              to_dev(w.sink_logits()), out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert kv.get_status() == 0
+        ref, Kr, Vr = _oracle(w, slots, pos, flags=flags)
+        assert_close(out.cpu().numpy(), ref, f"prefill options {flags}")
+        Kg, Vg = K.cpu().numpy(), V.cpu().numpy()
+        mask = np.zeros(shape[:2], dtype=bool)
+        mask[slots, pos] = True
+        assert_close(Kg[mask], Kr[mask], "prefill written K")
+        assert_close(Vg[mask], Vr[mask], "prefill written V")
+        assert np.array_equal(Kg[~mask].view(np.uint32), Kr[~mask].view(np.uint32))
     finally:
         kv.free()
 
