@@ -38,7 +38,7 @@ HBM_FALLBACK_GBS = 6800.0
 # the kernel source it was taken on (sha256 prefix of decode_attn.cuh); see
 # profiles/decode_attn_<workload>.md.
 MEASURED_TRAFFIC = {
-    "e6c1eed1e9aa80c9": {"mid": 555_917_056, "sinks": 2_342_451_456},
+    "dc783fcec7b078e4": {"mid": 556_234_240, "sinks": 2_342_272_504},
 }
 
 
