@@ -10,7 +10,7 @@ import torch
 import oracle
 import sequence_slot_kv_gb300 as skv
 import synth
-from gpu_harness import DeviceRun, assert_close, oracle_rows, to_dev
+from gpu_harness import DeviceRun, assert_close, check_kv_after, oracle_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -126,6 +126,42 @@ def test_default_policy_batch_and_alone():
                                  run.inv, run.sinks, outp, w.eps, w.scale)
         assert torch.equal(outp.cpu(), full[perm])
         assert run.status() == 0
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("layout", ["slots", "paged"])
+def test_many_rows(layout):
+    """3000 rows with short, mixed contexts: the plan kernel takes rows in
+    rounds of 1024 threads, so its later rounds (which re-read each row) and
+    many more items than CTAs run; every row against the oracle, every
+    written row, every other byte."""
+    B = 3000
+    w = synth.Workload("many_rows", 330, B=B, n_slots=B + 16, slot_ctx=192, n_head=4,
+                       n_kv_head=2, head_dim=64, theta=1e4, sinks=True, slot_rule="perm")
+    if layout == "slots":
+        run = DeviceRun(w)
+        try:
+            out = run.step(0)
+            torch.cuda.synchronize()
+            assert run.status() == 0
+            ref, _, _ = oracle_rows(w, range(B), n_threads=32)
+            assert_close(out.cpu().numpy(), ref[0], "3000 rows")
+            check_kv_after(run)
+        finally:
+            run.close()
+        return
+    from test_gpu_paged import PagedRun, check_pool, host_pool, oracle_paged, written_mask
+    run = PagedRun(w, 64)
+    try:
+        out = run.step(0)
+        torch.cuda.synchronize()
+        assert run.kv.get_status() == 0
+        Kr, Vr = host_pool(w, 64)
+        ref, skipped = oracle_paged(w, 64, Kr, Vr, run.tables_np)
+        assert skipped == 0
+        assert_close(out.cpu().numpy(), ref, "3000 paged rows")
+        check_pool(run, Kr, Vr, written_mask(run, run.tables_np, w.positions(0)))
     finally:
         run.close()
 
