@@ -480,8 +480,9 @@ def run_gpu(args, w):
                      "kernel": "slotkv_decode_attn_kernel"},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        # each decode call is two kernels: the work-list plan and the decode
-        "gpu_launches": args.steps * nsub * 2,
+        # the library's kernels per decode call (plan + decode, or decode alone)
+        "gpu_launches": args.steps * nsub * kv.call_shape(w.B, bt_stride=(
+            w.slot_ctx // bs if bs else 0))[2],
         "graph": bool(args.graph),
         "clocks": clk,
     }
@@ -562,7 +563,7 @@ def run_prefill(args):
                          "kernel": "slotkv_decode_attn_kernel (prefill mode)"},
             "key_bytes_read_per_step": per_token_bytes, "io_bytes_per_step": io,
             "effective_GBps": (per_token_bytes + io) / (ms / 1e3) / 1e9,
-            "gpu_launches": args.steps * 3}
+            "gpu_launches": args.steps * kv.call_shape(n_tok, prefill=True)[2]}
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         v, desc = time_oracle_prefill(w, slots, pos, n_seq, chunk, args.cpu_budget, cores)

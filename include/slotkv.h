@@ -342,6 +342,19 @@ int slot_kv_get_status(slotkv_t handle, slotkv_stream_t stream, uint32_t* flags)
 int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_splits);
 
 /*
+ * slot_kv_call_shape -- how a call of B rows on this handle runs, without
+ * running it (host only): *chunk_keys the split chunk C of the current policy,
+ * *ctas the persistent CTAs of the decode kernel, *kernels the kernels the
+ * call launches on its stream (KV write for prefill, work-list plan unless
+ * every item is a CTA's first item, decode).  bt_stride: 0 for slot calls,
+ * the table width for decode_batch_attn_paged; prefill: nonzero for
+ * prefill_batch_attn.  Any output pointer may be NULL.  SLOTKV_ERR_ARG for
+ * B = 0 or B > max_rows.
+ */
+int slot_kv_call_shape(slotkv_t handle, uint32_t B, uint32_t bt_stride, uint32_t prefill,
+                       uint32_t* chunk_keys, uint32_t* ctas, uint32_t* kernels);
+
+/*
  * slot_kv_set_options -- norm options of the per-head "V/Q/K norm" of the
  * Gemma path ("Forward Cuda Gemma", decodeBatch), for later decode calls on
  * this handle.  flags is a bitwise OR of:

@@ -47,6 +47,8 @@ EXPORTS = {
                                  _vp, _vp, _f32, _f32, _vp], _int),
     "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
     "slot_kv_set_split": ([_vp, _u32, _u32], _int),
+    "slot_kv_call_shape": ([_vp, _u32, _u32, _u32, ctypes.POINTER(_u32), ctypes.POINTER(_u32),
+                            ctypes.POINTER(_u32)], _int),
     "slot_kv_advance_positions": ([_vp, _u32, _u32, _vp], _int),
     "slot_kv_set_options": ([_vp, _u32], _int),
     "decode_batch_attn_noalloc": ([_vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp,
@@ -244,6 +246,14 @@ class SlotKV:
     def set_options(self, flags):
         """OPT_VNORM and/or OPT_NORM_PLUS_ONE (see slot_kv_set_options)."""
         _check(_lib.slot_kv_set_options(self._h, flags), "slot_kv_set_options")
+
+    def call_shape(self, B, bt_stride=0, prefill=False):
+        """(chunk_keys, ctas, kernels) of a call of B rows (slot_kv_call_shape)."""
+        c, n, k = _u32(), _u32(), _u32()
+        _check(_lib.slot_kv_call_shape(self._h, B, bt_stride, 1 if prefill else 0,
+                                       ctypes.byref(c), ctypes.byref(n), ctypes.byref(k)),
+               "slot_kv_call_shape")
+        return c.value, n.value, k.value
 
     def set_split(self, min_chunk_keys, max_splits):
         _check(_lib.slot_kv_set_split(self._h, min_chunk_keys, max_splits), "slot_kv_set_split")

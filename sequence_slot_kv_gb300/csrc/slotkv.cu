@@ -176,6 +176,29 @@ uint32_t auto_chunk(const slotkv_s* h, uint32_t B, uint64_t max_keys) {
     return (uint32_t)(c < lo ? lo : (c > hi ? hi : c));
 }
 
+// How a call of B rows runs: the split chunk, the persistent CTAs, the
+// static first items, whether the plan kernel runs, and the kernels launched.
+struct CallShape {
+    uint32_t chunk, ctas, static_items, no_plan, kernels;
+};
+
+CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill) {
+    CallShape c;
+    c.chunk = h->auto_split ? auto_chunk(h, B, max_keys) : h->chunk_min;
+    // persistent CTAs: two per SM, never more than there can be work items
+    const uint32_t gsplits = grid_splits(h, max_keys, c.chunk);
+    const uint64_t most = (uint64_t)B * h->n_kv_head * gsplits;
+    const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
+    c.ctas = (uint32_t)(most < want ? most : want);
+    // each CTA's first item is split 0 of one (row, kv head) pair; when that
+    // covers every item (one split per row, a CTA per pair) no plan is needed
+    const uint64_t pairs = (uint64_t)B * h->n_kv_head;
+    c.static_items = (uint32_t)(pairs < c.ctas ? pairs : c.ctas);
+    c.no_plan = (gsplits == 1 && pairs <= c.ctas) ? 1u : 0u;
+    c.kernels = (prefill ? 1u : 0u) + (c.no_plan ? 0u : 1u) + 1u;
+    return c;
+}
+
 int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float* k_new,
            const float* v_new, const uint32_t* positions, const uint32_t* slots,
            const float* q_norm_w, const float* k_norm_w, const float* inv_freq,
@@ -210,23 +233,16 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.n_kv_head = h->n_kv_head;
     P.B = B;
     const uint64_t max_keys = block_tables ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
-    const uint32_t chunk = h->auto_split ? auto_chunk(h, B, max_keys) : h->chunk_min;
-    P.chunk_min = chunk;
+    const CallShape cs = call_shape(h, B, max_keys, prefill);
+    P.chunk_min = cs.chunk;
     P.max_splits = h->max_splits;
     P.eps = eps;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.flags = h->options;
     const int G = (int)(n_head / h->n_kv_head);
-    // persistent CTAs: two per SM, never more than there can be work items
-    const uint32_t gsplits = grid_splits(h, max_keys, chunk);
-    const uint64_t most = (uint64_t)B * h->n_kv_head * gsplits;
-    const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
-    const unsigned ctas = (unsigned)(most < want ? most : want);
-    // each CTA's first item is split 0 of one (row, kv head) pair; when that
-    // covers every item (one split per row, a CTA per pair) no plan is needed
-    const uint64_t pairs = (uint64_t)B * h->n_kv_head;
-    P.static_items = (unsigned)(pairs < ctas ? pairs : ctas);
-    P.no_plan = (gsplits == 1 && pairs <= ctas) ? 1u : 0u;
+    const unsigned ctas = cs.ctas;
+    P.static_items = cs.static_items;
+    P.no_plan = cs.no_plan;
     int rc;
     switch (h->head_dim) {
         case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, ctas, stream); break;
@@ -614,6 +630,19 @@ int slot_kv_set_options(slotkv_t h, uint32_t flags) {
     if (flags & ~(SLOTKV_OPT_VNORM | SLOTKV_OPT_NORM_PLUS_ONE | SLOTKV_OPT_TEST_STALL))
         return fail(SLOTKV_ERR_ARG, "unknown option bits 0x%x", flags);
     h->options = flags;
+    return SLOTKV_OK;
+}
+
+int slot_kv_call_shape(slotkv_t h, uint32_t B, uint32_t bt_stride, uint32_t prefill,
+                       uint32_t* chunk_keys, uint32_t* ctas, uint32_t* kernels) {
+    g_err[0] = 0;
+    if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (B == 0 || B > h->max_rows) return fail(SLOTKV_ERR_ARG, "B=%u outside 1..max_rows", B);
+    const uint64_t max_keys = bt_stride ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
+    const CallShape cs = call_shape(h, B, max_keys, prefill != 0);
+    if (chunk_keys) *chunk_keys = cs.chunk;
+    if (ctas) *ctas = cs.ctas;
+    if (kernels) *kernels = cs.kernels;
     return SLOTKV_OK;
 }
 

@@ -166,6 +166,33 @@ def test_many_rows(layout):
         run.close()
 
 
+def test_call_shape():
+    """slot_kv_call_shape reports what a call launches: the decode kernel
+    alone when every item is a CTA's first item (a few short rows), with the
+    plan kernel otherwise, plus the KV-write kernel for prefill; and the
+    fixed policy's chunk once slot_kv_set_split is called."""
+    tiny = synth.WORKLOADS["tiny"]
+    run = DeviceRun(tiny)
+    try:
+        chunk, ctas, kernels = run.kv.call_shape(tiny.B)
+        assert kernels == 1 and ctas == tiny.B * tiny.n_kv_head
+        assert run.kv.call_shape(tiny.B, prefill=True)[2] == 2
+        run.kv.set_split(64, 8)
+        assert run.kv.call_shape(tiny.B)[0] == 64
+    finally:
+        run.close()
+    mid = synth.WORKLOADS["mid"].replace(n_slots=40, B=32)
+    kv = skv.SlotKV(mid.n_slots, mid.slot_ctx, mid.n_kv_head, mid.head_dim, mid.B, mid.n_head)
+    try:
+        chunk, ctas, kernels = kv.call_shape(mid.B)
+        assert kernels == 2 and chunk % (4096 // mid.head_dim) == 0
+        assert kv.call_shape(mid.B, prefill=True)[2] == 3
+        with pytest.raises(skv.SlotKVError):
+            kv.call_shape(0)
+    finally:
+        kv.free()
+
+
 def test_stale_history_is_never_read():
     """NaN in every position after pos of each row's slot changes nothing."""
     w = _wl(sinks=False, idx=301)
