@@ -24,6 +24,9 @@
  *     stream) and returns without synchronising, unless stated otherwise.
  *   - Calls that use one handle must be ordered on the GPU (same stream, or
  *     synchronised): they share the handle's workspace.
+ *   - A handle belongs to the device that was current at slot_kv_alloc; calls
+ *     that enqueue work or synchronise on it need that device current
+ *     (SLOTKV_ERR_STATE otherwise).  slot_kv_free switches to it by itself.
  *   - Every call returns SLOTKV_OK (0) or an SLOTKV_ERR_* code and never
  *     aborts the process; slot_kv_last_error() gives a message for the
  *     calling thread's last failure.

@@ -89,8 +89,11 @@ def _check(code, what):
         raise SlotKVError(code, what)
 
 
-def _ptr(t, dtype=None, what="tensor"):
-    """Device (or host) address of a contiguous tensor; None stays NULL."""
+def _ptr(t, dtype=None, what="tensor", cuda=True):
+    """Address of a contiguous tensor that lives on the GPU (cuda=True) or in
+    host memory (cuda=False); None stays NULL.  The library reads these
+    addresses from its kernels or copies, so a tensor in the wrong place is
+    refused here."""
     if t is None:
         return None
     import torch
@@ -100,6 +103,8 @@ def _ptr(t, dtype=None, what="tensor"):
         raise ValueError(f"{what} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if cuda is not None and t.is_cuda != cuda:
+        raise ValueError(f"{what} must be a {'CUDA' if cuda else 'CPU'} tensor")
     return t.data_ptr()
 
 
@@ -230,11 +235,13 @@ class SlotKV:
         B, n_head = int(q.shape[0]), int(q.shape[1])
         f, u = torch.float32, torch.int32
         _check(_lib.decode_batch_attn_host(
-            self._h, B, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
-            _ptr(v_new, f, "v_new"), _ptr(positions, u, "positions"), _ptr(slots, u, "slots"),
+            self._h, B, n_head, _ptr(q, f, "q", cuda=False),
+            _ptr(k_new, f, "k_new", cuda=False), _ptr(v_new, f, "v_new", cuda=False),
+            _ptr(positions, u, "positions", cuda=False), _ptr(slots, u, "slots", cuda=False),
             _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
-            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"), _ptr(out, f, "out"),
-            eps, scale, _stream_ptr(stream)), "decode_batch_attn_host")
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"),
+            _ptr(out, f, "out", cuda=False), eps, scale, _stream_ptr(stream)),
+            "decode_batch_attn_host")
         return out
 
     def get_status(self, stream=None):

@@ -93,6 +93,10 @@ void free_workspace(slotkv_s* h) {
 
 void release(slotkv_s* h) {
     if (!h) return;
+    // the handle's memory and work live on its own device
+    int cur = 0;
+    const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != h->device &&
+                          cudaSetDevice(h->device) == cudaSuccess;
     cudaDeviceSynchronize();
     free_workspace(h);
     cudaFree(h->status);
@@ -106,6 +110,7 @@ void release(slotkv_s* h) {
         cudaFree(h->K);
         cudaFree(h->V);
     }
+    if (switched) cudaSetDevice(cur);
     delete h;
 }
 
@@ -153,6 +158,16 @@ int encode_maps(slotkv_s* h) {
 }
 
 bool valid_handle(slotkv_t h) { return h && h->K && h->V && h->status; }
+
+// A handle's buffers, workspace and tensor maps belong to the device it was
+// allocated on; work is only enqueued with that device current.
+int check_device(slotkv_t h) {
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device)
+        return fail(SLOTKV_ERR_STATE, "the handle belongs to device %d but device %d is current",
+                    h->device, cur);
+    return SLOTKV_OK;
+}
 
 // The most splits any row of this slot_ctx can need: nsplit(n) <= ceil(n /
 // chunk_min) because chunks are >= chunk_min keys, and <= max_splits.
@@ -259,6 +274,7 @@ int check_decode_args(slotkv_t h, uint32_t B, uint32_t n_head, const void* q,
                       const void* slots, const void* q_norm_w, const void* k_norm_w,
                       const void* inv_freq, const void* out, bool device_ptrs = true) {
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (check_device(h) != SLOTKV_OK) return SLOTKV_ERR_STATE;
     if (B > h->max_rows) return fail(SLOTKV_ERR_ARG, "B=%u exceeds max_rows=%u", B, h->max_rows);
     if (n_head == 0 || n_head % h->n_kv_head != 0)
         return fail(SLOTKV_ERR_ARG, "n_head=%u is not a multiple of n_kv_head=%u", n_head,
@@ -430,6 +446,7 @@ size_t slot_kv_offset_bytes(slotkv_t h, uint32_t slot, uint32_t pos) {
 int slot_kv_reset(slotkv_t h, uint32_t slot, slotkv_stream_t stream) {
     g_err[0] = 0;
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
+    if (check_device(h) != SLOTKV_OK) return SLOTKV_ERR_STATE;
     if (slot >= h->n_slots) return fail(SLOTKV_ERR_ARG, "slot=%u >= n_slots=%u", slot, h->n_slots);
     const size_t off = slot_kv_offset_bytes(h, slot, 0);
     const size_t bytes = (size_t)h->slot_ctx * h->kv_dim * sizeof(float);
@@ -604,6 +621,7 @@ int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,
 int slot_kv_get_status(slotkv_t h, slotkv_stream_t stream, uint32_t* flags) {
     g_err[0] = 0;
     if (!valid_handle(h) || !flags) return fail(SLOTKV_ERR_ARG, "bad handle or flags pointer");
+    if (check_device(h) != SLOTKV_OK) return SLOTKV_ERR_STATE;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t v = 0;
     cudaError_t e;
@@ -650,6 +668,7 @@ int slot_kv_set_split(slotkv_t h, uint32_t min_chunk_keys, uint32_t max_splits) 
     g_err[0] = 0;
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
     const uint32_t T = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+    if (check_device(h) != SLOTKV_OK) return SLOTKV_ERR_STATE;
     if (min_chunk_keys == 0 || min_chunk_keys % T != 0)
         return fail(SLOTKV_ERR_ARG, "min_chunk_keys must be a positive multiple of %u", T);
     if (max_splits == 0 || max_splits > 256) return fail(SLOTKV_ERR_ARG, "max_splits 1..256");

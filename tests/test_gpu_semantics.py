@@ -363,6 +363,17 @@ def test_argument_errors():
                                           to_dev(pos.astype(np.int32)), run.slots, run.qw,
                                           run.kw, run.inv, None, out, w.eps, w.scale)
         assert ei.value.code == 1 and "aligned" in str(ei.value)
+        # tensors in the wrong place are refused by the binding
+        with pytest.raises(ValueError, match="CUDA"):
+            run.kv.decode_batch_attn(torch.from_numpy(q), to_dev(kn), to_dev(vn),
+                                     to_dev(pos.astype(np.int32)), run.slots, run.qw, run.kw,
+                                     run.inv, None, out, w.eps, w.scale)
+        with pytest.raises(ValueError, match="CPU"):
+            run.kv.decode_batch_attn_host(to_dev(q), torch.from_numpy(kn), torch.from_numpy(vn),
+                                          torch.from_numpy(pos.astype(np.int32)),
+                                          torch.from_numpy(run.slots_np.astype(np.int32)),
+                                          run.qw, run.kw, run.inv, None,
+                                          torch.empty(out.shape), w.eps, w.scale)
         with pytest.raises(skv.SlotKVError):
             run.kv.set_split(5, 8)                       # not a multiple of the tile
         h = ctypes.c_void_p()
