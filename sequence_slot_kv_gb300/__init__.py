@@ -6,18 +6,25 @@ no CPU fallback: importing this package raises if ``libslotkv.so`` has not
 been built (``__graft_entry__.build()`` or ``python -m
 sequence_slot_kv_gb300.build``).
 
-The functions mirror the C ABI in ``include/slotkv.h`` name for name:
-``slot_kv_alloc``, ``slot_kv_free``, ``slot_kv_offset_bytes``,
-``slot_kv_reset``, ``decode_batch_attn``, ``decode_batch_attn_host``,
-``slot_kv_get_status``, ``slot_kv_set_split``; ``SlotKV`` wraps a handle.
+The functions mirror the C ABI in ``include/slotkv.h`` name for name
+(``EXPORTS`` lists every symbol): the handle (``slot_kv_alloc``,
+``slot_kv_free``, ``slot_kv_offset_bytes``, ``slot_kv_reset``), the step
+(``decode_batch_attn``, its host-buffer form ``decode_batch_attn_host``,
+``prefill_batch_attn``, ``decode_batch_attn_paged``, the allocation-free
+``decode_batch_attn_noalloc``), multi-step support
+(``slot_kv_advance_positions``), and control (``slot_kv_get_status``,
+``slot_kv_set_split``, ``slot_kv_set_options``, ``slot_kv_call_shape``).
+``SlotKV`` wraps a handle.
 """
 import ctypes
 import os
 
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
-    "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn", "slot_kv_get_status",
-    "slot_kv_set_split", "slot_kv_advance_positions", "decode_batch_attn_paged", "decode_batch_attn_noalloc", "LIB_PATH", "EXPORTS", "DEV_RANGE", "DEV_TIMEOUT",
+    "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn",
+    "decode_batch_attn_paged", "decode_batch_attn_noalloc", "slot_kv_advance_positions",
+    "slot_kv_get_status", "slot_kv_set_split", "LIB_PATH", "EXPORTS", "DEV_RANGE",
+    "DEV_TIMEOUT", "OPT_VNORM", "OPT_NORM_PLUS_ONE", "OPT_TEST_STALL",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libslotkv.so")
