@@ -1,7 +1,9 @@
-"""Seeded random configurations of the decode step against the oracle: head
-dims, group sizes, kv heads, batch sizes, ragged positions (some rows out of
-range), default and fixed split policies, slot and paged layouts with random
-block sizes, and the norm options.  Each case checks every in-range row's
+"""Seeded random configurations against the oracle.
+
+Decode: head dims, group sizes, kv heads, batch sizes, ragged positions (some
+rows out of range), default and fixed split policies, slot and paged layouts
+with random block sizes, and the norm options.  Prefill: random sequences in
+one call, tokens in random order.  Each case checks every in-range row's
 output, the range flag, the written rows and that no other byte changed."""
 import numpy as np
 import pytest
@@ -119,5 +121,81 @@ def test_random_configuration(seed):
             assert_close(Vg, Vr, f"fuzz case {seed} V")
         else:
             assert np.array_equal(Vg.view(np.uint32), Vr.view(np.uint32))
+    finally:
+        kv.free()
+
+
+N_PREFILL = 60
+
+
+def _prefill_case(seed):
+    rng = np.random.default_rng(5000 + seed)
+    hd = int(rng.choice([64, 128, 256]))
+    T = 4096 // hd
+    G = int(rng.integers(1, 9))
+    nkv = int(rng.integers(1, 4))
+    n_seq = int(rng.integers(1, 6))
+    hist = rng.integers(0, 3 * T, size=n_seq)
+    plen = rng.integers(1, 2 * T + 1, size=n_seq)
+    slot_ctx = int((hist + plen).max()) + int(rng.integers(1, 9))
+    n_slots = n_seq + int(rng.integers(0, 3))
+    slots_of = rng.permutation(n_slots)[:n_seq]
+    toks = [(int(slots_of[i]), int(hist[i]) + j) for i in range(n_seq) for j in range(int(plen[i]))]
+    order = rng.permutation(len(toks))
+    slots = np.array([toks[k][0] for k in order], dtype=np.uint32)
+    pos = np.array([toks[k][1] for k in order], dtype=np.uint32)
+    split = (T * int(rng.integers(1, 4)), int(rng.integers(1, 9))) if rng.random() < 0.5 else None
+    flags = int(rng.integers(0, 4)) if rng.random() < 0.3 else 0
+    w = synth.Workload(f"pfuzz{seed}", 3000 + seed, B=len(toks), n_slots=n_slots,
+                       slot_ctx=slot_ctx, n_head=G * nkv, n_kv_head=nkv, head_dim=hd,
+                       theta=1e4, sinks=bool(rng.integers(0, 2)), pos_rule="fixed",
+                       fixed_positions=tuple([0] * len(toks)), slot_rule="perm")
+    return w, slots, pos, split, flags
+
+
+@pytest.mark.parametrize("seed", range(N_PREFILL))
+def test_random_prefill(seed):
+    """Random sequences (history, prompt length, slot) as one prefill call
+    with their tokens in random order: every token equals one decode step at
+    a time in position order; written rows and untouched bytes as for decode."""
+    w, slots, pos, split, flags = _prefill_case(seed)
+    o = oracle.default()
+    q, kn, vn = w.q(), w.k_new(), w.v_new()
+    Kh = synth.normal(w.kv_elems(), w.seed, synth.S_HIST_K).reshape(
+        w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    Vh = synth.normal(w.kv_elems(), w.seed, synth.S_HIST_V).reshape(Kh.shape)
+    Kd, Vd = to_dev(Kh), to_dev(Vh)
+    kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head,
+                    k_buf=Kd, v_buf=Vd)
+    try:
+        if split:
+            kv.set_split(*split)
+        if flags:
+            kv.set_options(flags)
+        out = torch.full((w.B, w.n_head, w.head_dim), float("nan"), device="cuda")
+        kv.prefill_batch_attn(to_dev(q), to_dev(kn), to_dev(vn), to_dev(pos.astype(np.int32)),
+                              to_dev(slots.astype(np.int32)), to_dev(w.q_norm_w()),
+                              to_dev(w.k_norm_w()), to_dev(w.inv_freq()),
+                              None if w.sink_logits() is None else to_dev(w.sink_logits()),
+                              out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert kv.get_status() == 0
+        Kr, Vr = Kh.copy(), Vh.copy()
+        ref = np.empty((w.B, w.n_head, w.head_dim), dtype=np.float32)
+        for i in np.lexsort((pos, slots)):
+            r, _, _ = o.decode_batch(Kr, Vr, q[i:i + 1], kn[i:i + 1], vn[i:i + 1], pos[i:i + 1],
+                                     slots[i:i + 1], w.q_norm_w(), w.k_norm_w(), w.inv_freq(),
+                                     w.sink_logits(), w.eps, w.scale, flags=flags)
+            ref[i] = r[0]
+        assert_close(out.cpu().numpy(), ref, f"prefill fuzz case {seed}")
+        Kg, Vg = Kd.cpu().numpy(), Vd.cpu().numpy()
+        mask = np.zeros(Kh.shape[:2], dtype=bool)
+        mask[slots, pos] = True
+        assert_close(Kg[mask], Kr[mask], f"prefill fuzz case {seed} K")
+        assert_close(Vg[mask], Vr[mask], f"prefill fuzz case {seed} V")
+        if not flags & 1:
+            assert np.array_equal(Vg[mask].view(np.uint32), Vr[mask].view(np.uint32))
+        assert np.array_equal(Kg[~mask].view(np.uint32), Kh[~mask].view(np.uint32))
+        assert np.array_equal(Vg[~mask].view(np.uint32), Vh[~mask].view(np.uint32))
     finally:
         kv.free()
