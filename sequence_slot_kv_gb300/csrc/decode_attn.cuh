@@ -13,7 +13,8 @@
 //   * slotkv_decode_attn_kernel (persistent, 2 CTAs per SM, launched as a
 //     programmatic dependent of the plan): each CTA starts on its static
 //     first item -- split 0 of (row, kv head) pair blockIdx.x -- while the
-//     plan runs, then takes items from the list until it is exhausted.  The
+//     plan runs, then takes items from the list, each claimed a few tiles
+//     before the current one ends, until it is exhausted.  The
 //     steps of "Forward Cuda Gemma", decodeBatch, fused:
 //       - warp 4 (producer) streams the items' history K and V tiles into a
 //         3-stage shared-memory ring with 2-D TMA copies (cp.async.bulk.tensor,
@@ -67,6 +68,7 @@ constexpr uint32_t kOptVNorm = 1u;        // SLOTKV_OPT_VNORM
 constexpr uint32_t kOptNormPlusOne = 2u;  // SLOTKV_OPT_NORM_PLUS_ONE
 constexpr uint32_t kOptTestStall = 0x80000000u;  // SLOTKV_OPT_TEST_STALL
 constexpr int kPlanThreads = 1024;
+constexpr uint32_t kClaimLead = 4;  // tiles left in an item when the next is claimed
 
 __host__ __device__ constexpr int pow2_floor(int x) {
     int r = 1;
@@ -902,10 +904,11 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
     if (warp >= W) {
         regs_decrease<C::REG_HELP>();
         // ------------------------------------------------------------ producer
-        // Items are staged one ahead: item k+1's descriptor and vectors go into
-        // its slot as soon as the consumers release that slot (they finish item
-        // k-1), while item k's tiles are still streaming, so the prep warp has
-        // item k+1 ready before the consumers reach it.
+        // Items are staged one ahead: item k+1 is claimed near the end of item
+        // k's tiles, and its descriptor and vectors go into its slot (free once
+        // the consumers have finished item k-1) while item k's last tiles are
+        // still streaming, so the prep warp has item k+1 ready before the
+        // consumers reach it.
         // Paged mode: the whole producer warp checks the static first item's
         // row the way the plan does (p within the table, every used entry in
         // the pool) and finds the row of key p.
@@ -1037,10 +1040,19 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             const uint32_t* nxt_tab = nullptr;
             uint32_t cur_blk = 0, nxt_blk = 0;
             bool cur_ok = stage(0, first_ok, rec, cur_kvh, cur_row, cur_nt, cur_tab, cur_blk);
-            // the record of the item after the staged one, claimed early (a
-            // static first item claims it once its tiles fill the ring)
+            // The next item is claimed late: when kClaimLead tiles of the
+            // current one are left to issue (at once for shorter items).  The
+            // claim, the record load and the staging then take one tile each,
+            // with tiles to spare before the next item's tiles are needed, and
+            // the hand-out follows the kernel's actual progress -- largest
+            // items first, the small ones to whichever CTAs free up at the end.
             uint32_t it_n = 0;
-            if (planned) it_n = cur_ok ? atomicAdd(P.plan + 1, 1u) : n_items;
+            bool claimed = false;
+            auto claim = [&]() {
+                if (!planned) await_plan();
+                it_n = atomicAdd(P.plan + 1, 1u);
+                claimed = true;
+            };
             uint4 rec_n = make_uint4(0, 0, 0, 0);
             bool rec_n_loaded = false;
             uint32_t tile_g = 0;
@@ -1072,13 +1084,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(cur_kvh * HD), trow,
                                 full);
                     misc[2] = static_cast<int>(tile_g + 1);
-                    if (!planned) {
-                        // the plan is needed only to stage the next item: wait
-                        // for it a few tiles in, by when it has long finished
-                        if (t + 1 >= 8u || t + 1 == cur_nt) {
-                            await_plan();
-                            it_n = atomicAdd(P.plan + 1, 1u);
-                        }
+                    // (a static first item waits for the plan here, by when
+                    // the plan kernel has long finished)
+                    if (!claimed) {
+                        if (t + kClaimLead >= cur_nt) claim();
                     } else if (!rec_n_loaded) {
                         if (it_n < n_items) rec_n = __ldcg(recs + it_n);
                         rec_n_loaded = true;
@@ -1089,10 +1098,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     }
                 }
                 if (misc[0]) break;
-                if (!planned) {  // a static first item without tiles
-                    await_plan();
-                    it_n = atomicAdd(P.plan + 1, 1u);
-                }
+                if (!claimed) claim();  // an item without tiles
                 if (!nxt_staged) {
                     if (!rec_n_loaded && it_n < n_items) rec_n = __ldcg(recs + it_n);
                     if (k >= 1 && !mbar_wait(nfree, nparity)) {
@@ -1103,7 +1109,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     nxt_ok = stage(k + 1, it_n < n_items, rec_n, nxt_kvh, nxt_row, nxt_nt,
                                    nxt_tab, nxt_blk);
                 }
-                if (nxt_ok) it_n = atomicAdd(P.plan + 1, 1u);
+                claimed = false;
                 rec_n_loaded = false;
                 cur_ok = nxt_ok;
                 cur_kvh = nxt_kvh;
