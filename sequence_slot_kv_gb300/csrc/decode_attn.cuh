@@ -7,14 +7,15 @@
 //
 // Kernels per call, on one stream:
 //   * slotkv_plan_kernel (one CTA): checks every row's slot and position,
-//     lists the valid work items, largest first (leaving out each CTA's
-//     static first item), and resets the hand-out counter.  Skipped when the
-//     static first items are all the work;
+//     lists the valid work items, largest first (leaving out the CTAs'
+//     static items), and resets the hand-out counter.  Skipped when the
+//     static items are all the work;
 //   * slotkv_decode_attn_kernel (persistent, 2 CTAs per SM, launched as a
 //     programmatic dependent of the plan): each CTA starts on its static
-//     first item -- split 0 of (row, kv head) pair blockIdx.x -- while the
-//     plan runs, then takes items from the list, each claimed a few tiles
-//     before the current one ends, until it is exhausted.  The
+//     item -- split 0 of (row, kv head) pair blockIdx.x, or, for CTAs beyond
+//     the pairs, split 1 of a pair -- while the plan runs, then takes items
+//     from the list, each claimed a few tiles before the current one ends,
+//     until it is exhausted.  The
 //     steps of "Forward Cuda Gemma", decodeBatch, fused:
 //       - warp 4 (producer) streams the items' history K and V tiles into a
 //         3-stage shared-memory ring with 2-D TMA copies (cp.async.bulk.tensor,
@@ -44,7 +45,7 @@
 // blocks and row b's key t sits in block block_tables[b][t / block_size].
 // Block sizes are multiples of T and tile starts are multiples of T, so each
 // tile lies inside one block: the producer only swaps the tile's first row
-// (looked up one tile ahead), and the plan (or, for a static first item, the
+// (looked up one tile ahead), and the plan (or, for a static item, the
 // producer warp) checks every used table entry.
 //
 // Every wait on an mbarrier is bounded; on expiry the CTA raises
@@ -659,7 +660,9 @@ __device__ __forceinline__ void warp_rms_norm_plain(const float* src, float* dst
 // the row alone).  Raises SLOTKV_DEV_RANGE for rows whose slot or position
 // is out of range -- in paged mode, whose position is past its table or any
 // of whose blocks 0..p/block_size is not in the pool -- (they get no items)
-// and resets the hand-out counter.
+// and resets the hand-out counter.  The decode CTAs' static items (split 0 of
+// the first static_items pairs, split 1 of the first static_second pairs)
+// are left out of the list.
 constexpr int kPlanBins = 64;
 constexpr int kPlanMaxRows = 65536;
 
@@ -720,11 +723,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     }
     __syncthreads();
     // A row's shape: position, row of key p in the [rows][kv_dim] view of K
-    // and V, split count, the tile counts of its full and last splits, and how
-    // many of its listed items are full / last splits (split 0 of the first
-    // static_items (row, kv head) pairs belongs to the decode CTAs).
+    // and V, split count, the tile counts of its full and last splits, how
+    // many of its listed items are full / last splits, and how many of its kv
+    // heads have split 0 (ns) and split 1 (ns1) held by decode CTAs as static
+    // items (split 0 of the first static_items pairs, split 1 of the first
+    // static_second pairs when the row has a second split).
     struct Shape {
-        uint32_t p, prow, nsplit, ft, lt, nfull, nlast, ns;
+        uint32_t p, prow, nsplit, ft, lt, nfull, nlast, ns, ns1;
     };
     auto row_shape = [&](uint32_t b, Shape& r) {
         r.p = P.positions[b];
@@ -745,8 +750,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         r.ns = P.static_items > first
                    ? (P.static_items - first < nkv ? P.static_items - first : nkv)
                    : 0u;
-        r.nfull = r.nsplit > 1 ? (r.nsplit - 1) * nkv - r.ns : 0u;
-        r.nlast = r.nsplit > 1 ? nkv : nkv - r.ns;
+        r.ns1 = r.nsplit > 1 && P.static_second > first
+                    ? (P.static_second - first < nkv ? P.static_second - first : nkv)
+                    : 0u;
+        // full splits 0 .. nsplit-2, less the static ones; the last split
+        // nsplit-1 (0 or 1 may be static)
+        r.nfull = r.nsplit > 1 ? (r.nsplit - 1) * nkv - r.ns - (r.nsplit > 2 ? r.ns1 : 0u) : 0u;
+        r.nlast = nkv - (r.nsplit == 1 ? r.ns : (r.nsplit == 2 ? r.ns1 : 0u));
         return true;
     };
     auto bin_of = [](uint32_t tiles) { return tiles < kPlanBins ? tiles : kPlanBins - 1u; };
@@ -791,7 +801,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     uint4* recs = reinterpret_cast<uint4*>(P.items);
     for (uint32_t r0 = 0; r0 < P.B; r0 += kPlanThreads) {
         const uint32_t b = r0 + tid;
-        uint32_t meta = 0;  // nsplit | ns << 16 of a row with items, else 0
+        uint32_t meta = 0;  // nsplit | ns << 9 | ns1 << 18 of a row with items, else 0
         if (b < P.B) {
             Shape r = mine;
             const bool ok = r0 == 0 ? mine_ok : row_shape(b, r);
@@ -802,7 +812,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
                 sh_nl[tid] = r.nlast;
                 sh_fb[tid] = r.nfull ? atomicAdd(&bin_cursor[bin_of(r.ft)], r.nfull) : 0u;
                 sh_lb[tid] = r.nlast ? atomicAdd(&bin_cursor[bin_of(r.lt)], r.nlast) : 0u;
-                meta = r.nsplit | (r.ns << 16);
+                meta = r.nsplit | (r.ns << 9) | (r.ns1 << 18);
             }
         }
         sh_meta[tid] = meta;
@@ -812,13 +822,27 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
         for (uint32_t i = warp; i < nrows; i += kPlanThreads / 32) {
             const uint32_t m = sh_meta[i];
             if (!m) continue;
-            const uint32_t row = r0 + i, nsplit = m & 0xffffu, ns = m >> 16;
+            const uint32_t row = r0 + i, nsplit = m & 511u, ns = (m >> 9) & 511u, ns1 = m >> 18;
             const uint32_t p = sh_p[i], prow = sh_prow[i];
             const uint32_t nfull = sh_nf[i], nlast = sh_nl[i], fb = sh_fb[i], lb = sh_lb[i];
-            // listed full splits: (split, kv head) = divmod(j + ns, nkv); listed
-            // last splits: kv heads nkv - nlast .. nkv - 1
-            for (uint32_t j = lane; j < nfull; j += 32)
-                recs[fb + j] = make_uint4(pack_item(row, (j + ns) / nkv, (j + ns) % nkv), p, prow, 0u);
+            // listed full splits, in (split, kv head) order: split 0 from kv
+            // head ns, split 1 from ns1 (when it is not the last split), the
+            // rest whole; listed last splits: kv heads nkv - nlast .. nkv - 1
+            for (uint32_t j = lane; j < nfull; j += 32) {
+                uint32_t split, kvh = j;
+                if (kvh < nkv - ns) {
+                    split = 0;
+                    kvh += ns;
+                } else if ((kvh -= nkv - ns) < nkv - ns1) {
+                    split = 1;
+                    kvh += ns1;
+                } else {
+                    kvh -= nkv - ns1;
+                    split = 2 + kvh / nkv;
+                    kvh %= nkv;
+                }
+                recs[fb + j] = make_uint4(pack_item(row, split, kvh), p, prow, 0u);
+            }
             for (uint32_t j = lane; j < nlast; j += 32)
                 recs[lb + j] = make_uint4(pack_item(row, nsplit - 1, j + (nkv - nlast)), p, prow, 0u);
         }
@@ -870,12 +894,17 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
     volatile uint32_t* pend = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_PEND);
     // misc[0]: abort, misc[2]: tiles issued, misc[3]: items staged
 
-    // The producer's static first item needs its row's position and slot:
-    // issue those loads before anything else so they land during set-up.
+    // The CTA's static item: split 0 of pair blockIdx.x, or, for the CTAs
+    // past the pairs, split 1 of pair blockIdx.x - static_items.  The producer
+    // needs its row's position and slot: issue those loads before anything
+    // else so they land during set-up.
+    const bool has_static = blockIdx.x < P.static_items + P.static_second;
+    const uint32_t st_split = blockIdx.x < P.static_items ? 0u : 1u;
+    const uint32_t st_row = (blockIdx.x - st_split * P.static_items) / P.n_kv_head;
     uint32_t pre_p = 0, pre_slot = 0;
-    if (warp == C::WARP_TMA && blockIdx.x < P.static_items) {
-        pre_p = __ldg(P.positions + blockIdx.x / P.n_kv_head);
-        if (!P.block_tables) pre_slot = __ldg(P.slots + blockIdx.x / P.n_kv_head);
+    if (warp == C::WARP_TMA && has_static) {
+        pre_p = __ldg(P.positions + st_row);
+        if (!P.block_tables) pre_slot = __ldg(P.slots + st_row);
     }
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
@@ -909,13 +938,12 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         // the consumers have finished item k-1) while item k's last tiles are
         // still streaming, so the prep warp has item k+1 ready before the
         // consumers reach it.
-        // Paged mode: the whole producer warp checks the static first item's
-        // row the way the plan does (p within the table, every used entry in
-        // the pool) and finds the row of key p.
+        // Paged mode: the whole producer warp checks the static item's row the
+        // way the plan does (p within the table, every used entry in the pool)
+        // and finds the row of key p.
         uint32_t pg_ok = 0, pg_prow = 0;
-        if (warp == C::WARP_TMA && P.block_tables != nullptr && blockIdx.x < P.static_items) {
-            const uint32_t* tab =
-                P.block_tables + static_cast<size_t>(blockIdx.x / P.n_kv_head) * P.bt_stride;
+        if (warp == C::WARP_TMA && P.block_tables != nullptr && has_static) {
+            const uint32_t* tab = P.block_tables + static_cast<size_t>(st_row) * P.bt_stride;
             bool bad = static_cast<uint64_t>(pre_p) >=
                        static_cast<uint64_t>(P.bt_stride) * P.slot_ctx;
             const uint32_t used = bad ? 0u : pre_p / P.slot_ctx + 1;
@@ -939,7 +967,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
             const bool paged = P.block_tables != nullptr;
             // The plan's list, its length and the hand-out counter may be read
             // only once the plan kernel has finished.  A CTA with a static
-            // first item waits for that lazily, streaming the item meanwhile.
+            // item waits for that lazily, streaming the item meanwhile.
             bool planned = false;
             uint32_t n_items = 0;
             auto await_plan = [&]() {
@@ -1006,27 +1034,26 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 }
                 return true;
             };
-            // first item: CTA c < static_items owns split 0 of (row, kv head)
-            // pair c.  Its inputs come from work that precedes the plan kernel
-            // on the stream, so they are complete; the plan checks the row the
-            // same way and leaves the item out of its list.  (The loads of p and
-            // the slot were issued at kernel entry.)
+            // first item: the CTA's static item (split st_split of pair
+            // blockIdx.x - st_split * static_items), if its row is in range
+            // and, for split 1, has a second split.  Its inputs come from work
+            // that precedes the plan kernel on the stream, so they are
+            // complete; the plan checks the row the same way and leaves the
+            // item out of its list.  (The loads of p and the slot were issued
+            // at kernel entry.)
             uint4 rec = make_uint4(0, 0, 0, 0);
             bool first_ok = false;
-            if (blockIdx.x < P.static_items) {
-                const uint32_t b = blockIdx.x / P.n_kv_head, kvh = blockIdx.x % P.n_kv_head;
+            if (has_static) {
+                const uint32_t kvh = (blockIdx.x - st_split * P.static_items) % P.n_kv_head;
                 const uint32_t p = pre_p, slot = pre_slot;
-                if (paged) {
-                    if (pg_ok) {
-                        rec = make_uint4(pack_item(b, 0, kvh), p, pg_prow, 0u);
-                        first_ok = true;
-                    }
-                } else if (slot < P.n_slots && p < P.slot_ctx) {
-                    rec = make_uint4(pack_item(b, 0, kvh), p, slot * P.slot_ctx + p, 0u);
-                    first_ok = true;
-                }
-                // without a plan kernel, the range flag is raised here
-                if (!first_ok && P.no_plan) atomicOr(P.status, kDevRange);
+                const bool in_range = paged ? pg_ok != 0u : (slot < P.n_slots && p < P.slot_ctx);
+                const uint32_t prow = paged ? pg_prow : slot * P.slot_ctx + p;
+                first_ok = in_range &&
+                           (st_split == 0 || p + 1 > split_chunk(p + 1, P.chunk_min, P.max_splits, T));
+                if (first_ok) rec = make_uint4(pack_item(st_row, st_split, kvh), p, prow, 0u);
+                // without a plan kernel (split-0 items only), the range flag
+                // is raised here
+                if (!in_range && P.no_plan) atomicOr(P.status, kDevRange);
             }
             if (!first_ok) {
                 await_plan();
@@ -1084,8 +1111,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                     tma_load_2d(dst + C::TILE_BYTES, &tmV, static_cast<int>(cur_kvh * HD), trow,
                                 full);
                     misc[2] = static_cast<int>(tile_g + 1);
-                    // (a static first item waits for the plan here, by when
-                    // the plan kernel has long finished)
+                    // (a static item waits for the plan here, by when the
+                    // plan kernel has long finished)
                     if (!claimed) {
                         if (t + kClaimLead >= cur_nt) claim();
                     } else if (!rec_n_loaded) {

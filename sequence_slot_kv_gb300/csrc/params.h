@@ -44,6 +44,11 @@ struct DecodeParams {
     // split 0 of (row c / n_kv_head, kv head c % n_kv_head) without waiting for
     // the plan, which leaves those items out of its list.  0: none.
     uint32_t static_items = 0;
+    // Static second items (only when static_items covers every pair): decode
+    // CTA static_items + q, q < static_second, starts with split 1 of pair q
+    // if that row has a second split, and the plan leaves those items out of
+    // its list too.  0: none.
+    uint32_t static_second = 0;
     // 1: every item is a static first item (no more (row, kv head) pairs than
     // CTAs, one split each): no plan kernel runs, its list is empty, and the
     // decode kernel is launched in plain stream order.

@@ -192,9 +192,10 @@ uint32_t auto_chunk(const slotkv_s* h, uint32_t B, uint64_t max_keys) {
 }
 
 // How a call of B rows runs: the split chunk, the persistent CTAs, the
-// static first items, whether the plan kernel runs, and the kernels launched.
+// static items (split 0 of the first pairs, then split 1 for CTAs to spare),
+// whether the plan kernel runs, and the kernels launched.
 struct CallShape {
-    uint32_t chunk, ctas, static_items, no_plan, kernels;
+    uint32_t chunk, ctas, static_items, static_second, no_plan, kernels;
 };
 
 CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill) {
@@ -205,10 +206,13 @@ CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool pref
     const uint64_t most = (uint64_t)B * h->n_kv_head * gsplits;
     const uint64_t want = 2ull * (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
     c.ctas = (uint32_t)(most < want ? most : want);
-    // each CTA's first item is split 0 of one (row, kv head) pair; when that
-    // covers every item (one split per row, a CTA per pair) no plan is needed
+    // CTA c < pairs starts on split 0 of pair c; when that covers every item
+    // (one split per row, a CTA per pair) no plan is needed
     const uint64_t pairs = (uint64_t)B * h->n_kv_head;
     c.static_items = (uint32_t)(pairs < c.ctas ? pairs : c.ctas);
+    // CTAs left over once every pair has one start on split 1 of a pair
+    const uint64_t spare = c.ctas - c.static_items;
+    c.static_second = (gsplits >= 2 && spare) ? (uint32_t)(spare < pairs ? spare : pairs) : 0u;
     c.no_plan = (gsplits == 1 && pairs <= c.ctas) ? 1u : 0u;
     c.kernels = (prefill ? 1u : 0u) + (c.no_plan ? 0u : 1u) + 1u;
     return c;
@@ -257,6 +261,7 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     const int G = (int)(n_head / h->n_kv_head);
     const unsigned ctas = cs.ctas;
     P.static_items = cs.static_items;
+    P.static_second = cs.static_second;
     P.no_plan = cs.no_plan;
     int rc;
     switch (h->head_dim) {

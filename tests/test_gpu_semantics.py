@@ -193,6 +193,43 @@ def test_call_shape():
         kv.free()
 
 
+@pytest.mark.parametrize("split", [None, (64, 16)])
+def test_spare_ctas_start_on_second_splits(split):
+    """With fewer (row, kv head) pairs than persistent CTAs, the CTAs past
+    the pairs start on split 1 of the first pairs: rows with one split, a
+    row out of range and a row whose kv heads straddle the end of that range
+    all come out as the oracle says, and the other rows too."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nkv, hd = 7, 64
+    B = (2 * sms - 24) // nkv          # 24 CTAs to spare: 3 rows and 3 kv heads
+    rng = np.random.default_rng(311)
+    pos = rng.integers(0, 2500, size=B)
+    pos[0], pos[2], pos[3], pos[4] = 5, 2499, 1024, 1023   # 1024 keys: one default chunk
+    w = synth.Workload("sem311", 311, B=B, n_slots=B + 3, slot_ctx=2500, n_head=2 * nkv,
+                       n_kv_head=nkv, head_dim=hd, theta=1e4, sinks=True, pos_rule="fixed",
+                       fixed_positions=tuple(int(x) for x in pos), slot_rule="perm")
+    run = DeviceRun(w, split=split)
+    try:
+        chunk, ctas, kernels = run.kv.call_shape(B)
+        assert kernels == 2 and ctas == 2 * sms > B * nkv
+        q, kn, vn, p = run.inputs(0)
+        slots = run.slots_np.copy()
+        slots[1] = w.n_slots + 1            # out of range, among the second splits
+        out = torch.full((B, w.n_head, hd), 7.0, device="cuda")
+        run.kv.decode_batch_attn(to_dev(q), to_dev(kn), to_dev(vn), to_dev(p.astype(np.int32)),
+                                 to_dev(slots.astype(np.int32)), run.qw, run.kw, run.inv,
+                                 run.sinks, out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert run.status() == skv.DEV_RANGE
+        got = out.cpu().numpy()
+        assert np.all(got[1] == 7.0)
+        rows = [b for b in range(B) if b != 1]
+        ref, _, _ = oracle_rows(w, rows)
+        assert_close(got[rows], ref[0], "rows")
+    finally:
+        run.close()
+
+
 def test_stale_history_is_never_read():
     """NaN in every position after pos of each row's slot changes nothing."""
     w = _wl(sinks=False, idx=301)
