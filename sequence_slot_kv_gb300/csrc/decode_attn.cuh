@@ -18,8 +18,9 @@
 //     until it is exhausted.  The
 //     steps of "Forward Cuda Gemma", decodeBatch, fused:
 //       - warp 4 (producer) streams the items' history K and V tiles into a
-//         3-stage shared-memory ring with 2-D TMA copies (cp.async.bulk.tensor,
-//         one [T keys x hd] box per tensor per stage) on mbarriers, running
+//         3-stage shared-memory ring (2 stages for hd 256 with G >= 4) with
+//         2-D TMA copies (cp.async.bulk.tensor, one [T keys x hd] box per
+//         tensor per stage) on mbarriers, running
 //         ahead across item boundaries, and stages each item's q (and, in the
 //         split holding key p, k_new and v_new) one item ahead;
 //       - warp 5 (prep) applies per-head RMS norm + RoPE to the staged vectors
@@ -70,6 +71,9 @@ constexpr uint32_t kOptNormPlusOne = 2u;  // SLOTKV_OPT_NORM_PLUS_ONE
 constexpr uint32_t kOptTestStall = 0x80000000u;  // SLOTKV_OPT_TEST_STALL
 constexpr int kPlanThreads = 1024;
 constexpr uint32_t kClaimLead = 4;  // tiles left in an item when the next is claimed
+// Dynamic shared memory a decode CTA may use for two to fit on an SM: 228 KB
+// per SM, of which 1 KB is reserved for each resident CTA.
+constexpr int kSmemPerCta = (228 * 1024) / 2 - 1024;
 
 __host__ __device__ constexpr int pow2_floor(int x) {
     int r = 1;
@@ -96,7 +100,6 @@ struct KCfg {
     // warpgroup 1 to warpgroup 0: 128 * REG_CONS + 128 * REG_HELP = 256 * 128
     static constexpr int REG_CONS = 184;
     static constexpr int REG_HELP = 72;
-    static constexpr int S = 3;                   // pipeline stages
     static constexpr int T = tile_keys(HD);       // keys per tile
     // elements per lane: keep G*E <= 64 (queries + accumulators in registers)
     static constexpr int E = cmax(4, cmax(HD / 32, cmin(32, pow2_floor(64 / G))));
@@ -114,27 +117,45 @@ struct KCfg {
     static constexpr int TILE_BYTES = T * HD * 4;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int NMS = 4;                 // split-merge hand-off slots
-    // shared memory: ring | chain scratch acc [G][HD], m, l [G] | per-item
+    // shared memory: ring [S] | chain scratch acc [G][HD], m, l [G] | per-item
     // slots [2] of (q [G][HD], k [HD], v [HD]) | norm weights, inv_freq |
-    // item descriptors [2] | hand-offs [NMS] | mbarriers | flags
-    static constexpr int OFF_CHAIN = S * STAGE_BYTES;
+    // item descriptors [2] | hand-offs [NMS] | mbarriers | flags.
+    // Offsets after the ring first, from 0:
     static constexpr int CHAIN_FLOATS = (G * HD + 2 * G + 3) / 4 * 4;
-    static constexpr int OFF_QBUF = OFF_CHAIN + CHAIN_FLOATS * 4;
-    static constexpr int OFF_KBUF = OFF_QBUF + 2 * G * HD * 4;
-    static constexpr int OFF_VBUF = OFF_KBUF + 2 * HD * 4;
-    static constexpr int OFF_QW = OFF_VBUF + 2 * HD * 4;
-    static constexpr int OFF_KW = OFF_QW + HD * 4;
-    static constexpr int OFF_IF = OFF_KW + HD * 4;
-    static constexpr int OFF_PBUF = OFF_IF + HD * 2;   // [NG][NV] probabilities
-    static constexpr int OFF_DESC = OFF_PBUF + (TR ? NG * NV * 4 : 0);
-    static constexpr int OFF_HAND = OFF_DESC + 2 * 64;
-    static constexpr int OFF_BAR = OFF_HAND + NMS * 16;
+    static constexpr int REL_QBUF = CHAIN_FLOATS * 4;
+    static constexpr int REL_KBUF = REL_QBUF + 2 * G * HD * 4;
+    static constexpr int REL_VBUF = REL_KBUF + 2 * HD * 4;
+    static constexpr int REL_QW = REL_VBUF + 2 * HD * 4;
+    static constexpr int REL_KW = REL_QW + HD * 4;
+    static constexpr int REL_IF = REL_KW + HD * 4;
+    static constexpr int REL_PBUF = REL_IF + HD * 2;   // [NG][NV] probabilities
+    static constexpr int REL_DESC = REL_PBUF + (TR ? NG * NV * 4 : 0);
+    static constexpr int REL_HAND = REL_DESC + 2 * 64;
+    static constexpr int REL_BAR = REL_HAND + NMS * 16;
     // mbarriers: full[S], empty[S], staged[2], prepared[2], slot_free[2],
-    // handed[NMS], hand_free[NMS]
-    static constexpr int NBAR = 2 * S + 6 + 2 * NMS;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int OFF_PEND = OFF_MISC + 16;  // the consumers' unmerged partial
-    static constexpr int SMEM = OFF_PEND + 32;
+    // handed[NMS], hand_free[NMS] (room kept for S = 3)
+    static constexpr int NBAR = 2 * 3 + 6 + 2 * NMS;
+    static constexpr int REL_MISC = REL_BAR + NBAR * 8;
+    static constexpr int REL_PEND = REL_MISC + 16;  // the consumers' unmerged partial
+    static constexpr int REL_END = REL_PEND + 32;
+    // pipeline stages: three, or two where three would leave no room for a
+    // second CTA on the SM (hd 256 with G >= 4)
+    static constexpr int S = 3 * STAGE_BYTES + REL_END <= kSmemPerCta ? 3 : 2;
+    static constexpr int OFF_CHAIN = S * STAGE_BYTES;
+    static constexpr int OFF_QBUF = OFF_CHAIN + REL_QBUF;
+    static constexpr int OFF_KBUF = OFF_CHAIN + REL_KBUF;
+    static constexpr int OFF_VBUF = OFF_CHAIN + REL_VBUF;
+    static constexpr int OFF_QW = OFF_CHAIN + REL_QW;
+    static constexpr int OFF_KW = OFF_CHAIN + REL_KW;
+    static constexpr int OFF_IF = OFF_CHAIN + REL_IF;
+    static constexpr int OFF_PBUF = OFF_CHAIN + REL_PBUF;
+    static constexpr int OFF_DESC = OFF_CHAIN + REL_DESC;
+    static constexpr int OFF_HAND = OFF_CHAIN + REL_HAND;
+    static constexpr int OFF_BAR = OFF_CHAIN + REL_BAR;
+    static constexpr int OFF_MISC = OFF_CHAIN + REL_MISC;
+    static constexpr int OFF_PEND = OFF_CHAIN + REL_PEND;
+    static constexpr int SMEM = OFF_CHAIN + REL_END;
+    static_assert(SMEM <= kSmemPerCta, "two CTAs per SM");
     static_assert(L >= 1 && L <= 32 && (32 % L) == 0, "lane group must divide a warp");
     static_assert(E % 4 == 0 && E * L == HD, "lane slice must be whole float4s");
     static_assert(R >= 1 && R * NG == T, "tile must split evenly over the groups");
@@ -1685,6 +1706,13 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
         e = cudaFuncGetAttributes(&fa, slotkv_decode_attn_kernel<HD, G>);
         if (e != cudaSuccess) return static_cast<int>(e);
         if (fa.numRegs != 128) return static_cast<int>(cudaErrorInvalidConfiguration);
+        // the grid (two CTAs per SM) and its static items assume that both
+        // CTAs of an SM are resident at once
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, slotkv_decode_attn_kernel<HD, G>,
+                                                          C::THREADS, C::SMEM);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        if (per_sm < 2) return static_cast<int>(cudaErrorInvalidConfiguration);
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     if (p.prefill) {
