@@ -40,7 +40,7 @@ FLUSH_BYTES = 256 * 1024 * 1024  # written between calls of a step that fits in 
 # the kernel source it was taken on (sha256 prefix of decode_attn.cuh); see
 # profiles/decode_attn_<workload>.md.
 MEASURED_TRAFFIC = {
-    "dc783fcec7b078e4": {"mid": 556_234_240, "sinks": 2_342_272_504},
+    "059be226d9cde986": {"mid": 555_429_632, "sinks": 2_342_728_192},
 }
 
 
@@ -570,13 +570,37 @@ def run_prefill(args):
         step()
     torch.cuda.synchronize(dev)
     assert kv.get_status(sp) == 0
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
     b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("begin")
     b.record(stream)
     for _ in range(args.steps):
         step()
     e.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark("end")
+    clk = clocks.stop()
     ms = b.elapsed_time(e) / args.steps
+
+    # End to end: every step copies its inputs from page-locked host memory,
+    # runs the call and reads the output back, on the call's stream.
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    hq, hkn, hvn, hps, hss = pin(w.q()), pin(w.k_new()), pin(w.v_new()), pin(pos), pin(slots)
+    hout = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            for dst, src in ((q, hq), (kn, hkn), (vn, hvn), (ps, hps), (ss, hss)):
+                dst.copy_(src, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hkn, hvn, hps, hss))
+    d2h = hout.numel() * hout.element_size()
     # bytes as the path reads them: every token reads its own keys 0..pos
     per_token_bytes = int((pos.astype(np.int64) + 1).sum()) * 2 * w.kv_dim * 4
     io = n_tok * (2 * w.n_head * w.head_dim + 4 * w.kv_dim) * 4
@@ -598,7 +622,10 @@ def run_prefill(args):
                          "kernel": "slotkv_decode_attn_kernel (prefill mode)"},
             "key_bytes_read_per_step": per_token_bytes, "io_bytes_per_step": io,
             "effective_GBps": (per_token_bytes + io) / (ms / 1e3) / 1e9,
-            "gpu_launches": args.steps * kv.call_shape(n_tok, prefill=True)[2]}
+            "e2e": {"value": n_tok / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * kv.call_shape(n_tok, prefill=True)[2],
+            "clocks": clk}
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         v, desc = time_oracle_prefill(w, slots, pos, n_seq, chunk, args.cpu_budget, cores)
