@@ -106,8 +106,13 @@ struct KCfg {
     static constexpr int L = HD / E;              // lanes per key group
     static constexpr int NG = CONS / L;           // key groups per CTA
     static constexpr int R = T / NG;              // keys per group per tile
-    // keys attended per softmax update: keeps the live scores (RC*G) <= 16
-    static constexpr int RC = pow2_floor(cmax(1, cmin(R, 16 / G)));
+    // keys attended per softmax update: keeps the live scores (RC*G) <= 16,
+    // or <= 32 where only that many give the transposed reduction (below)
+    // one value per lane (hd 256 with G >= 5)
+    static constexpr int RC_S = pow2_floor(cmax(1, cmin(R, 16 / G)));
+    static constexpr int RC_L = pow2_floor(cmax(1, cmin(R, 32 / G)));
+    static constexpr int RC =
+        RC_S * pow2_ceil(G) < L && RC_L * pow2_ceil(G) >= L ? RC_L : RC_S;
     // transposed reduction (see attend_rows_tr): G padded to a power of two,
     // values per lane after the reduction; used when every lane keeps >= 1
     static constexpr int GP = pow2_ceil(G);
