@@ -166,6 +166,69 @@ def test_many_rows(layout):
         run.close()
 
 
+def test_maximum_rows():
+    """65535 rows, the most a call takes: the plan kernel's 64 rounds, row
+    indices in all 16 bits of a work record; sampled rows against the oracle,
+    every written row, every other byte."""
+    B = 65535
+    w = synth.Workload("max_rows", 331, B=B, n_slots=B, slot_ctx=64, n_head=1, n_kv_head=1,
+                       head_dim=64, theta=1e4, sinks=False, slot_rule="perm")
+    run = DeviceRun(w)
+    try:
+        out = run.step(0)
+        torch.cuda.synchronize()
+        assert run.status() == 0
+        rng = np.random.default_rng(331)
+        rows = sorted({0, 1, 1023, 1024, 32767, 32768, B - 2, B - 1}
+                      | set(int(r) for r in rng.choice(B, size=400, replace=False)))
+        ref, _, _ = oracle_rows(w, rows, n_threads=32)
+        assert_close(out.cpu().numpy()[rows], ref[0], "sampled rows of 65535")
+        check_kv_after(run)
+    finally:
+        run.close()
+
+
+def test_maximum_splits():
+    """256 splits, the most a row can have (split indices in all 8 bits of a
+    work record): a fixed policy of one tile per split and rows at 256, 255
+    and fewer tiles."""
+    hd = 64
+    T = 4096 // hd
+    ctx = 256 * T
+    pos = (ctx - 1, ctx - T - 1, ctx - T, 255 * T - 1, 100 * T + 3, T - 1, 0)
+    w = synth.Workload("max_splits", 332, B=len(pos), n_slots=len(pos) + 1, slot_ctx=ctx,
+                       n_head=2, n_kv_head=1, head_dim=hd, theta=1e4, sinks=True,
+                       pos_rule="fixed", fixed_positions=pos, slot_rule="perm")
+    run = DeviceRun(w, split=(T, 256))
+    try:
+        out = run.step(0)
+        torch.cuda.synchronize()
+        assert run.status() == 0
+        ref, _, _ = oracle_rows(w, range(w.B))
+        assert_close(out.cpu().numpy(), ref[0], "256 splits")
+        check_kv_after(run)
+    finally:
+        run.close()
+
+
+def test_maximum_kv_heads():
+    """256 kv heads, the most a handle takes (kv head indices in all 8 bits
+    of a work record), one query head each."""
+    w = synth.Workload("max_kvh", 333, B=3, n_slots=4, slot_ctx=200, n_head=256, n_kv_head=256,
+                       head_dim=64, theta=1e4, sinks=True, pos_rule="fixed",
+                       fixed_positions=(199, 64, 0), slot_rule="perm")
+    run = DeviceRun(w)
+    try:
+        out = run.step(0)
+        torch.cuda.synchronize()
+        assert run.status() == 0
+        ref, _, _ = oracle_rows(w, range(w.B))
+        assert_close(out.cpu().numpy(), ref[0], "256 kv heads")
+        check_kv_after(run)
+    finally:
+        run.close()
+
+
 def test_call_shape():
     """slot_kv_call_shape reports what a call launches: the decode kernel
     alone when every item is a CTA's first item (a few short rows), with the
