@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <new>
 
 #include "../../include/slotkv.h"
@@ -37,17 +38,22 @@ typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     CUtensorMapSwizzle, CUtensorMapL2promotion,
                                     CUtensorMapFloatOOBfill);
 
+// Looked up on first use; an atomic, so handles may be allocated from
+// several threads at once (a failed lookup is retried on the next call).
 encode_tiled_fn get_encoder() {
-    static encode_tiled_fn fn = nullptr;
-    if (!fn) {
+    static std::atomic<encode_tiled_fn> fn{nullptr};
+    encode_tiled_fn f = fn.load(std::memory_order_acquire);
+    if (!f) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<encode_tiled_fn>(p);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<encode_tiled_fn>(p);
+            fn.store(f, std::memory_order_release);
+        }
     }
-    return fn;
+    return f;
 }
 
 }  // namespace
