@@ -252,24 +252,34 @@ def time_oracle(w, budget_s, n_threads, flags=0, paged_bs=0):
 
 
 def run_reference(args, w):
+    """The CPU oracle, as it stands, on this arm's workload (prefill, paged
+    layout and norm options included), each step a bounded sample of it."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
     cores = os.cpu_count() or 1
-    smp = OracleSample(w, cores)
+    if args.prefill:
+        w, slots, pos = prefill_workload()
+        smp = PrefillOracleSample(w, slots, pos, cores)
+        per_step, unit = smp.n_seq, "tokens/s"
+        metric, config = "slot-attn prefill tokens/s", prefill_config(w)
+    else:
+        smp = OracleSample(w, cores, flags=args.options, paged_bs=args.paged)
+        per_step, unit = len(smp.rows), "rows/s"
+        metric, config = "slot-attn decode rows/s", config_of(w, args)
     for _ in range(args.warmup):
         smp.step()
     spent = sum(smp.step() for _ in range(args.steps))
-    value = len(smp.rows) * args.steps / spent
+    value = per_step * args.steps / spent
     line = {
-        "impl": "reference", "metric": "slot-attn decode rows/s", "value": value,
-        "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "impl": "reference", "metric": metric, "value": value,
+        "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w),
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+        "config": config,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": smp.describe(args.steps, spent)},
-        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -281,14 +291,21 @@ OPTION_NAMES = {1: "weightless V norm", 2: "(1 + w) Q/K norm weights",
                 3: "weightless V norm and (1 + w) Q/K norm weights"}
 
 
-def config_of(w):
-    return {"workload": w.name, "B": w.B, "n_slots": w.n_slots, "slot_ctx": w.slot_ctx,
-            "n_head": w.n_head, "n_kv_head": w.n_kv_head, "head_dim": w.head_dim,
-            "steps_per_call_sequence": w.steps, "sinks": w.sinks,
-            "l2": ("inputs larger than L2 (history K/V read per step >> 129 MB)"
-                   if w.alg_bytes(w.positions(0)) >= 2 * L2_BYTES else
-                   f"L2 flushed between calls ({FLUSH_BYTES >> 20} MiB written outside "
-                   f"the timed calls)")}
+def config_of(w, args=None):
+    """The workload's config; with ``args``, its layout and norm options."""
+    cfg = {"workload": w.name, "B": w.B, "n_slots": w.n_slots, "slot_ctx": w.slot_ctx,
+           "n_head": w.n_head, "n_kv_head": w.n_kv_head, "head_dim": w.head_dim,
+           "steps_per_call_sequence": w.steps, "sinks": w.sinks,
+           "l2": ("inputs larger than L2 (history K/V read per step >> 129 MB)"
+                  if w.alg_bytes(w.positions(0)) >= 2 * L2_BYTES else
+                  f"L2 flushed between calls ({FLUSH_BYTES >> 20} MiB written outside "
+                  f"the timed calls)")}
+    if args is not None and args.paged:
+        cfg.update({"kv_layout": "paged", "block_size": args.paged,
+                    "block_order": "seeded shuffle over the pool"})
+    if args is not None and args.options:
+        cfg["norm_options"] = OPTION_NAMES[args.options]
+    return cfg
 
 
 def run_gpu(args, w):
@@ -502,10 +519,7 @@ def run_gpu(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_of(w), **({"kv_layout": "paged", "block_size": bs,
-                                          "block_order": "seeded shuffle over the pool"}
-                                         if bs else {}),
-                       **({"norm_options": OPTION_NAMES[args.options]} if args.options else {})),
+        "config": config_of(w, args),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": args.traffic if args.traffic is not None
@@ -533,17 +547,37 @@ def run_gpu(args, w):
         torch.distributed.destroy_process_group()
 
 
+PREFILL_SEQ, PREFILL_HIST, PREFILL_CHUNK = 8, 1536, 512
+
+
+def prefill_workload():
+    """The prefill workload at the mid geometry: 8 sequences in slots 0, 2,
+    .., 14, each adding a 512-token prompt chunk after 1536 positions of
+    history.  Returns the workload (one row per token) and the tokens' slots
+    and positions."""
+    n_seq, hist, chunk = PREFILL_SEQ, PREFILL_HIST, PREFILL_CHUNK
+    n_tok = n_seq * chunk
+    w = synth.WORKLOADS["mid"].replace(
+        name="prefill", index=20, B=n_tok, n_slots=16, slot_ctx=hist + chunk,
+        pos_rule="fixed", fixed_positions=tuple([0] * n_tok))
+    slots = np.repeat(np.arange(n_seq, dtype=np.int32) * 2, chunk)
+    pos = np.tile(np.arange(hist, hist + chunk, dtype=np.int32), n_seq)
+    return w, slots, pos
+
+
+def prefill_config(w):
+    return {"workload": "prefill", "sequences": PREFILL_SEQ, "history": PREFILL_HIST,
+            "prompt_chunk": PREFILL_CHUNK, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
+            "head_dim": w.head_dim}
+
+
 def run_prefill(args):
-    """Batched causal prefill at the mid geometry: 8 sequences, each adding a
-    512-token prompt chunk after 1536 positions of history.  A step is one
+    """Batched causal prefill (prefill_workload).  A step is one
     prefill_batch_attn call over all 4096 tokens."""
     import torch
     import sequence_slot_kv_gb300 as skv
-    n_seq, hist, chunk = 8, 1536, 512
-    base = synth.WORKLOADS["mid"]
-    n_tok = n_seq * chunk
-    w = base.replace(name="prefill", index=20, B=n_tok, n_slots=16, slot_ctx=hist + chunk,
-                     pos_rule="fixed", fixed_positions=tuple([0] * n_tok))
+    w, slots, pos = prefill_workload()
+    n_tok = w.B
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
@@ -554,8 +588,6 @@ def run_prefill(args):
     w.dev_fill_history(K.data_ptr(), V.data_ptr(), sp)
     kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, n_tok, w.n_head,
                     k_buf=K, v_buf=V)
-    slots = np.repeat(np.arange(n_seq, dtype=np.int32) * 2, chunk)
-    pos = np.tile(np.arange(hist, hist + chunk, dtype=np.int32), n_seq)
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     q, kn, vn = d(w.q()), d(w.k_new()), d(w.v_new())
     ps, ss = d(pos), d(slots)
@@ -613,9 +645,7 @@ def run_prefill(args):
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "prefill", "sequences": n_seq, "history": hist,
-                       "prompt_chunk": chunk, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
-                       "head_dim": w.head_dim},
+            "config": prefill_config(w),
             "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "peak_kind": peak_kind, "traffic": None,
                          "alg_flops_per_launch": flops, "avg_launch_us": ms * 1e3,
@@ -628,7 +658,7 @@ def run_prefill(args):
             "clocks": clk}
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        v, desc = time_oracle_prefill(w, slots, pos, n_seq, chunk, args.cpu_budget, cores)
+        v, desc = time_oracle_prefill(w, slots, pos, args.cpu_budget, cores)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
                                 "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
@@ -649,36 +679,60 @@ def alu_peak_f32(dev):
     return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 FP32 lanes x 2 x {mhz:.0f} MHz"
 
 
-def time_oracle_prefill(w, slots, pos, n_seq, chunk, budget_s, n_threads):
-    """tokens/s of the oracle on the prefill workload: each call takes the next
-    token of every sequence (one decode step per token, in position order,
-    the sequences' tokens in parallel) on host copies of their slots, until
-    ``budget_s``."""
-    import oracle
-    o = oracle.default()
-    seq_slots = slots[::chunk].astype(np.int64)
-    first = pos[::chunk].astype(np.int64)
-    ctx = int(first.max()) + chunk
-    K = np.empty((n_seq, ctx, w.n_kv_head, w.head_dim), dtype=np.float32)
-    V = np.empty_like(K)
-    for i, s_ in enumerate(seq_slots):
-        K[i] = w.hist_rows("k", s_, 0, ctx)
-        V[i] = w.hist_rows("v", s_, 0, ctx)
-    q, kn, vn = w.q(), w.k_new(), w.v_new()
-    compact = np.arange(n_seq, dtype=np.uint32)
-    calls, spent = 0, 0.0
-    while spent < budget_s and calls < chunk:
-        rows = np.arange(n_seq) * chunk + calls
+class PrefillOracleSample:
+    """The CPU oracle on the prefill workload, as it stands: each call takes
+    the next prompt token of every sequence (one decode step per token, in
+    position order, the sequences' tokens in parallel) on host copies of the
+    sequences' slots (regenerated once, outside any timing).  After the last
+    token of the chunk it starts again from the first; the rows a call
+    rewrites are the ones it wrote the first time, so calls repeat exactly."""
+
+    def __init__(self, w, slots, pos, n_threads):
+        import oracle
+        self.o = oracle.default()
+        self.w, self.pos = w, pos
+        n_seq, chunk = PREFILL_SEQ, PREFILL_CHUNK
+        self.n_seq, self.chunk = n_seq, chunk
+        self.n_threads = min(n_threads, n_seq)
+        seq_slots = slots[::chunk].astype(np.int64)
+        self.first = pos[::chunk].astype(np.int64)
+        ctx = int(self.first.max()) + chunk
+        self.K = np.empty((n_seq, ctx, w.n_kv_head, w.head_dim), dtype=np.float32)
+        self.V = np.empty_like(self.K)
+        for i, s_ in enumerate(seq_slots):
+            self.K[i] = w.hist_rows("k", s_, 0, ctx)
+            self.V[i] = w.hist_rows("v", s_, 0, ctx)
+        self.q, self.kn, self.vn = w.q(), w.k_new(), w.v_new()
+        self.compact = np.arange(n_seq, dtype=np.uint32)
+        self.calls = 0
+
+    def step(self):
+        w = self.w
+        rows = np.arange(self.n_seq) * self.chunk + self.calls % self.chunk
         t0 = time.perf_counter()
-        o.decode_batch(K, V, q[rows], kn[rows], vn[rows], pos[rows].astype(np.uint32), compact,
-                       w.q_norm_w(), w.k_norm_w(), w.inv_freq(), w.sink_logits(), w.eps,
-                       w.scale, n_threads=min(n_threads, n_seq))
-        spent += time.perf_counter() - t0
+        self.o.decode_batch(self.K, self.V, self.q[rows], self.kn[rows], self.vn[rows],
+                            self.pos[rows].astype(np.uint32), self.compact, w.q_norm_w(),
+                            w.k_norm_w(), w.inv_freq(), w.sink_logits(), w.eps, w.scale,
+                            n_threads=self.n_threads)
+        self.calls += 1
+        return time.perf_counter() - t0
+
+    def describe(self, calls, seconds):
+        last = int(self.first.max()) + min(calls, self.chunk) - 1
+        return (f"{calls} calls of one prompt token of each of the {self.n_seq} sequences "
+                f"(one decode step per token, positions {int(self.first.min())}..{last}), "
+                f"{seconds:.1f} s, the sequences split over {self.n_threads} threads")
+
+
+def time_oracle_prefill(w, slots, pos, budget_s, n_threads):
+    """tokens/s of the oracle on the prefill workload over calls until
+    ``budget_s`` (at most one pass over the chunk)."""
+    smp = PrefillOracleSample(w, slots, pos, n_threads)
+    calls, spent = 0, 0.0
+    while spent < budget_s and calls < PREFILL_CHUNK:
+        spent += smp.step()
         calls += 1
-    desc = (f"the first {calls} prompt tokens of each of the {n_seq} sequences (one decode "
-            f"step per token, positions {int(first.min())}..{int(first.max()) + calls - 1}), "
-            f"{spent:.1f} s, the sequences split over {min(n_threads, n_seq)} threads")
-    return n_seq * calls / spent, desc
+    return smp.n_seq * calls / spent, smp.describe(calls, spent)
 
 
 def main():
@@ -706,12 +760,11 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     args.options = {"": 0, "vnorm": 1, "plus_one": 2, "both": 3}[args.options]
-    if args.prefill:
-        run_prefill(args)
-        return
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.prefill:
+        run_prefill(args)
     else:
         run_gpu(args, w)
 
