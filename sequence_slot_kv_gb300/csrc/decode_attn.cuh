@@ -114,11 +114,12 @@ struct KCfg {
     static constexpr int RC =
         RC_S * pow2_ceil(G) < L && RC_L * pow2_ceil(G) >= L ? RC_L : RC_S;
     // transposed reduction (see attend_rows_tr): G padded to a power of two,
-    // values per lane after the reduction; used when every lane keeps >= 1
+    // values per lane after the reduction (each held by L / NV lanes when
+    // there are fewer values than lanes); used from four values up
     static constexpr int GP = pow2_ceil(G);
     static constexpr int NV = RC * GP;
-    static constexpr bool TR = NV >= L && NV >= 4;
-    static constexpr int CNT = TR ? NV / L : 1;
+    static constexpr bool TR = NV >= 4;
+    static constexpr int CNT = NV >= L ? NV / L : 1;
     static constexpr int TILE_BYTES = T * HD * 4;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int NMS = 4;                 // split-merge hand-off slots
@@ -412,9 +413,12 @@ __device__ __forceinline__ void attend_rows(const float* __restrict__ Kt,
 // NR * GP partial dots of a lane (key r, head h at index r * GP + h; heads
 // past G are zero) are summed over the L lanes of the group by halving, so
 // after log2(L) levels lane li holds the complete scores of indices
-// li * CNT + j, j < CNT: one key, CNT consecutive heads.  Only those scores
-// get exponentials; the probabilities go to the group's NV-float buffer
-// `pg` and every lane reads all of them back for the value update.
+// li * CNT + j, j < CNT: one key, CNT consecutive heads.  With fewer values
+// than lanes (NV < L) the halving stops at one value per lane and the last
+// log2(REP) levels sum by butterfly, so the REP = L / NV lanes li with the
+// same li / REP all hold index li / REP.  Only those scores get
+// exponentials; the probabilities go to the group's NV-float buffer `pg`
+// and every lane reads all of them back for the value update.
 // State: the running max m_t[j] and sum l_t[j] of this lane's heads (equal
 // across the lanes holding the same heads for other keys), acc as usual.
 // The running max is lazy: it is raised (and acc, l rescaled) only when a
@@ -428,6 +432,7 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
                                                float (&l_t)[CNT], float (&acc)[G][E],
                                                float* __restrict__ pg) {
     constexpr int NV = NR * GP;
+    constexpr int REP = NV >= L ? 1 : L / NV;  // lanes holding each score
     constexpr float kLazy = 8.0f;
     float s[NV];
 #pragma unroll
@@ -445,9 +450,10 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
 #pragma unroll
         for (int h = 0; h < GP; ++h) s[r * GP + h] = h < G ? dot_e<E>(q[h < G ? h : 0], kv) : 0.f;
     }
-    // halving reduction over the group's lanes
+    // halving reduction over the group's lanes, then (NV < L) a butterfly
+    // over the REP lanes left holding partial sums of the same value
 #pragma unroll
-    for (int off = L / 2, cnt = NV; off >= 1; off >>= 1, cnt >>= 1) {
+    for (int off = L / 2, cnt = NV; off >= REP; off >>= 1, cnt >>= 1) {
         const bool upper = (li & off) != 0;
 #pragma unroll
         for (int i = 0; i < cnt / 2; ++i) {
@@ -456,8 +462,10 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
             s[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
+#pragma unroll
+    for (int off = REP / 2; off >= 1; off >>= 1) s[0] += __shfl_xor_sync(0xffffffffu, s[0], off);
     // this lane's key and first head
-    const int v0 = li * CNT;
+    const int v0 = li / REP * CNT;
     const int my_r = v0 / GP;
     bool my_valid = valid[0];
 #pragma unroll
@@ -471,7 +479,7 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
     }
     // max over the keys, per head: lanes holding the same heads for other keys
 #pragma unroll
-    for (int off = GP / CNT; off < L && off < NR * GP / CNT; off <<= 1) {
+    for (int off = GP / CNT * REP; off < L; off <<= 1) {
 #pragma unroll
         for (int j = 0; j < CNT; ++j) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
     }
@@ -488,11 +496,11 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
             m_t[j] = mn;
         }
         // every lane rescales acc for every head: take head h's factor from
-        // the lane that holds it for key 0
+        // the (first) lane that holds it for key 0
         const int gbase = lane - li;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float c = __shfl_sync(0xffffffffu, corr[h % CNT], gbase + h / CNT);
+            const float c = __shfl_sync(0xffffffffu, corr[h % CNT], gbase + h / CNT * REP);
             scale_e<E>(c, acc[h]);
         }
     }
@@ -500,7 +508,7 @@ __device__ __forceinline__ void attend_rows_tr(const float* __restrict__ Kt,
     for (int j = 0; j < CNT; ++j) {
         const float pj = s[j] == -CUDART_INF_F ? 0.f : exp2f(s[j] - m_t[j]);
         l_t[j] += pj;
-        pg[v0 + j] = pj;
+        if (li % REP == 0) pg[v0 + j] = pj;
     }
     __syncwarp();
     float pr[NV];
@@ -540,16 +548,17 @@ template <int G, int L, int NR, int GP, int CNT>
 __device__ __forceinline__ void tr_state_to_heads(const int li, const int lane, float (&m_t)[CNT],
                                                   float (&l_t)[CNT], float (&m)[G],
                                                   float (&l)[G]) {
+    constexpr int REP = NR * GP >= L ? 1 : L / (NR * GP);  // as in attend_rows_tr
 #pragma unroll
-    for (int off = GP / CNT; off < L && off < NR * GP / CNT; off <<= 1) {
+    for (int off = GP / CNT * REP; off < L; off <<= 1) {
 #pragma unroll
         for (int j = 0; j < CNT; ++j) l_t[j] += __shfl_xor_sync(0xffffffffu, l_t[j], off);
     }
     const int gbase = lane - li;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        m[h] = __shfl_sync(0xffffffffu, m_t[h % CNT], gbase + h / CNT);
-        l[h] = __shfl_sync(0xffffffffu, l_t[h % CNT], gbase + h / CNT);
+        m[h] = __shfl_sync(0xffffffffu, m_t[h % CNT], gbase + h / CNT * REP);
+        l[h] = __shfl_sync(0xffffffffu, l_t[h % CNT], gbase + h / CNT * REP);
     }
 }
 
