@@ -71,7 +71,7 @@ enum slotkv_device_flags {
  *              frees any prior slot KV first).  Receives the new handle.
  *   n_slots    number of concurrent sequences (slots), >= 1.
  *   slot_ctx   positions per slot, >= 1; n_slots * slot_ctx < 2^31 - 256.
- *   n_kv_head  kv heads per position, >= 1.
+ *   n_kv_head  kv heads per position, 1..256.
  *   head_dim   64, 128 or 256.
  *   k_buf, v_buf
  *              NULL, NULL: the library allocates both buffers (zero-filled)
@@ -79,7 +79,7 @@ enum slotkv_device_flags {
  *              buffers of n_slots*slot_ctx*kv_dim f32, 16-byte aligned; they are
  *              adopted (used in place, never freed by the library).
  *              Layout of each: [n_slots][slot_ctx][n_kv_head][head_dim].
- *   max_rows   the largest B a decode call will pass, >= 1.
+ *   max_rows   the largest B a decode call will pass, 1..65535.
  *   max_n_head the largest n_head a decode call will pass; G = n_head /
  *              n_kv_head must be 1..8.
  *
@@ -161,7 +161,9 @@ int slot_kv_geometry(slotkv_t handle, uint32_t* n_slots, uint32_t* slot_ctx,
  * decodeBatch precondition) are skipped on the device and raise
  * SLOTKV_DEV_RANGE.  Host-side errors: SLOTKV_ERR_ARG (NULL or misaligned
  * pointer, B or n_head too large, n_head not a multiple of n_kv_head),
- * SLOTKV_ERR_UNSUPPORTED (G outside 1..8), SLOTKV_ERR_CUDA (launch failure).
+ * SLOTKV_ERR_UNSUPPORTED (G outside 1..8), SLOTKV_ERR_CUDA (launch failure,
+ * including a GPU on which two of the persistent decode CTAs do not fit on
+ * one SM).
  */
 int decode_batch_attn(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
                       const float* k_new, const float* v_new, const uint32_t* positions,
