@@ -45,3 +45,53 @@ def test_host_only_checks_without_gpu():
     assert not h.value
     assert lib.decode_batch_attn(None, 1, 2, *([None] * 10), 1e-6, 0.1, None) == 4
     assert lib.slot_kv_free(None) == 0
+
+
+def test_more_host_checks_without_gpu():
+    """Every size and pointer check that precedes a CUDA call, on the handle
+    entry points and on the allocation-free one."""
+    ARG, UNSUP, STATE = 1, 3, 4
+    lib = skv._lib
+    h = ctypes.c_void_p()
+    byref = ctypes.byref
+    # n_kv_head past 256, max_rows 0 and past 65535, max_n_head outside n_kv..8*n_kv
+    assert lib.slot_kv_alloc(byref(h), 4, 16, 257, 64, None, None, 1, 257) == ARG
+    assert "n_kv_head" in skv.last_error()
+    assert lib.slot_kv_alloc(byref(h), 4, 16, 2, 64, None, None, 0, 2) == ARG
+    assert lib.slot_kv_alloc(byref(h), 4, 16, 2, 64, None, None, 65536, 2) == ARG
+    assert "max_rows" in skv.last_error()
+    assert lib.slot_kv_alloc(byref(h), 4, 16, 2, 64, None, None, 1, 1) == ARG
+    assert "max_n_head" in skv.last_error()
+    # adopted buffers: both or neither, 16-byte aligned
+    assert lib.slot_kv_alloc(byref(h), 4, 16, 2, 64, None, ctypes.c_void_p(256), 1, 2) == ARG
+    assert lib.slot_kv_alloc(byref(h), 4, 16, 2, 64, ctypes.c_void_p(260), ctypes.c_void_p(256),
+                             1, 2) == ARG
+    assert "aligned" in skv.last_error()
+    assert lib.slot_kv_alloc(None, 4, 16, 2, 64, None, None, 1, 2) == ARG
+    assert not h.value
+    # calls on no handle
+    u = ctypes.c_uint32()
+    assert lib.slot_kv_set_split(None, 64, 8) == STATE
+    assert lib.slot_kv_set_options(None, 0) == STATE
+    assert lib.slot_kv_call_shape(None, 1, 0, 0, byref(u), byref(u), byref(u)) == STATE
+    assert lib.slot_kv_reset(None, 0, None) == STATE
+    assert lib.slot_kv_get_status(None, None, byref(u)) == ARG
+    # the allocation-free entry: checks before any device work
+    p16 = ctypes.c_void_p(1 << 20)     # never dereferenced: every call below fails first
+    p4 = ctypes.c_void_p((1 << 20) + 4)
+    args = lambda **kw: [kw.get(k, d) for k, d in (
+        ("K", p16), ("V", p16), ("n_slots", 4), ("slot_ctx", 16), ("n_kv", 2), ("hd", 64),
+        ("B", 1), ("n_head", 4), ("q", p16), ("k", p16), ("v", p16), ("pos", p16),
+        ("slots", p16), ("qw", p16), ("kw", p16), ("inv", p16), ("sinks", None),
+        ("out", p16), ("flags", None), ("eps", 1e-6), ("scale", 0.125), ("stream", None))]
+    na = lib.decode_batch_attn_noalloc
+    assert na(*args(B=0, K=None)) == 0                      # nothing to do
+    assert na(*args(K=None)) == ARG
+    assert na(*args(q=p4)) == ARG and "16-byte" in skv.last_error()
+    assert na(*args(pos=ctypes.c_void_p((1 << 20) + 2))) == ARG
+    assert na(*args(hd=96)) == UNSUP
+    assert na(*args(n_head=3)) == UNSUP
+    assert na(*args(n_head=18)) == UNSUP                    # G = 9
+    assert na(*args(n_kv=257, n_head=257)) == ARG
+    assert na(*args(B=65536)) == ARG
+    assert na(*args(n_slots=1 << 16, slot_ctx=1 << 15)) == ARG
