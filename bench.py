@@ -3,15 +3,23 @@
 A step is one decode_batch_attn call over the workload's B rows (for the
 multi-step workload, its 64 consecutive calls).  Prints one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mid]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large]
                     [--impl gpu|reference]
 
-value      rows/s with every input resident in HBM, CUDA events on the
-           launching stream around exactly K steps (max over ranks);
-e2e        the same metric through decode_batch_attn_host: per step the
-           inputs are copied from pinned host memory and the output back;
-roofline   the decode kernel's algorithmic HBM bytes per launch over its
-           average launch time, against the measured copy bandwidth;
+The default workload is the largest single-GPU configuration: 256 rows on
+512 slots of 2048 positions, 40 query / 8 kv heads, head dim 128, 64
+consecutive decode steps per bench step.
+
+value       rows/s with every input resident in HBM, CUDA events on the
+            launching stream around exactly K steps (max over ranks); the
+            W warm-up steps run directly before the timed region;
+e2e         the same metric through decode_batch_attn_host: per step the
+            inputs are copied from pinned host memory and the output back;
+roofline    one decode call's algorithmic HBM bytes over its mean (and
+            median) CUDA-event time, against the measured copy bandwidth;
+per_config  the same figures for each of the four bandwidth-target
+            workloads (mid, skewed, sinks, large), each timed on its own in
+            the same run;
 cpu_baseline  the CPU oracle on the host's cores over a bounded sample.
 Under torchrun each rank runs its own copy of the workload on its own GPU
 (rows are independent; no collective on the data path): weak scaling.
@@ -36,9 +44,9 @@ HBM_FALLBACK_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024     # GB300 L2
 FLUSH_BYTES = 256 * 1024 * 1024  # written between calls of a step that fits in L2
 
-# DRAM bytes (read + write) per decode launch from one ncu capture, valid for
-# the kernel source it was taken on (sha256 prefix of decode_attn.cuh); see
-# profiles/decode_attn_<workload>.md.
+# DRAM bytes (read + write) per decode call (plan + decode kernels) from ncu
+# captures of dram__bytes_read.sum and dram__bytes_write.sum, valid only for
+# the kernel source they were taken on (sha256 prefix of decode_attn.cuh).
 MEASURED_TRAFFIC = {
     "39235ddca432a3f1": {"mid": 555_406_848, "sinks": 2_342_313_216},
 }
@@ -308,188 +316,225 @@ def config_of(w, args=None):
     return cfg
 
 
-def run_gpu(args, w):
-    import torch
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    import sequence_slot_kv_gb300 as skv
+# The four workloads the bandwidth target covers; each is timed in every run
+# and reported under per_config.
+TARGET_WORKLOADS = ("mid", "skewed", "sinks", "large")
+# A per-config entry's timed region runs at least this long (more steps than
+# --steps where one step is short), so its clock record has several samples.
+MIN_REGION_S = 0.25
 
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.Stream(device=dev)
-    sp = stream.cuda_stream
-    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
-    with torch.cuda.stream(stream):
-        K = torch.empty(shape, dtype=torch.float32, device=dev)
-        V = torch.empty(shape, dtype=torch.float32, device=dev)
-    w.dev_fill_history(K.data_ptr(), V.data_ptr(), sp)
 
-    def dev_t(a, dtype=None):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.to(dtype) if dtype is not None else t).to(dev)
+class DeviceWorkload:
+    """A workload resident on one device: slot (or paged) K/V filled with the
+    history recipe, a handle adopting it, every step's inputs uploaded."""
 
-    bs = args.paged
-    if bs:
-        # paged layout: the same history cut into blocks of bs positions,
-        # shuffled over a pool; each row reads its blocks through its table
-        pshape = (w.n_slots * (w.slot_ctx // bs), bs, w.n_kv_head, w.head_dim)
-        perm = dev_t(w.block_perm(bs).astype(np.int64))
-        torch.cuda.synchronize(dev)
-        pools = []
-        for src in (K, V):
-            dst = torch.empty(pshape, dtype=torch.float32, device=dev)
-            dst[perm] = src.view(pshape)
-            pools.append(dst)
-        torch.cuda.synchronize(dev)
-        del K, V
-        K, V = pools
-        tables_np = w.block_tables(bs).astype(np.int32)
-        tables = dev_t(tables_np)
-        kv = skv.SlotKV(pshape[0], bs, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
-    else:
-        kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head,
-                        k_buf=K, v_buf=V)
-    if args.split:
-        kv.set_split(*args.split)
-    if args.options:
-        kv.set_options(args.options)
-
-    qw, kw, inv = dev_t(w.q_norm_w()), dev_t(w.k_norm_w()), dev_t(w.inv_freq())
-    sinks = None if not w.sinks else dev_t(w.sink_logits())
-    slots_np = w.slots().astype(np.int32)
-    slots = dev_t(slots_np)
-    nsub = w.steps
-    q = [dev_t(w.q(t)) for t in range(nsub)]
-    kn = [dev_t(w.k_new(t)) for t in range(nsub)]
-    vn = [dev_t(w.v_new(t)) for t in range(nsub)]
-    pos = [dev_t(w.positions(t).astype(np.int32)) for t in range(nsub)]
-    out = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32, device=dev)
-    # paged mode also reads each used table entry once
-    bytes_per_launch = [w.alg_bytes(w.positions(t)) +
-                        (int((w.positions(t).astype(np.int64) // bs + 1).sum()) * 4 if bs else 0)
-                        for t in range(nsub)]
-    torch.cuda.synchronize(dev)
-
-    def decode(t):
+    def __init__(self, w, dev, stream, paged=0, split=None, options=0):
+        import torch
+        import sequence_slot_kv_gb300 as skv
+        self.w, self.dev, self.stream, self.bs = w, dev, stream, paged
+        sp = self.sp = stream.cuda_stream
+        shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+        with torch.cuda.stream(stream):
+            K = torch.empty(shape, dtype=torch.float32, device=dev)
+            V = torch.empty(shape, dtype=torch.float32, device=dev)
+        w.dev_fill_history(K.data_ptr(), V.data_ptr(), sp)
+        bs = paged
+        self.tables_np = None
         if bs:
-            kv.decode_batch_attn_paged(q[t], kn[t], vn[t], pos[t], tables, qw, kw, inv, sinks,
-                                       out, w.eps, w.scale, stream=sp)
+            # paged layout: the same history cut into blocks of bs positions,
+            # shuffled over a pool; each row reads its blocks through its table
+            pshape = (w.n_slots * (w.slot_ctx // bs), bs, w.n_kv_head, w.head_dim)
+            perm = self.dev_t(w.block_perm(bs).astype(np.int64))
+            torch.cuda.synchronize(dev)
+            pools = []
+            for src in (K, V):
+                dst = torch.empty(pshape, dtype=torch.float32, device=dev)
+                dst[perm] = src.view(pshape)
+                pools.append(dst)
+            torch.cuda.synchronize(dev)
+            del K, V
+            K, V = pools
+            self.tables_np = w.block_tables(bs).astype(np.int32)
+            self.tables = self.dev_t(self.tables_np)
+            self.kv = skv.SlotKV(pshape[0], bs, w.n_kv_head, w.head_dim, w.B, w.n_head,
+                                 k_buf=K, v_buf=V)
         else:
-            kv.decode_batch_attn(q[t], kn[t], vn[t], pos[t], slots, qw, kw, inv, sinks, out,
-                                 w.eps, w.scale, stream=sp)
+            self.kv = skv.SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head,
+                                 k_buf=K, v_buf=V)
+        self.K, self.V = K, V
+        if split:
+            self.kv.set_split(*split)
+        if options:
+            self.kv.set_options(options)
+        self.qw, self.kw, self.inv = (self.dev_t(w.q_norm_w()), self.dev_t(w.k_norm_w()),
+                                      self.dev_t(w.inv_freq()))
+        self.sinks = None if not w.sinks else self.dev_t(w.sink_logits())
+        self.slots_np = w.slots().astype(np.int32)
+        self.slots = self.dev_t(self.slots_np)
+        self.nsub = w.steps
+        self.q = [self.dev_t(w.q(t)) for t in range(self.nsub)]
+        self.kn = [self.dev_t(w.k_new(t)) for t in range(self.nsub)]
+        self.vn = [self.dev_t(w.v_new(t)) for t in range(self.nsub)]
+        self.pos = [self.dev_t(w.positions(t).astype(np.int32)) for t in range(self.nsub)]
+        self.out = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32, device=dev)
+        # paged mode also reads each used table entry once
+        self.bytes_per_launch = [
+            w.alg_bytes(w.positions(t)) +
+            (int((w.positions(t).astype(np.int64) // bs + 1).sum()) * 4 if bs else 0)
+            for t in range(self.nsub)]
+        torch.cuda.synchronize(dev)
 
-    def one_step():
-        for t in range(nsub):
-            decode(t)
+    def dev_t(self, a):
+        import torch
+        return torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
 
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize(dev)
-    assert kv.get_status(sp) == 0
+    def decode(self, t):
+        w = self.w
+        if self.bs:
+            self.kv.decode_batch_attn_paged(self.q[t], self.kn[t], self.vn[t], self.pos[t],
+                                            self.tables, self.qw, self.kw, self.inv, self.sinks,
+                                            self.out, w.eps, w.scale, stream=self.sp)
+        else:
+            self.kv.decode_batch_attn(self.q[t], self.kn[t], self.vn[t], self.pos[t],
+                                      self.slots, self.qw, self.kw, self.inv, self.sinks,
+                                      self.out, w.eps, w.scale, stream=self.sp)
+
+    def one_step(self):
+        for t in range(self.nsub):
+            self.decode(t)
+
+    def launches_per_call(self):
+        w = self.w
+        return self.kv.call_shape(w.B, bt_stride=(w.slot_ctx // self.bs if self.bs else 0))[2]
+
+    def free(self):
+        import torch
+        self.kv.free()
+        for name in ("K", "V", "q", "kn", "vn", "pos", "out", "slots", "tables"):
+            if hasattr(self, name):
+                delattr(self, name)
+        torch.cuda.synchronize(self.dev)
+        torch.cuda.empty_cache()
+
+
+def time_device(dw, steps, warmup, local, world, graph=False):
+    """Time ``steps`` steps of ``dw`` on its stream with CUDA events, each call
+    bracketed by its own pair of events.  The warm-up runs directly before
+    the timed region (no idle gap in which clocks could drop), with the clock
+    sampler already running.  Returns (total_ms, per-call ms, clocks)."""
+    import torch
+    dev, stream = dw.dev, dw.stream
+    nsub = dw.nsub
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    graph = None
-    if args.graph:
+    g = None
+    if graph:
         # one step (all its decode calls) captured once and replayed per step
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream):
-                one_step()
-        for _ in range(args.warmup):
-            graph.replay()
+        dw.one_step()
         torch.cuda.synchronize(dev)
-
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                dw.one_step()
     # A step whose bytes fit in L2 twice over would be timed warm: write a
     # buffer larger than L2 between calls (outside their events) and take the
     # value from the summed per-call times instead.
     flush = None
-    small = statistics.mean(bytes_per_launch) < 2 * L2_BYTES
-    if small:
+    if statistics.mean(dw.bytes_per_launch) < 2 * L2_BYTES:
         flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    for _ in range(warmup):
+        g.replay() if g is not None else dw.one_step()
+    torch.cuda.synchronize(dev)
+    assert dw.kv.get_status(dw.sp) == 0
+    for _ in range(2):       # warm again after the status read, right before timing
+        g.replay() if g is not None else dw.one_step()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps * (1 if graph else nsub))]
+          for _ in range(steps * (1 if g is not None else nsub))]
     begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     clocks.mark("begin")
     begin.record(stream)
     i = 0
-    for _ in range(args.steps):
-        if graph is not None:
-            if flush is not None:
-                with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            for t in range(1 if g is not None else nsub):
+                if flush is not None:
                     flush.fill_(float(i))
-            ev[i][0].record(stream)
-            with torch.cuda.stream(stream):
-                graph.replay()
-            ev[i][1].record(stream)
-            i += 1
-            continue
-        for t in range(nsub):
-            if flush is not None:
-                with torch.cuda.stream(stream):
-                    flush.fill_(float(i))
-            ev[i][0].record(stream)
-            decode(t)
-            ev[i][1].record(stream)
-            i += 1
+                ev[i][0].record(stream)
+                g.replay() if g is not None else dw.decode(t)
+                ev[i][1].record(stream)
+                i += 1
     end.record(stream)
     barrier()
     clocks.mark("end")
     clk = clocks.stop()
     total_ms = begin.elapsed_time(end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if g is not None:
+        launch_ms = [x / nsub for x in launch_ms]
     if flush is not None:
-        total_ms = sum(launch_ms)   # the flushes between calls are not the step's
+        total_ms = sum(launch_ms) * (nsub if g is not None else 1)  # flushes are not the step's
         del flush
-    assert kv.get_status(sp) == 0
-    total_ms = max_over_ranks(total_ms, dev)
-    rows_per_step = w.B * nsub
-    value = whole_job_rows_per_s(rows_per_step, args.steps, world, total_ms / 1e3)
+    assert dw.kv.get_status(dw.sp) == 0
+    return total_ms, launch_ms, clk
 
-    # e2e: host inputs -> device -> host output through decode_batch_attn_host
+
+def roofline_of(dw, launch_ms, workload_name, traffic=None):
+    """The decode call's roofline entry: algorithmic bytes over the mean
+    per-call time, against the measured copy bandwidth."""
+    peak, peak_kind = peak_hbm()
+    mean_s = statistics.mean(launch_ms) / 1e3
+    alg = statistics.mean(dw.bytes_per_launch)
+    achieved = alg / mean_s / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+            "traffic_per_alg_byte": (traffic / alg if traffic else None),
+            "alg_bytes_per_launch": alg, "avg_launch_us": mean_s * 1e6,
+            "median_launch_us": statistics.median(launch_ms) * 1e3,
+            "median_frac": alg / (statistics.median(launch_ms) / 1e3) / 1e9 / peak,
+            "kernel": "slotkv_plan_kernel + slotkv_decode_attn_kernel (one decode call)"}
+
+
+def time_e2e(dw, steps, warmup, world):
+    """The same metric end to end: every step copies its inputs from pinned
+    host memory and reads the output back through the host entry
+    (decode_batch_attn_host, or decode_batch_attn_paged_host)."""
+    import torch
+    w, dev, stream, nsub, bs = dw.w, dw.dev, dw.stream, dw.nsub, dw.bs
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     hq = [pin(w.q(t)) for t in range(nsub)]
     hk = [pin(w.k_new(t)) for t in range(nsub)]
     hv = [pin(w.v_new(t)) for t in range(nsub)]
     hp = [pin(w.positions(t).astype(np.int32)) for t in range(nsub)]
-    hs = pin(tables_np if bs else slots_np)
+    hs = pin(dw.tables_np if bs else dw.slots_np)
     hout = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32).pin_memory()
-    if bs:
-        dq, dk, dv = torch.empty_like(q[0]), torch.empty_like(kn[0]), torch.empty_like(vn[0])
-        dp, dt = torch.empty_like(pos[0]), torch.empty_like(tables)
+    call = dw.kv.decode_batch_attn_paged_host if bs else dw.kv.decode_batch_attn_host
 
     def e2e_step():
         for t in range(nsub):
-            if not bs:
-                kv.decode_batch_attn_host(hq[t], hk[t], hv[t], hp[t], hs, qw, kw, inv, sinks,
-                                          hout, w.eps, w.scale, stream=sp)
-                continue
-            # no host entry for the paged step: the same copies around the call
-            with torch.cuda.stream(stream):
-                for d_, h_ in ((dq, hq[t]), (dk, hk[t]), (dv, hv[t]), (dp, hp[t]), (dt, hs)):
-                    d_.copy_(h_, non_blocking=True)
-                kv.decode_batch_attn_paged(dq, dk, dv, dp, dt, qw, kw, inv, sinks, out, w.eps,
-                                           w.scale, stream=sp)
-                hout.copy_(out, non_blocking=True)
-            stream.synchronize()
+            call(hq[t], hk[t], hv[t], hp[t], hs, dw.qw, dw.kw, dw.inv, dw.sinks, hout, w.eps,
+                 w.scale, stream=dw.sp)
 
-    for _ in range(max(1, args.warmup)):
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(1, warmup)):
         e2e_step()
     barrier()
-    if small:
+    if statistics.mean(dw.bytes_per_launch) < 2 * L2_BYTES:
         # as for the device time: L2 written over between steps, outside them
         flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         e2e_s = 0.0
-        for k in range(args.steps):
+        for k in range(steps):
             with torch.cuda.stream(stream):
                 flush.fill_(float(k))
             stream.synchronize()
@@ -500,49 +545,118 @@ def run_gpu(args, w):
         barrier()
     else:
         t0 = time.perf_counter()
-        for _ in range(args.steps):
+        for _ in range(steps):
             e2e_step()
         barrier()
         e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, dev)
-    e2e_value = whole_job_rows_per_s(rows_per_step, args.steps, world, e2e_s)
     h2d = nsub * (hq[0].numel() + hk[0].numel() + hv[0].numel() + hp[0].numel()
                   + hs.numel()) * 4
     d2h = nsub * hout.numel() * 4
+    return e2e_s, h2d, d2h
 
-    peak, peak_kind = peak_hbm()
-    avg_launch_s = statistics.mean(launch_ms) / 1e3 / (nsub if graph is not None else 1)
-    alg_bytes = statistics.mean(bytes_per_launch)
-    achieved = alg_bytes / avg_launch_s / 1e9
+
+def per_config_entry(name, args, dev, stream, local):
+    """One target workload timed on its own (same --warmup; at least --steps
+    steps, more where a step is short, so the region lasts MIN_REGION_S)."""
+    w = synth.WORKLOADS[name]
+    dw = DeviceWorkload(w, dev, stream, split=args.split)
+    try:
+        est_ms, _, _ = time_device(dw, 3, 1, local, 1)
+        steps = max(args.steps, int(np.ceil(MIN_REGION_S * 1e3 / max(est_ms / 3, 1e-3))))
+        total_ms, launch_ms, clk = time_device(dw, steps, args.warmup, local, 1)
+        rl = roofline_of(dw, launch_ms, name, traffic=measured_traffic(name))
+        return {"value": w.B * dw.nsub * steps / (total_ms / 1e3), "unit": "rows/s",
+                "steps": steps, "calls": len(launch_ms), "ms_per_step": total_ms / steps,
+                "avg_launch_us": rl["avg_launch_us"],
+                "median_launch_us": rl["median_launch_us"],
+                "alg_bytes_per_launch": rl["alg_bytes_per_launch"],
+                "achieved_GBps": rl["achieved"], "frac": rl["frac"],
+                "median_frac": rl["median_frac"], "traffic": rl["traffic"],
+                "traffic_per_alg_byte": rl["traffic_per_alg_byte"], "clocks": clk}
+    finally:
+        dw.free()
+
+
+def run_ncu_target(args, w):
+    """For profiler captures: set the workload up, make one warm-up call and
+    one more call of its first step, nothing else.  Prints no bench line."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    dw = DeviceWorkload(w, dev, stream, paged=args.paged, split=args.split, options=args.options)
+    for _ in range(2):
+        dw.decode(0)
+    torch.cuda.synchronize(dev)
+    assert dw.kv.get_status(dw.sp) == 0
+    print(json.dumps({"ncu_target": w.name, "calls": 2,
+                      "alg_bytes_per_launch": dw.bytes_per_launch[0],
+                      "chunk_ctas_kernels": dw.kv.call_shape(w.B)}), flush=True)
+    dw.free()
+
+
+def run_gpu(args, w):
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    dw = DeviceWorkload(w, dev, stream, paged=args.paged, split=args.split,
+                        options=args.options)
+    total_ms, launch_ms, clk = time_device(dw, args.steps, args.warmup, local, world,
+                                           graph=args.graph)
+    total_ms = max_over_ranks(total_ms, dev)
+    rows_per_step = w.B * dw.nsub
+    value = whole_job_rows_per_s(rows_per_step, args.steps, world, total_ms / 1e3)
+    e2e_s, h2d, d2h = time_e2e(dw, args.steps, args.warmup, world)
+    e2e_s = max_over_ranks(e2e_s, dev)
+    e2e_value = whole_job_rows_per_s(rows_per_step, args.steps, world, e2e_s)
+    traffic = (args.traffic if args.traffic is not None
+               else (None if args.paged or args.options else measured_traffic(w.name)))
     line = {
         "metric": "slot-attn decode rows/s", "value": value, "unit": "rows/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(w, args),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": args.traffic if args.traffic is not None
-                     else (None if bs or args.options else measured_traffic(w.name)),
-                     "alg_bytes_per_launch": alg_bytes,
-                     "avg_launch_us": avg_launch_s * 1e6,
-                     "kernel": "slotkv_decode_attn_kernel"},
+        "roofline": roofline_of(dw, launch_ms, w.name, traffic),
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         # the library's kernels per decode call (plan + decode, or decode alone)
-        "gpu_launches": args.steps * nsub * kv.call_shape(w.B, bt_stride=(
-            w.slot_ctx // bs if bs else 0))[2],
+        "gpu_launches": args.steps * dw.nsub * dw.launches_per_call(),
         "graph": bool(args.graph),
         "clocks": clk,
     }
+    headline_entry = None
+    if w.name in TARGET_WORKLOADS and not (args.paged or args.options or args.graph):
+        rl = line["roofline"]
+        headline_entry = {
+            "value": value, "unit": "rows/s", "steps": args.steps,
+            "calls": len(launch_ms), "ms_per_step": total_ms / args.steps,
+            "avg_launch_us": rl["avg_launch_us"], "median_launch_us": rl["median_launch_us"],
+            "alg_bytes_per_launch": rl["alg_bytes_per_launch"], "achieved_GBps": rl["achieved"],
+            "frac": rl["frac"], "median_frac": rl["median_frac"], "traffic": rl["traffic"],
+            "traffic_per_alg_byte": rl["traffic_per_alg_byte"], "clocks": clk}
+    dw.free()
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per = {}
+        for name in TARGET_WORKLOADS:
+            if headline_entry is not None and name == w.name:
+                per[name] = headline_entry
+            else:
+                per[name] = per_config_entry(name, args, dev, stream, local)
+        line["per_config"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        v, desc = time_oracle(w, args.cpu_budget, cores, flags=args.options, paged_bs=bs)
+        v, desc = time_oracle(w, args.cpu_budget, cores, flags=args.options, paged_bs=args.paged)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    kv.free()
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -738,9 +852,10 @@ def time_oracle_prefill(w, slots, pos, budget_s, n_threads):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mid", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="large",
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--split", type=int, nargs=2, default=None,
                     metavar=("MIN_CHUNK_KEYS", "MAX_SPLITS"))
@@ -756,12 +871,18 @@ def main():
                     help="capture one step in a CUDA graph and time its replays")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the decode kernel, if measured")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the four target workloads beside the headline")
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiler target: two calls of the workload's first step, no line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     args.options = {"": 0, "vnorm": 1, "plus_one": 2, "both": 3}[args.options]
-    w = synth.WORKLOADS[args.workload]
-    if args.impl == "reference":
+    w = synth.WORKLOADS.get(args.workload) or synth.PROFILE_WORKLOADS[args.workload]
+    if args.ncu:
+        run_ncu_target(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     elif args.prefill:
         run_prefill(args)

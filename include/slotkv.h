@@ -254,6 +254,28 @@ int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const f
                            float eps, float scale, slotkv_stream_t stream);
 
 /*
+ * decode_batch_attn_paged_host -- decode_batch_attn_paged for callers whose
+ * per-step inputs and output live in host memory (the paged counterpart of
+ * decode_batch_attn_host; the Qwen3SsmLayer page, decode_multi_seq over a
+ * paged cache).  q, k_new, v_new, positions, block_tables (u32[B][bt_stride])
+ * and out are HOST pointers; q_norm_w, k_norm_w, inv_freq and sinks stay
+ * device pointers.  The inputs move to handle-owned device staging (one
+ * gather kernel when all six host buffers are pinned, else cudaMemcpyAsync),
+ * the step runs, out moves back and `stream` is synchronised before the call
+ * returns.  The tables' staging grows to the largest B * bt_stride seen: a
+ * call with a larger table than any before allocates (and synchronises the
+ * device) first.  Errors as decode_batch_attn_paged, plus SLOTKV_ERR_CUDA
+ * for a failed copy or staging allocation.
+ */
+int decode_batch_attn_paged_host(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
+                                 const float* k_new, const float* v_new,
+                                 const uint32_t* positions, const uint32_t* block_tables,
+                                 uint32_t bt_stride, const float* q_norm_w,
+                                 const float* k_norm_w, const float* inv_freq,
+                                 const float* sinks, float* out, float eps, float scale,
+                                 slotkv_stream_t stream);
+
+/*
  * decode_batch_attn_noalloc -- the same decode step as decode_batch_attn for
  * callers that cannot allocate device memory.  The pages have no counterpart
  * to this entry point.
@@ -279,8 +301,10 @@ int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const f
  * host threads without ordering) race on it: order them.
  *
  * Set-up: the first call on each device looks up the array's device address
- * with that device current and caches it.  Make that first call before any
- * stream capture begins.
+ * with that device current and caches it, keyed on the current CUDA context
+ * (a new context -- after cudaDeviceReset, or a driver-API context made
+ * current -- looks it up again on its first call).  Make that first call
+ * before any stream capture begins.
  *
  *   K, V        device slot buffers, [n_slots][slot_ctx][n_kv_head][head_dim]
  *               f32, 16-byte aligned (the caller owns them).
@@ -291,7 +315,11 @@ int decode_batch_attn_host(slotkv_t handle, uint32_t B, uint32_t n_head, const f
  *               as decode_batch_attn (B <= 65535; G = n_head/n_kv_head 1..8).
  *   dev_flags   device u32 that receives the SLOTKV_DEV_* flags raised by
  *               this call (OR-ed in; the caller clears it), or NULL to
- *               discard them.
+ *               discard them.  With NULL an out-of-range row (slots[b] >=
+ *               n_slots or positions[b] >= slot_ctx) is skipped silently:
+ *               its out rows keep their previous contents and nothing
+ *               signals it, so pass dev_flags wherever the inputs are not
+ *               validated already.
  *
  * Returns SLOTKV_OK, SLOTKV_ERR_ARG, SLOTKV_ERR_UNSUPPORTED or
  * SLOTKV_ERR_CUDA; slot_kv_last_error() says why.  Results match

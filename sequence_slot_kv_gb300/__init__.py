@@ -10,7 +10,8 @@ The functions mirror the C ABI in ``include/slotkv.h`` name for name
 (``EXPORTS`` lists every symbol): the handle (``slot_kv_alloc``,
 ``slot_kv_free``, ``slot_kv_offset_bytes``, ``slot_kv_reset``), the step
 (``decode_batch_attn``, its host-buffer form ``decode_batch_attn_host``,
-``prefill_batch_attn``, ``decode_batch_attn_paged``, the allocation-free
+``prefill_batch_attn``, ``decode_batch_attn_paged`` and its host-buffer form
+``decode_batch_attn_paged_host``, the allocation-free
 ``decode_batch_attn_noalloc``), multi-step support
 (``slot_kv_advance_positions``), and control (``slot_kv_get_status``,
 ``slot_kv_set_split``, ``slot_kv_set_options``, ``slot_kv_call_shape``).
@@ -22,7 +23,8 @@ import os
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn",
-    "decode_batch_attn_paged", "decode_batch_attn_noalloc", "slot_kv_advance_positions",
+    "decode_batch_attn_paged", "decode_batch_attn_paged_host", "decode_batch_attn_noalloc",
+    "slot_kv_advance_positions",
     "slot_kv_get_status", "slot_kv_set_split", "LIB_PATH", "EXPORTS", "DEV_RANGE",
     "DEV_TIMEOUT", "OPT_VNORM", "OPT_NORM_PLUS_ONE", "OPT_TEST_STALL",
 ]
@@ -52,6 +54,8 @@ EXPORTS = {
     "prefill_batch_attn": (_DECODE_ARGS, _int),
     "decode_batch_attn_paged": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp, _vp,
                                  _vp, _vp, _f32, _f32, _vp], _int),
+    "decode_batch_attn_paged_host": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp,
+                                      _vp, _vp, _vp, _f32, _f32, _vp], _int),
     "slot_kv_get_status": ([_vp, _vp, ctypes.POINTER(_u32)], _int),
     "slot_kv_set_split": ([_vp, _u32, _u32], _int),
     "slot_kv_call_shape": ([_vp, _u32, _u32, _u32, ctypes.POINTER(_u32), ctypes.POINTER(_u32),
@@ -113,6 +117,38 @@ def _ptr(t, dtype=None, what="tensor", cuda=True):
     if cuda is not None and t.is_cuda != cuda:
         raise ValueError(f"{what} must be a {'CUDA' if cuda else 'CPU'} tensor")
     return t.data_ptr()
+
+
+def _shape(t):
+    return None if t is None else tuple(int(x) for x in t.shape)
+
+
+def _check_step(q, k_new, v_new, positions, rows_idx, out, q_norm_w, k_norm_w, inv_freq,
+                sinks, n_kv_head, head_dim, idx_name="slots"):
+    """Shapes of one step's tensors against (B, n_head) taken from q and the
+    slot geometry (n_kv_head, head_dim).  The library reads and writes these
+    buffers by those sizes, so a mismatch is refused before any call."""
+    if q is None or q.dim() != 3:
+        raise ValueError("q must be [B][n_head][head_dim]")
+    B, n_head, hd = _shape(q)
+    if hd != head_dim:
+        raise ValueError(f"q's head_dim {hd} != the slot buffers' {head_dim}")
+    want = {
+        "q": (q, (B, n_head, hd)), "k_new": (k_new, (B, n_kv_head, hd)),
+        "v_new": (v_new, (B, n_kv_head, hd)), "positions": (positions, (B,)),
+        "out": (out, (B, n_head, hd)), "q_norm_w": (q_norm_w, (hd,)),
+        "k_norm_w": (k_norm_w, (hd,)), "inv_freq": (inv_freq, (hd // 2,)),
+    }
+    if idx_name == "slots":
+        want["slots"] = (rows_idx, (B,))
+    for name, (t, shape) in want.items():
+        if t is None:
+            raise ValueError(f"{name} is required")
+        if _shape(t) != shape:
+            raise ValueError(f"{name} has shape {_shape(t)}, expected {shape}")
+    if sinks is not None and _shape(sinks) != (n_head,):
+        raise ValueError(f"sinks has shape {_shape(sinks)}, expected ({n_head},)")
+    return B, n_head
 
 
 def _stream_ptr(stream):
@@ -189,7 +225,8 @@ class SlotKV:
     def decode_batch_attn(self, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                           inv_freq, sinks, out, eps, scale, stream=None):
         import torch
-        B, n_head = int(q.shape[0]), int(q.shape[1])
+        B, n_head = _check_step(q, k_new, v_new, positions, slots, out, q_norm_w, k_norm_w,
+                                inv_freq, sinks, self.n_kv_head, self.head_dim)
         f, u = torch.float32, torch.int32
         _check(_lib.decode_batch_attn(
             self._h, B, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
@@ -205,7 +242,8 @@ class SlotKV:
         slots, out) are written into their slots and each attends keys
         0..pos of its slot, the call's other new rows included."""
         import torch
-        n, n_head = int(q.shape[0]), int(q.shape[1])
+        n, n_head = _check_step(q, k_new, v_new, positions, slots, out, q_norm_w, k_norm_w,
+                                inv_freq, sinks, self.n_kv_head, self.head_dim)
         f, u = torch.float32, torch.int32
         _check(_lib.prefill_batch_attn(
             self._h, n, n_head, _ptr(q, f, "q"), _ptr(k_new, f, "k_new"),
@@ -221,7 +259,9 @@ class SlotKV:
         slot_ctx positions): block_tables is int32 [B][max_blocks], row b's
         key t in block block_tables[b][t // slot_ctx]."""
         import torch
-        B, n_head = int(q.shape[0]), int(q.shape[1])
+        B, n_head = _check_step(q, k_new, v_new, positions, block_tables, out, q_norm_w,
+                                k_norm_w, inv_freq, sinks, self.n_kv_head, self.head_dim,
+                                idx_name="block_tables")
         f, u = torch.float32, torch.int32
         if block_tables.dim() != 2 or int(block_tables.shape[0]) != B:
             raise ValueError("block_tables must be [B][max_blocks]")
@@ -234,12 +274,35 @@ class SlotKV:
             eps, scale, _stream_ptr(stream)), "decode_batch_attn_paged")
         return out
 
+    def decode_batch_attn_paged_host(self, q, k_new, v_new, positions, block_tables, q_norm_w,
+                                     k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
+        """As decode_batch_attn_paged, with q/k_new/v_new/positions/block_tables/out
+        in host memory (CPU tensors, ideally pinned); synchronous."""
+        import torch
+        B, n_head = _check_step(q, k_new, v_new, positions, block_tables, out, q_norm_w,
+                                k_norm_w, inv_freq, sinks, self.n_kv_head, self.head_dim,
+                                idx_name="block_tables")
+        f, u = torch.float32, torch.int32
+        if block_tables.dim() != 2 or int(block_tables.shape[0]) != B:
+            raise ValueError("block_tables must be [B][max_blocks]")
+        _check(_lib.decode_batch_attn_paged_host(
+            self._h, B, n_head, _ptr(q, f, "q", cuda=False),
+            _ptr(k_new, f, "k_new", cuda=False), _ptr(v_new, f, "v_new", cuda=False),
+            _ptr(positions, u, "positions", cuda=False),
+            _ptr(block_tables, u, "block_tables", cuda=False), int(block_tables.shape[1]),
+            _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"),
+            _ptr(out, f, "out", cuda=False), eps, scale, _stream_ptr(stream)),
+            "decode_batch_attn_paged_host")
+        return out
+
     def decode_batch_attn_host(self, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
         """As decode_batch_attn, with q/k_new/v_new/positions/slots/out in host
         memory (CPU tensors, ideally pinned); synchronous."""
         import torch
-        B, n_head = int(q.shape[0]), int(q.shape[1])
+        B, n_head = _check_step(q, k_new, v_new, positions, slots, out, q_norm_w, k_norm_w,
+                                inv_freq, sinks, self.n_kv_head, self.head_dim)
         f, u = torch.float32, torch.int32
         _check(_lib.decode_batch_attn_host(
             self._h, B, n_head, _ptr(q, f, "q", cuda=False),
@@ -330,6 +393,12 @@ def decode_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_nor
                                     inv_freq, sinks, out, eps, scale, stream)
 
 
+def decode_batch_attn_paged_host(h, q, k_new, v_new, positions, block_tables, q_norm_w,
+                                 k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
+    return h.decode_batch_attn_paged_host(q, k_new, v_new, positions, block_tables, q_norm_w,
+                                          k_norm_w, inv_freq, sinks, out, eps, scale, stream)
+
+
 def slot_kv_get_status(h, stream=None):
     return h.get_status(stream)
 
@@ -356,8 +425,13 @@ def decode_batch_attn_noalloc(K, V, q, k_new, v_new, positions, slots, q_norm_w,
     flags.  The first call on a device should come before any stream capture;
     calls that overlap on the GPU race on the shared scratch."""
     import torch
-    n_slots, slot_ctx, n_kv_head, head_dim = (int(x) for x in K.shape)
-    B, n_head = int(q.shape[0]), int(q.shape[1])
+    if K.dim() != 4 or _shape(V) != _shape(K):
+        raise ValueError("K and V must both be [n_slots][slot_ctx][n_kv_head][head_dim]")
+    n_slots, slot_ctx, n_kv_head, head_dim = _shape(K)
+    B, n_head = _check_step(q, k_new, v_new, positions, slots, out, q_norm_w, k_norm_w,
+                            inv_freq, sinks, n_kv_head, head_dim)
+    if dev_flags is not None and int(dev_flags.numel()) < 1:
+        raise ValueError("dev_flags must hold one element")
     f, u = torch.float32, torch.int32
     _check(_lib.decode_batch_attn_noalloc(
         _ptr(K, f, "K"), _ptr(V, f, "V"), n_slots, slot_ctx, n_kv_head, head_dim, B, n_head,

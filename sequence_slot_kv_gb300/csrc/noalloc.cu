@@ -33,11 +33,48 @@ constexpr uint32_t kNoAllocMaxSplits = 16;
 constexpr int kMaxDevices = 64;
 
 // The scratch.  In host code this name is only a stand-in for the symbol; the
-// device address comes from cudaGetSymbolAddress, once per device.
+// device address comes from cudaGetSymbolAddress, once per device and CUDA
+// context.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// A __device__ symbol's address belongs to the context that loaded the
+// module: after cudaDeviceReset, or with another (driver-API) context
+// current, the address must be looked up again.  The cache is keyed on the
+// current context's unique id (cuCtxGetId), which no later context reuses.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    void* ptr;
+};
 std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+typedef CUresult (*ctx_get_current_fn)(CUcontext*);
+typedef CUresult (*ctx_get_id_fn)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current context; false when no
+// context is current yet or the driver cannot say.  Call with
+// g_setup_mutex held.
+bool current_context_id(unsigned long long* id) {
+    static ctx_get_current_fn get_current = nullptr;
+    static ctx_get_id_fn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+                cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess || !a || !b)
+            return false;
+        get_current = reinterpret_cast<ctx_get_current_fn>(a);
+        get_id = reinterpret_cast<ctx_get_id_fn>(b);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // Failures are reported like every other call: a status code, and a message
 // for slot_kv_last_error().
@@ -108,7 +145,8 @@ extern "C" int decode_batch_attn_noalloc(
                             "%zu (use decode_batch_attn with a handle for larger batches)",
                             need, kNoAllocScratchBytes);
 
-    // once per device, with that device current: the scratch's device address
+    // once per device and context, with that device current: the scratch's
+    // device address
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -116,15 +154,23 @@ extern "C" int decode_batch_attn_noalloc(
     unsigned char* scratch;
     {
         std::lock_guard<std::mutex> lock(g_setup_mutex);
-        if (!g_scratch_addr[dev]) {
+        unsigned long long ctx_id = 0;
+        const bool known = current_context_id(&ctx_id);
+        ScratchAddr& c = g_scratch_addr[dev];
+        if (!known || !c.ptr || c.ctx_id != ctx_id) {
+            // (the lookup also creates the device's primary context if no
+            // context is current yet)
             void* ptr = nullptr;
             e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
             if (e != cudaSuccess || !ptr)
                 return noalloc_fail(SLOTKV_ERR_CUDA, "cudaGetSymbolAddress: %s",
                                     cudaGetErrorString(e));
-            g_scratch_addr[dev] = ptr;
+            if (!current_context_id(&ctx_id))
+                return noalloc_fail(SLOTKV_ERR_CUDA, "no current CUDA context after set-up");
+            c.ctx_id = ctx_id;
+            c.ptr = ptr;
         }
-        scratch = static_cast<unsigned char*>(g_scratch_addr[dev]);
+        scratch = static_cast<unsigned char*>(c.ptr);
     }
 
     // the status word and the merge counters must start at zero

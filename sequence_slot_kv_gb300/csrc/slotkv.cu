@@ -82,6 +82,8 @@ struct slotkv_s {
     float* st_out = nullptr;
     uint32_t* st_pos = nullptr;
     uint32_t* st_slots = nullptr;
+    uint32_t* st_tab = nullptr;  // block tables for decode_batch_attn_paged_host
+    size_t st_tab_bytes = 0;     // (grown on demand)
     CUtensorMap tmK, tmV;
 };
 
@@ -112,6 +114,7 @@ void release(slotkv_s* h) {
     cudaFree(h->st_out);
     cudaFree(h->st_pos);
     cudaFree(h->st_slots);
+    cudaFree(h->st_tab);
     if (h->owns_kv) {
         cudaFree(h->K);
         cudaFree(h->V);
@@ -352,6 +355,97 @@ __global__ void advance_positions_kernel(uint32_t* __restrict__ pos, uint32_t B,
 }
 }  // namespace slotkv
 
+namespace {
+
+// The host entries' per-step buffers: q, k_new, v_new, positions and the row
+// index (slots, or block tables of idx_bytes) in host memory, and out.
+struct HostStep {
+    const float* q;
+    const float* k_new;
+    const float* v_new;
+    const uint32_t* positions;
+    const uint32_t* idx;
+    size_t idx_bytes;
+    uint32_t* idx_stage;  // device staging for idx
+    float* out;
+};
+
+// Move a step's host inputs into the handle's device staging on `s`, run the
+// step (`run(q, k_new, v_new, positions, idx, out)` with device pointers),
+// move out back and synchronise `s`.  When every host buffer is page-locked
+// (pinned, hence mapped into the device's address space), one copy kernel
+// gathers the inputs over the host link and the step writes out straight
+// into host memory (through a second copy kernel if out is not 16-byte
+// aligned), instead of separate copy-engine transfers; otherwise each buffer
+// is copied with cudaMemcpyAsync.
+template <typename Run>
+int host_step(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs, cudaStream_t s,
+              Run run) {
+    const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
+    const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
+    const size_t ni = (size_t)B * sizeof(uint32_t);
+    cudaError_t e;
+    int rc;
+    const void* hp[6] = {hs.q, hs.k_new, hs.v_new, hs.positions, hs.idx, hs.out};
+    void* dp[6];
+    bool mapped = true;
+    for (int i = 0; i < 6 && mapped; ++i) {
+        cudaPointerAttributes at;
+        mapped = cudaPointerGetAttributes(&at, hp[i]) == cudaSuccess &&
+                 at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
+        dp[i] = mapped ? at.devicePointer : nullptr;
+    }
+    cudaGetLastError();  // a failed attribute query leaves an error behind
+    if (mapped) {
+        const int threads = 256;
+        const unsigned grid = (unsigned)(h->sm_count > 0 ? h->sm_count : 1);
+        slotkv::CopySegs in{};
+        void* st[5] = {h->st_q, h->st_k, h->st_v, h->st_pos, hs.idx_stage};
+        const size_t nb[5] = {nq, nk, nk, ni, hs.idx_bytes};
+        for (int i = 0; i < 5; ++i) {
+            in.src[i] = static_cast<const uint8_t*>(dp[i]);
+            in.dst[i] = static_cast<uint8_t*>(st[i]);
+            in.bytes[i] = nb[i];
+        }
+        in.n = 5;
+        slotkv::copy_segments_kernel<<<grid, threads, 0, s>>>(in);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "input gather launch");
+        // an aligned out is written by the decode kernel itself, over the link
+        const bool direct_out = ((uintptr_t)dp[5] & 15) == 0;
+        rc = run(h->st_q, h->st_k, h->st_v, h->st_pos, hs.idx_stage,
+                 direct_out ? static_cast<float*>(dp[5]) : h->st_out);
+        if (rc != SLOTKV_OK) return rc;
+        if (!direct_out) {
+            slotkv::CopySegs outc{};
+            outc.src[0] = reinterpret_cast<const uint8_t*>(h->st_out);
+            outc.dst[0] = static_cast<uint8_t*>(dp[5]);
+            outc.bytes[0] = nq;
+            outc.n = 1;
+            slotkv::copy_segments_kernel<<<grid, threads, 0, s>>>(outc);
+            if ((e = cudaGetLastError()) != cudaSuccess)
+                return cuda_fail(e, "output scatter launch");
+        }
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+        return SLOTKV_OK;
+    }
+    if ((e = cudaMemcpyAsync(h->st_q, hs.q, nq, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_k, hs.k_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_v, hs.v_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->st_pos, hs.positions, ni, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(hs.idx_stage, hs.idx, hs.idx_bytes, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess)
+        return cuda_fail(e, "host-to-device input copy");
+    rc = run(h->st_q, h->st_k, h->st_v, h->st_pos, hs.idx_stage, h->st_out);
+    if (rc != SLOTKV_OK) return rc;
+    if ((e = cudaMemcpyAsync(hs.out, h->st_out, nq, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "device-to-host output copy");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+    return SLOTKV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* slot_kv_last_error(void) { return g_err; }
@@ -549,72 +643,51 @@ int decode_batch_attn_host(slotkv_t h, uint32_t B, uint32_t n_head, const float*
     int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, out, false);
     if (rc != SLOTKV_OK || B == 0) return rc;
-    cudaStream_t s = (cudaStream_t)stream;
-    const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
-    const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
-    const size_t ni = (size_t)B * sizeof(uint32_t);
-    cudaError_t e;
-    // Pinned host buffers are mapped into the device's address space: one
-    // copy kernel gathers the inputs over the host link and one returns the
-    // output, instead of six small copy-engine transfers.
-    const void* hp[6] = {q, k_new, v_new, positions, slots, out};
-    void* dp[6];
-    bool mapped = true;
-    for (int i = 0; i < 6 && mapped; ++i) {
-        cudaPointerAttributes at;
-        mapped = cudaPointerGetAttributes(&at, hp[i]) == cudaSuccess &&
-                 at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
-        dp[i] = mapped ? at.devicePointer : nullptr;
-    }
-    cudaGetLastError();  // a failed attribute query leaves an error behind
-    if (mapped) {
-        const int threads = 256;
-        const unsigned grid = (unsigned)(h->sm_count > 0 ? h->sm_count : 1);
-        slotkv::CopySegs in{};
-        void* st[5] = {h->st_q, h->st_k, h->st_v, h->st_pos, h->st_slots};
-        const size_t nb[5] = {nq, nk, nk, ni, ni};
-        for (int i = 0; i < 5; ++i) {
-            in.src[i] = static_cast<const uint8_t*>(dp[i]);
-            in.dst[i] = static_cast<uint8_t*>(st[i]);
-            in.bytes[i] = nb[i];
-        }
-        in.n = 5;
-        slotkv::copy_segments_kernel<<<grid, threads, 0, s>>>(in);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "input gather launch");
-        // an aligned out is written by the decode kernel itself, over the link
-        const bool direct_out = ((uintptr_t)dp[5] & 15) == 0;
-        rc = launch(h, B, n_head, h->st_q, h->st_k, h->st_v, h->st_pos, h->st_slots, q_norm_w,
-                    k_norm_w, inv_freq, sinks, direct_out ? static_cast<float*>(dp[5]) : h->st_out,
-                    eps, scale, s);
-        if (rc != SLOTKV_OK) return rc;
-        if (direct_out) {
-            if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
-            return SLOTKV_OK;
-        }
-        slotkv::CopySegs outc{};
-        outc.src[0] = reinterpret_cast<const uint8_t*>(h->st_out);
-        outc.dst[0] = static_cast<uint8_t*>(dp[5]);
-        outc.bytes[0] = nq;
-        outc.n = 1;
-        slotkv::copy_segments_kernel<<<grid, threads, 0, s>>>(outc);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "output scatter launch");
-        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
-        return SLOTKV_OK;
-    }
-    if ((e = cudaMemcpyAsync(h->st_q, q, nq, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(h->st_k, k_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(h->st_v, v_new, nk, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(h->st_pos, positions, ni, cudaMemcpyHostToDevice, s)) !=
-            cudaSuccess ||
-        (e = cudaMemcpyAsync(h->st_slots, slots, ni, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "host-to-device input copy");
-    rc = launch(h, B, n_head, h->st_q, h->st_k, h->st_v, h->st_pos, h->st_slots, q_norm_w,
-                k_norm_w, inv_freq, sinks, h->st_out, eps, scale, s);
+    const HostStep hs{q, k_new, v_new, positions, slots, (size_t)B * sizeof(uint32_t),
+                      h->st_slots, out};
+    return host_step(h, B, n_head, hs, (cudaStream_t)stream,
+                     [&](const float* dq, const float* dk, const float* dv, const uint32_t* dpos,
+                         const uint32_t* didx, float* dout) {
+                         return launch(h, B, n_head, dq, dk, dv, dpos, didx, q_norm_w, k_norm_w,
+                                       inv_freq, sinks, dout, eps, scale, (cudaStream_t)stream);
+                     });
+}
+
+int decode_batch_attn_paged_host(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
+                                 const float* k_new, const float* v_new,
+                                 const uint32_t* positions, const uint32_t* block_tables,
+                                 uint32_t bt_stride, const float* q_norm_w,
+                                 const float* k_norm_w, const float* inv_freq,
+                                 const float* sinks, float* out, float eps, float scale,
+                                 slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, block_tables,
+                               q_norm_w, k_norm_w, inv_freq, out, false);
     if (rc != SLOTKV_OK) return rc;
-    if ((e = cudaMemcpyAsync(out, h->st_out, nq, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return cuda_fail(e, "device-to-host output copy");
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
-    return SLOTKV_OK;
+    const uint32_t T = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+    if (h->slot_ctx % T != 0)
+        return fail(SLOTKV_ERR_UNSUPPORTED, "block size %u is not a multiple of %u keys",
+                    h->slot_ctx, T);
+    if (bt_stride == 0) return fail(SLOTKV_ERR_ARG, "bt_stride must be >= 1");
+    if (B == 0) return SLOTKV_OK;
+    // the tables' device staging grows to the largest B * bt_stride seen
+    const size_t tab_bytes = (size_t)B * bt_stride * sizeof(uint32_t);
+    if (tab_bytes > h->st_tab_bytes) {
+        cudaError_t e = cudaFree(h->st_tab);
+        h->st_tab = nullptr;
+        h->st_tab_bytes = 0;
+        if (e == cudaSuccess) e = cudaMalloc(&h->st_tab, tab_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "block-table staging");
+        h->st_tab_bytes = tab_bytes;
+    }
+    const HostStep hs{q, k_new, v_new, positions, block_tables, tab_bytes, h->st_tab, out};
+    return host_step(h, B, n_head, hs, (cudaStream_t)stream,
+                     [&](const float* dq, const float* dk, const float* dv, const uint32_t* dpos,
+                         const uint32_t* didx, float* dout) {
+                         return launch(h, B, n_head, dq, dk, dv, dpos, nullptr, q_norm_w,
+                                       k_norm_w, inv_freq, sinks, dout, eps, scale,
+                                       (cudaStream_t)stream, false, didx, bt_stride);
+                     });
 }
 
 int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,

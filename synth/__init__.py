@@ -264,3 +264,14 @@ WORKLOADS = {
                       n_kv_head=8, head_dim=128, theta=10000.0, sinks=False, steps=64,
                       pos_rule="uniform_start", start_hi=1983, slot_rule="subset"),
 }
+
+# Scaled-down cases of two workloads, for profiler captures that must hold a
+# few GB at most: the same head geometry, split chunk and persistent grid as
+# the full workload, fewer rows and slots.
+#   skewed_8:  8 rows (4 at position 16, 4 at 32767) on 8 slots of 32768;
+#   large_32:  32 rows of the batch-256 workload's first step on 64 slots
+#              (run with the full workload's 2048-key chunk: --split 2048 64).
+PROFILE_WORKLOADS = {
+    "skewed_8": WORKLOADS["skewed"].replace(name="skewed_8", index=30, B=8, n_slots=8),
+    "large_32": WORKLOADS["large"].replace(name="large_32", index=31, B=32, n_slots=64, steps=1),
+}

@@ -95,3 +95,40 @@ def test_more_host_checks_without_gpu():
     assert na(*args(n_kv=257, n_head=257)) == ARG
     assert na(*args(B=65536)) == ARG
     assert na(*args(n_slots=1 << 16, slot_ctx=1 << 15)) == ARG
+
+
+def test_binding_refuses_mismatched_shapes():
+    """The binding checks every step tensor's shape against (B, n_head) from
+    q and the slot geometry before it passes an address on: a mismatched out
+    or k_new would otherwise be read or written past its end."""
+    import pytest
+    import torch
+
+    B, nh, nkv, hd = 3, 8, 2, 64
+    K = torch.zeros((4, 16, nkv, hd))
+    good = dict(q=torch.zeros((B, nh, hd)), k_new=torch.zeros((B, nkv, hd)),
+                v_new=torch.zeros((B, nkv, hd)), positions=torch.zeros(B, dtype=torch.int32),
+                slots=torch.zeros(B, dtype=torch.int32), q_norm_w=torch.ones(hd),
+                k_norm_w=torch.ones(hd), inv_freq=torch.ones(hd // 2), sinks=None,
+                out=torch.zeros((B, nh, hd)))
+    bad = {"out": torch.zeros((B, nh - 1, hd)), "k_new": torch.zeros((B, nkv + 1, hd)),
+           "v_new": torch.zeros((B + 1, nkv, hd)), "positions": torch.zeros(B + 1),
+           "slots": torch.zeros(B - 1), "q_norm_w": torch.ones(hd + 1),
+           "inv_freq": torch.ones(hd), "sinks": torch.zeros(nh + 1)}
+    for name, t in bad.items():
+        args = dict(good, **{name: t})
+        with pytest.raises(ValueError, match=name):
+            skv.decode_batch_attn_noalloc(K, K, eps=1e-6, scale=0.1, **args)
+
+    class _Handle:          # the geometry a SlotKV carries, without a device
+        n_kv_head, head_dim = nkv, hd
+
+    with pytest.raises(ValueError, match="out"):
+        skv.SlotKV.decode_batch_attn(_Handle(), **dict(good, out=bad["out"]), eps=1e-6,
+                                     scale=0.1)
+    with pytest.raises(ValueError, match="k_new"):
+        skv.SlotKV.decode_batch_attn_host(_Handle(), **dict(good, k_new=bad["k_new"]),
+                                          eps=1e-6, scale=0.1)
+    # shapes that agree get as far as the placement check (CPU tensors here)
+    with pytest.raises(ValueError, match="CUDA"):
+        skv.decode_batch_attn_noalloc(K, K, eps=1e-6, scale=0.1, **good)

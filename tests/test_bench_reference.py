@@ -45,8 +45,8 @@ def test_reference_line(flags):
         assert d["unit"] == "tokens/s" and d["config"]["workload"] == "prefill"
         assert per_step == pytest.approx(8)
     else:
-        assert d["unit"] == "rows/s" and d["config"]["workload"] == "mid"
-        assert per_step == pytest.approx(min(32, cb["cores"]))
+        assert d["unit"] == "rows/s" and d["config"]["workload"] == "large"
+        assert per_step == pytest.approx(min(256, cb["cores"]))
     if "--paged" in flags:
         assert d["config"]["kv_layout"] == "paged" and d["config"]["block_size"] == 64
         assert "norm_options" in d["config"]

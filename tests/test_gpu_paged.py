@@ -306,3 +306,42 @@ def test_paged_argument_errors():
         assert run.kv.get_status() == 0
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_paged_host_entry_matches_device_entry_and_oracle(pinned):
+    """decode_batch_attn_paged_host (inputs, tables and out in host memory)
+    against the device entry on the same pool, bit for bit, and against the
+    paged oracle; twice, so the second call reuses the table staging, and a
+    wider table grows it."""
+    w, bs = small_paged_workload(128, 4, 1, 40, sinks=True)
+    run_d = PagedRun(w, bs)
+    run_h = PagedRun(w, bs)
+    try:
+        want = run_d.step(0)
+        torch.cuda.synchronize()
+        assert run_d.kv.get_status() == 0
+        Kr, Vr = host_pool(w, bs)
+        ref, skipped = oracle_paged(w, bs, Kr, Vr, run_d.tables_np)
+        assert skipped == 0
+        host = lambda a: (torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+                          if pinned else torch.from_numpy(np.ascontiguousarray(a)))
+        hq, hk, hv = host(w.q()), host(w.k_new()), host(w.v_new())
+        hp = host(w.positions(0).astype(np.int32))
+        for width in (run_d.tables_np.shape[1], run_d.tables_np.shape[1] + 5):
+            # padded tables: entries past a row's last used block are never read
+            tab = np.full((w.B, width), 2**31 - 1, dtype=np.int32)
+            tab[:, :run_d.tables_np.shape[1]] = run_d.tables_np
+            K0, V0 = run_h.fresh_pool()
+            run_h.K.copy_(K0)
+            run_h.V.copy_(V0)
+            out = host(np.full((w.B, w.n_head, w.head_dim), np.nan, dtype=np.float32))
+            run_h.kv.decode_batch_attn_paged_host(hq, hk, hv, hp, host(tab), run_h.qw, run_h.kw,
+                                                  run_h.inv, run_h.sinks, out, w.eps, w.scale)
+            assert run_h.kv.get_status() == 0
+            assert torch.equal(out, want.cpu()), f"table width {width}"
+            assert_close(out.numpy(), ref, f"paged host entry, table width {width}")
+            assert torch.equal(run_h.K, run_d.K) and torch.equal(run_h.V, run_d.V)
+    finally:
+        run_d.close()
+        run_h.close()

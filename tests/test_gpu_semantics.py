@@ -434,10 +434,10 @@ def test_argument_errors():
         q, kn, vn, pos = run.inputs(0)
         out = torch.empty((w.B, w.n_head, w.head_dim), device="cuda")
         with pytest.raises(skv.SlotKVError) as ei:      # B > max_rows
-            big = np.concatenate([q] * 3)
-            run.kv.decode_batch_attn(to_dev(big), to_dev(kn), to_dev(vn),
-                                     to_dev(pos.astype(np.int32)), run.slots, run.qw, run.kw,
-                                     run.inv, None, out, w.eps, w.scale)
+            big = [to_dev(np.concatenate([a] * 3)) for a in (q, kn, vn, pos.astype(np.int32))]
+            run.kv.decode_batch_attn(*big, run.slots.repeat(3), run.qw, run.kw, run.inv, None,
+                                     torch.empty((3 * w.B, w.n_head, w.head_dim), device="cuda"),
+                                     w.eps, w.scale)
         assert ei.value.code == 1
         with pytest.raises(skv.SlotKVError):            # null output
             rc = skv._lib.decode_batch_attn(run.kv._h, w.B, w.n_head, 1, 1, 1, 1, 1, 1, 1, 1,
