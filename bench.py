@@ -855,7 +855,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="large",
-                    choices=sorted(synth.WORKLOADS) + sorted(synth.PROFILE_WORKLOADS))
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.EXTRA_WORKLOADS) +
+                    sorted(synth.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--split", type=int, nargs=2, default=None,
                     metavar=("MIN_CHUNK_KEYS", "MAX_SPLITS"))
@@ -879,7 +880,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     args.options = {"": 0, "vnorm": 1, "plus_one": 2, "both": 3}[args.options]
-    w = synth.WORKLOADS.get(args.workload) or synth.PROFILE_WORKLOADS[args.workload]
+    w = {**synth.WORKLOADS, **synth.EXTRA_WORKLOADS, **synth.PROFILE_WORKLOADS}[args.workload]
     if args.ncu:
         run_ncu_target(args, w)
     elif args.impl == "reference":

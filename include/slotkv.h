@@ -350,6 +350,43 @@ int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,
                               slotkv_stream_t stream);
 
 /*
+ * Slot-ownership sharding over several GPUs.  The rows of a decode step are
+ * independent sequences in disjoint slots ("Forward Cuda Gemma", decodeBatch:
+ * B sequences each advance by one token over their own slot; allocSlotKv:
+ * one slot per concurrent sequence), so the step shards by slot ownership:
+ * each rank (one GPU) holds the KV of a contiguous range of the global slots
+ * in its own handle and runs the rows whose slots it owns.  No rank reads
+ * another's memory and the step needs no collective; only a consumer that
+ * wants every row's output on one device gathers out afterwards.
+ *
+ * slot_kv_shard_range -- the global slots rank `rank` of n_ranks owns:
+ * [*first, *first + *count) with first = floor(rank * n_slots / n_ranks)
+ * (balanced contiguous ranges; count >= 1).  Global slot s is local slot
+ * s - first of its owner, which allocates a handle of `count` slots.
+ * SLOTKV_ERR_ARG unless 1 <= n_ranks <= n_slots and rank < n_ranks.  Host
+ * only; first and count may be NULL.
+ */
+int slot_kv_shard_range(uint32_t n_ranks, uint32_t n_slots, uint32_t rank, uint32_t* first,
+                        uint32_t* count);
+
+/*
+ * slot_kv_shard_route -- route one step's rows to the ranks that own their
+ * slots.  slots: HOST u32[B], global slot ids.  Outputs (host, caller-owned):
+ *   order[B]            the row indices grouped by owning rank, in
+ *                       increasing order within a rank (a permutation of
+ *                       0..B-1);
+ *   offsets[n_ranks+1]  rank r's rows are order[offsets[r] .. offsets[r+1]);
+ *   local_slots[B]      local_slots[i] = the owner's local slot of row
+ *                       order[i].
+ * A row whose slot is >= n_slots goes to the last rank with a local slot
+ * past that rank's range, so its decode step skips it and raises
+ * SLOTKV_DEV_RANGE, as for an out-of-range slot on one GPU.  Host only.
+ * SLOTKV_ERR_ARG unless 1 <= n_ranks <= n_slots, or for a NULL pointer.
+ */
+int slot_kv_shard_route(uint32_t n_ranks, uint32_t n_slots, uint32_t B, const uint32_t* slots,
+                        uint32_t* order, uint32_t* offsets, uint32_t* local_slots);
+
+/*
  * slot_kv_get_status -- synchronise `stream`, return the sticky device flags
  * (SLOTKV_DEV_*) raised since the last call in *flags, and clear them.  After
  * SLOTKV_DEV_TIMEOUT the workspace is also cleared so later calls are valid.

@@ -65,6 +65,9 @@ EXPORTS = {
     "decode_batch_attn_noalloc": ([_vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp],
                                   _int),
+    "slot_kv_shard_range": ([_u32, _u32, _u32, ctypes.POINTER(_u32), ctypes.POINTER(_u32)],
+                            _int),
+    "slot_kv_shard_route": ([_u32, _u32, _u32, _vp, _vp, _vp, _vp], _int),
     "slot_kv_last_error": ([], ctypes.c_char_p),
 }
 

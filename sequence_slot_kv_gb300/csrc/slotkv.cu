@@ -690,6 +690,56 @@ int decode_batch_attn_paged_host(slotkv_t h, uint32_t B, uint32_t n_head, const 
                      });
 }
 
+// Slot ownership: rank r of n_ranks owns the global slots
+// [floor(r*n/N), floor((r+1)*n/N)); every rank owns at least one when
+// n_slots >= n_ranks.  The owner of slot s < n is the largest r whose range
+// starts at or below s: r = floor((s*N + N - 1) / n).
+static uint32_t shard_first(uint32_t n_ranks, uint32_t n_slots, uint32_t r) {
+    return (uint32_t)(((uint64_t)r * n_slots) / n_ranks);
+}
+
+int slot_kv_shard_range(uint32_t n_ranks, uint32_t n_slots, uint32_t rank, uint32_t* first,
+                        uint32_t* count) {
+    g_err[0] = 0;
+    if (n_ranks == 0 || n_slots < n_ranks)
+        return fail(SLOTKV_ERR_ARG, "need 1 <= n_ranks <= n_slots (n_ranks=%u, n_slots=%u)",
+                    n_ranks, n_slots);
+    if (rank >= n_ranks) return fail(SLOTKV_ERR_ARG, "rank=%u >= n_ranks=%u", rank, n_ranks);
+    const uint32_t a = shard_first(n_ranks, n_slots, rank);
+    const uint32_t b = shard_first(n_ranks, n_slots, rank + 1);
+    if (first) *first = a;
+    if (count) *count = b - a;
+    return SLOTKV_OK;
+}
+
+int slot_kv_shard_route(uint32_t n_ranks, uint32_t n_slots, uint32_t B, const uint32_t* slots,
+                        uint32_t* order, uint32_t* offsets, uint32_t* local_slots) {
+    g_err[0] = 0;
+    if (n_ranks == 0 || n_slots < n_ranks)
+        return fail(SLOTKV_ERR_ARG, "need 1 <= n_ranks <= n_slots (n_ranks=%u, n_slots=%u)",
+                    n_ranks, n_slots);
+    if (!offsets || (B > 0 && (!slots || !order || !local_slots)))
+        return fail(SLOTKV_ERR_ARG, "null pointer");
+    auto owner = [&](uint32_t s) -> uint32_t {
+        if (s >= n_slots) return n_ranks - 1;  // out of range: the last rank skips it
+        return (uint32_t)(((uint64_t)s * n_ranks + n_ranks - 1) / n_slots);
+    };
+    // counting sort by owner: stable, so rows keep their order within a rank
+    for (uint32_t r = 0; r <= n_ranks; ++r) offsets[r] = 0;
+    for (uint32_t b = 0; b < B; ++b) ++offsets[owner(slots[b]) + 1];
+    for (uint32_t r = 0; r < n_ranks; ++r) offsets[r + 1] += offsets[r];
+    for (uint32_t b = 0; b < B; ++b) {
+        const uint32_t r = owner(slots[b]);
+        // offsets[r] is used as rank r's cursor, then restored below
+        const uint32_t at = offsets[r]++;
+        order[at] = b;
+        local_slots[at] = slots[b] - shard_first(n_ranks, n_slots, r);
+    }
+    for (uint32_t r = n_ranks; r > 0; --r) offsets[r] = offsets[r - 1];
+    offsets[0] = 0;
+    return SLOTKV_OK;
+}
+
 int slot_kv_advance_positions(uint32_t* positions, uint32_t B, uint32_t delta,
                               slotkv_stream_t stream) {
     g_err[0] = 0;

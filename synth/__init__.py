@@ -265,6 +265,16 @@ WORKLOADS = {
                       pos_rule="uniform_start", start_hi=1983, slot_rule="subset"),
 }
 
+# Shapes the library accepts beyond the five workloads: eight query heads per
+# kv head (the most the kernels take), where the per-key arithmetic is
+# highest.  Same slots, positions and KV bytes per key as the batch-32
+# workload.
+EXTRA_WORKLOADS = {
+    "gqa8_hd128": WORKLOADS["mid"].replace(name="gqa8_hd128", index=40, n_head=64),
+    "gqa8_hd256": WORKLOADS["mid"].replace(name="gqa8_hd256", index=41, n_head=32, n_kv_head=4,
+                                           head_dim=256),
+}
+
 # Scaled-down cases of two workloads, for profiler captures that must hold a
 # few GB at most: the same head geometry, split chunk and persistent grid as
 # the full workload, fewer rows and slots.

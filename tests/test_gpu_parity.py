@@ -71,9 +71,10 @@ def _sample_rows(w, k, seed):
     return sorted(rows)[: max(k, 2)]
 
 
-@pytest.mark.parametrize("name,k", [("mid", 32), ("skewed", 4), ("sinks", 24)])
+@pytest.mark.parametrize("name,k", [("mid", 32), ("skewed", 4), ("sinks", 24),
+                                    ("gqa8_hd128", 12), ("gqa8_hd256", 12)])
 def test_full_size_workload(name, k):
-    w = synth.WORKLOADS[name]
+    w = {**synth.WORKLOADS, **synth.EXTRA_WORKLOADS}[name]
     run = DeviceRun(w)
     try:
         out = run.step(0)
