@@ -712,13 +712,14 @@ def run_prefill(args):
         kv.prefill_batch_attn(q, kn, vn, ps, ss, qw, kw, inv, None, out, w.eps, w.scale,
                               stream=sp)
 
-    for _ in range(args.warmup):
-        step()
+    step()
     torch.cuda.synchronize(dev)
     assert kv.get_status(sp) == 0
     clocks = ClockSampler(0)
     clocks.start()
     time.sleep(0.3)
+    for _ in range(args.warmup):      # directly before the timed region
+        step()
     b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.mark("begin")
     b.record(stream)
@@ -729,6 +730,7 @@ def run_prefill(args):
     clocks.mark("end")
     clk = clocks.stop()
     ms = b.elapsed_time(e) / args.steps
+    assert kv.get_status(sp) == 0
 
     # End to end: every step copies its inputs from page-locked host memory,
     # runs the call and reads the output back, on the call's stream.
@@ -747,25 +749,37 @@ def run_prefill(args):
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     h2d = sum(t.numel() * t.element_size() for t in (hq, hkn, hvn, hps, hss))
     d2h = hout.numel() * hout.element_size()
-    # bytes as the path reads them: every token reads its own keys 0..pos
-    per_token_bytes = int((pos.astype(np.int64) + 1).sum()) * 2 * w.kv_dim * 4
+    # distinct K/V bytes the call reads (each sequence's keys once per kv
+    # head) and its per-token inputs and outputs
+    seq_keys = int(sum(int(pos[slots == s].max()) + 1 for s in np.unique(slots)))
+    key_bytes = seq_keys * 2 * w.kv_dim * 4
     io = n_tok * (2 * w.n_head * w.head_dim + 4 * w.kv_dim) * 4
-    # The prefill is bound by f32 arithmetic: per token and query head, 2 hd
-    # flops per key for the score and 2 hd per key for the value sum.
+    # Useful f32 flops: per token and query head, 2 hd per key for the score
+    # and 2 hd per key for the value sum, over keys 0..pos.
     flops = 4 * w.head_dim * w.n_head * int((pos.astype(np.int64) + 1).sum())
     tflops = flops / (ms / 1e3) / 1e12
-    peak, peak_kind = alu_peak_f32(dev)
+    if kv.call_shape(n_tok, prefill=True)[2] == 3:
+        # tensor cores: every f32 product is three TF32 products (hi*hi,
+        # hi*lo, lo*hi), against the dense TF32 peak
+        peak, peak_kind = tf32_peak()
+        roof = {"bound": "tensor", "achieved": 3 * tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": 3 * tflops / peak, "peak_kind": peak_kind,
+                "achieved_is": "3 TF32 products per useful f32 product, useful (causal) keys only",
+                "kernel": "slotkv_prefill_tc_kernel (with its prep and plan kernels)"}
+    else:
+        peak, peak_kind = alu_peak_f32(dev)
+        roof = {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": tflops / peak, "peak_kind": peak_kind,
+                "kernel": "slotkv_decode_attn_kernel (prefill mode)"}
+    roof.update({"traffic": None, "alg_flops_per_launch": flops, "avg_launch_us": ms * 1e3,
+                 "effective_f32_TFLOPs": tflops})
     line = {"metric": "slot-attn prefill tokens/s", "value": n_tok / (ms / 1e3),
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": prefill_config(w),
-            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "peak_kind": peak_kind, "traffic": None,
-                         "alg_flops_per_launch": flops, "avg_launch_us": ms * 1e3,
-                         "kernel": "slotkv_decode_attn_kernel (prefill mode)"},
-            "key_bytes_read_per_step": per_token_bytes, "io_bytes_per_step": io,
-            "effective_GBps": (per_token_bytes + io) / (ms / 1e3) / 1e9,
+            "roofline": roof,
+            "key_bytes_per_step": key_bytes, "io_bytes_per_step": io,
             "e2e": {"value": n_tok / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * kv.call_shape(n_tok, prefill=True)[2],
@@ -777,6 +791,18 @@ def run_prefill(args):
                                 "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     kv.free()
+
+
+def tf32_peak():
+    """Dense TF32 tensor peak: the measured bf16 GEMM peak (burst) times the
+    nominal TF32/bf16 ratio 1.1/2.25, in TFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        kind = "measured bf16 burst x 1.1/2.25"
+    except (OSError, KeyError, ValueError):
+        bf16, kind = 1900.0, "fallback bf16 1.9 PFLOP/s x 1.1/2.25"
+    return bf16 * 1.1 / 2.25, kind
 
 
 def alu_peak_f32(dev):

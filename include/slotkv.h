@@ -186,6 +186,17 @@ int decode_batch_attn(slotkv_t handle, uint32_t B, uint32_t n_head, const float*
  * Arguments as decode_batch_attn with B = n_tok (<= max_rows); q, k_new,
  * v_new, positions, slots and out are indexed by token.  The options of
  * slot_kv_set_options apply.  Errors as decode_batch_attn.
+ *
+ * Head dims 64 and 128 run on the tensor cores: consecutive tokens of one
+ * slot (a run; give each sequence's tokens one after another) are cut into
+ * tiles of 128 / G tokens, and each tile reads its slot's keys once for all
+ * its rows.  Products are formed from three TF32 tensor-core products (high
+ * and low parts of both operands), which keeps them within f32 rounding of
+ * the f32 result.  Tokens in any order stay correct; interleaved slots only
+ * make the tiles smaller.  This path keeps a workspace in the handle (the
+ * rotated queries and the tile list), grown to the largest n_tok * n_head
+ * seen: a call larger than any before allocates (and synchronises the
+ * device) first.  Head dim 256 runs the decode kernel once per token.
  */
 int prefill_batch_attn(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const float* q,
                        const float* k_new, const float* v_new, const uint32_t* positions,
@@ -416,7 +427,9 @@ int slot_kv_set_split(slotkv_t handle, uint32_t min_chunk_keys, uint32_t max_spl
  * running it (host only): *chunk_keys the split chunk C of the current policy,
  * *ctas the persistent CTAs of the decode kernel, *kernels the kernels the
  * call launches on its stream (KV write for prefill, work-list plan unless
- * every item is a CTA's first item, decode).  bt_stride: 0 for slot calls,
+ * every item is a CTA's first item, decode).  For a tensor-core prefill
+ * (head dims 64 and 128): the keys per pipeline stage, one CTA per SM, and
+ * three kernels (prep, plan, attention).  bt_stride: 0 for slot calls,
  * the table width for decode_batch_attn_paged; prefill: nonzero for
  * prefill_batch_attn.  Any output pointer may be NULL.  SLOTKV_ERR_ARG for
  * B = 0 or B > max_rows.

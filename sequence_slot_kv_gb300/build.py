@@ -1,7 +1,8 @@
 """Build libslotkv.so in place for sm_103a.
 
-The translation units compile in parallel (one per head dim, the host side,
-the allocation-free entry point), then link into ``sequence_slot_kv_gb300/libslotkv.so``.
+The translation units compile in parallel (one per head dim for the decode
+and the tensor-core prefill kernels, the host side, the allocation-free
+entry point), then link into ``sequence_slot_kv_gb300/libslotkv.so``.
 """
 import os
 import subprocess
@@ -13,8 +14,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libslotkv.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = ["slotkv.cu", "decode_attn_hd64.cu", "decode_attn_hd128.cu", "decode_attn_hd256.cu",
-           "noalloc.cu"]
-DEPS = ["params.h", "decode_attn.cuh"]
+           "noalloc.cu", "prefill_tc_hd64.cu", "prefill_tc_hd128.cu"]
+DEPS = ["params.h", "decode_attn.cuh", "prefill_tc.cuh", "tc_ops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE] + ARCH
 

@@ -55,6 +55,32 @@ struct DecodeParams {
     uint32_t no_plan = 0;
 };
 
+// The tensor-core prefill (head dims 64 and 128): prep, plan and attention
+// kernels over tiles of consecutive same-slot tokens (see prefill_tc.cuh).
+struct PrefillParams {
+    const float* q;          // [n_tok][n_head][hd]
+    const float* k_new;      // [n_tok][n_kv_head][hd]
+    const float* v_new;      // [n_tok][n_kv_head][hd]
+    const uint32_t* positions;
+    const uint32_t* slots;
+    const float* q_norm_w;
+    const float* k_norm_w;
+    const float* inv_freq;
+    const float* sinks;      // [n_head] or null
+    float* out;              // [n_tok][n_head][hd]
+    float* K;                // slot buffers [n_slots][slot_ctx][n_kv_head][hd]
+    float* V;
+    float* q_rot;            // workspace [n_tok][n_head][hd]: normed, rotated, scaled q
+    uint32_t* tiles;         // workspace [n_tok][4]: first token, tokens, slot, largest position
+    uint32_t* tile_of;       // workspace [n_tok]: each token's tile
+    uint32_t* plan;          // [0] items (tiles * n_kv_head), [1] next item to hand out
+    uint32_t* status;        // sticky SLOTKV_DEV_* flags
+    uint32_t n_slots, slot_ctx, n_head, n_kv_head, n_tok;
+    float eps;
+    float scale_log2;        // softmax scale * log2(e)
+    uint32_t flags;          // SLOTKV_OPT_* norm options
+};
+
 // Keys per split chunk for a row with n_keys keys (p + 1).  Depends only on
 // n_keys and the geometry so that a row's result never depends on the batch.
 __host__ __device__ inline uint32_t split_chunk(uint32_t n_keys, uint32_t chunk_min,
@@ -92,5 +118,16 @@ int launch_decode_hd128(int G, const DecodeParams& p, const CUtensorMap& tmK,
                         const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
 int launch_decode_hd256(int G, const DecodeParams& p, const CUtensorMap& tmK,
                         const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
+
+// Tensor-core prefill launchers (prep, plan, attention on `stream`); tmK and
+// tmV are the 128-byte-swizzled views of the slot buffers with a box of 32
+// floats x prefill_tile_keys(hd) rows.  Return a cudaError_t value.
+int launch_prefill_tc_hd64(int G, const PrefillParams& p, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
+int launch_prefill_tc_hd128(int G, const PrefillParams& p, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
+
+// Keys per pipeline stage of the tensor-core prefill.
+__host__ __device__ constexpr int prefill_tile_keys(int hd) { return hd == 64 ? 64 : 32; }
 
 }  // namespace slotkv

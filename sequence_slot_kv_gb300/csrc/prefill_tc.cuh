@@ -1,0 +1,675 @@
+// prefill_tc.cuh -- batched causal prefill on the tensor cores, for head dims
+// 64 and 128 ("Forward Cuda Gemma", prefillBatched: all prompt tokens of a
+// call at once, equal to running them one decode step at a time; "Forward
+// Cuda", batched prefill into the given slot).
+//
+// Three kernels per call, on one stream:
+//   * slotkv_prefill_prep_kernel: one warp per (token, head).  Query heads:
+//     q' = RoPE(RMSnorm(q) * w) * scale * log2(e) into a workspace; kv heads:
+//     k' = RoPE(RMSnorm(k_new) * w) and v into the token's slot row.  The
+//     vector routines are the decode kernel's, so q' and k' are the same
+//     bits as a decode step's.
+//   * slotkv_prefill_plan_kernel (one CTA): cuts each run of consecutive
+//     same-slot tokens into tiles of MT = 128 / G tokens -- a tile's G query
+//     heads per token make the 128 rows of one MMA -- and lists the tiles.
+//     A work item is one (tile, kv head): keys 0 .. the tile's largest
+//     position, read once for all its rows.
+//   * slotkv_prefill_tc_kernel (persistent, one CTA per SM): flash attention
+//     of each item with f32 accuracy from TF32 tensor-core products, split
+//     in three: a = a_hi + a_lo with a_hi = a with its low 13 mantissa bits
+//     cleared (exact in TF32) and a_lo = a - a_hi (exact in f32), and
+//     a.b ~ a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the dropped a_lo.b_lo and the
+//     TF32 rounding of the lo parts are ~2^-20 relative).
+//       - warp 4 (producer): claims items, streams the key tiles' K and V
+//         (BK keys x hd, 128-byte swizzled boxes of 32 floats) into a
+//         3-stage ring with TMA;
+//       - warps 6-7 (converters): split each landed K and V tile in place
+//         into hi and lo operand buffers (and zero keys past the item's
+//         last);
+//       - warp 5 (MMA issuer, one thread): S = Q K^T into a double-buffered
+//         TMEM score tile (A = Q from TMEM), then O += P V (A = P from TMEM,
+//         B = V read as an MN-major operand);
+//       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
+//         the item's q rows (hi, lo) into TMEM, then per key tile read S,
+//         apply the causal mask (key <= the row's position), run a base-2
+//         online softmax with a lazily raised max, rescale O in TMEM when
+//         the max moves, write P (hi, lo) into TMEM; at the end read O,
+//         normalise (sink included) and store out.
+// Every mbarrier wait is bounded; on expiry the CTA raises SLOTKV_DEV_TIMEOUT
+// and every role leaves its loop; the MMA thread waits for its MMAs and the
+// producer for its copies before tensor memory is freed.
+#pragma once
+
+#include "decode_attn.cuh"
+#include "tc_ops.cuh"
+
+namespace slotkv {
+
+template <int HD, int G>
+struct PCfg {
+    static constexpr int M = 128;               // query rows per tile (MMA M)
+    static constexpr int MT = M / G;            // tokens per tile
+    static constexpr int ROWS = MT * G;         // rows in use (<= 128)
+    static constexpr int BK = prefill_tile_keys(HD);  // keys per stage
+    static constexpr int NB = HD / 32;          // 128-byte column blocks per row
+    static constexpr int S = 3;                 // pipeline stages
+    static constexpr int BLK = BK * 128;        // one column block: BK rows x 128 B
+    static constexpr int BUF = NB * BLK;        // one operand buffer, [BK][HD] f32
+    static constexpr int STAGE = 4 * BUF;       // K hi | K lo | V hi | V lo
+    static constexpr int NSW = 4;               // softmax warps
+    static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
+    static constexpr int THREADS = 256;
+    // tensor memory columns: Q hi | Q lo | O | S[2] | P hi | P lo
+    static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_O = 2 * HD, C_S = 3 * HD;
+    static constexpr uint32_t C_PHI = 3 * HD + 2 * BK, C_PLO = 3 * HD + 3 * BK;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(3 * HD + 4 * BK <= 512, "tensor memory columns");
+    static_assert(BK % 32 == 0 && HD % 32 == 0, "32-column tensor memory accesses");
+    // shared memory after the ring: item descriptors [2][8] | stage meta [S][4]
+    // | barriers | tensor memory address | abort flag
+    static constexpr int OFF_DESC = S * STAGE;
+    static constexpr int OFF_META = OFF_DESC + 2 * 32;
+    static constexpr int OFF_BAR = OFF_META + S * 16;
+    // full[S], conv[S], empty[S], s_full[2], s_free[2], p_ready, pv_done,
+    // q_ready, item_full[2], item_free[2], drain
+    static constexpr int NBAR = 3 * S + 12;
+    static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_MISC = OFF_TSLOT + 16;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM = SMEM_USED + 1024;   // slack to align the ring to 1 KiB
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(BLK % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
+    static constexpr uint32_t IDESC_QK = tc::idesc_tf32(M, BK, false);
+    static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, true);
+};
+
+// Split x into an exactly-TF32 high part and the f32 remainder.
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+    const uint32_t h = __float_as_uint(x) & 0xFFFFE000u;
+    hi = h;
+    lo = __float_as_uint(x - __uint_as_float(h));
+}
+
+// ------------------------------------------------------------------ prep
+template <int HD>
+__global__ void __launch_bounds__(128) slotkv_prefill_prep_kernel(const PrefillParams P) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t wg = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const uint32_t per_tok = P.n_head + P.n_kv_head;
+    const uint32_t tok = wg / per_tok, x = wg % per_tok;
+    if (tok >= P.n_tok) return;
+    const uint32_t p = P.positions[tok], slot = P.slots[tok];
+    if (slot >= P.n_slots || p >= P.slot_ctx) return;  // the plan raises the flag
+    float cs[HD / 64], sn[HD / 64];
+    warp_rope_angles<HD>(p, P.inv_freq, cs, sn, lane);
+    const float w1 = (P.flags & kOptNormPlusOne) ? 1.0f : 0.0f;
+    if (x < P.n_head) {
+        const size_t at = (static_cast<size_t>(tok) * P.n_head + x) * HD;
+        warp_norm_rope<HD>(P.q + at, P.q_rot + at, P.q_norm_w, w1, P.scale_log2, P.eps, cs, sn,
+                           lane);
+        return;
+    }
+    const uint32_t kvh = x - P.n_head;
+    const size_t src = (static_cast<size_t>(tok) * P.n_kv_head + kvh) * HD;
+    const size_t dst = ((static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh) * HD;
+    warp_norm_rope<HD>(P.k_new + src, P.K + dst, P.k_norm_w, w1, 1.0f, P.eps, cs, sn, lane);
+    if (P.flags & kOptVNorm) {
+        warp_rms_norm_plain<HD>(P.v_new + src, P.V + dst, P.eps, lane);
+    } else {
+#pragma unroll
+        for (int j = 0; j < HD / 32; ++j) P.V[dst + lane + 32 * j] = P.v_new[src + lane + 32 * j];
+    }
+}
+
+// ------------------------------------------------------------------ plan
+// One CTA of 1024 threads, tokens in rounds of 1024.  A run is a maximal
+// sequence of consecutive in-range tokens with the same slot; token i starts
+// a tile when its index within its run is a multiple of MT.  Tile records:
+// (first token, tokens, slot, largest position).  Out-of-range tokens raise
+// SLOTKV_DEV_RANGE and belong to no tile.
+template <int MT>
+__global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const PrefillParams P) {
+    __shared__ int warp_max[32];
+    __shared__ uint32_t warp_sum[32];
+    __shared__ int carry_start;
+    __shared__ uint32_t carry_tiles;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        carry_start = -1;
+        carry_tiles = 0;
+    }
+    __syncthreads();
+    uint4* tiles = reinterpret_cast<uint4*>(P.tiles);
+    for (uint32_t r0 = 0; r0 < P.n_tok; r0 += 1024) {
+        const uint32_t i = r0 + tid;
+        bool valid = false, start = false;
+        uint32_t slot = 0;
+        if (i < P.n_tok) {
+            slot = P.slots[i];
+            valid = slot < P.n_slots && P.positions[i] < P.slot_ctx;
+            if (!valid) atomicOr(P.status, kDevRange);
+            if (valid) {
+                if (i == 0) {
+                    start = true;
+                } else {
+                    const uint32_t ps = P.slots[i - 1];
+                    start = ps != slot || P.positions[i - 1] >= P.slot_ctx;
+                }
+            }
+        }
+        // the latest run start at or before i: an inclusive prefix max
+        int a = start ? static_cast<int>(i) : -1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, a, off);
+            if (lane >= off) a = a > o ? a : o;
+        }
+        if (lane == 31) warp_max[warp] = a;
+        __syncthreads();
+        if (warp == 0) {
+            int v = warp_max[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v = v > o ? v : o;
+            }
+            warp_max[lane] = v;
+        }
+        __syncthreads();
+        int rs = warp > 0 ? warp_max[warp - 1] : -1;
+        rs = rs > carry_start ? rs : carry_start;
+        rs = rs > a ? rs : a;
+        const bool tflag = valid && ((i - static_cast<uint32_t>(rs)) % MT) == 0;
+        // tile index: an inclusive prefix sum of the tile starts
+        uint32_t c = tflag ? 1u : 0u;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, c, off);
+            if (lane >= off) c += o;
+        }
+        if (lane == 31) warp_sum[warp] = c;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t v = warp_sum[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += o;
+            }
+            warp_sum[lane] = v;
+        }
+        __syncthreads();
+        const uint32_t incl = c + (warp > 0 ? warp_sum[warp - 1] : 0u) + carry_tiles;
+        if (tflag) tiles[incl - 1] = make_uint4(i, 0u, slot, 0u);
+        if (i < P.n_tok) P.tile_of[i] = valid ? incl - 1 : 0xFFFFFFFFu;
+        __syncthreads();  // every thread has read the carries
+        if (tid == 1023) {
+            carry_start = rs;
+            carry_tiles = incl;
+        }
+        __syncthreads();
+    }
+    // each tile's token count and largest position
+    for (uint32_t i = tid; i < P.n_tok; i += 1024) {
+        const uint32_t t = P.tile_of[i];
+        if (t == 0xFFFFFFFFu) continue;
+        uint32_t* rec = P.tiles + 4 * static_cast<size_t>(t);
+        atomicAdd(rec + 1, 1u);
+        atomicMax(rec + 3, P.positions[i]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        P.plan[0] = carry_tiles * P.n_kv_head;
+        P.plan[1] = 0;
+    }
+}
+
+// ------------------------------------------------------------------ attention
+template <int HD, int G>
+__global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
+    slotkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+                             const __grid_constant__ CUtensorMap tmV, const PrefillParams P) {
+    using C = PCfg<HD, G>;
+    constexpr int S = C::S, BK = C::BK, NB = C::NB;
+    constexpr float kLog2e = 1.4426950408889634f;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile uint32_t* desc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_DESC);
+    volatile uint32_t* meta = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_META);
+    volatile int* misc = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
+    const uint32_t FULL = bar0, CONV = bar0 + 8 * S, EMPTY = bar0 + 16 * S;
+    const uint32_t SFULL = bar0 + 24 * S, SFREE = SFULL + 16, PREADY = SFREE + 16;
+    const uint32_t PVDONE = PREADY + 8, QREADY = PVDONE + 8, IFULL = QREADY + 8;
+    const uint32_t IFREE = IFULL + 16, DRAIN = IFREE + 16;
+    // operand buffers of a stage
+    auto k_hi = [&](uint32_t st) { return ring + st * C::STAGE; };
+    auto k_lo = [&](uint32_t st) { return ring + st * C::STAGE + C::BUF; };
+    auto v_hi = [&](uint32_t st) { return ring + st * C::STAGE + 2 * C::BUF; };
+    auto v_lo = [&](uint32_t st) { return ring + st * C::STAGE + 3 * C::BUF; };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(FULL + 8 * s, 1);
+            mbar_init(CONV + 8 * s, C::NCONV);
+            mbar_init(EMPTY + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(SFULL + 8 * b, 1);
+            mbar_init(SFREE + 8 * b, C::NSW);
+            mbar_init(IFULL + 8 * b, 1);
+            mbar_init(IFREE + 8 * b, C::NSW + 1);
+        }
+        mbar_init(PREADY, C::NSW);
+        mbar_init(PVDONE, 1);
+        mbar_init(QREADY, C::NSW);
+        mbar_init(DRAIN, 1);
+        misc[0] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(smem_addr(tslot), C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tslot;
+    auto timeout = [&]() {
+        atomicOr(P.status, kDevTimeout);
+        misc[0] = 1;
+    };
+
+    if (warp == C::WARP_TMA) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t n_items = __ldcg(P.plan);
+            const uint4* tiles = reinterpret_cast<const uint4*>(P.tiles);
+            uint32_t tile_g = 0;
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t is = k & 1;
+                if (k >= 2 && !mbar_wait(IFREE + 8 * is, ((k >> 1) - 1) & 1)) {
+                    timeout();
+                    break;
+                }
+                if (misc[0]) break;
+                volatile uint32_t* d = desc + 8 * is;
+                const uint32_t it = atomicAdd(P.plan + 1, 1u);
+                if (it >= n_items) {
+                    d[6] = 1;
+                    mbar_arrive(IFULL + 8 * is);
+                    // tell the converters: an end marker in the next stage
+                    const uint32_t st = tile_g % S;
+                    if (tile_g >= static_cast<uint32_t>(S) &&
+                        !mbar_wait(EMPTY + 8 * st, ((tile_g / S) - 1) & 1)) {
+                        timeout();
+                        break;
+                    }
+                    meta[4 * st + 1] = 1;
+                    mbar_arrive(FULL + 8 * st);
+                    break;
+                }
+                const uint4 rec = __ldcg(tiles + it / P.n_kv_head);
+                const uint32_t kvh = it % P.n_kv_head;
+                const uint32_t max_pos = rec.w;
+                const uint32_t ntiles = (max_pos + BK) / BK;  // keys 0 .. max_pos
+                d[0] = rec.x;
+                d[1] = rec.y;
+                d[2] = rec.z;
+                d[3] = max_pos;
+                d[4] = kvh;
+                d[5] = ntiles;
+                d[6] = 0;
+                mbar_arrive(IFULL + 8 * is);
+                const int y0 = static_cast<int>(rec.z * P.slot_ctx);
+                for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
+                    const uint32_t st = tile_g % S;
+                    if (tile_g >= static_cast<uint32_t>(S) &&
+                        !mbar_wait(EMPTY + 8 * st, ((tile_g / S) - 1) & 1)) {
+                        timeout();
+                        break;
+                    }
+                    if (misc[0]) break;
+                    const uint32_t left = max_pos + 1 - t * BK;
+                    meta[4 * st + 0] = left < static_cast<uint32_t>(BK) ? left : BK;
+                    meta[4 * st + 1] = 0;
+                    mbar_expect_tx(FULL + 8 * st, 2 * C::BUF);
+                    const int y = y0 + static_cast<int>(t * BK);
+#pragma unroll
+                    for (int c = 0; c < NB; ++c) {
+                        const int x = static_cast<int>(kvh * HD) + 32 * c;
+                        tma_load_2d(k_hi(st) + c * C::BLK, &tmK, x, y, FULL + 8 * st);
+                        tma_load_2d(v_hi(st) + c * C::BLK, &tmV, x, y, FULL + 8 * st);
+                    }
+                }
+                if (misc[0]) break;
+            }
+            if (misc[0]) {
+                // drain this CTA's copies that may still be in flight
+                for (uint32_t u = tile_g > static_cast<uint32_t>(S) ? tile_g - S : 0; u < tile_g; ++u)
+                    mbar_wait(FULL + 8 * (u % S), (u / S) & 1, 1ll << 28);
+            }
+        }
+    } else if (warp >= C::WARP_CONV) {
+        // ------------------------------------------------------------ converters
+        const int ct = tid - C::WARP_CONV * 32;
+        constexpr int NT = C::NCONV * 32;
+        for (uint32_t tile_g = 0;; ++tile_g) {
+            const uint32_t st = tile_g % S;
+            if (!mbar_wait(FULL + 8 * st, (tile_g / S) & 1)) {
+                timeout();
+                break;
+            }
+            if (misc[0] || meta[4 * st + 1]) break;
+            const uint32_t rows = meta[4 * st + 0];
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                float4* hi = reinterpret_cast<float4*>(smem + st * C::STAGE + 2 * which * C::BUF);
+                float4* lo = reinterpret_cast<float4*>(smem + st * C::STAGE + (2 * which + 1) * C::BUF);
+#pragma unroll 4
+                for (int i = ct; i < C::BUF / 16; i += NT) {
+                    // each 128-byte row of a column block is 8 float4s
+                    const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
+                    float4 x = hi[i];
+                    if (row >= rows) x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                    tf32_split(x.x, h0, l0);
+                    tf32_split(x.y, h1, l1);
+                    tf32_split(x.z, h2, l2);
+                    tf32_split(x.w, h3, l3);
+                    hi[i] = make_float4(__uint_as_float(h0), __uint_as_float(h1),
+                                        __uint_as_float(h2), __uint_as_float(h3));
+                    lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
+                                        __uint_as_float(l2), __uint_as_float(l3));
+                }
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(CONV + 8 * st);
+        }
+    } else if (warp == C::WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t tile_g = 0, pv_n = 0;
+            bool ok = true;
+            // O += P V for tile t of the item (global tile g)
+            auto issue_pv = [&](uint32_t t, uint32_t g) {
+                if (!mbar_wait(PREADY, pv_n & 1)) {
+                    timeout();
+                    return false;
+                }
+                tc::fence_after_sync();
+                const uint32_t st = g % S;
+#pragma unroll
+                for (int term = 0; term < 3; ++term) {
+                    const uint32_t pcol = term == 2 ? C::C_PLO : C::C_PHI;
+                    const uint32_t vb = term == 1 ? v_lo(st) : v_hi(st);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        const uint64_t b = tc::smem_desc(vb + kk * 1024, C::BLK, 1024, tc::kSwizzle128B);
+                        tc::mma_tf32_ts(tbase + C::C_O, tbase + pcol + kk * 8, b, C::IDESC_PV,
+                                        (t | term | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                tc::mma_commit(PVDONE);
+                tc::mma_commit(EMPTY + 8 * st);
+                ++pv_n;
+                return true;
+            };
+            for (uint32_t k = 0; ok; ++k) {
+                const uint32_t is = k & 1;
+                if (!mbar_wait(IFULL + 8 * is, (k >> 1) & 1)) {
+                    timeout();
+                    break;
+                }
+                const uint32_t ntiles = desc[8 * is + 5], end = desc[8 * is + 6];
+                mbar_arrive(IFREE + 8 * is);
+                if (end || misc[0]) break;
+                if (!mbar_wait(QREADY, k & 1)) {
+                    timeout();
+                    break;
+                }
+                tc::fence_after_sync();
+                for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
+                    const uint32_t st = tile_g % S, sb = tile_g & 1;
+                    if (!mbar_wait(CONV + 8 * st, (tile_g / S) & 1) ||
+                        (tile_g >= 2 && !mbar_wait(SFREE + 8 * sb, ((tile_g >> 1) - 1) & 1))) {
+                        timeout();
+                        ok = false;
+                        break;
+                    }
+                    if (misc[0]) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    // S = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
+#pragma unroll
+                    for (int term = 0; term < 3; ++term) {
+                        const uint32_t qcol = term == 2 ? C::C_QLO : C::C_QHI;
+                        const uint32_t kb = term == 1 ? k_lo(st) : k_hi(st);
+#pragma unroll
+                        for (int kk = 0; kk < HD / 8; ++kk) {
+                            const uint64_t b = tc::smem_desc(kb + (kk / 4) * C::BLK + (kk % 4) * 32, 16,
+                                                             1024, tc::kSwizzle128B);
+                            tc::mma_tf32_ts(tbase + C::C_S + sb * BK, tbase + qcol + kk * 8, b,
+                                            C::IDESC_QK, (term | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    tc::mma_commit(SFULL + 8 * sb);
+                    if (t >= 1 && !issue_pv(t - 1, tile_g - 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (ok && ntiles && !misc[0] && !issue_pv(ntiles - 1, tile_g - 1)) ok = false;
+            }
+            // every MMA issued above has completed before tensor memory is freed
+            tc::mma_commit(DRAIN);
+            mbar_wait(DRAIN, 0, 1ll << 28);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const uint32_t r = static_cast<uint32_t>(tid);  // query row = TMEM lane
+        const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t t_local = r / G, h_local = r % G;
+        uint32_t tile_g = 0, pv_w = 0;
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t is = k & 1;
+            if (!mbar_wait(IFULL + 8 * is, (k >> 1) & 1)) {
+                timeout();
+                break;
+            }
+            const uint32_t first = desc[8 * is + 0], cnt = desc[8 * is + 1];
+            const uint32_t kvh = desc[8 * is + 4], ntiles = desc[8 * is + 5];
+            const uint32_t end = desc[8 * is + 6];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(IFREE + 8 * is);
+            if (end || misc[0]) break;
+            const bool vrow = r < static_cast<uint32_t>(C::ROWS) && t_local < cnt;
+            const uint32_t tok = first + t_local;
+            const uint32_t pos = vrow ? __ldg(P.positions + tok) : 0u;
+            const uint32_t head = kvh * G + h_local;
+            // the item's q rows into tensor memory, split hi / lo
+            {
+                const float* qrow = P.q_rot + (static_cast<size_t>(vrow ? tok : 0) * P.n_head + head) * HD;
+#pragma unroll
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t hi[32], lo[32];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 x = vrow ? __ldcg(reinterpret_cast<const float4*>(qrow + c0 + c))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                        tf32_split(x.x, hi[c + 0], lo[c + 0]);
+                        tf32_split(x.y, hi[c + 1], lo[c + 1]);
+                        tf32_split(x.z, hi[c + 2], lo[c + 2]);
+                        tf32_split(x.w, hi[c + 3], lo[c + 3]);
+                    }
+                    tc::tmem_st32(lrow + C::C_QHI + c0, hi);
+                    tc::tmem_st32(lrow + C::C_QLO + c0, lo);
+                }
+                tc::tmem_st_wait();
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(QREADY);
+            float m = -CUDART_INF_F, l = 0.f;
+            bool failed = false;
+            for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
+                const uint32_t sb = tile_g & 1;
+                if (!mbar_wait(SFULL + 8 * sb, (tile_g >> 1) & 1)) {
+                    timeout();
+                    failed = true;
+                    break;
+                }
+                tc::fence_after_sync();
+                float s[BK];
+#pragma unroll
+                for (int c0 = 0; c0 < BK; c0 += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lrow + C::C_S + sb * BK + c0, v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(v[c]);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(SFREE + 8 * sb);
+                // causal mask: key kbase + c is attended iff it is <= pos
+                const uint32_t kbase = t * BK;
+                float mx = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < BK; ++c) {
+                    s[c] = kbase + static_cast<uint32_t>(c) <= pos ? s[c] : -CUDART_INF_F;
+                    mx = fmaxf(mx, s[c]);
+                }
+                // lazy running max: raised only when a score passes it by 2^8
+                float corr = 1.f;
+                bool rescale = false;
+                if (mx > m + 8.f) {
+                    corr = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
+                    rescale = t > 0;
+                    l *= corr;
+                    m = mx;
+                }
+#pragma unroll
+                for (int c = 0; c < BK; ++c) {
+                    s[c] = s[c] == -CUDART_INF_F ? 0.f : exp2f(s[c] - m);
+                    l += s[c];
+                }
+                // P and O are free once the previous tile's O += P V has completed
+                if (t > 0) {
+                    if (!mbar_wait(PVDONE, pv_w & 1)) {
+                        timeout();
+                        failed = true;
+                        break;
+                    }
+                    ++pv_w;
+                    tc::fence_after_sync();
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int c0 = 0; c0 < HD; c0 += 32) {
+                        uint32_t v[32];
+                        tc::tmem_ld32(lrow + C::C_O + c0, v);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            v[c] = __float_as_uint(__uint_as_float(v[c]) * corr);
+                        tc::tmem_st32(lrow + C::C_O + c0, v);
+                    }
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < BK; c0 += 32) {
+                    uint32_t hi[32], lo[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) tf32_split(s[c0 + c], hi[c], lo[c]);
+                    tc::tmem_st32(lrow + C::C_PHI + c0, hi);
+                    tc::tmem_st32(lrow + C::C_PLO + c0, lo);
+                }
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(PREADY);
+            }
+            if (failed || misc[0]) break;
+            // the item's last O += P V, then out = O / l (sink included)
+            if (!mbar_wait(PVDONE, pv_w & 1)) {
+                timeout();
+                break;
+            }
+            ++pv_w;
+            tc::fence_after_sync();
+            float f = 1.f / l;
+            if (P.sinks) {
+                const float sk = __ldg(P.sinks + head) * kLog2e;
+                const float M2 = fmaxf(m, sk);
+                const float c = exp2f(m - M2);
+                f = c / (l * c + exp2f(sk - M2));
+            }
+            float* orow = P.out + (static_cast<size_t>(tok) * P.n_head + head) * HD;
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(lrow + C::C_O + c0, v);
+                tc::tmem_ld_wait();
+                if (vrow) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(orow + c0 + c) =
+                            make_float4(__uint_as_float(v[c]) * f, __uint_as_float(v[c + 1]) * f,
+                                        __uint_as_float(v[c + 2]) * f, __uint_as_float(v[c + 3]) * f);
+                }
+            }
+            tc::fence_before_sync();
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tbase, C::TMEM_COLS);
+}
+
+template <int HD, int G>
+int launch_prefill_one(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       unsigned ctas, cudaStream_t stream) {
+    using C = PCfg<HD, G>;
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!(configured.load(std::memory_order_acquire) & bit) || bit == 0) {
+        cudaError_t e = cudaFuncSetAttribute(slotkv_prefill_tc_kernel<HD, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const uint32_t warps = p.n_tok * (p.n_head + p.n_kv_head);
+    slotkv_prefill_prep_kernel<HD><<<(warps + 3) / 4, 128, 0, stream>>>(p);
+    slotkv_prefill_plan_kernel<C::MT><<<1, 1024, 0, stream>>>(p);
+    slotkv_prefill_tc_kernel<HD, G><<<ctas, C::THREADS, C::SMEM, stream>>>(tmK, tmV, p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+template <int HD>
+int launch_prefill_hd(int G, const PrefillParams& p, const CUtensorMap& tmK,
+                      const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream) {
+    switch (G) {
+        case 1: return launch_prefill_one<HD, 1>(p, tmK, tmV, ctas, stream);
+        case 2: return launch_prefill_one<HD, 2>(p, tmK, tmV, ctas, stream);
+        case 3: return launch_prefill_one<HD, 3>(p, tmK, tmV, ctas, stream);
+        case 4: return launch_prefill_one<HD, 4>(p, tmK, tmV, ctas, stream);
+        case 5: return launch_prefill_one<HD, 5>(p, tmK, tmV, ctas, stream);
+        case 6: return launch_prefill_one<HD, 6>(p, tmK, tmV, ctas, stream);
+        case 7: return launch_prefill_one<HD, 7>(p, tmK, tmV, ctas, stream);
+        case 8: return launch_prefill_one<HD, 8>(p, tmK, tmV, ctas, stream);
+        default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+}
+
+}  // namespace slotkv

@@ -85,6 +85,15 @@ struct slotkv_s {
     uint32_t* st_tab = nullptr;  // block tables for decode_batch_attn_paged_host
     size_t st_tab_bytes = 0;     // (grown on demand)
     CUtensorMap tmK, tmV;
+    // tensor-core prefill (head dims 64, 128): 128-byte-swizzled views of the
+    // slot buffers, and a workspace grown on demand by prefill calls
+    bool tc_prefill = false;
+    CUtensorMap tmKs, tmVs;
+    float* pf_q = nullptr;           // [tokens][n_head][hd] rotated q
+    uint32_t* pf_tiles = nullptr;    // [tokens][4] tile records
+    uint32_t* pf_tile_of = nullptr;  // [tokens]
+    uint32_t* pf_plan = nullptr;     // item count, hand-out counter
+    size_t pf_q_elems = 0, pf_tok = 0;
 };
 
 namespace {
@@ -115,6 +124,10 @@ void release(slotkv_s* h) {
     cudaFree(h->st_pos);
     cudaFree(h->st_slots);
     cudaFree(h->st_tab);
+    cudaFree(h->pf_q);
+    cudaFree(h->pf_tiles);
+    cudaFree(h->pf_tile_of);
+    cudaFree(h->pf_plan);
     if (h->owns_kv) {
         cudaFree(h->K);
         cudaFree(h->V);
@@ -163,6 +176,49 @@ int encode_maps(slotkv_s* h) {
         if (r != CUDA_SUCCESS)
             return fail(SLOTKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
+    // the tensor-core prefill reads [keys][32 floats] boxes, 128-byte swizzled
+    h->tc_prefill = h->head_dim == 64 || h->head_dim == 128;
+    if (h->tc_prefill) {
+        const cuuint32_t sbox[2] = {32, (cuuint32_t)slotkv::prefill_tile_keys((int)h->head_dim)};
+        CUtensorMap* smaps[2] = {&h->tmKs, &h->tmVs};
+        for (int i = 0; i < 2; ++i) {
+            CUresult r = enc(smaps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, bufs[i], dims, strides,
+                             sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS)
+                return fail(SLOTKV_ERR_CUDA, "cuTensorMapEncodeTiled (swizzled) failed (%d)",
+                            (int)r);
+        }
+    }
+    return SLOTKV_OK;
+}
+
+// The tensor-core prefill's workspace, grown to n_tok tokens of n_head heads
+// (cudaMalloc synchronises the device the first time it grows).
+int prefill_workspace(slotkv_s* h, uint32_t n_tok, uint32_t n_head) {
+    const size_t qe = (size_t)n_tok * n_head * h->head_dim;
+    cudaError_t e;
+    if (qe > h->pf_q_elems) {
+        cudaFree(h->pf_q);
+        h->pf_q = nullptr;
+        h->pf_q_elems = 0;
+        if ((e = cudaMalloc(&h->pf_q, qe * sizeof(float))) != cudaSuccess)
+            return cuda_fail(e, "prefill workspace (q)");
+        h->pf_q_elems = qe;
+    }
+    if (n_tok > h->pf_tok) {
+        cudaFree(h->pf_tiles);
+        cudaFree(h->pf_tile_of);
+        h->pf_tiles = h->pf_tile_of = nullptr;
+        h->pf_tok = 0;
+        if ((e = cudaMalloc(&h->pf_tiles, (size_t)n_tok * 16)) != cudaSuccess ||
+            (e = cudaMalloc(&h->pf_tile_of, (size_t)n_tok * 4)) != cudaSuccess)
+            return cuda_fail(e, "prefill workspace (tiles)");
+        h->pf_tok = n_tok;
+    }
+    if (!h->pf_plan && (e = cudaMalloc(&h->pf_plan, 2 * sizeof(uint32_t))) != cudaSuccess)
+        return cuda_fail(e, "prefill workspace (plan)");
     return SLOTKV_OK;
 }
 
@@ -209,6 +265,15 @@ struct CallShape {
 
 CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill) {
     CallShape c;
+    if (prefill && h->tc_prefill) {
+        // prep, plan and the persistent tensor-core kernel (one CTA per SM)
+        c.chunk = (uint32_t)slotkv::prefill_tile_keys((int)h->head_dim);
+        c.ctas = (uint32_t)(h->sm_count > 0 ? h->sm_count : 1);
+        c.static_items = c.static_second = 0;
+        c.no_plan = 0;
+        c.kernels = 3;
+        return c;
+    }
     c.chunk = h->auto_split ? auto_chunk(h, B, max_keys) : h->chunk_min;
     // persistent CTAs: two per SM, never more than there can be work items
     const uint32_t gsplits = grid_splits(h, max_keys, c.chunk);
@@ -609,8 +674,43 @@ int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float*
     int rc = check_decode_args(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, out);
     if (rc != SLOTKV_OK || n_tok == 0) return rc;
-    return launch(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
-                  inv_freq, sinks, out, eps, scale, (cudaStream_t)stream, true);
+    if (!h->tc_prefill)  // head dim 256: the decode kernel in prefill mode
+        return launch(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                      inv_freq, sinks, out, eps, scale, (cudaStream_t)stream, true);
+    if ((rc = prefill_workspace(h, n_tok, n_head)) != SLOTKV_OK) return rc;
+    slotkv::PrefillParams P;
+    P.q = q;
+    P.k_new = k_new;
+    P.v_new = v_new;
+    P.positions = positions;
+    P.slots = slots;
+    P.q_norm_w = q_norm_w;
+    P.k_norm_w = k_norm_w;
+    P.inv_freq = inv_freq;
+    P.sinks = sinks;
+    P.out = out;
+    P.K = h->K;
+    P.V = h->V;
+    P.q_rot = h->pf_q;
+    P.tiles = h->pf_tiles;
+    P.tile_of = h->pf_tile_of;
+    P.plan = h->pf_plan;
+    P.status = h->status;
+    P.n_slots = h->n_slots;
+    P.slot_ctx = h->slot_ctx;
+    P.n_head = n_head;
+    P.n_kv_head = h->n_kv_head;
+    P.n_tok = n_tok;
+    P.eps = eps;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.flags = h->options;
+    const int G = (int)(n_head / h->n_kv_head);
+    const unsigned ctas = (unsigned)(h->sm_count > 0 ? h->sm_count : 1);
+    rc = h->head_dim == 64
+             ? slotkv::launch_prefill_tc_hd64(G, P, h->tmKs, h->tmVs, ctas, (cudaStream_t)stream)
+             : slotkv::launch_prefill_tc_hd128(G, P, h->tmKs, h->tmVs, ctas, (cudaStream_t)stream);
+    if (rc != 0) return cuda_fail((cudaError_t)rc, "prefill kernel launch");
+    return SLOTKV_OK;
 }
 
 int decode_batch_attn_paged(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,

@@ -1,0 +1,125 @@
+"""The tensor-core prefill (head dims 64 and 128) on the shapes it tiles:
+long runs of consecutive same-slot tokens cut into tiles of 128 / G tokens
+(several tiles per run, a partial last tile, tiles whose 128 rows are not all
+used when G does not divide 128), histories spanning many key tiles (every
+stage of the ring reused), positions out of order within a run, and the
+benchmark's prefill workload at full size.  Every token must equal one decode
+step at a time in position order ("Forward Cuda Gemma", prefillBatched), as
+the oracle computes it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_harness import assert_close, to_dev
+from sequence_slot_kv_gb300 import SlotKV
+
+pytestmark = pytest.mark.gpu
+
+
+def _workload(hd, G, n_kv, idx, n_tok, n_slots, slot_ctx, sinks=True):
+    return synth.Workload(f"pftc_hd{hd}_g{G}", 900 + idx, B=n_tok, n_slots=n_slots,
+                          slot_ctx=slot_ctx, n_head=G * n_kv, n_kv_head=n_kv, head_dim=hd,
+                          theta=1e4, sinks=sinks, pos_rule="fixed",
+                          fixed_positions=tuple([0] * n_tok), slot_rule="perm")
+
+
+def _run(w, slots, pos):
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    K = torch.empty(shape, device="cuda")
+    V = torch.empty(shape, device="cuda")
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    kv = SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
+    try:
+        assert kv.call_shape(w.B, prefill=True)[2] == 3     # prep, plan, tensor-core kernel
+        out = torch.full((w.B, w.n_head, w.head_dim), float("nan"), device="cuda")
+        s = w.sink_logits()
+        kv.prefill_batch_attn(to_dev(w.q()), to_dev(w.k_new()), to_dev(w.v_new()),
+                              to_dev(pos.astype(np.int32)), to_dev(slots.astype(np.int32)),
+                              to_dev(w.q_norm_w()), to_dev(w.k_norm_w()), to_dev(w.inv_freq()),
+                              None if s is None else to_dev(s), out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert kv.get_status() == 0
+        return out.cpu().numpy(), K, V
+    finally:
+        kv.free()
+
+
+def _oracle_rows(w, slots, pos, rows):
+    """The oracle for tokens ``rows``: every token's k' and v written into
+    host copies of the slots first (what the earlier tokens of the sequential
+    definition leave there; a token reads only positions <= its own), then
+    one decode step per sampled token."""
+    o = oracle.default()
+    used = sorted(set(int(s) for s in slots))
+    Kh = np.stack([w.hist_rows("k", s, 0, w.slot_ctx) for s in used])
+    Vh = np.stack([w.hist_rows("v", s, 0, w.slot_ctx) for s in used])
+    at = {s: i for i, s in enumerate(used)}
+    kn, vn = w.k_new(), w.v_new()
+    kw, inv = w.k_norm_w(), w.inv_freq()
+    for i in range(w.B):
+        c, p = at[int(slots[i])], int(pos[i])
+        for g in range(w.n_kv_head):
+            Kh[c, p, g] = o.norm_rope_head(kn[i, g], kw, w.eps, p, inv).astype(np.float32)
+        Vh[c, p] = vn[i]
+    rows = list(rows)
+    compact = np.array([at[int(slots[i])] for i in rows], dtype=np.uint32)
+    ref, _, skipped = o.decode_batch(Kh, Vh, w.q()[rows], kn[rows], vn[rows], pos[rows], compact,
+                                     w.q_norm_w(), kw, inv, w.sink_logits(), w.eps, w.scale,
+                                     n_threads=min(len(rows), 32))
+    assert skipped == 0
+    return ref
+
+
+SHAPES = [(hd, G) for hd in (64, 128) for G in range(1, 9)]
+
+
+@pytest.mark.parametrize("hd,G", SHAPES, ids=[f"hd{h}_g{g}" for h, g in SHAPES])
+def test_long_runs_every_group_size(hd, G):
+    """Three sequences given one after another: a run of 2.5 tiles after a
+    history of several key tiles, a one-token run, and a run starting at
+    position 0; the tokens of each run in increasing position."""
+    MT = 128 // G
+    BK = 64 if hd == 64 else 32
+    seqs = [(3, 7 * BK + 5, MT * 2 + MT // 2), (0, 41, 1), (1, 0, MT + 3)]
+    slots = np.concatenate([np.full(n, s, np.uint32) for s, _, n in seqs])
+    pos = np.concatenate([np.arange(h, h + n, dtype=np.uint32) for _, h, n in seqs])
+    w = _workload(hd, G, 2, SHAPES.index((hd, G)), len(pos), 5, int(pos.max()) + 7,
+                  sinks=(G % 2 == 1))
+    got, K, V = _run(w, slots, pos)
+    ref = _oracle_rows(w, slots, pos, range(w.B))
+    assert_close(got, ref, f"tensor-core prefill hd={hd} G={G}")
+    # the written rows: V exact, K as a decode step writes it
+    Vg = V[torch.from_numpy(slots.astype(np.int64)).cuda(),
+           torch.from_numpy(pos.astype(np.int64)).cuda()].cpu().numpy()
+    assert np.array_equal(Vg.view(np.uint32), w.v_new().view(np.uint32))
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_unordered_positions_within_a_run(hd):
+    """One slot's tokens in a shuffled order (a run is consecutive tokens of
+    one slot, in any position order): each row's causal mask follows its own
+    position."""
+    G, n = 4, 150
+    rng = np.random.default_rng(hd)
+    pos = (300 + rng.permutation(n)).astype(np.uint32)
+    slots = np.full(n, 2, np.uint32)
+    w = _workload(hd, G, 2, 40 + hd, n, 3, 300 + n + 3)
+    got, _, _ = _run(w, slots, pos)
+    ref = _oracle_rows(w, slots, pos, range(n))
+    assert_close(got, ref, f"unordered run hd={hd}")
+
+
+def test_bench_prefill_workload_full_size():
+    """The benchmark's prefill: 8 sequences, a 512-token chunk each after
+    1536 positions of history, 32 query / 8 kv heads, head dim 128; sampled
+    tokens of every sequence against the oracle."""
+    import bench
+    w, slots, pos = bench.prefill_workload()
+    got, _, _ = _run(w, slots.astype(np.uint32), pos.astype(np.uint32))
+    assert np.all(np.isfinite(got))
+    chunk = bench.PREFILL_CHUNK
+    rows = sorted({s * chunk + j for s in range(bench.PREFILL_SEQ) for j in (0, 31, 32, 257, 511)})
+    ref = _oracle_rows(w, slots, pos, rows)
+    assert_close(got[rows], ref, "prefill workload sampled tokens")
