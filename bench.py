@@ -48,7 +48,10 @@ FLUSH_BYTES = 256 * 1024 * 1024  # written between calls of a step that fits in 
 # captures of dram__bytes_read.sum and dram__bytes_write.sum, valid only for
 # the kernel source they were taken on (sha256 prefix of decode_attn.cuh).
 MEASURED_TRAFFIC = {
-    "39235ddca432a3f1": {"mid": 555_406_848, "sinks": 2_342_313_216},
+    # all at full size; large's is its first step's ratio to the algorithmic
+    # bytes times the mean algorithmic bytes of its 64 steps
+    "39235ddca432a3f1": {"mid": 555_406_848, "sinks": 2_342_313_216,
+                         "skewed": 17_226_702_464, "large": 2_238_538_410},
 }
 
 

@@ -239,7 +239,8 @@ def test_call_shape():
     try:
         chunk, ctas, kernels = run.kv.call_shape(tiny.B)
         assert kernels == 1 and ctas == tiny.B * tiny.n_kv_head
-        assert run.kv.call_shape(tiny.B, prefill=True)[2] == 2
+        # head dim 64 prefills on the tensor cores: prep, plan, attention
+        assert run.kv.call_shape(tiny.B, prefill=True)[2] == 3
         run.kv.set_split(64, 8)
         assert run.kv.call_shape(tiny.B)[0] == 64
     finally:
