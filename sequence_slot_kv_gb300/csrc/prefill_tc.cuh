@@ -23,12 +23,14 @@
 //       - warp 4 (producer): claims items, streams the key tiles' K and V
 //         (BK keys x hd, 128-byte swizzled boxes of 32 floats) into a
 //         3-stage ring with TMA;
-//       - warps 6-7 (converters): split each landed K and V tile in place
-//         into hi and lo operand buffers (and zero keys past the item's
-//         last);
+//       - warps 6-7 (converters): split each landed K tile in place into
+//         hi and lo operand buffers, and transpose each landed V tile into
+//         a keys-contiguous layout while splitting it (TF32 MMA operands
+//         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
+//         keys past the item's last are zeroed;
 //       - warp 5 (MMA issuer, one thread): S = Q K^T into a double-buffered
 //         TMEM score tile (A = Q from TMEM), then O += P V (A = P from TMEM,
-//         B = V read as an MN-major operand);
+//         B = the transposed V tile);
 //       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
 //         the item's q rows (hi, lo) into TMEM, then per key tile read S,
 //         apply the causal mask (key <= the row's position), run a base-2
@@ -56,6 +58,11 @@ struct PCfg {
     static constexpr int BLK = BK * 128;        // one column block: BK rows x 128 B
     static constexpr int BUF = NB * BLK;        // one operand buffer, [BK][HD] f32
     static constexpr int STAGE = 4 * BUF;       // K hi | K lo | V hi | V lo
+    // V transposed: KB column blocks of 32 keys, each [HD rows][128 B]; the
+    // 32 x 32 sub-block (key block kb, dim block db) lands at kb * VT_BLK +
+    // db * 4096 (TMA put it at db * BLK + kb * 4096)
+    static constexpr int KB = BK / 32;
+    static constexpr int VT_BLK = HD * 128;
     static constexpr int NSW = 4;               // softmax warps
     static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
     static constexpr int THREADS = 256;
@@ -80,8 +87,16 @@ struct PCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(BLK % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
     static constexpr uint32_t IDESC_QK = tc::idesc_tf32(M, BK, false);
-    static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, true);
+    static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, false);
+    static_assert(KB * NB <= 2 * NCONV, "two V sub-blocks per converter warp");
+    static_assert(NCONV == 2, "the converters' stop flags are misc[2], misc[3]");
 };
+
+// Named barrier 2 over the converter warps (N threads).
+template <int N>
+__device__ __forceinline__ void named_sync_conv() {
+    asm volatile("bar.sync 2, %0;" ::"n"(N) : "memory");
+}
 
 // Split x into an exactly-TF32 high part and the f32 remainder.
 __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
@@ -360,16 +375,21 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         constexpr int NT = C::NCONV * 32;
         for (uint32_t tile_g = 0;; ++tile_g) {
             const uint32_t st = tile_g % S;
-            if (!mbar_wait(FULL + 8 * st, (tile_g / S) & 1)) {
-                timeout();
-                break;
-            }
-            if (misc[0] || meta[4 * st + 1]) break;
+            // Both converter warps meet at named barriers below, so they must
+            // stop at the same tile: each publishes its own reason to stop
+            // (a wait that expired, an abort, the end marker) and both
+            // decide from the two published flags.
+            const bool ok = mbar_wait(FULL + 8 * st, (tile_g / S) & 1);
+            if (!ok) timeout();
+            if (lane == 0) misc[2 + (ct >> 5)] = (!ok || misc[0] || meta[4 * st + 1]) ? 1 : 0;
+            named_sync_conv<C::NCONV * 32>();
+            if (misc[2] | misc[3]) break;
             const uint32_t rows = meta[4 * st + 0];
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                float4* hi = reinterpret_cast<float4*>(smem + st * C::STAGE + 2 * which * C::BUF);
-                float4* lo = reinterpret_cast<float4*>(smem + st * C::STAGE + (2 * which + 1) * C::BUF);
+            uint8_t* stage = smem + st * C::STAGE;
+            // K: hi in place, lo beside it (both K-major, as TMA laid them)
+            {
+                float4* hi = reinterpret_cast<float4*>(stage);
+                float4* lo = reinterpret_cast<float4*>(stage + C::BUF);
 #pragma unroll 4
                 for (int i = ct; i < C::BUF / 16; i += NT) {
                     // each 128-byte row of a column block is 8 float4s
@@ -385,6 +405,50 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                                         __uint_as_float(h2), __uint_as_float(h3));
                     lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
                                         __uint_as_float(l2), __uint_as_float(l3));
+                }
+            }
+            // V: every 32 x 32 sub-block transposed (keys along the 128-byte
+            // rows), hi into the V buffer, lo into the V lo buffer.  Each warp
+            // reads its sub-blocks (lane = dim, one key per load) before any
+            // converter thread writes, so the in-place permutation is safe.
+            {
+                uint8_t* vh = stage + 2 * C::BUF;
+                uint8_t* vl = stage + 3 * C::BUF;
+                const int w = ct >> 5;
+                float x[2][32];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int sb = w + C::NCONV * j;
+                    if (sb < C::KB * NB) {
+                        const int kb = sb / NB, db = sb % NB;
+                        const uint8_t* src = vh + db * C::BLK + kb * 4096;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 +
+                                                 (((lane / 4) ^ (k % 8)) * 16) + (lane % 4) * 4;
+                            const float v = *reinterpret_cast<const float*>(src + off);
+                            x[j][k] = static_cast<uint32_t>(kb * 32 + k) < rows ? v : 0.f;
+                        }
+                    }
+                }
+                named_sync_conv<C::NCONV * 32>();
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int sb = w + C::NCONV * j;
+                    if (sb < C::KB * NB) {
+                        const int kb = sb / NB, db = sb % NB;
+                        const uint32_t base = kb * C::VT_BLK + db * 4096 + (lane / 8) * 1024 +
+                                              (lane % 8) * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t h[4], l[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) tf32_split(x[j][4 * c + e], h[e], l[e]);
+                            const uint32_t off = base + ((c ^ (lane % 8)) * 16);
+                            *reinterpret_cast<uint4*>(vh + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<uint4*>(vl + off) = make_uint4(l[0], l[1], l[2], l[3]);
+                        }
+                    }
                 }
             }
             tc::fence_proxy_async_smem();
@@ -410,7 +474,8 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     const uint32_t vb = term == 1 ? v_lo(st) : v_hi(st);
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
-                        const uint64_t b = tc::smem_desc(vb + kk * 1024, C::BLK, 1024, tc::kSwizzle128B);
+                        const uint64_t b = tc::smem_desc(vb + (kk / 4) * C::VT_BLK + (kk % 4) * 32, 16,
+                                                         1024, tc::kSwizzle128B);
                         tc::mma_tf32_ts(tbase + C::C_O, tbase + pcol + kk * 8, b, C::IDESC_PV,
                                         (t | term | kk) != 0 ? 1u : 0u);
                     }
