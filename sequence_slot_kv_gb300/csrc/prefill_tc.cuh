@@ -28,15 +28,19 @@
 //         a keys-contiguous layout while splitting it (TF32 MMA operands
 //         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
 //         keys past the item's last are zeroed;
-//       - warp 5 (MMA issuer, one thread): S = Q K^T into a double-buffered
-//         TMEM score tile (A = Q from TMEM), then O += P V (A = P from TMEM,
-//         B = the transposed V tile);
+//       - warp 5 (MMA issuer, one thread): S = Q K^T into one of two TMEM
+//         score buffers (A = Q from TMEM), then O += P V (A = P from TMEM,
+//         B = the transposed V tile).  Issue order QK(t+1), PV(t), QK(t+2),
+//         PV(t+1), ...; MMAs from one thread run in issue order, so QK(t+2)
+//         reuses buffer t % 2 only after PV(t) has read it;
 //       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
 //         the item's q rows (hi, lo) into TMEM, then per key tile read S,
 //         apply the causal mask (key <= the row's position), run a base-2
-//         online softmax with a lazily raised max, rescale O in TMEM when
-//         the max moves, write P (hi, lo) into TMEM; at the end read O,
-//         normalise (sink included) and store out.
+//         online softmax with a lazily raised max, write P (hi over S, lo
+//         beside it) into the same buffer -- while the previous tile's
+//         O += P V runs -- and, only when the max moves, wait for that PV
+//         and rescale O in TMEM; at the end read O, normalise (sink
+//         included) and store out.
 // Every mbarrier wait is bounded; on expiry the CTA raises SLOTKV_DEV_TIMEOUT
 // and every role leaves its loop; the MMA thread waits for its MMAs and the
 // producer for its copies before tensor memory is freed.
@@ -66,9 +70,10 @@ struct PCfg {
     static constexpr int NSW = 4;               // softmax warps
     static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
     static constexpr int THREADS = 256;
-    // tensor memory columns: Q hi | Q lo | O | S[2] | P hi | P lo
+    // tensor memory columns: Q hi | Q lo | O | two buffers of (S, then P hi
+    // over it | P lo)
     static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_O = 2 * HD, C_S = 3 * HD;
-    static constexpr uint32_t C_PHI = 3 * HD + 2 * BK, C_PLO = 3 * HD + 3 * BK;
+    static constexpr uint32_t C_BUF = 2 * BK;   // columns per score buffer
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(3 * HD + 4 * BK <= 512, "tensor memory columns");
     static_assert(BK % 32 == 0 && HD % 32 == 0, "32-column tensor memory accesses");
@@ -77,8 +82,8 @@ struct PCfg {
     static constexpr int OFF_DESC = S * STAGE;
     static constexpr int OFF_META = OFF_DESC + 2 * 32;
     static constexpr int OFF_BAR = OFF_META + S * 16;
-    // full[S], conv[S], empty[S], s_full[2], s_free[2], p_ready, pv_done,
-    // q_ready, item_full[2], item_free[2], drain
+    // full[S], conv[S], empty[S], s_full[2], p_ready[2], pv_done, q_ready,
+    // item_full[2], item_free[2], drain, (one spare)
     static constexpr int NBAR = 3 * S + 12;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
@@ -257,8 +262,8 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     const uint32_t ring = smem_addr(smem);
     const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
     const uint32_t FULL = bar0, CONV = bar0 + 8 * S, EMPTY = bar0 + 16 * S;
-    const uint32_t SFULL = bar0 + 24 * S, SFREE = SFULL + 16, PREADY = SFREE + 16;
-    const uint32_t PVDONE = PREADY + 8, QREADY = PVDONE + 8, IFULL = QREADY + 8;
+    const uint32_t SFULL = bar0 + 24 * S, PREADY = SFULL + 16;
+    const uint32_t PVDONE = PREADY + 16, QREADY = PVDONE + 8, IFULL = QREADY + 8;
     const uint32_t IFREE = IFULL + 16, DRAIN = IFREE + 16;
     // operand buffers of a stage
     auto k_hi = [&](uint32_t st) { return ring + st * C::STAGE; };
@@ -274,11 +279,10 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(SFULL + 8 * b, 1);
-            mbar_init(SFREE + 8 * b, C::NSW);
+            mbar_init(PREADY + 8 * b, C::NSW);
             mbar_init(IFULL + 8 * b, 1);
             mbar_init(IFREE + 8 * b, C::NSW + 1);
         }
-        mbar_init(PREADY, C::NSW);
         mbar_init(PVDONE, 1);
         mbar_init(QREADY, C::NSW);
         mbar_init(DRAIN, 1);
@@ -460,17 +464,19 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         if (lane == 0) {
             uint32_t tile_g = 0, pv_n = 0;
             bool ok = true;
-            // O += P V for tile t of the item (global tile g)
+            // O += P V for tile t of the item (global tile g == pv_n)
             auto issue_pv = [&](uint32_t t, uint32_t g) {
-                if (!mbar_wait(PREADY, pv_n & 1)) {
+                const uint32_t pb = g & 1;
+                if (!mbar_wait(PREADY + 8 * pb, (g >> 1) & 1)) {
                     timeout();
                     return false;
                 }
                 tc::fence_after_sync();
                 const uint32_t st = g % S;
+                const uint32_t pcol0 = C::C_S + pb * C::C_BUF;
 #pragma unroll
                 for (int term = 0; term < 3; ++term) {
-                    const uint32_t pcol = term == 2 ? C::C_PLO : C::C_PHI;
+                    const uint32_t pcol = term == 2 ? pcol0 + BK : pcol0;
                     const uint32_t vb = term == 1 ? v_lo(st) : v_hi(st);
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
@@ -501,8 +507,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 tc::fence_after_sync();
                 for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
                     const uint32_t st = tile_g % S, sb = tile_g & 1;
-                    if (!mbar_wait(CONV + 8 * st, (tile_g / S) & 1) ||
-                        (tile_g >= 2 && !mbar_wait(SFREE + 8 * sb, ((tile_g >> 1) - 1) & 1))) {
+                    if (!mbar_wait(CONV + 8 * st, (tile_g / S) & 1)) {
                         timeout();
                         ok = false;
                         break;
@@ -521,8 +526,8 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                         for (int kk = 0; kk < HD / 8; ++kk) {
                             const uint64_t b = tc::smem_desc(kb + (kk / 4) * C::BLK + (kk % 4) * 32, 16,
                                                              1024, tc::kSwizzle128B);
-                            tc::mma_tf32_ts(tbase + C::C_S + sb * BK, tbase + qcol + kk * 8, b,
-                                            C::IDESC_QK, (term | kk) != 0 ? 1u : 0u);
+                            tc::mma_tf32_ts(tbase + C::C_S + sb * C::C_BUF, tbase + qcol + kk * 8,
+                                            b, C::IDESC_QK, (term | kk) != 0 ? 1u : 0u);
                         }
                     }
                     tc::mma_commit(SFULL + 8 * sb);
@@ -542,7 +547,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         const uint32_t r = static_cast<uint32_t>(tid);  // query row = TMEM lane
         const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
         const uint32_t t_local = r / G, h_local = r % G;
-        uint32_t tile_g = 0, pv_w = 0;
+        uint32_t tile_g = 0;
         for (uint32_t k = 0;; ++k) {
             const uint32_t is = k & 1;
             if (!mbar_wait(IFULL + 8 * is, (k >> 1) & 1)) {
@@ -596,14 +601,11 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
 #pragma unroll
                 for (int c0 = 0; c0 < BK; c0 += 32) {
                     uint32_t v[32];
-                    tc::tmem_ld32(lrow + C::C_S + sb * BK + c0, v);
+                    tc::tmem_ld32(lrow + C::C_S + sb * C::C_BUF + c0, v);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(v[c]);
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(SFREE + 8 * sb);
                 // causal mask: key kbase + c is attended iff it is <= pos
                 const uint32_t kbase = t * BK;
                 float mx = -CUDART_INF_F;
@@ -626,17 +628,17 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     s[c] = s[c] == -CUDART_INF_F ? 0.f : exp2f(s[c] - m);
                     l += s[c];
                 }
-                // P and O are free once the previous tile's O += P V has completed
-                if (t > 0) {
-                    if (!mbar_wait(PVDONE, pv_w & 1)) {
+                // O may be rescaled only once the previous tile's O += P V
+                // (global tile tile_g - 1) has completed.  Phases of pv_done
+                // may pass unobserved, but never two ahead of this wait:
+                // the next PV needs this tile's P.
+                if (__any_sync(0xffffffffu, rescale)) {
+                    if (!mbar_wait(PVDONE, (tile_g - 1) & 1)) {
                         timeout();
                         failed = true;
                         break;
                     }
-                    ++pv_w;
                     tc::fence_after_sync();
-                }
-                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                     for (int c0 = 0; c0 < HD; c0 += 32) {
                         uint32_t v[32];
@@ -653,21 +655,21 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     uint32_t hi[32], lo[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) tf32_split(s[c0 + c], hi[c], lo[c]);
-                    tc::tmem_st32(lrow + C::C_PHI + c0, hi);
-                    tc::tmem_st32(lrow + C::C_PLO + c0, lo);
+                    tc::tmem_st32(lrow + C::C_S + sb * C::C_BUF + c0, hi);
+                    tc::tmem_st32(lrow + C::C_S + sb * C::C_BUF + BK + c0, lo);
                 }
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(PREADY);
+                if (lane == 0) mbar_arrive(PREADY + 8 * sb);
             }
             if (failed || misc[0]) break;
-            // the item's last O += P V, then out = O / l (sink included)
-            if (!mbar_wait(PVDONE, pv_w & 1)) {
+            // the item's last O += P V (global tile tile_g - 1), then
+            // out = O / l (sink included)
+            if (!mbar_wait(PVDONE, (tile_g - 1) & 1)) {
                 timeout();
                 break;
             }
-            ++pv_w;
             tc::fence_after_sync();
             float f = 1.f / l;
             if (P.sinks) {
