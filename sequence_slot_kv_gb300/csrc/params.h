@@ -128,6 +128,6 @@ int launch_prefill_tc_hd128(int G, const PrefillParams& p, const CUtensorMap& tm
                             const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
 
 // Keys per pipeline stage of the tensor-core prefill.
-__host__ __device__ constexpr int prefill_tile_keys(int hd) { return hd == 64 ? 64 : 32; }
+__host__ __device__ constexpr int prefill_tile_keys(int) { return 64; }
 
 }  // namespace slotkv

@@ -20,27 +20,29 @@
 //     cleared (exact in TF32) and a_lo = a - a_hi (exact in f32), and
 //     a.b ~ a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the dropped a_lo.b_lo and the
 //     TF32 rounding of the lo parts are ~2^-20 relative).
-//       - warp 4 (producer): claims items, streams the key tiles' K and V
-//         (BK keys x hd, 128-byte swizzled boxes of 32 floats) into a
-//         3-stage ring with TMA;
+//       - warp 4 (producer): claims items and streams each key tile's K
+//         and then V (BK = 64 keys x hd, 128-byte swizzled boxes of 32
+//         floats) with TMA into a ring of half-stage slots (one operand's
+//         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
 //       - warps 6-7 (converters): split each landed K tile in place into
 //         hi and lo operand buffers, and transpose each landed V tile into
 //         a keys-contiguous layout while splitting it (TF32 MMA operands
 //         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
 //         keys past the item's last are zeroed;
-//       - warp 5 (MMA issuer, one thread): S = Q K^T into one of two TMEM
-//         score buffers (A = Q from TMEM), then O += P V (A = P from TMEM,
-//         B = the transposed V tile).  Issue order QK(t+1), PV(t), QK(t+2),
-//         PV(t+1), ...; MMAs from one thread run in issue order, so QK(t+2)
-//         reuses buffer t % 2 only after PV(t) has read it;
+//       - warp 5 (MMA issuer, one thread): S = Q K^T into a TMEM score
+//         buffer (A = Q from TMEM), then O += P V (A = P from TMEM, B = the
+//         transposed V tile).  With two score buffers (hd 64) the issue order
+//         is QK(t+1), PV(t), QK(t+2), ...; with one (hd 128, where Q's hi and
+//         lo parts take half of tensor memory) QK(t), PV(t), QK(t+1), ....
+//         MMAs from one thread run in issue order, so a QK reuses a buffer
+//         only after the PV before it has read it;
 //       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
 //         the item's q rows (hi, lo) into TMEM, then per key tile read S,
 //         apply the causal mask (key <= the row's position), run a base-2
 //         online softmax with a lazily raised max, write P (hi over S, lo
-//         beside it) into the same buffer -- while the previous tile's
-//         O += P V runs -- and, only when the max moves, wait for that PV
-//         and rescale O in TMEM; at the end read O, normalise (sink
-//         included) and store out.
+//         beside it) into the same buffer and, only when the max moves,
+//         wait for the previous PV and rescale O in TMEM; at the end read O,
+//         normalise (sink included) and store out.
 // Every mbarrier wait is bounded; on expiry the CTA raises SLOTKV_DEV_TIMEOUT
 // and every role leaves its loop; the MMA thread waits for its MMAs and the
 // producer for its copies before tensor memory is freed.
@@ -56,12 +58,12 @@ struct PCfg {
     static constexpr int M = 128;               // query rows per tile (MMA M)
     static constexpr int MT = M / G;            // tokens per tile
     static constexpr int ROWS = MT * G;         // rows in use (<= 128)
-    static constexpr int BK = prefill_tile_keys(HD);  // keys per stage
-    static constexpr int NB = HD / 32;          // 128-byte column blocks per row
-    static constexpr int S = 3;                 // pipeline stages
+    static constexpr int BK = prefill_tile_keys(HD);  // keys per tile (QK's N)
+    static constexpr int NB = HD / 32;          // 128-byte column blocks per key row
     static constexpr int BLK = BK * 128;        // one column block: BK rows x 128 B
     static constexpr int BUF = NB * BLK;        // one operand buffer, [BK][HD] f32
-    static constexpr int STAGE = 4 * BUF;       // K hi | K lo | V hi | V lo
+    static constexpr int SLOT = 2 * BUF;        // half-stage slot: hi | lo of K or V
+    static constexpr int NSLOT = (192 * 1024) / SLOT;  // 3 (hd 128) or 6 (hd 64)
     // V transposed: KB column blocks of 32 keys, each [HD rows][128 B]; the
     // 32 x 32 sub-block (key block kb, dim block db) lands at kb * VT_BLK +
     // db * 4096 (TMA put it at db * BLK + kb * 4096)
@@ -69,31 +71,33 @@ struct PCfg {
     static constexpr int VT_BLK = HD * 128;
     static constexpr int NSW = 4;               // softmax warps
     static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
+    static constexpr int SB_PER_WARP = KB * NB / NCONV;  // V sub-blocks per converter warp
     static constexpr int THREADS = 256;
-    // tensor memory columns: Q hi | Q lo | O | two buffers of (S, then P hi
+    // tensor memory columns: Q hi | Q lo | O | NBUF buffers of (S, then P hi
     // over it | P lo)
     static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_O = 2 * HD, C_S = 3 * HD;
     static constexpr uint32_t C_BUF = 2 * BK;   // columns per score buffer
+    static constexpr int NBUF = (512 - 3 * HD) / (2 * BK) >= 2 ? 2 : 1;
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(3 * HD + 4 * BK <= 512, "tensor memory columns");
+    static_assert(3 * HD + NBUF * 2 * BK <= 512, "tensor memory columns");
     static_assert(BK % 32 == 0 && HD % 32 == 0, "32-column tensor memory accesses");
-    // shared memory after the ring: item descriptors [2][8] | stage meta [S][4]
-    // | barriers | tensor memory address | abort flag
-    static constexpr int OFF_DESC = S * STAGE;
+    // shared memory after the ring: item descriptors [2][8] | slot meta
+    // [NSLOT][4] | barriers | tensor memory address | flags
+    static constexpr int OFF_DESC = NSLOT * SLOT;
     static constexpr int OFF_META = OFF_DESC + 2 * 32;
-    static constexpr int OFF_BAR = OFF_META + S * 16;
-    // full[S], conv[S], empty[S], s_full[2], p_ready[2], pv_done, q_ready,
-    // item_full[2], item_free[2], drain, (one spare)
-    static constexpr int NBAR = 3 * S + 12;
+    static constexpr int OFF_BAR = OFF_META + NSLOT * 16;
+    // full[NSLOT], conv[NSLOT], empty[NSLOT], s_full[2], p_ready[2],
+    // pv_done, q_ready, item_full[2], item_free[2], drain, (one spare)
+    static constexpr int NBAR = 3 * NSLOT + 12;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM = SMEM_USED + 1024;   // slack to align the ring to 1 KiB
     static_assert(SMEM <= 227 * 1024, "shared memory");
-    static_assert(BLK % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
+    static_assert(BLK % 1024 == 0 && SLOT % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
     static constexpr uint32_t IDESC_QK = tc::idesc_tf32(M, BK, false);
     static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, false);
-    static_assert(KB * NB <= 2 * NCONV, "two V sub-blocks per converter warp");
+    static_assert(KB * NB == SB_PER_WARP * NCONV, "V sub-blocks split evenly over the converters");
     static_assert(NCONV == 2, "the converters' stop flags are misc[2], misc[3]");
 };
 
@@ -245,12 +249,14 @@ __global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const Pref
 }
 
 // ------------------------------------------------------------------ attention
+// Half-tile h of the CTA's stream of key tiles: h = 2g is tile g's K, h = 2g + 1
+// its V; it lives in slot h % NSLOT.
 template <int HD, int G>
 __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     slotkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const PrefillParams P) {
     using C = PCfg<HD, G>;
-    constexpr int S = C::S, BK = C::BK, NB = C::NB;
+    constexpr int BK = C::BK, NB = C::NB, NSLOT = C::NSLOT, NBUF = C::NBUF;
     constexpr float kLog2e = 1.4426950408889634f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -261,21 +267,19 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
     const uint32_t ring = smem_addr(smem);
     const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
-    const uint32_t FULL = bar0, CONV = bar0 + 8 * S, EMPTY = bar0 + 16 * S;
-    const uint32_t SFULL = bar0 + 24 * S, PREADY = SFULL + 16;
+    const uint32_t FULL = bar0, CONV = bar0 + 8 * NSLOT, EMPTY = bar0 + 16 * NSLOT;
+    const uint32_t SFULL = bar0 + 24 * NSLOT, PREADY = SFULL + 16;
     const uint32_t PVDONE = PREADY + 16, QREADY = PVDONE + 8, IFULL = QREADY + 8;
     const uint32_t IFREE = IFULL + 16, DRAIN = IFREE + 16;
-    // operand buffers of a stage
-    auto k_hi = [&](uint32_t st) { return ring + st * C::STAGE; };
-    auto k_lo = [&](uint32_t st) { return ring + st * C::STAGE + C::BUF; };
-    auto v_hi = [&](uint32_t st) { return ring + st * C::STAGE + 2 * C::BUF; };
-    auto v_lo = [&](uint32_t st) { return ring + st * C::STAGE + 3 * C::BUF; };
+    // hi and lo operand buffers of a slot
+    auto slot_hi = [&](uint32_t sl) { return ring + sl * C::SLOT; };
+    auto slot_lo = [&](uint32_t sl) { return ring + sl * C::SLOT + C::BUF; };
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(FULL + 8 * s, 1);
-            mbar_init(CONV + 8 * s, C::NCONV);
-            mbar_init(EMPTY + 8 * s, 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(FULL + 8 * i, 1);
+            mbar_init(CONV + 8 * i, C::NCONV);
+            mbar_init(EMPTY + 8 * i, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(SFULL + 8 * b, 1);
@@ -308,7 +312,12 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         if (lane == 0) {
             const uint32_t n_items = __ldcg(P.plan);
             const uint4* tiles = reinterpret_cast<const uint4*>(P.tiles);
-            uint32_t tile_g = 0;
+            uint32_t h = 0;  // half-tiles issued
+            // wait until slot h % NSLOT is free again
+            auto slot_free = [&](uint32_t hh) {
+                return hh < static_cast<uint32_t>(NSLOT) ||
+                       mbar_wait(EMPTY + 8 * (hh % NSLOT), ((hh / NSLOT) - 1) & 1);
+            };
             for (uint32_t k = 0;; ++k) {
                 const uint32_t is = k & 1;
                 if (k >= 2 && !mbar_wait(IFREE + 8 * is, ((k >> 1) - 1) & 1)) {
@@ -321,15 +330,13 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 if (it >= n_items) {
                     d[6] = 1;
                     mbar_arrive(IFULL + 8 * is);
-                    // tell the converters: an end marker in the next stage
-                    const uint32_t st = tile_g % S;
-                    if (tile_g >= static_cast<uint32_t>(S) &&
-                        !mbar_wait(EMPTY + 8 * st, ((tile_g / S) - 1) & 1)) {
+                    // tell the converters: an end marker in the next slot
+                    if (!slot_free(h)) {
                         timeout();
                         break;
                     }
-                    meta[4 * st + 1] = 1;
-                    mbar_arrive(FULL + 8 * st);
+                    meta[4 * (h % NSLOT) + 1] = 1;
+                    mbar_arrive(FULL + 8 * (h % NSLOT));
                     break;
                 }
                 const uint4 rec = __ldcg(tiles + it / P.n_kv_head);
@@ -345,55 +352,55 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 d[6] = 0;
                 mbar_arrive(IFULL + 8 * is);
                 const int y0 = static_cast<int>(rec.z * P.slot_ctx);
-                for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
-                    const uint32_t st = tile_g % S;
-                    if (tile_g >= static_cast<uint32_t>(S) &&
-                        !mbar_wait(EMPTY + 8 * st, ((tile_g / S) - 1) & 1)) {
-                        timeout();
-                        break;
-                    }
-                    if (misc[0]) break;
+                for (uint32_t t = 0; t < ntiles && !misc[0]; ++t) {
                     const uint32_t left = max_pos + 1 - t * BK;
-                    meta[4 * st + 0] = left < static_cast<uint32_t>(BK) ? left : BK;
-                    meta[4 * st + 1] = 0;
-                    mbar_expect_tx(FULL + 8 * st, 2 * C::BUF);
                     const int y = y0 + static_cast<int>(t * BK);
+                    for (int which = 0; which < 2; ++which, ++h) {  // K, then V
+                        if (!slot_free(h)) {
+                            timeout();
+                            break;
+                        }
+                        const uint32_t sl = h % NSLOT;
+                        meta[4 * sl + 0] = left < static_cast<uint32_t>(BK) ? left : BK;
+                        meta[4 * sl + 1] = 0;
+                        mbar_expect_tx(FULL + 8 * sl, C::BUF);
 #pragma unroll
-                    for (int c = 0; c < NB; ++c) {
-                        const int x = static_cast<int>(kvh * HD) + 32 * c;
-                        tma_load_2d(k_hi(st) + c * C::BLK, &tmK, x, y, FULL + 8 * st);
-                        tma_load_2d(v_hi(st) + c * C::BLK, &tmV, x, y, FULL + 8 * st);
+                        for (int c = 0; c < NB; ++c)
+                            tma_load_2d(slot_hi(sl) + c * C::BLK, which ? &tmV : &tmK,
+                                        static_cast<int>(kvh * HD) + 32 * c, y, FULL + 8 * sl);
                     }
                 }
                 if (misc[0]) break;
             }
             if (misc[0]) {
                 // drain this CTA's copies that may still be in flight
-                for (uint32_t u = tile_g > static_cast<uint32_t>(S) ? tile_g - S : 0; u < tile_g; ++u)
-                    mbar_wait(FULL + 8 * (u % S), (u / S) & 1, 1ll << 28);
+                for (uint32_t u = h > static_cast<uint32_t>(NSLOT) ? h - NSLOT : 0; u < h; ++u)
+                    mbar_wait(FULL + 8 * (u % NSLOT), (u / NSLOT) & 1, 1ll << 28);
             }
         }
     } else if (warp >= C::WARP_CONV) {
         // ------------------------------------------------------------ converters
         const int ct = tid - C::WARP_CONV * 32;
+        const int w = ct >> 5;
         constexpr int NT = C::NCONV * 32;
-        for (uint32_t tile_g = 0;; ++tile_g) {
-            const uint32_t st = tile_g % S;
+        for (uint32_t h = 0;; ++h) {
+            const uint32_t sl = h % NSLOT;
             // Both converter warps meet at named barriers below, so they must
-            // stop at the same tile: each publishes its own reason to stop
-            // (a wait that expired, an abort, the end marker) and both
+            // stop at the same half-tile: each publishes its own reason to
+            // stop (a wait that expired, an abort, the end marker) and both
             // decide from the two published flags.
-            const bool ok = mbar_wait(FULL + 8 * st, (tile_g / S) & 1);
+            const bool ok = mbar_wait(FULL + 8 * sl, (h / NSLOT) & 1);
             if (!ok) timeout();
-            if (lane == 0) misc[2 + (ct >> 5)] = (!ok || misc[0] || meta[4 * st + 1]) ? 1 : 0;
-            named_sync_conv<C::NCONV * 32>();
+            if (lane == 0) misc[2 + w] = (!ok || misc[0] || meta[4 * sl + 1]) ? 1 : 0;
+            named_sync_conv<NT>();
             if (misc[2] | misc[3]) break;
-            const uint32_t rows = meta[4 * st + 0];
-            uint8_t* stage = smem + st * C::STAGE;
-            // K: hi in place, lo beside it (both K-major, as TMA laid them)
-            {
-                float4* hi = reinterpret_cast<float4*>(stage);
-                float4* lo = reinterpret_cast<float4*>(stage + C::BUF);
+            const uint32_t rows = meta[4 * sl + 0];
+            uint8_t* hib = smem + sl * C::SLOT;
+            uint8_t* lob = hib + C::BUF;
+            if ((h & 1) == 0) {
+                // K: hi in place, lo beside it (both K-major, as TMA laid them)
+                float4* hi = reinterpret_cast<float4*>(hib);
+                float4* lo = reinterpret_cast<float4*>(lob);
 #pragma unroll 4
                 for (int i = ct; i < C::BUF / 16; i += NT) {
                     // each 128-byte row of a column block is 8 float4s
@@ -410,74 +417,70 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
                                         __uint_as_float(l2), __uint_as_float(l3));
                 }
-            }
-            // V: every 32 x 32 sub-block transposed (keys along the 128-byte
-            // rows), hi into the V buffer, lo into the V lo buffer.  Each warp
-            // reads its sub-blocks (lane = dim, one key per load) before any
-            // converter thread writes, so the in-place permutation is safe.
-            {
-                uint8_t* vh = stage + 2 * C::BUF;
-                uint8_t* vl = stage + 3 * C::BUF;
-                const int w = ct >> 5;
-                float x[2][32];
+            } else {
+                // V: every 32 x 32 sub-block transposed (keys along the
+                // 128-byte rows), hi in place, lo into the lo buffer.  All
+                // converter threads read their sub-blocks (lane = dim, one
+                // key per load) before any writes, so the in-place
+                // permutation is safe whatever its cycles.
+                float x[C::SB_PER_WARP][32];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < C::SB_PER_WARP; ++j) {
                     const int sb = w + C::NCONV * j;
-                    if (sb < C::KB * NB) {
-                        const int kb = sb / NB, db = sb % NB;
-                        const uint8_t* src = vh + db * C::BLK + kb * 4096;
+                    const int kb = sb / NB, db = sb % NB;
+                    const uint8_t* src = hib + db * C::BLK + kb * 4096;
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 +
-                                                 (((lane / 4) ^ (k % 8)) * 16) + (lane % 4) * 4;
-                            const float v = *reinterpret_cast<const float*>(src + off);
-                            x[j][k] = static_cast<uint32_t>(kb * 32 + k) < rows ? v : 0.f;
-                        }
+                    for (int k = 0; k < 32; ++k) {
+                        const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 +
+                                             (((lane / 4) ^ (k % 8)) * 16) + (lane % 4) * 4;
+                        const float v = *reinterpret_cast<const float*>(src + off);
+                        x[j][k] = static_cast<uint32_t>(kb * 32 + k) < rows ? v : 0.f;
                     }
                 }
-                named_sync_conv<C::NCONV * 32>();
+                named_sync_conv<NT>();
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < C::SB_PER_WARP; ++j) {
                     const int sb = w + C::NCONV * j;
-                    if (sb < C::KB * NB) {
-                        const int kb = sb / NB, db = sb % NB;
-                        const uint32_t base = kb * C::VT_BLK + db * 4096 + (lane / 8) * 1024 +
-                                              (lane % 8) * 128;
+                    const int kb = sb / NB, db = sb % NB;
+                    const uint32_t base = kb * C::VT_BLK + db * 4096 + (lane / 8) * 1024 +
+                                          (lane % 8) * 128;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint32_t h[4], l[4];
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t hh[4], ll[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) tf32_split(x[j][4 * c + e], h[e], l[e]);
-                            const uint32_t off = base + ((c ^ (lane % 8)) * 16);
-                            *reinterpret_cast<uint4*>(vh + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                            *reinterpret_cast<uint4*>(vl + off) = make_uint4(l[0], l[1], l[2], l[3]);
-                        }
+                        for (int e = 0; e < 4; ++e) tf32_split(x[j][4 * c + e], hh[e], ll[e]);
+                        const uint32_t off = base + ((c ^ (lane % 8)) * 16);
+                        *reinterpret_cast<uint4*>(hib + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<uint4*>(lob + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
                     }
                 }
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(CONV + 8 * st);
+            if (lane == 0) mbar_arrive(CONV + 8 * sl);
         }
     } else if (warp == C::WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t tile_g = 0, pv_n = 0;
+            uint32_t g = 0;  // key tiles whose QK was issued
             bool ok = true;
-            // O += P V for tile t of the item (global tile g == pv_n)
-            auto issue_pv = [&](uint32_t t, uint32_t g) {
-                const uint32_t pb = g & 1;
-                if (!mbar_wait(PREADY + 8 * pb, (g >> 1) & 1)) {
+            auto converted = [&](uint32_t hh) {
+                return mbar_wait(CONV + 8 * (hh % NSLOT), (hh / NSLOT) & 1);
+            };
+            // O += P V for tile t of the item (global tile gp)
+            auto issue_pv = [&](uint32_t t, uint32_t gp) {
+                const uint32_t hv = 2 * gp + 1;
+                if (!converted(hv) || !mbar_wait(PREADY + 8 * (gp & 1), (gp >> 1) & 1)) {
                     timeout();
                     return false;
                 }
                 tc::fence_after_sync();
-                const uint32_t st = g % S;
-                const uint32_t pcol0 = C::C_S + pb * C::C_BUF;
+                const uint32_t sl = hv % NSLOT;
+                const uint32_t pcol0 = C::C_S + (gp % NBUF) * C::C_BUF;
 #pragma unroll
                 for (int term = 0; term < 3; ++term) {
                     const uint32_t pcol = term == 2 ? pcol0 + BK : pcol0;
-                    const uint32_t vb = term == 1 ? v_lo(st) : v_hi(st);
+                    const uint32_t vb = term == 1 ? slot_lo(sl) : slot_hi(sl);
 #pragma unroll
                     for (int kk = 0; kk < BK / 8; ++kk) {
                         const uint64_t b = tc::smem_desc(vb + (kk / 4) * C::VT_BLK + (kk % 4) * 32, 16,
@@ -487,8 +490,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     }
                 }
                 tc::mma_commit(PVDONE);
-                tc::mma_commit(EMPTY + 8 * st);
-                ++pv_n;
+                tc::mma_commit(EMPTY + 8 * sl);
                 return true;
             };
             for (uint32_t k = 0; ok; ++k) {
@@ -505,9 +507,9 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
-                    const uint32_t st = tile_g % S, sb = tile_g & 1;
-                    if (!mbar_wait(CONV + 8 * st, (tile_g / S) & 1)) {
+                for (uint32_t t = 0; t < ntiles; ++t, ++g) {
+                    const uint32_t hk = 2 * g;
+                    if (!converted(hk)) {
                         timeout();
                         ok = false;
                         break;
@@ -518,25 +520,34 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     }
                     tc::fence_after_sync();
                     // S = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
+                    const uint32_t sl = hk % NSLOT;
+                    const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF;
 #pragma unroll
                     for (int term = 0; term < 3; ++term) {
                         const uint32_t qcol = term == 2 ? C::C_QLO : C::C_QHI;
-                        const uint32_t kb = term == 1 ? k_lo(st) : k_hi(st);
+                        const uint32_t kb = term == 1 ? slot_lo(sl) : slot_hi(sl);
 #pragma unroll
                         for (int kk = 0; kk < HD / 8; ++kk) {
                             const uint64_t b = tc::smem_desc(kb + (kk / 4) * C::BLK + (kk % 4) * 32, 16,
                                                              1024, tc::kSwizzle128B);
-                            tc::mma_tf32_ts(tbase + C::C_S + sb * C::C_BUF, tbase + qcol + kk * 8,
-                                            b, C::IDESC_QK, (term | kk) != 0 ? 1u : 0u);
+                            tc::mma_tf32_ts(tbase + scol, tbase + qcol + kk * 8, b, C::IDESC_QK,
+                                            (term | kk) != 0 ? 1u : 0u);
                         }
                     }
-                    tc::mma_commit(SFULL + 8 * sb);
-                    if (t >= 1 && !issue_pv(t - 1, tile_g - 1)) {
+                    tc::mma_commit(SFULL + 8 * (g & 1));
+                    tc::mma_commit(EMPTY + 8 * sl);  // K slot free once QK has read it
+                    // one buffer: this tile's PV next; two: the previous tile's
+                    if (NBUF == 1) {
+                        if (!issue_pv(t, g)) {
+                            ok = false;
+                            break;
+                        }
+                    } else if (t >= 1 && !issue_pv(t - 1, g - 1)) {
                         ok = false;
                         break;
                     }
                 }
-                if (ok && ntiles && !misc[0] && !issue_pv(ntiles - 1, tile_g - 1)) ok = false;
+                if (NBUF == 2 && ok && ntiles && !misc[0] && !issue_pv(ntiles - 1, g - 1)) ok = false;
             }
             // every MMA issued above has completed before tensor memory is freed
             tc::mma_commit(DRAIN);
@@ -547,7 +558,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         const uint32_t r = static_cast<uint32_t>(tid);  // query row = TMEM lane
         const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
         const uint32_t t_local = r / G, h_local = r % G;
-        uint32_t tile_g = 0;
+        uint32_t g = 0;  // key tiles processed
         for (uint32_t k = 0;; ++k) {
             const uint32_t is = k & 1;
             if (!mbar_wait(IFULL + 8 * is, (k >> 1) & 1)) {
@@ -589,19 +600,19 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             if (lane == 0) mbar_arrive(QREADY);
             float m = -CUDART_INF_F, l = 0.f;
             bool failed = false;
-            for (uint32_t t = 0; t < ntiles; ++t, ++tile_g) {
-                const uint32_t sb = tile_g & 1;
-                if (!mbar_wait(SFULL + 8 * sb, (tile_g >> 1) & 1)) {
+            for (uint32_t t = 0; t < ntiles; ++t, ++g) {
+                if (!mbar_wait(SFULL + 8 * (g & 1), (g >> 1) & 1)) {
                     timeout();
                     failed = true;
                     break;
                 }
                 tc::fence_after_sync();
+                const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF;
                 float s[BK];
 #pragma unroll
                 for (int c0 = 0; c0 < BK; c0 += 32) {
                     uint32_t v[32];
-                    tc::tmem_ld32(lrow + C::C_S + sb * C::C_BUF + c0, v);
+                    tc::tmem_ld32(lrow + scol + c0, v);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(v[c]);
@@ -609,10 +620,15 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 // causal mask: key kbase + c is attended iff it is <= pos
                 const uint32_t kbase = t * BK;
                 float mx = -CUDART_INF_F;
+                if (kbase + BK - 1 <= pos) {
 #pragma unroll
-                for (int c = 0; c < BK; ++c) {
-                    s[c] = kbase + static_cast<uint32_t>(c) <= pos ? s[c] : -CUDART_INF_F;
-                    mx = fmaxf(mx, s[c]);
+                    for (int c = 0; c < BK; ++c) mx = fmaxf(mx, s[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BK; ++c) {
+                        s[c] = kbase + static_cast<uint32_t>(c) <= pos ? s[c] : -CUDART_INF_F;
+                        mx = fmaxf(mx, s[c]);
+                    }
                 }
                 // lazy running max: raised only when a score passes it by 2^8
                 float corr = 1.f;
@@ -629,11 +645,11 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     l += s[c];
                 }
                 // O may be rescaled only once the previous tile's O += P V
-                // (global tile tile_g - 1) has completed.  Phases of pv_done
-                // may pass unobserved, but never two ahead of this wait:
-                // the next PV needs this tile's P.
+                // (global tile g - 1) has completed.  Phases of pv_done may
+                // pass unobserved, but never two ahead of this wait: the
+                // next PV needs this tile's P.
                 if (__any_sync(0xffffffffu, rescale)) {
-                    if (!mbar_wait(PVDONE, (tile_g - 1) & 1)) {
+                    if (!mbar_wait(PVDONE, (g - 1) & 1)) {
                         timeout();
                         failed = true;
                         break;
@@ -655,18 +671,18 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     uint32_t hi[32], lo[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) tf32_split(s[c0 + c], hi[c], lo[c]);
-                    tc::tmem_st32(lrow + C::C_S + sb * C::C_BUF + c0, hi);
-                    tc::tmem_st32(lrow + C::C_S + sb * C::C_BUF + BK + c0, lo);
+                    tc::tmem_st32(lrow + scol + c0, hi);
+                    tc::tmem_st32(lrow + scol + BK + c0, lo);
                 }
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(PREADY + 8 * sb);
+                if (lane == 0) mbar_arrive(PREADY + 8 * (g & 1));
             }
             if (failed || misc[0]) break;
-            // the item's last O += P V (global tile tile_g - 1), then
-            // out = O / l (sink included)
-            if (!mbar_wait(PVDONE, (tile_g - 1) & 1)) {
+            // the item's last O += P V (global tile g - 1), then out = O / l
+            // (sink included)
+            if (!mbar_wait(PVDONE, (g - 1) & 1)) {
                 timeout();
                 break;
             }
