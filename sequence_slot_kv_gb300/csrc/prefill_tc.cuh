@@ -87,7 +87,7 @@ struct PCfg {
     static constexpr int OFF_META = OFF_DESC + 2 * 32;
     static constexpr int OFF_BAR = OFF_META + NSLOT * 16;
     // full[NSLOT], conv[NSLOT], empty[NSLOT], s_full[2], p_ready[2],
-    // pv_done, q_ready, item_full[2], item_free[2], drain, (one spare)
+    // pv_done[2], q_ready, item_full[2], item_free[2], drain
     static constexpr int NBAR = 3 * NSLOT + 12;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
@@ -105,6 +105,15 @@ struct PCfg {
 template <int N>
 __device__ __forceinline__ void named_sync_conv() {
     asm volatile("bar.sync 2, %0;" ::"n"(N) : "memory");
+}
+
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz:
+// a few ulp of relative error, subnormal results flushed to zero), far
+// inside the f32 tolerance of the step.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Split x into an exactly-TF32 high part and the f32 remainder.
@@ -269,7 +278,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
     const uint32_t FULL = bar0, CONV = bar0 + 8 * NSLOT, EMPTY = bar0 + 16 * NSLOT;
     const uint32_t SFULL = bar0 + 24 * NSLOT, PREADY = SFULL + 16;
-    const uint32_t PVDONE = PREADY + 16, QREADY = PVDONE + 8, IFULL = QREADY + 8;
+    const uint32_t PVDONE = PREADY + 16, QREADY = PVDONE + 16, IFULL = QREADY + 8;
     const uint32_t IFREE = IFULL + 16, DRAIN = IFREE + 16;
     // hi and lo operand buffers of a slot
     auto slot_hi = [&](uint32_t sl) { return ring + sl * C::SLOT; };
@@ -284,10 +293,10 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(SFULL + 8 * b, 1);
             mbar_init(PREADY + 8 * b, C::NSW);
+            mbar_init(PVDONE + 8 * b, 1);
             mbar_init(IFULL + 8 * b, 1);
             mbar_init(IFREE + 8 * b, C::NSW + 1);
         }
-        mbar_init(PVDONE, 1);
         mbar_init(QREADY, C::NSW);
         mbar_init(DRAIN, 1);
         misc[0] = 0;
@@ -401,7 +410,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 // K: hi in place, lo beside it (both K-major, as TMA laid them)
                 float4* hi = reinterpret_cast<float4*>(hib);
                 float4* lo = reinterpret_cast<float4*>(lob);
-#pragma unroll 4
+#pragma unroll
                 for (int i = ct; i < C::BUF / 16; i += NT) {
                     // each 128-byte row of a column block is 8 float4s
                     const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                                         (t | term | kk) != 0 ? 1u : 0u);
                     }
                 }
-                tc::mma_commit(PVDONE);
+                tc::mma_commit(PVDONE + 8 * (gp & 1));
                 tc::mma_commit(EMPTY + 8 * sl);
                 return true;
             };
@@ -634,22 +643,27 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 float corr = 1.f;
                 bool rescale = false;
                 if (mx > m + 8.f) {
-                    corr = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
+                    corr = m == -CUDART_INF_F ? 0.f : fast_exp2(m - mx);
                     rescale = t > 0;
                     l *= corr;
                     m = mx;
                 }
 #pragma unroll
                 for (int c = 0; c < BK; ++c) {
-                    s[c] = s[c] == -CUDART_INF_F ? 0.f : exp2f(s[c] - m);
+                    s[c] = s[c] == -CUDART_INF_F ? 0.f : fast_exp2(s[c] - m);
                     l += s[c];
                 }
                 // O may be rescaled only once the previous tile's O += P V
-                // (global tile g - 1) has completed.  Phases of pv_done may
-                // pass unobserved, but never two ahead of this wait: the
-                // next PV needs this tile's P.
+                // (global tile g - 1) has completed.  PV(j) completes a phase
+                // of pv_done[j % 2]; at any wait for PV(j), PV(j - 2) has
+                // completed (the S this softmax already read was committed
+                // after it) and PV(j + 2) cannot start (it needs P from this
+                // softmax), so the parity of phase j / 2 is unambiguous.
+                // (One barrier for all PVs would not do: with two score
+                // buffers PV(j - 1) may still be running at the wait for
+                // PV(j), and its parity would read as already complete.)
                 if (__any_sync(0xffffffffu, rescale)) {
-                    if (!mbar_wait(PVDONE, (g - 1) & 1)) {
+                    if (!mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
                         timeout();
                         failed = true;
                         break;
@@ -680,9 +694,9 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 if (lane == 0) mbar_arrive(PREADY + 8 * (g & 1));
             }
             if (failed || misc[0]) break;
-            // the item's last O += P V (global tile g - 1), then out = O / l
-            // (sink included)
-            if (!mbar_wait(PVDONE, (g - 1) & 1)) {
+            // the item's last O += P V (global tile g - 1; its commit covers
+            // every earlier MMA), then out = O / l (sink included)
+            if (!mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
                 timeout();
                 break;
             }
