@@ -25,10 +25,7 @@
 //         floats) with TMA into a ring of half-stage slots (one operand's
 //         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
 //       - warps 6-7 (converters): split each landed K tile in place into
-//         hi and lo operand buffers, and transpose each landed V tile into
-//         a keys-contiguous layout while splitting it (TF32 MMA operands
-//         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
-//         keys past the item's last are zeroed;
+//         hi and lo operand buffers (keys past the item's last zeroed);
 //       - warp 5 (MMA issuer, one thread): S = Q K^T into a TMEM score
 //         buffer (A = Q from TMEM), then O += P V (A = P from TMEM, B = the
 //         transposed V tile).  With two score buffers (hd 64) the issue order
@@ -37,7 +34,13 @@
 //         MMAs from one thread run in issue order, so a QK reuses a buffer
 //         only after the PV before it has read it;
 //       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
-//         the item's q rows (hi, lo) into TMEM, then per key tile read S,
+//         the item's q rows (hi, lo) into TMEM; per key tile, while its QK
+//         runs, transpose the landed V tile in place into a keys-contiguous
+//         layout and split it (TF32 MMA operands in shared memory are
+//         K-major: for O += P V that is V^T, [hd][keys]; keys past the
+//         item's last zeroed) -- each warp takes whole cycles of the
+//         32 x 32 sub-block permutation, so no other warp touches its
+//         sub-blocks -- then read S,
 //         apply the causal mask (key <= the row's position), run a base-2
 //         online softmax with a lazily raised max, write P (hi over S, lo
 //         beside it) into the same buffer and, only when the max moves,
@@ -71,7 +74,6 @@ struct PCfg {
     static constexpr int VT_BLK = HD * 128;
     static constexpr int NSW = 4;               // softmax warps
     static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
-    static constexpr int SB_PER_WARP = KB * NB / NCONV;  // V sub-blocks per converter warp
     static constexpr int THREADS = 256;
     // tensor memory columns: Q hi | Q lo | O | NBUF buffers of (S, then P hi
     // over it | P lo)
@@ -97,15 +99,8 @@ struct PCfg {
     static_assert(BLK % 1024 == 0 && SLOT % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
     static constexpr uint32_t IDESC_QK = tc::idesc_tf32(M, BK, false);
     static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, false);
-    static_assert(KB * NB == SB_PER_WARP * NCONV, "V sub-blocks split evenly over the converters");
-    static_assert(NCONV == 2, "the converters' stop flags are misc[2], misc[3]");
-};
 
-// Named barrier 2 over the converter warps (N threads).
-template <int N>
-__device__ __forceinline__ void named_sync_conv() {
-    asm volatile("bar.sync 2, %0;" ::"n"(N) : "memory");
-}
+};
 
 // 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz:
 // a few ulp of relative error, subnormal results flushed to zero), far
@@ -121,6 +116,100 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) 
     const uint32_t h = __float_as_uint(x) & 0xFFFFE000u;
     hi = h;
     lo = __float_as_uint(x - __uint_as_float(h));
+}
+
+// ------------------------------------------------------------------ V transpose
+// The V tile of a stage lands as NB column blocks of BK rows x 128 bytes
+// (128-byte swizzled TMA boxes): the 32 x 32 sub-block (key block kb, dim
+// block db) sits at source location L = db * KB + kb (4 KiB each).  The PV
+// MMA reads it transposed (keys contiguous), at location kb * NB + db, the
+// layout of a K-major [HD][BK] operand.  The transpose is done in place, a
+// sub-block at a time, by whole cycles of that permutation, each cycle by one
+// warp: read the first sub-block, then for each next one read it and write
+// the previous one into its place, and finally write the last into the
+// first's place (two sub-blocks in registers at most).  Keys past `rows` are
+// zeroed; hi goes in place and lo to the same offset of the lo buffer.
+
+// this lane's 32 keys of a sub-block at location L (lane = dim)
+template <int KB>
+__device__ __forceinline__ void v_read(const uint8_t* hib, int L, uint32_t rows, int lane,
+                                       float (&x)[32]) {
+    const uint8_t* src = hib + L * 4096;
+    const uint32_t kb = static_cast<uint32_t>(L % KB);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 + (((lane / 4) ^ (k % 8)) * 16) +
+                             (lane % 4) * 4;
+        const float v = *reinterpret_cast<const float*>(src + off);
+        x[k] = kb * 32 + static_cast<uint32_t>(k) < rows ? v : 0.f;
+    }
+}
+
+// write sub-block data x (read from location L) transposed into its target
+template <int KB, int NB>
+__device__ __forceinline__ void v_write(uint8_t* hib, uint8_t* lob, int L, int lane,
+                                        const float (&x)[32]) {
+    const int kb = L % KB, db = L / KB;
+    const uint32_t base = (kb * NB + db) * 4096 + (lane / 8) * 1024 + (lane % 8) * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t hh[4], ll[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tf32_split(x[4 * c + e], hh[e], ll[e]);
+        const uint32_t off = base + ((c ^ (lane % 8)) * 16);
+        *reinterpret_cast<uint4*>(hib + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        *reinterpret_cast<uint4*>(lob + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+    }
+}
+
+// one permutation cycle A -> B -> C -> A (B, C = -1: shorter cycles)
+template <int KB, int NB, int A, int B = -1, int C = -1>
+__device__ __forceinline__ void v_cycle(uint8_t* hib, uint8_t* lob, uint32_t rows, int lane) {
+    float x[32], y[32];
+    v_read<KB>(hib, A, rows, lane, x);
+    if constexpr (B >= 0) {
+        v_read<KB>(hib, B, rows, lane, y);
+        __syncwarp();
+        v_write<KB, NB>(hib, lob, A, lane, x);  // A's data into B's place
+        if constexpr (C >= 0) {
+            v_read<KB>(hib, C, rows, lane, x);
+            __syncwarp();
+            v_write<KB, NB>(hib, lob, B, lane, y);  // B's data into C's place
+            v_write<KB, NB>(hib, lob, C, lane, x);  // C's data into A's place
+        } else {
+            v_write<KB, NB>(hib, lob, B, lane, y);  // B's data into A's place
+        }
+    } else {
+        __syncwarp();
+        v_write<KB, NB>(hib, lob, A, lane, x);  // a fixed point
+    }
+}
+
+// the cycles of softmax warp `warp`: (KB, NB) = (2, 4): {0} {7} | {1 4 2} |
+// {3 5 6} | -; (2, 2): {0} | {3} | {1 2} | -; (1, NB): {warp} (identity)
+template <int KB, int NB>
+__device__ __forceinline__ void v_transpose_warp(uint8_t* hib, uint8_t* lob, uint32_t rows,
+                                                 int warp, int lane) {
+    if constexpr (KB == 2 && NB == 4) {
+        if (warp == 0) {
+            v_cycle<2, 4, 0>(hib, lob, rows, lane);
+            v_cycle<2, 4, 7>(hib, lob, rows, lane);
+        } else if (warp == 1) {
+            v_cycle<2, 4, 1, 4, 2>(hib, lob, rows, lane);
+        } else if (warp == 2) {
+            v_cycle<2, 4, 3, 5, 6>(hib, lob, rows, lane);
+        }
+    } else if constexpr (KB == 2 && NB == 2) {
+        if (warp == 0) v_cycle<2, 2, 0>(hib, lob, rows, lane);
+        else if (warp == 1) v_cycle<2, 2, 3>(hib, lob, rows, lane);
+        else if (warp == 2) v_cycle<2, 2, 1, 2>(hib, lob, rows, lane);
+    } else {
+        static_assert(KB == 1 && NB <= 4, "the V sub-block cycles are listed for these shapes");
+        if (warp == 0) v_cycle<1, NB, 0>(hib, lob, rows, lane);
+        if constexpr (NB > 1) if (warp == 1) v_cycle<1, NB, 1>(hib, lob, rows, lane);
+        if constexpr (NB > 2) if (warp == 2) v_cycle<1, NB, 2>(hib, lob, rows, lane);
+        if constexpr (NB > 3) if (warp == 3) v_cycle<1, NB, 3>(hib, lob, rows, lane);
+    }
 }
 
 // ------------------------------------------------------------------ prep
@@ -389,80 +478,35 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         }
     } else if (warp >= C::WARP_CONV) {
         // ------------------------------------------------------------ converters
+        // the K half-tiles (even h); the softmax warps convert the V ones
         const int ct = tid - C::WARP_CONV * 32;
-        const int w = ct >> 5;
         constexpr int NT = C::NCONV * 32;
-        for (uint32_t h = 0;; ++h) {
+        for (uint32_t h = 0;; h += 2) {
             const uint32_t sl = h % NSLOT;
-            // Both converter warps meet at named barriers below, so they must
-            // stop at the same half-tile: each publishes its own reason to
-            // stop (a wait that expired, an abort, the end marker) and both
-            // decide from the two published flags.
-            const bool ok = mbar_wait(FULL + 8 * sl, (h / NSLOT) & 1);
-            if (!ok) timeout();
-            if (lane == 0) misc[2 + w] = (!ok || misc[0] || meta[4 * sl + 1]) ? 1 : 0;
-            named_sync_conv<NT>();
-            if (misc[2] | misc[3]) break;
+            if (!mbar_wait(FULL + 8 * sl, (h / NSLOT) & 1)) {
+                timeout();
+                break;
+            }
+            if (misc[0] || meta[4 * sl + 1]) break;
             const uint32_t rows = meta[4 * sl + 0];
-            uint8_t* hib = smem + sl * C::SLOT;
-            uint8_t* lob = hib + C::BUF;
-            if ((h & 1) == 0) {
-                // K: hi in place, lo beside it (both K-major, as TMA laid them)
-                float4* hi = reinterpret_cast<float4*>(hib);
-                float4* lo = reinterpret_cast<float4*>(lob);
+            float4* hi = reinterpret_cast<float4*>(smem + sl * C::SLOT);
+            float4* lo = reinterpret_cast<float4*>(smem + sl * C::SLOT + C::BUF);
+            // hi in place, lo beside it (both K-major, as TMA laid them)
 #pragma unroll
-                for (int i = ct; i < C::BUF / 16; i += NT) {
-                    // each 128-byte row of a column block is 8 float4s
-                    const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
-                    float4 x = hi[i];
-                    if (row >= rows) x = make_float4(0.f, 0.f, 0.f, 0.f);
-                    uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-                    tf32_split(x.x, h0, l0);
-                    tf32_split(x.y, h1, l1);
-                    tf32_split(x.z, h2, l2);
-                    tf32_split(x.w, h3, l3);
-                    hi[i] = make_float4(__uint_as_float(h0), __uint_as_float(h1),
-                                        __uint_as_float(h2), __uint_as_float(h3));
-                    lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
-                                        __uint_as_float(l2), __uint_as_float(l3));
-                }
-            } else {
-                // V: every 32 x 32 sub-block transposed (keys along the
-                // 128-byte rows), hi in place, lo into the lo buffer.  All
-                // converter threads read their sub-blocks (lane = dim, one
-                // key per load) before any writes, so the in-place
-                // permutation is safe whatever its cycles.
-                float x[C::SB_PER_WARP][32];
-#pragma unroll
-                for (int j = 0; j < C::SB_PER_WARP; ++j) {
-                    const int sb = w + C::NCONV * j;
-                    const int kb = sb / NB, db = sb % NB;
-                    const uint8_t* src = hib + db * C::BLK + kb * 4096;
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 +
-                                             (((lane / 4) ^ (k % 8)) * 16) + (lane % 4) * 4;
-                        const float v = *reinterpret_cast<const float*>(src + off);
-                        x[j][k] = static_cast<uint32_t>(kb * 32 + k) < rows ? v : 0.f;
-                    }
-                }
-                named_sync_conv<NT>();
-#pragma unroll
-                for (int j = 0; j < C::SB_PER_WARP; ++j) {
-                    const int sb = w + C::NCONV * j;
-                    const int kb = sb / NB, db = sb % NB;
-                    const uint32_t base = kb * C::VT_BLK + db * 4096 + (lane / 8) * 1024 +
-                                          (lane % 8) * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t hh[4], ll[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) tf32_split(x[j][4 * c + e], hh[e], ll[e]);
-                        const uint32_t off = base + ((c ^ (lane % 8)) * 16);
-                        *reinterpret_cast<uint4*>(hib + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                        *reinterpret_cast<uint4*>(lob + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-                    }
-                }
+            for (int i = ct; i < C::BUF / 16; i += NT) {
+                // each 128-byte row of a column block is 8 float4s
+                const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
+                float4 x = hi[i];
+                if (row >= rows) x = make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                tf32_split(x.x, h0, l0);
+                tf32_split(x.y, h1, l1);
+                tf32_split(x.z, h2, l2);
+                tf32_split(x.w, h3, l3);
+                hi[i] = make_float4(__uint_as_float(h0), __uint_as_float(h1),
+                                    __uint_as_float(h2), __uint_as_float(h3));
+                lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
+                                    __uint_as_float(l2), __uint_as_float(l3));
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -478,8 +522,9 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             };
             // O += P V for tile t of the item (global tile gp)
             auto issue_pv = [&](uint32_t t, uint32_t gp) {
+                // (the softmax warps convert V(gp) before they hand over P(gp))
                 const uint32_t hv = 2 * gp + 1;
-                if (!converted(hv) || !mbar_wait(PREADY + 8 * (gp & 1), (gp >> 1) & 1)) {
+                if (!mbar_wait(PREADY + 8 * (gp & 1), (gp >> 1) & 1)) {
                     timeout();
                     return false;
                 }
@@ -610,6 +655,19 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             float m = -CUDART_INF_F, l = 0.f;
             bool failed = false;
             for (uint32_t t = 0; t < ntiles; ++t, ++g) {
+                // V(g), while QK(g) runs: this warp's cycles of the in-place
+                // transpose (see v_transpose_warp)
+                {
+                    const uint32_t hv = 2 * g + 1, vs = hv % NSLOT;
+                    if (!mbar_wait(FULL + 8 * vs, (hv / NSLOT) & 1)) {
+                        timeout();
+                        failed = true;
+                        break;
+                    }
+                    uint8_t* hib = smem + vs * C::SLOT;
+                    v_transpose_warp<C::KB, NB>(hib, hib + C::BUF, meta[4 * vs + 0], warp, lane);
+                    tc::fence_proxy_async_smem();
+                }
                 if (!mbar_wait(SFULL + 8 * (g & 1), (g >> 1) & 1)) {
                     timeout();
                     failed = true;
