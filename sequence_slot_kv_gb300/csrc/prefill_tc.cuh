@@ -21,9 +21,11 @@
 //     a.b ~ a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the dropped a_lo.b_lo and the
 //     TF32 rounding of the lo parts are ~2^-20 relative).
 //       - warp 4 (producer): claims items and streams each key tile's K
-//         and then V (BK = 64 keys x hd, 128-byte swizzled boxes of 32
-//         floats) with TMA into a ring of half-stage slots (one operand's
-//         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
+//         and V (BK keys x hd, 128-byte swizzled boxes of 32 floats) with
+//         TMA into two rings of slots, one for K and one for V (a slot holds
+//         one operand's hi and lo buffers; hd 128: 1 K + 2 V slots, hd 64:
+//         3 + 3).  Each ring has one kind of consumer, which waits for every
+//         slot phase in order;
 //       - warps 6-7 (converters): split each landed K tile in place into
 //         hi and lo operand buffers (keys past the item's last zeroed);
 //       - warp 5 (MMA issuer, one thread): S = Q K^T into a TMEM score
@@ -65,8 +67,11 @@ struct PCfg {
     static constexpr int NB = HD / 32;          // 128-byte column blocks per key row
     static constexpr int BLK = BK * 128;        // one column block: BK rows x 128 B
     static constexpr int BUF = NB * BLK;        // one operand buffer, [BK][HD] f32
-    static constexpr int SLOT = 2 * BUF;        // half-stage slot: hi | lo of K or V
-    static constexpr int NSLOT = (192 * 1024) / SLOT;  // 3 (hd 128) or 6 (hd 64)
+    static constexpr int SLOT = 2 * BUF;        // one operand's hi | lo buffers
+    static constexpr int NSLOT = (192 * 1024) / SLOT;  // 3 (hd 128, 64 keys) or 6
+    static constexpr int NVS = (NSLOT + 1) / 2;        // V slots (after the K slots)
+    static constexpr int NKS = NSLOT - NVS;            // K slots
+    static_assert(NKS >= 1 && NVS >= 1, "slots");
     // V transposed: KB column blocks of 32 keys, each [HD rows][128 B]; the
     // 32 x 32 sub-block (key block kb, dim block db) lands at kb * VT_BLK +
     // db * 4096 (TMA put it at db * BLK + kb * 4096)
@@ -88,9 +93,10 @@ struct PCfg {
     static constexpr int OFF_DESC = NSLOT * SLOT;
     static constexpr int OFF_META = OFF_DESC + 2 * 32;
     static constexpr int OFF_BAR = OFF_META + NSLOT * 16;
-    // full[NSLOT], conv[NSLOT], empty[NSLOT], s_full[2], p_ready[2],
-    // pv_done[2], q_ready, item_full[2], item_free[2], drain
-    static constexpr int NBAR = 3 * NSLOT + 12;
+    // K ring: full[NKS], conv[NKS], empty[NKS]; V ring: full[NVS],
+    // empty[NVS]; s_full[2], p_ready[2], pv_done[2], q_ready,
+    // item_full[2], item_free[2], drain
+    static constexpr int NBAR = 3 * NKS + 2 * NVS + 12;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
     static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -347,14 +353,14 @@ __global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const Pref
 }
 
 // ------------------------------------------------------------------ attention
-// Half-tile h of the CTA's stream of key tiles: h = 2g is tile g's K, h = 2g + 1
-// its V; it lives in slot h % NSLOT.
+// The CTA's key tiles are numbered g = 0, 1, ... across its items; tile g's K
+// uses K slot g % NKS and its V uses V slot g % NVS.
 template <int HD, int G>
 __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     slotkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const PrefillParams P) {
     using C = PCfg<HD, G>;
-    constexpr int BK = C::BK, NB = C::NB, NSLOT = C::NSLOT, NBUF = C::NBUF;
+    constexpr int BK = C::BK, NB = C::NB, NBUF = C::NBUF;
     constexpr float kLog2e = 1.4426950408889634f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -365,19 +371,25 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
     const uint32_t ring = smem_addr(smem);
     const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
-    const uint32_t FULL = bar0, CONV = bar0 + 8 * NSLOT, EMPTY = bar0 + 16 * NSLOT;
-    const uint32_t SFULL = bar0 + 24 * NSLOT, PREADY = SFULL + 16;
+    constexpr int NKS = C::NKS, NVS = C::NVS;
+    const uint32_t FULLK = bar0, CONVK = FULLK + 8 * NKS, EMPTYK = CONVK + 8 * NKS;
+    const uint32_t FULLV = EMPTYK + 8 * NKS, EMPTYV = FULLV + 8 * NVS;
+    const uint32_t SFULL = EMPTYV + 8 * NVS, PREADY = SFULL + 16;
     const uint32_t PVDONE = PREADY + 16, QREADY = PVDONE + 16, IFULL = QREADY + 8;
     const uint32_t IFREE = IFULL + 16, DRAIN = IFREE + 16;
-    // hi and lo operand buffers of a slot
+    // hi and lo operand buffers of K slot i and V slot j (slot index NKS + j)
     auto slot_hi = [&](uint32_t sl) { return ring + sl * C::SLOT; };
     auto slot_lo = [&](uint32_t sl) { return ring + sl * C::SLOT + C::BUF; };
 
     if (tid == 0) {
-        for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(FULL + 8 * i, 1);
-            mbar_init(CONV + 8 * i, C::NCONV);
-            mbar_init(EMPTY + 8 * i, 1);
+        for (int i = 0; i < NKS; ++i) {
+            mbar_init(FULLK + 8 * i, 1);
+            mbar_init(CONVK + 8 * i, C::NCONV);
+            mbar_init(EMPTYK + 8 * i, 1);
+        }
+        for (int j = 0; j < NVS; ++j) {
+            mbar_init(FULLV + 8 * j, 1);
+            mbar_init(EMPTYV + 8 * j, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(SFULL + 8 * b, 1);
@@ -410,11 +422,15 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         if (lane == 0) {
             const uint32_t n_items = __ldcg(P.plan);
             const uint4* tiles = reinterpret_cast<const uint4*>(P.tiles);
-            uint32_t h = 0;  // half-tiles issued
-            // wait until slot h % NSLOT is free again
-            auto slot_free = [&](uint32_t hh) {
-                return hh < static_cast<uint32_t>(NSLOT) ||
-                       mbar_wait(EMPTY + 8 * (hh % NSLOT), ((hh / NSLOT) - 1) & 1);
+            uint32_t g = 0;  // key tiles issued (each: a K slot use and a V slot use)
+            // slot of use u of a ring of n slots is free again
+            auto free_k = [&](uint32_t u) {
+                return u < static_cast<uint32_t>(NKS) ||
+                       mbar_wait(EMPTYK + 8 * (u % NKS), ((u / NKS) - 1) & 1);
+            };
+            auto free_v = [&](uint32_t u) {
+                return u < static_cast<uint32_t>(NVS) ||
+                       mbar_wait(EMPTYV + 8 * (u % NVS), ((u / NVS) - 1) & 1);
             };
             for (uint32_t k = 0;; ++k) {
                 const uint32_t is = k & 1;
@@ -428,13 +444,13 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 if (it >= n_items) {
                     d[6] = 1;
                     mbar_arrive(IFULL + 8 * is);
-                    // tell the converters: an end marker in the next slot
-                    if (!slot_free(h)) {
+                    // tell the converters: an end marker in the next K slot
+                    if (!free_k(g)) {
                         timeout();
                         break;
                     }
-                    meta[4 * (h % NSLOT) + 1] = 1;
-                    mbar_arrive(FULL + 8 * (h % NSLOT));
+                    meta[4 * (g % NKS) + 1] = 1;
+                    mbar_arrive(FULLK + 8 * (g % NKS));
                     break;
                 }
                 const uint4 rec = __ldcg(tiles + it / P.n_kv_head);
@@ -450,40 +466,53 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 d[6] = 0;
                 mbar_arrive(IFULL + 8 * is);
                 const int y0 = static_cast<int>(rec.z * P.slot_ctx);
-                for (uint32_t t = 0; t < ntiles && !misc[0]; ++t) {
+                for (uint32_t t = 0; t < ntiles; ++t, ++g) {
                     const uint32_t left = max_pos + 1 - t * BK;
+                    const uint32_t rows = left < static_cast<uint32_t>(BK) ? left : BK;
                     const int y = y0 + static_cast<int>(t * BK);
-                    for (int which = 0; which < 2; ++which, ++h) {  // K, then V
-                        if (!slot_free(h)) {
-                            timeout();
-                            break;
-                        }
-                        const uint32_t sl = h % NSLOT;
-                        meta[4 * sl + 0] = left < static_cast<uint32_t>(BK) ? left : BK;
-                        meta[4 * sl + 1] = 0;
-                        mbar_expect_tx(FULL + 8 * sl, C::BUF);
-#pragma unroll
-                        for (int c = 0; c < NB; ++c)
-                            tma_load_2d(slot_hi(sl) + c * C::BLK, which ? &tmV : &tmK,
-                                        static_cast<int>(kvh * HD) + 32 * c, y, FULL + 8 * sl);
+                    const int x0 = static_cast<int>(kvh * HD);
+                    if (!free_k(g)) {
+                        timeout();
+                        break;
                     }
+                    const uint32_t ks = g % NKS;
+                    meta[4 * ks + 0] = rows;
+                    meta[4 * ks + 1] = 0;
+                    mbar_expect_tx(FULLK + 8 * ks, C::BUF);
+#pragma unroll
+                    for (int c = 0; c < NB; ++c)
+                        tma_load_2d(slot_hi(ks) + c * C::BLK, &tmK, x0 + 32 * c, y, FULLK + 8 * ks);
+                    if (!free_v(g)) {
+                        timeout();
+                        break;
+                    }
+                    const uint32_t vs = NKS + g % NVS;
+                    meta[4 * vs + 0] = rows;
+                    mbar_expect_tx(FULLV + 8 * (g % NVS), C::BUF);
+#pragma unroll
+                    for (int c = 0; c < NB; ++c)
+                        tma_load_2d(slot_hi(vs) + c * C::BLK, &tmV, x0 + 32 * c, y,
+                                    FULLV + 8 * (g % NVS));
+                    if (misc[0]) break;
                 }
                 if (misc[0]) break;
             }
             if (misc[0]) {
                 // drain this CTA's copies that may still be in flight
-                for (uint32_t u = h > static_cast<uint32_t>(NSLOT) ? h - NSLOT : 0; u < h; ++u)
-                    mbar_wait(FULL + 8 * (u % NSLOT), (u / NSLOT) & 1, 1ll << 28);
+                for (uint32_t u = g > static_cast<uint32_t>(NKS) ? g - NKS : 0; u < g; ++u)
+                    mbar_wait(FULLK + 8 * (u % NKS), (u / NKS) & 1, 1ll << 28);
+                for (uint32_t u = g > static_cast<uint32_t>(NVS) ? g - NVS : 0; u < g; ++u)
+                    mbar_wait(FULLV + 8 * (u % NVS), (u / NVS) & 1, 1ll << 28);
             }
         }
     } else if (warp >= C::WARP_CONV) {
         // ------------------------------------------------------------ converters
-        // the K half-tiles (even h); the softmax warps convert the V ones
+        // the K ring; the softmax warps convert the V tiles
         const int ct = tid - C::WARP_CONV * 32;
         constexpr int NT = C::NCONV * 32;
-        for (uint32_t h = 0;; h += 2) {
-            const uint32_t sl = h % NSLOT;
-            if (!mbar_wait(FULL + 8 * sl, (h / NSLOT) & 1)) {
+        for (uint32_t u = 0;; ++u) {
+            const uint32_t sl = u % NKS;
+            if (!mbar_wait(FULLK + 8 * sl, (u / NKS) & 1)) {
                 timeout();
                 break;
             }
@@ -510,26 +539,25 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(CONV + 8 * sl);
+            if (lane == 0) mbar_arrive(CONVK + 8 * sl);
         }
     } else if (warp == C::WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t g = 0;  // key tiles whose QK was issued
             bool ok = true;
-            auto converted = [&](uint32_t hh) {
-                return mbar_wait(CONV + 8 * (hh % NSLOT), (hh / NSLOT) & 1);
+            auto converted = [&](uint32_t u) {
+                return mbar_wait(CONVK + 8 * (u % NKS), (u / NKS) & 1);
             };
             // O += P V for tile t of the item (global tile gp)
             auto issue_pv = [&](uint32_t t, uint32_t gp) {
                 // (the softmax warps convert V(gp) before they hand over P(gp))
-                const uint32_t hv = 2 * gp + 1;
                 if (!mbar_wait(PREADY + 8 * (gp & 1), (gp >> 1) & 1)) {
                     timeout();
                     return false;
                 }
                 tc::fence_after_sync();
-                const uint32_t sl = hv % NSLOT;
+                const uint32_t sl = NKS + gp % NVS;
                 const uint32_t pcol0 = C::C_S + (gp % NBUF) * C::C_BUF;
 #pragma unroll
                 for (int term = 0; term < 3; ++term) {
@@ -544,7 +572,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     }
                 }
                 tc::mma_commit(PVDONE + 8 * (gp & 1));
-                tc::mma_commit(EMPTY + 8 * sl);
+                tc::mma_commit(EMPTYV + 8 * (gp % NVS));
                 return true;
             };
             for (uint32_t k = 0; ok; ++k) {
@@ -562,8 +590,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 }
                 tc::fence_after_sync();
                 for (uint32_t t = 0; t < ntiles; ++t, ++g) {
-                    const uint32_t hk = 2 * g;
-                    if (!converted(hk)) {
+                    if (!converted(g)) {
                         timeout();
                         ok = false;
                         break;
@@ -574,7 +601,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     }
                     tc::fence_after_sync();
                     // S = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
-                    const uint32_t sl = hk % NSLOT;
+                    const uint32_t sl = g % NKS;
                     const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF;
 #pragma unroll
                     for (int term = 0; term < 3; ++term) {
@@ -589,7 +616,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                         }
                     }
                     tc::mma_commit(SFULL + 8 * (g & 1));
-                    tc::mma_commit(EMPTY + 8 * sl);  // K slot free once QK has read it
+                    tc::mma_commit(EMPTYK + 8 * sl);  // K slot free once QK has read it
                     // one buffer: this tile's PV next; two: the previous tile's
                     if (NBUF == 1) {
                         if (!issue_pv(t, g)) {
@@ -658,8 +685,8 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 // V(g), while QK(g) runs: this warp's cycles of the in-place
                 // transpose (see v_transpose_warp)
                 {
-                    const uint32_t hv = 2 * g + 1, vs = hv % NSLOT;
-                    if (!mbar_wait(FULL + 8 * vs, (hv / NSLOT) & 1)) {
+                    const uint32_t vs = NKS + g % NVS;
+                    if (!mbar_wait(FULLV + 8 * (g % NVS), (g / NVS) & 1)) {
                         timeout();
                         failed = true;
                         break;
