@@ -21,13 +21,14 @@
 //     a.b ~ a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the dropped a_lo.b_lo and the
 //     TF32 rounding of the lo parts are ~2^-20 relative).
 //       - warp 4 (producer): claims items and streams each key tile's K
-//         and V (BK keys x hd, 128-byte swizzled boxes of 32 floats) with
-//         TMA into two rings of slots, one for K and one for V (a slot holds
-//         one operand's hi and lo buffers; hd 128: 1 K + 2 V slots, hd 64:
-//         3 + 3).  Each ring has one kind of consumer, which waits for every
-//         slot phase in order;
+//         and then V (BK = 64 keys x hd, 128-byte swizzled boxes of 32
+//         floats) with TMA into a ring of half-stage slots (one operand's
+//         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
 //       - warps 6-7 (converters): split each landed K tile in place into
-//         hi and lo operand buffers (keys past the item's last zeroed);
+//         hi and lo operand buffers, and transpose each landed V tile into
+//         a keys-contiguous layout while splitting it (TF32 MMA operands
+//         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
+//         keys past the item's last are zeroed;
 //       - warp 5 (MMA issuer, one thread): S = Q K^T into a TMEM score
 //         buffer (A = Q from TMEM), then O += P V (A = P from TMEM, B = the
 //         transposed V tile).  With two score buffers (hd 64) the issue order
@@ -36,13 +37,7 @@
 //         MMAs from one thread run in issue order, so a QK reuses a buffer
 //         only after the PV before it has read it;
 //       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
-//         the item's q rows (hi, lo) into TMEM; per key tile, while its QK
-//         runs, transpose the landed V tile in place into a keys-contiguous
-//         layout and split it (TF32 MMA operands in shared memory are
-//         K-major: for O += P V that is V^T, [hd][keys]; keys past the
-//         item's last zeroed) -- each warp takes whole cycles of the
-//         32 x 32 sub-block permutation, so no other warp touches its
-//         sub-blocks -- then read S,
+//         the item's q rows (hi, lo) into TMEM, then per key tile read S,
 //         apply the causal mask (key <= the row's position), run a base-2
 //         online softmax with a lazily raised max, write P (hi over S, lo
 //         beside it) into the same buffer and, only when the max moves,
@@ -67,11 +62,8 @@ struct PCfg {
     static constexpr int NB = HD / 32;          // 128-byte column blocks per key row
     static constexpr int BLK = BK * 128;        // one column block: BK rows x 128 B
     static constexpr int BUF = NB * BLK;        // one operand buffer, [BK][HD] f32
-    static constexpr int SLOT = 2 * BUF;        // one operand's hi | lo buffers
-    static constexpr int NSLOT = (192 * 1024) / SLOT;  // 3 (hd 128, 64 keys) or 6
-    static constexpr int NVS = (NSLOT + 1) / 2;        // V slots (after the K slots)
-    static constexpr int NKS = NSLOT - NVS;            // K slots
-    static_assert(NKS >= 1 && NVS >= 1, "slots");
+    static constexpr int SLOT = 2 * BUF;        // half-stage slot: hi | lo of K or V
+    static constexpr int NSLOT = (192 * 1024) / SLOT;  // 3 (hd 128) or 6 (hd 64)
     // V transposed: KB column blocks of 32 keys, each [HD rows][128 B]; the
     // 32 x 32 sub-block (key block kb, dim block db) lands at kb * VT_BLK +
     // db * 4096 (TMA put it at db * BLK + kb * 4096)
@@ -79,6 +71,7 @@ struct PCfg {
     static constexpr int VT_BLK = HD * 128;
     static constexpr int NSW = 4;               // softmax warps
     static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
+    static constexpr int SB_PER_WARP = KB * NB / NCONV;  // V sub-blocks per converter warp
     static constexpr int THREADS = 256;
     // tensor memory columns: Q hi | Q lo | O | NBUF buffers of (S, then P hi
     // over it | P lo)
@@ -93,10 +86,9 @@ struct PCfg {
     static constexpr int OFF_DESC = NSLOT * SLOT;
     static constexpr int OFF_META = OFF_DESC + 2 * 32;
     static constexpr int OFF_BAR = OFF_META + NSLOT * 16;
-    // K ring: full[NKS], conv[NKS], empty[NKS]; V ring: full[NVS],
-    // empty[NVS]; s_full[2], p_ready[2], pv_done[2], q_ready,
-    // item_full[2], item_free[2], drain
-    static constexpr int NBAR = 3 * NKS + 2 * NVS + 12;
+    // full[NSLOT], conv[NSLOT], empty[NSLOT], s_full[2], p_ready[2],
+    // pv_done[2], q_ready, item_full[2], item_free[2], drain
+    static constexpr int NBAR = 3 * NSLOT + 12;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
     static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -105,8 +97,15 @@ struct PCfg {
     static_assert(BLK % 1024 == 0 && SLOT % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
     static constexpr uint32_t IDESC_QK = tc::idesc_tf32(M, BK, false);
     static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, false);
-
+    static_assert(KB * NB == SB_PER_WARP * NCONV, "V sub-blocks split evenly over the converters");
+    static_assert(NCONV == 2, "the converters' stop flags are misc[2], misc[3]");
 };
+
+// Named barrier 2 over the converter warps (N threads).
+template <int N>
+__device__ __forceinline__ void named_sync_conv() {
+    asm volatile("bar.sync 2, %0;" ::"n"(N) : "memory");
+}
 
 // 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz:
 // a few ulp of relative error, subnormal results flushed to zero), far
@@ -122,100 +121,6 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) 
     const uint32_t h = __float_as_uint(x) & 0xFFFFE000u;
     hi = h;
     lo = __float_as_uint(x - __uint_as_float(h));
-}
-
-// ------------------------------------------------------------------ V transpose
-// The V tile of a stage lands as NB column blocks of BK rows x 128 bytes
-// (128-byte swizzled TMA boxes): the 32 x 32 sub-block (key block kb, dim
-// block db) sits at source location L = db * KB + kb (4 KiB each).  The PV
-// MMA reads it transposed (keys contiguous), at location kb * NB + db, the
-// layout of a K-major [HD][BK] operand.  The transpose is done in place, a
-// sub-block at a time, by whole cycles of that permutation, each cycle by one
-// warp: read the first sub-block, then for each next one read it and write
-// the previous one into its place, and finally write the last into the
-// first's place (two sub-blocks in registers at most).  Keys past `rows` are
-// zeroed; hi goes in place and lo to the same offset of the lo buffer.
-
-// this lane's 32 keys of a sub-block at location L (lane = dim)
-template <int KB>
-__device__ __forceinline__ void v_read(const uint8_t* hib, int L, uint32_t rows, int lane,
-                                       float (&x)[32]) {
-    const uint8_t* src = hib + L * 4096;
-    const uint32_t kb = static_cast<uint32_t>(L % KB);
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 + (((lane / 4) ^ (k % 8)) * 16) +
-                             (lane % 4) * 4;
-        const float v = *reinterpret_cast<const float*>(src + off);
-        x[k] = kb * 32 + static_cast<uint32_t>(k) < rows ? v : 0.f;
-    }
-}
-
-// write sub-block data x (read from location L) transposed into its target
-template <int KB, int NB>
-__device__ __forceinline__ void v_write(uint8_t* hib, uint8_t* lob, int L, int lane,
-                                        const float (&x)[32]) {
-    const int kb = L % KB, db = L / KB;
-    const uint32_t base = (kb * NB + db) * 4096 + (lane / 8) * 1024 + (lane % 8) * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint32_t hh[4], ll[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) tf32_split(x[4 * c + e], hh[e], ll[e]);
-        const uint32_t off = base + ((c ^ (lane % 8)) * 16);
-        *reinterpret_cast<uint4*>(hib + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-        *reinterpret_cast<uint4*>(lob + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-    }
-}
-
-// one permutation cycle A -> B -> C -> A (B, C = -1: shorter cycles)
-template <int KB, int NB, int A, int B = -1, int C = -1>
-__device__ __forceinline__ void v_cycle(uint8_t* hib, uint8_t* lob, uint32_t rows, int lane) {
-    float x[32], y[32];
-    v_read<KB>(hib, A, rows, lane, x);
-    if constexpr (B >= 0) {
-        v_read<KB>(hib, B, rows, lane, y);
-        __syncwarp();
-        v_write<KB, NB>(hib, lob, A, lane, x);  // A's data into B's place
-        if constexpr (C >= 0) {
-            v_read<KB>(hib, C, rows, lane, x);
-            __syncwarp();
-            v_write<KB, NB>(hib, lob, B, lane, y);  // B's data into C's place
-            v_write<KB, NB>(hib, lob, C, lane, x);  // C's data into A's place
-        } else {
-            v_write<KB, NB>(hib, lob, B, lane, y);  // B's data into A's place
-        }
-    } else {
-        __syncwarp();
-        v_write<KB, NB>(hib, lob, A, lane, x);  // a fixed point
-    }
-}
-
-// the cycles of softmax warp `warp`: (KB, NB) = (2, 4): {0} {7} | {1 4 2} |
-// {3 5 6} | -; (2, 2): {0} | {3} | {1 2} | -; (1, NB): {warp} (identity)
-template <int KB, int NB>
-__device__ __forceinline__ void v_transpose_warp(uint8_t* hib, uint8_t* lob, uint32_t rows,
-                                                 int warp, int lane) {
-    if constexpr (KB == 2 && NB == 4) {
-        if (warp == 0) {
-            v_cycle<2, 4, 0>(hib, lob, rows, lane);
-            v_cycle<2, 4, 7>(hib, lob, rows, lane);
-        } else if (warp == 1) {
-            v_cycle<2, 4, 1, 4, 2>(hib, lob, rows, lane);
-        } else if (warp == 2) {
-            v_cycle<2, 4, 3, 5, 6>(hib, lob, rows, lane);
-        }
-    } else if constexpr (KB == 2 && NB == 2) {
-        if (warp == 0) v_cycle<2, 2, 0>(hib, lob, rows, lane);
-        else if (warp == 1) v_cycle<2, 2, 3>(hib, lob, rows, lane);
-        else if (warp == 2) v_cycle<2, 2, 1, 2>(hib, lob, rows, lane);
-    } else {
-        static_assert(KB == 1 && NB <= 4, "the V sub-block cycles are listed for these shapes");
-        if (warp == 0) v_cycle<1, NB, 0>(hib, lob, rows, lane);
-        if constexpr (NB > 1) if (warp == 1) v_cycle<1, NB, 1>(hib, lob, rows, lane);
-        if constexpr (NB > 2) if (warp == 2) v_cycle<1, NB, 2>(hib, lob, rows, lane);
-        if constexpr (NB > 3) if (warp == 3) v_cycle<1, NB, 3>(hib, lob, rows, lane);
-    }
 }
 
 // ------------------------------------------------------------------ prep
@@ -353,14 +258,14 @@ __global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const Pref
 }
 
 // ------------------------------------------------------------------ attention
-// The CTA's key tiles are numbered g = 0, 1, ... across its items; tile g's K
-// uses K slot g % NKS and its V uses V slot g % NVS.
+// Half-tile h of the CTA's stream of key tiles: h = 2g is tile g's K, h = 2g + 1
+// its V; it lives in slot h % NSLOT.
 template <int HD, int G>
 __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     slotkv_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const PrefillParams P) {
     using C = PCfg<HD, G>;
-    constexpr int BK = C::BK, NB = C::NB, NBUF = C::NBUF;
+    constexpr int BK = C::BK, NB = C::NB, NSLOT = C::NSLOT, NBUF = C::NBUF;
     constexpr float kLog2e = 1.4426950408889634f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -371,25 +276,19 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
     const uint32_t ring = smem_addr(smem);
     const uint32_t bar0 = smem_addr(smem + C::OFF_BAR);
-    constexpr int NKS = C::NKS, NVS = C::NVS;
-    const uint32_t FULLK = bar0, CONVK = FULLK + 8 * NKS, EMPTYK = CONVK + 8 * NKS;
-    const uint32_t FULLV = EMPTYK + 8 * NKS, EMPTYV = FULLV + 8 * NVS;
-    const uint32_t SFULL = EMPTYV + 8 * NVS, PREADY = SFULL + 16;
+    const uint32_t FULL = bar0, CONV = bar0 + 8 * NSLOT, EMPTY = bar0 + 16 * NSLOT;
+    const uint32_t SFULL = bar0 + 24 * NSLOT, PREADY = SFULL + 16;
     const uint32_t PVDONE = PREADY + 16, QREADY = PVDONE + 16, IFULL = QREADY + 8;
     const uint32_t IFREE = IFULL + 16, DRAIN = IFREE + 16;
-    // hi and lo operand buffers of K slot i and V slot j (slot index NKS + j)
+    // hi and lo operand buffers of a slot
     auto slot_hi = [&](uint32_t sl) { return ring + sl * C::SLOT; };
     auto slot_lo = [&](uint32_t sl) { return ring + sl * C::SLOT + C::BUF; };
 
     if (tid == 0) {
-        for (int i = 0; i < NKS; ++i) {
-            mbar_init(FULLK + 8 * i, 1);
-            mbar_init(CONVK + 8 * i, C::NCONV);
-            mbar_init(EMPTYK + 8 * i, 1);
-        }
-        for (int j = 0; j < NVS; ++j) {
-            mbar_init(FULLV + 8 * j, 1);
-            mbar_init(EMPTYV + 8 * j, 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(FULL + 8 * i, 1);
+            mbar_init(CONV + 8 * i, C::NCONV);
+            mbar_init(EMPTY + 8 * i, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(SFULL + 8 * b, 1);
@@ -422,15 +321,11 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         if (lane == 0) {
             const uint32_t n_items = __ldcg(P.plan);
             const uint4* tiles = reinterpret_cast<const uint4*>(P.tiles);
-            uint32_t g = 0;  // key tiles issued (each: a K slot use and a V slot use)
-            // slot of use u of a ring of n slots is free again
-            auto free_k = [&](uint32_t u) {
-                return u < static_cast<uint32_t>(NKS) ||
-                       mbar_wait(EMPTYK + 8 * (u % NKS), ((u / NKS) - 1) & 1);
-            };
-            auto free_v = [&](uint32_t u) {
-                return u < static_cast<uint32_t>(NVS) ||
-                       mbar_wait(EMPTYV + 8 * (u % NVS), ((u / NVS) - 1) & 1);
+            uint32_t h = 0;  // half-tiles issued
+            // wait until slot h % NSLOT is free again
+            auto slot_free = [&](uint32_t hh) {
+                return hh < static_cast<uint32_t>(NSLOT) ||
+                       mbar_wait(EMPTY + 8 * (hh % NSLOT), ((hh / NSLOT) - 1) & 1);
             };
             for (uint32_t k = 0;; ++k) {
                 const uint32_t is = k & 1;
@@ -444,13 +339,13 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 if (it >= n_items) {
                     d[6] = 1;
                     mbar_arrive(IFULL + 8 * is);
-                    // tell the converters: an end marker in the next K slot
-                    if (!free_k(g)) {
+                    // tell the converters: an end marker in the next slot
+                    if (!slot_free(h)) {
                         timeout();
                         break;
                     }
-                    meta[4 * (g % NKS) + 1] = 1;
-                    mbar_arrive(FULLK + 8 * (g % NKS));
+                    meta[4 * (h % NSLOT) + 1] = 1;
+                    mbar_arrive(FULL + 8 * (h % NSLOT));
                     break;
                 }
                 const uint4 rec = __ldcg(tiles + it / P.n_kv_head);
@@ -466,98 +361,130 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 d[6] = 0;
                 mbar_arrive(IFULL + 8 * is);
                 const int y0 = static_cast<int>(rec.z * P.slot_ctx);
-                for (uint32_t t = 0; t < ntiles; ++t, ++g) {
+                for (uint32_t t = 0; t < ntiles && !misc[0]; ++t) {
                     const uint32_t left = max_pos + 1 - t * BK;
-                    const uint32_t rows = left < static_cast<uint32_t>(BK) ? left : BK;
                     const int y = y0 + static_cast<int>(t * BK);
-                    const int x0 = static_cast<int>(kvh * HD);
-                    if (!free_k(g)) {
-                        timeout();
-                        break;
-                    }
-                    const uint32_t ks = g % NKS;
-                    meta[4 * ks + 0] = rows;
-                    meta[4 * ks + 1] = 0;
-                    mbar_expect_tx(FULLK + 8 * ks, C::BUF);
+                    for (int which = 0; which < 2; ++which, ++h) {  // K, then V
+                        if (!slot_free(h)) {
+                            timeout();
+                            break;
+                        }
+                        const uint32_t sl = h % NSLOT;
+                        meta[4 * sl + 0] = left < static_cast<uint32_t>(BK) ? left : BK;
+                        meta[4 * sl + 1] = 0;
+                        mbar_expect_tx(FULL + 8 * sl, C::BUF);
 #pragma unroll
-                    for (int c = 0; c < NB; ++c)
-                        tma_load_2d(slot_hi(ks) + c * C::BLK, &tmK, x0 + 32 * c, y, FULLK + 8 * ks);
-                    if (!free_v(g)) {
-                        timeout();
-                        break;
+                        for (int c = 0; c < NB; ++c)
+                            tma_load_2d(slot_hi(sl) + c * C::BLK, which ? &tmV : &tmK,
+                                        static_cast<int>(kvh * HD) + 32 * c, y, FULL + 8 * sl);
                     }
-                    const uint32_t vs = NKS + g % NVS;
-                    meta[4 * vs + 0] = rows;
-                    mbar_expect_tx(FULLV + 8 * (g % NVS), C::BUF);
-#pragma unroll
-                    for (int c = 0; c < NB; ++c)
-                        tma_load_2d(slot_hi(vs) + c * C::BLK, &tmV, x0 + 32 * c, y,
-                                    FULLV + 8 * (g % NVS));
-                    if (misc[0]) break;
                 }
                 if (misc[0]) break;
             }
             if (misc[0]) {
                 // drain this CTA's copies that may still be in flight
-                for (uint32_t u = g > static_cast<uint32_t>(NKS) ? g - NKS : 0; u < g; ++u)
-                    mbar_wait(FULLK + 8 * (u % NKS), (u / NKS) & 1, 1ll << 28);
-                for (uint32_t u = g > static_cast<uint32_t>(NVS) ? g - NVS : 0; u < g; ++u)
-                    mbar_wait(FULLV + 8 * (u % NVS), (u / NVS) & 1, 1ll << 28);
+                for (uint32_t u = h > static_cast<uint32_t>(NSLOT) ? h - NSLOT : 0; u < h; ++u)
+                    mbar_wait(FULL + 8 * (u % NSLOT), (u / NSLOT) & 1, 1ll << 28);
             }
         }
     } else if (warp >= C::WARP_CONV) {
         // ------------------------------------------------------------ converters
-        // the K ring; the softmax warps convert the V tiles
         const int ct = tid - C::WARP_CONV * 32;
+        const int w = ct >> 5;
         constexpr int NT = C::NCONV * 32;
-        for (uint32_t u = 0;; ++u) {
-            const uint32_t sl = u % NKS;
-            if (!mbar_wait(FULLK + 8 * sl, (u / NKS) & 1)) {
-                timeout();
-                break;
-            }
-            if (misc[0] || meta[4 * sl + 1]) break;
+        for (uint32_t h = 0;; ++h) {
+            const uint32_t sl = h % NSLOT;
+            // Both converter warps meet at named barriers below, so they must
+            // stop at the same half-tile: each publishes its own reason to
+            // stop (a wait that expired, an abort, the end marker) and both
+            // decide from the two published flags.
+            const bool ok = mbar_wait(FULL + 8 * sl, (h / NSLOT) & 1);
+            if (!ok) timeout();
+            if (lane == 0) misc[2 + w] = (!ok || misc[0] || meta[4 * sl + 1]) ? 1 : 0;
+            named_sync_conv<NT>();
+            if (misc[2] | misc[3]) break;
             const uint32_t rows = meta[4 * sl + 0];
-            float4* hi = reinterpret_cast<float4*>(smem + sl * C::SLOT);
-            float4* lo = reinterpret_cast<float4*>(smem + sl * C::SLOT + C::BUF);
-            // hi in place, lo beside it (both K-major, as TMA laid them)
+            uint8_t* hib = smem + sl * C::SLOT;
+            uint8_t* lob = hib + C::BUF;
+            if ((h & 1) == 0) {
+                // K: hi in place, lo beside it (both K-major, as TMA laid them)
+                float4* hi = reinterpret_cast<float4*>(hib);
+                float4* lo = reinterpret_cast<float4*>(lob);
 #pragma unroll
-            for (int i = ct; i < C::BUF / 16; i += NT) {
-                // each 128-byte row of a column block is 8 float4s
-                const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
-                float4 x = hi[i];
-                if (row >= rows) x = make_float4(0.f, 0.f, 0.f, 0.f);
-                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-                tf32_split(x.x, h0, l0);
-                tf32_split(x.y, h1, l1);
-                tf32_split(x.z, h2, l2);
-                tf32_split(x.w, h3, l3);
-                hi[i] = make_float4(__uint_as_float(h0), __uint_as_float(h1),
-                                    __uint_as_float(h2), __uint_as_float(h3));
-                lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
-                                    __uint_as_float(l2), __uint_as_float(l3));
+                for (int i = ct; i < C::BUF / 16; i += NT) {
+                    // each 128-byte row of a column block is 8 float4s
+                    const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
+                    float4 x = hi[i];
+                    if (row >= rows) x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                    tf32_split(x.x, h0, l0);
+                    tf32_split(x.y, h1, l1);
+                    tf32_split(x.z, h2, l2);
+                    tf32_split(x.w, h3, l3);
+                    hi[i] = make_float4(__uint_as_float(h0), __uint_as_float(h1),
+                                        __uint_as_float(h2), __uint_as_float(h3));
+                    lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
+                                        __uint_as_float(l2), __uint_as_float(l3));
+                }
+            } else {
+                // V: every 32 x 32 sub-block transposed (keys along the
+                // 128-byte rows), hi in place, lo into the lo buffer.  All
+                // converter threads read their sub-blocks (lane = dim, one
+                // key per load) before any writes, so the in-place
+                // permutation is safe whatever its cycles.
+                float x[C::SB_PER_WARP][32];
+#pragma unroll
+                for (int j = 0; j < C::SB_PER_WARP; ++j) {
+                    const int sb = w + C::NCONV * j;
+                    const int kb = sb / NB, db = sb % NB;
+                    const uint8_t* src = hib + db * C::BLK + kb * 4096;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const uint32_t off = (k / 8) * 1024 + (k % 8) * 128 +
+                                             (((lane / 4) ^ (k % 8)) * 16) + (lane % 4) * 4;
+                        const float v = *reinterpret_cast<const float*>(src + off);
+                        x[j][k] = static_cast<uint32_t>(kb * 32 + k) < rows ? v : 0.f;
+                    }
+                }
+                named_sync_conv<NT>();
+#pragma unroll
+                for (int j = 0; j < C::SB_PER_WARP; ++j) {
+                    const int sb = w + C::NCONV * j;
+                    const int kb = sb / NB, db = sb % NB;
+                    const uint32_t base = kb * C::VT_BLK + db * 4096 + (lane / 8) * 1024 +
+                                          (lane % 8) * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t hh[4], ll[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) tf32_split(x[j][4 * c + e], hh[e], ll[e]);
+                        const uint32_t off = base + ((c ^ (lane % 8)) * 16);
+                        *reinterpret_cast<uint4*>(hib + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<uint4*>(lob + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+                    }
+                }
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(CONVK + 8 * sl);
+            if (lane == 0) mbar_arrive(CONV + 8 * sl);
         }
     } else if (warp == C::WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t g = 0;  // key tiles whose QK was issued
             bool ok = true;
-            auto converted = [&](uint32_t u) {
-                return mbar_wait(CONVK + 8 * (u % NKS), (u / NKS) & 1);
+            auto converted = [&](uint32_t hh) {
+                return mbar_wait(CONV + 8 * (hh % NSLOT), (hh / NSLOT) & 1);
             };
             // O += P V for tile t of the item (global tile gp)
             auto issue_pv = [&](uint32_t t, uint32_t gp) {
-                // (the softmax warps convert V(gp) before they hand over P(gp))
-                if (!mbar_wait(PREADY + 8 * (gp & 1), (gp >> 1) & 1)) {
+                const uint32_t hv = 2 * gp + 1;
+                if (!converted(hv) || !mbar_wait(PREADY + 8 * (gp & 1), (gp >> 1) & 1)) {
                     timeout();
                     return false;
                 }
                 tc::fence_after_sync();
-                const uint32_t sl = NKS + gp % NVS;
+                const uint32_t sl = hv % NSLOT;
                 const uint32_t pcol0 = C::C_S + (gp % NBUF) * C::C_BUF;
 #pragma unroll
                 for (int term = 0; term < 3; ++term) {
@@ -572,7 +499,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     }
                 }
                 tc::mma_commit(PVDONE + 8 * (gp & 1));
-                tc::mma_commit(EMPTYV + 8 * (gp % NVS));
+                tc::mma_commit(EMPTY + 8 * sl);
                 return true;
             };
             for (uint32_t k = 0; ok; ++k) {
@@ -590,7 +517,8 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 }
                 tc::fence_after_sync();
                 for (uint32_t t = 0; t < ntiles; ++t, ++g) {
-                    if (!converted(g)) {
+                    const uint32_t hk = 2 * g;
+                    if (!converted(hk)) {
                         timeout();
                         ok = false;
                         break;
@@ -601,7 +529,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     }
                     tc::fence_after_sync();
                     // S = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
-                    const uint32_t sl = g % NKS;
+                    const uint32_t sl = hk % NSLOT;
                     const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF;
 #pragma unroll
                     for (int term = 0; term < 3; ++term) {
@@ -616,7 +544,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                         }
                     }
                     tc::mma_commit(SFULL + 8 * (g & 1));
-                    tc::mma_commit(EMPTYK + 8 * sl);  // K slot free once QK has read it
+                    tc::mma_commit(EMPTY + 8 * sl);  // K slot free once QK has read it
                     // one buffer: this tile's PV next; two: the previous tile's
                     if (NBUF == 1) {
                         if (!issue_pv(t, g)) {
@@ -682,19 +610,6 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             float m = -CUDART_INF_F, l = 0.f;
             bool failed = false;
             for (uint32_t t = 0; t < ntiles; ++t, ++g) {
-                // V(g), while QK(g) runs: this warp's cycles of the in-place
-                // transpose (see v_transpose_warp)
-                {
-                    const uint32_t vs = NKS + g % NVS;
-                    if (!mbar_wait(FULLV + 8 * (g % NVS), (g / NVS) & 1)) {
-                        timeout();
-                        failed = true;
-                        break;
-                    }
-                    uint8_t* hib = smem + vs * C::SLOT;
-                    v_transpose_warp<C::KB, NB>(hib, hib + C::BUF, meta[4 * vs + 0], warp, lane);
-                    tc::fence_proxy_async_smem();
-                }
                 if (!mbar_wait(SFULL + 8 * (g & 1), (g >> 1) & 1)) {
                     timeout();
                     failed = true;
