@@ -97,9 +97,12 @@ struct KCfg {
     static constexpr int THREADS = CONS + 128;
     static constexpr int WARP_TMA = 4, WARP_PREP = 5, WARP_MERGE = 6;
     // registers per thread: launched at 128 (two CTAs per SM), then moved from
-    // warpgroup 1 to warpgroup 0: 128 * REG_CONS + 128 * REG_HELP = 256 * 128
-    static constexpr int REG_CONS = 184;
-    static constexpr int REG_HELP = 72;
+    // warpgroup 1 to warpgroup 0: 128 * REG_CONS + 128 * REG_HELP = 256 * 128.
+    // (200 / 56 leaves the consumers of the eight-heads-per-kv-head shapes
+    // almost spill-free; the merge warp keeps four loads in flight to live
+    // in 56.)
+    static constexpr int REG_CONS = 200;
+    static constexpr int REG_HELP = 56;
     static constexpr int T = tile_keys(HD);       // keys per tile
     // elements per lane: keep G*E <= 64 (queries + accumulators in registers)
     static constexpr int E = cmax(4, cmax(HD / 32, cmin(32, pow2_floor(64 / G))));
@@ -1277,7 +1280,7 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                                     P.sinks ? P.sinks + hq0 + h0 : nullptr, lane, Mh, Lh);
                     // outputs: lanes over the hd/4 float4 columns (every lane
                     // runs every iteration: the shuffles name the whole warp),
-                    // one head at a time, 8 splits' loads in flight per round
+                    // one head at a time, 4 splits' loads in flight per round
 #pragma unroll
                     for (int h = 0; h < HG; ++h) {
                         if (h >= nh) break;
@@ -1296,17 +1299,17 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                                 // this lane's split's weight; lanes past the end weigh 0
                                 const float wl = mine < nsplit ? exp2f(__ldcg(wsm + mine * 2) - Mhh) : 0.f;
                                 const uint32_t n = nsplit - r0 < 32u ? nsplit - r0 : 32u;
-                                for (uint32_t i0 = 0; i0 < n; i0 += 8) {
-                                    float4 v[8];
+                                for (uint32_t i0 = 0; i0 < n; i0 += 4) {
+                                    float4 v[4];
 #pragma unroll
-                                    for (int u = 0; u < 8; ++u) {
+                                    for (int u = 0; u < 4; ++u) {
                                         v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                                         if (act && i0 + u < n)
                                             v[u] = __ldcg(reinterpret_cast<const float4*>(
                                                               wsa + (r0 + i0 + u) * HD) + d4);
                                     }
 #pragma unroll
-                                    for (int u = 0; u < 8; ++u) {
+                                    for (int u = 0; u < 4; ++u) {
                                         const float w = __shfl_sync(0xffffffffu, wl, (i0 + u) & 31);
                                         a.x = __fmaf_rn(w, v[u].x, a.x);
                                         a.y = __fmaf_rn(w, v[u].y, a.y);
