@@ -15,7 +15,7 @@ LIB = os.path.join(HERE, "libslotkv.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = ["slotkv.cu", "decode_attn_hd64.cu", "decode_attn_hd128.cu", "decode_attn_hd256.cu",
            "noalloc.cu", "prefill_tc_hd64.cu", "prefill_tc_hd128.cu"]
-DEPS = ["params.h", "decode_attn.cuh", "prefill_tc.cuh", "tc_ops.cuh"]
+DEPS = ["params.h", "decode_attn.cuh", "decode_small.cuh", "prefill_tc.cuh", "tc_ops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE] + ARCH
 

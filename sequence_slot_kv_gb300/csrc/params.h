@@ -119,6 +119,14 @@ int launch_decode_hd128(int G, const DecodeParams& p, const CUtensorMap& tmK,
 int launch_decode_hd256(int G, const DecodeParams& p, const CUtensorMap& tmK,
                         const CUtensorMap& tmV, unsigned ctas, cudaStream_t stream);
 
+// The small-call decode kernel (one CTA per (row, kv head), see
+// decode_small.cuh): taken when a decode call has at most two CTAs' worth
+// of (row, kv head) pairs per SM and slots of at most small_max_keys keys.
+int launch_small_hd64(int G, const DecodeParams& p, cudaStream_t stream);
+int launch_small_hd128(int G, const DecodeParams& p, cudaStream_t stream);
+int launch_small_hd256(int G, const DecodeParams& p, cudaStream_t stream);
+__host__ __device__ constexpr int small_max_keys(int hd) { return 8 * tile_keys(hd); }
+
 // Tensor-core prefill launchers (prep, plan, attention on `stream`); tmK and
 // tmV are the 128-byte-swizzled views of the slot buffers with a box of 32
 // floats x prefill_tile_keys(hd) rows.  Return a cudaError_t value.

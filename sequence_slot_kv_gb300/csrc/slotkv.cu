@@ -261,10 +261,27 @@ uint32_t auto_chunk(const slotkv_s* h, uint32_t B, uint64_t max_keys) {
 // whether the plan kernel runs, and the kernels launched.
 struct CallShape {
     uint32_t chunk, ctas, static_items, static_second, no_plan, kernels;
+    uint32_t small;  // the small-call kernel (one CTA per (row, kv head))
 };
 
-CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill) {
+CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill,
+                     bool paged = false) {
     CallShape c;
+    c.small = 0;
+    // a few rows over short slots: one CTA per (row, kv head), no persistent
+    // pipeline to set up (the stall test option needs the pipeline's waits)
+    const uint64_t sms = (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
+    if (!prefill && !paged && !(h->options & SLOTKV_OPT_TEST_STALL) &&
+        (uint64_t)B * h->n_kv_head <= 2 * sms &&
+        max_keys <= (uint64_t)slotkv::small_max_keys((int)h->head_dim)) {
+        c.small = 1;
+        c.chunk = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+        c.ctas = B * h->n_kv_head;
+        c.static_items = c.static_second = 0;
+        c.no_plan = 1;
+        c.kernels = 1;
+        return c;
+    }
     if (prefill && h->tc_prefill) {
         // prep, plan and the persistent tensor-core kernel (one CTA per SM)
         c.chunk = (uint32_t)slotkv::prefill_tile_keys((int)h->head_dim);
@@ -326,7 +343,7 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.n_kv_head = h->n_kv_head;
     P.B = B;
     const uint64_t max_keys = block_tables ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
-    const CallShape cs = call_shape(h, B, max_keys, prefill);
+    const CallShape cs = call_shape(h, B, max_keys, prefill, block_tables != nullptr);
     P.chunk_min = cs.chunk;
     P.max_splits = h->max_splits;
     P.eps = eps;
@@ -338,6 +355,15 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.static_second = cs.static_second;
     P.no_plan = cs.no_plan;
     int rc;
+    if (cs.small) {
+        switch (h->head_dim) {
+            case 64: rc = slotkv::launch_small_hd64(G, P, stream); break;
+            case 128: rc = slotkv::launch_small_hd128(G, P, stream); break;
+            default: rc = slotkv::launch_small_hd256(G, P, stream); break;
+        }
+        if (rc != 0) return cuda_fail((cudaError_t)rc, "small decode kernel launch");
+        return SLOTKV_OK;
+    }
     switch (h->head_dim) {
         case 64: rc = slotkv::launch_decode_hd64(G, P, h->tmK, h->tmV, ctas, stream); break;
         case 128: rc = slotkv::launch_decode_hd128(G, P, h->tmK, h->tmV, ctas, stream); break;
@@ -891,7 +917,7 @@ int slot_kv_call_shape(slotkv_t h, uint32_t B, uint32_t bt_stride, uint32_t pref
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
     if (B == 0 || B > h->max_rows) return fail(SLOTKV_ERR_ARG, "B=%u outside 1..max_rows", B);
     const uint64_t max_keys = bt_stride ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
-    const CallShape cs = call_shape(h, B, max_keys, prefill != 0);
+    const CallShape cs = call_shape(h, B, max_keys, prefill != 0, bt_stride != 0);
     if (chunk_keys) *chunk_keys = cs.chunk;
     if (ctas) *ctas = cs.ctas;
     if (kernels) *kernels = cs.kernels;
