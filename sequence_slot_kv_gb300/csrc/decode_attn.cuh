@@ -626,6 +626,49 @@ __device__ __forceinline__ float partial_weight(float m, float M) {
     return m == -CUDART_INF_F ? 0.f : exp2f(m - M);
 }
 
+// Merge the (m, l, acc) states of a warp's 32 / L key groups by halving: at
+// each level a lane keeps half of its elements (the upper half if its group
+// bit is set) and takes its partner group's share of that half, so afterwards
+// lane (li, group bits) holds, for every head, the warp's merged elements
+// e0 .. e0 + hd/32 - 1 of its slice in acc[h][0 .. hd/32); e0 is returned.
+// m and l are merged in one fixed order (lower group first) and stay equal on
+// all lanes.  All 32 lanes call it together.
+template <int G, int E, int L>
+__device__ __forceinline__ int merge_warp_groups(const int lane, float (&m)[G], float (&l)[G],
+                                                 float (&acc)[G][E]) {
+    int e0 = 0;
+#pragma unroll
+    for (int off = L, cnt = E; off < 32; off <<= 1, cnt >>= 1) {
+        const bool upper = (lane & off) != 0;
+        float c_lo[G], c_hi[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+            const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+            const float m_lo = upper ? mo : m[h], m_hi = upper ? m[h] : mo;
+            const float l_lo = upper ? lo : l[h], l_hi = upper ? l[h] : lo;
+            const float M = fmaxf(m_lo, m_hi);
+            c_lo[h] = partial_weight(m_lo, M);
+            c_hi[h] = partial_weight(m_hi, M);
+            l[h] = __fmaf_rn(l_lo, c_lo[h], __fmul_rn(l_hi, c_hi[h]));
+            m[h] = M;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int i = 0; i < cnt / 2; ++i) {
+                const float send = upper ? acc[h][i] : acc[h][i + cnt / 2];
+                const float keep = upper ? acc[h][i + cnt / 2] : acc[h][i];
+                const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+                const float v_lo = upper ? recv : keep, v_hi = upper ? keep : recv;
+                acc[h][i] = __fmaf_rn(v_lo, c_lo[h], __fmul_rn(v_hi, c_hi[h]));
+            }
+        }
+        e0 += upper ? cnt / 2 : 0;
+    }
+    return e0;
+}
+
 // ------------------------------------------------ per-warp vector routines
 // Shared by the decode kernel's prep warp and the prefill KV-write kernel, so
 // both produce bit-identical vectors.  A lane owns the rotation pairs
@@ -1524,43 +1567,8 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
         }
 
         // ------------------------------------ merge the groups of each warp
-        // Halving: at each level a lane keeps half of its elements (the upper
-        // half if its group bit is set) and takes its partner group's share of
-        // that half, so afterwards lane (li, group bits) holds, for every head,
-        // the warp's merged elements e0 .. e0 + EF - 1 of its slice in
-        // acc[h][0 .. EF), EF = hd / 32.  m and l are merged in one fixed
-        // order (lower group first) and stay equal on all lanes.
         constexpr int EF = HD / 32;
-        int e0 = 0;
-#pragma unroll
-        for (int off = L, cnt = E; off < 32; off <<= 1, cnt >>= 1) {
-            const bool upper = (lane & off) != 0;
-            float c_lo[G], c_hi[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
-                const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
-                const float m_lo = upper ? mo : m[h], m_hi = upper ? m[h] : mo;
-                const float l_lo = upper ? lo : l[h], l_hi = upper ? l[h] : lo;
-                const float M = fmaxf(m_lo, m_hi);
-                c_lo[h] = partial_weight(m_lo, M);
-                c_hi[h] = partial_weight(m_hi, M);
-                l[h] = __fmaf_rn(l_lo, c_lo[h], __fmul_rn(l_hi, c_hi[h]));
-                m[h] = M;
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-#pragma unroll
-                for (int i = 0; i < cnt / 2; ++i) {
-                    const float send = upper ? acc[h][i] : acc[h][i + cnt / 2];
-                    const float keep = upper ? acc[h][i + cnt / 2] : acc[h][i];
-                    const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-                    const float v_lo = upper ? recv : keep, v_hi = upper ? keep : recv;
-                    acc[h][i] = __fmaf_rn(v_lo, c_lo[h], __fmul_rn(v_hi, c_hi[h]));
-                }
-            }
-            e0 += upper ? cnt / 2 : 0;
-        }
+        const int e0 = merge_warp_groups<G, E, L>(lane, m, l, acc);
         // element t < EF of this lane's slice sits at dimension dim(t) of a head
         // (pairs t, t + 1 are adjacent: EF and e0 are even)
         auto dim = [&](int t) { return ((e0 + t) >> 2) * 4 * L + 4 * li + ((e0 + t) & 3); };

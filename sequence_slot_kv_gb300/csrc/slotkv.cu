@@ -264,14 +264,16 @@ struct CallShape {
     uint32_t small;  // the small-call kernel (one CTA per (row, kv head))
 };
 
-CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill,
-                     bool paged = false) {
+CallShape call_shape(const slotkv_s* h, uint32_t B, uint64_t max_keys, bool prefill) {
     CallShape c;
     c.small = 0;
     // a few rows over short slots: one CTA per (row, kv head), no persistent
-    // pipeline to set up (the stall test option needs the pipeline's waits)
+    // pipeline to set up.  Only under the default policy, whose bits may
+    // already depend on the batch's shape (a fixed policy promises a row the
+    // same bits in any batch); the stall test option needs the pipeline's
+    // waits.  Slot and paged calls of the same capacity take the same path.
     const uint64_t sms = (uint64_t)(h->sm_count > 0 ? h->sm_count : 1);
-    if (!prefill && !paged && !(h->options & SLOTKV_OPT_TEST_STALL) &&
+    if (!prefill && h->auto_split && !(h->options & SLOTKV_OPT_TEST_STALL) &&
         (uint64_t)B * h->n_kv_head <= 2 * sms &&
         max_keys <= (uint64_t)slotkv::small_max_keys((int)h->head_dim)) {
         c.small = 1;
@@ -343,7 +345,7 @@ int launch(slotkv_s* h, uint32_t B, uint32_t n_head, const float* q, const float
     P.n_kv_head = h->n_kv_head;
     P.B = B;
     const uint64_t max_keys = block_tables ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
-    const CallShape cs = call_shape(h, B, max_keys, prefill, block_tables != nullptr);
+    const CallShape cs = call_shape(h, B, max_keys, prefill);
     P.chunk_min = cs.chunk;
     P.max_splits = h->max_splits;
     P.eps = eps;
@@ -917,7 +919,7 @@ int slot_kv_call_shape(slotkv_t h, uint32_t B, uint32_t bt_stride, uint32_t pref
     if (!valid_handle(h)) return fail(SLOTKV_ERR_STATE, "handle is not allocated");
     if (B == 0 || B > h->max_rows) return fail(SLOTKV_ERR_ARG, "B=%u outside 1..max_rows", B);
     const uint64_t max_keys = bt_stride ? (uint64_t)bt_stride * h->slot_ctx : h->slot_ctx;
-    const CallShape cs = call_shape(h, B, max_keys, prefill != 0, bt_stride != 0);
+    const CallShape cs = call_shape(h, B, max_keys, prefill != 0);
     if (chunk_keys) *chunk_keys = cs.chunk;
     if (ctas) *ctas = cs.ctas;
     if (kernels) *kernels = cs.kernels;

@@ -311,16 +311,17 @@ def test_paged_argument_errors():
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 def test_paged_host_entry_matches_device_entry_and_oracle(pinned):
     """decode_batch_attn_paged_host (inputs, tables and out in host memory)
-    against the device entry on the same pool, bit for bit, and against the
-    paged oracle; twice, so the second call reuses the table staging, and a
-    wider table grows it."""
+    against the device entry with the same table on the same pool, bit for
+    bit, and against the paged oracle; twice, so the second call reuses the
+    table staging, and a wider table grows it.  (The table's width is the
+    call's context capacity, which the default policy may size its work
+    from -- here the narrow table takes the small-call kernel, the wide one
+    the persistent kernel -- so each width is compared with its own device
+    call.)"""
     w, bs = small_paged_workload(128, 4, 1, 40, sinks=True)
     run_d = PagedRun(w, bs)
     run_h = PagedRun(w, bs)
     try:
-        want = run_d.step(0)
-        torch.cuda.synchronize()
-        assert run_d.kv.get_status() == 0
         Kr, Vr = host_pool(w, bs)
         ref, skipped = oracle_paged(w, bs, Kr, Vr, run_d.tables_np)
         assert skipped == 0
@@ -333,8 +334,13 @@ def test_paged_host_entry_matches_device_entry_and_oracle(pinned):
             tab = np.full((w.B, width), 2**31 - 1, dtype=np.int32)
             tab[:, :run_d.tables_np.shape[1]] = run_d.tables_np
             K0, V0 = run_h.fresh_pool()
-            run_h.K.copy_(K0)
-            run_h.V.copy_(V0)
+            for r in (run_d, run_h):
+                r.K.copy_(K0)
+                r.V.copy_(V0)
+            del K0, V0
+            want = run_d.step(0, tables=to_dev(tab))
+            torch.cuda.synchronize()
+            assert run_d.kv.get_status() == 0
             out = host(np.full((w.B, w.n_head, w.head_dim), np.nan, dtype=np.float32))
             run_h.kv.decode_batch_attn_paged_host(hq, hk, hv, hp, host(tab), run_h.qw, run_h.kw,
                                                   run_h.inv, run_h.sinks, out, w.eps, w.scale)
