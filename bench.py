@@ -50,8 +50,9 @@ FLUSH_BYTES = 256 * 1024 * 1024  # written between calls of a step that fits in 
 MEASURED_TRAFFIC = {
     # all at full size; large's is its first step's ratio to the algorithmic
     # bytes times the mean algorithmic bytes of its 64 steps
-    "f55bc892aa55a62a": {"mid": 551_971_968, "sinks": 2_336_639_488,
-                         "skewed": 17_227_313_024, "large": 2_238_903_123},
+    # (plan + decode kernel bytes, the mean of two calls)
+    "4e8294f487abe411": {"mid": 551_830_912, "sinks": 2_336_513_024,
+                         "skewed": 17_227_054_208, "large": 2_238_835_960},
 }
 
 
@@ -420,11 +421,26 @@ class DeviceWorkload:
         torch.cuda.empty_cache()
 
 
+GROUP_CALLS = 64   # calls between two events of the timed region
+
+
 def time_device(dw, steps, warmup, local, world, graph=False):
-    """Time ``steps`` steps of ``dw`` on its stream with CUDA events, each call
-    bracketed by its own pair of events.  The warm-up runs directly before
-    the timed region (no idle gap in which clocks could drop), with the clock
-    sampler already running.  Returns (total_ms, per-call ms, clocks)."""
+    """Time ``steps`` steps of ``dw`` on its stream with CUDA events.  The
+    warm-up runs directly before the timed region (no idle gap in which
+    clocks could drop), with the clock sampler already running.
+
+    Calls run back to back, as a decode loop runs them: events are recorded
+    only at the boundaries of groups of about GROUP_CALLS calls (whole
+    steps).  An event between two calls would serialise the stream there
+    (about 4 us a call on GB300) and keep the next call's plan kernel from
+    launching during the previous call's tail.  The per-call samples are the
+    groups' mean call times.
+
+    A workload whose bytes fit in L2 twice over would be timed warm: a buffer
+    larger than L2 is written before every call, outside a pair of events
+    around the call, and the step time is the sum of the calls' times.
+
+    Returns (total_ms, calls, per-call ms samples, clocks)."""
     import torch
     dev, stream = dw.dev, dw.stream
     nsub = dw.nsub
@@ -443,9 +459,6 @@ def time_device(dw, steps, warmup, local, world, graph=False):
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
                 dw.one_step()
-    # A step whose bytes fit in L2 twice over would be timed warm: write a
-    # buffer larger than L2 between calls (outside their events) and take the
-    # value from the summed per-call times instead.
     flush = None
     if statistics.mean(dw.bytes_per_launch) < 2 * L2_BYTES:
         flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -458,50 +471,64 @@ def time_device(dw, steps, warmup, local, world, graph=False):
     assert dw.kv.get_status(dw.sp) == 0
     for _ in range(2):       # warm again after the status read, right before timing
         g.replay() if g is not None else dw.one_step()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps * (1 if g is not None else nsub))]
-    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    clocks.mark("begin")
-    begin.record(stream)
-    i = 0
-    with torch.cuda.stream(stream):
-        for _ in range(steps):
-            for t in range(1 if g is not None else nsub):
-                if flush is not None:
-                    flush.fill_(float(i))
-                ev[i][0].record(stream)
-                g.replay() if g is not None else dw.decode(t)
-                ev[i][1].record(stream)
-                i += 1
-    end.record(stream)
-    barrier()
-    clocks.mark("end")
-    clk = clocks.stop()
-    total_ms = begin.elapsed_time(end)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if g is not None:
-        launch_ms = [x / nsub for x in launch_ms]
+    calls = steps * nsub
+    event = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     if flush is not None:
-        total_ms = sum(launch_ms) * (nsub if g is not None else 1)  # flushes are not the step's
+        # one (flush, timed unit) per call, or per replay of a captured step
+        units = steps if g is not None else calls
+        ev = [(event(), event()) for _ in range(units)]
+        barrier()
+        clocks.mark("begin")
+        with torch.cuda.stream(stream):
+            for i in range(units):
+                flush.fill_(float(i))
+                ev[i][0].record(stream)
+                g.replay() if g is not None else dw.decode(i % nsub)
+                ev[i][1].record(stream)
+        barrier()
+        clocks.mark("end")
+        unit_ms = [a.elapsed_time(b) for a, b in ev]
+        total_ms = sum(unit_ms)  # the flushes are not the step's
+        samples = [x / nsub for x in unit_ms] if g is not None else unit_ms
         del flush
+    else:
+        group = max(1, -(-GROUP_CALLS // nsub))  # steps per group
+        marks = [event() for _ in range(-(-steps // group) + 1)]
+        barrier()
+        clocks.mark("begin")
+        with torch.cuda.stream(stream):
+            for s in range(steps):
+                if s % group == 0:
+                    marks[s // group].record(stream)
+                g.replay() if g is not None else dw.one_step()
+            marks[-1].record(stream)
+        barrier()
+        clocks.mark("end")
+        total_ms = marks[0].elapsed_time(marks[-1])
+        samples = []
+        for k in range(len(marks) - 1):
+            n = (min(steps, (k + 1) * group) - k * group) * nsub
+            samples.append(marks[k].elapsed_time(marks[k + 1]) / n)
+    clk = clocks.stop()
     assert dw.kv.get_status(dw.sp) == 0
-    return total_ms, launch_ms, clk
+    return total_ms, calls, samples, clk
 
 
-def roofline_of(dw, launch_ms, workload_name, traffic=None):
-    """The decode call's roofline entry: algorithmic bytes over the mean
-    per-call time, against the measured copy bandwidth."""
+def roofline_of(dw, total_ms, calls, samples, traffic=None):
+    """The decode call's roofline entry: algorithmic bytes over the mean call
+    time (the timed region over its calls), against the measured copy
+    bandwidth; the median over the per-call samples beside it."""
     peak, peak_kind = peak_hbm()
-    mean_s = statistics.mean(launch_ms) / 1e3
+    mean_s = total_ms / calls / 1e3
+    med_s = statistics.median(samples) / 1e3
     alg = statistics.mean(dw.bytes_per_launch)
     achieved = alg / mean_s / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
             "traffic_per_alg_byte": (traffic / alg if traffic else None),
             "alg_bytes_per_launch": alg, "avg_launch_us": mean_s * 1e6,
-            "median_launch_us": statistics.median(launch_ms) * 1e3,
-            "median_frac": alg / (statistics.median(launch_ms) / 1e3) / 1e9 / peak,
+            "median_launch_us": med_s * 1e6,
+            "median_frac": alg / med_s / 1e9 / peak,
             "kernel": "slotkv_plan_kernel + slotkv_decode_attn_kernel (one decode call)"}
 
 
@@ -564,12 +591,12 @@ def per_config_entry(name, args, dev, stream, local):
     w = synth.WORKLOADS[name]
     dw = DeviceWorkload(w, dev, stream, split=args.split)
     try:
-        est_ms, _, _ = time_device(dw, 3, 1, local, 1)
+        est_ms, _, _, _ = time_device(dw, 3, 1, local, 1)
         steps = max(args.steps, int(np.ceil(MIN_REGION_S * 1e3 / max(est_ms / 3, 1e-3))))
-        total_ms, launch_ms, clk = time_device(dw, steps, args.warmup, local, 1)
-        rl = roofline_of(dw, launch_ms, name, traffic=measured_traffic(name))
+        total_ms, calls, samples, clk = time_device(dw, steps, args.warmup, local, 1)
+        rl = roofline_of(dw, total_ms, calls, samples, traffic=measured_traffic(name))
         return {"value": w.B * dw.nsub * steps / (total_ms / 1e3), "unit": "rows/s",
-                "steps": steps, "calls": len(launch_ms), "ms_per_step": total_ms / steps,
+                "steps": steps, "calls": calls, "ms_per_step": total_ms / steps,
                 "avg_launch_us": rl["avg_launch_us"],
                 "median_launch_us": rl["median_launch_us"],
                 "alg_bytes_per_launch": rl["alg_bytes_per_launch"],
@@ -610,8 +637,8 @@ def run_gpu(args, w):
 
     dw = DeviceWorkload(w, dev, stream, paged=args.paged, split=args.split,
                         options=args.options)
-    total_ms, launch_ms, clk = time_device(dw, args.steps, args.warmup, local, world,
-                                           graph=args.graph)
+    total_ms, calls, samples, clk = time_device(dw, args.steps, args.warmup, local, world,
+                                                graph=args.graph)
     total_ms = max_over_ranks(total_ms, dev)
     rows_per_step = w.B * dw.nsub
     value = whole_job_rows_per_s(rows_per_step, args.steps, world, total_ms / 1e3)
@@ -626,7 +653,7 @@ def run_gpu(args, w):
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(w, args),
-        "roofline": roofline_of(dw, launch_ms, w.name, traffic),
+        "roofline": roofline_of(dw, total_ms, calls, samples, traffic),
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         # the library's kernels per decode call (plan + decode, or decode alone)
@@ -639,7 +666,7 @@ def run_gpu(args, w):
         rl = line["roofline"]
         headline_entry = {
             "value": value, "unit": "rows/s", "steps": args.steps,
-            "calls": len(launch_ms), "ms_per_step": total_ms / args.steps,
+            "calls": calls, "ms_per_step": total_ms / args.steps,
             "avg_launch_us": rl["avg_launch_us"], "median_launch_us": rl["median_launch_us"],
             "alg_bytes_per_launch": rl["alg_bytes_per_launch"], "achieved_GBps": rl["achieved"],
             "frac": rl["frac"], "median_frac": rl["median_frac"], "traffic": rl["traffic"],

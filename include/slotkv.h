@@ -164,6 +164,18 @@ int slot_kv_geometry(slotkv_t handle, uint32_t* n_slots, uint32_t* slot_ctx,
  * SLOTKV_ERR_UNSUPPORTED (G outside 1..8), SLOTKV_ERR_CUDA (launch failure,
  * including a GPU on which two of the persistent decode CTAs do not fit on
  * one SM).
+ *
+ * Which kernels run (slot_kv_call_shape reports it): under the default split
+ * policy, a call of at most two CTAs' worth of (row, kv head) pairs per SM
+ * over slots of at most 8 * 4096 / hd keys runs one CTA per pair; any other
+ * call runs a plan kernel and the persistent decode kernel (the decode kernel
+ * alone when every row fits in one chunk and the pairs fit in its CTAs).
+ * Stream order holds as for any kernel, with one addition: the persistent
+ * decode kernel lets a programmatic dependent launch (a kernel launched with
+ * cudaLaunchAttributeProgrammaticStreamSerialization right after the call)
+ * once every CTA has run out of work, before the kernel has finished; such a
+ * dependent must wait for it (cudaGridDependencySynchronize) before reading
+ * out, K or V.  The next call's plan kernel is such a dependent, and waits.
  */
 int decode_batch_attn(slotkv_t handle, uint32_t B, uint32_t n_head, const float* q,
                       const float* k_new, const float* v_new, const uint32_t* positions,

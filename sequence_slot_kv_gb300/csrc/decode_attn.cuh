@@ -757,6 +757,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) slotkv_plan_kernel(const Deco
     __shared__ uint32_t sh_p[kPlanThreads], sh_prow[kPlanThreads], sh_meta[kPlanThreads];
     __shared__ uint32_t sh_fb[kPlanThreads], sh_lb[kPlanThreads];
     __shared__ uint32_t sh_nf[kPlanThreads], sh_nl[kPlanThreads];
+    // The plan kernel is a programmatic dependent of whatever precedes it on
+    // the stream (the previous call's decode kernel lets it launch once every
+    // CTA of that grid has run out of items): nothing may be read before the
+    // preceding grid has finished.  The decode kernel may launch from here on.
+    grid_dependency_wait();
     grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t nkv = P.n_kv_head;
@@ -1160,6 +1165,10 @@ __global__ void __launch_bounds__(KCfg<HD, G>::THREADS, 2)
                 if (!planned) await_plan();
                 it_n = atomicAdd(P.plan + 1, 1u);
                 claimed = true;
+                // nothing left for this CTA: the next call's plan kernel may
+                // launch once every CTA is here (it waits for this grid to
+                // finish before it reads anything)
+                if (it_n >= n_items) grid_launch_dependents();
             };
             uint4 rec_n = make_uint4(0, 0, 0, 0);
             bool rec_n_loaded = false;
@@ -1745,9 +1754,18 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
         slotkv_write_kv_kernel<HD><<<(warps + 3) / 4, 128, 0, stream>>>(p);
     }
     cudaError_t e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (!p.no_plan) {
-        slotkv_plan_kernel<C::T><<<1, kPlanThreads, 0, stream>>>(p);
-        e = cudaGetLastError();
+        // a programmatic dependent of the preceding work (see the plan kernel)
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(1);
+        pc.blockDim = dim3(kPlanThreads);
+        pc.stream = stream;
+        pc.attrs = attr;
+        pc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&pc, slotkv_plan_kernel<C::T>, p);
         if (e != cudaSuccess) return static_cast<int>(e);
     }
     cudaLaunchConfig_t cfg = {};
@@ -1755,9 +1773,6 @@ int launch_one(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap&
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.no_plan ? 0 : 1;  // programmatic dependent of the plan kernel
     e = cudaLaunchKernelEx(&cfg, slotkv_decode_attn_kernel<HD, G>, tmK, tmV, p);
