@@ -24,7 +24,7 @@
 //         and then V (BK = 64 keys x hd, 128-byte swizzled boxes of 32
 //         floats) with TMA into a ring of half-stage slots (one operand's
 //         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
-//       - warps 6-7 (converters): split each landed K tile in place into
+//       - warps 6-9 (converters): split each landed K tile in place into
 //         hi and lo operand buffers, and transpose each landed V tile into
 //         a keys-contiguous layout while splitting it (TF32 MMA operands
 //         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
@@ -70,9 +70,9 @@ struct PCfg {
     static constexpr int KB = BK / 32;
     static constexpr int VT_BLK = HD * 128;
     static constexpr int NSW = 4;               // softmax warps
-    static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 2;
+    static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 4;
     static constexpr int SB_PER_WARP = KB * NB / NCONV;  // V sub-blocks per converter warp
-    static constexpr int THREADS = 256;
+    static constexpr int THREADS = 32 * (WARP_CONV + NCONV);
     // tensor memory columns: Q hi | Q lo | O | NBUF buffers of (S, then P hi
     // over it | P lo)
     static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_O = 2 * HD, C_S = 3 * HD;
@@ -91,14 +91,14 @@ struct PCfg {
     static constexpr int NBAR = 3 * NSLOT + 12;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
-    static constexpr int SMEM_USED = OFF_MISC + 16;
+    // misc[0]: abort; misc[2 + w]: converter warp w's stop flag
+    static constexpr int SMEM_USED = OFF_MISC + 4 * (2 + NCONV);
     static constexpr int SMEM = SMEM_USED + 1024;   // slack to align the ring to 1 KiB
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(BLK % 1024 == 0 && SLOT % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
     static constexpr uint32_t IDESC_QK = tc::idesc_tf32(M, BK, false);
     static constexpr uint32_t IDESC_PV = tc::idesc_tf32(M, HD, false);
     static_assert(KB * NB == SB_PER_WARP * NCONV, "V sub-blocks split evenly over the converters");
-    static_assert(NCONV == 2, "the converters' stop flags are misc[2], misc[3]");
 };
 
 // Named barrier 2 over the converter warps (N threads).
@@ -394,15 +394,18 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         constexpr int NT = C::NCONV * 32;
         for (uint32_t h = 0;; ++h) {
             const uint32_t sl = h % NSLOT;
-            // Both converter warps meet at named barriers below, so they must
-            // stop at the same half-tile: each publishes its own reason to
-            // stop (a wait that expired, an abort, the end marker) and both
-            // decide from the two published flags.
+            // The converter warps meet at named barriers below, so they must
+            // all stop at the same half-tile: each publishes its own reason
+            // to stop (a wait that expired, an abort, the end marker) and all
+            // decide from the published flags.
             const bool ok = mbar_wait(FULL + 8 * sl, (h / NSLOT) & 1);
             if (!ok) timeout();
             if (lane == 0) misc[2 + w] = (!ok || misc[0] || meta[4 * sl + 1]) ? 1 : 0;
             named_sync_conv<NT>();
-            if (misc[2] | misc[3]) break;
+            int stop = 0;
+#pragma unroll
+            for (int w2 = 0; w2 < C::NCONV; ++w2) stop |= misc[2 + w2];
+            if (stop) break;
             const uint32_t rows = meta[4 * sl + 0];
             uint8_t* hib = smem + sl * C::SLOT;
             uint8_t* lob = hib + C::BUF;
