@@ -410,22 +410,28 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             uint8_t* hib = smem + sl * C::SLOT;
             uint8_t* lob = hib + C::BUF;
             if ((h & 1) == 0) {
-                // K: hi in place, lo beside it (both K-major, as TMA laid them)
+                // K: the landed f32 tile is its own hi part (the tensor core
+                // reads a TF32 operand's f32 bits with the low 13 mantissa
+                // bits ignored, i.e. as x & 0xFFFFE000), so only the lo part
+                // is written beside it (K-major, as TMA laid the tile out);
+                // rows past the item's last key are zeroed in both
                 float4* hi = reinterpret_cast<float4*>(hib);
                 float4* lo = reinterpret_cast<float4*>(lob);
 #pragma unroll
                 for (int i = ct; i < C::BUF / 16; i += NT) {
                     // each 128-byte row of a column block is 8 float4s
                     const uint32_t row = static_cast<uint32_t>(i % (C::BLK / 16)) / 8;
-                    float4 x = hi[i];
-                    if (row >= rows) x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row >= rows) {
+                        hi[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        lo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        continue;
+                    }
+                    const float4 x = hi[i];
                     uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
                     tf32_split(x.x, h0, l0);
                     tf32_split(x.y, h1, l1);
                     tf32_split(x.z, h2, l2);
                     tf32_split(x.w, h3, l3);
-                    hi[i] = make_float4(__uint_as_float(h0), __uint_as_float(h1),
-                                        __uint_as_float(h2), __uint_as_float(h3));
                     lo[i] = make_float4(__uint_as_float(l0), __uint_as_float(l1),
                                         __uint_as_float(l2), __uint_as_float(l3));
                 }
