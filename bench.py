@@ -534,8 +534,11 @@ def roofline_of(dw, total_ms, calls, samples, traffic=None):
 
 def time_e2e(dw, steps, warmup, world):
     """The same metric end to end: every step copies its inputs from pinned
-    host memory and reads the output back through the host entry
-    (decode_batch_attn_host, or decode_batch_attn_paged_host)."""
+    host memory and reads the output back, through prepared host calls
+    (SlotKV.prepare_host_call: the host entry decode_batch_attn_host, or
+    decode_batch_attn_paged_host, with its arguments checked once, as a
+    serving loop that reuses its pinned buffers would call it).  The calls
+    are prepared before the timed region; each run is synchronous."""
     import torch
     w, dev, stream, nsub, bs = dw.w, dw.dev, dw.stream, dw.nsub, dw.bs
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -545,12 +548,14 @@ def time_e2e(dw, steps, warmup, world):
     hp = [pin(w.positions(t).astype(np.int32)) for t in range(nsub)]
     hs = pin(dw.tables_np if bs else dw.slots_np)
     hout = torch.empty((w.B, w.n_head, w.head_dim), dtype=torch.float32).pin_memory()
-    call = dw.kv.decode_batch_attn_paged_host if bs else dw.kv.decode_batch_attn_host
+    calls = [dw.kv.prepare_host_call(hq[t], hk[t], hv[t], hp[t], None if bs else hs, dw.qw,
+                                     dw.kw, dw.inv, dw.sinks, hout, w.eps, w.scale,
+                                     block_tables=hs if bs else None)
+             for t in range(nsub)]
 
     def e2e_step():
-        for t in range(nsub):
-            call(hq[t], hk[t], hv[t], hp[t], hs, dw.qw, dw.kw, dw.inv, dw.sinks, hout, w.eps,
-                 w.scale, stream=dw.sp)
+        for c in calls:
+            c(stream=dw.sp)
 
     def barrier():
         if world > 1:
@@ -579,6 +584,8 @@ def time_e2e(dw, steps, warmup, world):
             e2e_step()
         barrier()
         e2e_s = time.perf_counter() - t0
+    for c in calls:
+        c.free()
     h2d = nsub * (hq[0].numel() + hk[0].numel() + hv[0].numel() + hp[0].numel()
                   + hs.numel()) * 4
     d2h = nsub * hout.numel() * 4

@@ -42,6 +42,7 @@ extern "C" {
 #endif
 
 typedef struct slotkv_s* slotkv_t;
+typedef struct slotkv_host_call_s* slotkv_host_call_t;
 typedef void* slotkv_stream_t; /* a cudaStream_t */
 
 enum slotkv_status {
@@ -297,6 +298,37 @@ int decode_batch_attn_paged_host(slotkv_t handle, uint32_t B, uint32_t n_head, c
                                  const float* k_norm_w, const float* inv_freq,
                                  const float* sinks, float* out, float eps, float scale,
                                  slotkv_stream_t stream);
+
+/*
+ * slot_kv_host_call_create / _run / _free -- a prepared host step: the
+ * arguments of decode_batch_attn_host (bt_stride = 0, idx = slots) or of
+ * decode_batch_attn_paged_host (bt_stride >= 1, idx = block_tables), checked
+ * once and with the device aliases of the page-locked host buffers resolved
+ * once, for a serving loop that refills the same host buffers every step
+ * ("Forward Cuda Gemma", decodeBatch, with the per-step inputs in host
+ * memory; "Forward Cuda", the decode graph keyed by its buffers).
+ *   create   checks the arguments as the host entry does (errors as there;
+ *            B >= 1), grows the block-table staging once in paged mode, and
+ *            returns *call (owned by the caller).  Only the pointers are
+ *            kept: the buffers must stay allocated, at the same addresses,
+ *            until the call is freed.
+ *   run      one step on `stream` exactly as the host entry with these
+ *            arguments would run it (the same kernels, the same bits): it
+ *            reads the host buffers' current contents, writes out and K/V,
+ *            and synchronises `stream` before returning.  SLOTKV_ERR_STATE
+ *            once the handle has been freed (slot_kv_free detaches its
+ *            calls), or when another device is current.
+ *   free     releases the call (NULL is a no-op); a handle may be freed
+ *            before or after its calls.
+ */
+int slot_kv_host_call_create(slotkv_t handle, slotkv_host_call_t* call, uint32_t B,
+                             uint32_t n_head, const float* q, const float* k_new,
+                             const float* v_new, const uint32_t* positions,
+                             const uint32_t* idx, uint32_t bt_stride, const float* q_norm_w,
+                             const float* k_norm_w, const float* inv_freq, const float* sinks,
+                             float* out, float eps, float scale);
+int slot_kv_host_call_run(slotkv_host_call_t call, slotkv_stream_t stream);
+int slot_kv_host_call_free(slotkv_host_call_t call);
 
 /*
  * decode_batch_attn_noalloc -- the same decode step as decode_batch_attn for

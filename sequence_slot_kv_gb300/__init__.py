@@ -25,7 +25,7 @@ __all__ = [
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn",
     "decode_batch_attn_paged", "decode_batch_attn_paged_host", "decode_batch_attn_noalloc",
     "slot_kv_advance_positions",
-    "slot_kv_get_status", "slot_kv_set_split", "LIB_PATH", "EXPORTS", "DEV_RANGE",
+    "slot_kv_get_status", "slot_kv_set_split", "HostCall", "LIB_PATH", "EXPORTS", "DEV_RANGE",
     "DEV_TIMEOUT", "OPT_VNORM", "OPT_NORM_PLUS_ONE", "OPT_TEST_STALL",
 ]
 
@@ -68,6 +68,10 @@ EXPORTS = {
     "slot_kv_shard_range": ([_u32, _u32, _u32, ctypes.POINTER(_u32), ctypes.POINTER(_u32)],
                             _int),
     "slot_kv_shard_route": ([_u32, _u32, _u32, _vp, _vp, _vp, _vp], _int),
+    "slot_kv_host_call_create": ([_vp, ctypes.POINTER(_vp), _u32, _u32, _vp, _vp, _vp, _vp, _vp,
+                                  _u32, _vp, _vp, _vp, _vp, _vp, _f32, _f32], _int),
+    "slot_kv_host_call_run": ([_vp, _vp], _int),
+    "slot_kv_host_call_free": ([_vp], _int),
     "slot_kv_last_error": ([], ctypes.c_char_p),
 }
 
@@ -299,6 +303,16 @@ class SlotKV:
             "decode_batch_attn_paged_host")
         return out
 
+    def prepare_host_call(self, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                          inv_freq, sinks, out, eps, scale, block_tables=None):
+        """A prepared host step (slot_kv_host_call_create): the arguments of
+        decode_batch_attn_host -- or, with ``block_tables`` given in place of
+        ``slots`` (pass slots=None), of decode_batch_attn_paged_host --
+        checked once.  Calling the returned HostCall runs one step on the
+        buffers' current contents, synchronously."""
+        return HostCall(self, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
+                        sinks, out, eps, scale, block_tables)
+
     def decode_batch_attn_host(self, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
         """As decode_batch_attn, with q/k_new/v_new/positions/slots/out in host
@@ -388,6 +402,57 @@ def decode_batch_attn_paged(h, q, k_new, v_new, positions, block_tables, q_norm_
                             inv_freq, sinks, out, eps, scale, stream=None):
     return h.decode_batch_attn_paged(q, k_new, v_new, positions, block_tables, q_norm_w,
                                      k_norm_w, inv_freq, sinks, out, eps, scale, stream)
+
+
+class HostCall:
+    """A prepared host step on a SlotKV handle (slot_kv_host_call_create):
+    the host tensors (q, k_new, v_new, positions, slots or block_tables, out;
+    ideally pinned) and the device parameters are checked once and kept
+    referenced; ``call(stream=None)`` runs one synchronous step on their
+    current contents (slot_kv_host_call_run), the same step the host entry
+    runs.  ``free()`` releases it (also on garbage collection)."""
+
+    def __init__(self, kv, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
+                 sinks, out, eps, scale, block_tables=None):
+        import torch
+        paged = block_tables is not None
+        idx = block_tables if paged else slots
+        B, n_head = _check_step(q, k_new, v_new, positions, idx, out, q_norm_w, k_norm_w,
+                                inv_freq, sinks, kv.n_kv_head, kv.head_dim,
+                                idx_name="block_tables" if paged else "slots")
+        if paged and (block_tables.dim() != 2 or int(block_tables.shape[0]) != B):
+            raise ValueError("block_tables must be [B][max_blocks]")
+        f, u = torch.float32, torch.int32
+        self._c = _vp()
+        self._kv = kv
+        self._keep = (q, k_new, v_new, positions, idx, q_norm_w, k_norm_w, inv_freq, sinks, out)
+        _check(_lib.slot_kv_host_call_create(
+            kv._h, ctypes.byref(self._c), B, n_head, _ptr(q, f, "q", cuda=False),
+            _ptr(k_new, f, "k_new", cuda=False), _ptr(v_new, f, "v_new", cuda=False),
+            _ptr(positions, u, "positions", cuda=False),
+            _ptr(idx, u, "block_tables" if paged else "slots", cuda=False),
+            int(block_tables.shape[1]) if paged else 0,
+            _ptr(q_norm_w, f, "q_norm_w"), _ptr(k_norm_w, f, "k_norm_w"),
+            _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"),
+            _ptr(out, f, "out", cuda=False), eps, scale), "slot_kv_host_call_create")
+        self.out = out
+
+    def __call__(self, stream=None):
+        _check(_lib.slot_kv_host_call_run(self._c, _stream_ptr(stream)),
+               "slot_kv_host_call_run")
+        return self.out
+
+    def free(self):
+        if self._c.value:
+            _check(_lib.slot_kv_host_call_free(self._c), "slot_kv_host_call_free")
+            self._c = _vp()
+        self._keep = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
 
 
 def decode_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,

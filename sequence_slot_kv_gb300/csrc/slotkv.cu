@@ -8,8 +8,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <new>
+#include <vector>
 
 #include "../../include/slotkv.h"
 #include "params.h"
@@ -94,6 +96,23 @@ struct slotkv_s {
     uint32_t* pf_tile_of = nullptr;  // [tokens]
     uint32_t* pf_plan = nullptr;     // item count, hand-out counter
     size_t pf_q_elems = 0, pf_tok = 0;
+    std::vector<slotkv_host_call_s*> calls;  // prepared host calls on this handle
+};
+
+// A prepared host call (slot_kv_host_call_create): the arguments of
+// decode_batch_attn_host or decode_batch_attn_paged_host, checked once, and
+// the device aliases of its host buffers resolved once.  h is cleared when
+// the handle is freed first.
+struct slotkv_host_call_s {
+    slotkv_s* h = nullptr;
+    uint32_t B = 0, n_head = 0, bt_stride = 0;  // bt_stride 0: slots
+    const float *q = nullptr, *k_new = nullptr, *v_new = nullptr;
+    const uint32_t *positions = nullptr, *idx = nullptr;
+    const float *q_norm_w = nullptr, *k_norm_w = nullptr, *inv_freq = nullptr, *sinks = nullptr;
+    float* out = nullptr;
+    float eps = 0.f, scale = 0.f;
+    bool mapped = false;
+    void* dp[6] = {};
 };
 
 namespace {
@@ -110,6 +129,7 @@ void free_workspace(slotkv_s* h) {
 
 void release(slotkv_s* h) {
     if (!h) return;
+    for (slotkv_host_call_s* c : h->calls) c->h = nullptr;  // they refuse to run from now on
     // the handle's memory and work live on its own device
     int cur = 0;
     const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != h->device &&
@@ -471,16 +491,11 @@ struct HostStep {
 // into host memory (through a second copy kernel if out is not 16-byte
 // aligned), instead of separate copy-engine transfers; otherwise each buffer
 // is copied with cudaMemcpyAsync.
-template <typename Run>
-int host_step(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs, cudaStream_t s,
-              Run run) {
-    const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
-    const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
-    const size_t ni = (size_t)B * sizeof(uint32_t);
-    cudaError_t e;
-    int rc;
+// The device aliases dp of the step's six host buffers (q, k_new, v_new,
+// positions, idx, out) when every one is page-locked (mapped into the
+// device's address space); false when any is not.
+bool resolve_mapped(const HostStep& hs, void* dp[6]) {
     const void* hp[6] = {hs.q, hs.k_new, hs.v_new, hs.positions, hs.idx, hs.out};
-    void* dp[6];
     bool mapped = true;
     for (int i = 0; i < 6 && mapped; ++i) {
         cudaPointerAttributes at;
@@ -489,6 +504,18 @@ int host_step(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs, cuda
         dp[i] = mapped ? at.devicePointer : nullptr;
     }
     cudaGetLastError();  // a failed attribute query leaves an error behind
+    return mapped;
+}
+
+// host_step with the buffers already resolved (mapped, dp from resolve_mapped).
+template <typename Run>
+int host_step_resolved(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs,
+                       bool mapped, void* const dp[6], cudaStream_t s, Run run) {
+    const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
+    const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
+    const size_t ni = (size_t)B * sizeof(uint32_t);
+    cudaError_t e;
+    int rc;
     if (mapped) {
         const int threads = 256;
         const unsigned grid = (unsigned)(h->sm_count > 0 ? h->sm_count : 1);
@@ -535,6 +562,14 @@ int host_step(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs, cuda
         return cuda_fail(e, "device-to-host output copy");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
     return SLOTKV_OK;
+}
+
+template <typename Run>
+int host_step(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs, cudaStream_t s,
+              Run run) {
+    void* dp[6];
+    const bool mapped = resolve_mapped(hs, dp);
+    return host_step_resolved(h, B, n_head, hs, mapped, dp, s, run);
 }
 
 }  // namespace
@@ -816,6 +851,95 @@ int decode_batch_attn_paged_host(slotkv_t h, uint32_t B, uint32_t n_head, const 
                                        k_norm_w, inv_freq, sinks, dout, eps, scale,
                                        (cudaStream_t)stream, false, didx, bt_stride);
                      });
+}
+
+int slot_kv_host_call_create(slotkv_t h, slotkv_host_call_t* call, uint32_t B,
+                             uint32_t n_head, const float* q, const float* k_new,
+                             const float* v_new, const uint32_t* positions,
+                             const uint32_t* idx, uint32_t bt_stride, const float* q_norm_w,
+                             const float* k_norm_w, const float* inv_freq, const float* sinks,
+                             float* out, float eps, float scale) {
+    g_err[0] = 0;
+    if (!call) return fail(SLOTKV_ERR_ARG, "call pointer is null");
+    *call = nullptr;
+    int rc = check_decode_args(h, B, n_head, q, k_new, v_new, positions, idx, q_norm_w,
+                               k_norm_w, inv_freq, out, false);
+    if (rc != SLOTKV_OK) return rc;
+    if (B == 0) return fail(SLOTKV_ERR_ARG, "a prepared call needs B >= 1");
+    size_t idx_bytes = (size_t)B * sizeof(uint32_t);
+    if (bt_stride) {
+        const uint32_t T = (uint32_t)slotkv::tile_keys((int)h->head_dim);
+        if (h->slot_ctx % T != 0)
+            return fail(SLOTKV_ERR_UNSUPPORTED, "block size %u is not a multiple of %u keys",
+                        h->slot_ctx, T);
+        idx_bytes = (size_t)B * bt_stride * sizeof(uint32_t);
+        if (idx_bytes > h->st_tab_bytes) {  // the tables' staging, grown once here
+            cudaError_t e = cudaFree(h->st_tab);
+            h->st_tab = nullptr;
+            h->st_tab_bytes = 0;
+            if (e == cudaSuccess) e = cudaMalloc(&h->st_tab, idx_bytes);
+            if (e != cudaSuccess) return cuda_fail(e, "block-table staging");
+            h->st_tab_bytes = idx_bytes;
+        }
+    }
+    slotkv_host_call_s* c = new (std::nothrow) slotkv_host_call_s();
+    if (!c) return fail(SLOTKV_ERR_ARG, "out of host memory");
+    c->h = h;
+    c->B = B;
+    c->n_head = n_head;
+    c->bt_stride = bt_stride;
+    c->q = q;
+    c->k_new = k_new;
+    c->v_new = v_new;
+    c->positions = positions;
+    c->idx = idx;
+    c->q_norm_w = q_norm_w;
+    c->k_norm_w = k_norm_w;
+    c->inv_freq = inv_freq;
+    c->sinks = sinks;
+    c->out = out;
+    c->eps = eps;
+    c->scale = scale;
+    const HostStep hs{q, k_new, v_new, positions, idx, idx_bytes, nullptr, out};
+    c->mapped = resolve_mapped(hs, c->dp);
+    h->calls.push_back(c);
+    *call = c;
+    return SLOTKV_OK;
+}
+
+int slot_kv_host_call_run(slotkv_host_call_t c, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    if (!c) return fail(SLOTKV_ERR_ARG, "call is null");
+    slotkv_s* h = c->h;
+    if (!h) return fail(SLOTKV_ERR_STATE, "the call's handle has been freed");
+    if (check_device(h) != SLOTKV_OK) return SLOTKV_ERR_STATE;
+    const uint32_t B = c->B, n_head = c->n_head, bt_stride = c->bt_stride;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const size_t idx_bytes = (size_t)B * (bt_stride ? bt_stride : 1u) * sizeof(uint32_t);
+    const HostStep hs{c->q, c->k_new, c->v_new, c->positions, c->idx, idx_bytes,
+                      bt_stride ? h->st_tab : h->st_slots, c->out};
+    return host_step_resolved(
+        h, B, n_head, hs, c->mapped, c->dp, s,
+        [&](const float* dq, const float* dk, const float* dv, const uint32_t* dpos,
+            const uint32_t* didx, float* dout) {
+            return bt_stride
+                       ? launch(h, B, n_head, dq, dk, dv, dpos, nullptr, c->q_norm_w,
+                                c->k_norm_w, c->inv_freq, c->sinks, dout, c->eps, c->scale, s,
+                                false, didx, bt_stride)
+                       : launch(h, B, n_head, dq, dk, dv, dpos, didx, c->q_norm_w, c->k_norm_w,
+                                c->inv_freq, c->sinks, dout, c->eps, c->scale, s);
+        });
+}
+
+int slot_kv_host_call_free(slotkv_host_call_t c) {
+    g_err[0] = 0;
+    if (!c) return SLOTKV_OK;
+    if (c->h) {
+        std::vector<slotkv_host_call_s*>& v = c->h->calls;
+        v.erase(std::remove(v.begin(), v.end(), c), v.end());
+    }
+    delete c;
+    return SLOTKV_OK;
 }
 
 // Slot ownership: rank r of n_ranks owns the global slots

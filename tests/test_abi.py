@@ -132,3 +132,17 @@ def test_binding_refuses_mismatched_shapes():
     # shapes that agree get as far as the placement check (CPU tensors here)
     with pytest.raises(ValueError, match="CUDA"):
         skv.decode_batch_attn_noalloc(K, K, eps=1e-6, scale=0.1, **good)
+
+
+def test_host_call_checks_without_gpu():
+    """The prepared host call refuses a missing handle or call pointer before
+    any CUDA work; running or freeing a NULL call is refused or a no-op."""
+    ARG, STATE = 1, 4
+    lib = skv._lib
+    c = ctypes.c_void_p()
+    args = [1, 2] + [None] * 5 + [0] + [None] * 5 + [1e-6, 0.1]
+    assert lib.slot_kv_host_call_create(None, ctypes.byref(c), *args) == STATE
+    assert lib.slot_kv_host_call_create(None, None, *args) == ARG
+    assert not c.value
+    assert lib.slot_kv_host_call_run(None, None) == ARG
+    assert lib.slot_kv_host_call_free(None) == 0
