@@ -20,24 +20,26 @@
 //     cleared (exact in TF32) and a_lo = a - a_hi (exact in f32), and
 //     a.b ~ a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the dropped a_lo.b_lo and the
 //     TF32 rounding of the lo parts are ~2^-20 relative).
-//       - warp 4 (producer): claims items and streams each key tile's K
+//       - warp 8 (producer): claims items and streams each key tile's K
 //         and then V (BK = 64 keys x hd, 128-byte swizzled boxes of 32
 //         floats) with TMA into a ring of half-stage slots (one operand's
 //         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
-//       - warps 6-9 (converters): split each landed K tile in place into
+//       - warps 10-13 (converters): split each landed K tile in place into
 //         hi and lo operand buffers, and transpose each landed V tile into
 //         a keys-contiguous layout while splitting it (TF32 MMA operands
 //         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
 //         keys past the item's last are zeroed;
-//       - warp 5 (MMA issuer, one thread): S = Q K^T into a TMEM score
+//       - warp 9 (MMA issuer, one thread): S = Q K^T into a TMEM score
 //         buffer (A = Q from TMEM), then O += P V (A = P from TMEM, B = the
 //         transposed V tile).  With two score buffers (hd 64) the issue order
 //         is QK(t+1), PV(t), QK(t+2), ...; with one (hd 128, where Q's hi and
 //         lo parts take half of tensor memory) QK(t), PV(t), QK(t+1), ....
 //         MMAs from one thread run in issue order, so a QK reuses a buffer
 //         only after the PV before it has read it;
-//       - warps 0-3 (softmax, one thread per query row = TMEM lane): put
-//         the item's q rows (hi, lo) into TMEM, then per key tile read S,
+//       - warps 0-7 (softmax; two threads per query row = TMEM lane, each
+//         with half of the columns, combining maxima and sums at pairwise
+//         named barriers): put the item's q rows (hi, lo) into TMEM, then
+//         per key tile read S,
 //         apply the causal mask (key <= the row's position), run a base-2
 //         online softmax with a lazily raised max, write P (hi over S, lo
 //         beside it) into the same buffer and, only when the max moves,
@@ -69,8 +71,10 @@ struct PCfg {
     // db * 4096 (TMA put it at db * BLK + kb * 4096)
     static constexpr int KB = BK / 32;
     static constexpr int VT_BLK = HD * 128;
-    static constexpr int NSW = 4;               // softmax warps
-    static constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_CONV = 6, NCONV = 4;
+    // softmax warps: two per tensor-memory lane quarter (warps q and q + 4),
+    // each taking half of a score tile's columns
+    static constexpr int NSW = 8;
+    static constexpr int WARP_TMA = 8, WARP_MMA = 9, WARP_CONV = 10, NCONV = 4;
     static constexpr int SB_PER_WARP = KB * NB / NCONV;  // V sub-blocks per converter warp
     static constexpr int THREADS = 32 * (WARP_CONV + NCONV);
     // tensor memory columns: Q hi | Q lo | O | NBUF buffers of (S, then P hi
@@ -92,7 +96,10 @@ struct PCfg {
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_MISC = OFF_TSLOT + 16;
     // misc[0]: abort; misc[2 + w]: converter warp w's stop flag
-    static constexpr int SMEM_USED = OFF_MISC + 4 * (2 + NCONV);
+    // the softmax halves' exchange: row maxima [2 parities][2 halves][M],
+    // row sums [2 halves][M], and a stop flag beside each
+    static constexpr int OFF_XCH = OFF_MISC + 64;
+    static constexpr int SMEM_USED = OFF_XCH + 2 * 6 * M * 4;
     static constexpr int SMEM = SMEM_USED + 1024;   // slack to align the ring to 1 KiB
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(BLK % 1024 == 0 && SLOT % 1024 == 0, "128-byte swizzle atoms stay 1 KiB aligned");
@@ -573,31 +580,67 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const uint32_t r = static_cast<uint32_t>(tid);  // query row = TMEM lane
-        const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        // Warps q and q + 4 share tensor-memory lane quarter q (rows 32 q ..
+        // 32 q + 31); half hf = warp / 4 takes columns [hf BK/2, (hf+1) BK/2)
+        // of each score tile and columns [hf HD/2, (hf+1) HD/2) of Q and O.
+        // The two halves of a row meet at a pairwise named barrier to combine
+        // their maxima (every tile) and their sums (at an item's end); both
+        // keep the same running max.  Every exit from the loops is decided
+        // at one of these meetings from both halves' published state (a
+        // failed bounded wait or the CTA's abort flag is published, never
+        // acted on alone), so neither half can leave its partner waiting at
+        // the barrier.
+        constexpr int HB = BK / 2, HH = HD / 2;
+        static_assert(HB == 32 && HH % 32 == 0, "one 32-column access per half of a score tile");
+        const int quarter = warp & 3, hf = warp >> 2;
+        const uint32_t r = static_cast<uint32_t>(quarter * 32 + lane);  // query row = TMEM lane
+        const uint32_t lrow = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t t_local = r / G, h_local = r % G;
+        float* xmax = reinterpret_cast<float*>(smem + C::OFF_XCH);   // [2 parities][2][M]
+        float* xsum = xmax + 4 * C::M;                               // [2][M]
+        int* xflag = reinterpret_cast<int*>(xmax + 6 * C::M);       // beside each value
+        auto pair_sync = [&]() {
+            asm volatile("bar.sync %0, 64;" ::"r"(3 + quarter) : "memory");
+        };
+        // Publish v and this warp's stop flag (any lane's) in slot [hf][r] of
+        // buf, meet, and return the partner's value; stop becomes the pair's
+        // decision (either warp's flag), the same in all 64 threads.
+        auto exchange = [&](float* buf, float v, bool& stop) {
+            const int at = static_cast<int>(buf - xmax);
+            stop = __any_sync(0xffffffffu, stop);
+            buf[hf * C::M + r] = v;
+            xflag[at + hf * C::M + r] = stop ? 1 : 0;
+            pair_sync();
+            stop = stop || xflag[at + (1 - hf) * C::M + r] != 0;
+            return buf[(1 - hf) * C::M + r];
+        };
         uint32_t g = 0;  // key tiles processed
         for (uint32_t k = 0;; ++k) {
             const uint32_t is = k & 1;
-            if (!mbar_wait(IFULL + 8 * is, (k >> 1) & 1)) {
-                timeout();
-                break;
-            }
+            const bool got = mbar_wait(IFULL + 8 * is, (k >> 1) & 1);
+            if (!got) timeout();
+            // meeting 1: both halves hold the item (xsum is free: the end of
+            // the previous item met twice after reading it); the decision
+            // uses only the two published values
+            bool stop1 = !got || misc[0];
+            exchange(xsum, 0.f, stop1);
+            if (stop1) break;
             const uint32_t first = desc[8 * is + 0], cnt = desc[8 * is + 1];
             const uint32_t kvh = desc[8 * is + 4], ntiles = desc[8 * is + 5];
             const uint32_t end = desc[8 * is + 6];
+            pair_sync();  // both have read meeting 1 before xsum is written again
             __syncwarp();
             if (lane == 0) mbar_arrive(IFREE + 8 * is);
-            if (end || misc[0]) break;
+            if (end) break;
             const bool vrow = r < static_cast<uint32_t>(C::ROWS) && t_local < cnt;
             const uint32_t tok = first + t_local;
             const uint32_t pos = vrow ? __ldg(P.positions + tok) : 0u;
             const uint32_t head = kvh * G + h_local;
-            // the item's q rows into tensor memory, split hi / lo
+            // this half of the item's q rows into tensor memory, split hi / lo
             {
                 const float* qrow = P.q_rot + (static_cast<size_t>(vrow ? tok : 0) * P.n_head + head) * HD;
 #pragma unroll
-                for (int c0 = 0; c0 < HD; c0 += 32) {
+                for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
                     uint32_t hi[32], lo[32];
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
@@ -616,38 +659,47 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(QREADY);
-            float m = -CUDART_INF_F, l = 0.f;
+            float m = -CUDART_INF_F, l = 0.f;  // l: this half's share of the row sum
             bool failed = false;
             for (uint32_t t = 0; t < ntiles; ++t, ++g) {
                 if (!mbar_wait(SFULL + 8 * (g & 1), (g >> 1) & 1)) {
                     timeout();
                     failed = true;
-                    break;
                 }
                 tc::fence_after_sync();
-                const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF;
-                float s[BK];
-#pragma unroll
-                for (int c0 = 0; c0 < BK; c0 += 32) {
+                const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF + hf * HB;
+                float s[HB];
+                {
                     uint32_t v[32];
-                    tc::tmem_ld32(lrow + scol + c0, v);
+                    tc::tmem_ld32(lrow + scol, v);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(v[c]);
+                    for (int c = 0; c < HB; ++c) s[c] = __uint_as_float(v[c]);
                 }
                 // causal mask: key kbase + c is attended iff it is <= pos
-                const uint32_t kbase = t * BK;
+                const uint32_t kbase = t * BK + hf * HB;
                 float mx = -CUDART_INF_F;
-                if (kbase + BK - 1 <= pos) {
+                if (kbase + HB - 1 <= pos) {
 #pragma unroll
-                    for (int c = 0; c < BK; ++c) mx = fmaxf(mx, s[c]);
+                    for (int c = 0; c < HB; ++c) mx = fmaxf(mx, s[c]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BK; ++c) {
+                    for (int c = 0; c < HB; ++c) {
                         s[c] = kbase + static_cast<uint32_t>(c) <= pos ? s[c] : -CUDART_INF_F;
                         mx = fmaxf(mx, s[c]);
                     }
                 }
+                // meeting 2 (every tile): the row's max over both halves
+                // (double-buffered by tile parity: a half writes parity p
+                // again only after the next meeting, which its partner
+                // reaches after reading p)
+                bool stop2 = failed || misc[0];
+                const float other = exchange(xmax + (g & 1) * 2 * C::M, mx, stop2);
+                if (stop2) {
+                    failed = true;
+                    break;
+                }
+                mx = fmaxf(mx, other);
                 // lazy running max: raised only when a score passes it by 2^8
                 float corr = 1.f;
                 bool rescale = false;
@@ -658,7 +710,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     m = mx;
                 }
 #pragma unroll
-                for (int c = 0; c < BK; ++c) {
+                for (int c = 0; c < HB; ++c) {
                     s[c] = s[c] == -CUDART_INF_F ? 0.f : fast_exp2(s[c] - m);
                     l += s[c];
                 }
@@ -671,55 +723,65 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 // (One barrier for all PVs would not do: with two score
                 // buffers PV(j - 1) may still be running at the wait for
                 // PV(j), and its parity would read as already complete.)
+                // Both halves of a row take the same decision; a wait that
+                // runs out is published at the next meeting.
                 if (__any_sync(0xffffffffu, rescale)) {
                     if (!mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
                         timeout();
                         failed = true;
-                        break;
-                    }
-                    tc::fence_after_sync();
+                    } else {
+                        tc::fence_after_sync();
 #pragma unroll
-                    for (int c0 = 0; c0 < HD; c0 += 32) {
-                        uint32_t v[32];
-                        tc::tmem_ld32(lrow + C::C_O + c0, v);
-                        tc::tmem_ld_wait();
+                        for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
+                            uint32_t v[32];
+                            tc::tmem_ld32(lrow + C::C_O + c0, v);
+                            tc::tmem_ld_wait();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            v[c] = __float_as_uint(__uint_as_float(v[c]) * corr);
-                        tc::tmem_st32(lrow + C::C_O + c0, v);
+                            for (int c = 0; c < 32; ++c)
+                                v[c] = __float_as_uint(__uint_as_float(v[c]) * corr);
+                            tc::tmem_st32(lrow + C::C_O + c0, v);
+                        }
                     }
                 }
-#pragma unroll
-                for (int c0 = 0; c0 < BK; c0 += 32) {
+                {
                     uint32_t hi[32], lo[32];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) tf32_split(s[c0 + c], hi[c], lo[c]);
-                    tc::tmem_st32(lrow + scol + c0, hi);
-                    tc::tmem_st32(lrow + scol + BK + c0, lo);
+                    for (int c = 0; c < HB; ++c) tf32_split(s[c], hi[c], lo[c]);
+                    tc::tmem_st32(lrow + scol, hi);
+                    tc::tmem_st32(lrow + scol + BK, lo);
                 }
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(PREADY + 8 * (g & 1));
             }
-            if (failed || misc[0]) break;
-            // the item's last O += P V (global tile g - 1; its commit covers
-            // every earlier MMA), then out = O / l (sink included)
-            if (!mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
+            // The item's last O += P V (global tile g - 1; its commit covers
+            // every earlier MMA), then out = O / l (both halves' sums, sink
+            // included).  Meeting 3, the sums, is reached by both halves
+            // whether the tile loop ran out or both left it at a meeting;
+            // failed (set there, or by a wait that ran out after the last
+            // meeting) is published here.
+            bool ok = !failed;
+            if (ok && !mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
                 timeout();
-                break;
+                ok = false;
             }
+            bool stop3 = !ok;
+            const float l_other = exchange(xsum, l, stop3);
+            pair_sync();  // both have read the sums before xsum is written again
+            if (stop3) break;
             tc::fence_after_sync();
-            float f = 1.f / l;
+            const float lt = l + l_other;
+            float f = 1.f / lt;
             if (P.sinks) {
                 const float sk = __ldg(P.sinks + head) * kLog2e;
                 const float M2 = fmaxf(m, sk);
                 const float c = exp2f(m - M2);
-                f = c / (l * c + exp2f(sk - M2));
+                f = c / (lt * c + exp2f(sk - M2));
             }
             float* orow = P.out + (static_cast<size_t>(tok) * P.n_head + head) * HD;
 #pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
+            for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
                 uint32_t v[32];
                 tc::tmem_ld32(lrow + C::C_O + c0, v);
                 tc::tmem_ld_wait();
