@@ -67,6 +67,19 @@ def measured_traffic(workload):
     return MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(workload)
 
 
+# DRAM read + write bytes of one tensor-core prefill kernel launch on the
+# prefill workload (ncu, one launch of --set full), keyed by the source hash of
+# prefill_tc.cuh; reported only while the kernel is the one measured.
+MEASURED_PREFILL_TRAFFIC = {"fc9181eece2b854b": 201_450_240 + 48_247_296}
+
+
+def prefill_source_hash():
+    import hashlib
+    path = os.path.join(ROOT, "sequence_slot_kv_gb300", "csrc", "prefill_tc.cuh")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -802,13 +815,16 @@ def run_prefill(args):
         roof = {"bound": "tensor", "achieved": 3 * tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": 3 * tflops / peak, "peak_kind": peak_kind,
                 "achieved_is": "3 TF32 products per useful f32 product, useful (causal) keys only",
-                "kernel": "slotkv_prefill_tc_kernel (with its prep and plan kernels)"}
+                "kernel": "slotkv_prefill_tc_kernel (with its prep and plan kernels)",
+                "traffic": MEASURED_PREFILL_TRAFFIC.get(prefill_source_hash()),
+                "traffic_unit": "DRAM bytes per tensor-core kernel launch (read + write)"}
     else:
         peak, peak_kind = alu_peak_f32(dev)
         roof = {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": tflops / peak, "peak_kind": peak_kind,
                 "kernel": "slotkv_decode_attn_kernel (prefill mode)"}
-    roof.update({"traffic": None, "alg_flops_per_launch": flops, "avg_launch_us": ms * 1e3,
+    roof.setdefault("traffic", None)
+    roof.update({"alg_flops_per_launch": flops, "avg_launch_us": ms * 1e3,
                  "effective_f32_TFLOPs": tflops})
     line = {"metric": "slot-attn prefill tokens/s", "value": n_tok / (ms / 1e3),
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
