@@ -502,17 +502,17 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                 tc::fence_after_sync();
                 const uint32_t sl = hv % NSLOT;
                 const uint32_t pcol0 = C::C_S + (gp % NBUF) * C::C_BUF;
+                // O += P_lo V_hi + P_hi V_hi + P_hi V_lo, K-step by K-step
+                // (consecutive products share their B, then their A, slice)
 #pragma unroll
-                for (int term = 0; term < 3; ++term) {
-                    const uint32_t pcol = term == 2 ? pcol0 + BK : pcol0;
-                    const uint32_t vb = term == 1 ? slot_lo(sl) : slot_hi(sl);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 8; ++kk) {
-                        const uint64_t b = tc::smem_desc(vb + (kk / 4) * C::VT_BLK + (kk % 4) * 32, 16,
-                                                         1024, tc::kSwizzle128B);
-                        tc::mma_tf32_ts(tbase + C::C_O, tbase + pcol + kk * 8, b, C::IDESC_PV,
-                                        (t | term | kk) != 0 ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    const uint32_t off = (kk / 4) * C::VT_BLK + (kk % 4) * 32;
+                    const uint64_t bh = tc::smem_desc(slot_hi(sl) + off, 16, 1024, tc::kSwizzle128B);
+                    const uint64_t bl = tc::smem_desc(slot_lo(sl) + off, 16, 1024, tc::kSwizzle128B);
+                    tc::mma_tf32_ts(tbase + C::C_O, tbase + pcol0 + BK + kk * 8, bh, C::IDESC_PV,
+                                    (t | kk) != 0 ? 1u : 0u);
+                    tc::mma_tf32_ts(tbase + C::C_O, tbase + pcol0 + kk * 8, bh, C::IDESC_PV, 1u);
+                    tc::mma_tf32_ts(tbase + C::C_O, tbase + pcol0 + kk * 8, bl, C::IDESC_PV, 1u);
                 }
                 tc::mma_commit(PVDONE + 8 * (gp & 1));
                 tc::mma_commit(EMPTY + 8 * sl);
@@ -544,20 +544,19 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    // S = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
+                    // S = Q_lo K_hi + Q_hi K_hi + Q_hi K_lo, K-step by K-step
+                    // (consecutive products share their B, then their A, slice)
                     const uint32_t sl = hk % NSLOT;
                     const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF;
 #pragma unroll
-                    for (int term = 0; term < 3; ++term) {
-                        const uint32_t qcol = term == 2 ? C::C_QLO : C::C_QHI;
-                        const uint32_t kb = term == 1 ? slot_lo(sl) : slot_hi(sl);
-#pragma unroll
-                        for (int kk = 0; kk < HD / 8; ++kk) {
-                            const uint64_t b = tc::smem_desc(kb + (kk / 4) * C::BLK + (kk % 4) * 32, 16,
-                                                             1024, tc::kSwizzle128B);
-                            tc::mma_tf32_ts(tbase + scol, tbase + qcol + kk * 8, b, C::IDESC_QK,
-                                            (term | kk) != 0 ? 1u : 0u);
-                        }
+                    for (int kk = 0; kk < HD / 8; ++kk) {
+                        const uint32_t off = (kk / 4) * C::BLK + (kk % 4) * 32;
+                        const uint64_t bh = tc::smem_desc(slot_hi(sl) + off, 16, 1024, tc::kSwizzle128B);
+                        const uint64_t bl = tc::smem_desc(slot_lo(sl) + off, 16, 1024, tc::kSwizzle128B);
+                        tc::mma_tf32_ts(tbase + scol, tbase + C::C_QLO + kk * 8, bh, C::IDESC_QK,
+                                        kk != 0 ? 1u : 0u);
+                        tc::mma_tf32_ts(tbase + scol, tbase + C::C_QHI + kk * 8, bh, C::IDESC_QK, 1u);
+                        tc::mma_tf32_ts(tbase + scol, tbase + C::C_QHI + kk * 8, bl, C::IDESC_QK, 1u);
                     }
                     tc::mma_commit(SFULL + 8 * (g & 1));
                     tc::mma_commit(EMPTY + 8 * sl);  // K slot free once QK has read it
