@@ -70,7 +70,7 @@ def measured_traffic(workload):
 # DRAM read + write bytes of one tensor-core prefill kernel launch on the
 # prefill workload (ncu, one launch of --set full), keyed by the source hash of
 # prefill_tc.cuh; reported only while the kernel is the one measured.
-MEASURED_PREFILL_TRAFFIC = {"fc9181eece2b854b": 201_450_240 + 48_247_296}
+MEASURED_PREFILL_TRAFFIC = {"8cc15edda80ad76e": 201_495_040 + 48_018_688}
 
 
 def prefill_source_hash():
