@@ -46,21 +46,32 @@ FLUSH_BYTES = 256 * 1024 * 1024  # written between calls of a step that fits in 
 
 # DRAM bytes (read + write) per decode call (plan + decode kernels) from ncu
 # captures of dram__bytes_read.sum and dram__bytes_write.sum, valid only for
-# the kernel source they were taken on (sha256 prefix of decode_attn.cuh).
+# the kernel code they were taken on (code_hash of decode_attn.cuh).
 MEASURED_TRAFFIC = {
     # all at full size; large's is its first step's ratio to the algorithmic
     # bytes times the mean algorithmic bytes of its 64 steps
     # (plan + decode kernel bytes, the mean of two calls)
-    "4e8294f487abe411": {"mid": 551_830_912, "sinks": 2_336_513_024,
+    "26542fcb3b784732": {"mid": 551_830_912, "sinks": 2_336_513_024,
                          "skewed": 17_227_054_208, "large": 2_238_835_960},
 }
 
 
-def kernel_source_hash():
+def code_hash(name):
+    """sha256 prefix of a kernel source with its comments and whitespace
+    removed: the measured counters below stay tied to the code, not to the
+    wording of its comments."""
     import hashlib
-    path = os.path.join(ROOT, "sequence_slot_kv_gb300", "csrc", "decode_attn.cuh")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    import re
+    with open(os.path.join(ROOT, "sequence_slot_kv_gb300", "csrc", name)) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
+def kernel_source_hash():
+    return code_hash("decode_attn.cuh")
 
 
 def measured_traffic(workload):
@@ -68,16 +79,13 @@ def measured_traffic(workload):
 
 
 # DRAM read + write bytes of one tensor-core prefill kernel launch on the
-# prefill workload (ncu, one launch of --set full), keyed by the source hash of
+# prefill workload (ncu, one launch of --set full), keyed by code_hash of
 # prefill_tc.cuh; reported only while the kernel is the one measured.
-MEASURED_PREFILL_TRAFFIC = {"8cc15edda80ad76e": 201_495_040 + 48_018_688}
+MEASURED_PREFILL_TRAFFIC = {"8fcf52bae1bbb24f": 201_495_040 + 48_018_688}
 
 
 def prefill_source_hash():
-    import hashlib
-    path = os.path.join(ROOT, "sequence_slot_kv_gb300", "csrc", "prefill_tc.cuh")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    return code_hash("prefill_tc.cuh")
 
 
 def peak_hbm():

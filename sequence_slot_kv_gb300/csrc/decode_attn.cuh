@@ -5,11 +5,15 @@
 // history K/V byte is read from HBM exactly once.  C comes from the split
 // policy (see split_chunk and the host's choice of chunk_min).
 //
-// Kernels per call, on one stream:
+// Kernels per call, on one stream (a call of a few rows over short slots
+// runs slotkv_decode_small_kernel instead, see decode_small.cuh):
 //   * slotkv_plan_kernel (one CTA): checks every row's slot and position,
 //     lists the valid work items, largest first (leaving out the CTAs'
 //     static items), and resets the hand-out counter.  Skipped when the
-//     static items are all the work;
+//     static items are all the work.  Launched as a programmatic dependent
+//     of whatever precedes it, it waits for that grid before reading
+//     anything; the previous call's decode kernel lets it launch once every
+//     CTA has run out of items, so its launch overlaps that call's tail;
 //   * slotkv_decode_attn_kernel (persistent, 2 CTAs per SM, launched as a
 //     programmatic dependent of the plan): each CTA starts on its static
 //     item -- split 0 of (row, kv head) pair blockIdx.x, or, for CTAs beyond
