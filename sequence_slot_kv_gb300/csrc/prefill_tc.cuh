@@ -4,7 +4,7 @@
 // Cuda", batched prefill into the given slot).
 //
 // Three kernels per call, on one stream:
-//   * slotkv_prefill_prep_kernel: one warp per (token, head).  Query heads:
+//   * slotkv_prefill_prep_kernel: one warp per (token, 8 heads).  Query heads:
 //     q' = RoPE(RMSnorm(q) * w) * scale * log2(e) into a workspace; kv heads:
 //     k' = RoPE(RMSnorm(k_new) * w) and v into the token's slot row.  The
 //     vector routines are the decode kernel's, so q' and k' are the same
@@ -131,33 +131,76 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) 
 }
 
 // ------------------------------------------------------------------ prep
+// One warp per (token, group of kPrepHeads heads).  The group's rows (q rows,
+// or k_new and v_new rows) are staged into the warp's shared memory with
+// cp.async, all in flight at once, while the warp forms the token's RoPE
+// angles; then each row goes through the decode kernel's vector routine
+// (the same arithmetic on the same values, so the same bits as a decode
+// step).
+constexpr int kPrepHeads = 8;
+
+__device__ __forceinline__ void prep_cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
+template <int HD>
+__host__ __device__ constexpr int prep_smem_bytes() {
+    return 4 * 2 * kPrepHeads * HD * 4;  // four warps x (rows, v rows)
+}
+
 template <int HD>
 __global__ void __launch_bounds__(128) slotkv_prefill_prep_kernel(const PrefillParams P) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t wg = blockIdx.x * 4 + (threadIdx.x >> 5);
+    extern __shared__ __align__(16) uint8_t prep_smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t per_tok = P.n_head + P.n_kv_head;
-    const uint32_t tok = wg / per_tok, x = wg % per_tok;
+    const uint32_t groups = (per_tok + kPrepHeads - 1) / kPrepHeads;
+    const uint32_t wg = blockIdx.x * 4 + warp;
+    const uint32_t tok = wg / groups, x0 = (wg % groups) * kPrepHeads;
     if (tok >= P.n_tok) return;
     const uint32_t p = P.positions[tok], slot = P.slots[tok];
     if (slot >= P.n_slots || p >= P.slot_ctx) return;  // the plan raises the flag
+    const uint32_t nx = per_tok - x0 < static_cast<uint32_t>(kPrepHeads) ? per_tok - x0
+                                                                           : kPrepHeads;
+    float* rows = reinterpret_cast<float*>(prep_smem) + warp * 2 * kPrepHeads * HD;
+    float* vrows = rows + kPrepHeads * HD;
+    for (uint32_t i = 0; i < nx; ++i) {
+        const uint32_t x = x0 + i;
+        const float* src = x < P.n_head
+                               ? P.q + (static_cast<size_t>(tok) * P.n_head + x) * HD
+                               : P.k_new + (static_cast<size_t>(tok) * P.n_kv_head + (x - P.n_head)) * HD;
+        for (int c = lane; c < HD / 4; c += 32) prep_cp_async16(rows + i * HD + 4 * c, src + 4 * c);
+        if (x >= P.n_head) {
+            const float* vsrc =
+                P.v_new + (static_cast<size_t>(tok) * P.n_kv_head + (x - P.n_head)) * HD;
+            for (int c = lane; c < HD / 4; c += 32)
+                prep_cp_async16(vrows + i * HD + 4 * c, vsrc + 4 * c);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     float cs[HD / 64], sn[HD / 64];
     warp_rope_angles<HD>(p, P.inv_freq, cs, sn, lane);
     const float w1 = (P.flags & kOptNormPlusOne) ? 1.0f : 0.0f;
-    if (x < P.n_head) {
-        const size_t at = (static_cast<size_t>(tok) * P.n_head + x) * HD;
-        warp_norm_rope<HD>(P.q + at, P.q_rot + at, P.q_norm_w, w1, P.scale_log2, P.eps, cs, sn,
-                           lane);
-        return;
-    }
-    const uint32_t kvh = x - P.n_head;
-    const size_t src = (static_cast<size_t>(tok) * P.n_kv_head + kvh) * HD;
-    const size_t dst = ((static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh) * HD;
-    warp_norm_rope<HD>(P.k_new + src, P.K + dst, P.k_norm_w, w1, 1.0f, P.eps, cs, sn, lane);
-    if (P.flags & kOptVNorm) {
-        warp_rms_norm_plain<HD>(P.v_new + src, P.V + dst, P.eps, lane);
-    } else {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    for (uint32_t i = 0; i < nx; ++i) {
+        const uint32_t x = x0 + i;
+        if (x < P.n_head) {
+            const size_t at = (static_cast<size_t>(tok) * P.n_head + x) * HD;
+            warp_norm_rope<HD>(rows + i * HD, P.q_rot + at, P.q_norm_w, w1, P.scale_log2, P.eps,
+                               cs, sn, lane);
+            continue;
+        }
+        const uint32_t kvh = x - P.n_head;
+        const size_t dst = ((static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh) * HD;
+        warp_norm_rope<HD>(rows + i * HD, P.K + dst, P.k_norm_w, w1, 1.0f, P.eps, cs, sn, lane);
+        if (P.flags & kOptVNorm) {
+            warp_rms_norm_plain<HD>(vrows + i * HD, P.V + dst, P.eps, lane);
+        } else {
 #pragma unroll
-        for (int j = 0; j < HD / 32; ++j) P.V[dst + lane + 32 * j] = P.v_new[src + lane + 32 * j];
+            for (int j = 0; j < HD / 32; ++j) P.V[dst + lane + 32 * j] = vrows[i * HD + lane + 32 * j];
+        }
     }
 }
 
@@ -816,8 +859,9 @@ int launch_prefill_one(const PrefillParams& p, const CUtensorMap& tmK, const CUt
         if (e != cudaSuccess) return static_cast<int>(e);
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const uint32_t warps = p.n_tok * (p.n_head + p.n_kv_head);
-    slotkv_prefill_prep_kernel<HD><<<(warps + 3) / 4, 128, 0, stream>>>(p);
+    const uint32_t groups = (p.n_head + p.n_kv_head + kPrepHeads - 1) / kPrepHeads;
+    const uint32_t warps = p.n_tok * groups;
+    slotkv_prefill_prep_kernel<HD><<<(warps + 3) / 4, 128, prep_smem_bytes<HD>(), stream>>>(p);
     slotkv_prefill_plan_kernel<C::MT><<<1, 1024, 0, stream>>>(p);
     slotkv_prefill_tc_kernel<HD, G><<<ctas, C::THREADS, C::SMEM, stream>>>(tmK, tmV, p);
     return static_cast<int>(cudaGetLastError());
