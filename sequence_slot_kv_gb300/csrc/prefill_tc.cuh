@@ -47,7 +47,9 @@
 //         normalise (sink included) and store out.
 // Every mbarrier wait is bounded; on expiry the CTA raises SLOTKV_DEV_TIMEOUT
 // and every role leaves its loop; the MMA thread waits for its MMAs and the
-// producer for its copies before tensor memory is freed.
+// producer for its copies before tensor memory is freed.  The test option
+// SLOTKV_OPT_TEST_STALL withholds each CTA's first score-ready signal to
+// exercise that path.
 #pragma once
 
 #include "decode_attn.cuh"
@@ -601,7 +603,9 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                         tc::mma_tf32_ts(tbase + scol, tbase + C::C_QHI + kk * 8, bh, C::IDESC_QK, 1u);
                         tc::mma_tf32_ts(tbase + scol, tbase + C::C_QHI + kk * 8, bl, C::IDESC_QK, 1u);
                     }
-                    tc::mma_commit(SFULL + 8 * (g & 1));
+                    // (the failure-path test option withholds the CTA's first
+                    // score-ready signal, so the softmax's bounded wait runs out)
+                    if (!(g == 0 && (P.flags & kOptTestStall))) tc::mma_commit(SFULL + 8 * (g & 1));
                     tc::mma_commit(EMPTY + 8 * sl);  // K slot free once QK has read it
                     // one buffer: this tile's PV next; two: the previous tile's
                     if (NBUF == 1) {
