@@ -81,7 +81,7 @@ def measured_traffic(workload):
 # DRAM read + write bytes of one tensor-core prefill kernel launch on the
 # prefill workload (ncu, one launch of --set full), keyed by code_hash of
 # prefill_tc.cuh; reported only while the kernel is the one measured.
-MEASURED_PREFILL_TRAFFIC = {"b541b933da06552c": 201_566_720 + 48_157_440}
+MEASURED_PREFILL_TRAFFIC = {"583552d513b61cd5": 201_554_944 + 48_571_904}
 
 
 def prefill_source_hash():
