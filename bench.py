@@ -559,7 +559,8 @@ def time_e2e(dw, steps, warmup, world):
     (SlotKV.prepare_host_call: the host entry decode_batch_attn_host, or
     decode_batch_attn_paged_host, with its arguments checked once, as a
     serving loop that reuses its pinned buffers would call it).  The calls
-    are prepared before the timed region; each run is synchronous."""
+    are prepared before the timed region; a step enqueues its calls and
+    synchronises its stream once at its end."""
     import torch
     w, dev, stream, nsub, bs = dw.w, dw.dev, dw.stream, dw.nsub, dw.bs
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -575,8 +576,11 @@ def time_e2e(dw, steps, warmup, world):
              for t in range(nsub)]
 
     def e2e_step():
+        # the step's calls are enqueued back to back; the step ends when its
+        # stream is synchronised (its outputs are then in host memory)
         for c in calls:
-            c(stream=dw.sp)
+            c(stream=dw.sp, sync=False)
+        dw.stream.synchronize()
 
     def barrier():
         if world > 1:

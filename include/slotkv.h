@@ -300,7 +300,7 @@ int decode_batch_attn_paged_host(slotkv_t handle, uint32_t B, uint32_t n_head, c
                                  slotkv_stream_t stream);
 
 /*
- * slot_kv_host_call_create / _run / _free -- a prepared host step: the
+ * slot_kv_host_call_create / _run / _enqueue / _free -- a prepared host step: the
  * arguments of decode_batch_attn_host (bt_stride = 0, idx = slots) or of
  * decode_batch_attn_paged_host (bt_stride >= 1, idx = block_tables), checked
  * once and with the device aliases of the page-locked host buffers resolved
@@ -318,6 +318,14 @@ int decode_batch_attn_paged_host(slotkv_t handle, uint32_t B, uint32_t n_head, c
  *            and synchronises `stream` before returning.  SLOTKV_ERR_STATE
  *            once the handle has been freed (slot_kv_free detaches its
  *            calls), or when another device is current.
+ *   enqueue  the same step without the final synchronisation: the step's
+ *            work (input gather or copies, kernels, output write or copy) is
+ *            enqueued on `stream` and the call returns.  out and K/V are
+ *            complete, and the host input buffers may be refilled, only once
+ *            `stream` has been synchronised (cudaStreamSynchronize, or an
+ *            event recorded after the call); a caller running several steps
+ *            synchronises once, when it needs the results.  With pageable
+ *            (not page-locked) buffers the copies themselves may block.
  *   free     releases the call (NULL is a no-op); a handle may be freed
  *            before or after its calls.
  */
@@ -328,6 +336,7 @@ int slot_kv_host_call_create(slotkv_t handle, slotkv_host_call_t* call, uint32_t
                              const float* k_norm_w, const float* inv_freq, const float* sinks,
                              float* out, float eps, float scale);
 int slot_kv_host_call_run(slotkv_host_call_t call, slotkv_stream_t stream);
+int slot_kv_host_call_enqueue(slotkv_host_call_t call, slotkv_stream_t stream);
 int slot_kv_host_call_free(slotkv_host_call_t call);
 
 /*

@@ -71,6 +71,7 @@ EXPORTS = {
     "slot_kv_host_call_create": ([_vp, ctypes.POINTER(_vp), _u32, _u32, _vp, _vp, _vp, _vp, _vp,
                                   _u32, _vp, _vp, _vp, _vp, _vp, _f32, _f32], _int),
     "slot_kv_host_call_run": ([_vp, _vp], _int),
+    "slot_kv_host_call_enqueue": ([_vp, _vp], _int),
     "slot_kv_host_call_free": ([_vp], _int),
     "slot_kv_last_error": ([], ctypes.c_char_p),
 }
@@ -410,7 +411,9 @@ class HostCall:
     ideally pinned) and the device parameters are checked once and kept
     referenced; ``call(stream=None)`` runs one synchronous step on their
     current contents (slot_kv_host_call_run), the same step the host entry
-    runs.  ``free()`` releases it (also on garbage collection)."""
+    runs; ``call(stream, sync=False)`` only enqueues it
+    (slot_kv_host_call_enqueue).  ``free()`` releases it (also on garbage
+    collection)."""
 
     def __init__(self, kv, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w, inv_freq,
                  sinks, out, eps, scale, block_tables=None):
@@ -437,9 +440,16 @@ class HostCall:
             _ptr(out, f, "out", cuda=False), eps, scale), "slot_kv_host_call_create")
         self.out = out
 
-    def __call__(self, stream=None):
-        _check(_lib.slot_kv_host_call_run(self._c, _stream_ptr(stream)),
-               "slot_kv_host_call_run")
+    def __call__(self, stream=None, sync=True):
+        """One step.  sync=False only enqueues it (slot_kv_host_call_enqueue):
+        out is complete, and the host inputs may be refilled, once the stream
+        has been synchronised."""
+        if sync:
+            _check(_lib.slot_kv_host_call_run(self._c, _stream_ptr(stream)),
+                   "slot_kv_host_call_run")
+        else:
+            _check(_lib.slot_kv_host_call_enqueue(self._c, _stream_ptr(stream)),
+                   "slot_kv_host_call_enqueue")
         return self.out
 
     def free(self):

@@ -507,10 +507,12 @@ bool resolve_mapped(const HostStep& hs, void* dp[6]) {
     return mapped;
 }
 
-// host_step with the buffers already resolved (mapped, dp from resolve_mapped).
+// host_step with the buffers already resolved (mapped, dp from resolve_mapped);
+// sync false leaves the final synchronisation of s to the caller.
 template <typename Run>
 int host_step_resolved(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep& hs,
-                       bool mapped, void* const dp[6], cudaStream_t s, Run run) {
+                       bool mapped, void* const dp[6], cudaStream_t s, Run run,
+                       bool sync = true) {
     const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
     const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
     const size_t ni = (size_t)B * sizeof(uint32_t);
@@ -545,7 +547,8 @@ int host_step_resolved(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep&
             if ((e = cudaGetLastError()) != cudaSuccess)
                 return cuda_fail(e, "output scatter launch");
         }
-        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+        if (sync && (e = cudaStreamSynchronize(s)) != cudaSuccess)
+            return cuda_fail(e, "stream sync");
         return SLOTKV_OK;
     }
     if ((e = cudaMemcpyAsync(h->st_q, hs.q, nq, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
@@ -560,7 +563,7 @@ int host_step_resolved(slotkv_s* h, uint32_t B, uint32_t n_head, const HostStep&
     if (rc != SLOTKV_OK) return rc;
     if ((e = cudaMemcpyAsync(hs.out, h->st_out, nq, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e, "device-to-host output copy");
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+    if (sync && (e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
     return SLOTKV_OK;
 }
 
@@ -907,8 +910,8 @@ int slot_kv_host_call_create(slotkv_t h, slotkv_host_call_t* call, uint32_t B,
     return SLOTKV_OK;
 }
 
-int slot_kv_host_call_run(slotkv_host_call_t c, slotkv_stream_t stream) {
-    g_err[0] = 0;
+namespace {
+int host_call_step(slotkv_host_call_t c, slotkv_stream_t stream, bool sync) {
     if (!c) return fail(SLOTKV_ERR_ARG, "call is null");
     slotkv_s* h = c->h;
     if (!h) return fail(SLOTKV_ERR_STATE, "the call's handle has been freed");
@@ -928,7 +931,19 @@ int slot_kv_host_call_run(slotkv_host_call_t c, slotkv_stream_t stream) {
                                 false, didx, bt_stride)
                        : launch(h, B, n_head, dq, dk, dv, dpos, didx, c->q_norm_w, c->k_norm_w,
                                 c->inv_freq, c->sinks, dout, c->eps, c->scale, s);
-        });
+        },
+        sync);
+}
+}  // namespace
+
+int slot_kv_host_call_run(slotkv_host_call_t c, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    return host_call_step(c, stream, true);
+}
+
+int slot_kv_host_call_enqueue(slotkv_host_call_t c, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    return host_call_step(c, stream, false);
 }
 
 int slot_kv_host_call_free(slotkv_host_call_t c) {

@@ -124,3 +124,38 @@ def test_host_call_argument_errors():
                                                              np.float32)), w.eps, w.scale)
     finally:
         run.close()
+
+
+def test_enqueued_host_calls_equal_synchronous_runs():
+    """Three steps at advancing positions, each a prepared call with buffers
+    of its own, enqueued back to back with one synchronisation at the end:
+    every output and the final K/V equal three synchronous runs bit for
+    bit."""
+    w = _wl(1120)
+    runs = [DeviceRun(w), DeviceRun(w)]
+    try:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        outs = {}
+        for mode, run in zip(("sync", "enqueue"), runs):
+            calls, houts = [], []
+            for t in range(3):
+                hout = pin(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+                calls.append(run.kv.prepare_host_call(
+                    pin(w.q(t)), pin(w.k_new(t)), pin(w.v_new(t)),
+                    pin(w.positions(t).astype(np.int32)), pin(run.slots_np.astype(np.int32)),
+                    run.qw, run.kw, run.inv, run.sinks, hout, w.eps, w.scale))
+                houts.append(hout)
+            stream = torch.cuda.Stream()
+            for c in calls:
+                c(stream=stream, sync=(mode == "sync"))
+            stream.synchronize()
+            outs[mode] = [h.clone() for h in houts]
+            for c in calls:
+                c.free()
+        for t in range(3):
+            assert torch.equal(outs["sync"][t], outs["enqueue"][t]), f"step {t}"
+        assert torch.equal(runs[0].K, runs[1].K) and torch.equal(runs[0].V, runs[1].V)
+        assert runs[0].status() == 0 and runs[1].status() == 0
+    finally:
+        for r in runs:
+            r.close()
