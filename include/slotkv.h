@@ -318,16 +318,23 @@ int decode_batch_attn_paged_host(slotkv_t handle, uint32_t B, uint32_t n_head, c
  *            and synchronises `stream` before returning.  SLOTKV_ERR_STATE
  *            once the handle has been freed (slot_kv_free detaches its
  *            calls), or when another device is current.
- *   enqueue  the same step without the final synchronisation: the step's
- *            work (input gather or copies, kernels, output write or copy) is
- *            enqueued on `stream` and the call returns.  out and K/V are
- *            complete, and the host input buffers may be refilled, only once
- *            `stream` has been synchronised (cudaStreamSynchronize, or an
- *            event recorded after the call); a caller running several steps
- *            synchronises once, when it needs the results.  With pageable
- *            (not page-locked) buffers the copies themselves may block.
- *   free     releases the call (NULL is a no-op); a handle may be freed
- *            before or after its calls.
+ *   enqueue  the same step (the same kernels, the same bits) without the
+ *            final synchronisation.  While work is in flight on `stream`, the
+ *            inputs are copied by the copy engines into device staging owned
+ *            by the call (allocated by its first such enqueue) on a copy
+ *            stream of the handle, so they overlap that work, and the step
+ *            runs on `stream` after them; on an idle stream the step takes
+ *            run's lower-latency path (one gather kernel).  The call returns
+ *            without waiting.  out and K/V are complete, and the host
+ *            input buffers may be refilled, only once `stream` has been
+ *            synchronised (cudaStreamSynchronize, or an event recorded after
+ *            the call); a caller running several steps synchronises once,
+ *            when it needs the results.  Enqueuing the same call again
+ *            orders its copies after its previous step.  With pageable (not
+ *            page-locked) buffers the copies themselves may block.
+ *   free     releases the call and its staging, after its last enqueued
+ *            step has run (NULL is a no-op); a handle may be freed before or
+ *            after its calls.
  */
 int slot_kv_host_call_create(slotkv_t handle, slotkv_host_call_t* call, uint32_t B,
                              uint32_t n_head, const float* q, const float* k_new,

@@ -97,6 +97,7 @@ struct slotkv_s {
     uint32_t* pf_plan = nullptr;     // item count, hand-out counter
     size_t pf_q_elems = 0, pf_tok = 0;
     std::vector<slotkv_host_call_s*> calls;  // prepared host calls on this handle
+    cudaStream_t copy_stream = nullptr;      // their enqueued input copies (created on demand)
 };
 
 // A prepared host call (slot_kv_host_call_create): the arguments of
@@ -113,6 +114,15 @@ struct slotkv_host_call_s {
     float eps = 0.f, scale = 0.f;
     bool mapped = false;
     void* dp[6] = {};
+    // the enqueue path: the call's own device staging (allocated by its first
+    // enqueue), filled by the copy engines on the handle's copy stream;
+    // in_ready orders the step after its copies, done the next copies after
+    // the step that read the staging
+    int device = 0;
+    float *st_q = nullptr, *st_k = nullptr, *st_v = nullptr, *st_out = nullptr;
+    uint32_t *st_pos = nullptr, *st_idx = nullptr;
+    cudaEvent_t in_ready = nullptr, done = nullptr;
+    bool used = false;
 };
 
 namespace {
@@ -135,6 +145,7 @@ void release(slotkv_s* h) {
     const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != h->device &&
                           cudaSetDevice(h->device) == cudaSuccess;
     cudaDeviceSynchronize();
+    if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     free_workspace(h);
     cudaFree(h->status);
     cudaFree(h->st_q);
@@ -936,6 +947,95 @@ int host_call_step(slotkv_host_call_t c, slotkv_stream_t stream, bool sync) {
 }
 }  // namespace
 
+namespace {
+void free_call_staging(slotkv_host_call_s* c) {
+    cudaFree(c->st_q);
+    cudaFree(c->st_k);
+    cudaFree(c->st_v);
+    cudaFree(c->st_out);
+    cudaFree(c->st_pos);
+    cudaFree(c->st_idx);
+    if (c->in_ready) cudaEventDestroy(c->in_ready);
+    if (c->done) cudaEventDestroy(c->done);
+    c->st_q = c->st_k = c->st_v = c->st_out = nullptr;
+    c->st_pos = c->st_idx = nullptr;
+    c->in_ready = c->done = nullptr;
+    c->used = false;
+}
+
+// The enqueued step.  With work still in flight on `stream`, the inputs go
+// to the call's own staging by the copy engines on the handle's copy stream
+// (so they overlap that work), the step waits for them, and the next copies
+// into this staging wait for the step.  On an idle stream nothing would
+// overlap, and the lower-latency path of run (one gather kernel over the host
+// link) is taken, without its final synchronisation.  Both run the same
+// kernels on the same values.
+int host_call_enqueue(slotkv_host_call_t c, slotkv_stream_t stream) {
+    if (!c) return fail(SLOTKV_ERR_ARG, "call is null");
+    slotkv_s* h = c->h;
+    if (!h) return fail(SLOTKV_ERR_STATE, "the call's handle has been freed");
+    if (check_device(h) != SLOTKV_OK) return SLOTKV_ERR_STATE;
+    {
+        const cudaError_t q = cudaStreamQuery((cudaStream_t)stream);
+        if (q == cudaSuccess) return host_call_step(c, stream, false);
+        if (q != cudaErrorNotReady) return cuda_fail(q, "stream query");
+    }
+    const uint32_t B = c->B, n_head = c->n_head, bt_stride = c->bt_stride;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const size_t nq = (size_t)B * n_head * h->head_dim * sizeof(float);
+    const size_t nk = (size_t)B * h->kv_dim * sizeof(float);
+    const size_t ni = (size_t)B * sizeof(uint32_t);
+    const size_t nidx = (size_t)B * (bt_stride ? bt_stride : 1u) * sizeof(uint32_t);
+    cudaError_t e;
+    if (!c->st_q) {
+        c->device = h->device;
+        if ((e = cudaMalloc(&c->st_q, nq)) != cudaSuccess ||
+            (e = cudaMalloc(&c->st_k, nk)) != cudaSuccess ||
+            (e = cudaMalloc(&c->st_v, nk)) != cudaSuccess ||
+            (e = cudaMalloc(&c->st_out, nq)) != cudaSuccess ||
+            (e = cudaMalloc(&c->st_pos, ni)) != cudaSuccess ||
+            (e = cudaMalloc(&c->st_idx, nidx)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->in_ready, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming)) != cudaSuccess) {
+            free_call_staging(c);
+            return cuda_fail(e, "prepared call staging");
+        }
+    }
+    if (!h->copy_stream &&
+        (e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "copy stream");
+    const cudaStream_t cs = h->copy_stream;
+    if (c->used && (e = cudaStreamWaitEvent(cs, c->done, 0)) != cudaSuccess)
+        return cuda_fail(e, "staging reuse order");
+    if ((e = cudaMemcpyAsync(c->st_q, c->q, nq, cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(c->st_k, c->k_new, nk, cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(c->st_v, c->v_new, nk, cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(c->st_pos, c->positions, ni, cudaMemcpyHostToDevice, cs)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(c->st_idx, c->idx, nidx, cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+        (e = cudaEventRecord(c->in_ready, cs)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, c->in_ready, 0)) != cudaSuccess)
+        return cuda_fail(e, "enqueued input copies");
+    // out straight into host memory when it is page-locked and 16-byte aligned
+    const bool direct_out = c->mapped && ((uintptr_t)c->dp[5] & 15) == 0;
+    float* dout = direct_out ? static_cast<float*>(c->dp[5]) : c->st_out;
+    const int rc = bt_stride
+                       ? launch(h, B, n_head, c->st_q, c->st_k, c->st_v, c->st_pos, nullptr,
+                                c->q_norm_w, c->k_norm_w, c->inv_freq, c->sinks, dout, c->eps,
+                                c->scale, s, false, c->st_idx, bt_stride)
+                       : launch(h, B, n_head, c->st_q, c->st_k, c->st_v, c->st_pos, c->st_idx,
+                                c->q_norm_w, c->k_norm_w, c->inv_freq, c->sinks, dout, c->eps,
+                                c->scale, s);
+    if (rc != SLOTKV_OK) return rc;
+    if (!direct_out &&
+        (e = cudaMemcpyAsync(c->out, c->st_out, nq, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "enqueued output copy");
+    if ((e = cudaEventRecord(c->done, s)) != cudaSuccess) return cuda_fail(e, "step order");
+    c->used = true;
+    return SLOTKV_OK;
+}
+}  // namespace
+
 int slot_kv_host_call_run(slotkv_host_call_t c, slotkv_stream_t stream) {
     g_err[0] = 0;
     return host_call_step(c, stream, true);
@@ -943,7 +1043,7 @@ int slot_kv_host_call_run(slotkv_host_call_t c, slotkv_stream_t stream) {
 
 int slot_kv_host_call_enqueue(slotkv_host_call_t c, slotkv_stream_t stream) {
     g_err[0] = 0;
-    return host_call_step(c, stream, false);
+    return host_call_enqueue(c, stream);
 }
 
 int slot_kv_host_call_free(slotkv_host_call_t c) {
@@ -952,6 +1052,15 @@ int slot_kv_host_call_free(slotkv_host_call_t c) {
     if (c->h) {
         std::vector<slotkv_host_call_s*>& v = c->h->calls;
         v.erase(std::remove(v.begin(), v.end(), c), v.end());
+    }
+    if (c->st_q || c->in_ready) {
+        // the call's staging belongs to its device; its last step must be done
+        int cur = 0;
+        const bool switched = cudaGetDevice(&cur) == cudaSuccess && cur != c->device &&
+                              cudaSetDevice(c->device) == cudaSuccess;
+        if (c->done && c->used) cudaEventSynchronize(c->done);
+        free_call_staging(c);
+        if (switched) cudaSetDevice(cur);
     }
     delete c;
     return SLOTKV_OK;

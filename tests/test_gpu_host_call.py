@@ -159,3 +159,60 @@ def test_enqueued_host_calls_equal_synchronous_runs():
     finally:
         for r in runs:
             r.close()
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_enqueued_call_twice_in_flight_and_paged(pinned):
+    """The same prepared call enqueued twice before one synchronisation (the
+    first on an idle stream takes the gather path, the second, with work in
+    flight, the copy-engine path; the step is idempotent at the same
+    positions) equals one synchronous run; and a paged call enqueued the same
+    way equals the paged host entry."""
+    from test_gpu_paged import PagedRun, small_paged_workload
+    host = lambda a: (torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+                      if pinned else torch.from_numpy(np.ascontiguousarray(a)))
+    w = _wl(1130 + pinned)
+    a, b = DeviceRun(w), DeviceRun(w)
+    try:
+        args = lambda r: (host(w.q(0)), host(w.k_new(0)), host(w.v_new(0)),  # noqa: E731
+                          host(w.positions(0).astype(np.int32)), host(r.slots_np.astype(np.int32)),
+                          r.qw, r.kw, r.inv, r.sinks)
+        oa = host(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+        ca = a.kv.prepare_host_call(*args(a), oa, w.eps, w.scale)
+        ca()
+        ob = host(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+        cb = b.kv.prepare_host_call(*args(b), ob, w.eps, w.scale)
+        stream = torch.cuda.Stream()
+        cb(stream=stream, sync=False)
+        cb(stream=stream, sync=False)
+        stream.synchronize()
+        assert torch.equal(oa, ob)
+        assert torch.equal(a.K, b.K) and torch.equal(a.V, b.V)
+        assert a.status() == 0 and b.status() == 0
+        ca.free()
+        cb.free()
+    finally:
+        a.close()
+        b.close()
+    w, bs = small_paged_workload(128, 4, 1, 61, sinks=True)
+    ref, run = PagedRun(w, bs), PagedRun(w, bs)
+    try:
+        hq, hk, hv = host(w.q(0)), host(w.k_new(0)), host(w.v_new(0))
+        hp, ht = host(w.positions(0).astype(np.int32)), host(run.tables_np.astype(np.int32))
+        out = host(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+        call = run.kv.prepare_host_call(hq, hk, hv, hp, None, run.qw, run.kw, run.inv, run.sinks,
+                                        out, w.eps, w.scale, block_tables=ht)
+        stream = torch.cuda.Stream()
+        call(stream=stream, sync=False)   # an idle stream: the gather path
+        call(stream=stream, sync=False)   # work in flight: the copy-engine path
+        stream.synchronize()
+        want = host(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+        ref.kv.decode_batch_attn_paged_host(hq, hk, hv, hp, ht, ref.qw, ref.kw, ref.inv,
+                                            ref.sinks, want, w.eps, w.scale)
+        assert torch.equal(out, want)
+        assert torch.equal(run.K, ref.K) and torch.equal(run.V, ref.V)
+        assert run.kv.get_status() == 0 and ref.kv.get_status() == 0
+        call.free()
+    finally:
+        ref.close()
+        run.close()
