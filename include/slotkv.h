@@ -218,6 +218,26 @@ int prefill_batch_attn(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const f
                        float scale, slotkv_stream_t stream);
 
 /*
+ * prefill_batch_attn_host -- prefill_batch_attn for callers whose per-call
+ * inputs and output live in host memory ("Forward Cuda Gemma",
+ * prefillBatched, with the prompt's tensors on the host).  q, k_new, v_new,
+ * positions, slots and out are HOST pointers; q_norm_w, k_norm_w, inv_freq
+ * and sinks stay device pointers.  The inputs move to handle-owned device
+ * staging with cudaMemcpyAsync (the copy engines: a prefill's tens of MB move
+ * faster that way than through a gather kernel), the prefill runs (the same
+ * kernels as prefill_batch_attn, the same bits) into device staging, out
+ * moves back the same way, and `stream` is synchronised before the call
+ * returns (page-locked buffers make the copies asynchronous DMA).  n_tok <=
+ * max_rows.  Errors as prefill_batch_attn, plus SLOTKV_ERR_CUDA for a failed
+ * copy.
+ */
+int prefill_batch_attn_host(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const float* q,
+                            const float* k_new, const float* v_new, const uint32_t* positions,
+                            const uint32_t* slots, const float* q_norm_w,
+                            const float* k_norm_w, const float* inv_freq, const float* sinks,
+                            float* out, float eps, float scale, slotkv_stream_t stream);
+
+/*
  * decode_batch_attn_paged -- the decode step over a paged KV pool: instead of
  * one contiguous slot per sequence, each row's keys live in fixed-size blocks
  * named by its block table (the paged cache with per-sequence block tables of

@@ -23,6 +23,7 @@ import os
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn",
+    "prefill_batch_attn_host",
     "decode_batch_attn_paged", "decode_batch_attn_paged_host", "decode_batch_attn_noalloc",
     "slot_kv_advance_positions",
     "slot_kv_get_status", "slot_kv_set_split", "HostCall", "LIB_PATH", "EXPORTS", "DEV_RANGE",
@@ -52,6 +53,7 @@ EXPORTS = {
     "decode_batch_attn": (_DECODE_ARGS, _int),
     "decode_batch_attn_host": (_DECODE_ARGS, _int),
     "prefill_batch_attn": (_DECODE_ARGS, _int),
+    "prefill_batch_attn_host": (_DECODE_ARGS, _int),
     "decode_batch_attn_paged": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp, _vp,
                                  _vp, _vp, _f32, _f32, _vp], _int),
     "decode_batch_attn_paged_host": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp,
@@ -261,6 +263,23 @@ class SlotKV:
             eps, scale, _stream_ptr(stream)), "prefill_batch_attn")
         return out
 
+    def prefill_batch_attn_host(self, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                                inv_freq, sinks, out, eps, scale, stream=None):
+        """As prefill_batch_attn, with q/k_new/v_new/positions/slots/out in host
+        memory (CPU tensors, ideally pinned); synchronous."""
+        import torch
+        n, n_head = _check_step(q, k_new, v_new, positions, slots, out, q_norm_w, k_norm_w,
+                                inv_freq, sinks, self.n_kv_head, self.head_dim)
+        f, u = torch.float32, torch.int32
+        _check(_lib.prefill_batch_attn_host(
+            self._h, n, n_head, _ptr(q, f, "q", cuda=False), _ptr(k_new, f, "k_new", cuda=False),
+            _ptr(v_new, f, "v_new", cuda=False), _ptr(positions, u, "positions", cuda=False),
+            _ptr(slots, u, "slots", cuda=False), _ptr(q_norm_w, f, "q_norm_w"),
+            _ptr(k_norm_w, f, "k_norm_w"), _ptr(inv_freq, f, "inv_freq"), _ptr(sinks, f, "sinks"),
+            _ptr(out, f, "out", cuda=False), eps, scale, _stream_ptr(stream)),
+            "prefill_batch_attn_host")
+        return out
+
     def decode_batch_attn_paged(self, q, k_new, v_new, positions, block_tables, q_norm_w,
                                 k_norm_w, inv_freq, sinks, out, eps, scale, stream=None):
         """Decode over a paged pool (this handle's buffers as blocks of
@@ -397,6 +416,12 @@ def prefill_batch_attn(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                        sinks, out, eps, scale, stream=None):
     return h.prefill_batch_attn(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                                 inv_freq, sinks, out, eps, scale, stream)
+
+
+def prefill_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                            inv_freq, sinks, out, eps, scale, stream=None):
+    return h.prefill_batch_attn_host(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                                     inv_freq, sinks, out, eps, scale, stream)
 
 
 def decode_batch_attn_paged(h, q, k_new, v_new, positions, block_tables, q_norm_w, k_norm_w,

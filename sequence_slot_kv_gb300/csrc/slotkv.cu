@@ -742,19 +742,20 @@ int decode_batch_attn(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
                   sinks, out, eps, scale, (cudaStream_t)stream);
 }
 
-int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
-                       const float* k_new, const float* v_new, const uint32_t* positions,
-                       const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
-                       const float* inv_freq, const float* sinks, float* out, float eps,
-                       float scale, slotkv_stream_t stream) {
-    g_err[0] = 0;
-    int rc = check_decode_args(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w,
-                               k_norm_w, inv_freq, out);
-    if (rc != SLOTKV_OK || n_tok == 0) return rc;
+}  // extern "C"
+
+namespace {
+// The prefill step on device pointers (arguments already checked).
+int run_prefill(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
+                const float* k_new, const float* v_new, const uint32_t* positions,
+                const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
+                const float* inv_freq, const float* sinks, float* out, float eps, float scale,
+                cudaStream_t stream) {
     if (!h->tc_prefill)  // head dim 256: the decode kernel in prefill mode
         return launch(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
-                      inv_freq, sinks, out, eps, scale, (cudaStream_t)stream, true);
-    if ((rc = prefill_workspace(h, n_tok, n_head)) != SLOTKV_OK) return rc;
+                      inv_freq, sinks, out, eps, scale, stream, true);
+    int rc = prefill_workspace(h, n_tok, n_head);
+    if (rc != SLOTKV_OK) return rc;
     slotkv::PrefillParams P;
     P.q = q;
     P.k_new = k_new;
@@ -784,10 +785,51 @@ int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float*
     const int G = (int)(n_head / h->n_kv_head);
     const unsigned ctas = (unsigned)(h->sm_count > 0 ? h->sm_count : 1);
     rc = h->head_dim == 64
-             ? slotkv::launch_prefill_tc_hd64(G, P, h->tmKs, h->tmVs, ctas, (cudaStream_t)stream)
-             : slotkv::launch_prefill_tc_hd128(G, P, h->tmKs, h->tmVs, ctas, (cudaStream_t)stream);
+             ? slotkv::launch_prefill_tc_hd64(G, P, h->tmKs, h->tmVs, ctas, stream)
+             : slotkv::launch_prefill_tc_hd128(G, P, h->tmKs, h->tmVs, ctas, stream);
     if (rc != 0) return cuda_fail((cudaError_t)rc, "prefill kernel launch");
     return SLOTKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
+                       const float* k_new, const float* v_new, const uint32_t* positions,
+                       const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
+                       const float* inv_freq, const float* sinks, float* out, float eps,
+                       float scale, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w,
+                               k_norm_w, inv_freq, out);
+    if (rc != SLOTKV_OK || n_tok == 0) return rc;
+    return run_prefill(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
+                       inv_freq, sinks, out, eps, scale, (cudaStream_t)stream);
+}
+
+int prefill_batch_attn_host(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
+                            const float* k_new, const float* v_new, const uint32_t* positions,
+                            const uint32_t* slots, const float* q_norm_w,
+                            const float* k_norm_w, const float* inv_freq, const float* sinks,
+                            float* out, float eps, float scale, slotkv_stream_t stream) {
+    g_err[0] = 0;
+    int rc = check_decode_args(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w,
+                               k_norm_w, inv_freq, out, false);
+    if (rc != SLOTKV_OK || n_tok == 0) return rc;
+    const HostStep hs{q, k_new, v_new, positions, slots, (size_t)n_tok * sizeof(uint32_t),
+                      h->st_slots, out};
+    // A prefill moves tens of MB each way: the copy engines move them faster
+    // than a gather kernel, and an out written into host memory by the
+    // attention kernel itself would stall its epilogue on the host link, so
+    // every buffer goes through cudaMemcpyAsync and device staging.
+    void* const none[6] = {};
+    return host_step_resolved(
+        h, n_tok, n_head, hs, false, none, (cudaStream_t)stream,
+        [&](const float* dq, const float* dk, const float* dv, const uint32_t* dpos,
+            const uint32_t* didx, float* dout) {
+            return run_prefill(h, n_tok, n_head, dq, dk, dv, dpos, didx, q_norm_w, k_norm_w,
+                               inv_freq, sinks, dout, eps, scale, (cudaStream_t)stream);
+        });
 }
 
 int decode_batch_attn_paged(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,

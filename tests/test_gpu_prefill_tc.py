@@ -123,3 +123,35 @@ def test_bench_prefill_workload_full_size():
     rows = sorted({s * chunk + j for s in range(bench.PREFILL_SEQ) for j in (0, 31, 32, 257, 511)})
     ref = _oracle_rows(w, slots, pos, rows)
     assert_close(got[rows], ref, "prefill workload sampled tokens")
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_prefill_host_entry_equals_device_entry(pinned):
+    """prefill_batch_attn_host (tokens' tensors and out in host memory) runs
+    the same kernels as the device entry on the same values: the same output
+    and the same slot bytes, bit for bit."""
+    hd, G = 128, 4
+    slots = np.concatenate([np.full(70, 1, np.uint32), np.full(33, 3, np.uint32)])
+    pos = np.concatenate([np.arange(200, 270, dtype=np.uint32), np.arange(0, 33, dtype=np.uint32)])
+    w = _workload(hd, G, 2, 95, len(pos), 5, 300)
+    got_dev, Kd, Vd = _run(w, slots, pos)
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    K = torch.empty(shape, device="cuda")
+    V = torch.empty(shape, device="cuda")
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    kv = SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
+    try:
+        host = lambda a: (torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+                          if pinned else torch.from_numpy(np.ascontiguousarray(a)))
+        out = host(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+        s = w.sink_logits()
+        kv.prefill_batch_attn_host(host(w.q()), host(w.k_new()), host(w.v_new()),
+                                   host(pos.astype(np.int32)), host(slots.astype(np.int32)),
+                                   to_dev(w.q_norm_w()), to_dev(w.k_norm_w()),
+                                   to_dev(w.inv_freq()), None if s is None else to_dev(s), out,
+                                   w.eps, w.scale)
+        assert kv.get_status() == 0
+        assert np.array_equal(out.numpy().view(np.uint32), got_dev.view(np.uint32))
+        assert torch.equal(K, Kd) and torch.equal(V, Vd)
+    finally:
+        kv.free()
