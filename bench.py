@@ -292,7 +292,7 @@ def run_reference(args, w):
         return
     cores = os.cpu_count() or 1
     if args.prefill:
-        w, slots, pos = prefill_workload()
+        w, slots, pos = prefill_workload(args.prefill_geometry)
         smp = PrefillOracleSample(w, slots, pos, cores)
         per_step, unit = smp.n_seq, "tokens/s"
         metric, config = "slot-attn prefill tokens/s", prefill_config(w)
@@ -726,23 +726,25 @@ def run_gpu(args, w):
 PREFILL_SEQ, PREFILL_HIST, PREFILL_CHUNK = 8, 1536, 512
 
 
-def prefill_workload():
-    """The prefill workload at the mid geometry: 8 sequences in slots 0, 2,
-    .., 14, each adding a 512-token prompt chunk after 1536 positions of
+def prefill_workload(geometry="mid"):
+    """The prefill workload at a decode workload's head geometry (mid: 32 / 8
+    heads at hd 128; sinks: 64 / 8 heads at hd 64): 8 sequences in slots 0,
+    2, .., 14, each adding a 512-token prompt chunk after 1536 positions of
     history.  Returns the workload (one row per token) and the tokens' slots
     and positions."""
     n_seq, hist, chunk = PREFILL_SEQ, PREFILL_HIST, PREFILL_CHUNK
     n_tok = n_seq * chunk
-    w = synth.WORKLOADS["mid"].replace(
-        name="prefill", index=20, B=n_tok, n_slots=16, slot_ctx=hist + chunk,
-        pos_rule="fixed", fixed_positions=tuple([0] * n_tok))
+    w = synth.WORKLOADS[geometry].replace(
+        name="prefill" if geometry == "mid" else f"prefill_{geometry}", index=20, B=n_tok,
+        n_slots=16, slot_ctx=hist + chunk, pos_rule="fixed",
+        fixed_positions=tuple([0] * n_tok))
     slots = np.repeat(np.arange(n_seq, dtype=np.int32) * 2, chunk)
     pos = np.tile(np.arange(hist, hist + chunk, dtype=np.int32), n_seq)
     return w, slots, pos
 
 
 def prefill_config(w):
-    return {"workload": "prefill", "sequences": PREFILL_SEQ, "history": PREFILL_HIST,
+    return {"workload": w.name, "sequences": PREFILL_SEQ, "history": PREFILL_HIST,
             "prompt_chunk": PREFILL_CHUNK, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
             "head_dim": w.head_dim}
 
@@ -752,7 +754,7 @@ def run_prefill(args):
     prefill_batch_attn call over all 4096 tokens."""
     import torch
     import sequence_slot_kv_gb300 as skv
-    w, slots, pos = prefill_workload()
+    w, slots, pos = prefill_workload(args.prefill_geometry)
     n_tok = w.B
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -957,6 +959,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="time batched causal prefill instead of the decode step")
+    ap.add_argument("--prefill-geometry", default="mid", choices=["mid", "sinks"],
+                    help="head geometry of the prefill workload (mid: hd 128; sinks: hd 64)")
     ap.add_argument("--options", default="", choices=["", "vnorm", "plus_one", "both"],
                     help="Gemma norm forms: weightless V norm, (1 + w) Q/K weights, or both")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
