@@ -5,6 +5,8 @@ rows out of range), default and fixed split policies, slot and paged layouts
 with random block sizes, and the norm options.  Prefill: random sequences in
 one call, tokens in random order.  Each case checks every in-range row's
 output, the range flag, the written rows and that no other byte changed."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +19,9 @@ from gpu_harness import assert_close, to_dev
 pytestmark = pytest.mark.gpu
 
 N_CASES = 200
+# SLOTKV_FUZZ_OFFSET shifts every case's seed, for a stress run over fresh
+# configurations; the suite's own cases are offset 0.
+OFFSET = int(os.environ.get("SLOTKV_FUZZ_OFFSET", "0"))
 
 
 def _case(seed):
@@ -50,7 +55,7 @@ def _case(seed):
     return w, bs, split, flags, bad
 
 
-@pytest.mark.parametrize("seed", range(N_CASES))
+@pytest.mark.parametrize("seed", range(OFFSET, OFFSET + N_CASES))
 def test_random_configuration(seed):
     w, bs, split, flags, bad = _case(seed)
     o = oracle.default()
@@ -153,7 +158,7 @@ def _prefill_case(seed):
     return w, slots, pos, split, flags
 
 
-@pytest.mark.parametrize("seed", range(N_PREFILL))
+@pytest.mark.parametrize("seed", range(OFFSET, OFFSET + N_PREFILL))
 def test_random_prefill(seed):
     """Random sequences (history, prompt length, slot) as one prefill call
     with their tokens in random order: every token equals one decode step at
