@@ -79,9 +79,10 @@ def measured_traffic(workload):
 
 
 # DRAM read + write bytes of one tensor-core prefill kernel launch on the
-# prefill workload (ncu, one launch of --set full), keyed by code_hash of
-# prefill_tc.cuh; reported only while the kernel is the one measured.
-MEASURED_PREFILL_TRAFFIC = {"583552d513b61cd5": 201_554_944 + 48_571_904}
+# prefill workload of a geometry (ncu, one launch of --set full), keyed by
+# code_hash of prefill_tc.cuh; reported only while the kernel is the one
+# measured.
+MEASURED_PREFILL_TRAFFIC = {"583552d513b61cd5": {"mid": 201_554_944 + 48_571_904}}
 
 
 def prefill_source_hash():
@@ -832,7 +833,8 @@ def run_prefill(args):
                 "frac": 3 * tflops / peak, "peak_kind": peak_kind,
                 "achieved_is": "3 TF32 products per useful f32 product, useful (causal) keys only",
                 "kernel": "slotkv_prefill_tc_kernel (with its prep and plan kernels)",
-                "traffic": MEASURED_PREFILL_TRAFFIC.get(prefill_source_hash()),
+                "traffic": MEASURED_PREFILL_TRAFFIC.get(prefill_source_hash(), {}).get(
+                    args.prefill_geometry),
                 "traffic_unit": "DRAM bytes per tensor-core kernel launch (read + write)"}
     else:
         peak, peak_kind = alu_peak_f32(dev)
