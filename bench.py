@@ -79,10 +79,10 @@ def measured_traffic(workload):
 
 
 # DRAM read + write bytes of one tensor-core prefill kernel launch on the
-# prefill workload of a geometry (ncu, one launch of --set full), keyed by
-# code_hash of prefill_tc.cuh; reported only while the kernel is the one
-# measured.
-MEASURED_PREFILL_TRAFFIC = {"583552d513b61cd5": {"mid": 201_554_944 + 48_571_904}}
+# prefill workload of a geometry (ncu, the mean of ten launches' one-pass
+# counters), keyed by code_hash of prefill_tc.cuh; reported only while the
+# kernel is the one measured.
+MEASURED_PREFILL_TRAFFIC = {"b7663287658bb425": {"mid": 244_639_155, "sinks": 172_958_515}}
 
 
 def prefill_source_hash():

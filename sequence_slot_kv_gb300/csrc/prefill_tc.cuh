@@ -661,185 +661,217 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
             return buf[(1 - hf) * C::M + r];
         };
         uint32_t g = 0;  // key tiles processed
-        for (uint32_t k = 0;; ++k) {
+        // Meeting 1 opens item k: both halves hold its descriptor (xsum is
+        // free: every meeting on it is followed by a pair barrier).  stop
+        // carries a failure not yet published and becomes the pair's
+        // decision; on success the descriptor's slot is released.
+        auto open_item = [&](uint32_t k, bool stop, uint32_t (&d)[5]) {
             const uint32_t is = k & 1;
-            const bool got = mbar_wait(IFULL + 8 * is, (k >> 1) & 1);
-            if (!got) timeout();
-            // meeting 1: both halves hold the item (xsum is free: the end of
-            // the previous item met twice after reading it); the decision
-            // uses only the two published values
-            bool stop1 = !got || misc[0];
-            exchange(xsum, 0.f, stop1);
-            if (stop1) break;
-            const uint32_t first = desc[8 * is + 0], cnt = desc[8 * is + 1];
-            const uint32_t kvh = desc[8 * is + 4], ntiles = desc[8 * is + 5];
-            const uint32_t end = desc[8 * is + 6];
+            stop = stop || misc[0];
+            if (!stop && !mbar_wait(IFULL + 8 * is, (k >> 1) & 1)) {
+                timeout();
+                stop = true;
+            }
+            exchange(xsum, 0.f, stop);
+            if (stop) return false;
+            d[0] = desc[8 * is + 0];  // first token
+            d[1] = desc[8 * is + 1];  // tokens
+            d[2] = desc[8 * is + 4];  // kv head
+            d[3] = desc[8 * is + 5];  // key tiles
+            d[4] = desc[8 * is + 6];  // end marker
             pair_sync();  // both have read meeting 1 before xsum is written again
             __syncwarp();
             if (lane == 0) mbar_arrive(IFREE + 8 * is);
-            if (end) break;
-            const bool vrow = r < static_cast<uint32_t>(C::ROWS) && t_local < cnt;
-            const uint32_t tok = first + t_local;
-            const uint32_t pos = vrow ? __ldg(P.positions + tok) : 0u;
-            const uint32_t head = kvh * G + h_local;
-            // this half of the item's q rows into tensor memory, split hi / lo
-            {
-                const float* qrow = P.q_rot + (static_cast<size_t>(vrow ? tok : 0) * P.n_head + head) * HD;
+            return true;
+        };
+        struct ItemRow {
+            bool valid;
+            uint32_t tok, pos, head;
+        };
+        auto row_of = [&](const uint32_t (&d)[5]) {
+            ItemRow w;
+            w.valid = r < static_cast<uint32_t>(C::ROWS) && t_local < d[1];
+            w.tok = d[0] + t_local;
+            w.pos = w.valid ? __ldg(P.positions + w.tok) : 0u;
+            w.head = d[2] * G + h_local;
+            return w;
+        };
+        // this half of the item's q rows into tensor memory, split hi / lo
+        auto load_q = [&](const ItemRow& w) {
+            const float* qrow = P.q_rot + (static_cast<size_t>(w.valid ? w.tok : 0) * P.n_head + w.head) * HD;
 #pragma unroll
-                for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
-                    uint32_t hi[32], lo[32];
+            for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
+                uint32_t hi[32], lo[32];
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 x = vrow ? __ldcg(reinterpret_cast<const float4*>(qrow + c0 + c))
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                        tf32_split(x.x, hi[c + 0], lo[c + 0]);
-                        tf32_split(x.y, hi[c + 1], lo[c + 1]);
-                        tf32_split(x.z, hi[c + 2], lo[c + 2]);
-                        tf32_split(x.w, hi[c + 3], lo[c + 3]);
-                    }
-                    tc::tmem_st32(lrow + C::C_QHI + c0, hi);
-                    tc::tmem_st32(lrow + C::C_QLO + c0, lo);
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 x = w.valid ? __ldcg(reinterpret_cast<const float4*>(qrow + c0 + c))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    tf32_split(x.x, hi[c + 0], lo[c + 0]);
+                    tf32_split(x.y, hi[c + 1], lo[c + 1]);
+                    tf32_split(x.z, hi[c + 2], lo[c + 2]);
+                    tf32_split(x.w, hi[c + 3], lo[c + 3]);
                 }
-                tc::tmem_st_wait();
+                tc::tmem_st32(lrow + C::C_QHI + c0, hi);
+                tc::tmem_st32(lrow + C::C_QLO + c0, lo);
             }
+            tc::tmem_st_wait();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(QREADY);
-            float m = -CUDART_INF_F, l = 0.f;  // l: this half's share of the row sum
-            bool failed = false;
-            for (uint32_t t = 0; t < ntiles; ++t, ++g) {
-                if (!mbar_wait(SFULL + 8 * (g & 1), (g >> 1) & 1)) {
-                    timeout();
-                    failed = true;
-                }
-                tc::fence_after_sync();
-                const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF + hf * HB;
-                float s[HB];
-                {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lrow + scol, v);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < HB; ++c) s[c] = __uint_as_float(v[c]);
-                }
-                // causal mask: key kbase + c is attended iff it is <= pos
-                const uint32_t kbase = t * BK + hf * HB;
-                float mx = -CUDART_INF_F;
-                if (kbase + HB - 1 <= pos) {
-#pragma unroll
-                    for (int c = 0; c < HB; ++c) mx = fmaxf(mx, s[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < HB; ++c) {
-                        s[c] = kbase + static_cast<uint32_t>(c) <= pos ? s[c] : -CUDART_INF_F;
-                        mx = fmaxf(mx, s[c]);
-                    }
-                }
-                // meeting 2 (every tile): the row's max over both halves
-                // (double-buffered by tile parity: a half writes parity p
-                // again only after the next meeting, which its partner
-                // reaches after reading p)
-                bool stop2 = failed || misc[0];
-                const float other = exchange(xmax + (g & 1) * 2 * C::M, mx, stop2);
-                if (stop2) {
-                    failed = true;
-                    break;
-                }
-                mx = fmaxf(mx, other);
-                // lazy running max: raised only when a score passes it by 2^8
-                float corr = 1.f;
-                bool rescale = false;
-                if (mx > m + 8.f) {
-                    corr = m == -CUDART_INF_F ? 0.f : fast_exp2(m - mx);
-                    rescale = t > 0;
-                    l *= corr;
-                    m = mx;
-                }
-#pragma unroll
-                for (int c = 0; c < HB; ++c) {
-                    s[c] = s[c] == -CUDART_INF_F ? 0.f : fast_exp2(s[c] - m);
-                    l += s[c];
-                }
-                // O may be rescaled only once the previous tile's O += P V
-                // (global tile g - 1) has completed.  PV(j) completes a phase
-                // of pv_done[j % 2]; at any wait for PV(j), PV(j - 2) has
-                // completed (the S this softmax already read was committed
-                // after it) and PV(j + 2) cannot start (it needs P from this
-                // softmax), so the parity of phase j / 2 is unambiguous.
-                // (One barrier for all PVs would not do: with two score
-                // buffers PV(j - 1) may still be running at the wait for
-                // PV(j), and its parity would read as already complete.)
-                // Both halves of a row take the same decision; a wait that
-                // runs out is published at the next meeting.
-                if (__any_sync(0xffffffffu, rescale)) {
-                    if (!mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
+        };
+        uint32_t d[5];
+        if (open_item(0, false, d) && !d[4]) {
+            ItemRow cur = row_of(d);
+            load_q(cur);
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t ntiles = d[3];
+                float m = -CUDART_INF_F, l = 0.f;  // l: this half's share of the row sum
+                bool failed = false;
+                for (uint32_t t = 0; t < ntiles; ++t, ++g) {
+                    if (!mbar_wait(SFULL + 8 * (g & 1), (g >> 1) & 1)) {
                         timeout();
                         failed = true;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t scol = C::C_S + (g % NBUF) * C::C_BUF + hf * HB;
+                    float s[HB];
+                    {
+                        uint32_t v[32];
+                        tc::tmem_ld32(lrow + scol, v);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < HB; ++c) s[c] = __uint_as_float(v[c]);
+                    }
+                    // causal mask: key kbase + c is attended iff it is <= cur.pos
+                    const uint32_t kbase = t * BK + hf * HB;
+                    float mx = -CUDART_INF_F;
+                    if (kbase + HB - 1 <= cur.pos) {
+#pragma unroll
+                        for (int c = 0; c < HB; ++c) mx = fmaxf(mx, s[c]);
                     } else {
-                        tc::fence_after_sync();
 #pragma unroll
-                        for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
-                            uint32_t v[32];
-                            tc::tmem_ld32(lrow + C::C_O + c0, v);
-                            tc::tmem_ld_wait();
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                v[c] = __float_as_uint(__uint_as_float(v[c]) * corr);
-                            tc::tmem_st32(lrow + C::C_O + c0, v);
+                        for (int c = 0; c < HB; ++c) {
+                            s[c] = kbase + static_cast<uint32_t>(c) <= cur.pos ? s[c] : -CUDART_INF_F;
+                            mx = fmaxf(mx, s[c]);
                         }
                     }
-                }
-                {
-                    uint32_t hi[32], lo[32];
+                    // meeting 2 (every tile): the row's max over both halves
+                    // (double-buffered by tile parity: a half writes parity p
+                    // again only after the next meeting, which its partner
+                    // reaches after reading p)
+                    bool stop2 = failed || misc[0];
+                    const float other = exchange(xmax + (g & 1) * 2 * C::M, mx, stop2);
+                    if (stop2) {
+                        failed = true;
+                        break;
+                    }
+                    mx = fmaxf(mx, other);
+                    // lazy running max: raised only when a score passes it by 2^8
+                    float corr = 1.f;
+                    bool rescale = false;
+                    if (mx > m + 8.f) {
+                        corr = m == -CUDART_INF_F ? 0.f : fast_exp2(m - mx);
+                        rescale = t > 0;
+                        l *= corr;
+                        m = mx;
+                    }
 #pragma unroll
-                    for (int c = 0; c < HB; ++c) tf32_split(s[c], hi[c], lo[c]);
-                    tc::tmem_st32(lrow + scol, hi);
-                    tc::tmem_st32(lrow + scol + BK, lo);
+                    for (int c = 0; c < HB; ++c) {
+                        s[c] = s[c] == -CUDART_INF_F ? 0.f : fast_exp2(s[c] - m);
+                        l += s[c];
+                    }
+                    // O may be rescaled only once the previous tile's O += P V
+                    // (global tile g - 1) has completed.  PV(j) completes a phase
+                    // of pv_done[j % 2]; at any wait for PV(j), PV(j - 2) has
+                    // completed (the S this softmax already read was committed
+                    // after it) and PV(j + 2) cannot start (it needs P from this
+                    // softmax), so the parity of phase j / 2 is unambiguous.
+                    // (One barrier for all PVs would not do: with two score
+                    // buffers PV(j - 1) may still be running at the wait for
+                    // PV(j), and its parity would read as already complete.)
+                    // Both halves of a row take the same decision; a wait that
+                    // runs out is published at the next meeting.
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        if (!mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
+                            timeout();
+                            failed = true;
+                        } else {
+                            tc::fence_after_sync();
+#pragma unroll
+                            for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
+                                uint32_t v[32];
+                                tc::tmem_ld32(lrow + C::C_O + c0, v);
+                                tc::tmem_ld_wait();
+#pragma unroll
+                                for (int c = 0; c < 32; ++c)
+                                    v[c] = __float_as_uint(__uint_as_float(v[c]) * corr);
+                                tc::tmem_st32(lrow + C::C_O + c0, v);
+                            }
+                        }
+                    }
+                    {
+                        uint32_t hi[32], lo[32];
+#pragma unroll
+                        for (int c = 0; c < HB; ++c) tf32_split(s[c], hi[c], lo[c]);
+                        tc::tmem_st32(lrow + scol, hi);
+                        tc::tmem_st32(lrow + scol + BK, lo);
+                    }
+                    tc::tmem_st_wait();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(PREADY + 8 * (g & 1));
                 }
-                tc::tmem_st_wait();
+                // The next item opens before this one ends: every QK of this
+                // item has completed (its last S was read above), so the next
+                // item's Q may replace this one's in tensor memory while the
+                // last O += P V runs, and the next item's first QK overlaps
+                // this item's epilogue.  Its first O += P V overwrites O only
+                // after its P is published, which this softmax does after
+                // reading O below.  A failure so far is published at this
+                // meeting, and both halves leave together.
+                if (!open_item(k + 1, failed, d)) break;
+                const bool last = d[4] != 0;
+                ItemRow nxt{};
+                if (!last) {
+                    nxt = row_of(d);
+                    load_q(nxt);
+                }
+                // This item's last O += P V (global tile g - 1; its commit
+                // covers every earlier MMA), then out = O / l (both halves'
+                // sums, sink included).  Meeting 3, the sums, publishes a
+                // wait that ran out.
+                bool stop3 = !mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1);
+                if (stop3) timeout();
+                const float l_other = exchange(xsum, l, stop3);
+                pair_sync();  // both have read the sums before xsum is written again
+                if (stop3) break;
+                tc::fence_after_sync();
+                const float lt = l + l_other;
+                float f = 1.f / lt;
+                if (P.sinks) {
+                    const float sk = __ldg(P.sinks + cur.head) * kLog2e;
+                    const float M2 = fmaxf(m, sk);
+                    const float c = exp2f(m - M2);
+                    f = c / (lt * c + exp2f(sk - M2));
+                }
+                float* orow = P.out + (static_cast<size_t>(cur.tok) * P.n_head + cur.head) * HD;
+#pragma unroll
+                for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lrow + C::C_O + c0, v);
+                    tc::tmem_ld_wait();
+                    if (cur.valid) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            *reinterpret_cast<float4*>(orow + c0 + c) =
+                                make_float4(__uint_as_float(v[c]) * f, __uint_as_float(v[c + 1]) * f,
+                                            __uint_as_float(v[c + 2]) * f, __uint_as_float(v[c + 3]) * f);
+                    }
+                }
                 tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(PREADY + 8 * (g & 1));
+                if (last) break;
+                cur = nxt;
             }
-            // The item's last O += P V (global tile g - 1; its commit covers
-            // every earlier MMA), then out = O / l (both halves' sums, sink
-            // included).  Meeting 3, the sums, is reached by both halves
-            // whether the tile loop ran out or both left it at a meeting;
-            // failed (set there, or by a wait that ran out after the last
-            // meeting) is published here.
-            bool ok = !failed;
-            if (ok && !mbar_wait(PVDONE + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1)) {
-                timeout();
-                ok = false;
-            }
-            bool stop3 = !ok;
-            const float l_other = exchange(xsum, l, stop3);
-            pair_sync();  // both have read the sums before xsum is written again
-            if (stop3) break;
-            tc::fence_after_sync();
-            const float lt = l + l_other;
-            float f = 1.f / lt;
-            if (P.sinks) {
-                const float sk = __ldg(P.sinks + head) * kLog2e;
-                const float M2 = fmaxf(m, sk);
-                const float c = exp2f(m - M2);
-                f = c / (lt * c + exp2f(sk - M2));
-            }
-            float* orow = P.out + (static_cast<size_t>(tok) * P.n_head + head) * HD;
-#pragma unroll
-            for (int c0 = hf * HH; c0 < (hf + 1) * HH; c0 += 32) {
-                uint32_t v[32];
-                tc::tmem_ld32(lrow + C::C_O + c0, v);
-                tc::tmem_ld_wait();
-                if (vrow) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4*>(orow + c0 + c) =
-                            make_float4(__uint_as_float(v[c]) * f, __uint_as_float(v[c + 1]) * f,
-                                        __uint_as_float(v[c + 2]) * f, __uint_as_float(v[c + 3]) * f);
-                }
-            }
-            tc::fence_before_sync();
         }
     }
     // ---------------------------------------------------------------- teardown
