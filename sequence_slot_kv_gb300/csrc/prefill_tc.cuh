@@ -24,8 +24,10 @@
 //         and then V (BK = 64 keys x hd, 128-byte swizzled boxes of 32
 //         floats) with TMA into a ring of half-stage slots (one operand's
 //         hi and lo buffers each: 3 slots for hd 128, 6 for hd 64);
-//       - warps 10-13 (converters): split each landed K tile in place into
-//         hi and lo operand buffers, and transpose each landed V tile into
+//       - warps 10-13 (converters): write each landed K tile's lo part
+//         beside it (the tensor core reads a TF32 operand's f32 bits with the
+//         low 13 mantissa bits ignored, so the landed tile is its own hi
+//         part), and transpose each landed V tile into
 //         a keys-contiguous layout while splitting it (TF32 MMA operands
 //         in shared memory are K-major: for O += P V that is V^T, [hd][keys]);
 //         keys past the item's last are zeroed;
@@ -38,8 +40,10 @@
 //         only after the PV before it has read it;
 //       - warps 0-7 (softmax; two threads per query row = TMEM lane, each
 //         with half of the columns, combining maxima and sums at pairwise
-//         named barriers): put the item's q rows (hi, lo) into TMEM, then
-//         per key tile read S,
+//         named barriers): put the item's q rows (hi, lo) into TMEM -- the
+//         next item's as soon as the current item's last P is written, so
+//         the next item's first QK overlaps the current item's epilogue --
+//         then per key tile read S,
 //         apply the causal mask (key <= the row's position), run a base-2
 //         online softmax with a lazily raised max, write P (hi over S, lo
 //         beside it) into the same buffer and, only when the max moves,
