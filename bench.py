@@ -20,7 +20,8 @@ roofline    one decode call's algorithmic HBM bytes over its mean (and
 per_config  the same figures for each of the four bandwidth-target
             workloads (mid, skewed, sinks, large), each timed on its own in
             the same run;
-cpu_baseline  the CPU oracle on the host's cores over a bounded sample.
+cpu_baseline  the CPU oracle on the host's cores over a bounded sample, and
+            the same rows on one thread.
 Under torchrun each rank runs its own copy of the workload on its own GPU
 (rows are independent; no collective on the data path): weak scaling.
 """
@@ -209,7 +210,7 @@ class OracleSample:
     history is regenerated on the host once, outside any timing; the oracle
     rewrites the same K/V rows on every call, so calls repeat exactly."""
 
-    def __init__(self, w, n_threads, flags=0, paged_bs=0):
+    def __init__(self, w, n_threads, flags=0, paged_bs=0, n_rows=None):
         import oracle
         self.o = oracle.default()
         self.w = w
@@ -218,7 +219,7 @@ class OracleSample:
         self.paged_bs = paged_bs
         # rows at evenly spaced quantiles of position, so the sample has the
         # workload's mix of history lengths
-        k = min(w.B, n_threads)
+        k = min(w.B, n_rows or n_threads)
         order = np.argsort(w.positions(0), kind="stable")
         self.rows = sorted(int(order[int(i)]) for i in
                            np.linspace(0, w.B - 1, k).round().astype(int))
@@ -249,8 +250,9 @@ class OracleSample:
               (f", norm options {self.flags}" if self.flags else "")
         return (f"{len(self.rows)} rows (positions {pos.min()}..{pos.max()}, mean "
                 f"{pos.mean():.0f}) of the {self.w.name} workload's "
-                f"first step per oracle call{how}, {steps} calls, {seconds:.1f} s, rows split "
-                f"over {self.n_threads} threads")
+                f"first step per oracle call{how}, {steps} calls, {seconds:.1f} s, "
+                + ("on one thread" if self.n_threads == 1 else
+                   f"rows split over {self.n_threads} threads"))
 
 
 def paged_oracle_sample(w, rows, bs):
@@ -274,9 +276,9 @@ def paged_oracle_sample(w, rows, bs):
     return K, V, tab
 
 
-def time_oracle(w, budget_s, n_threads, flags=0, paged_bs=0):
+def time_oracle(w, budget_s, n_threads, flags=0, paged_bs=0, n_rows=None):
     """rows/s of the oracle over calls on its sample until ``budget_s``."""
-    smp = OracleSample(w, n_threads, flags, paged_bs)
+    smp = OracleSample(w, n_threads, flags, paged_bs, n_rows)
     smp.step()                                       # warm caches and pages
     calls, spent = 0, 0.0
     while spent < budget_s:
@@ -716,8 +718,12 @@ def run_gpu(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         v, desc = time_oracle(w, args.cpu_budget, cores, flags=args.options, paged_bs=args.paged)
+        # the same rows on one thread
+        v1, desc1 = time_oracle(w, args.cpu_budget / 3, 1, flags=args.options,
+                                paged_bs=args.paged, n_rows=cores)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc,
+                                "single_thread": {"value": v1, "sample": desc1}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -858,8 +864,10 @@ def run_prefill(args):
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         v, desc = time_oracle_prefill(w, slots, pos, args.cpu_budget, cores)
+        v1, desc1 = time_oracle_prefill(w, slots, pos, args.cpu_budget / 3, 1)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc,
+                                "single_thread": {"value": v1, "sample": desc1}}
     print(json.dumps(line), flush=True)
     kv.free()
 
@@ -932,7 +940,8 @@ class PrefillOracleSample:
         last = int(self.first.max()) + min(calls, self.chunk) - 1
         return (f"{calls} calls of one prompt token of each of the {self.n_seq} sequences "
                 f"(one decode step per token, positions {int(self.first.min())}..{last}), "
-                f"{seconds:.1f} s, the sequences split over {self.n_threads} threads")
+                f"{seconds:.1f} s, " + ("on one thread" if self.n_threads == 1 else
+                                         f"the sequences split over {self.n_threads} threads"))
 
 
 def time_oracle_prefill(w, slots, pos, budget_s, n_threads):

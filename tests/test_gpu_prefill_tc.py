@@ -81,7 +81,7 @@ def test_long_runs_every_group_size(hd, G):
     history of several key tiles, a one-token run, and a run starting at
     position 0; the tokens of each run in increasing position."""
     MT = 128 // G
-    BK = 64 if hd == 64 else 32
+    BK = 64  # keys per key tile of the tensor-core prefill
     seqs = [(3, 7 * BK + 5, MT * 2 + MT // 2), (0, 41, 1), (1, 0, MT + 3)]
     slots = np.concatenate([np.full(n, s, np.uint32) for s, _, n in seqs])
     pos = np.concatenate([np.arange(h, h + n, dtype=np.uint32) for _, h, n in seqs])
