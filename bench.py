@@ -234,6 +234,11 @@ class OracleSample:
                      addr, w.q_norm_w(), w.k_norm_w(),
                      w.inv_freq(), w.sink_logits(), w.eps, w.scale)
 
+    @property
+    def threads(self):
+        """Threads the oracle actually runs (one row per thread at most)."""
+        return min(self.n_threads, len(self.rows))
+
     def step(self):
         t0 = time.perf_counter()
         if self.paged_bs:
@@ -284,7 +289,7 @@ def time_oracle(w, budget_s, n_threads, flags=0, paged_bs=0, n_rows=None):
     while spent < budget_s:
         spent += smp.step()
         calls += 1
-    return len(smp.rows) * calls / spent, smp.describe(calls, spent)
+    return len(smp.rows) * calls / spent, smp.describe(calls, spent), smp.threads
 
 
 def run_reference(args, w):
@@ -313,7 +318,7 @@ def run_reference(args, w):
         "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config,
-        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": smp.threads, "kind": "oracle",
                          "sample": smp.describe(args.steps, spent)},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -717,11 +722,12 @@ def run_gpu(args, w):
         line["per_config"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        v, desc = time_oracle(w, args.cpu_budget, cores, flags=args.options, paged_bs=args.paged)
+        v, desc, used = time_oracle(w, args.cpu_budget, cores, flags=args.options,
+                                    paged_bs=args.paged)
         # the same rows on one thread
-        v1, desc1 = time_oracle(w, args.cpu_budget / 3, 1, flags=args.options,
-                                paged_bs=args.paged, n_rows=cores)
-        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+        v1, desc1, _ = time_oracle(w, args.cpu_budget / 3, 1, flags=args.options,
+                                   paged_bs=args.paged, n_rows=cores)
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": used, "kind": "oracle",
                                 "sample": desc,
                                 "single_thread": {"value": v1, "sample": desc1}}
     if rank == 0:
@@ -863,9 +869,9 @@ def run_prefill(args):
             "clocks": clk}
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        v, desc = time_oracle_prefill(w, slots, pos, args.cpu_budget, cores)
-        v1, desc1 = time_oracle_prefill(w, slots, pos, args.cpu_budget / 3, 1)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores,
+        v, desc, used = time_oracle_prefill(w, slots, pos, args.cpu_budget, cores)
+        v1, desc1, _ = time_oracle_prefill(w, slots, pos, args.cpu_budget / 3, 1)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": used,
                                 "kind": "oracle", "sample": desc,
                                 "single_thread": {"value": v1, "sample": desc1}}
     print(json.dumps(line), flush=True)
@@ -924,6 +930,7 @@ class PrefillOracleSample:
         self.q, self.kn, self.vn = w.q(), w.k_new(), w.v_new()
         self.compact = np.arange(n_seq, dtype=np.uint32)
         self.calls = 0
+        self.threads = self.n_threads  # one sequence per thread at most
 
     def step(self):
         w = self.w
@@ -952,7 +959,7 @@ def time_oracle_prefill(w, slots, pos, budget_s, n_threads):
     while spent < budget_s and calls < PREFILL_CHUNK:
         spent += smp.step()
         calls += 1
-    return smp.n_seq * calls / spent, smp.describe(calls, spent)
+    return smp.n_seq * calls / spent, smp.describe(calls, spent), smp.threads
 
 
 def main():

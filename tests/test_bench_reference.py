@@ -44,6 +44,8 @@ def test_reference_line(flags):
     if "--prefill" in flags:
         assert d["unit"] == "tokens/s" and d["config"]["workload"] == "prefill"
         assert per_step == pytest.approx(8)
+        # one sequence per thread: the threads the oracle actually ran
+        assert cb["cores"] == min(os.cpu_count() or 1, 8)
     else:
         assert d["unit"] == "rows/s" and d["config"]["workload"] == "large"
         assert per_step == pytest.approx(min(256, cb["cores"]))
