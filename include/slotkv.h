@@ -53,6 +53,9 @@ enum slotkv_status {
     SLOTKV_ERR_STATE = 4        /* handle not allocated / already freed */
 };
 
+/* The most parts prefill_batch_attn_host cuts a call into. */
+#define SLOTKV_PREFILL_HOST_MAX_PARTS 4u
+
 /* Sticky device-side flags, read and cleared by slot_kv_get_status. */
 enum slotkv_device_flags {
     SLOTKV_DEV_RANGE = 1u,  /* some row had slots[b] >= n_slots or
@@ -230,12 +233,35 @@ int prefill_batch_attn(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const f
  * returns (page-locked buffers make the copies asynchronous DMA).  n_tok <=
  * max_rows.  Errors as prefill_batch_attn, plus SLOTKV_ERR_CUDA for a failed
  * copy.
+ *
+ * At head dims 64 and 128 a call of 2048 tokens or more is cut into parts
+ * whose tokens share no slot (slot_kv_prefill_host_parts says where): each
+ * part is a prefill of its own, with the same tiles and so the same bits,
+ * and one part's copies (inputs on one copy stream, outputs on another, both
+ * owned by the handle) overlap the other parts' kernels on `stream`.  A call
+ * that cannot be cut that way runs as one part.
  */
 int prefill_batch_attn_host(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const float* q,
                             const float* k_new, const float* v_new, const uint32_t* positions,
                             const uint32_t* slots, const float* q_norm_w,
                             const float* k_norm_w, const float* inv_freq, const float* sinks,
                             float* out, float eps, float scale, slotkv_stream_t stream);
+
+/*
+ * slot_kv_prefill_host_parts -- where prefill_batch_attn_host cuts a call of
+ * n_tok tokens with these slots (HOST pointer, by token) at head dims 64 and
+ * 128.  A cut before token m is allowed when no slot has tokens on both
+ * sides; the call gets one part per 1024 tokens, at most
+ * SLOTKV_PREFILL_HOST_MAX_PARTS, none under 512 tokens, each cut the allowed
+ * one nearest an equal share (fewer parts when too few cuts are allowed).
+ * Writes the part boundaries cuts[0] = 0 < cuts[1] < ... < cuts[*n_parts] =
+ * n_tok and the count to *n_parts (an empty call: one part, cuts {0, 0}).
+ * cuts_len is the number of entries cuts holds, at least
+ * SLOTKV_PREFILL_HOST_MAX_PARTS + 1.  Host only: no handle, no device work.
+ * Returns SLOTKV_ERR_ARG for a null pointer or a cuts_len below that.
+ */
+int slot_kv_prefill_host_parts(uint32_t n_tok, const uint32_t* slots, uint32_t* cuts,
+                               uint32_t cuts_len, uint32_t* n_parts);
 
 /*
  * decode_batch_attn_paged -- the decode step over a paged KV pool: instead of

@@ -10,8 +10,9 @@ The functions mirror the C ABI in ``include/slotkv.h`` name for name
 (``EXPORTS`` lists every symbol): the handle (``slot_kv_alloc``,
 ``slot_kv_free``, ``slot_kv_offset_bytes``, ``slot_kv_reset``), the step
 (``decode_batch_attn``, its host-buffer form ``decode_batch_attn_host``,
-``prefill_batch_attn``, ``decode_batch_attn_paged`` and its host-buffer form
-``decode_batch_attn_paged_host``, the allocation-free
+``prefill_batch_attn`` and its host-buffer form ``prefill_batch_attn_host``
+(with ``slot_kv_prefill_host_parts``), ``decode_batch_attn_paged`` and its
+host-buffer form ``decode_batch_attn_paged_host``, the allocation-free
 ``decode_batch_attn_noalloc``), multi-step support
 (``slot_kv_advance_positions``), and control (``slot_kv_get_status``,
 ``slot_kv_set_split``, ``slot_kv_set_options``, ``slot_kv_call_shape``).
@@ -23,7 +24,7 @@ import os
 __all__ = [
     "SlotKV", "SlotKVError", "slot_kv_alloc", "slot_kv_free", "slot_kv_offset_bytes",
     "slot_kv_reset", "decode_batch_attn", "decode_batch_attn_host", "prefill_batch_attn",
-    "prefill_batch_attn_host",
+    "prefill_batch_attn_host", "slot_kv_prefill_host_parts", "PREFILL_HOST_MAX_PARTS",
     "decode_batch_attn_paged", "decode_batch_attn_paged_host", "decode_batch_attn_noalloc",
     "slot_kv_advance_positions",
     "slot_kv_get_status", "slot_kv_set_split", "HostCall", "LIB_PATH", "EXPORTS", "DEV_RANGE",
@@ -36,6 +37,7 @@ DEV_TIMEOUT = 2
 OPT_VNORM = 1
 OPT_NORM_PLUS_ONE = 2
 OPT_TEST_STALL = 0x80000000
+PREFILL_HOST_MAX_PARTS = 4  # SLOTKV_PREFILL_HOST_MAX_PARTS
 SIZE_MAX = ctypes.c_size_t(-1).value
 
 _u32, _f32, _vp, _int = ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
@@ -54,6 +56,8 @@ EXPORTS = {
     "decode_batch_attn_host": (_DECODE_ARGS, _int),
     "prefill_batch_attn": (_DECODE_ARGS, _int),
     "prefill_batch_attn_host": (_DECODE_ARGS, _int),
+    "slot_kv_prefill_host_parts": ([_u32, _vp, ctypes.POINTER(_u32), _u32,
+                                    ctypes.POINTER(_u32)], _int),
     "decode_batch_attn_paged": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp, _vp,
                                  _vp, _vp, _f32, _f32, _vp], _int),
     "decode_batch_attn_paged_host": ([_vp, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _u32, _vp, _vp,
@@ -422,6 +426,20 @@ def prefill_batch_attn_host(h, q, k_new, v_new, positions, slots, q_norm_w, k_no
                             inv_freq, sinks, out, eps, scale, stream=None):
     return h.prefill_batch_attn_host(q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                                      inv_freq, sinks, out, eps, scale, stream)
+
+
+def slot_kv_prefill_host_parts(slots):
+    """Where prefill_batch_attn_host cuts a call with these slots (one per
+    token, a host sequence of ints): the part boundaries [0, ..., n_tok].
+    Host only."""
+    import numpy as np
+    sl = np.ascontiguousarray(np.asarray(slots).astype(np.uint32, copy=False))
+    cuts = (_u32 * (PREFILL_HOST_MAX_PARTS + 1))()
+    n = _u32()
+    _check(_lib.slot_kv_prefill_host_parts(len(sl), sl.ctypes.data if len(sl) else None, cuts,
+                                           len(cuts), ctypes.byref(n)),
+           "slot_kv_prefill_host_parts")
+    return [int(cuts[i]) for i in range(n.value + 1)]
 
 
 def decode_batch_attn_paged(h, q, k_new, v_new, positions, block_tables, q_norm_w, k_norm_w,

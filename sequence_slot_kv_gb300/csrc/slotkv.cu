@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <atomic>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/slotkv.h"
@@ -98,6 +99,10 @@ struct slotkv_s {
     size_t pf_q_elems = 0, pf_tok = 0;
     std::vector<slotkv_host_call_s*> calls;  // prepared host calls on this handle
     cudaStream_t copy_stream = nullptr;      // their enqueued input copies (created on demand)
+    // prefill_batch_attn_host in parts: its outputs' copies, and the order of
+    // copies and kernels (created on demand)
+    cudaStream_t out_stream = nullptr;
+    cudaEvent_t pf_ev[2 * SLOTKV_PREFILL_HOST_MAX_PARTS + 1] = {};
 };
 
 // A prepared host call (slot_kv_host_call_create): the arguments of
@@ -146,6 +151,9 @@ void release(slotkv_s* h) {
                           cudaSetDevice(h->device) == cudaSuccess;
     cudaDeviceSynchronize();
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+    if (h->out_stream) cudaStreamDestroy(h->out_stream);
+    for (cudaEvent_t ev : h->pf_ev)
+        if (ev) cudaEventDestroy(ev);
     free_workspace(h);
     cudaFree(h->status);
     cudaFree(h->st_q);
@@ -745,6 +753,48 @@ int decode_batch_attn(slotkv_t h, uint32_t B, uint32_t n_head, const float* q,
 }  // extern "C"
 
 namespace {
+// prefill_batch_attn_host cuts a call into parts whose tokens share no slot
+// (one part's host-link copies then overlap another part's kernels): one
+// part per kPfPartTok tokens, at most SLOTKV_PREFILL_HOST_MAX_PARTS, none
+// under kPfPartMin, each cut the allowed one nearest an equal share.
+constexpr uint32_t kPfPartTok = 1024, kPfPartMin = 512;
+
+uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
+    const uint32_t want = std::min<uint32_t>(SLOTKV_PREFILL_HOST_MAX_PARTS, n / kPfPartTok);
+    cut[0] = 0;
+    uint32_t np = 0;
+    if (want >= 2) {
+        // a cut before token m is allowed when tokens [0, m) hold every
+        // occurrence of their slots
+        std::unordered_map<uint32_t, uint32_t> last;
+        last.reserve(n);
+        for (uint32_t i = 0; i < n; ++i) last[slots[i]] = i;
+        std::vector<uint32_t> allowed;
+        uint32_t reach = 0;
+        for (uint32_t i = 0; i + 1 < n; ++i) {
+            reach = std::max(reach, last[slots[i]]);
+            if (reach == i) allowed.push_back(i + 1);
+        }
+        for (uint32_t j = 1; j < want; ++j) {
+            const uint64_t target = (uint64_t)n * j / want;
+            uint32_t best = 0;
+            uint64_t best_d = UINT64_MAX;
+            for (uint32_t m : allowed) {
+                if (m < cut[np] + kPfPartMin || (uint64_t)m + kPfPartMin > n) continue;
+                const uint64_t d = m > target ? m - target : target - m;
+                if (d < best_d) {
+                    best_d = d;
+                    best = m;
+                }
+            }
+            if (best == 0) break;
+            cut[++np] = best;
+        }
+    }
+    cut[++np] = n;
+    return np;
+}
+
 // The prefill step on device pointers (arguments already checked).
 int run_prefill(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
                 const float* k_new, const float* v_new, const uint32_t* positions,
@@ -790,9 +840,102 @@ int run_prefill(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
     if (rc != 0) return cuda_fail((cudaError_t)rc, "prefill kernel launch");
     return SLOTKV_OK;
 }
+
+// prefill_batch_attn_host in parts [cut[i], cut[i+1]) (slot-disjoint, so each
+// part is a prefill of its own with the same tiles and bits): inputs in on
+// the handle's copy stream part by part, each part's kernels on `s` once its
+// inputs have landed, its out back on the out stream while the next part
+// runs; `s` waits for the last copy and is synchronised.
+int prefill_host_in_parts(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
+                          const float* k_new, const float* v_new, const uint32_t* positions,
+                          const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
+                          const float* inv_freq, const float* sinks, float* out, float eps,
+                          float scale, cudaStream_t s, const uint32_t* cut, uint32_t parts) {
+    // the workspace at its full size first: a later part must not regrow
+    // (free) it while an earlier part's kernels still use it
+    int rc = prefill_workspace(h, n_tok, n_head);
+    if (rc != SLOTKV_OK) return rc;
+    cudaError_t e = cudaSuccess;
+    if (!h->copy_stream)
+        e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess && !h->out_stream)
+        e = cudaStreamCreateWithFlags(&h->out_stream, cudaStreamNonBlocking);
+    for (cudaEvent_t& ev : h->pf_ev)
+        if (e == cudaSuccess && !ev) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill copy streams");
+    const cudaStream_t cin = h->copy_stream, cout = h->out_stream;
+    cudaEvent_t* in_ready = h->pf_ev;                                // [parts]
+    cudaEvent_t* done = h->pf_ev + SLOTKV_PREFILL_HOST_MAX_PARTS;    // [parts]
+    cudaEvent_t entry = h->pf_ev[2 * SLOTKV_PREFILL_HOST_MAX_PARTS];  // then: outputs back
+    // whatever fails, nothing of this call is left running on return
+    auto bail = [&](cudaError_t err, const char* what) {
+        cudaStreamSynchronize(cin);
+        cudaStreamSynchronize(cout);
+        cudaStreamSynchronize(s);
+        return err == cudaSuccess ? rc : cuda_fail(err, what);
+    };
+    const size_t qrow = (size_t)n_head * h->head_dim, krow = h->kv_dim;
+    // the staging may still be read by work enqueued on s before this call
+    if ((e = cudaEventRecord(entry, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cin, entry, 0)) != cudaSuccess)
+        return bail(e, "prefill copy order");
+    for (uint32_t i = 0; i < parts; ++i) {
+        const size_t t0 = cut[i], nt = cut[i + 1] - cut[i];
+        if ((e = cudaMemcpyAsync(h->st_q + t0 * qrow, q + t0 * qrow, nt * qrow * sizeof(float),
+                                 cudaMemcpyHostToDevice, cin)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(h->st_k + t0 * krow, k_new + t0 * krow,
+                                 nt * krow * sizeof(float), cudaMemcpyHostToDevice, cin)) !=
+                cudaSuccess ||
+            (e = cudaMemcpyAsync(h->st_v + t0 * krow, v_new + t0 * krow,
+                                 nt * krow * sizeof(float), cudaMemcpyHostToDevice, cin)) !=
+                cudaSuccess ||
+            (e = cudaMemcpyAsync(h->st_pos + t0, positions + t0, nt * sizeof(uint32_t),
+                                 cudaMemcpyHostToDevice, cin)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(h->st_slots + t0, slots + t0, nt * sizeof(uint32_t),
+                                 cudaMemcpyHostToDevice, cin)) != cudaSuccess ||
+            (e = cudaEventRecord(in_ready[i], cin)) != cudaSuccess)
+            return bail(e, "host-to-device input copy");
+    }
+    for (uint32_t i = 0; i < parts; ++i) {
+        const size_t t0 = cut[i];
+        if ((e = cudaStreamWaitEvent(s, in_ready[i], 0)) != cudaSuccess)
+            return bail(e, "prefill copy order");
+        rc = run_prefill(h, cut[i + 1] - cut[i], n_head, h->st_q + t0 * qrow, h->st_k + t0 * krow,
+                         h->st_v + t0 * krow, h->st_pos + t0, h->st_slots + t0, q_norm_w,
+                         k_norm_w, inv_freq, sinks, h->st_out + t0 * qrow, eps, scale, s);
+        if (rc != SLOTKV_OK) return bail(cudaSuccess, nullptr);
+        if ((e = cudaEventRecord(done[i], s)) != cudaSuccess)
+            return bail(e, "prefill copy order");
+    }
+    for (uint32_t i = 0; i < parts; ++i) {
+        const size_t t0 = cut[i], nt = cut[i + 1] - cut[i];
+        if ((e = cudaStreamWaitEvent(cout, done[i], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(out + t0 * qrow, h->st_out + t0 * qrow,
+                                 nt * qrow * sizeof(float), cudaMemcpyDeviceToHost, cout)) !=
+                cudaSuccess)
+            return bail(e, "device-to-host output copy");
+    }
+    if ((e = cudaEventRecord(entry, cout)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, entry, 0)) != cudaSuccess)
+        return bail(e, "prefill copy order");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+    return SLOTKV_OK;
+}
 }  // namespace
 
 extern "C" {
+
+int slot_kv_prefill_host_parts(uint32_t n_tok, const uint32_t* slots, uint32_t* cuts,
+                               uint32_t cuts_len, uint32_t* n_parts) {
+    g_err[0] = 0;
+    if (!cuts || !n_parts || (n_tok && !slots))
+        return fail(SLOTKV_ERR_ARG, "slots, cuts and n_parts must not be null");
+    if (cuts_len < SLOTKV_PREFILL_HOST_MAX_PARTS + 1)
+        return fail(SLOTKV_ERR_ARG, "cuts holds %u entries, fewer than %u", cuts_len,
+                    SLOTKV_PREFILL_HOST_MAX_PARTS + 1);
+    *n_parts = prefill_parts(n_tok, slots, cuts);
+    return SLOTKV_OK;
+}
 
 int prefill_batch_attn(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
                        const float* k_new, const float* v_new, const uint32_t* positions,
@@ -816,12 +959,18 @@ int prefill_batch_attn_host(slotkv_t h, uint32_t n_tok, uint32_t n_head, const f
     int rc = check_decode_args(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w,
                                k_norm_w, inv_freq, out, false);
     if (rc != SLOTKV_OK || n_tok == 0) return rc;
-    const HostStep hs{q, k_new, v_new, positions, slots, (size_t)n_tok * sizeof(uint32_t),
-                      h->st_slots, out};
     // A prefill moves tens of MB each way: the copy engines move them faster
     // than a gather kernel, and an out written into host memory by the
     // attention kernel itself would stall its epilogue on the host link, so
     // every buffer goes through cudaMemcpyAsync and device staging.
+    uint32_t cut[SLOTKV_PREFILL_HOST_MAX_PARTS + 1];
+    const uint32_t parts = h->tc_prefill ? prefill_parts(n_tok, slots, cut) : 1u;
+    if (parts > 1)
+        return prefill_host_in_parts(h, n_tok, n_head, q, k_new, v_new, positions, slots,
+                                     q_norm_w, k_norm_w, inv_freq, sinks, out, eps, scale,
+                                     (cudaStream_t)stream, cut, parts);
+    const HostStep hs{q, k_new, v_new, positions, slots, (size_t)n_tok * sizeof(uint32_t),
+                      h->st_slots, out};
     void* const none[6] = {};
     return host_step_resolved(
         h, n_tok, n_head, hs, false, none, (cudaStream_t)stream,

@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 from gpu_harness import assert_close, to_dev
-from sequence_slot_kv_gb300 import SlotKV
+from sequence_slot_kv_gb300 import SlotKV, slot_kv_prefill_host_parts
 
 pytestmark = pytest.mark.gpu
 
@@ -125,16 +125,8 @@ def test_bench_prefill_workload_full_size():
     assert_close(got[rows], ref, "prefill workload sampled tokens")
 
 
-@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
-def test_prefill_host_entry_equals_device_entry(pinned):
-    """prefill_batch_attn_host (tokens' tensors and out in host memory) runs
-    the same kernels as the device entry on the same values: the same output
-    and the same slot bytes, bit for bit."""
-    hd, G = 128, 4
-    slots = np.concatenate([np.full(70, 1, np.uint32), np.full(33, 3, np.uint32)])
-    pos = np.concatenate([np.arange(200, 270, dtype=np.uint32), np.arange(0, 33, dtype=np.uint32)])
-    w = _workload(hd, G, 2, 95, len(pos), 5, 300)
-    got_dev, Kd, Vd = _run(w, slots, pos)
+def _run_host(w, slots, pos, pinned):
+    """prefill_batch_attn_host on fresh slots holding the same history."""
     shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
     K = torch.empty(shape, device="cuda")
     V = torch.empty(shape, device="cuda")
@@ -151,7 +143,56 @@ def test_prefill_host_entry_equals_device_entry(pinned):
                                    to_dev(w.inv_freq()), None if s is None else to_dev(s), out,
                                    w.eps, w.scale)
         assert kv.get_status() == 0
-        assert np.array_equal(out.numpy().view(np.uint32), got_dev.view(np.uint32))
-        assert torch.equal(K, Kd) and torch.equal(V, Vd)
+        return out.numpy(), K, V
     finally:
         kv.free()
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_prefill_host_entry_equals_device_entry(pinned):
+    """prefill_batch_attn_host (tokens' tensors and out in host memory) runs
+    the same kernels as the device entry on the same values: the same output
+    and the same slot bytes, bit for bit."""
+    hd, G = 128, 4
+    slots = np.concatenate([np.full(70, 1, np.uint32), np.full(33, 3, np.uint32)])
+    pos = np.concatenate([np.arange(200, 270, dtype=np.uint32), np.arange(0, 33, dtype=np.uint32)])
+    w = _workload(hd, G, 2, 95, len(pos), 5, 300)
+    got_dev, Kd, Vd = _run(w, slots, pos)
+    got, K, V = _run_host(w, slots, pos, pinned)
+    assert np.array_equal(got.view(np.uint32), got_dev.view(np.uint32))
+    assert torch.equal(K, Kd) and torch.equal(V, Vd)
+
+
+# (head dim, G, run lengths, the runs' slots, parts the host entry makes)
+PART_LAYOUTS = {
+    "equal_hd128": (128, 4, [512] * 8, None, 4),
+    "uneven_hd64": (64, 8, [1500, 100, 900, 1700], None, 3),
+    "returning_slot_hd128": (128, 2, [800] * 4, [0, 1, 0, 2], 2),
+    "interleaved_hd64": (64, 4, [1] * 2048, [0, 1] * 1024, 1),
+}
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("name", list(PART_LAYOUTS))
+def test_prefill_host_entry_in_parts_equals_device_entry(name, pinned):
+    """A host call of 2048 tokens or more is cut into parts whose tokens
+    share no slot, each run as a prefill of its own while the others' copies
+    move: the output and the slot bytes stay those of one device call, bit
+    for bit (the parts hold the same runs, so the same tiles)."""
+    hd, G, lengths, ids, n_parts = PART_LAYOUTS[name]
+    ids = list(range(len(lengths))) if ids is None else ids
+    slots = np.concatenate([np.full(n, s, np.uint32) for s, n in zip(ids, lengths)])
+    # each slot's runs continue its positions after a history of its own
+    nxt, pos = {}, []
+    for s_, n in zip(ids, lengths):
+        p0 = nxt.get(s_, 40 + 13 * s_)
+        pos.append(np.arange(p0, p0 + n, dtype=np.uint32))
+        nxt[s_] = p0 + n
+    pos = np.concatenate(pos)
+    assert len(slot_kv_prefill_host_parts(slots)) - 1 == n_parts
+    w = _workload(hd, G, 2, 960 + list(PART_LAYOUTS).index(name), len(pos), int(slots.max()) + 1,
+                  int(pos.max()) + 3)
+    got_dev, Kd, Vd = _run(w, slots, pos)
+    got, K, V = _run_host(w, slots, pos, pinned)
+    assert np.array_equal(got.view(np.uint32), got_dev.view(np.uint32))
+    assert torch.equal(K, Kd) and torch.equal(V, Vd)

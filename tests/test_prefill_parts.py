@@ -1,0 +1,99 @@
+"""Where prefill_batch_attn_host cuts a call (slot_kv_prefill_host_parts,
+host logic only): parts whose tokens share no slot, one per 1024 tokens and
+at most four, none under 512 tokens, each cut the allowed one nearest an
+equal share; a call that cannot be cut that way stays whole.  Each part is a
+prefill of its own, so a cut with a slot on both sides would let one part's
+tokens miss keys the other part writes ("Forward Cuda Gemma", prefillBatched:
+every token attends its own slot's keys 0..pos)."""
+import numpy as np
+import pytest
+
+import sequence_slot_kv_gb300 as skv
+from sequence_slot_kv_gb300 import slot_kv_prefill_host_parts as parts
+
+
+def _seqs(lengths, slot_ids=None):
+    ids = range(len(lengths)) if slot_ids is None else slot_ids
+    return np.concatenate([np.full(n, s, np.uint32) for s, n in zip(ids, lengths)])
+
+
+def _check_valid(slots, cuts):
+    n = len(slots)
+    assert cuts[0] == 0 and cuts[-1] == n
+    assert all(a < b for a, b in zip(cuts, cuts[1:]))
+    assert len(cuts) - 1 <= min(skv.PREFILL_HOST_MAX_PARTS, max(1, n // 1024))
+    if len(cuts) > 2:
+        assert all(b - a >= 512 for a, b in zip(cuts, cuts[1:]))
+    for m in cuts[1:-1]:
+        assert not set(slots[:m].tolist()) & set(slots[m:].tolist())
+
+
+def test_small_calls_stay_whole():
+    assert parts([]) == [0, 0]  # one empty part
+    assert parts(_seqs([700, 700])) == [0, 1400]
+    assert parts(_seqs([1023, 1024])) == [0, 2047]
+
+
+def test_equal_sequences_cut_into_equal_parts():
+    assert parts(_seqs([512] * 8)) == [0, 1024, 2048, 3072, 4096]
+    assert parts(_seqs([1024] * 2)) == [0, 1024, 2048]
+    # more tokens than four parts' worth: still four parts
+    assert parts(_seqs([1000] * 7)) == [0, 2000, 3000, 5000, 7000]
+
+
+def test_no_allowed_cut_keeps_one_part():
+    assert parts(np.full(3000, 5, np.uint32)) == [0, 3000]
+    # two slots interleaved token by token: every prefix holds both
+    assert parts(np.tile(np.array([1, 2], np.uint32), 2048)) == [0, 4096]
+    # a slot at both ends
+    assert parts(_seqs([10, 4000, 10], [7, 8, 7])) == [0, 4020]
+
+
+def test_uneven_sequences_take_the_nearest_allowed_cuts():
+    # targets 1050, 2100, 3150; allowed cuts 1500, 1600, 2500; a third part
+    # boundary would leave a part under 512 tokens
+    assert parts(_seqs([1500, 100, 900, 1700])) == [0, 1500, 2500, 4200]
+
+
+def test_a_slot_returning_later_joins_its_part():
+    # slot 0 again after slot 1: nothing may cut between its runs
+    s = _seqs([800, 800, 800, 800], [0, 1, 0, 2])
+    cuts = parts(s)
+    _check_valid(s, cuts)
+    assert cuts == [0, 2400, 3200]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_layouts(seed):
+    rng = np.random.default_rng(seed)
+    k = int(rng.integers(1, 12))
+    lengths = rng.integers(1, 1500, size=k)
+    ids = rng.integers(0, max(1, k - int(rng.integers(0, 3))), size=k)
+    s = _seqs(lengths, ids)
+    if seed % 4 == 0:  # a few tokens moved to other places
+        idx = rng.choice(len(s), size=min(len(s), 5), replace=False)
+        s[idx] = s[rng.permutation(idx)]
+    _check_valid(s, parts(s))
+
+
+def test_bad_arguments_are_refused():
+    import ctypes
+    n = ctypes.c_uint32()
+    cuts = (ctypes.c_uint32 * 5)()
+    assert skv._lib.slot_kv_prefill_host_parts(4, None, cuts, 5, ctypes.byref(n)) == 1
+    assert skv._lib.slot_kv_prefill_host_parts(0, None, None, 5, ctypes.byref(n)) == 1
+    # a cuts array too short for the most parts a call can have
+    s = _seqs([512] * 8)
+    assert skv._lib.slot_kv_prefill_host_parts(len(s), s.ctypes.data, cuts, 4,
+                                               ctypes.byref(n)) == 1
+    assert skv._lib.slot_kv_prefill_host_parts(0, None, cuts, 5, ctypes.byref(n)) == 0
+    assert n.value == 1 and cuts[0] == 0 and cuts[1] == 0
+
+
+def test_python_constant_matches_the_header():
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "include", "slotkv.h")) as f:
+        m = re.search(r"#define SLOTKV_PREFILL_HOST_MAX_PARTS (\d+)u", f.read())
+    assert m and int(m.group(1)) == skv.PREFILL_HOST_MAX_PARTS
