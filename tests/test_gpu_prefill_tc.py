@@ -196,3 +196,40 @@ def test_prefill_host_entry_in_parts_equals_device_entry(name, pinned):
     got, K, V = _run_host(w, slots, pos, pinned)
     assert np.array_equal(got.view(np.uint32), got_dev.view(np.uint32))
     assert torch.equal(K, Kd) and torch.equal(V, Vd)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefill_host_in_parts_random_layouts(seed):
+    """Seeded random calls of 2048 to 3500 tokens: runs of random lengths on
+    slots that may come back later in the call, at either head dim and a
+    random G; the host entry (cut where its parts allow) equals one device
+    call bit for bit."""
+    rng = np.random.default_rng(7100 + seed)
+    hd = (64, 128)[seed % 2]
+    G = int(rng.integers(1, 9))
+    n_target = int(rng.integers(2048, 3500))
+    lengths, ids = [], []
+    n_slots = int(rng.integers(3, 10))
+    while sum(lengths) < n_target:
+        lengths.append(int(rng.integers(1, 900)))
+        ids.append(int(rng.integers(0, n_slots)))
+    lengths[-1] -= sum(lengths) - n_target
+    if lengths[-1] == 0:
+        lengths.pop()
+        ids.pop()
+    slots = np.concatenate([np.full(n, s, np.uint32) for s, n in zip(ids, lengths)])
+    nxt, pos = {}, []
+    for s_, n in zip(ids, lengths):
+        p0 = nxt.get(s_, int(rng.integers(0, 200)))
+        pos.append(np.arange(p0, p0 + n, dtype=np.uint32))
+        nxt[s_] = p0 + n
+    pos = np.concatenate(pos)
+    cuts = slot_kv_prefill_host_parts(slots)
+    for m in cuts[1:-1]:
+        assert not set(slots[:m].tolist()) & set(slots[m:].tolist())
+    w = _workload(hd, G, 2, 980 + seed, len(pos), n_slots, int(pos.max()) + 3,
+                  sinks=(seed % 3 == 0))
+    got_dev, Kd, Vd = _run(w, slots, pos)
+    got, K, V = _run_host(w, slots, pos, pinned=True)
+    assert np.array_equal(got.view(np.uint32), got_dev.view(np.uint32))
+    assert torch.equal(K, Kd) and torch.equal(V, Vd)
