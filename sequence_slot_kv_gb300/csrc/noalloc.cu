@@ -52,7 +52,7 @@ typedef CUresult (*ctx_get_current_fn)(CUcontext*);
 typedef CUresult (*ctx_get_id_fn)(CUcontext, unsigned long long*);
 
 // The unique id of the calling thread's current context; false when no
-// context is current yet or the driver cannot say.  Call with
+// context is current yet or the CUDA driver API cannot say.  Call with
 // g_setup_mutex held.
 bool current_context_id(unsigned long long* id) {
     static ctx_get_current_fn get_current = nullptr;
