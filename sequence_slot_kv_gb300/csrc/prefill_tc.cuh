@@ -3,7 +3,8 @@
 // call at once, equal to running them one decode step at a time; "Forward
 // Cuda", batched prefill into the given slot).
 //
-// Three kernels per call, on one stream:
+// Three kernels per call, on one stream (the plan launched first, prep
+// beside it as a programmatic dependent, the attention kernel after both):
 //   * slotkv_prefill_prep_kernel: one warp per (token, 8 heads).  Query heads:
 //     q' = RoPE(RMSnorm(q) * w) * scale * log2(e) into a workspace; kv heads:
 //     k' = RoPE(RMSnorm(k_new) * w) and v into the token's slot row.  The
@@ -222,6 +223,10 @@ __global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const Pref
     __shared__ uint32_t warp_sum[32];
     __shared__ int carry_start;
     __shared__ uint32_t carry_tiles;
+    // The prep kernel, launched next as a programmatic dependent, may start
+    // at once: it reads none of what this kernel writes and writes none of
+    // what it reads, and the attention kernel after both waits for both.
+    grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         carry_start = -1;
@@ -901,8 +906,24 @@ int launch_prefill_one(const PrefillParams& p, const CUtensorMap& tmK, const CUt
     }
     const uint32_t groups = (p.n_head + p.n_kv_head + kPrepHeads - 1) / kPrepHeads;
     const uint32_t warps = p.n_tok * groups;
-    slotkv_prefill_prep_kernel<HD><<<(warps + 3) / 4, 128, prep_smem_bytes<HD>(), stream>>>(p);
+    // the plan (one CTA) first, then prep beside it as its programmatic
+    // dependent; the attention kernel, launched in stream order, waits for
+    // both.  Prep starts only once the plan runs, hence after the previous
+    // call's attention kernel has finished reading the rows and q workspace
+    // that prep overwrites.
     slotkv_prefill_plan_kernel<C::MT><<<1, 1024, 0, stream>>>(p);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((warps + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = prep_smem_bytes<HD>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, slotkv_prefill_prep_kernel<HD>, p);
+    if (e != cudaSuccess) return static_cast<int>(e);
     slotkv_prefill_tc_kernel<HD, G><<<ctas, C::THREADS, C::SMEM, stream>>>(tmK, tmV, p);
     return static_cast<int>(cudaGetLastError());
 }
