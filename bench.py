@@ -80,10 +80,10 @@ def measured_traffic(workload):
 
 
 # DRAM read + write bytes of one tensor-core prefill kernel launch on the
-# prefill workload of a geometry (ncu, the mean of ten launches' one-pass
-# counters), keyed by code_hash of prefill_tc.cuh; reported only while the
-# kernel is the one measured.
-MEASURED_PREFILL_TRAFFIC = {"b7663287658bb425": {"mid": 244_639_155, "sinks": 172_958_515}}
+# prefill workload of a geometry (ncu one-pass counters, the mean over the
+# full-size calls' launches), keyed by code_hash of prefill_tc.cuh; reported
+# only while the kernel is the one measured.
+MEASURED_PREFILL_TRAFFIC = {"162167dbdc64de45": {"mid": 245_160_106, "sinks": 172_854_186}}
 
 
 def prefill_source_hash():
