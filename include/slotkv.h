@@ -253,7 +253,10 @@ int prefill_batch_attn_host(slotkv_t handle, uint32_t n_tok, uint32_t n_head, co
  * 128.  A cut before token m is allowed when no slot has tokens on both
  * sides; the call gets one part per 1024 tokens, at most
  * SLOTKV_PREFILL_HOST_MAX_PARTS, none under 512 tokens, each cut the allowed
- * one nearest an equal share (fewer parts when too few cuts are allowed).
+ * one nearest its target (fewer parts when too few cuts are allowed).  The
+ * targets n_tok (2j - 1) / (2 (parts - 1)), j = 1 .. parts - 1, make the
+ * first and the last part half the size of the others, since the first
+ * part's input copies and the last part's output copies overlap nothing.
  * Writes the part boundaries cuts[0] = 0 < cuts[1] < ... < cuts[*n_parts] =
  * n_tok and the count to *n_parts (an empty call: one part, cuts {0, 0}).
  * cuts_len is the number of entries cuts holds, at least

@@ -756,7 +756,9 @@ namespace {
 // prefill_batch_attn_host cuts a call into parts whose tokens share no slot
 // (one part's host-link copies then overlap another part's kernels): one
 // part per kPfPartTok tokens, at most SLOTKV_PREFILL_HOST_MAX_PARTS, none
-// under kPfPartMin, each cut the allowed one nearest an equal share.
+// under kPfPartMin, each cut the allowed one nearest its target.  The
+// targets make the first and the last part half the size of the others:
+// the first part's inputs and the last part's output overlap nothing.
 constexpr uint32_t kPfPartTok = 1024, kPfPartMin = 512;
 
 uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
@@ -776,7 +778,7 @@ uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
             if (reach == i) allowed.push_back(i + 1);
         }
         for (uint32_t j = 1; j < want; ++j) {
-            const uint64_t target = (uint64_t)n * j / want;
+            const uint64_t target = (uint64_t)n * (2 * j - 1) / (2 * (want - 1));
             uint32_t best = 0;
             uint64_t best_d = UINT64_MAX;
             for (uint32_t m : allowed) {

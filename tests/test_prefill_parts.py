@@ -1,7 +1,8 @@
 """Where prefill_batch_attn_host cuts a call (slot_kv_prefill_host_parts,
 host logic only): parts whose tokens share no slot, one per 1024 tokens and
-at most four, none under 512 tokens, each cut the allowed one nearest an
-equal share; a call that cannot be cut that way stays whole.  Each part is a
+at most four, none under 512 tokens, each cut the allowed one nearest its
+target, the targets giving the first and the last part half the size of the
+others; a call that cannot be cut that way stays whole.  Each part is a
 prefill of its own, so a cut with a slot on both sides would let one part's
 tokens miss keys the other part writes ("Forward Cuda Gemma", prefillBatched:
 every token attends its own slot's keys 0..pos)."""
@@ -34,11 +35,13 @@ def test_small_calls_stay_whole():
     assert parts(_seqs([1023, 1024])) == [0, 2047]
 
 
-def test_equal_sequences_cut_into_equal_parts():
-    assert parts(_seqs([512] * 8)) == [0, 1024, 2048, 3072, 4096]
+def test_equal_sequences_cut_with_half_size_ends():
+    # targets 4096 * (1, 3, 5) / 6 = 683, 2048, 3413
+    assert parts(_seqs([512] * 8)) == [0, 512, 2048, 3584, 4096]
     assert parts(_seqs([1024] * 2)) == [0, 1024, 2048]
-    # more tokens than four parts' worth: still four parts
-    assert parts(_seqs([1000] * 7)) == [0, 2000, 3000, 5000, 7000]
+    # more tokens than four parts' worth: still four parts (targets 1167,
+    # 3500, 5833; of two cuts equally near, the first)
+    assert parts(_seqs([1000] * 7)) == [0, 1000, 3000, 6000, 7000]
 
 
 def test_no_allowed_cut_keeps_one_part():
@@ -50,7 +53,7 @@ def test_no_allowed_cut_keeps_one_part():
 
 
 def test_uneven_sequences_take_the_nearest_allowed_cuts():
-    # targets 1050, 2100, 3150; allowed cuts 1500, 1600, 2500; a third part
+    # targets 700, 2100, 3500; allowed cuts 1500, 1600, 2500; a third part
     # boundary would leave a part under 512 tokens
     assert parts(_seqs([1500, 100, 900, 1700])) == [0, 1500, 2500, 4200]
 
