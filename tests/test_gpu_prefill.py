@@ -201,3 +201,42 @@ def test_prefill_of_one_token_matches_decode():
         kv.free()
     assert_close(outs[1], outs[0], "one-token prefill vs decode")
     assert torch.equal(bufs[0][0], bufs[1][0]) and torch.equal(bufs[0][1], bufs[1][1])
+
+
+HOST_CASES = [(64, 4), (128, 2), (256, 2)]
+
+
+@pytest.mark.parametrize("hd,G", HOST_CASES, ids=[f"hd{h}_g{g}" for h, g in HOST_CASES])
+def test_prefill_host_entry_every_head_dim(hd, G):
+    """prefill_batch_attn_host with pageable host tensors, at every head
+    dim (hd 256 runs the decode kernel once per token behind it): the same
+    output and slot bytes as the device entry, bit for bit, and the oracle's
+    token-by-token result within tolerance."""
+    T = 4096 // hd
+    seqs = [(2, 3, 2 * T + 7), (0, 4 * T + 1, T - 2), (1, 0, 5)]
+    w, slots, pos = _setup(hd, G, 80 + HOST_CASES.index((hd, G)), seqs)
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    outs, kvs = [], []
+    for host in (False, True):
+        K = torch.empty(shape, device="cuda")
+        V = torch.empty(shape, device="cuda")
+        w.dev_fill_history(K.data_ptr(), V.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        kv = SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K,
+                    v_buf=V)
+        try:
+            put = (lambda a: torch.from_numpy(np.ascontiguousarray(a))) if host else to_dev
+            out = put(np.full((w.B, w.n_head, w.head_dim), np.nan, np.float32))
+            fn = kv.prefill_batch_attn_host if host else kv.prefill_batch_attn
+            fn(put(w.q()), put(w.k_new()), put(w.v_new()), put(pos.astype(np.int32)),
+               put(slots.astype(np.int32)), to_dev(w.q_norm_w()), to_dev(w.k_norm_w()),
+               to_dev(w.inv_freq()), to_dev(w.sink_logits()), out, w.eps, w.scale)
+            torch.cuda.synchronize()
+            assert kv.get_status() == 0
+            outs.append(out.cpu().numpy())
+            kvs.append((K, V))
+        finally:
+            kv.free()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert torch.equal(kvs[0][0], kvs[1][0]) and torch.equal(kvs[0][1], kvs[1][1])
+    ref, _, _ = _oracle(w, slots, pos)
+    assert_close(outs[1], ref, f"host-entry prefill hd={hd} G={G}")
