@@ -765,7 +765,8 @@ uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
     const uint32_t want = std::min<uint32_t>(SLOTKV_PREFILL_HOST_MAX_PARTS, n / kPfPartTok);
     cut[0] = 0;
     uint32_t np = 0;
-    if (want >= 2) {
+    // (host memory for the search; should it run out, the call stays whole)
+    if (want >= 2) try {
         // a cut before token m is allowed when tokens [0, m) hold every
         // occurrence of their slots
         std::unordered_map<uint32_t, uint32_t> last;
@@ -792,6 +793,8 @@ uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
             if (best == 0) break;
             cut[++np] = best;
         }
+    } catch (const std::bad_alloc&) {
+        np = 0;
     }
     cut[++np] = n;
     return np;
