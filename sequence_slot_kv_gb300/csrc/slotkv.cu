@@ -1112,7 +1112,12 @@ int slot_kv_host_call_create(slotkv_t h, slotkv_host_call_t* call, uint32_t B,
     c->scale = scale;
     const HostStep hs{q, k_new, v_new, positions, idx, idx_bytes, nullptr, out};
     c->mapped = resolve_mapped(hs, c->dp);
-    h->calls.push_back(c);
+    try {
+        h->calls.push_back(c);
+    } catch (const std::bad_alloc&) {
+        delete c;
+        return fail(SLOTKV_ERR_ARG, "out of host memory");
+    }
     *call = c;
     return SLOTKV_OK;
 }
