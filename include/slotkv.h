@@ -54,7 +54,7 @@ enum slotkv_status {
 };
 
 /* The most parts prefill_batch_attn_host cuts a call into. */
-#define SLOTKV_PREFILL_HOST_MAX_PARTS 4u
+#define SLOTKV_PREFILL_HOST_MAX_PARTS 8u
 
 /* Sticky device-side flags, read and cleared by slot_kv_get_status. */
 enum slotkv_device_flags {
@@ -234,12 +234,15 @@ int prefill_batch_attn(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const f
  * max_rows.  Errors as prefill_batch_attn, plus SLOTKV_ERR_CUDA for a failed
  * copy.
  *
- * At head dims 64 and 128 a call of 2048 tokens or more is cut into parts
+ * At head dims 64 and 128 a call of 1024 tokens or more is cut into parts
  * whose tokens share no slot (slot_kv_prefill_host_parts says where): each
  * part is a prefill of its own, with the same tiles and so the same bits,
- * and one part's copies (inputs on one copy stream, outputs on another, both
- * owned by the handle) overlap the other parts' kernels on `stream`.  A call
- * that cannot be cut that way runs as one part.
+ * its own rows of the handle's workspace and its own plan counters.  Inputs
+ * go in on a copy stream owned by the handle, the parts' kernels run on
+ * `stream` and a second stream of the handle by turns (a part's kernels
+ * start on the SMs the previous part frees), and each part's output comes
+ * back on a second copy stream while later parts run.  A call that cannot
+ * be cut that way runs as one part.
  */
 int prefill_batch_attn_host(slotkv_t handle, uint32_t n_tok, uint32_t n_head, const float* q,
                             const float* k_new, const float* v_new, const uint32_t* positions,
@@ -251,8 +254,8 @@ int prefill_batch_attn_host(slotkv_t handle, uint32_t n_tok, uint32_t n_head, co
  * slot_kv_prefill_host_parts -- where prefill_batch_attn_host cuts a call of
  * n_tok tokens with these slots (HOST pointer, by token) at head dims 64 and
  * 128.  A cut before token m is allowed when no slot has tokens on both
- * sides; the call gets one part per 1024 tokens, at most
- * SLOTKV_PREFILL_HOST_MAX_PARTS, none under 512 tokens, each cut the allowed
+ * sides; the call gets one part per 512 tokens, at most
+ * SLOTKV_PREFILL_HOST_MAX_PARTS, none under 256 tokens, each cut the allowed
  * one nearest its target (fewer parts when too few cuts are allowed).  The
  * targets n_tok (2j - 1) / (2 (parts - 1)), j = 1 .. parts - 1, make the
  * first and the last part half the size of the others, since the first

@@ -37,7 +37,7 @@ DEV_TIMEOUT = 2
 OPT_VNORM = 1
 OPT_NORM_PLUS_ONE = 2
 OPT_TEST_STALL = 0x80000000
-PREFILL_HOST_MAX_PARTS = 4  # SLOTKV_PREFILL_HOST_MAX_PARTS
+PREFILL_HOST_MAX_PARTS = 8  # SLOTKV_PREFILL_HOST_MAX_PARTS
 SIZE_MAX = ctypes.c_size_t(-1).value
 
 _u32, _f32, _vp, _int = ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p, ctypes.c_int

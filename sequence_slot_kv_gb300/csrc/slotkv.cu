@@ -99,10 +99,11 @@ struct slotkv_s {
     size_t pf_q_elems = 0, pf_tok = 0;
     std::vector<slotkv_host_call_s*> calls;  // prepared host calls on this handle
     cudaStream_t copy_stream = nullptr;      // their enqueued input copies (created on demand)
-    // prefill_batch_attn_host in parts: its outputs' copies, and the order of
-    // copies and kernels (created on demand)
-    cudaStream_t out_stream = nullptr;
-    cudaEvent_t pf_ev[2 * SLOTKV_PREFILL_HOST_MAX_PARTS + 1] = {};
+    // prefill_batch_attn_host in parts: its outputs' copies, the second
+    // stream its parts alternate on, and the order of copies and kernels
+    // (created on demand)
+    cudaStream_t out_stream = nullptr, pf_stream2 = nullptr;
+    cudaEvent_t pf_ev[2 * SLOTKV_PREFILL_HOST_MAX_PARTS + 2] = {};
 };
 
 // A prepared host call (slot_kv_host_call_create): the arguments of
@@ -152,6 +153,7 @@ void release(slotkv_s* h) {
     cudaDeviceSynchronize();
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     if (h->out_stream) cudaStreamDestroy(h->out_stream);
+    if (h->pf_stream2) cudaStreamDestroy(h->pf_stream2);
     for (cudaEvent_t ev : h->pf_ev)
         if (ev) cudaEventDestroy(ev);
     free_workspace(h);
@@ -256,7 +258,9 @@ int prefill_workspace(slotkv_s* h, uint32_t n_tok, uint32_t n_head) {
             return cuda_fail(e, "prefill workspace (tiles)");
         h->pf_tok = n_tok;
     }
-    if (!h->pf_plan && (e = cudaMalloc(&h->pf_plan, 2 * sizeof(uint32_t))) != cudaSuccess)
+    // one (items, hand-out counter) pair per part of a host call in parts
+    if (!h->pf_plan && (e = cudaMalloc(&h->pf_plan, 2 * SLOTKV_PREFILL_HOST_MAX_PARTS *
+                                                        sizeof(uint32_t))) != cudaSuccess)
         return cuda_fail(e, "prefill workspace (plan)");
     return SLOTKV_OK;
 }
@@ -759,7 +763,7 @@ namespace {
 // under kPfPartMin, each cut the allowed one nearest its target.  The
 // targets make the first and the last part half the size of the others:
 // the first part's inputs and the last part's output overlap nothing.
-constexpr uint32_t kPfPartTok = 1024, kPfPartMin = 512;
+constexpr uint32_t kPfPartTok = 512, kPfPartMin = 256;
 
 uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
     const uint32_t want = std::min<uint32_t>(SLOTKV_PREFILL_HOST_MAX_PARTS, n / kPfPartTok);
@@ -800,12 +804,14 @@ uint32_t prefill_parts(uint32_t n, const uint32_t* slots, uint32_t* cut) {
     return np;
 }
 
-// The prefill step on device pointers (arguments already checked).
+// The prefill step on device pointers (arguments already checked).  A part
+// of a host call in parts uses the workspace rows from token ws_tok on and
+// its own plan counters (plan_slot), so parts can run concurrently.
 int run_prefill(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
                 const float* k_new, const float* v_new, const uint32_t* positions,
                 const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
                 const float* inv_freq, const float* sinks, float* out, float eps, float scale,
-                cudaStream_t stream) {
+                cudaStream_t stream, size_t ws_tok = 0, uint32_t plan_slot = 0) {
     if (!h->tc_prefill)  // head dim 256: the decode kernel in prefill mode
         return launch(h, n_tok, n_head, q, k_new, v_new, positions, slots, q_norm_w, k_norm_w,
                       inv_freq, sinks, out, eps, scale, stream, true);
@@ -824,10 +830,10 @@ int run_prefill(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
     P.out = out;
     P.K = h->K;
     P.V = h->V;
-    P.q_rot = h->pf_q;
-    P.tiles = h->pf_tiles;
-    P.tile_of = h->pf_tile_of;
-    P.plan = h->pf_plan;
+    P.q_rot = h->pf_q + ws_tok * n_head * h->head_dim;
+    P.tiles = h->pf_tiles + 4 * ws_tok;
+    P.tile_of = h->pf_tile_of + ws_tok;
+    P.plan = h->pf_plan + 2 * plan_slot;
     P.status = h->status;
     P.n_slots = h->n_slots;
     P.slot_ctx = h->slot_ctx;
@@ -848,9 +854,12 @@ int run_prefill(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
 
 // prefill_batch_attn_host in parts [cut[i], cut[i+1]) (slot-disjoint, so each
 // part is a prefill of its own with the same tiles and bits): inputs in on
-// the handle's copy stream part by part, each part's kernels on `s` once its
-// inputs have landed, its out back on the out stream while the next part
-// runs; `s` waits for the last copy and is synchronised.
+// the handle's copy stream part by part; each part's kernels, once its
+// inputs have landed, on `s` or the handle's second stream by turns, with
+// its own workspace rows and plan counters, so that a part's kernels start
+// on the SMs the previous part's attention kernel leaves in its tail; each
+// part's out back on the out stream as soon as it is done.  `s` waits for
+// the second stream and the last copy and is synchronised.
 int prefill_host_in_parts(slotkv_t h, uint32_t n_tok, uint32_t n_head, const float* q,
                           const float* k_new, const float* v_new, const uint32_t* positions,
                           const uint32_t* slots, const float* q_norm_w, const float* k_norm_w,
@@ -865,24 +874,30 @@ int prefill_host_in_parts(slotkv_t h, uint32_t n_tok, uint32_t n_head, const flo
         e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess && !h->out_stream)
         e = cudaStreamCreateWithFlags(&h->out_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess && !h->pf_stream2)
+        e = cudaStreamCreateWithFlags(&h->pf_stream2, cudaStreamNonBlocking);
     for (cudaEvent_t& ev : h->pf_ev)
         if (e == cudaSuccess && !ev) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "prefill copy streams");
-    const cudaStream_t cin = h->copy_stream, cout = h->out_stream;
+    const cudaStream_t cin = h->copy_stream, cout = h->out_stream, s2 = h->pf_stream2;
     cudaEvent_t* in_ready = h->pf_ev;                                // [parts]
     cudaEvent_t* done = h->pf_ev + SLOTKV_PREFILL_HOST_MAX_PARTS;    // [parts]
     cudaEvent_t entry = h->pf_ev[2 * SLOTKV_PREFILL_HOST_MAX_PARTS];  // then: outputs back
+    cudaEvent_t joined = h->pf_ev[2 * SLOTKV_PREFILL_HOST_MAX_PARTS + 1];  // s2's parts done
     // whatever fails, nothing of this call is left running on return
     auto bail = [&](cudaError_t err, const char* what) {
         cudaStreamSynchronize(cin);
+        cudaStreamSynchronize(s2);
         cudaStreamSynchronize(cout);
         cudaStreamSynchronize(s);
         return err == cudaSuccess ? rc : cuda_fail(err, what);
     };
     const size_t qrow = (size_t)n_head * h->head_dim, krow = h->kv_dim;
-    // the staging may still be read by work enqueued on s before this call
+    // the staging and the workspace may still be in use by work enqueued on
+    // s before this call
     if ((e = cudaEventRecord(entry, s)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(cin, entry, 0)) != cudaSuccess)
+        (e = cudaStreamWaitEvent(cin, entry, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s2, entry, 0)) != cudaSuccess)
         return bail(e, "prefill copy order");
     for (uint32_t i = 0; i < parts; ++i) {
         const size_t t0 = cut[i], nt = cut[i + 1] - cut[i];
@@ -903,13 +918,14 @@ int prefill_host_in_parts(slotkv_t h, uint32_t n_tok, uint32_t n_head, const flo
     }
     for (uint32_t i = 0; i < parts; ++i) {
         const size_t t0 = cut[i];
-        if ((e = cudaStreamWaitEvent(s, in_ready[i], 0)) != cudaSuccess)
+        const cudaStream_t cs = (i & 1) ? s2 : s;
+        if ((e = cudaStreamWaitEvent(cs, in_ready[i], 0)) != cudaSuccess)
             return bail(e, "prefill copy order");
         rc = run_prefill(h, cut[i + 1] - cut[i], n_head, h->st_q + t0 * qrow, h->st_k + t0 * krow,
                          h->st_v + t0 * krow, h->st_pos + t0, h->st_slots + t0, q_norm_w,
-                         k_norm_w, inv_freq, sinks, h->st_out + t0 * qrow, eps, scale, s);
+                         k_norm_w, inv_freq, sinks, h->st_out + t0 * qrow, eps, scale, cs, t0, i);
         if (rc != SLOTKV_OK) return bail(cudaSuccess, nullptr);
-        if ((e = cudaEventRecord(done[i], s)) != cudaSuccess)
+        if ((e = cudaEventRecord(done[i], cs)) != cudaSuccess)
             return bail(e, "prefill copy order");
     }
     for (uint32_t i = 0; i < parts; ++i) {
@@ -921,7 +937,9 @@ int prefill_host_in_parts(slotkv_t h, uint32_t n_tok, uint32_t n_head, const flo
             return bail(e, "device-to-host output copy");
     }
     if ((e = cudaEventRecord(entry, cout)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s, entry, 0)) != cudaSuccess)
+        (e = cudaStreamWaitEvent(s, entry, 0)) != cudaSuccess ||
+        (e = cudaEventRecord(joined, s2)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, joined, 0)) != cudaSuccess)
         return bail(e, "prefill copy order");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
     return SLOTKV_OK;

@@ -165,7 +165,7 @@ def test_prefill_host_entry_equals_device_entry(pinned):
 
 # (head dim, G, run lengths, the runs' slots, parts the host entry makes)
 PART_LAYOUTS = {
-    "equal_hd128": (128, 4, [512] * 8, None, 4),
+    "equal_hd128": (128, 4, [512] * 8, None, 8),
     "uneven_hd64": (64, 8, [1500, 100, 900, 1700], None, 3),
     "returning_slot_hd128": (128, 2, [800] * 4, [0, 1, 0, 2], 2),
     "interleaved_hd64": (64, 4, [1] * 2048, [0, 1] * 1024, 1),
@@ -175,7 +175,7 @@ PART_LAYOUTS = {
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 @pytest.mark.parametrize("name", list(PART_LAYOUTS))
 def test_prefill_host_entry_in_parts_equals_device_entry(name, pinned):
-    """A host call of 2048 tokens or more is cut into parts whose tokens
+    """A host call of 1024 tokens or more is cut into parts whose tokens
     share no slot, each run as a prefill of its own while the others' copies
     move: the output and the slot bytes stay those of one device call, bit
     for bit (the parts hold the same runs, so the same tiles)."""

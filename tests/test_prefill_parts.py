@@ -1,6 +1,6 @@
 """Where prefill_batch_attn_host cuts a call (slot_kv_prefill_host_parts,
-host logic only): parts whose tokens share no slot, one per 1024 tokens and
-at most four, none under 512 tokens, each cut the allowed one nearest its
+host logic only): parts whose tokens share no slot, one per 512 tokens and
+at most eight, none under 256 tokens, each cut the allowed one nearest its
 target, the targets giving the first and the last part half the size of the
 others; a call that cannot be cut that way stays whole.  Each part is a
 prefill of its own, so a cut with a slot on both sides would let one part's
@@ -22,26 +22,38 @@ def _check_valid(slots, cuts):
     n = len(slots)
     assert cuts[0] == 0 and cuts[-1] == n
     assert all(a < b for a, b in zip(cuts, cuts[1:]))
-    assert len(cuts) - 1 <= min(skv.PREFILL_HOST_MAX_PARTS, max(1, n // 1024))
+    assert len(cuts) - 1 <= min(skv.PREFILL_HOST_MAX_PARTS, max(1, n // 512))
     if len(cuts) > 2:
-        assert all(b - a >= 512 for a, b in zip(cuts, cuts[1:]))
+        assert all(b - a >= 256 for a, b in zip(cuts, cuts[1:]))
     for m in cuts[1:-1]:
         assert not set(slots[:m].tolist()) & set(slots[m:].tolist())
 
 
 def test_small_calls_stay_whole():
     assert parts([]) == [0, 0]  # one empty part
-    assert parts(_seqs([700, 700])) == [0, 1400]
-    assert parts(_seqs([1023, 1024])) == [0, 2047]
+    assert parts(_seqs([400, 500])) == [0, 900]
+    assert parts(_seqs([511, 512])) == [0, 1023]
+    # from 1024 tokens on: two parts
+    assert parts(_seqs([700, 700])) == [0, 700, 1400]
 
 
-def test_equal_sequences_cut_with_half_size_ends():
-    # targets 4096 * (1, 3, 5) / 6 = 683, 2048, 3413
-    assert parts(_seqs([512] * 8)) == [0, 512, 2048, 3584, 4096]
+def test_equal_sequences_cut_at_their_boundaries():
+    # eight parts, targets 4096 * (1, 3, .., 13) / 14 = 293, 878, .., 3803:
+    # every sequence boundary is the nearest allowed cut of one target
+    assert parts(_seqs([512] * 8)) == [0, 512, 1024, 1536, 2048, 2560, 3072, 3584, 4096]
+    # four parts wanted (targets 341, 1024, 1707); one cut allowed
     assert parts(_seqs([1024] * 2)) == [0, 1024, 2048]
-    # more tokens than four parts' worth: still four parts (targets 1167,
-    # 3500, 5833; of two cuts equally near, the first)
-    assert parts(_seqs([1000] * 7)) == [0, 1000, 3000, 6000, 7000]
+    # eight parts wanted, seven sequences: targets 500, 1500, ..; of two
+    # cuts equally near, the first not too close to the previous cut
+    assert parts(_seqs([1000] * 7)) == [0, 1000, 2000, 3000, 4000, 5000, 6000, 7000]
+
+
+def test_half_size_ends():
+    # sixteen 256-token sequences, eight parts: the targets 4096 * (1, 3, ..,
+    # 13) / 14 = 292, 877, 1462, 2048, 2633, 3218, 3803 snap to the nearest
+    # sequence boundaries, so the first and the last part hold one sequence
+    # and the others two or three
+    assert parts(_seqs([256] * 16)) == [0, 256, 768, 1536, 2048, 2560, 3328, 3840, 4096]
 
 
 def test_no_allowed_cut_keeps_one_part():
@@ -53,8 +65,9 @@ def test_no_allowed_cut_keeps_one_part():
 
 
 def test_uneven_sequences_take_the_nearest_allowed_cuts():
-    # targets 700, 2100, 3500; allowed cuts 1500, 1600, 2500; a third part
-    # boundary would leave a part under 512 tokens
+    # targets 4200 * (1, 3, .., 13) / 14 = 300, 900, ..; allowed cuts 1500,
+    # 1600, 2500: the first two targets take 1500 and 2500, and no allowed
+    # cut is left for the others
     assert parts(_seqs([1500, 100, 900, 1700])) == [0, 1500, 2500, 4200]
 
 
@@ -82,14 +95,15 @@ def test_random_layouts(seed):
 def test_bad_arguments_are_refused():
     import ctypes
     n = ctypes.c_uint32()
-    cuts = (ctypes.c_uint32 * 5)()
-    assert skv._lib.slot_kv_prefill_host_parts(4, None, cuts, 5, ctypes.byref(n)) == 1
-    assert skv._lib.slot_kv_prefill_host_parts(0, None, None, 5, ctypes.byref(n)) == 1
+    k = skv.PREFILL_HOST_MAX_PARTS + 1
+    cuts = (ctypes.c_uint32 * k)()
+    assert skv._lib.slot_kv_prefill_host_parts(4, None, cuts, k, ctypes.byref(n)) == 1
+    assert skv._lib.slot_kv_prefill_host_parts(0, None, None, k, ctypes.byref(n)) == 1
     # a cuts array too short for the most parts a call can have
     s = _seqs([512] * 8)
-    assert skv._lib.slot_kv_prefill_host_parts(len(s), s.ctypes.data, cuts, 4,
+    assert skv._lib.slot_kv_prefill_host_parts(len(s), s.ctypes.data, cuts, k - 1,
                                                ctypes.byref(n)) == 1
-    assert skv._lib.slot_kv_prefill_host_parts(0, None, cuts, 5, ctypes.byref(n)) == 0
+    assert skv._lib.slot_kv_prefill_host_parts(0, None, cuts, k, ctypes.byref(n)) == 0
     assert n.value == 1 and cuts[0] == 0 and cuts[1] == 0
 
 
