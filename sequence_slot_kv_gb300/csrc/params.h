@@ -72,7 +72,7 @@ struct PrefillParams {
     float* V;
     float* q_rot;            // workspace [n_tok][n_head][hd]: normed, rotated, scaled q
     uint32_t* tiles;         // workspace [n_tok][4]: first token, tokens, slot, largest position
-    uint32_t* tile_of;       // workspace [n_tok]: each token's tile
+    uint32_t* tile_of;       // workspace [n_tok]: each token's tile, then the tiles' hand-out order
     uint32_t* plan;          // [0] items (tiles * n_kv_head), [1] next item to hand out
     uint32_t* status;        // sticky SLOTKV_DEV_* flags
     uint32_t n_slots, slot_ctx, n_head, n_kv_head, n_tok;
