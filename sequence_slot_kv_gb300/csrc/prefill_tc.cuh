@@ -13,8 +13,9 @@
 //   * slotkv_prefill_plan_kernel (one CTA): cuts each run of consecutive
 //     same-slot tokens into tiles of MT = 128 / G tokens -- a tile's G query
 //     heads per token make the 128 rows of one MMA -- and lists the tiles,
-//     largest first.  A work item is one (tile, kv head): keys 0 .. the
-//     tile's largest position, read once for all its rows.
+//     handed out in reverse (each run from its last tile to its first).  A
+//     work item is one (tile, kv head): keys 0 .. the tile's largest
+//     position, read once for all its rows.
 //   * slotkv_prefill_tc_kernel (persistent, one CTA per SM): flash attention
 //     of each item with f32 accuracy from TF32 tensor-core products, split
 //     in three: a = a_hi + a_lo with a_hi = a with its low 13 mantissa bits
@@ -217,14 +218,11 @@ __global__ void __launch_bounds__(128) slotkv_prefill_prep_kernel(const PrefillP
 // a tile when its index within its run is a multiple of MT.  Tile records:
 // (first token, tokens, slot, largest position).  Out-of-range tokens raise
 // SLOTKV_DEV_RANGE and belong to no tile.  Then the tiles' hand-out order.
-constexpr uint32_t kOrderBins = 64;  // hand-out order bins (two per lane of one warp)
-static_assert(kOrderBins == 64, "the order scan covers 64 bins with one warp");
 
 template <int MT>
 __global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const PrefillParams P) {
     __shared__ int warp_max[32];
     __shared__ uint32_t warp_sum[32];
-    __shared__ uint32_t order_count[kOrderBins];
     __shared__ int carry_start;
     __shared__ uint32_t carry_tiles;
     // The prep kernel, launched next as a programmatic dependent, may start
@@ -316,34 +314,14 @@ __global__ void __launch_bounds__(1024, 1) slotkv_prefill_plan_kernel(const Pref
         atomicMax(rec + 3, P.positions[i]);
     }
     __syncthreads();
-    // The hand-out order, into tile_of (its per-token use is over): largest
-    // first, binned by the tile's largest position, so that the items with
-    // the fewest keys end the attention kernel.  (Any order gives the same
-    // bits: items are independent.)
+    // The hand-out order, into tile_of (its per-token use is over): the
+    // tiles in reverse, so each run is handed out from its last tile (the
+    // most keys, when its positions increase) to its first, one run after
+    // the other -- the attention kernel ends on small items while a run's
+    // keys stay in L2 across its tiles.  (Any order gives the same bits:
+    // items are independent.)
     const uint32_t n_tiles = carry_tiles;
-    const uint32_t span = (P.slot_ctx + kOrderBins - 1) / kOrderBins;
-    auto order_bin = [&](uint32_t t) {
-        const uint32_t b = __ldcg(P.tiles + 4 * static_cast<size_t>(t) + 3) / span;
-        return kOrderBins - 1 - (b < kOrderBins - 1 ? b : kOrderBins - 1);
-    };
-    if (tid < kOrderBins) order_count[tid] = 0;
-    __syncthreads();
-    for (uint32_t t = tid; t < n_tiles; t += 1024) atomicAdd(&order_count[order_bin(t)], 1u);
-    __syncthreads();
-    if (warp == 0) {  // exclusive scan over the bins, two per lane
-        const uint32_t a = order_count[2 * lane], c = order_count[2 * lane + 1];
-        uint32_t incl = a + c;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        order_count[2 * lane] = incl - a - c;
-        order_count[2 * lane + 1] = incl - c;
-    }
-    __syncthreads();
-    for (uint32_t t = tid; t < n_tiles; t += 1024)
-        P.tile_of[atomicAdd(&order_count[order_bin(t)], 1u)] = t;
+    for (uint32_t t = tid; t < n_tiles; t += 1024) P.tile_of[t] = n_tiles - 1 - t;
     __syncthreads();
     if (tid == 0) {
         P.plan[0] = carry_tiles * P.n_kv_head;
@@ -442,7 +420,7 @@ __global__ void __launch_bounds__(PCfg<HD, G>::THREADS, 1)
                     mbar_arrive(FULL + 8 * (h % NSLOT));
                     break;
                 }
-                // the plan's hand-out order: largest tiles first
+                // in the plan's hand-out order
                 const uint4 rec = __ldcg(tiles + __ldcg(P.tile_of + it / P.n_kv_head));
                 const uint32_t kvh = it % P.n_kv_head;
                 const uint32_t max_pos = rec.w;
