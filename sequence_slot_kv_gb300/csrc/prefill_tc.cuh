@@ -5,7 +5,8 @@
 //
 // Three kernels per call, on one stream (the plan launched first, prep
 // beside it as a programmatic dependent, the attention kernel after both):
-//   * slotkv_prefill_prep_kernel: one warp per (token, 8 heads).  Query heads:
+//   * slotkv_prefill_prep_kernel: one warp per (token, 8 query heads or 4 kv
+//     heads).  Query heads:
 //     q' = RoPE(RMSnorm(q) * w) * scale * log2(e) into a workspace; kv heads:
 //     k' = RoPE(RMSnorm(k_new) * w) and v into the token's slot row.  The
 //     vector routines are the decode kernel's, so q' and k' are the same
@@ -139,13 +140,14 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) 
 }
 
 // ------------------------------------------------------------------ prep
-// One warp per (token, group of kPrepHeads heads).  The group's rows (q rows,
-// or k_new and v_new rows) are staged into the warp's shared memory with
-// cp.async, all in flight at once, while the warp forms the token's RoPE
-// angles; then each row goes through the decode kernel's vector routine
-// (the same arithmetic on the same values, so the same bits as a decode
-// step).
-constexpr int kPrepHeads = 8;
+// One warp per (token, group of heads): kPrepHeads query heads, or
+// kPrepKvHeads kv heads (their k_new and v_new rows), so that every warp
+// stages kPrepHeads rows.  The group's rows are staged into the warp's
+// shared memory with cp.async, all in flight at once, while the warp forms
+// the token's RoPE angles; then each row goes through the decode kernel's
+// vector routine (the same arithmetic on the same values, so the same bits
+// as a decode step).
+constexpr int kPrepHeads = 8, kPrepKvHeads = kPrepHeads / 2;
 
 __device__ __forceinline__ void prep_cp_async16(void* smem_dst, const void* gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
@@ -155,35 +157,46 @@ __device__ __forceinline__ void prep_cp_async16(void* smem_dst, const void* gmem
 
 template <int HD>
 __host__ __device__ constexpr int prep_smem_bytes() {
-    return 4 * 2 * kPrepHeads * HD * 4;  // four warps x (rows, v rows)
+    return 4 * kPrepHeads * HD * 4;  // four warps x kPrepHeads rows
+}
+
+// query-head groups and kv-head groups per token
+__host__ __device__ inline uint32_t prep_q_groups(uint32_t n_head) {
+    return (n_head + kPrepHeads - 1) / kPrepHeads;
+}
+__host__ __device__ inline uint32_t prep_groups(uint32_t n_head, uint32_t n_kv_head) {
+    return prep_q_groups(n_head) + (n_kv_head + kPrepKvHeads - 1) / kPrepKvHeads;
 }
 
 template <int HD>
 __global__ void __launch_bounds__(128) slotkv_prefill_prep_kernel(const PrefillParams P) {
     extern __shared__ __align__(16) uint8_t prep_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t per_tok = P.n_head + P.n_kv_head;
-    const uint32_t groups = (per_tok + kPrepHeads - 1) / kPrepHeads;
+    const uint32_t qg = prep_q_groups(P.n_head), groups = prep_groups(P.n_head, P.n_kv_head);
     const uint32_t wg = blockIdx.x * 4 + warp;
-    const uint32_t tok = wg / groups, x0 = (wg % groups) * kPrepHeads;
+    const uint32_t tok = wg / groups, grp = wg % groups;
     if (tok >= P.n_tok) return;
     const uint32_t p = P.positions[tok], slot = P.slots[tok];
     if (slot >= P.n_slots || p >= P.slot_ctx) return;  // the plan raises the flag
-    const uint32_t nx = per_tok - x0 < static_cast<uint32_t>(kPrepHeads) ? per_tok - x0
-                                                                           : kPrepHeads;
-    float* rows = reinterpret_cast<float*>(prep_smem) + warp * 2 * kPrepHeads * HD;
-    float* vrows = rows + kPrepHeads * HD;
+    const bool is_q = grp < qg;
+    // the group's first head (a query head, or a kv head) and its size
+    const uint32_t x0 = is_q ? grp * kPrepHeads : (grp - qg) * kPrepKvHeads;
+    const uint32_t left = (is_q ? P.n_head : P.n_kv_head) - x0;
+    const uint32_t cap = is_q ? kPrepHeads : kPrepKvHeads;
+    const uint32_t nx = left < cap ? left : cap;
+    float* rows = reinterpret_cast<float*>(prep_smem) + warp * kPrepHeads * HD;
+    float* vrows = rows + kPrepKvHeads * HD;  // kv groups: v rows after the k rows
     for (uint32_t i = 0; i < nx; ++i) {
         const uint32_t x = x0 + i;
-        const float* src = x < P.n_head
-                               ? P.q + (static_cast<size_t>(tok) * P.n_head + x) * HD
-                               : P.k_new + (static_cast<size_t>(tok) * P.n_kv_head + (x - P.n_head)) * HD;
-        for (int c = lane; c < HD / 4; c += 32) prep_cp_async16(rows + i * HD + 4 * c, src + 4 * c);
-        if (x >= P.n_head) {
-            const float* vsrc =
-                P.v_new + (static_cast<size_t>(tok) * P.n_kv_head + (x - P.n_head)) * HD;
-            for (int c = lane; c < HD / 4; c += 32)
-                prep_cp_async16(vrows + i * HD + 4 * c, vsrc + 4 * c);
+        if (is_q) {
+            const float* src = P.q + (static_cast<size_t>(tok) * P.n_head + x) * HD;
+            for (int c = lane; c < HD / 4; c += 32) prep_cp_async16(rows + i * HD + 4 * c, src + 4 * c);
+        } else {
+            const size_t at = (static_cast<size_t>(tok) * P.n_kv_head + x) * HD;
+            for (int c = lane; c < HD / 4; c += 32) {
+                prep_cp_async16(rows + i * HD + 4 * c, P.k_new + at + 4 * c);
+                prep_cp_async16(vrows + i * HD + 4 * c, P.v_new + at + 4 * c);
+            }
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -194,14 +207,13 @@ __global__ void __launch_bounds__(128) slotkv_prefill_prep_kernel(const PrefillP
     __syncwarp();
     for (uint32_t i = 0; i < nx; ++i) {
         const uint32_t x = x0 + i;
-        if (x < P.n_head) {
+        if (is_q) {
             const size_t at = (static_cast<size_t>(tok) * P.n_head + x) * HD;
             warp_norm_rope<HD>(rows + i * HD, P.q_rot + at, P.q_norm_w, w1, P.scale_log2, P.eps,
                                cs, sn, lane);
             continue;
         }
-        const uint32_t kvh = x - P.n_head;
-        const size_t dst = ((static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + kvh) * HD;
+        const size_t dst = ((static_cast<size_t>(slot) * P.slot_ctx + p) * P.n_kv_head + x) * HD;
         warp_norm_rope<HD>(rows + i * HD, P.K + dst, P.k_norm_w, w1, 1.0f, P.eps, cs, sn, lane);
         if (P.flags & kOptVNorm) {
             warp_rms_norm_plain<HD>(vrows + i * HD, P.V + dst, P.eps, lane);
@@ -916,8 +928,7 @@ int launch_prefill_one(const PrefillParams& p, const CUtensorMap& tmK, const CUt
         if (e != cudaSuccess) return static_cast<int>(e);
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const uint32_t groups = (p.n_head + p.n_kv_head + kPrepHeads - 1) / kPrepHeads;
-    const uint32_t warps = p.n_tok * groups;
+    const uint32_t warps = p.n_tok * prep_groups(p.n_head, p.n_kv_head);
     // the plan (one CTA) first, then prep beside it as its programmatic
     // dependent; the attention kernel, launched in stream order, waits for
     // both.  Prep starts only once the plan runs, hence after the previous
