@@ -83,7 +83,7 @@ def measured_traffic(workload):
 # prefill workload of a geometry (ncu one-pass counters, the mean over the
 # full-size calls' launches), keyed by code_hash of prefill_tc.cuh; reported
 # only while the kernel is the one measured.
-MEASURED_PREFILL_TRAFFIC = {"4eefb6b80abde9df": {"mid": 247_506_730, "sinks": 170_451_754}}
+MEASURED_PREFILL_TRAFFIC = {"56858cc248ba86b3": {"mid": 247_501_909, "sinks": 170_577_280}}
 
 
 def prefill_source_hash():
