@@ -51,9 +51,11 @@ FLUSH_BYTES = 256 * 1024 * 1024  # written between calls of a step that fits in 
 MEASURED_TRAFFIC = {
     # all at full size; large's is its first step's ratio to the algorithmic
     # bytes times the mean algorithmic bytes of its 64 steps
-    # (plan + decode kernel bytes, the mean of two calls)
+    # (plan + decode kernel bytes, the mean of two calls; of 18 calls for the
+    # eight-heads-per-kv-head workloads)
     "26542fcb3b784732": {"mid": 551_830_912, "sinks": 2_336_513_024,
-                         "skewed": 17_227_054_208, "large": 2_238_835_960},
+                         "skewed": 17_227_054_208, "large": 2_238_835_960,
+                         "gqa8_hd128": 509_073_606, "gqa8_hd256": 627_442_587},
 }
 
 
