@@ -233,3 +233,65 @@ def test_prefill_host_in_parts_random_layouts(seed):
     got, K, V = _run_host(w, slots, pos, pinned=True)
     assert np.array_equal(got.view(np.uint32), got_dev.view(np.uint32))
     assert torch.equal(K, Kd) and torch.equal(V, Vd)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_out_of_range_tokens_are_skipped(hd):
+    """Tokens whose slot or position is out of range raise SLOTKV_DEV_RANGE,
+    join no tile and write nothing (their out rows keep their contents);
+    every other token is the oracle's, as if the bad ones were not in the
+    call, and only the good tokens' slot rows change."""
+    import sequence_slot_kv_gb300 as skv
+    G, n_slots, ctx = 4, 5, 240
+    slots = np.concatenate([np.full(60, 1, np.uint32), np.full(40, 3, np.uint32)])
+    pos = np.concatenate([np.arange(100, 160, dtype=np.uint32), np.arange(0, 40, dtype=np.uint32)])
+    bad = [10, 70, 99]
+    pos[10] = ctx              # position past the slot
+    slots[70] = n_slots        # slot past the pool
+    pos[99] = ctx + 5
+    good = [i for i in range(len(pos)) if i not in bad]
+    w = _workload(hd, G, 2, 60 + hd, len(pos), n_slots, ctx)
+    shape = (w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim)
+    K = torch.empty(shape, device="cuda")
+    V = torch.empty(shape, device="cuda")
+    w.dev_fill_history(K.data_ptr(), V.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    K0, V0 = K.cpu().numpy(), V.cpu().numpy()
+    kv = SlotKV(w.n_slots, w.slot_ctx, w.n_kv_head, w.head_dim, w.B, w.n_head, k_buf=K, v_buf=V)
+    try:
+        out = torch.full((w.B, w.n_head, w.head_dim), 7.0, device="cuda")
+        s = w.sink_logits()
+        kv.prefill_batch_attn(to_dev(w.q()), to_dev(w.k_new()), to_dev(w.v_new()),
+                              to_dev(pos.astype(np.int32)), to_dev(slots.astype(np.int32)),
+                              to_dev(w.q_norm_w()), to_dev(w.k_norm_w()), to_dev(w.inv_freq()),
+                              None if s is None else to_dev(s), out, w.eps, w.scale)
+        torch.cuda.synchronize()
+        assert kv.get_status() == skv.DEV_RANGE
+        got = out.cpu().numpy()
+        Kg, Vg = K.cpu().numpy(), V.cpu().numpy()
+    finally:
+        kv.free()
+    assert np.all(got[bad] == 7.0)
+    # the oracle on host copies of the two slots, the good tokens' rows
+    # written first, then one decode step per good token
+    o = oracle.default()
+    Kh, Vh = K0[[1, 3]].copy(), V0[[1, 3]].copy()
+    at = {1: 0, 3: 1}
+    kn, vn = w.k_new(), w.v_new()
+    for i in good:
+        c, p = at[int(slots[i])], int(pos[i])
+        for g in range(w.n_kv_head):
+            Kh[c, p, g] = o.norm_rope_head(kn[i, g], w.k_norm_w(), w.eps, p,
+                                           w.inv_freq()).astype(np.float32)
+        Vh[c, p] = vn[i]
+    compact = np.array([at[int(slots[i])] for i in good], dtype=np.uint32)
+    ref, _, skipped = o.decode_batch(Kh, Vh, w.q()[good], kn[good], vn[good], pos[good], compact,
+                                     w.q_norm_w(), w.k_norm_w(), w.inv_freq(), s, w.eps,
+                                     w.scale, n_threads=16)
+    assert skipped == 0
+    assert_close(got[good], ref, f"prefill with out-of-range tokens hd={hd}")
+    # only the good tokens' rows changed; the bad tokens wrote nothing
+    mask = np.zeros(shape[:2], dtype=bool)
+    mask[slots[good], pos[good]] = True
+    assert np.array_equal(Kg[~mask].view(np.uint32), K0[~mask].view(np.uint32))
+    assert np.array_equal(Vg[~mask].view(np.uint32), V0[~mask].view(np.uint32))
+    assert np.array_equal(Vg[mask].view(np.uint32), vn[good].view(np.uint32).reshape(Vg[mask].shape))
